@@ -1,0 +1,297 @@
+/*
+ * k3mx_oracle.c - plain, slow CPU reference of the MXFP4 routed-expert layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or
+ * calls this file: only the tests, the smoke check and the bench's CPU
+ * baseline do.  It shares no code with the CUDA kernels.
+ *
+ * Every step is the plain definition, written in the order the pages give it,
+ * with double accumulation, no blocking and no reordering.  Build with
+ * -ffp-contract=off so that every multiply and add rounds as written.  OpenMP
+ * splits independent output rows across threads; each row is still summed by
+ * one thread in one fixed order, so results do not depend on the thread count
+ * (the determinism argument of "A floating-point contract, not a convention",
+ * kimi-k3-in-c: 2.78 trillion parameters, one CPU, 8 GB of RAM).
+ *
+ * Sources (page title, section):
+ *   [W]  Kimi K3 engine (c/kimi_k3.c), "Weights": e2m1 nibbles two per byte,
+ *        low nibble = even column, bit 3 = sign, one ue8m0 scale per 32
+ *        columns, w = v * 2^(scale - 127).
+ *   [R1] kimi-k3-in-c: 2.78 trillion parameters, one CPU, 8 GB of RAM,
+ *        "Reduction one: the experts already ship at half a byte": per
+ *        32-group sub-dot, one scale per group, scale byte 255 (NaN) skipped,
+ *        double accumulator, result rounded to float once per row.
+ *   [A]  Kimi K3 engine (c/kimi_k3.c), "Architecture notes", Stable LatentMoE
+ *        bullet: sigmoid router, top-16 on biased scores, weights are the raw
+ *        scores renormalised, experts are GLUs of inter width 3072 in the
+ *        3584 latent, activation SiTU-GLU 4 tanh(g/4) sigma(g) 25 tanh(u/25).
+ *   [I3] kimi-k3-in-c README, "Three invariants", item 3: the routing bias
+ *        steers selection only; the combining weights use the unbiased
+ *        sigmoid scores.
+ *   [C]  kimi-k3-in-c README, "2. The config reader that refuses to guess",
+ *        K3Cfg: n_experts 896, topk 16, latent 3584, moe_inter 3072,
+ *        routed_scale 1.0, moe_renorm 1, situ_b1 4.0, situ_b2 25.0.
+ *   [P]  Kimi K3 engine (c/kimi_k3.c), "Chunked prefill": within a chunk every
+ *        unique expert is loaded once for all the tokens that chose it.
+ *
+ * Readings where the pages are silent (each listed in the design notes):
+ *   - sigma is evaluated in double with libm exp and rounded to fp32 once;
+ *     the selection key is that fp32 score plus the fp32 bias, one fp32 add.
+ *   - ties between equal keys go to the lower expert index; -0 counts as +0;
+ *     a NaN key ranks below every number.
+ *   - the 16 indices are returned in selection order (key descending).
+ *   - renormalisation has no epsilon; routed_scale 1.0 is applied explicitly.
+ *   - g = W1 x and u = W3 x (W1 is the gate).  g and u are the fp32 outputs
+ *     of the GEMV; h is evaluated in double and rounded to fp32.
+ *   - tokens are grouped by expert with a stable order (token, slot).
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* [W]: code = nibble; bit 3 is the sign, bits 2..0 index the magnitudes
+ * {0, 0.5, 1, 1.5, 2, 3, 4, 6}. */
+static const double ORC_E2M1[16] = {
+    0.0,  0.5,  1.0,  1.5,  2.0,  3.0,  4.0,  6.0,
+   -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0,
+};
+
+double orc_e2m1(int code) { return ORC_E2M1[code & 15]; }
+
+/* [W]: ue8m0 byte s means 2^(s - 127); 255 is NaN and is never used. */
+double orc_e8m0(int s)
+{
+    if (s == 255) return NAN;
+    return ldexp(1.0, s - 127);
+}
+
+/* the nibble of column c of a packed row: low nibble = even column [W] */
+static inline int nib(const uint8_t *row_packed, int c)
+{
+    return (row_packed[c >> 1] >> (4 * (c & 1))) & 15;
+}
+
+/*
+ * y[r] = sum_g 2^(s_rg - 127) * sum_{i<32} v(r, 32g+i) * x[32g+i]   [R1]
+ * packed: [rows][in/2] bytes, scales: [rows][in/32] bytes, row-major.
+ * Groups whose scale byte is 255 contribute nothing.
+ */
+void orc_gemv(float *y, const float *x, const uint8_t *packed,
+              const uint8_t *scales, int in, int rows)
+{
+    const int ngrp = in / 32;
+    #pragma omp parallel for schedule(static)
+    for (int r = 0; r < rows; r++) {
+        const uint8_t *pr = packed + (size_t)r * (in / 2);
+        const uint8_t *sr = scales + (size_t)r * ngrp;
+        double acc = 0.0;
+        for (int g = 0; g < ngrp; g++) {
+            const int sb = sr[g];
+            if (sb == 255) continue;                 /* NaN scale: nothing */
+            double sub = 0.0;
+            for (int i = 0; i < 32; i++) {
+                const int c = 32 * g + i;
+                sub += ORC_E2M1[nib(pr, c)] * (double)x[c];
+            }
+            acc += sub * orc_e8m0(sb);
+        }
+        y[r] = (float)acc;
+    }
+}
+
+/*
+ * Tolerance helper, not part of the method: b[r] = sum_c |w_rc| |x_c| over
+ * the groups whose scale is not 255, in double.
+ */
+void orc_gemv_absdot(double *b, const double *xabs, const uint8_t *packed,
+                     const uint8_t *scales, int in, int rows)
+{
+    const int ngrp = in / 32;
+    #pragma omp parallel for schedule(static)
+    for (int r = 0; r < rows; r++) {
+        const uint8_t *pr = packed + (size_t)r * (in / 2);
+        const uint8_t *sr = scales + (size_t)r * ngrp;
+        double acc = 0.0;
+        for (int g = 0; g < ngrp; g++) {
+            const int sb = sr[g];
+            if (sb == 255) continue;
+            double sub = 0.0;
+            for (int i = 0; i < 32; i++) {
+                const int c = 32 * g + i;
+                sub += fabs(ORC_E2M1[nib(pr, c)]) * xabs[c];
+            }
+            acc += sub * orc_e8m0(sb);
+        }
+        b[r] = acc;
+    }
+}
+
+/* sigma(z) = 1 / (1 + exp(-z)), in double */
+double orc_sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
+
+/* SiTU-GLU [A], betas 4.0 and 25.0 [C]: 4 tanh(g/4) sigma(g) * 25 tanh(u/25) */
+double orc_situ(double g, double u)
+{
+    const double b1 = 4.0, b2 = 25.0;
+    return (b1 * tanh(g / b1) * orc_sigmoid(g)) * (b2 * tanh(u / b2));
+}
+
+/*
+ * One routed expert [A]: g = W1 x, u = W3 x (each [F x D], fp32 results),
+ * h_j = SiTU(g_j, u_j) rounded to fp32, y = W2 h (W2 is [D x F]).
+ * g, u, h may be NULL; otherwise they receive the intermediate vectors.
+ * The scratch for g, u and h when NULL is the caller's buffer `tmp` of 3F
+ * floats.
+ */
+void orc_expert(float *y, float *g, float *u, float *h, float *tmp,
+                const float *x,
+                const uint8_t *w1p, const uint8_t *w1s,
+                const uint8_t *w3p, const uint8_t *w3s,
+                const uint8_t *w2p, const uint8_t *w2s, int D, int F)
+{
+    float *gg = g ? g : tmp, *uu = u ? u : tmp + F, *hh = h ? h : tmp + 2 * F;
+    orc_gemv(gg, x, w1p, w1s, D, F);
+    orc_gemv(uu, x, w3p, w3s, D, F);
+    for (int j = 0; j < F; j++) hh[j] = (float)orc_situ((double)gg[j], (double)uu[j]);
+    orc_gemv(y, hh, w2p, w2s, F, D);
+}
+
+/*
+ * Tolerance helper, not part of the method.  bound[i] =
+ *   sum_j |w2_ij| (|h_j| + 30 E_j),  E_j = sum_c (|w1_jc| + |w3_jc|) |x_c|.
+ * 30 bounds how far an error in g or u moves h:  |dh/dg| <= 25 max|A'(g)|
+ * with A(g) = 4 tanh(g/4) sigma(g) (about 0.93, so about 23.3) and
+ * |dh/du| <= 4.  `work` holds 2D + 3F doubles.
+ */
+void orc_expert_bound(double *bound, double *work, const float *x, const float *h,
+                      const uint8_t *w1p, const uint8_t *w1s,
+                      const uint8_t *w3p, const uint8_t *w3s,
+                      const uint8_t *w2p, const uint8_t *w2s, int D, int F)
+{
+    double *xa = work, *e1 = work + D, *e3 = e1 + F, *hb = e3 + F;
+    for (int c = 0; c < D; c++) xa[c] = fabs((double)x[c]);
+    orc_gemv_absdot(e1, xa, w1p, w1s, D, F);
+    orc_gemv_absdot(e3, xa, w3p, w3s, D, F);
+    for (int j = 0; j < F; j++) hb[j] = fabs((double)h[j]) + 30.0 * (e1[j] + e3[j]);
+    orc_gemv_absdot(bound, hb, w2p, w2s, F, D);
+}
+
+/* order used by the selection: -0 -> +0, NaN -> -inf [reading] */
+static inline float canon_key(float k)
+{
+    if (k != k) return -INFINITY;
+    if (k == 0.0f) return 0.0f;
+    return k;
+}
+
+/*
+ * Router [A][I3][C], per token t:
+ *   s_e   = (float) sigma(logit_e)           (double, rounded once)
+ *   key_e = s_e + bias_e                     (one fp32 add)
+ *   idx   = the K experts of largest key, by repeated argmax:
+ *           the largest key wins, equal keys go to the lower e
+ *   w_k   = (float)( s_{idx_k} / sum_j s_{idx_j} ) * routed_scale
+ * The sum over the selected raw scores is taken in double in slot order.
+ * `s_out` (T x E, may be NULL) receives the fp32 scores.
+ */
+void orc_route(int32_t *idx, float *w, float *s_out, const float *logits,
+               const float *bias, int T, int E, int K, float routed_scale)
+{
+    #pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; t++) {
+        float s[1024], key[1024];
+        unsigned char taken[1024];
+        const float *lt = logits + (size_t)t * E;
+        for (int e = 0; e < E; e++) {
+            s[e] = (float)orc_sigmoid((double)lt[e]);
+            key[e] = canon_key(s[e] + bias[e]);
+            taken[e] = 0;
+        }
+        if (s_out) memcpy(s_out + (size_t)t * E, s, sizeof(float) * (size_t)E);
+        for (int k = 0; k < K; k++) {
+            int best = -1;
+            for (int e = 0; e < E; e++) {
+                if (taken[e]) continue;
+                if (best < 0 || key[e] > key[best]) best = e;   /* strict: ties keep lower e */
+            }
+            taken[best] = 1;
+            idx[(size_t)t * K + k] = best;
+        }
+        double sum = 0.0;
+        for (int k = 0; k < K; k++) sum += (double)s[idx[(size_t)t * K + k]];
+        for (int k = 0; k < K; k++)
+            w[(size_t)t * K + k] =
+                (float)((double)s[idx[(size_t)t * K + k]] / sum) * routed_scale;
+    }
+}
+
+/*
+ * Token-to-expert grouping [P]:
+ *   counts[e]   = number of (t, k) with idx[t][k] = e
+ *   offsets[0]  = 0, offsets[e+1] = offsets[e] + counts[e]
+ *   perm        = the pairs p = t*K + k listed expert by expert, and inside an
+ *                 expert in increasing p (stable).
+ * Returns 0, or -1 if an index lies outside 0..E-1.
+ */
+int orc_group(int32_t *counts, int32_t *offsets, int32_t *perm,
+              const int32_t *idx, int T, int E, int K)
+{
+    const long long n = (long long)T * K;
+    for (int e = 0; e < E; e++) counts[e] = 0;
+    for (long long p = 0; p < n; p++) {
+        if (idx[p] < 0 || idx[p] >= E) return -1;
+        counts[idx[p]]++;
+    }
+    offsets[0] = 0;
+    for (int e = 0; e < E; e++) offsets[e + 1] = offsets[e] + counts[e];
+    /* fill each expert's list by walking the pairs in order */
+    for (int e = 0; e < E; e++) counts[e] = 0;
+    for (long long p = 0; p < n; p++) {
+        const int e = idx[p];
+        perm[offsets[e] + counts[e]] = (int32_t)p;
+        counts[e]++;
+    }
+    return 0;
+}
+
+/*
+ * The routed weighted sum [A]:  y_t = (float) sum_k w_tk * expert_{idx_tk}(x_t)
+ * with each expert output the fp32 result of orc_expert, widened to double,
+ * and the K terms added in slot order.  `ptrs` holds 6 pointers per expert
+ * (w1p, w1s, w3p, w3s, w2p, w2s) indexed by expert id; only the selected
+ * experts are read, so unselected entries may be NULL.  `tmp` holds
+ * 3F + D floats.  Tokens run one after another; rows inside each GEMV run in
+ * parallel.
+ */
+void orc_moe(float *y, const float *x, int T, const uint8_t *const *ptrs,
+             const int32_t *idx, const float *w, int D, int F, int K, float *tmp)
+{
+    float *ye = tmp + 3 * F;
+    double acc[8192];
+    for (int t = 0; t < T; t++) {
+        for (int i = 0; i < D; i++) acc[i] = 0.0;
+        for (int k = 0; k < K; k++) {
+            const int e = idx[(size_t)t * K + k];
+            const uint8_t *const *p = ptrs + (size_t)6 * e;
+            orc_expert(ye, NULL, NULL, NULL, tmp, x + (size_t)t * D,
+                       p[0], p[1], p[2], p[3], p[4], p[5], D, F);
+            const double wk = (double)w[(size_t)t * K + k];
+            for (int i = 0; i < D; i++) acc[i] += wk * (double)ye[i];
+        }
+        for (int i = 0; i < D; i++) y[(size_t)t * D + i] = (float)acc[i];
+    }
+}
+
+int orc_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
