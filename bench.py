@@ -1,0 +1,415 @@
+"""Benchmark of the MXFP4 routed-expert layer on GB300.
+
+One JSON line on rank 0.  A step is one pass of the layer over one batch of
+synthetic tokens through the public C ABI (k3mx_moe_routed): routing,
+grouping, the selected experts and the weighted sum.  The headline workload
+is the batch-1 decode step: all 896 experts (15.72 GB of packed MXFP4)
+resident in HBM, one fp32 token per step with fresh seeded router logits, so
+every step streams 16 different experts (280.8 MB).  `value` is expert bytes
+streamed per second (GB/s); the line also carries the batch-64 decode and
+4096-token prefill workloads under "secondary".
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+Timing: CUDA events on the launching stream around each step; L2 (129 MB)
+is flushed by a 256 MB write between timed steps, outside the events.
+N > 1 runs independent replicas, one per GPU (weak scaling), timed between
+barriers; rank 0 reports the maximum over ranks.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MXFP4 expert GB/s (% HBM peak) at decode; prefill tokens/s per MoE layer"
+EXPERT_BYTES = 17547264
+GATE_UP_BYTES = 2 * (5505024 + 344064)          # w1 + w3 of one expert, packed + scales
+D, F, E, K = 3584, 3072, 896, 16
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+# kernels per traced launch group
+KERNELS_PER_GROUP = {"route_group": 1, "route": 1, "group": 3, "bf16_to_f32": 1,
+                     "decode_gate_up": 1, "decode_down": 1, "combine": 1}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", FALLBACK_HBM_GBS), d.get("bf16_tflops", FALLBACK_BF16_TFLOPS), \
+            d.get("bf16_tflops_sustained"), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "mxfp4_routed_expert_k3mx_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel, workload, src_hash):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    rec = d.get(f"{kernel}/{workload}")
+    if not rec or rec.get("source_hash") != src_hash:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle samples during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ oracle --
+
+def oracle_decode_sample(steps_inputs, budget_s, max_tokens, seed=0):
+    """The CPU oracle on decode tokens of the workload until `budget_s`
+    seconds of oracle work: returns (expert bytes, seconds, tokens, cores).
+    Expert bytes are drawn on the host first, outside the timed part."""
+    import numpy as np
+    import oracle
+    import synth
+    total_s, nbytes, tokens = 0.0, 0, 0
+    for x, logits, bias in steps_inputs:
+        if total_s >= budget_s or tokens >= max_tokens:
+            break
+        idx, w = oracle.route(logits, bias)
+        experts = {int(e): synth.split_expert(synth.expert(int(e), seed=seed)) for e in np.unique(idx)}
+        t0 = time.perf_counter()
+        oracle.moe(x, idx, w, experts)
+        total_s += time.perf_counter() - t0
+        nbytes += len(experts) * EXPERT_BYTES
+        tokens += x.shape[0]
+    return nbytes, total_s, tokens, oracle.num_threads()
+
+
+def decode_inputs(step, T, seed_base=1000):
+    import synth
+    x = synth.token_inputs(T, seed=seed_base + step)
+    logits, _ = synth.router_inputs(T, seed=seed_base + step)
+    _, bias = synth.router_inputs(1, seed=0)
+    return x, logits, bias
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle, as it stands, on the machine's host cores."""
+    steps = [decode_inputs(i, 1) for i in range(args.warmup + args.steps)]
+    # warm-up steps: one token each, untimed
+    oracle_decode_sample(steps[:args.warmup], 1e9, args.warmup)
+    nbytes, secs, tokens, cores = oracle_decode_sample(steps[args.warmup:], 1e9, args.steps)
+    v = nbytes / secs / 1e9
+    line = {
+        "metric": METRIC, "value": round(v, 3), "unit": "GB/s", "impl": "reference",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * secs / max(1, args.steps), 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "moe_decode_b1", "tokens_per_step": 1, "n_experts": E, "topk": K,
+                   "latent": D, "inter": F},
+        "cpu_baseline": {"value": round(v, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{tokens} decode tokens x 16 experts (one token per step)"},
+        "e2e": {"value": round(v, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------- GPU steps --
+
+class Workload:
+    def __init__(self, name, T, x_bf16, path):
+        self.name, self.T, self.x_bf16, self.path = name, T, x_bf16, path
+
+
+def prepare(wl, n_steps, dev):
+    import numpy as np
+    import torch
+    import synth
+    xs, lgs = [], []
+    _, bias = synth.router_inputs(1, seed=0)
+    for i in range(n_steps):
+        x, logits, _ = decode_inputs(i, wl.T)
+        if wl.x_bf16:
+            xb = synth.f32_to_bf16(x)
+            xs.append(torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).to(dev))
+        else:
+            xs.append(torch.from_numpy(x).to(dev))
+        lgs.append(torch.from_numpy(logits).to(dev))
+    return xs, lgs, torch.from_numpy(bias).to(dev)
+
+
+def time_workload(k3mx, wl, table, dev, steps, warmup, dist, flush):
+    """Device-timed steps: returns dict of timings and trace."""
+    import torch
+    xs, lgs, bias = prepare(wl, warmup + steps, dev)
+    T = wl.T
+    dt = k3mx.K3MX_BF16 if wl.x_bf16 else k3mx.K3MX_F32
+    ws = torch.empty(k3mx.k3mx_moe_workspace_size(T, dt, wl.path), dtype=torch.uint8, device=dev)
+    y = torch.empty((T, D), dtype=torch.float32, device=dev)
+    idx = torch.empty((steps, T, K), dtype=torch.int32, device=dev)
+    w = torch.empty((T, K), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for i in range(warmup):
+        k3mx.k3mx_moe_routed(y, xs[i], table, lgs[i], bias, ws, path=wl.path, idx_out=idx[0], w_out=w)
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    k3mx.k3mx_trace_read()
+    k3mx.k3mx_trace_enable(True)
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        k3mx.k3mx_moe_routed(y, xs[warmup + i], table, lgs[warmup + i], bias, ws, path=wl.path,
+                             idx_out=idx[i], w_out=w)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    k3mx.k3mx_trace_enable(False)
+    trace = k3mx.k3mx_trace_read()
+    if dist is not None:
+        dist.barrier()
+    st, det = k3mx.k3mx_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} ({det})")
+    ms = [a.elapsed_time(b) for a, b in ev]
+    distinct = [int(torch.unique(idx[i]).numel()) for i in range(steps)]
+    return {"ms": ms, "trace": trace, "distinct": distinct}
+
+
+def time_e2e(k3mx, wl, table, dev, steps, warmup, flush):
+    """Steps through k3mx_moe_routed_host with pinned host buffers: the
+    host->device copies of x, logits and bias and the device->host copy of y
+    are inside the timed region."""
+    import numpy as np
+    import torch
+    import synth
+    T = wl.T
+    dt = k3mx.K3MX_BF16 if wl.x_bf16 else k3mx.K3MX_F32
+    ws = torch.empty(k3mx.k3mx_moe_host_workspace_size(T, dt, wl.path), dtype=torch.uint8, device=dev)
+    y = torch.empty((T, D), dtype=torch.float32).pin_memory()
+    _, bias = synth.router_inputs(1, seed=0)
+    bias_h = torch.from_numpy(bias).pin_memory()
+    hx, hl = [], []
+    for i in range(warmup + steps):
+        x, logits, _ = decode_inputs(i, T)
+        if wl.x_bf16:
+            hx.append(torch.from_numpy(synth.f32_to_bf16(x).view(np.int16)).view(torch.bfloat16).pin_memory())
+        else:
+            hx.append(torch.from_numpy(x).pin_memory())
+        hl.append(torch.from_numpy(logits).pin_memory())
+    for i in range(warmup):
+        k3mx.k3mx_moe_routed_host(y, hx[i], table, hl[i], bias_h, ws, path=wl.path)
+    stream = torch.cuda.current_stream(dev)
+    ms = []
+    for i in range(steps):
+        flush.zero_()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        k3mx.k3mx_moe_routed_host(y, hx[warmup + i], table, hl[warmup + i], bias_h, ws, path=wl.path)
+        b.record(stream)
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    h2d = hx[0].numel() * hx[0].element_size() + hl[0].numel() * 4 + bias_h.numel() * 4
+    d2h = y.numel() * 4
+    return ms, h2d, d2h
+
+
+def run_ours(args):
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import mxfp4_routed_expert_k3mx_gb300 as k3mx
+    import synth
+
+    hbm_peak, bf16_peak, bf16_sust, peak_src = load_peaks()
+    t0 = time.time()
+    arena = synth.expert_arena_device(dev, seed=0, lo=118, hi=128)
+    table = k3mx.expert_table(arena)
+    arena_s = time.time() - t0
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    primary = Workload("moe_decode_b1", 1, False, k3mx.K3MX_PATH_DECODE)
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    clocks = ClockSampler(f"GPU-{uuid}" if uuid is not None else str(local))
+    clocks.start()
+    res = time_workload(k3mx, primary, table, dev, args.steps, args.warmup, dist, flush)
+    clk = clocks.stop()
+
+    total_ms = sum(res["ms"])
+    bytes_total = sum(d * EXPERT_BYTES for d in res["distinct"])
+    if dist is not None:
+        t = torch.tensor([total_ms, bytes_total], dtype=torch.float64, device=dev)
+        tmax = t.clone()
+        dist.all_reduce(tmax[:1], op=dist.ReduceOp.MAX)
+        dist.all_reduce(t[1:], op=dist.ReduceOp.SUM)
+        total_ms_max, bytes_all = float(tmax[0]), float(t[1])
+    else:
+        total_ms_max, bytes_all = total_ms, float(bytes_total)
+    value = bytes_all / (total_ms_max / 1e3) / 1e9
+
+    # dominant kernel: the fused gate/up + SiTU pass (two thirds of the bytes)
+    tr = res["trace"]
+    n_launch, ms_gu = tr.get("decode_gate_up", (0, 0.0))
+    gu_bytes = sum(d * GATE_UP_BYTES for d in res["distinct"]) / max(1, len(res["distinct"]))
+    gu_bytes += primary.T * D * 4 + primary.T * K * F * 4           # x read, h written
+    achieved = gu_bytes / (ms_gu / max(1, n_launch) / 1e3) / 1e9 if n_launch else None
+    src_hash = kernel_source_hash(["decode.cu", "common.cuh"])
+    traffic = profiled_traffic("decode_gate_up", primary.name, src_hash)
+    launches = sum(KERNELS_PER_GROUP.get(k, 1) * v[0] for k, v in tr.items())
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms_max / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": "moe_decode_b1", "tokens_per_step": 1, "n_experts": E, "topk": K,
+                   "latent": D, "inter": F, "arena_gb": round(E * EXPERT_BYTES / 1e9, 2),
+                   "expert_bytes_per_step": 16 * EXPERT_BYTES, "x": "fp32 N(0,1)",
+                   "logits": "fresh seeded N(0,1) per step", "bias": "N(0,0.1)",
+                   "l2": "flushed between timed steps (256 MB write, outside the events)",
+                   "parallelism": f"replicas x{world}"},
+        "hbm_frac": round(value / world / hbm_peak, 4),
+        "hbm_frac_nominal_8tbs": round(value / world / 8000.0, 4),
+        "roofline": {"kernel": "decode_gate_up", "bound": "hbm",
+                     "achieved": round(achieved, 1) if achieved else None, "peak": hbm_peak,
+                     "unit": "GB/s", "frac": round(achieved / hbm_peak, 4) if achieved else None,
+                     "traffic": traffic, "algorithmic_bytes_per_launch": int(gu_bytes),
+                     "peak_source": f"{peak_src} HBM copy"},
+        "kernels": {k: {"launches": v[0], "avg_us": round(1e3 * v[1] / max(1, v[0]), 2)} for k, v in tr.items()},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "setup_s": {"arena": round(arena_s, 1)},
+    }
+
+    if rank == 0:
+        # end to end through the host-buffer entry point
+        e2e_ms, h2d, d2h = time_e2e(k3mx, primary, table, dev, args.steps, args.warmup, flush)
+        e2e_gbs = 16 * EXPERT_BYTES * len(e2e_ms) / (sum(e2e_ms) / 1e3) / 1e9 * world
+        line["e2e"] = {"value": round(e2e_gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": d2h, "ms_per_step": round(sum(e2e_ms) / len(e2e_ms), 4)}
+        # secondary workloads: batch 64 decode (bf16 -> fp32)
+        sec = {}
+        if not args.primary_only:
+            wl = Workload("moe_decode_b64", 64, True, k3mx.K3MX_PATH_DECODE)
+            r = time_workload(k3mx, wl, table, dev, max(3, args.steps // 2), args.warmup, None, flush)
+            ms = sum(r["ms"])
+            b = sum(d * EXPERT_BYTES for d in r["distinct"])
+            sec["moe_decode_b64"] = {"GB_s": round(b / (ms / 1e3) / 1e9, 2),
+                                     "tokens_per_s": round(64 * len(r["ms"]) / (ms / 1e3), 1),
+                                     "ms_per_step": round(ms / len(r["ms"]), 4),
+                                     "distinct_experts_per_step": round(sum(r["distinct"]) / len(r["distinct"]), 1),
+                                     "hbm_frac": round(b / (ms / 1e3) / 1e9 / hbm_peak, 4),
+                                     "kernels": {k: {"launches": v[0], "avg_us": round(1e3 * v[1] / max(1, v[0]), 2)}
+                                                 for k, v in r["trace"].items()}}
+        line["secondary"] = sec
+        if not args.no_cpu_baseline:
+            steps_in = [decode_inputs(i, 1) for i in range(64)]
+            nb, secs, toks, cores = oracle_decode_sample(steps_in, args.cpu_budget_s, 64)
+            line["cpu_baseline"] = {"value": round(nb / secs / 1e9, 3), "unit": "GB/s", "cores": cores,
+                                    "kind": "oracle",
+                                    "sample": f"{toks} decode tokens of the same workload, 16 experts each"}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--primary-only", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=10.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)            # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        if int(os.environ.get("RANK", "0")) != 0:
+            return
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

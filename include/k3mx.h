@@ -1,0 +1,230 @@
+/*
+ * k3mx.h - C ABI of the MXFP4 routed-expert layer on GB300 (sm_103a).
+ *
+ * One library, libk3mx.so, computes the Kimi-K3 Stable LatentMoE routed-expert
+ * layer straight out of packed MXFP4 weights on one GPU.  Plain pointers and
+ * sizes only: every array argument is DEVICE memory owned by the caller unless
+ * the function name ends in _host.  Nothing here allocates device memory;
+ * scratch comes from a caller-provided workspace whose size the *_workspace_size
+ * functions return.
+ *
+ * Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ * default stream).  The return value reports argument validation and launch
+ * errors only.  On any error no kernel has been enqueued and the outputs are
+ * untouched.  Device-side bounded waits that give up are reported later by
+ * k3mx_device_status().  Arguments are refused, never defaulted: a size or
+ * pointer outside what a function documents returns an error code.
+ *
+ * Weight format (Kimi K3 engine (c/kimi_k3.c), "Weights"): a matrix of
+ * `rows` x `in` weights is two arrays, both row-major:
+ *   packed [rows][in/2] bytes: e2m1 codes, two per byte, the LOW nibble is
+ *          the EVEN column; bit 3 of a code is its sign, bits 2..0 index the
+ *          magnitudes {0, 0.5, 1, 1.5, 2, 3, 4, 6};
+ *   scales [rows][in/32] bytes: one ue8m0 byte s per 32 consecutive columns,
+ *          weight = code value * 2^(s - 127); s = 255 (NaN) means the group
+ *          contributes nothing.
+ */
+#ifndef K3MX_H_
+#define K3MX_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Fixed shapes of the routed-expert layer (kimi-k3-in-c README, "2. The
+ * config reader that refuses to guess", K3Cfg: n_experts, topk, latent,
+ * moe_inter; "Part II" shard census for the byte count). */
+#define K3MX_GROUP          32
+#define K3MX_N_EXPERTS      896
+#define K3MX_TOPK           16
+#define K3MX_LATENT         3584        /* D: expert input and output width */
+#define K3MX_INTER          3072        /* F: expert intermediate width    */
+#define K3MX_EXPERT_BYTES   17547264    /* w1 + w3 + w2, packed + scales    */
+
+/* a cudaStream_t without including CUDA headers */
+typedef struct CUstream_st *k3mx_stream_t;
+
+typedef enum k3mx_status {
+    K3MX_OK = 0,
+    K3MX_EINVAL = 1,      /* NULL pointer, unknown enum value              */
+    K3MX_EALIGN = 2,      /* a pointer is not 16-byte aligned              */
+    K3MX_ESHAPE = 3,      /* a size outside the documented range           */
+    K3MX_EWORKSPACE = 4,  /* workspace NULL or smaller than required       */
+    K3MX_ECUDA = 5,       /* a CUDA runtime call or a launch failed        */
+    K3MX_ETIMEOUT = 6,    /* a bounded device-side wait gave up            */
+    K3MX_EDEVICE = 7      /* the current device is not sm_103              */
+} k3mx_status;
+
+/* activation element type */
+enum { K3MX_F32 = 0, K3MX_BF16 = 1 };
+
+/* execution path of k3mx_moe_routed */
+enum {
+    K3MX_PATH_AUTO = 0,     /* PREFILL when x is bf16 and n_tokens >= K3MX_PREFILL_MIN_TOKENS, else DECODE */
+    K3MX_PATH_DECODE = 1,   /* fp32 activations, grouped CUDA-core GEMV, fp32 h      */
+    K3MX_PATH_PREFILL = 2   /* bf16 activations, grouped tcgen05 GEMM, bf16 h        */
+};
+#define K3MX_PREFILL_MIN_TOKENS 256
+#define K3MX_MAX_TOKENS         65536
+
+/*
+ * One routed expert: six device pointers (Kimi K3 engine (c/kimi_k3.c),
+ * "Streaming design": the six tensors of an expert; "Architecture notes":
+ * GLU experts, inter 3072, in the 3584 latent).  w1 (gate) and w3 (up) are
+ * [F x D] = [3072 x 3584]; w2 (down) is [D x F] = [3584 x 3072].  Each
+ * pointer must be 16-byte aligned.
+ */
+typedef struct k3mx_expert {
+    const uint8_t *w1, *s1;     /* gate: packed [F][D/2], scales [F][D/32] */
+    const uint8_t *w3, *s3;     /* up:   packed [F][D/2], scales [F][D/32] */
+    const uint8_t *w2, *s2;     /* down: packed [D][F/2], scales [D][F/32] */
+} k3mx_expert;
+
+/*
+ * y[r] = sum_g 2^(s_rg - 127) * sum_{i<32} v(r, 32g+i) * x[32g+i]
+ * (kimi-k3-in-c: 2.78 trillion parameters, one CPU, 8 GB of RAM,
+ * "Reduction one: the experts already ship at half a byte").
+ *   y      [rows] fp32, written (not accumulated)
+ *   x      [in] fp32
+ *   packed [rows][in/2], scales [rows][in/32] as described above
+ *   in     multiple of 32, 32 <= in <= 16384;  1 <= rows <= 2^24
+ * y, x, packed must be 16-byte aligned; scales needs no alignment.
+ * fp32 products, per-group fp32 sums, fp32 row sums: |error| is within
+ * 1e-5 * sum_c |w_rc| |x_c| of the double-accumulated result.
+ */
+k3mx_status k3mx_gemv(float *y, const float *x, const uint8_t *packed,
+                      const uint8_t *scales, int in, int rows,
+                      k3mx_stream_t stream);
+
+/*
+ * One routed expert, one token (Kimi K3 engine (c/kimi_k3.c), "Architecture
+ * notes": SiTU-GLU 4 tanh(g/4) sigma(g) 25 tanh(u/25)):
+ *   g = W1 x, u = W3 x, h = SiTU(g, u), y = W2 h.
+ *   y [3584] fp32 (written), x [3584] fp32, *expert a HOST struct of device
+ *   pointers.  workspace: device, >= k3mx_expert_ffn_workspace_size() bytes,
+ *   16-byte aligned; it holds h between the two phases.
+ */
+size_t k3mx_expert_ffn_workspace_size(void);
+k3mx_status k3mx_expert_ffn(float *y, const float *x, const k3mx_expert *expert,
+                            void *workspace, size_t ws_bytes,
+                            k3mx_stream_t stream);
+
+/*
+ * Router selection (Kimi K3 engine (c/kimi_k3.c), "Architecture notes",
+ * Stable LatentMoE; kimi-k3-in-c README, "Three invariants", item 3), per
+ * token t:  s_e = sigma(logit_e) (double, rounded to fp32 once);
+ * key_e = s_e + bias_e (fp32); idx = the 16 largest keys, ties to the lower
+ * expert index, in key-descending order; w_k = s_{idx_k} / sum_j s_{idx_j}
+ * (double, rounded to fp32) * routed_scale (1.0).
+ *   idx [n_tokens][16] int32, w [n_tokens][16] fp32 (written)
+ *   logits [n_tokens][896] fp32, bias [896] fp32
+ *   1 <= n_tokens <= K3MX_MAX_TOKENS
+ * Index results are bit-identical to a CPU evaluation in the same precision.
+ */
+k3mx_status k3mx_route_topk(int32_t *idx, float *w, const float *logits,
+                            const float *bias, int n_tokens,
+                            k3mx_stream_t stream);
+
+/*
+ * Token-to-expert grouping (Kimi K3 engine (c/kimi_k3.c), "Chunked prefill":
+ * each unique expert of a chunk is loaded once for all its tokens):
+ *   counts [896]          pairs routed to each expert
+ *   offsets [897]         exclusive prefix sum of counts, offsets[896] = 16 T
+ *   perm [16 T]           pair indices p = t*16 + k sorted by (expert, p)
+ *   idx [n_tokens][16]    int32 expert ids in 0..895 (entries outside that
+ *                         range are clamped out: they are not counted and
+ *                         the device status reports K3MX_EINVAL)
+ * Bit-exact and deterministic.  workspace: device, 16-byte aligned,
+ * >= k3mx_group_workspace_size(n_tokens) bytes.
+ */
+size_t k3mx_group_workspace_size(int n_tokens);
+k3mx_status k3mx_group(int32_t *counts, int32_t *offsets, int32_t *perm,
+                       const int32_t *idx, int n_tokens,
+                       void *workspace, size_t ws_bytes,
+                       k3mx_stream_t stream);
+
+/*
+ * The routed-expert layer: route, group, run the selected experts, and form
+ * y_t = sum_k w_tk * expert_{idx_tk}(x_t) (Kimi K3 engine (c/kimi_k3.c),
+ * "Architecture notes", Stable LatentMoE).
+ *   y        [n_tokens][3584] fp32 (written)
+ *   x        [n_tokens][3584], fp32 (x_dtype K3MX_F32) or bf16 bits (K3MX_BF16)
+ *   experts  DEVICE array of 896 k3mx_expert
+ *   logits   [n_tokens][896] fp32, bias [896] fp32
+ *   path     K3MX_PATH_*; PREFILL requires bf16 x
+ *   idx_out, w_out: optional DEVICE arrays [n_tokens][16] (NULL to skip)
+ *            receiving the routing result
+ *   workspace: device, 256-byte aligned, >= k3mx_moe_workspace_size(...)
+ * DECODE keeps fp32 activations and h: |error| within 1e-5 of the
+ * abs-weighted sums.  PREFILL rounds h to bf16 and multiplies bf16 x bf16 on
+ * the tensor cores with fp32 accumulation: per-token relative L2 error
+ * within 1e-2.  DECODE is deterministic; PREFILL adds the 16 expert
+ * contributions of a token with fp32 atomics, so the order of those adds,
+ * and the last bits of y, may vary between runs.
+ */
+size_t k3mx_moe_workspace_size(int n_tokens, int x_dtype, int path);
+k3mx_status k3mx_moe_routed(float *y, const void *x, int x_dtype, int n_tokens,
+                            const k3mx_expert *experts, const float *logits,
+                            const float *bias, int path,
+                            int32_t *idx_out, float *w_out,
+                            void *workspace, size_t ws_bytes,
+                            k3mx_stream_t stream);
+
+/*
+ * k3mx_moe_routed with HOST activations, logits, bias and output: copies
+ * x, logits and bias to the workspace, runs the layer, copies y back, and
+ * waits for the stream.  Weights (experts) stay DEVICE-resident.  Host
+ * buffers may be pageable; page-locked buffers copy faster.
+ *   workspace: >= k3mx_moe_host_workspace_size(...) bytes.
+ */
+size_t k3mx_moe_host_workspace_size(int n_tokens, int x_dtype, int path);
+k3mx_status k3mx_moe_routed_host(float *y_host, const void *x_host, int x_dtype,
+                                 int n_tokens, const k3mx_expert *experts,
+                                 const float *logits_host, const float *bias_host,
+                                 int path, void *workspace, size_t ws_bytes,
+                                 k3mx_stream_t stream);
+
+/*
+ * Waits for `stream`, then reports and clears the device status word: K3MX_OK,
+ * K3MX_ETIMEOUT when a bounded device-side wait gave up since the last call,
+ * K3MX_EINVAL when a device-side range check rejected an index, K3MX_EALIGN
+ * when a weight pointer read from a device expert table is not 16-byte
+ * aligned (that expert's work is skipped), or K3MX_ECUDA
+ * when the stream reports a CUDA error.  `detail` (may be NULL) receives a
+ * kernel-specific code of the first failure.
+ */
+k3mx_status k3mx_device_status(k3mx_stream_t stream, int *detail);
+
+/*
+ * Launch tracing, a measurement aid with no counterpart on the pages.  While
+ * enabled, every kernel launch group the library issues is bracketed by a
+ * pair of CUDA events recorded on the caller's stream, so durations are
+ * those of the kernels themselves.  k3mx_trace_read waits for the recorded
+ * events, writes one entry per kernel name (launch count and summed
+ * milliseconds, at most max_entries), clears the record and returns the
+ * number of entries.  Not for streams under graph capture; not thread-safe.
+ * Events come from a fixed pool of 8192 pairs: launches beyond it are not
+ * traced.
+ */
+typedef struct k3mx_trace_entry {
+    char name[32];
+    int launches;
+    double total_ms;
+} k3mx_trace_entry;
+k3mx_status k3mx_trace_enable(int on);
+int k3mx_trace_read(k3mx_trace_entry *out, int max_entries);
+
+/* a static string naming a status code */
+const char *k3mx_status_str(k3mx_status status);
+
+/* version of this ABI, (major << 16) | minor */
+int k3mx_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* K3MX_H_ */

@@ -1,0 +1,436 @@
+// abi.cu - the extern "C" entry points of libk3mx.so: argument checks,
+// workspace layout and kernel launches.  No entry point allocates device
+// memory; scratch lives in the caller's workspace.
+#include <cstdio>
+#include <cstring>
+
+#include "common.cuh"
+#include "prefill.cuh"
+
+namespace k3mx {
+namespace {
+
+__device__ int g_status[4];       // [0] first failure code, [1] detail
+
+constexpr int kMaxDevices = 64;
+struct DevInfo {
+    bool init;
+    bool ok;
+    int num_sms;
+    int *status;
+};
+DevInfo g_dev[kMaxDevices];
+
+// Per-device set-up on first use: capability check, SM count, and the device
+// address of the status word.
+k3mx_status device_ctx(cudaStream_t stream, Ctx &c) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return K3MX_ECUDA;
+    DevInfo &di = g_dev[dev];
+    if (!di.init) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return K3MX_ECUDA;
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return K3MX_ECUDA;
+        di.ok = (major == 10 && minor == 3);
+        di.num_sms = sms;
+        di.status = static_cast<int *>(p);
+        di.init = true;
+    }
+    if (!di.ok) return K3MX_EDEVICE;
+    c.stream = stream;
+    c.num_sms = di.num_sms;
+    c.status = di.status;
+    return K3MX_OK;
+}
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned256(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+inline size_t up256(size_t n) { return (n + 255) & ~size_t(255); }
+
+bool expert_ok(const k3mx_expert *e) {
+    return e && e->w1 && e->s1 && e->w3 && e->s3 && e->w2 && e->s2 && aligned16(e->w1) &&
+           aligned16(e->s1) && aligned16(e->w3) && aligned16(e->s3) && aligned16(e->w2) &&
+           aligned16(e->s2);
+}
+
+k3mx_status from_cuda(cudaError_t err) { return err == cudaSuccess ? K3MX_OK : K3MX_ECUDA; }
+
+// ---------------------------------------------------------------- tracing --
+
+constexpr int kTracePool = 8192;
+struct TraceRec {
+    const char *name;
+    int slot;
+};
+bool g_trace_on = false;
+cudaEvent_t g_ev[kTracePool][2];
+int g_ev_made = 0;
+TraceRec g_rec[kTracePool];
+int g_nrec = 0;
+
+// Runs `launch` (a callable returning cudaError_t) between two events when
+// tracing is on.
+template <typename F>
+cudaError_t traced(const char *name, cudaStream_t s, F launch) {
+    if (!g_trace_on || g_nrec >= kTracePool) return launch();
+    const int slot = g_nrec;
+    if (slot >= g_ev_made) {
+        if (cudaEventCreate(&g_ev[slot][0]) != cudaSuccess ||
+            cudaEventCreate(&g_ev[slot][1]) != cudaSuccess)
+            return launch();
+        g_ev_made = slot + 1;
+    }
+    cudaEventRecord(g_ev[slot][0], s);
+    const cudaError_t err = launch();
+    cudaEventRecord(g_ev[slot][1], s);
+    g_rec[g_nrec++] = TraceRec{name, slot};
+    return err;
+}
+
+// ------------------------------------------------------- workspace layout --
+
+struct MoeLayout {
+    size_t idx, w, counts, offsets, act, n_active, perm, hist, xf, h, stage, total;
+    // prefill-only regions
+    size_t pre;
+    // host-variant staging
+    size_t x_in, logits_in, bias_in, y_out, total_host;
+};
+
+int resolve_path(int n_tokens, int x_dtype, int path) {
+    if (path == K3MX_PATH_AUTO)
+        return (x_dtype == K3MX_BF16 && n_tokens >= K3MX_PREFILL_MIN_TOKENS) ? K3MX_PATH_PREFILL
+                                                                             : K3MX_PATH_DECODE;
+    return path;
+}
+
+MoeLayout moe_layout(int n_tokens, int x_dtype, int path) {
+    MoeLayout L{};
+    const size_t P = (size_t)n_tokens * kK;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o += up256(bytes);
+        return at;
+    };
+    L.idx = take(P * 4);
+    L.w = take(P * 4);
+    L.counts = take(kE * 4);
+    L.offsets = take((kE + 1) * 4);
+    L.act = take(kE * 4);
+    L.n_active = take(4);
+    L.perm = take(P * 4);
+    L.hist = take(group_scratch_bytes(n_tokens));
+    if (path == K3MX_PATH_DECODE) {
+        L.xf = take(x_dtype == K3MX_BF16 ? (size_t)n_tokens * kD * 4 : 0);
+        L.h = take(P * kF * 4);
+        L.stage = take(P * kD * 4);
+    } else {
+        L.pre = take(prefill_scratch_bytes(n_tokens));
+    }
+    L.total = o;
+    L.x_in = take((size_t)n_tokens * kD * (x_dtype == K3MX_BF16 ? 2 : 4));
+    L.logits_in = take((size_t)n_tokens * kE * 4);
+    L.bias_in = take(kE * 4);
+    L.y_out = take((size_t)n_tokens * kD * 4);
+    L.total_host = o;
+    return L;
+}
+
+template <typename T>
+T *at(void *base, size_t off) {
+    return reinterpret_cast<T *>(static_cast<char *>(base) + off);
+}
+
+k3mx_status check_moe_args(const void *y, const void *x, int x_dtype, int n_tokens,
+                           const k3mx_expert *experts, const float *logits, const float *bias,
+                           int path) {
+    if (!y || !x || !experts || !logits || !bias) return K3MX_EINVAL;
+    if (x_dtype != K3MX_F32 && x_dtype != K3MX_BF16) return K3MX_EINVAL;
+    if (path < K3MX_PATH_AUTO || path > K3MX_PATH_PREFILL) return K3MX_EINVAL;
+    if (n_tokens < 1 || n_tokens > K3MX_MAX_TOKENS) return K3MX_ESHAPE;
+    if (resolve_path(n_tokens, x_dtype, path) == K3MX_PATH_PREFILL && x_dtype != K3MX_BF16)
+        return K3MX_EINVAL;
+    if (!aligned16(y) || !aligned16(x) || !aligned16(logits) || !aligned16(bias) ||
+        !aligned16(experts))
+        return K3MX_EALIGN;
+    return K3MX_OK;
+}
+
+// The layer on device buffers; `ws` is already checked.
+k3mx_status run_moe(const Ctx &c, float *y, const void *x, int x_dtype, int n_tokens,
+                    const k3mx_expert *experts, const float *logits, const float *bias, int path,
+                    int32_t *idx_out, float *w_out, void *ws, const MoeLayout &L) {
+    int32_t *idx = idx_out ? idx_out : at<int32_t>(ws, L.idx);
+    float *w = w_out ? w_out : at<float>(ws, L.w);
+    GroupOut g{at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.perm),
+               at<int32_t>(ws, L.act), at<int32_t>(ws, L.n_active)};
+    cudaError_t err;
+    if (n_tokens * kK <= 1024) {
+        err = traced("route_group", c.stream,
+                     [&] { return launch_route_group_small(c, idx, w, logits, bias, n_tokens, g); });
+    } else {
+        err = traced("route", c.stream,
+                     [&] { return launch_route(c, idx, w, logits, bias, n_tokens); });
+        if (err == cudaSuccess)
+            err = traced("group", c.stream,
+                         [&] { return launch_group(c, idx, n_tokens, g, at<void>(ws, L.hist)); });
+    }
+    if (err != cudaSuccess) return K3MX_ECUDA;
+    const int max_active = n_tokens * kK < kE ? n_tokens * kK : kE;
+
+    if (path == K3MX_PATH_PREFILL) {
+        PrefillArgs a{};
+        a.y = y;
+        a.x = static_cast<const uint16_t *>(x);
+        a.n_tokens = n_tokens;
+        a.experts = experts;
+        a.w = w;
+        a.counts = g.counts;
+        a.offsets = g.offsets;
+        a.perm = g.perm;
+        a.act = g.act;
+        a.n_active = g.n_active;
+        a.max_active = max_active;
+        a.scratch = at<void>(ws, L.pre);
+        return from_cuda(launch_prefill(c, a));  // traced per kernel inside
+    }
+
+    const float *xf = static_cast<const float *>(x);
+    if (x_dtype == K3MX_BF16) {
+        float *conv = at<float>(ws, L.xf);
+        err = traced("bf16_to_f32", c.stream, [&] {
+            return launch_bf16_to_f32(c, conv, static_cast<const uint16_t *>(x), (size_t)n_tokens * kD);
+        });
+        if (err != cudaSuccess) return K3MX_ECUDA;
+        xf = conv;
+    }
+    DecodeExperts d{experts, nullptr, g.act, g.n_active, g.offsets, g.perm, max_active};
+    float *h = at<float>(ws, L.h);
+    float *stage = at<float>(ws, L.stage);
+    err = traced("decode_gate_up", c.stream, [&] { return launch_decode_phase_a(c, d, xf, h); });
+    if (err == cudaSuccess)
+        err = traced("decode_down", c.stream, [&] { return launch_decode_phase_b(c, d, h, stage); });
+    if (err == cudaSuccess)
+        err = traced("combine", c.stream, [&] { return launch_combine(c, y, stage, w, n_tokens); });
+    return from_cuda(err);
+}
+
+}  // namespace
+}  // namespace k3mx
+
+using namespace k3mx;
+
+extern "C" {
+
+int k3mx_abi_version(void) { return (1 << 16) | 0; }
+
+const char *k3mx_status_str(k3mx_status s) {
+    switch (s) {
+    case K3MX_OK: return "ok";
+    case K3MX_EINVAL: return "invalid argument";
+    case K3MX_EALIGN: return "pointer not 16-byte aligned";
+    case K3MX_ESHAPE: return "size out of range";
+    case K3MX_EWORKSPACE: return "workspace missing or too small";
+    case K3MX_ECUDA: return "CUDA error";
+    case K3MX_ETIMEOUT: return "device wait timed out";
+    case K3MX_EDEVICE: return "device is not sm_103";
+    }
+    return "unknown status";
+}
+
+k3mx_status k3mx_gemv(float *y, const float *x, const uint8_t *packed, const uint8_t *scales,
+                      int in, int rows, k3mx_stream_t stream) {
+    if (!y || !x || !packed || !scales) return K3MX_EINVAL;
+    if (in < 32 || in > 16384 || in % 32 != 0 || rows < 1 || rows > (1 << 24)) return K3MX_ESHAPE;
+    if (!aligned16(y) || !aligned16(x) || !aligned16(packed)) return K3MX_EALIGN;
+    Ctx c;
+    k3mx_status st = device_ctx(reinterpret_cast<cudaStream_t>(stream), c);
+    if (st != K3MX_OK) return st;
+    return from_cuda(traced("gemv", c.stream,
+                            [&] { return launch_gemv(c, y, x, packed, scales, in, rows); }));
+}
+
+size_t k3mx_expert_ffn_workspace_size(void) { return (size_t)kF * sizeof(float); }
+
+k3mx_status k3mx_expert_ffn(float *y, const float *x, const k3mx_expert *expert, void *workspace,
+                            size_t ws_bytes, k3mx_stream_t stream) {
+    if (!y || !x || !expert) return K3MX_EINVAL;
+    if (!expert_ok(expert))
+        return expert->w1 && expert->s1 && expert->w3 && expert->s3 && expert->w2 && expert->s2
+                   ? K3MX_EALIGN
+                   : K3MX_EINVAL;
+    if (!aligned16(y) || !aligned16(x)) return K3MX_EALIGN;
+    if (!workspace || ws_bytes < k3mx_expert_ffn_workspace_size()) return K3MX_EWORKSPACE;
+    if (!aligned16(workspace)) return K3MX_EALIGN;
+    Ctx c;
+    k3mx_status st = device_ctx(reinterpret_cast<cudaStream_t>(stream), c);
+    if (st != K3MX_OK) return st;
+    DecodeExperts d{nullptr, expert, nullptr, nullptr, nullptr, nullptr, 1};
+    float *h = static_cast<float *>(workspace);
+    cudaError_t err = traced("decode_gate_up", c.stream, [&] { return launch_decode_phase_a(c, d, x, h); });
+    if (err == cudaSuccess)
+        err = traced("decode_down", c.stream, [&] { return launch_decode_phase_b(c, d, h, y); });
+    return from_cuda(err);
+}
+
+k3mx_status k3mx_route_topk(int32_t *idx, float *w, const float *logits, const float *bias,
+                            int n_tokens, k3mx_stream_t stream) {
+    if (!idx || !w || !logits || !bias) return K3MX_EINVAL;
+    if (n_tokens < 1 || n_tokens > K3MX_MAX_TOKENS) return K3MX_ESHAPE;
+    if (!aligned16(idx) || !aligned16(w) || !aligned16(logits) || !aligned16(bias))
+        return K3MX_EALIGN;
+    Ctx c;
+    k3mx_status st = device_ctx(reinterpret_cast<cudaStream_t>(stream), c);
+    if (st != K3MX_OK) return st;
+    return from_cuda(traced("route", c.stream,
+                            [&] { return launch_route(c, idx, w, logits, bias, n_tokens); }));
+}
+
+size_t k3mx_group_workspace_size(int n_tokens) {
+    if (n_tokens < 1 || n_tokens > K3MX_MAX_TOKENS) return 0;
+    return up256((kE + 1) * 4) + up256(kE * 4) + up256(group_scratch_bytes(n_tokens));
+}
+
+k3mx_status k3mx_group(int32_t *counts, int32_t *offsets, int32_t *perm, const int32_t *idx,
+                       int n_tokens, void *workspace, size_t ws_bytes, k3mx_stream_t stream) {
+    if (!counts || !offsets || !perm || !idx) return K3MX_EINVAL;
+    if (n_tokens < 1 || n_tokens > K3MX_MAX_TOKENS) return K3MX_ESHAPE;
+    if (!aligned16(counts) || !aligned16(offsets) || !aligned16(perm) || !aligned16(idx))
+        return K3MX_EALIGN;
+    if (!workspace || ws_bytes < k3mx_group_workspace_size(n_tokens)) return K3MX_EWORKSPACE;
+    if (!aligned16(workspace)) return K3MX_EALIGN;
+    Ctx c;
+    k3mx_status st = device_ctx(reinterpret_cast<cudaStream_t>(stream), c);
+    if (st != K3MX_OK) return st;
+    // the active-expert list is a by-product of the scan: keep it in the workspace
+    char *ws = static_cast<char *>(workspace);
+    GroupOut g{counts, offsets, perm, reinterpret_cast<int32_t *>(ws + up256((kE + 1) * 4)),
+               reinterpret_cast<int32_t *>(ws)};
+    return from_cuda(traced("group", c.stream, [&] {
+        return launch_group(c, idx, n_tokens, g, ws + up256((kE + 1) * 4) + up256(kE * 4));
+    }));
+}
+
+size_t k3mx_moe_workspace_size(int n_tokens, int x_dtype, int path) {
+    if (n_tokens < 1 || n_tokens > K3MX_MAX_TOKENS) return 0;
+    if (x_dtype != K3MX_F32 && x_dtype != K3MX_BF16) return 0;
+    return moe_layout(n_tokens, x_dtype, resolve_path(n_tokens, x_dtype, path)).total;
+}
+
+size_t k3mx_moe_host_workspace_size(int n_tokens, int x_dtype, int path) {
+    if (n_tokens < 1 || n_tokens > K3MX_MAX_TOKENS) return 0;
+    if (x_dtype != K3MX_F32 && x_dtype != K3MX_BF16) return 0;
+    return moe_layout(n_tokens, x_dtype, resolve_path(n_tokens, x_dtype, path)).total_host;
+}
+
+k3mx_status k3mx_moe_routed(float *y, const void *x, int x_dtype, int n_tokens,
+                            const k3mx_expert *experts, const float *logits, const float *bias,
+                            int path, int32_t *idx_out, float *w_out, void *workspace,
+                            size_t ws_bytes, k3mx_stream_t stream) {
+    k3mx_status st = check_moe_args(y, x, x_dtype, n_tokens, experts, logits, bias, path);
+    if (st != K3MX_OK) return st;
+    if ((idx_out && !aligned16(idx_out)) || (w_out && !aligned16(w_out))) return K3MX_EALIGN;
+    path = resolve_path(n_tokens, x_dtype, path);
+    const MoeLayout L = moe_layout(n_tokens, x_dtype, path);
+    if (!workspace || ws_bytes < L.total) return K3MX_EWORKSPACE;
+    if (!aligned256(workspace)) return K3MX_EALIGN;
+    Ctx c;
+    st = device_ctx(reinterpret_cast<cudaStream_t>(stream), c);
+    if (st != K3MX_OK) return st;
+    return run_moe(c, y, x, x_dtype, n_tokens, experts, logits, bias, path, idx_out, w_out,
+                   workspace, L);
+}
+
+k3mx_status k3mx_moe_routed_host(float *y_host, const void *x_host, int x_dtype, int n_tokens,
+                                 const k3mx_expert *experts, const float *logits_host,
+                                 const float *bias_host, int path, void *workspace,
+                                 size_t ws_bytes, k3mx_stream_t stream) {
+    if (!y_host || !x_host || !logits_host || !bias_host || !experts) return K3MX_EINVAL;
+    if (x_dtype != K3MX_F32 && x_dtype != K3MX_BF16) return K3MX_EINVAL;
+    if (path < K3MX_PATH_AUTO || path > K3MX_PATH_PREFILL) return K3MX_EINVAL;
+    if (n_tokens < 1 || n_tokens > K3MX_MAX_TOKENS) return K3MX_ESHAPE;
+    path = resolve_path(n_tokens, x_dtype, path);
+    if (path == K3MX_PATH_PREFILL && x_dtype != K3MX_BF16) return K3MX_EINVAL;
+    if (!aligned16(experts)) return K3MX_EALIGN;
+    const MoeLayout L = moe_layout(n_tokens, x_dtype, path);
+    if (!workspace || ws_bytes < L.total_host) return K3MX_EWORKSPACE;
+    if (!aligned256(workspace)) return K3MX_EALIGN;
+    Ctx c;
+    k3mx_status st = device_ctx(reinterpret_cast<cudaStream_t>(stream), c);
+    if (st != K3MX_OK) return st;
+    const size_t xb = (size_t)n_tokens * kD * (x_dtype == K3MX_BF16 ? 2 : 4);
+    void *x_dev = at<void>(workspace, L.x_in);
+    float *logits_dev = at<float>(workspace, L.logits_in);
+    float *bias_dev = at<float>(workspace, L.bias_in);
+    float *y_dev = at<float>(workspace, L.y_out);
+    cudaStream_t s = c.stream;
+    if (cudaMemcpyAsync(x_dev, x_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(logits_dev, logits_host, (size_t)n_tokens * kE * 4, cudaMemcpyHostToDevice,
+                        s) != cudaSuccess ||
+        cudaMemcpyAsync(bias_dev, bias_host, kE * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return K3MX_ECUDA;
+    st = run_moe(c, y_dev, x_dev, x_dtype, n_tokens, experts, logits_dev, bias_dev, path, nullptr,
+                 nullptr, workspace, L);
+    if (st != K3MX_OK) return st;
+    if (cudaMemcpyAsync(y_host, y_dev, (size_t)n_tokens * kD * 4, cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return K3MX_ECUDA;
+    return K3MX_OK;
+}
+
+k3mx_status k3mx_trace_enable(int on) {
+    g_trace_on = on != 0;
+    return K3MX_OK;
+}
+
+int k3mx_trace_read(k3mx_trace_entry *out, int max_entries) {
+    int n = 0;
+    for (int i = 0; i < g_nrec; i++) {
+        const TraceRec &r = g_rec[i];
+        float ms = 0.f;
+        if (cudaEventSynchronize(g_ev[r.slot][1]) != cudaSuccess ||
+            cudaEventElapsedTime(&ms, g_ev[r.slot][0], g_ev[r.slot][1]) != cudaSuccess)
+            continue;
+        int j = 0;
+        while (j < n && std::strncmp(out[j].name, r.name, sizeof(out[j].name)) != 0) j++;
+        if (j == n) {
+            if (n >= max_entries) continue;
+            std::memset(&out[n], 0, sizeof(out[n]));
+            std::strncpy(out[n].name, r.name, sizeof(out[n].name) - 1);
+            n++;
+        }
+        out[j].launches++;
+        out[j].total_ms += ms;
+    }
+    g_nrec = 0;
+    return n;
+}
+
+k3mx_status k3mx_device_status(k3mx_stream_t stream, int *detail) {
+    Ctx c;
+    k3mx_status st = device_ctx(reinterpret_cast<cudaStream_t>(stream), c);
+    if (st != K3MX_OK) return st;
+    if (cudaStreamSynchronize(c.stream) != cudaSuccess) return K3MX_ECUDA;
+    int word[2] = {0, 0};
+    if (cudaMemcpy(word, c.status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return K3MX_ECUDA;
+    const int zero[2] = {0, 0};
+    if (cudaMemcpy(c.status, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+        return K3MX_ECUDA;
+    if (detail) *detail = word[1];
+    switch (word[0]) {
+    case kStatusOk: return K3MX_OK;
+    case kStatusBadIndex: return K3MX_EINVAL;
+    case kStatusWaitTimeout: return K3MX_ETIMEOUT;
+    case kStatusBadPointer: return K3MX_EALIGN;
+    default: return K3MX_ECUDA;
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,250 @@
+// common.cuh - shapes, MXFP4 decoding helpers and launch plumbing shared by
+// the sm_103a kernels of the MXFP4 routed-expert layer.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+
+#include "k3mx.h"
+
+namespace k3mx {
+
+// Kimi-K3 routed-expert shapes (kimi-k3-in-c README, K3Cfg).
+constexpr int kD = K3MX_LATENT;      // 3584
+constexpr int kF = K3MX_INTER;       // 3072
+constexpr int kE = K3MX_N_EXPERTS;   // 896
+constexpr int kK = K3MX_TOPK;        // 16
+constexpr int kG = K3MX_GROUP;       // 32 columns per ue8m0 scale
+
+// device status word codes (first failure wins)
+enum : int {
+    kStatusOk = 0,
+    kStatusBadIndex = 1,       // an expert index outside 0..895 reached a kernel
+    kStatusWaitTimeout = 2,    // a bounded mbarrier / flag wait gave up
+    kStatusBadPointer = 3,     // a weight pointer from a device table is not 16-byte aligned
+};
+
+// Per-launch context shared by the launchers: stream, SM count, status word.
+struct Ctx {
+    cudaStream_t stream;
+    int num_sms;
+    int *status;               // device int[4]: [0] first code, [1] detail
+};
+
+// ---------------------------------------------------------------- decoding --
+//
+// MXFP4 (Kimi K3 engine (c/kimi_k3.c), "Weights"): e2m1 codes two per byte,
+// the low nibble is the even column, bit 3 is the sign; one ue8m0 byte per
+// 32 columns, weight = value * 2^(s - 127), s = 255 contributes nothing.
+//
+// The decode uses the sm_100-family conversion cvt.rn.f16x2.e2m1x2, which
+// turns one byte (two codes) into two exact halves: the low nibble lands in
+// the low half.  Every e2m1 value is exact in f16 and in fp32.
+
+__device__ __forceinline__ void e2m1x8_to_h2x4(uint32_t q, uint32_t (&h)[4]) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(q));
+}
+
+__device__ __forceinline__ float2 h2_to_f2(uint32_t h) {
+    __half2 v = *reinterpret_cast<__half2 *>(&h);
+    return __half22float2(v);
+}
+
+// 2^(s - 127) for a ue8m0 byte s in 0..254 (s = 0 is the fp32 subnormal 2^-127)
+__device__ __forceinline__ float e8m0_to_f32(uint32_t s) {
+    return s == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(s << 23);
+}
+
+// One 32-column group: sum_i v_i x_i in fp32.  `w` holds the group's 16
+// packed bytes; `x` holds its 32 activations as 16 (even, odd) pairs.  Two
+// packed-fp32 accumulators (bytes 0,2 and 1,3 of each word) keep the FMA
+// chains short; they are added at the end in a fixed order.
+__device__ __forceinline__ float group_dot(const uint4 &w, const float2 (&x)[16]) {
+    float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+    const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        uint32_t h[4];
+        e2m1x8_to_h2x4(words[q], h);
+        a0 = __ffma2_rn(h2_to_f2(h[0]), x[4 * q + 0], a0);
+        a1 = __ffma2_rn(h2_to_f2(h[1]), x[4 * q + 1], a1);
+        a0 = __ffma2_rn(h2_to_f2(h[2]), x[4 * q + 2], a0);
+        a1 = __ffma2_rn(h2_to_f2(h[3]), x[4 * q + 3], a1);
+    }
+    return (a0.x + a1.x) + (a0.y + a1.y);
+}
+
+// the scaled contribution of one group; a NaN scale (255) contributes 0 even
+// when the activations hold inf or NaN
+__device__ __forceinline__ float group_term(const uint4 &w, uint32_t s, const float2 (&x)[16]) {
+    const float d = group_dot(w, x);
+    return s == 255u ? 0.f : d * e8m0_to_f32(s);
+}
+
+// 32 fp32 activations of group g from a row of fp32 values (read-only path)
+__device__ __forceinline__ void load_x_group(const float *row, int g, float2 (&x)[16]) {
+    const float4 *p = reinterpret_cast<const float4 *>(row + 32 * g);
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        float4 v = __ldg(p + j);
+        x[2 * j] = make_float2(v.x, v.y);
+        x[2 * j + 1] = make_float2(v.z, v.w);
+    }
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const void *p) {
+    // weights are read once: do not keep them in L1
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ldg_u8(const uint8_t *p) {
+    return (uint32_t)__ldg(p);
+}
+
+// SiTU-GLU (Kimi K3 engine (c/kimi_k3.c), "Architecture notes"; betas 4.0 and
+// 25.0 from K3Cfg): 4 tanh(g/4) sigma(g) * 25 tanh(u/25), in fp32.
+__device__ __forceinline__ float situ_glu(float g, float u) {
+    const float sig = 1.0f / (1.0f + expf(-g));
+    return (4.0f * tanhf(g * 0.25f) * sig) * (25.0f * tanhf(u / 25.0f));
+}
+
+__device__ __forceinline__ void report_status(int *status, int code, int detail) {
+    if (status != nullptr && atomicCAS(status, 0, code) == 0) status[1] = detail;
+}
+
+// --------------------------------------------- async copies and barriers --
+//
+// Hand-written PTX for the bulk-copy engine (cp.async.bulk) and mbarriers.
+// Every wait is bounded: after kWaitLimit polls it gives up and the caller
+// reports kStatusWaitTimeout instead of spinning forever.
+
+constexpr uint32_t kWaitLimit = 1u << 22;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// true when the phase of parity `parity` completed, false after kWaitLimit polls
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kWaitLimit; i++)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+// L2 policy for data read exactly once (weights): evict first
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 1-D bulk copy global -> shared; completion is counted on `bar` in bytes.
+// dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(const uint8_t *p) {
+    return *reinterpret_cast<const uint4 *>(p);
+}
+
+// programmatic dependent launch: let the next kernel in the stream start its
+// independent prologue; wait until the previous kernel's results are visible
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ------------------------------------------------------------ launchers --
+// (defined in the .cu files; called by the C-ABI layer)
+
+struct GroupOut {
+    int32_t *counts;     // [896]
+    int32_t *offsets;    // [897]
+    int32_t *perm;       // [16 T]
+    int32_t *act;        // [896] active experts, increasing id
+    int32_t *n_active;   // [1]
+};
+
+cudaError_t launch_route(const Ctx &c, int32_t *idx, float *w, const float *logits,
+                         const float *bias, int n_tokens);
+// route + group in one CTA (n_tokens * 16 <= 1024)
+cudaError_t launch_route_group_small(const Ctx &c, int32_t *idx, float *w, const float *logits,
+                                     const float *bias, int n_tokens, const GroupOut &g);
+size_t group_scratch_bytes(int n_tokens);
+cudaError_t launch_group(const Ctx &c, const int32_t *idx, int n_tokens, const GroupOut &g,
+                         void *scratch);
+
+cudaError_t launch_gemv(const Ctx &c, float *y, const float *x, const uint8_t *packed,
+                        const uint8_t *scales, int in, int rows);
+
+// Decode path over the grouped pairs.  x: [T][D] fp32; h: [16T][F] fp32;
+// stage: [16T][D] fp32; y: [T][D] fp32.  When `single` is non-null the
+// grouping arguments are ignored and the one expert runs for token 0.
+struct DecodeExperts {
+    const k3mx_expert *experts;   // device [896]
+    const k3mx_expert *single;    // host struct, or nullptr
+    const int32_t *act, *n_active, *offsets, *perm;
+    int max_active;               // upper bound of *n_active
+};
+cudaError_t launch_decode_phase_a(const Ctx &c, const DecodeExperts &d, const float *x, float *h);
+cudaError_t launch_decode_phase_b(const Ctx &c, const DecodeExperts &d, const float *h,
+                                  float *stage);
+cudaError_t launch_combine(const Ctx &c, float *y, const float *stage, const float *w,
+                           int n_tokens);
+cudaError_t launch_bf16_to_f32(const Ctx &c, float *out, const uint16_t *in, size_t n);
+
+}  // namespace k3mx

@@ -1,0 +1,21 @@
+// prefill.cuh - grouped tcgen05 GEMM path for bf16 activations (many tokens).
+#pragma once
+#include "common.cuh"
+
+namespace k3mx {
+
+struct PrefillArgs {
+    float *y;                      // [T][D] fp32, written
+    const uint16_t *x;             // [T][D] bf16 bits
+    int n_tokens;
+    const k3mx_expert *experts;    // device [896]
+    const float *w;                // [T][16] routing weights
+    const int32_t *counts, *offsets, *perm, *act, *n_active;
+    int max_active;
+    void *scratch;                 // prefill_scratch_bytes(n_tokens), 256-byte aligned
+};
+
+size_t prefill_scratch_bytes(int n_tokens);
+cudaError_t launch_prefill(const Ctx &c, const PrefillArgs &a);
+
+}  // namespace k3mx

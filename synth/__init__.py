@@ -162,3 +162,30 @@ def router_inputs(n_tokens, seed=0, E=N_EXPERTS, bias_std=0.1):
     logits = normal_f32(n_tokens * E, seed, STREAM_LOGITS).reshape(n_tokens, E)
     bias = normal_f32(E, seed, STREAM_BIAS, 0.0, bias_std)
     return logits, bias
+
+
+def expert_arena_device(device, seed=0, lo=118, hi=128, n_experts=N_EXPERTS, chunk=16):
+    """All routed experts drawn with `seed`, back to back in one device buffer
+    (896 x 17,547,264 B = 15.72 GB), copied through two pinned staging
+    buffers.  Returns a torch uint8 tensor on `device`."""
+    import torch
+    n = expert_nbytes()
+    buf = torch.empty(n_experts * n, dtype=torch.uint8, device=device)
+    stage = [torch.empty(chunk * n, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    events = [None, None]
+    stream = torch.cuda.current_stream(device)
+    for i, e0 in enumerate(range(0, n_experts, chunk)):
+        m = min(chunk, n_experts - e0)
+        s = stage[i % 2]
+        if events[i % 2] is not None:
+            events[i % 2].synchronize()
+        host = s.numpy()
+        for j in range(m):
+            expert(e0 + j, seed=seed, lo=lo, hi=hi, out=host[j * n:(j + 1) * n])
+        with torch.cuda.stream(stream):
+            buf[e0 * n:(e0 + m) * n].copy_(s[:m * n], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(stream)
+        events[i % 2] = ev
+    torch.cuda.synchronize(device)
+    return buf

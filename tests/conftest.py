@@ -22,3 +22,30 @@ def read_golden(name):
                 k, v = line.split(None, 1)
                 out[k] = v.strip()
     return out
+
+
+# ------------------------------------------------------------ GPU fixtures --
+
+ARENA_SEED = 0
+ARENA_SCALE_LO, ARENA_SCALE_HI = 118, 128
+
+
+@pytest.fixture(scope="session")
+def cuda_dev():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    return torch.device("cuda:0")
+
+
+@pytest.fixture(scope="session")
+def arena(cuda_dev):
+    """All 896 routed experts of the seeded workload, back to back in one
+    device buffer (about 15.7 GB), and their pointer table."""
+    import synth
+    import mxfp4_routed_expert_k3mx_gb300 as k3mx
+    buf = synth.expert_arena_device(cuda_dev, seed=ARENA_SEED, lo=ARENA_SCALE_LO, hi=ARENA_SCALE_HI)
+    table = k3mx.expert_table(buf)
+    return buf, table

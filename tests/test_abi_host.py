@@ -1,0 +1,90 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every function include/k3mx.h declares, and refuses bad arguments before it
+touches the device."""
+import re
+import subprocess
+
+import pytest
+import torch
+
+import mxfp4_routed_expert_k3mx_gb300 as k3mx
+
+FAKE = 0x10000          # an aligned, non-null address that is never dereferenced
+
+
+def test_library_exports_every_declared_symbol():
+    L = k3mx.lib()
+    declared = k3mx.declared_symbols()
+    assert len(declared) == 15
+    out = subprocess.run(["nm", "-D", "--defined-only", k3mx.LIB_PATH],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\sT\s(k3mx_\w+)", out))
+    assert set(declared) <= exported, set(declared) - exported
+    for name in declared:
+        assert hasattr(L, name)
+
+
+def test_status_strings_and_version():
+    assert k3mx.k3mx_abi_version() >> 16 == 1
+    for code in range(8):
+        assert k3mx.k3mx_status_str(code)
+    assert k3mx.k3mx_status_str(99) == "unknown status"
+
+
+def test_gemv_refuses_bad_arguments():
+    L = k3mx.lib()
+    assert L.k3mx_gemv(None, FAKE, FAKE, FAKE, 64, 4, None) == 1            # NULL
+    assert L.k3mx_gemv(FAKE, FAKE, FAKE, FAKE, 33, 4, None) == 3            # in % 32
+    assert L.k3mx_gemv(FAKE, FAKE, FAKE, FAKE, 0, 4, None) == 3
+    assert L.k3mx_gemv(FAKE, FAKE, FAKE, FAKE, 16384 + 32, 4, None) == 3    # in too large
+    assert L.k3mx_gemv(FAKE, FAKE, FAKE, FAKE, 64, 0, None) == 3            # rows < 1
+    assert L.k3mx_gemv(FAKE + 4, FAKE, FAKE, FAKE, 64, 4, None) == 2        # y misaligned
+    assert L.k3mx_gemv(FAKE, FAKE, FAKE + 8, FAKE, 64, 4, None) == 2        # packed misaligned
+
+
+def test_route_group_refuse_bad_arguments():
+    L = k3mx.lib()
+    assert L.k3mx_route_topk(FAKE, FAKE, FAKE, None, 1, None) == 1
+    assert L.k3mx_route_topk(FAKE, FAKE, FAKE, FAKE, 0, None) == 3
+    assert L.k3mx_route_topk(FAKE, FAKE, FAKE, FAKE, 65537, None) == 3
+    assert L.k3mx_route_topk(FAKE, FAKE + 4, FAKE, FAKE, 1, None) == 2
+    ws = k3mx.k3mx_group_workspace_size(64)
+    assert ws > 0 and k3mx.k3mx_group_workspace_size(0) == 0
+    assert L.k3mx_group(FAKE, FAKE, FAKE, FAKE, 64, FAKE, ws - 1, None) == 4
+    assert L.k3mx_group(FAKE, FAKE, FAKE, FAKE, 64, None, ws, None) == 4
+
+
+def test_moe_refuses_bad_arguments():
+    L = k3mx.lib()
+    ws = k3mx.k3mx_moe_workspace_size(1, k3mx.K3MX_F32, k3mx.K3MX_PATH_DECODE)
+    args = lambda **kw: dict(dict(y=FAKE, x=FAKE, dt=0, T=1, ex=FAKE, lg=FAKE, b=FAKE, path=1,
+                                  io=None, wo=None, ws=FAKE, wsb=ws), **kw)
+    call = lambda a: L.k3mx_moe_routed(a["y"], a["x"], a["dt"], a["T"], a["ex"], a["lg"], a["b"],
+                                       a["path"], a["io"], a["wo"], a["ws"], a["wsb"], None)
+    assert call(args(ex=None)) == 1
+    assert call(args(dt=2)) == 1                     # unknown dtype
+    assert call(args(path=3)) == 1                   # unknown path
+    assert call(args(path=2)) == 1                   # prefill needs bf16 x
+    assert call(args(T=0)) == 3
+    assert call(args(x=FAKE + 2)) == 2
+    assert call(args(wsb=ws - 1)) == 4
+    assert call(args(ws=FAKE + 16)) == 2             # workspace must be 256-byte aligned
+
+
+def test_workspace_sizes():
+    d = [k3mx.k3mx_moe_workspace_size(t, 0, 1) for t in (1, 2, 64, 1000)]
+    assert all(a < b for a, b in zip(d, d[1:]))
+    # the decode path keeps h and the per-pair outputs in fp32
+    assert k3mx.k3mx_moe_workspace_size(64, 0, 1) >= 64 * 16 * (3072 + 3584) * 4
+    # AUTO picks prefill for bf16 and many tokens; its h is bf16
+    assert k3mx.k3mx_moe_workspace_size(4096, 1, 0) == k3mx.k3mx_moe_workspace_size(4096, 1, 2)
+    assert k3mx.k3mx_moe_workspace_size(4096, 1, 2) >= 4096 * 16 * 3072 * 2
+    assert k3mx.k3mx_moe_host_workspace_size(64, 1, 1) > k3mx.k3mx_moe_workspace_size(64, 1, 1)
+    assert k3mx.k3mx_expert_ffn_workspace_size() == 3072 * 4
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU behaviour only")
+def test_valid_call_without_gpu_fails_loudly():
+    """With no device the library reports a CUDA error; it has no CPU path."""
+    L = k3mx.lib()
+    assert L.k3mx_gemv(FAKE, FAKE, FAKE, FAKE, 64, 4, None) in (5, 7)
