@@ -105,7 +105,7 @@ k3mx_status k3mx_gemv(float *y, const float *x, const uint8_t *packed,
  *   g = W1 x, u = W3 x, h = SiTU(g, u), y = W2 h.
  *   y [3584] fp32 (written), x [3584] fp32, *expert a HOST struct of device
  *   pointers.  workspace: device, >= k3mx_expert_ffn_workspace_size() bytes,
- *   16-byte aligned; it holds h between the two phases.
+ *   16-byte aligned; it holds g and u between the two phases ([2][3072] fp32).
  */
 size_t k3mx_expert_ffn_workspace_size(void);
 k3mx_status k3mx_expert_ffn(float *y, const float *x, const k3mx_expert *expert,

@@ -94,7 +94,7 @@ cudaError_t traced(const char *name, cudaStream_t s, F launch) {
 // ------------------------------------------------------- workspace layout --
 
 struct MoeLayout {
-    size_t idx, w, counts, offsets, act, n_active, perm, hist, xf, h, stage, total;
+    size_t idx, w, counts, offsets, act, n_active, units, n_units, perm, hist, xf, h, stage, total;
     // prefill-only regions
     size_t pre;
     // host-variant staging
@@ -123,11 +123,13 @@ MoeLayout moe_layout(int n_tokens, int x_dtype, int path) {
     L.offsets = take((kE + 1) * 4);
     L.act = take(kE * 4);
     L.n_active = take(4);
+    L.units = take((size_t)max_units(n_tokens) * 3 * 4);
+    L.n_units = take(4);
     L.perm = take(P * 4);
     L.hist = take(group_scratch_bytes(n_tokens));
     if (path == K3MX_PATH_DECODE) {
         L.xf = take(x_dtype == K3MX_BF16 ? (size_t)n_tokens * kD * 4 : 0);
-        L.h = take(P * kF * 4);
+        L.h = take(P * 2 * kF * 4);          // g and u per pair
         L.stage = take(P * kD * 4);
     } else {
         L.pre = take(prefill_scratch_bytes(n_tokens));
@@ -168,7 +170,8 @@ k3mx_status run_moe(const Ctx &c, float *y, const void *x, int x_dtype, int n_to
     int32_t *idx = idx_out ? idx_out : at<int32_t>(ws, L.idx);
     float *w = w_out ? w_out : at<float>(ws, L.w);
     GroupOut g{at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.perm),
-               at<int32_t>(ws, L.act), at<int32_t>(ws, L.n_active)};
+               at<int32_t>(ws, L.act), at<int32_t>(ws, L.n_active), at<int32_t>(ws, L.units),
+               at<int32_t>(ws, L.n_units)};
     cudaError_t err;
     if (n_tokens * kK <= 1024) {
         err = traced("route_group", c.stream,
@@ -209,7 +212,7 @@ k3mx_status run_moe(const Ctx &c, float *y, const void *x, int x_dtype, int n_to
         if (err != cudaSuccess) return K3MX_ECUDA;
         xf = conv;
     }
-    DecodeExperts d{experts, nullptr, g.act, g.n_active, g.offsets, g.perm, max_active};
+    DecodeExperts d{experts, nullptr, g.units, g.n_units, g.perm, max_units(n_tokens)};
     float *h = at<float>(ws, L.h);
     float *stage = at<float>(ws, L.stage);
     err = traced("decode_gate_up", c.stream, [&] { return launch_decode_phase_a(c, d, xf, h); });
@@ -255,7 +258,7 @@ k3mx_status k3mx_gemv(float *y, const float *x, const uint8_t *packed, const uin
                             [&] { return launch_gemv(c, y, x, packed, scales, in, rows); }));
 }
 
-size_t k3mx_expert_ffn_workspace_size(void) { return (size_t)kF * sizeof(float); }
+size_t k3mx_expert_ffn_workspace_size(void) { return (size_t)2 * kF * sizeof(float); }
 
 k3mx_status k3mx_expert_ffn(float *y, const float *x, const k3mx_expert *expert, void *workspace,
                             size_t ws_bytes, k3mx_stream_t stream) {
@@ -270,7 +273,7 @@ k3mx_status k3mx_expert_ffn(float *y, const float *x, const k3mx_expert *expert,
     Ctx c;
     k3mx_status st = device_ctx(reinterpret_cast<cudaStream_t>(stream), c);
     if (st != K3MX_OK) return st;
-    DecodeExperts d{nullptr, expert, nullptr, nullptr, nullptr, nullptr, 1};
+    DecodeExperts d{nullptr, expert, nullptr, nullptr, nullptr, 1};
     float *h = static_cast<float *>(workspace);
     cudaError_t err = traced("decode_gate_up", c.stream, [&] { return launch_decode_phase_a(c, d, x, h); });
     if (err == cudaSuccess)
@@ -310,7 +313,7 @@ k3mx_status k3mx_group(int32_t *counts, int32_t *offsets, int32_t *perm, const i
     // the active-expert list is a by-product of the scan: keep it in the workspace
     char *ws = static_cast<char *>(workspace);
     GroupOut g{counts, offsets, perm, reinterpret_cast<int32_t *>(ws + up256((kE + 1) * 4)),
-               reinterpret_cast<int32_t *>(ws)};
+               reinterpret_cast<int32_t *>(ws), nullptr, nullptr};
     return from_cuda(traced("group", c.stream, [&] {
         return launch_group(c, idx, n_tokens, g, ws + up256((kE + 1) * 4) + up256(kE * 4));
     }));

@@ -154,14 +154,18 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// one poll; the thread may sleep in hardware up to kWaitSuspendNs while the
+// phase is incomplete, so waiting warps do not compete for issue slots
+constexpr uint32_t kWaitSuspendNs = 2000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(kWaitSuspendNs)
         : "memory");
     return ok != 0;
 }
@@ -211,12 +215,23 @@ __device__ __forceinline__ void pdl_wait() {
 // ------------------------------------------------------------ launchers --
 // (defined in the .cu files; called by the C-ABI layer)
 
+// Work units of the decode kernels: each active expert's pairs cut into
+// runs of at most kUnitPairs, so one unit has one fixed token set.
+constexpr int kUnitPairs = 4;
+inline int max_units(int n_tokens) {
+    const int pairs = n_tokens * kK;
+    const int experts = pairs < kE ? pairs : kE;
+    return pairs / kUnitPairs + experts;
+}
+
 struct GroupOut {
     int32_t *counts;     // [896]
     int32_t *offsets;    // [897]
     int32_t *perm;       // [16 T]
     int32_t *act;        // [896] active experts, increasing id
     int32_t *n_active;   // [1]
+    int32_t *units;      // [max_units][3]: expert, first pair slot, end slot (or null)
+    int32_t *n_units;    // [1] (or null)
 };
 
 cudaError_t launch_route(const Ctx &c, int32_t *idx, float *w, const float *logits,
@@ -231,17 +246,18 @@ cudaError_t launch_group(const Ctx &c, const int32_t *idx, int n_tokens, const G
 cudaError_t launch_gemv(const Ctx &c, float *y, const float *x, const uint8_t *packed,
                         const uint8_t *scales, int in, int rows);
 
-// Decode path over the grouped pairs.  x: [T][D] fp32; h: [16T][F] fp32;
-// stage: [16T][D] fp32; y: [T][D] fp32.  When `single` is non-null the
-// grouping arguments are ignored and the one expert runs for token 0.
+// Decode path over the grouped pairs.  x: [T][D] fp32; gu: [16T][2][F] fp32
+// (g = W1 x and u = W3 x per pair); stage: [16T][D] fp32 (W2 SiTU(g, u) per
+// pair); y: [T][D] fp32.  When `single` is non-null the grouping arguments
+// are ignored and the one expert runs for token 0.
 struct DecodeExperts {
     const k3mx_expert *experts;   // device [896]
     const k3mx_expert *single;    // host struct, or nullptr
-    const int32_t *act, *n_active, *offsets, *perm;
-    int max_active;               // upper bound of *n_active
+    const int32_t *units, *n_units, *perm;
+    int max_units;                // upper bound of *n_units
 };
-cudaError_t launch_decode_phase_a(const Ctx &c, const DecodeExperts &d, const float *x, float *h);
-cudaError_t launch_decode_phase_b(const Ctx &c, const DecodeExperts &d, const float *h,
+cudaError_t launch_decode_phase_a(const Ctx &c, const DecodeExperts &d, const float *x, float *gu);
+cudaError_t launch_decode_phase_b(const Ctx &c, const DecodeExperts &d, const float *gu,
                                   float *stage);
 cudaError_t launch_combine(const Ctx &c, float *y, const float *stage, const float *w,
                            int n_tokens);

@@ -275,9 +275,12 @@ __device__ void finish_counts(int *cnt_sm, const GroupOut &g, int *tmp) {
         sum += c[j];
         nz += c[j] > 0;
     }
-    int total, n_act;
+    int nu = 0;
+    for (int j = 0; j < ept; j++) nu += (c[j] + kUnitPairs - 1) / kUnitPairs;
+    int total, n_act, n_un;
     int off = block_excl_scan(sum, tmp, &total);
     int apos = block_excl_scan(nz, tmp, &n_act);
+    int upos = block_excl_scan(nu, tmp, &n_un);
     for (int j = 0; j < ept; j++) {
         const int e = e0 + j;
         if (e < kE) {
@@ -285,12 +288,19 @@ __device__ void finish_counts(int *cnt_sm, const GroupOut &g, int *tmp) {
             g.offsets[e] = off;
             cnt_sm[e] = off;
             if (c[j] > 0) g.act[apos++] = e;
+            if (g.units != nullptr)
+                for (int q = 0; q < c[j]; q += kUnitPairs, upos++) {
+                    g.units[3 * upos + 0] = e;
+                    g.units[3 * upos + 1] = off + q;
+                    g.units[3 * upos + 2] = off + min(q + kUnitPairs, c[j]);
+                }
             off += c[j];
         }
     }
     if (threadIdx.x == 0) {
         g.offsets[kE] = total;
         *g.n_active = n_act;
+        if (g.n_units != nullptr) *g.n_units = n_un;
     }
     __syncthreads();
 }

@@ -75,12 +75,12 @@ def test_workspace_sizes():
     d = [k3mx.k3mx_moe_workspace_size(t, 0, 1) for t in (1, 2, 64, 1000)]
     assert all(a < b for a, b in zip(d, d[1:]))
     # the decode path keeps h and the per-pair outputs in fp32
-    assert k3mx.k3mx_moe_workspace_size(64, 0, 1) >= 64 * 16 * (3072 + 3584) * 4
+    assert k3mx.k3mx_moe_workspace_size(64, 0, 1) >= 64 * 16 * (2 * 3072 + 3584) * 4
     # AUTO picks prefill for bf16 and many tokens; its h is bf16
     assert k3mx.k3mx_moe_workspace_size(4096, 1, 0) == k3mx.k3mx_moe_workspace_size(4096, 1, 2)
     assert k3mx.k3mx_moe_workspace_size(4096, 1, 2) >= 4096 * 16 * 3072 * 2
     assert k3mx.k3mx_moe_host_workspace_size(64, 1, 1) > k3mx.k3mx_moe_workspace_size(64, 1, 1)
-    assert k3mx.k3mx_expert_ffn_workspace_size() == 3072 * 4
+    assert k3mx.k3mx_expert_ffn_workspace_size() == 2 * 3072 * 4
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU behaviour only")

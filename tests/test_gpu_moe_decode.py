@@ -1,7 +1,8 @@
 """The routed-expert layer on the decode path (fp32 activations) against the
 oracle, on the full 896-expert arena:
   - batch 1, x fp32 ~ N(0,1), logits ~ N(0,1), bias ~ N(0, 0.1);
-  - batch 64, x bf16 -> fp32, each token routed independently.
+  - batch 64, x bf16 -> fp32, each token routed independently with flat
+    routing (no score-correction bias), so about 610 distinct experts run.
 Routing bit-exact; y within sum_k w_k * (per-expert decode bound)."""
 import numpy as np
 import pytest
@@ -46,7 +47,8 @@ def test_decode_batch64_bf16(arena, cuda_dev):
     T = 64
     xb = synth.f32_to_bf16(synth.token_inputs(T, seed=0))
     x = synth.bf16_to_f32(xb)                         # exact widening, as the layer sees it
-    logits, bias = synth.router_inputs(T, seed=0)
+    logits, _ = synth.router_inputs(T, seed=0)
+    bias = np.zeros(896, np.float32)                  # flat routing
     x_t = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16)
     y, idx, w = run_moe(cuda_dev, table, x_t, logits, bias, k3mx.K3MX_PATH_DECODE)
     ir, wr = oracle.route(logits, bias)
@@ -78,3 +80,20 @@ def test_decode_is_deterministic(arena, cuda_dev):
     a, _, _ = run_moe(cuda_dev, table, torch.from_numpy(x), logits, bias, k3mx.K3MX_PATH_DECODE)
     b, _, _ = run_moe(cuda_dev, table, torch.from_numpy(x), logits, bias, k3mx.K3MX_PATH_DECODE)
     assert np.array_equal(a, b)
+
+
+def test_decode_experts_shared_by_many_tokens(arena, cuda_dev):
+    """Nine tokens routed to the same 16 experts: every expert runs for nine
+    tokens (three work units of at most four), the grouping's longest lists."""
+    _, table = arena
+    T = 9
+    x = synth.token_inputs(T, seed=21)
+    logits, _ = synth.router_inputs(T, seed=21)
+    bias = np.zeros(896, np.float32)
+    logits[:, 100:116] += 8.0                         # the same 16 winners for every token
+    y, idx, w = run_moe(cuda_dev, table, torch.from_numpy(x), logits, bias, k3mx.K3MX_PATH_DECODE)
+    ir, wr = oracle.route(logits, bias)
+    assert np.array_equal(idx, ir) and np.array_equal(w, wr)
+    assert sorted(set(ir.ravel().tolist())) == list(range(100, 116))
+    yr, bound = moe_oracle(x, ir, wr, list(range(T)))
+    assert_within(y, yr, 1e-5 * bound, "shared experts")

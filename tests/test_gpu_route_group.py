@@ -59,7 +59,8 @@ def test_route_ties_bias_and_special_keys(cuda_dev):
     ir, wr = oracle.route(logits, bias)
     assert np.array_equal(idx, ir)
     assert np.array_equal(w.view(np.uint32), wr.view(np.uint32))
-    assert list(idx[0]) == list(range(16))
+    # row 0: sigma(-12) + 0.5 > sigma(0) + 0, so the bias lifts experts 16..31
+    assert sorted(idx[0]) == list(range(16, 32))
 
 
 @pytest.mark.parametrize("T", [1, 64, 300, 4096])
@@ -80,3 +81,25 @@ def test_group_skewed_routing(cuda_dev):
     c, o, p = gpu_group(cuda_dev, idx)
     cr, orr, pr = oracle.group(idx)
     assert np.array_equal(c, cr) and np.array_equal(o, orr) and np.array_equal(p, pr)
+
+
+@pytest.mark.parametrize("case", ["all_equal", "inf_bias", "clustered"])
+def test_route_exact_fallbacks(cuda_dev, case):
+    """Cases where the fp32 candidate filter keeps more than 64 experts or
+    meets infinite keys, so the exact all-expert path decides."""
+    E, T = 896, 4
+    logits, bias = synth.router_inputs(T, seed=11)
+    if case == "all_equal":
+        logits[:] = 0.25
+        bias[:] = 0.0
+    elif case == "inf_bias":
+        bias[100:120] = np.inf
+        bias[7] = -np.inf
+    else:
+        logits[:, :200] = 3.0                    # 200 experts within float rounding of each other
+        logits[:, :200] += np.linspace(0, 1e-6, 200, dtype=np.float32)
+        bias[:] = 0.0
+    idx, w = gpu_route(cuda_dev, logits, bias)
+    ir, wr = oracle.route(logits, bias)
+    assert np.array_equal(idx, ir)
+    assert np.array_equal(w.view(np.uint32), wr.view(np.uint32))
