@@ -38,7 +38,10 @@ FALLBACK_BF16_TFLOPS = 1900.0
 
 # kernels per traced launch group
 KERNELS_PER_GROUP = {"route_group": 1, "route": 1, "group": 3, "bf16_to_f32": 1,
-                     "decode_gate_up": 1, "decode_down": 1, "combine": 1}
+                     "decode_gate_up": 1, "decode_down": 1, "combine": 1,
+                     "prefill_prep": 2, "prefill_gate_up": 1, "prefill_down": 1}
+PARAMS_PER_EXPERT = 33030144
+GATE_UP_PARAMS = 2 * 3072 * 3584
 
 
 def load_peaks():
@@ -383,6 +386,29 @@ def run_ours(args):
                                      "hbm_frac": round(b / (ms / 1e3) / 1e9 / hbm_peak, 4),
                                      "kernels": {k: {"launches": v[0], "avg_us": round(1e3 * v[1] / max(1, v[0]), 2)}
                                                  for k, v in r["trace"].items()}}
+            # prefill, 4096 bf16 tokens, flat routing: tcgen05 grouped GEMMs
+            wl = Workload("moe_prefill_4096", 4096, True, k3mx.K3MX_PATH_PREFILL)
+            r = time_workload(k3mx, wl, table, dev, max(3, args.steps // 4), args.warmup, None, flush)
+            ms = sum(r["ms"]) / len(r["ms"])
+            pairs = 4096 * K
+            flops = 2.0 * PARAMS_PER_EXPERT * pairs
+            tr = r["trace"]
+            kern = {}
+            for name, params in (("prefill_gate_up", GATE_UP_PARAMS), ("prefill_down", PARAMS_PER_EXPERT - GATE_UP_PARAMS)):
+                if name in tr:
+                    kms = tr[name][1] / tr[name][0]
+                    tf = 2.0 * params * pairs / (kms / 1e3) / 1e12
+                    kern[name] = {"avg_ms": round(kms, 4), "TFLOP_s": round(tf, 1),
+                                  "frac_bf16_peak": round(tf / bf16_peak, 4)}
+            sec["moe_prefill_4096"] = {
+                "tokens_per_s": round(4096 / (ms / 1e3), 1), "ms_per_step": round(ms, 4),
+                "TFLOP_s": round(flops / (ms / 1e3) / 1e12, 1),
+                "frac_bf16_peak": round(flops / (ms / 1e3) / 1e12 / bf16_peak, 4),
+                "expert_GB_s": round(E * EXPERT_BYTES / (ms / 1e3) / 1e9, 1),
+                "peak_source": f"{peak_src} bf16 burst {bf16_peak} TFLOP/s (f16 MMA, same rate)",
+                "tensor_kernels": kern,
+                "kernels": {k: {"launches": v[0], "avg_us": round(1e3 * v[1] / max(1, v[0]), 2)}
+                            for k, v in tr.items()}}
         line["secondary"] = sec
         if not args.no_cpu_baseline:
             steps_in = [decode_inputs(i, 1) for i in range(64)]

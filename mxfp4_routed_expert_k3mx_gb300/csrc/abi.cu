@@ -72,24 +72,29 @@ int g_ev_made = 0;
 TraceRec g_rec[kTracePool];
 int g_nrec = 0;
 
-// Runs `launch` (a callable returning cudaError_t) between two events when
-// tracing is on.
-template <typename F>
-cudaError_t traced(const char *name, cudaStream_t s, F launch) {
-    if (!g_trace_on || g_nrec >= kTracePool) return launch();
-    const int slot = g_nrec;
-    if (slot >= g_ev_made) {
-        if (cudaEventCreate(&g_ev[slot][0]) != cudaSuccess ||
-            cudaEventCreate(&g_ev[slot][1]) != cudaSuccess)
-            return launch();
-        g_ev_made = slot + 1;
+}  // namespace
+
+// The event pair of the next traced launch, or false when tracing is off or
+// the pool is used up.
+bool trace_begin(cudaStream_t s, int *slot) {
+    if (!g_trace_on || g_nrec >= kTracePool) return false;
+    const int k = g_nrec;
+    if (k >= g_ev_made) {
+        if (cudaEventCreate(&g_ev[k][0]) != cudaSuccess || cudaEventCreate(&g_ev[k][1]) != cudaSuccess)
+            return false;
+        g_ev_made = k + 1;
     }
-    cudaEventRecord(g_ev[slot][0], s);
-    const cudaError_t err = launch();
+    cudaEventRecord(g_ev[k][0], s);
+    *slot = k;
+    return true;
+}
+
+void trace_end(cudaStream_t s, int slot, const char *name) {
     cudaEventRecord(g_ev[slot][1], s);
     g_rec[g_nrec++] = TraceRec{name, slot};
-    return err;
 }
+
+namespace {
 
 // ------------------------------------------------------- workspace layout --
 
