@@ -147,32 +147,62 @@ __global__ void __launch_bounds__(kThreads, 1) k_prefill(PArgs a) {
 
     if (warp < kEpiWarp0) {
         // ------------------------------------------------------ dequant --
-        const int r = tid & (kBM - 1);
-        const int sub = tid >> 7;                      // gate/up: matrix; down: half of the chunk
-        constexpr int NB = NMAT == 2 ? 32 : 16;        // packed bytes per thread per chunk
-        constexpr int NW = NB / 16;                    // uint4 loads per chunk
+        // Lanes 2i and 2i+1 take the two 16-byte halves (one 32-column
+        // group each) of a row's 32 packed bytes per chunk, so a warp reads
+        // 16 rows x 32 contiguous bytes.  Gate/up: threads 0-127 take W1 and
+        // 128-255 W3, each thread two rows (r and r + 64); down: each thread
+        // one row of W2.
+        constexpr int RPT = NMAT;                      // rows per thread
+        const int half = tid & 1;
+        const int mat = NMAT == 2 ? (tid >> 7) : 0;
+        const int rb = NMAT == 2 ? ((tid & 127) >> 1) : (tid >> 1);
         long long c = 0;                               // stage-use counter
         for (long long item = beg; item < end && !*abort_flag; item++) {
             const int unit = (int)(item / MT), mt = (int)(item % MT);
             const int e = a.units[3 * unit];
             const k3mx_expert ex = a.experts[e];
-            const uint8_t *W = (PH == kPhaseGateUp) ? (sub ? ex.w3 : ex.w1) : ex.w2;
-            const uint8_t *Sc = (PH == kPhaseGateUp) ? (sub ? ex.s3 : ex.s1) : ex.s2;
+            const uint8_t *W = (PH == kPhaseGateUp) ? (mat ? ex.w3 : ex.w1) : ex.w2;
+            const uint8_t *Sc = (PH == kPhaseGateUp) ? (mat ? ex.s3 : ex.s1) : ex.s2;
             if (((reinterpret_cast<uintptr_t>(W) | reinterpret_cast<uintptr_t>(Sc)) & 15u) != 0) {
                 report_status(a.status, kStatusBadPointer, e);
                 *abort_flag = 1;
                 break;
             }
-            const int row = mt * kBM + r;
-            const uint8_t *rowp = W + (size_t)row * ROWB + (PH == kPhaseGateUp ? 0 : 16 * sub);
-            const uint8_t *srow = Sc + (size_t)row * G;
-            const int sref = row_sref(srow, G);
-            uint4 raw[kPF][NW];
+            const uint8_t *rowp[RPT];
+            const uint8_t *srow[RPT];
+            int sref[RPT];
+#pragma unroll
+            for (int i = 0; i < RPT; i++) {
+                const int row = mt * kBM + rb + 64 * i;
+                rowp[i] = W + (size_t)row * ROWB + 16 * half;
+                srow[i] = Sc + (size_t)row * G;
+                // the row's largest non-NaN scale: the lane pair scans
+                // alternate 16-byte blocks of the row's G scale bytes
+                int mx = -1;
+                for (int blk = half; blk < G / 16; blk += 2) {
+                    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(srow[i] + 16 * blk));
+                    const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int q = 0; q < 4; q++)
+#pragma unroll
+                        for (int k = 0; k < 4; k++) {
+                            const int bb = (ws[q] >> (8 * k)) & 0xFF;
+                            if (bb != 255 && bb > mx) mx = bb;
+                        }
+                }
+                mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                sref[i] = mx < 0 ? 127 : mx;
+            }
+            // packed bytes and the group's scale byte, kPF chunks ahead
+            uint4 raw[kPF][RPT];
+            uint32_t scb[kPF][RPT];
 #pragma unroll
             for (int j = 0; j < kPF; j++)
 #pragma unroll
-                for (int q = 0; q < NW; q++)
-                    raw[j][q] = ldg_stream(rowp + (size_t)j * 32 + 16 * q);
+                for (int i = 0; i < RPT; i++) {
+                    raw[j][i] = ldg_stream(rowp[i] + (size_t)j * 32);
+                    scb[j][i] = __ldg(srow[i] + 2 * j + half);
+                }
             bool stop = false;
             for (int kc0 = 0; kc0 < KC && !stop; kc0 += kPF) {
 #pragma unroll
@@ -190,34 +220,31 @@ __global__ void __launch_bounds__(kThreads, 1) k_prefill(PArgs a) {
                         stop = true;
                         break;
                     }
-                    uint8_t *tile = stage0 + (size_t)s * STAGE + (PH == kPhaseGateUp ? sub * kTileBytes : 0);
+                    uint8_t *tile = stage0 + (size_t)s * STAGE + mat * kTileBytes;
 #pragma unroll
-                    for (int q = 0; q < NW; q++) {
-                        // 16 packed bytes = one 32-column group = 4 f16 chunks
-                        const int grp = (PH == kPhaseGateUp) ? 2 * kc + q : 2 * kc + sub;
-                        const int sb = srow[grp];
-                        const __half2 m = sb == 255 ? pow2_h2(-100) : pow2_h2(sb - sref);
-                        const uint32_t words[4] = {raw[j][q].x, raw[j][q].y, raw[j][q].z, raw[j][q].w};
+                    for (int i = 0; i < RPT; i++) {
+                        const int r = rb + 64 * i;
+                        const int sb = (int)scb[j][i];
+                        const __half2 m = sb == 255 ? pow2_h2(-100) : pow2_h2(sb - sref[i]);
+                        const uint32_t words[4] = {raw[j][i].x, raw[j][i].y, raw[j][i].z, raw[j][i].w};
 #pragma unroll
                         for (int wd = 0; wd < 4; wd++) {
                             uint32_t hv[4];
                             e2m1x8_to_h2x4(words[wd], hv);
                             uint32_t o[4];
 #pragma unroll
-                            for (int b = 0; b < 4; b++) {
-                                __half2 v = __hmul2(*reinterpret_cast<__half2 *>(&hv[b]), m);
-                                o[b] = *reinterpret_cast<uint32_t *>(&v);
+                            for (int bq = 0; bq < 4; bq++) {
+                                __half2 v = __hmul2(*reinterpret_cast<__half2 *>(&hv[bq]), m);
+                                o[bq] = *reinterpret_cast<uint32_t *>(&v);
                             }
-                            const int chunk = (PH == kPhaseGateUp) ? 4 * q + wd : 4 * sub + wd;
-                            *reinterpret_cast<uint4 *>(tile + sw128_offset(r, chunk)) =
+                            *reinterpret_cast<uint4 *>(tile + sw128_offset(r, 4 * half + wd)) =
                                 make_uint4(o[0], o[1], o[2], o[3]);
                         }
-                    }
-                    // refill this slot with the chunk kPF ahead
-                    if (kc + kPF < KC) {
-#pragma unroll
-                        for (int q = 0; q < NW; q++)
-                            raw[j][q] = ldg_stream(rowp + (size_t)(kc + kPF) * 32 + 16 * q);
+                        // refill this slot with the chunk kPF ahead
+                        if (kc + kPF < KC) {
+                            raw[j][i] = ldg_stream(rowp[i] + (size_t)(kc + kPF) * 32);
+                            scb[j][i] = __ldg(srow[i] + 2 * (kc + kPF) + half);
+                        }
                     }
                     fence_async_smem();
                     mbar_arrive(full0 + 8 * s);
