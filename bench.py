@@ -166,6 +166,20 @@ def decode_inputs(step, T, seed_base=1000):
     return x, logits, bias
 
 
+def reduce_over_ranks(dist, total_ms, nbytes, device=None):
+    """Whole-job figures of a timed region: the slowest rank's time and the
+    bytes all ranks streamed.  `dist` is torch.distributed (or None for one
+    rank)."""
+    if dist is None:
+        return float(total_ms), float(nbytes)
+    import torch
+    t = torch.tensor([float(total_ms)], dtype=torch.float64, device=device)
+    b = torch.tensor([float(nbytes)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return float(t[0]), float(b[0])
+
+
 def run_reference(args):
     """--impl reference: the CPU oracle, as it stands, on the machine's host cores."""
     steps = [decode_inputs(i, 1) for i in range(args.warmup + args.steps)]
@@ -322,14 +336,7 @@ def run_ours(args):
 
     total_ms = sum(res["ms"])
     bytes_total = sum(d * EXPERT_BYTES for d in res["distinct"])
-    if dist is not None:
-        t = torch.tensor([total_ms, bytes_total], dtype=torch.float64, device=dev)
-        tmax = t.clone()
-        dist.all_reduce(tmax[:1], op=dist.ReduceOp.MAX)
-        dist.all_reduce(t[1:], op=dist.ReduceOp.SUM)
-        total_ms_max, bytes_all = float(tmax[0]), float(t[1])
-    else:
-        total_ms_max, bytes_all = total_ms, float(bytes_total)
+    total_ms_max, bytes_all = reduce_over_ranks(dist, total_ms, bytes_total, dev)
     value = bytes_all / (total_ms_max / 1e3) / 1e9
 
     # dominant kernel: the fused gate/up + SiTU pass (two thirds of the bytes)
