@@ -10,6 +10,15 @@ streamed per second (GB/s); the line also carries the batch-64 decode and
 4096-token prefill workloads under "secondary".
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+  python bench.py --profile-case decode|prefill --tokens T [--resident R]
+                  [--confine] [--iters I]
+
+The --profile-case form runs a small case of one path for Nsight Compute
+captures (a few GB on the device): R experts (default 64, 1.1 GB, larger
+than L2) behind the full 896-entry table (entry e -> expert e mod R), I
+calls with fresh logits, then prints the device status.  With --confine the
+bias keeps routing on the R resident experts, so each expert a launch
+touches is a distinct one, as in the full workload.
 
 Timing: CUDA events on the launching stream around each step; L2 (129 MB)
 is flushed by a 256 MB write between timed steps, outside the events.
@@ -429,6 +438,41 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_profile_case(args):
+    import numpy as np
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import mxfp4_routed_expert_k3mx_gb300 as k3mx
+    import synth
+    dev = torch.device("cuda:0")
+    T, R = args.tokens, args.resident
+    arena = synth.expert_arena_device(dev, seed=0, lo=118, hi=128, n_experts=R)
+    table = k3mx.expert_table(arena, n_experts=R)[torch.arange(E, device=dev) % R].contiguous()
+    bias = torch.zeros(E, dtype=torch.float32, device=dev)
+    if args.confine:
+        bias[R:] = -100.0
+    prefill = args.profile_case == "prefill"
+    path = k3mx.K3MX_PATH_PREFILL if prefill else k3mx.K3MX_PATH_DECODE
+    dt = k3mx.K3MX_BF16 if prefill else k3mx.K3MX_F32
+    ws = torch.empty(k3mx.k3mx_moe_workspace_size(T, dt, path), dtype=torch.uint8, device=dev)
+    y = torch.empty((T, D), dtype=torch.float32, device=dev)
+    for i in range(args.iters):
+        x, logits, _ = decode_inputs(i, T)
+        if prefill:
+            xt = torch.from_numpy(synth.f32_to_bf16(x).view(np.int16)).view(torch.bfloat16).to(dev)
+        else:
+            xt = torch.from_numpy(x).to(dev)
+        k3mx.k3mx_moe_routed(y, xt, table, torch.from_numpy(logits).to(dev), bias, ws, path=path)
+    torch.cuda.synchronize(dev)
+    st = k3mx.k3mx_device_status()
+    print(json.dumps({"profile_case": args.profile_case, "tokens": T, "resident": R,
+                      "confine": args.confine, "iters": args.iters, "status": st,
+                      "y_abs_sum": float(y.abs().sum())}), flush=True)
+    if st[0] != 0:
+        sys.exit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -438,7 +482,15 @@ def main():
     ap.add_argument("--primary-only", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
+    ap.add_argument("--profile-case", choices=["decode", "prefill"])
+    ap.add_argument("--tokens", type=int, default=1)
+    ap.add_argument("--resident", type=int, default=64)
+    ap.add_argument("--confine", action="store_true")
+    ap.add_argument("--iters", type=int, default=4)
     args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args)
+        return
     args.warmup = max(args.warmup, 3)            # at least 3 untimed warm-up steps
     if args.impl == "reference":
         if int(os.environ.get("RANK", "0")) != 0:

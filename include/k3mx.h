@@ -159,9 +159,9 @@ k3mx_status k3mx_group(int32_t *counts, int32_t *offsets, int32_t *perm,
  *            receiving the routing result
  *   workspace: device, 256-byte aligned, >= k3mx_moe_workspace_size(...)
  * DECODE keeps fp32 activations and h: |error| within 1e-5 of the
- * abs-weighted sums.  PREFILL rounds h to bf16 and multiplies bf16 x bf16 on
- * the tensor cores with fp32 accumulation: per-token relative L2 error
- * within 1e-2.  DECODE is deterministic; PREFILL adds the 16 expert
+ * abs-weighted sums.  PREFILL converts x (bf16) to f16, dequantises the
+ * weights to f16, rounds h to f16 and multiplies f16 x f16 on the tensor
+ * cores with fp32 accumulation: per-token relative L2 error within 1e-2.  DECODE is deterministic; PREFILL adds the 16 expert
  * contributions of a token with fp32 atomics, so the order of those adds,
  * and the last bits of y, may vary between runs.
  */
