@@ -188,6 +188,29 @@ k3mx_status k3mx_moe_routed_host(float *y_host, const void *x_host, int x_dtype,
                                  k3mx_stream_t stream);
 
 /*
+ * The DECODE path of k3mx_moe_routed without a caller workspace: the pages
+ * have no counterpart; it serves callers that cannot allocate device memory
+ * at the point of the call: a runtime that owns the whole device memory
+ * budget and hands the library no scratch, or a latency-critical loop that
+ * must not take the synchronisation an allocation can imply.  Its scratch is
+ * one fixed array in
+ * the library's device memory, 6 MiB, enough for K3MX_NOALLOC_MAX_TOKENS
+ * tokens.  Arguments as for k3mx_moe_routed with path DECODE.
+ *   1 <= n_tokens <= K3MX_NOALLOC_MAX_TOKENS, else K3MX_ESHAPE.
+ * The first call on each device looks up that array's address (with the
+ * device current); make that first call before any stream capture.
+ * Calls that overlap on the GPU (concurrent streams, or several host
+ * threads) share the one array and race: serialise them on one stream.
+ * Results are bit-identical to k3mx_moe_routed with path DECODE.
+ */
+#define K3MX_NOALLOC_MAX_TOKENS 8
+k3mx_status k3mx_moe_decode_noalloc(float *y, const void *x, int x_dtype,
+                                    int n_tokens, const k3mx_expert *experts,
+                                    const float *logits, const float *bias,
+                                    int32_t *idx_out, float *w_out,
+                                    k3mx_stream_t stream);
+
+/*
  * Waits for `stream`, then reports and clears the device status word: K3MX_OK,
  * K3MX_ETIMEOUT when a bounded device-side wait gave up since the last call,
  * K3MX_EINVAL when a device-side range check rejected an index, K3MX_EALIGN

@@ -26,6 +26,7 @@ K3MX_F32, K3MX_BF16 = 0, 1
 K3MX_PATH_AUTO, K3MX_PATH_DECODE, K3MX_PATH_PREFILL = 0, 1, 2
 K3MX_PREFILL_MIN_TOKENS = 256
 K3MX_MAX_TOKENS = 65536
+K3MX_NOALLOC_MAX_TOKENS = 8
 
 STATUS = {0: "K3MX_OK", 1: "K3MX_EINVAL", 2: "K3MX_EALIGN", 3: "K3MX_ESHAPE",
           4: "K3MX_EWORKSPACE", 5: "K3MX_ECUDA", 6: "K3MX_ETIMEOUT", 7: "K3MX_EDEVICE"}
@@ -69,6 +70,7 @@ def lib():
             "k3mx_moe_routed": ([vp, vp, i, i, vp, vp, vp, i, vp, vp, vp, sz, vp], i),
             "k3mx_moe_host_workspace_size": ([i, i, i], sz),
             "k3mx_moe_routed_host": ([vp, vp, i, i, vp, vp, vp, i, vp, sz, vp], i),
+            "k3mx_moe_decode_noalloc": ([vp, vp, i, i, vp, vp, vp, vp, vp, vp], i),
             "k3mx_device_status": ([vp, ctypes.POINTER(ctypes.c_int)], i),
             "k3mx_status_str": ([i], ctypes.c_char_p),
             "k3mx_abi_version": ([], i),
@@ -209,6 +211,20 @@ def k3mx_moe_routed(y, x, experts, logits, bias, workspace, path=K3MX_PATH_AUTO,
         _ptr(y), _ptr(x), _x_dtype(x), T, _ptr(experts), _ptr(logits), _ptr(bias), path,
         _ptr(idx_out), _ptr(w_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)))
+    return y
+
+
+def k3mx_moe_decode_noalloc(y, x, experts, logits, bias, idx_out=None, w_out=None, stream=None):
+    """The decode path on device tensors with the library's fixed scratch
+    instead of a workspace (at most K3MX_NOALLOC_MAX_TOKENS tokens)."""
+    _dev(y, torch.float32, "y")
+    if not (x.is_cuda and x.is_contiguous()):
+        raise TypeError("x: contiguous CUDA tensor expected")
+    _dev(logits, torch.float32, "logits")
+    _dev(bias, torch.float32, "bias")
+    _check("k3mx_moe_decode_noalloc", lib().k3mx_moe_decode_noalloc(
+        _ptr(y), _ptr(x), _x_dtype(x), x.shape[0], _ptr(experts), _ptr(logits), _ptr(bias),
+        _ptr(idx_out), _ptr(w_out), _stream(stream)))
     return y
 
 

@@ -47,6 +47,16 @@ k3mx_status device_ctx(cudaStream_t stream, Ctx &c) {
     return K3MX_OK;
 }
 
+// Scratch of k3mx_moe_decode_noalloc.  Callers that may not allocate
+// device memory when they run the layer (a runtime that keeps the whole
+// memory budget to itself and hands out no scratch, a loop that must not
+// take the synchronisation an allocation can imply) use this fixed array
+// instead of a workspace.  The decode path writes every scratch word
+// before it reads it, so nothing here needs clearing between calls.
+constexpr size_t kNoallocBytes = size_t(6) << 20;
+__device__ __align__(256) unsigned char g_noalloc_ws[kNoallocBytes];
+void *g_noalloc_ptr[kMaxDevices];
+
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned256(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
 inline size_t up256(size_t n) { return (n + 255) & ~size_t(255); }
@@ -328,6 +338,31 @@ size_t k3mx_moe_workspace_size(int n_tokens, int x_dtype, int path) {
     if (n_tokens < 1 || n_tokens > K3MX_MAX_TOKENS) return 0;
     if (x_dtype != K3MX_F32 && x_dtype != K3MX_BF16) return 0;
     return moe_layout(n_tokens, x_dtype, resolve_path(n_tokens, x_dtype, path)).total;
+}
+
+k3mx_status k3mx_moe_decode_noalloc(float *y, const void *x, int x_dtype, int n_tokens,
+                                    const k3mx_expert *experts, const float *logits,
+                                    const float *bias, int32_t *idx_out, float *w_out,
+                                    k3mx_stream_t stream) {
+    k3mx_status st =
+        check_moe_args(y, x, x_dtype, n_tokens, experts, logits, bias, K3MX_PATH_DECODE);
+    if (st != K3MX_OK) return st;
+    if (n_tokens > K3MX_NOALLOC_MAX_TOKENS) return K3MX_ESHAPE;
+    if ((idx_out && !aligned16(idx_out)) || (w_out && !aligned16(w_out))) return K3MX_EALIGN;
+    const MoeLayout L = moe_layout(n_tokens, x_dtype, K3MX_PATH_DECODE);
+    if (L.total > kNoallocBytes) return K3MX_EWORKSPACE;
+    Ctx c;
+    st = device_ctx(reinterpret_cast<cudaStream_t>(stream), c);
+    if (st != K3MX_OK) return st;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return K3MX_ECUDA;  // device_ctx bounded dev
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_ws) != cudaSuccess || !p) return K3MX_ECUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    return run_moe(c, y, x, x_dtype, n_tokens, experts, logits, bias, K3MX_PATH_DECODE, idx_out,
+                   w_out, g_noalloc_ptr[dev], L);
 }
 
 size_t k3mx_moe_host_workspace_size(int n_tokens, int x_dtype, int path) {

@@ -15,7 +15,7 @@ FAKE = 0x10000          # an aligned, non-null address that is never dereference
 def test_library_exports_every_declared_symbol():
     L = k3mx.lib()
     declared = k3mx.declared_symbols()
-    assert len(declared) == 15
+    assert len(declared) == 16
     out = subprocess.run(["nm", "-D", "--defined-only", k3mx.LIB_PATH],
                          capture_output=True, text=True, check=True).stdout
     exported = set(re.findall(r"\sT\s(k3mx_\w+)", out))
@@ -76,7 +76,7 @@ def test_workspace_sizes():
     assert all(a < b for a, b in zip(d, d[1:]))
     # the decode path keeps h and the per-pair outputs in fp32
     assert k3mx.k3mx_moe_workspace_size(64, 0, 1) >= 64 * 16 * (2 * 3072 + 3584) * 4
-    # AUTO picks prefill for bf16 and many tokens; its h is bf16
+    # AUTO picks prefill for bf16 and many tokens; its h is f16
     assert k3mx.k3mx_moe_workspace_size(4096, 1, 0) == k3mx.k3mx_moe_workspace_size(4096, 1, 2)
     assert k3mx.k3mx_moe_workspace_size(4096, 1, 2) >= 4096 * 16 * 3072 * 2
     assert k3mx.k3mx_moe_host_workspace_size(64, 1, 1) > k3mx.k3mx_moe_workspace_size(64, 1, 1)
@@ -88,3 +88,17 @@ def test_valid_call_without_gpu_fails_loudly():
     """With no device the library reports a CUDA error; it has no CPU path."""
     L = k3mx.lib()
     assert L.k3mx_gemv(FAKE, FAKE, FAKE, FAKE, 64, 4, None) in (5, 7)
+
+
+def test_noalloc_refuses_bad_arguments():
+    L = k3mx.lib()
+    call = lambda T, dt=0, x=FAKE, io=None: L.k3mx_moe_decode_noalloc(
+        FAKE, x, dt, T, FAKE, FAKE, FAKE, io, None, None)
+    assert call(k3mx.K3MX_NOALLOC_MAX_TOKENS + 1) == 3       # above the fixed scratch
+    assert call(0) == 3
+    assert call(1, dt=2) == 1
+    assert call(1, x=FAKE + 2) == 2
+    assert call(1, io=FAKE + 4) == 2
+    # the fixed 6 MiB array holds the decode layout of the largest batch, either dtype
+    for dt in (0, 1):
+        assert k3mx.k3mx_moe_workspace_size(k3mx.K3MX_NOALLOC_MAX_TOKENS, dt, 1) <= 6 << 20
