@@ -410,12 +410,14 @@ def run_ours(args):
             flops = 2.0 * PARAMS_PER_EXPERT * pairs
             tr = r["trace"]
             kern = {}
+            pf_hash = kernel_source_hash(["prefill.cu", "prefill.cuh", "common.cuh"])
             for name, params in (("prefill_gate_up", GATE_UP_PARAMS), ("prefill_down", PARAMS_PER_EXPERT - GATE_UP_PARAMS)):
                 if name in tr:
                     kms = tr[name][1] / tr[name][0]
                     tf = 2.0 * params * pairs / (kms / 1e3) / 1e12
                     kern[name] = {"avg_ms": round(kms, 4), "TFLOP_s": round(tf, 1),
-                                  "frac_bf16_peak": round(tf / bf16_peak, 4)}
+                                  "frac_bf16_peak": round(tf / bf16_peak, 4),
+                                  "traffic": profiled_traffic(name, wl.name, pf_hash)}
             sec["moe_prefill_4096"] = {
                 "tokens_per_s": round(4096 / (ms / 1e3), 1), "ms_per_step": round(ms, 4),
                 "TFLOP_s": round(flops / (ms / 1e3) / 1e12, 1),
