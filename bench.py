@@ -46,10 +46,12 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
 # kernels per traced launch group
-KERNELS_PER_GROUP = {"route_group": 1, "route": 1, "group": 3, "bf16_to_f32": 1,
+KERNELS_PER_GROUP = {"route_group": 1, "route": 1, "group": 3, "bf16_to_f32": 1, "mx_pieces": 1,
                      "decode_gate_up": 1, "decode_down": 1, "combine": 1,
                      "prefill_prep": 2, "prefill_gate_up": 1, "prefill_down": 1}
 PARAMS_PER_EXPERT = 33030144
+X_IMAGE_BYTES = 8 * 3584 // 2 + 3584          # 8 MXFP4 pieces of x and their scale lines
+H_IMAGE_BYTES = 8 * 3072 // 2 + 3072
 GATE_UP_PARAMS = 2 * 3072 * 3584
 
 
@@ -352,9 +354,10 @@ def run_ours(args):
     tr = res["trace"]
     n_launch, ms_gu = tr.get("decode_gate_up", (0, 0.0))
     gu_bytes = sum(d * GATE_UP_BYTES for d in res["distinct"]) / max(1, len(res["distinct"]))
-    gu_bytes += primary.T * D * 4 + primary.T * K * F * 4           # x read, h written
+    # x pieces read; per pair g, u (fp32) and the pieces of h written
+    gu_bytes += primary.T * X_IMAGE_BYTES + primary.T * K * (H_IMAGE_BYTES + 2 * F * 4)
     achieved = gu_bytes / (ms_gu / max(1, n_launch) / 1e3) / 1e9 if n_launch else None
-    src_hash = kernel_source_hash(["decode.cu", "common.cuh"])
+    src_hash = kernel_source_hash(["mx.cu", "common.cuh"])
     traffic = profiled_traffic("decode_gate_up", primary.name, src_hash)
     launches = sum(KERNELS_PER_GROUP.get(k, 1) * v[0] for k, v in tr.items())
 

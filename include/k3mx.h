@@ -105,7 +105,12 @@ k3mx_status k3mx_gemv(float *y, const float *x, const uint8_t *packed,
  *   g = W1 x, u = W3 x, h = SiTU(g, u), y = W2 h.
  *   y [3584] fp32 (written), x [3584] fp32, *expert a HOST struct of device
  *   pointers.  workspace: device, >= k3mx_expert_ffn_workspace_size() bytes,
- *   16-byte aligned; it holds g and u between the two phases ([2][3072] fp32).
+ *   256-byte aligned; it begins with g and u ([2][3072] fp32, written),
+ *   followed by the pieces of x and h and per-CTA tensor-map slots.
+ * The multiplies run on the tensor cores with MXFP4 operands (kind::mxf4):
+ * x and h are each split exactly into eight MXFP4 vectors plus a residual
+ * of at most 4^-8 of the largest magnitude of its 32-column block, and the
+ * tensor cores accumulate in fp32: g, u within 1e-5 * sum_c |w_rc| |x_c|.
  */
 size_t k3mx_expert_ffn_workspace_size(void);
 k3mx_status k3mx_expert_ffn(float *y, const float *x, const k3mx_expert *expert,
@@ -158,8 +163,10 @@ k3mx_status k3mx_group(int32_t *counts, int32_t *offsets, int32_t *perm,
  *   idx_out, w_out: optional DEVICE arrays [n_tokens][16] (NULL to skip)
  *            receiving the routing result
  *   workspace: device, 256-byte aligned, >= k3mx_moe_workspace_size(...)
- * DECODE keeps fp32 activations and h: |error| within 1e-5 of the
- * abs-weighted sums.  PREFILL converts x (bf16) to f16, dequantises the
+ * DECODE runs the tensor-core multiplies of k3mx_expert_ffn (x and h as
+ * eight exact MXFP4 pieces, fp32 accumulation): |error| within 1e-5 of the
+ * abs-weighted sums.
+ * PREFILL converts x (bf16) to f16, dequantises the
  * weights to f16, rounds h to f16 and multiplies f16 x f16 on the tensor
  * cores with fp32 accumulation: per-token relative L2 error within 1e-2.  DECODE is deterministic; PREFILL adds the 16 expert
  * contributions of a token with fp32 atomics, so the order of those adds,
@@ -194,7 +201,7 @@ k3mx_status k3mx_moe_routed_host(float *y_host, const void *x_host, int x_dtype,
  * budget and hands the library no scratch, or a latency-critical loop that
  * must not take the synchronisation an allocation can imply.  Its scratch is
  * one fixed array in
- * the library's device memory, 6 MiB, enough for K3MX_NOALLOC_MAX_TOKENS
+ * the library's device memory, 8 MiB, enough for K3MX_NOALLOC_MAX_TOKENS
  * tokens.  Arguments as for k3mx_moe_routed with path DECODE.
  *   1 <= n_tokens <= K3MX_NOALLOC_MAX_TOKENS, else K3MX_ESHAPE.
  * The first call on each device looks up that array's address (with the

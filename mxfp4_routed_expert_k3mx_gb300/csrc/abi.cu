@@ -53,9 +53,27 @@ k3mx_status device_ctx(cudaStream_t stream, Ctx &c) {
 // take the synchronisation an allocation can imply) use this fixed array
 // instead of a workspace.  The decode path writes every scratch word
 // before it reads it, so nothing here needs clearing between calls.
-constexpr size_t kNoallocBytes = size_t(6) << 20;
+constexpr size_t kNoallocBytes = size_t(8) << 20;
 __device__ __align__(256) unsigned char g_noalloc_ws[kNoallocBytes];
 void *g_noalloc_ptr[kMaxDevices];
+
+}  // namespace
+
+// Device address of the library's fixed scratch array on the current device
+// (looked up once per device), or nullptr.
+void *library_scratch() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_ws) != cudaSuccess) return nullptr;
+        g_noalloc_ptr[dev] = p;
+    }
+    return g_noalloc_ptr[dev];
+}
+size_t library_scratch_bytes() { return kNoallocBytes; }
+
+namespace {
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned256(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
@@ -109,7 +127,8 @@ namespace {
 // ------------------------------------------------------- workspace layout --
 
 struct MoeLayout {
-    size_t idx, w, counts, offsets, act, n_active, units, n_units, perm, hist, xf, h, stage, total;
+    size_t idx, w, counts, offsets, act, n_active, units, n_units, perm, hist, ximg, himg, maps, h,
+        stage, total;
     // prefill-only regions
     size_t pre;
     // host-variant staging
@@ -143,7 +162,9 @@ MoeLayout moe_layout(int n_tokens, int x_dtype, int path) {
     L.perm = take(P * 4);
     L.hist = take(group_scratch_bytes(n_tokens));
     if (path == K3MX_PATH_DECODE) {
-        L.xf = take(x_dtype == K3MX_BF16 ? (size_t)n_tokens * kD * 4 : 0);
+        L.ximg = take(mx_ximg_bytes(n_tokens));  // x of every token as MXFP4 pieces
+        L.himg = take(mx_himg_bytes((int)P));    // h of every pair as MXFP4 pieces
+        L.maps = take(mx_maps_bytes());
         L.h = take(P * 2 * kF * 4);          // g and u per pair
         L.stage = take(P * kD * 4);
     } else {
@@ -218,21 +239,19 @@ k3mx_status run_moe(const Ctx &c, float *y, const void *x, int x_dtype, int n_to
         return from_cuda(launch_prefill(c, a));  // traced per kernel inside
     }
 
-    const float *xf = static_cast<const float *>(x);
-    if (x_dtype == K3MX_BF16) {
-        float *conv = at<float>(ws, L.xf);
-        err = traced("bf16_to_f32", c.stream, [&] {
-            return launch_bf16_to_f32(c, conv, static_cast<const uint16_t *>(x), (size_t)n_tokens * kD);
-        });
-        if (err != cudaSuccess) return K3MX_ECUDA;
-        xf = conv;
-    }
     DecodeExperts d{experts, nullptr, g.units, g.n_units, g.perm, max_units(n_tokens)};
-    float *h = at<float>(ws, L.h);
+    uint8_t *ximg = at<uint8_t>(ws, L.ximg), *himg = at<uint8_t>(ws, L.himg), *maps = at<uint8_t>(ws, L.maps);
+    float *gu = at<float>(ws, L.h);
     float *stage = at<float>(ws, L.stage);
-    err = traced("decode_gate_up", c.stream, [&] { return launch_decode_phase_a(c, d, xf, h); });
+    const int upairs = n_tokens == 1 ? 1 : kUnitPairs;
+    err = traced("mx_pieces", c.stream, [&] {
+        return launch_mx_ximg(c, x, x_dtype == K3MX_BF16 ? 1 : 0, n_tokens, ximg);
+    });
     if (err == cudaSuccess)
-        err = traced("decode_down", c.stream, [&] { return launch_decode_phase_b(c, d, h, stage); });
+        err = traced("decode_gate_up", c.stream,
+                     [&] { return launch_mx_gate_up(c, d, upairs, ximg, himg, gu, maps); });
+    if (err == cudaSuccess)
+        err = traced("decode_down", c.stream, [&] { return launch_mx_down(c, d, upairs, himg, stage, maps); });
     if (err == cudaSuccess)
         err = traced("combine", c.stream, [&] { return launch_combine(c, y, stage, w, n_tokens); });
     return from_cuda(err);
@@ -273,7 +292,11 @@ k3mx_status k3mx_gemv(float *y, const float *x, const uint8_t *packed, const uin
                             [&] { return launch_gemv(c, y, x, packed, scales, in, rows); }));
 }
 
-size_t k3mx_expert_ffn_workspace_size(void) { return (size_t)2 * kF * sizeof(float); }
+// expert_ffn workspace: g and u [2][F] fp32, x and h piece images, tensor-map slots
+size_t k3mx_expert_ffn_workspace_size(void) {
+    return up256((size_t)2 * kF * sizeof(float)) + up256(mx_ximg_bytes(1)) + up256(mx_himg_bytes(1)) +
+           up256(mx_maps_bytes());
+}
 
 k3mx_status k3mx_expert_ffn(float *y, const float *x, const k3mx_expert *expert, void *workspace,
                             size_t ws_bytes, k3mx_stream_t stream) {
@@ -284,15 +307,22 @@ k3mx_status k3mx_expert_ffn(float *y, const float *x, const k3mx_expert *expert,
                    : K3MX_EINVAL;
     if (!aligned16(y) || !aligned16(x)) return K3MX_EALIGN;
     if (!workspace || ws_bytes < k3mx_expert_ffn_workspace_size()) return K3MX_EWORKSPACE;
-    if (!aligned16(workspace)) return K3MX_EALIGN;
+    if (!aligned256(workspace)) return K3MX_EALIGN;
     Ctx c;
     k3mx_status st = device_ctx(reinterpret_cast<cudaStream_t>(stream), c);
     if (st != K3MX_OK) return st;
     DecodeExperts d{nullptr, expert, nullptr, nullptr, nullptr, 1};
-    float *h = static_cast<float *>(workspace);
-    cudaError_t err = traced("decode_gate_up", c.stream, [&] { return launch_decode_phase_a(c, d, x, h); });
+    char *ws = static_cast<char *>(workspace);
+    float *gu = reinterpret_cast<float *>(ws);
+    uint8_t *ximg = reinterpret_cast<uint8_t *>(ws + up256((size_t)2 * kF * sizeof(float)));
+    uint8_t *himg = ximg + up256(mx_ximg_bytes(1));
+    uint8_t *maps = himg + up256(mx_himg_bytes(1));
+    cudaError_t err = traced("mx_pieces", c.stream, [&] { return launch_mx_ximg(c, x, 0, 1, ximg); });
     if (err == cudaSuccess)
-        err = traced("decode_down", c.stream, [&] { return launch_decode_phase_b(c, d, h, y); });
+        err = traced("decode_gate_up", c.stream,
+                     [&] { return launch_mx_gate_up(c, d, 1, ximg, himg, gu, maps); });
+    if (err == cudaSuccess)
+        err = traced("decode_down", c.stream, [&] { return launch_mx_down(c, d, 1, himg, y, maps); });
     return from_cuda(err);
 }
 
@@ -354,15 +384,10 @@ k3mx_status k3mx_moe_decode_noalloc(float *y, const void *x, int x_dtype, int n_
     Ctx c;
     st = device_ctx(reinterpret_cast<cudaStream_t>(stream), c);
     if (st != K3MX_OK) return st;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return K3MX_ECUDA;  // device_ctx bounded dev
-    if (!g_noalloc_ptr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_ws) != cudaSuccess || !p) return K3MX_ECUDA;
-        g_noalloc_ptr[dev] = p;
-    }
+    void *scratch = library_scratch();
+    if (!scratch) return K3MX_ECUDA;
     return run_moe(c, y, x, x_dtype, n_tokens, experts, logits, bias, K3MX_PATH_DECODE, idx_out,
-                   w_out, g_noalloc_ptr[dev], L);
+                   w_out, scratch, L);
 }
 
 size_t k3mx_moe_host_workspace_size(int n_tokens, int x_dtype, int path) {

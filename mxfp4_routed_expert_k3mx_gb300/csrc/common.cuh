@@ -276,6 +276,25 @@ cudaError_t launch_decode_phase_b(const Ctx &c, const DecodeExperts &d, const fl
                                   float *stage);
 cudaError_t launch_combine(const Ctx &c, float *y, const float *stage, const float *w,
                            int n_tokens);
+
+// The library's fixed device scratch array (abi.cu): its address on the
+// current device, looked up on first use, and its size.
+void *library_scratch();
+size_t library_scratch_bytes();
+
+// Block-scaled tensor-core decode path (mx.cu).  Piece images: every token's
+// x and every pair's h split exactly into MXFP4 pieces in the layout the
+// MMA reads; tensor-map slots: per-CTA copies of the weight tensor maps.
+size_t mx_ximg_bytes(int n_tokens);
+size_t mx_himg_bytes(int n_pairs);
+size_t mx_maps_bytes();
+cudaError_t launch_mx_ximg(const Ctx &c, const void *x, int x_bf16, int n_tokens, uint8_t *ximg);
+// gate/up: g, u -> gu [pair][2][F]; h = SiTU(g, u) -> piece images himg
+cudaError_t launch_mx_gate_up(const Ctx &c, const DecodeExperts &d, int max_pairs_per_unit,
+                              const uint8_t *ximg, uint8_t *himg, float *gu, uint8_t *maps);
+// down: W2 h of every pair -> out [pair][D] (launched as a dependent of gate/up)
+cudaError_t launch_mx_down(const Ctx &c, const DecodeExperts &d, int max_pairs_per_unit,
+                           const uint8_t *himg, float *out, uint8_t *maps);
 cudaError_t launch_bf16_to_f32(const Ctx &c, float *out, const uint16_t *in, size_t n);
 
 }  // namespace k3mx

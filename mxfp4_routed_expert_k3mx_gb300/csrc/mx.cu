@@ -1,0 +1,765 @@
+// mx.cu - the decode path of the routed-expert layer on block-scaled
+// 5th-generation tensor-core MMAs (tcgen05 kind::mxf4): the packed MXFP4
+// weights and their ue8m0 group scales reach the tensor cores exactly as
+// they are stored (Kimi K3 engine (c/kimi_k3.c), "Weights"), with no
+// per-weight work in registers.
+//
+// Activations.  kind::mxf4 multiplies e2m1 by e2m1, so the activation
+// vector v (x for gate/up, h for down) is split exactly into kPieces MXFP4
+// vectors, v = p_0 + ... + p_7 + r.  Piece i takes, per 32-column block,
+// the ue8m0 scale 2^e that maps the block's largest residual |value| into
+// (3, 6] and the nearest e2m1 value of every residual; the new residual is
+// formed exactly in fp32.  Each piece cuts the block's largest residual by
+// at least 4, so |r| <= 4^-8 of the block's largest |v|.  Every piece is one
+// N column of the MMA, D[:, n] = W p_n, and the epilogue adds a token's
+// eight columns in fp32.
+//
+// Work.  item = (unit, 128-row tile); a unit is one expert and at most four
+// of its pairs (so one fixed token set).  A CTA per SM takes a contiguous
+// range of items.  Per item the K dimension streams in 256-column chunks:
+//   warp 0      TMA: each matrix's 128 x 128-byte tile (128-byte swizzle,
+//               K-major) through a per-CTA tensor map whose global address is
+//               replaced on the device for each expert; bulk copies of the
+//               unit's piece images (B operand and its scales) once per unit
+//   warp 1      scale loader: the tile's 128 x 8 scale bytes per matrix into
+//               the 32-row scale-factor atoms tcgen05.cp reads (scale 255,
+//               "contributes nothing", becomes 0, i.e. 2^-127)
+//   warp 2      TMEM owner; lane 0 copies the scale atoms to TMEM and issues
+//               four K=64 MMAs per matrix and chunk, M=128, N = 8 per token
+//   warps 3-6   epilogue (TMEM lane quarter = warp % 4): adds the pieces;
+//               gate/up writes g, u, h = SiTU(g, u) as piece images for the
+//               down pass; down writes the per-pair rows of y
+// Two accumulator buffers let the epilogue of one item overlap the MMAs of
+// the next.  Every wait is bounded; a timeout is reported on the device
+// status word and every role leaves its loop.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+
+namespace k3mx {
+namespace {
+
+constexpr int kPieces = 8;
+constexpr int kChunk = 256;                    // K columns per stage
+constexpr int kTileBytes = 128 * 128;          // 128 rows x 128 packed bytes
+constexpr int kAtomBytes = 512;                // scale-factor atom: 32 lines x 16 B
+constexpr int kThreads = 7 * 32;
+constexpr int kProdWarp = 0, kSfWarp = 1, kMmaWarp = 2;   // warps 3-6: epilogue
+constexpr int kTmemCols = 512;
+constexpr int kMaxGrid = 256;
+constexpr int kSmemLimit = 227 * 1024;
+
+// piece image of a K-long vector: B part [K/256][8 rows][128 B] (128-byte
+// swizzle, 1024 B per chunk), scale part [K/128][8 lines][16 B] (bytes 0-3
+// of a line: the row's scales of the atom's 4 blocks)
+__host__ __device__ constexpr int img_b(int K) { return K / kChunk * 1024; }
+__host__ __device__ constexpr int img_s(int K) { return K / 128 * 128; }
+__host__ __device__ constexpr int img_bytes(int K) { return img_b(K) + img_s(K); }
+
+template <int PH> struct MxCfg;
+template <> struct MxCfg<0> { static constexpr int NMAT = 2, K = kD, M = kF; };   // gate/up
+template <> struct MxCfg<1> { static constexpr int NMAT = 1, K = kF, M = kD; };   // down
+
+template <int PH, int NTOK> struct MxShape {
+    static constexpr int NMAT = MxCfg<PH>::NMAT, K = MxCfg<PH>::K, M = MxCfg<PH>::M;
+    static constexpr int KC = K / kChunk, MT = M / 128, G = K / 32;
+    static constexpr int NCOL = 8 * NTOK;                          // D columns per matrix
+    static constexpr int STAGE = NMAT * (kTileBytes + 2 * kAtomBytes);
+    static constexpr int TOKB = img_b(K), TOKS = img_s(K);
+    static constexpr int FIXED = 1024 + NTOK * (TOKB + TOKS);      // header + piece images
+    static constexpr int S_FIT = (kSmemLimit - 1024 - FIXED) / STAGE;
+    static constexpr int S = S_FIT > 10 ? 10 : S_FIT;
+    static constexpr int SMEM = 1024 + FIXED + S * STAGE;          // + 1024 alignment slack
+    // TMEM columns: accumulators [2][NMAT][NCOL], A scales [S][NMAT][2 atoms][4],
+    // B scales [K/128 atoms][4]
+    static constexpr int SFA_COL = 2 * NMAT * NCOL;
+    static constexpr int SFB_COL = SFA_COL + S * NMAT * 8;
+    static_assert(S >= 3, "pipeline too shallow");
+    static_assert(SFB_COL + (K / 128) * 4 <= kTmemCols, "TMEM budget");
+    static_assert(SMEM <= kSmemLimit, "shared memory budget");
+};
+
+struct MxArgs {
+    const k3mx_expert *experts;     // device table [896], or nullptr: `one`, pair 0
+    k3mx_expert one;
+    const int32_t *units, *n_units, *perm;
+    const uint8_t *img_in;          // gate/up: per-token x images; down: per-pair h images
+    uint8_t *img_out;               // gate/up: per-pair h images
+    float *gu;                      // gate/up: [pair][2][F]
+    float *out;                     // down: [pair][D]
+    uint8_t *maps;                  // this pass's tensor-map slots [grid][2][NMAT][128 B]
+    int *status;
+};
+
+struct Hdr {
+    uint64_t full[10], empty[10], accf[2], acce[2], bfull, bempty, done;
+    uint32_t tmem;
+    int abort;
+};
+
+// ------------------------------------------------------------ PTX helpers --
+
+// K-major operand in the 128-byte swizzle with a given stride between
+// 8-row groups
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t sbo) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | (uint64_t)(16u >> 4) << 16 |
+           (uint64_t)((sbo >> 4) & 0x3FFFu) << 32 | (uint64_t)1 << 46 | (uint64_t)2 << 61;
+}
+// tcgen05.cp source: 32 lines of 16 B in four 8-line groups `sbo` apart, no swizzle
+__device__ __forceinline__ uint64_t desc_atom(uint32_t saddr, uint32_t sbo) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | (uint64_t)((sbo >> 4) & 0x3FFFu) << 32 |
+           (uint64_t)1 << 46;
+}
+// one scale-factor atom (32 lines x 16 B) into 4 TMEM columns of all 128
+// lanes (each lane quarter gets the same copy); scale of row m, block kb of
+// the atom: column m / 32, byte kb, line m % 32
+__device__ __forceinline__ void tmem_cp_atom(uint32_t taddr, uint64_t desc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
+// instruction descriptor, kind::mxf4: e2m1 A and B, ue8m0 scales, K-major,
+// M = 128, N = n; sf_id picks the byte pair of the scale columns
+__device__ __forceinline__ uint32_t idesc_mxf4(int n, int sf_id) {
+    return ((uint32_t)sf_id << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | (1u << 23) |
+           ((uint32_t)(128 >> 4) << 24) | ((uint32_t)sf_id << 29);
+}
+__device__ __forceinline__ void mma_mxf4(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t sfa, uint32_t sfb, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void tma_2d(uint32_t dst, const void *map, int x, int y, uint32_t bar,
+                                       uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(map), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+// a copy of a tensor map (staged in shared memory) with its global address
+// replaced, published to `gmap` for the tensor-map proxy (whole warp)
+__device__ __forceinline__ void publish_map(void *gmap, uint32_t smap, const CUtensorMap &tmpl,
+                                            const void *addr) {
+    const int lane = threadIdx.x & 31;
+    if (lane < 8) {
+        const uint4 v = reinterpret_cast<const uint4 *>(&tmpl)[lane];
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(smap + 16 * lane), "r"(v.x),
+                     "r"(v.y), "r"(v.z), "r"(v.w)
+                     : "memory");
+    }
+    __syncwarp();
+    if (lane == 0)
+        asm volatile("tensormap.replace.tile.global_address.shared::cta.b1024.b64 [%0], %1;" ::"r"(smap),
+                     "l"(reinterpret_cast<uint64_t>(addr))
+                     : "memory");
+    __syncwarp();
+    asm volatile(
+        "tensormap.cp_fenceproxy.global.shared::cta.tensormap::generic.release.cta.sync.aligned "
+        "[%0], [%1], 128;" ::"l"(gmap),
+        "r"(smap)
+        : "memory");
+    asm volatile("fence.proxy.tensormap::generic.acquire.cta [%0], 128;" ::"l"(gmap) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&v)[N]);
+template <>
+__device__ __forceinline__ void tmem_ld<8>(uint32_t taddr, uint32_t (&v)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+                 : "r"(taddr));
+}
+template <>
+__device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
+          "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
+          "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
+          "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ uint2 ldg_u2(const uint8_t *p) {
+    uint2 v;
+    asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+// scale byte 255 (a group that contributes nothing) -> 0 (2^-127)
+__device__ __forceinline__ uint32_t drop_nan_scales(uint32_t w) { return w & ~__vcmpeq4(w, 0xFFFFFFFFu); }
+
+// ----------------------------------------------------- activation pieces --
+
+// 2^k for -126 <= k <= 127
+__device__ __forceinline__ float exp2i(int k) { return __uint_as_float((uint32_t)(k + 127) << 23); }
+
+// index of the e2m1 magnitude nearest to a in [0, 6]: 0, .5, 1, 1.5, 2, 3, 4, 6
+__device__ __forceinline__ int e2m1_index(float a) {
+    return (a >= 0.25f) + (a >= 0.75f) + (a >= 1.25f) + (a >= 1.75f) + (a >= 2.5f) + (a >= 3.5f) +
+           (a >= 5.0f);
+}
+__device__ __forceinline__ float e2m1_mag(int i) {
+    return i < 2 ? 0.5f * (float)i : __uint_as_float((uint32_t)(126 + (i >> 1)) << 23 | (uint32_t)(i & 1) << 22);
+}
+// bits 0-7 of x to bits 0, 4, ..., 28
+__device__ __forceinline__ uint32_t spread_nibbles(uint32_t x) {
+    x = (x | (x << 12)) & 0x000F000Fu;
+    x = (x | (x << 6)) & 0x03030303u;
+    x = (x | (x << 3)) & 0x11111111u;
+    return x;
+}
+
+// The 32 values of a warp (lane = column of one 32-column block `kb` of a
+// vector) as kPieces MXFP4 pieces, stored into the vector's piece image
+// (B part `ib`, scale part `is`).  Whole warp.
+__device__ __forceinline__ void store_pieces(float r, uint8_t *ib, uint8_t *is, int kb) {
+    const int lane = threadIdx.x & 31;
+    uint32_t m0 = 0, m1 = 0, m2 = 0, m3 = 0, msb = 0;
+#pragma unroll
+    for (int p = 0; p < kPieces; p++) {
+        float mx = fabsf(r);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const uint32_t mb = __float_as_uint(mx);
+        const int E = (int)(mb >> 23) - 127;
+        int code = 0;
+        uint32_t sb = 0;
+        if (E == 128) {
+            sb = 255;                                   // Inf or NaN in the block: NaN scale
+        } else if (E >= -124) {
+            const int e = (mb & 0x7FFFFFu) <= 0x400000u ? E - 2 : E - 1;   // max / 2^e in (3, 6]
+            const int i = e2m1_index(fabsf(r) * exp2i(-e));
+            const float v = e2m1_mag(i) * exp2i(e);
+            code = i | ((r < 0.f && i != 0) ? 8 : 0);
+            r -= copysignf(v, r);                       // exact
+            sb = (uint32_t)(e + 127);
+        }
+        const uint32_t b0 = __ballot_sync(0xffffffffu, code & 1), b1 = __ballot_sync(0xffffffffu, code & 2);
+        const uint32_t b2 = __ballot_sync(0xffffffffu, code & 4), b3 = __ballot_sync(0xffffffffu, code & 8);
+        if (lane == p) {
+            m0 = b0;
+            m1 = b1;
+            m2 = b2;
+            m3 = b3;
+            msb = sb;
+        }
+    }
+    if (lane < kPieces) {
+        uint32_t w[4];
+#pragma unroll
+        for (int q = 0; q < 4; q++)
+            w[q] = spread_nibbles((m0 >> (8 * q)) & 0xFFu) | spread_nibbles((m1 >> (8 * q)) & 0xFFu) << 1 |
+                   spread_nibbles((m2 >> (8 * q)) & 0xFFu) << 2 | spread_nibbles((m3 >> (8 * q)) & 0xFFu) << 3;
+        *reinterpret_cast<uint4 *>(ib + (kb >> 3) * 1024 + lane * 128 + (((kb & 7) ^ lane) << 4)) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+        is[(kb >> 2) * 128 + lane * 16 + (kb & 3)] = (uint8_t)msb;
+    }
+}
+
+// x (fp32 or bf16 bits) of every token -> its piece image; one warp per
+// 32-column block
+__global__ void __launch_bounds__(256) k_mx_ximg(const void *__restrict__ x, int bf16, int n_tokens,
+                                                 uint8_t *__restrict__ img) {
+    constexpr int NB = kD / 32;
+    const int w = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (w >= n_tokens * NB) return;
+    const int t = w / NB, kb = w % NB;
+    const size_t i = (size_t)t * kD + (size_t)kb * 32 + lane;
+    const float v = bf16 ? __uint_as_float((uint32_t)static_cast<const uint16_t *>(x)[i] << 16)
+                         : static_cast<const float *>(x)[i];
+    uint8_t *ib = img + (size_t)t * img_bytes(kD);
+    store_pieces(v, ib, ib + img_b(kD), kb);
+}
+
+// ------------------------------------------------------------ work units --
+
+struct Unit {
+    int e, p0, p1;          // expert, pair slots [p0, p1) of perm
+    k3mx_expert ex;
+    bool ok;                // every pointer 16-byte aligned
+};
+
+__device__ __forceinline__ Unit unit_at(const MxArgs &a, int u) {
+    Unit r;
+    if (a.experts == nullptr) {
+        r.e = 0;
+        r.p0 = 0;
+        r.p1 = 1;
+        r.ex = a.one;
+    } else {
+        r.e = __ldg(a.units + 3 * u);
+        r.p0 = __ldg(a.units + 3 * u + 1);
+        r.p1 = __ldg(a.units + 3 * u + 2);
+        const uint4 *q = reinterpret_cast<const uint4 *>(a.experts + r.e);
+        const uint4 v0 = __ldg(q), v1 = __ldg(q + 1), v2 = __ldg(q + 2);
+        r.ex.w1 = reinterpret_cast<const uint8_t *>((uint64_t)v0.y << 32 | v0.x);
+        r.ex.s1 = reinterpret_cast<const uint8_t *>((uint64_t)v0.w << 32 | v0.z);
+        r.ex.w3 = reinterpret_cast<const uint8_t *>((uint64_t)v1.y << 32 | v1.x);
+        r.ex.s3 = reinterpret_cast<const uint8_t *>((uint64_t)v1.w << 32 | v1.z);
+        r.ex.w2 = reinterpret_cast<const uint8_t *>((uint64_t)v2.y << 32 | v2.x);
+        r.ex.s2 = reinterpret_cast<const uint8_t *>((uint64_t)v2.w << 32 | v2.z);
+    }
+    const uint64_t orp = reinterpret_cast<uint64_t>(r.ex.w1) | reinterpret_cast<uint64_t>(r.ex.s1) |
+                         reinterpret_cast<uint64_t>(r.ex.w3) | reinterpret_cast<uint64_t>(r.ex.s3) |
+                         reinterpret_cast<uint64_t>(r.ex.w2) | reinterpret_cast<uint64_t>(r.ex.s2);
+    r.ok = (orp & 15u) == 0;
+    return r;
+}
+__device__ __forceinline__ int pair_at(const MxArgs &a, int slot) {
+    return a.experts == nullptr ? 0 : __ldg(a.perm + slot);
+}
+
+template <int PH, int NTOK>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_mx(const MxArgs a, const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1) {
+    using Sh = MxShape<PH, NTOK>;
+    constexpr int NMAT = Sh::NMAT, KC = Sh::KC, MT = Sh::MT, G = Sh::G, S = Sh::S, NCOL = Sh::NCOL;
+
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Hdr *hd = reinterpret_cast<Hdr *>(smem);
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t smap0 = sbase + 512;                           // 2 x 128 B tensor-map staging
+    const uint32_t st0 = sbase + 1024;                            // stages
+    const uint32_t bimg = st0 + S * Sh::STAGE;                    // unit's B images [NTOK][TOKB]
+    const uint32_t simg = bimg + NTOK * Sh::TOKB;                 // unit's scale images [NTOK][TOKS]
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t full0 = smem_addr(hd->full), empty0 = smem_addr(hd->empty);
+    const uint32_t accf0 = smem_addr(hd->accf), acce0 = smem_addr(hd->acce);
+    const uint32_t bfull = smem_addr(&hd->bfull), bempty = smem_addr(&hd->bempty);
+    const uint32_t done = smem_addr(&hd->done);
+
+    if (tid == 0) {
+        for (int i = 0; i < S; i++) {
+            mbar_init(full0 + 8 * i, 1 + 32);      // producer's expect_tx + the scale loader's lanes
+            mbar_init(empty0 + 8 * i, 1);
+        }
+        for (int i = 0; i < 2; i++) {
+            mbar_init(accf0 + 8 * i, 1);
+            mbar_init(acce0 + 8 * i, 128);
+        }
+        mbar_init(bfull, 1);
+        mbar_init(bempty, 1);
+        mbar_init(done, 1);
+        hd->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) tmem_alloc(smem_addr(&hd->tmem), kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = hd->tmem;
+    volatile int *abort_flag = &hd->abort;
+    if (PH == 0) pdl_launch_dependents();
+
+    const int n_units = a.experts == nullptr ? 1 : __ldg(a.n_units);
+    const long long total = (long long)n_units * MT;
+    const long long beg = total * blockIdx.x / gridDim.x;
+    const long long end = total * (blockIdx.x + 1) / gridDim.x;
+    auto fail = [&](int detail) {
+        report_status(a.status, kStatusWaitTimeout, detail);
+        *abort_flag = 1;
+    };
+    // the token set of a unit: the token (gate/up, one token per unit), else
+    // the unit's slot range
+    auto unit_key = [&](const Unit &u) -> long long {
+        if (NTOK == 1 && PH == 0) return a.experts == nullptr ? 0 : __ldg(a.perm + u.p0) / kK;
+        return (long long)u.p0 << 32 | (uint32_t)u.p1;
+    };
+
+    if (warp == kProdWarp) {
+        // ---------------------------------------------------- TMA producer --
+        const uint64_t pol = l2_evict_first_policy();     // weights: read once
+        const uint64_t pol_img = l2_evict_last_policy();   // piece images: read by every CTA
+        uint8_t *gmaps = a.maps + (size_t)blockIdx.x * (2 * NMAT * 128);
+        int cur_e = -1, slot = 0;
+        long long cur_key = -1;
+        uint32_t su = 0, bl = 0;
+        bool waited = PH == 0;
+        for (long long item = beg; item < end && !*abort_flag; item++) {
+            const int unit = (int)(item / MT), mt = (int)(item % MT);
+            const Unit u = unit_at(a, unit);
+            if (!u.ok) {
+                if (lane == 0 && mt == 0) report_status(a.status, kStatusBadPointer, u.e);
+                continue;
+            }
+            if (u.e != cur_e) {
+                slot ^= 1;
+                publish_map(gmaps + (slot * NMAT + 0) * 128, smap0, tm0, PH == 0 ? u.ex.w1 : u.ex.w2);
+                if (NMAT == 2) publish_map(gmaps + (slot * NMAT + 1) * 128, smap0 + 128, tm1, u.ex.w3);
+                cur_e = u.e;
+            }
+            const long long key = unit_key(u);
+            if (key != cur_key) {
+                if (!waited) {
+                    pdl_wait();
+                    waited = true;
+                }
+                if (bl > 0 && !mbar_wait(bempty, (bl - 1) & 1)) {
+                    if (lane == 0) fail(1);
+                    break;
+                }
+                const int ntok = u.p1 - u.p0;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bfull, (uint32_t)(ntok * (Sh::TOKB + Sh::TOKS)));
+                    for (int j = 0; j < ntok; j++) {
+                        const int pair = pair_at(a, u.p0 + j);
+                        const int src = PH == 0 ? pair / kK : pair;
+                        const uint8_t *img = a.img_in + (size_t)src * img_bytes(Sh::K);
+                        bulk_g2s(bimg + j * Sh::TOKB, img, Sh::TOKB, bfull, pol_img);
+                        bulk_g2s(simg + j * Sh::TOKS, img + Sh::TOKB, Sh::TOKS, bfull, pol_img);
+                    }
+                }
+                bl++;
+                cur_key = key;
+            }
+            const uint8_t *map0 = gmaps + (slot * NMAT + 0) * 128;
+            const uint8_t *map1 = gmaps + (slot * NMAT + (NMAT - 1)) * 128;
+            for (int c = 0; c < KC; c++, su++) {
+                const int s = su % S;
+                if (!mbar_wait(empty0 + 8 * s, ((su / S) & 1) ^ 1)) {
+                    if (lane == 0) fail(2);
+                    break;
+                }
+                if (lane == 0) {
+                    const uint32_t dst = st0 + s * Sh::STAGE;
+                    mbar_arrive_expect_tx(full0 + 8 * s, NMAT * kTileBytes);
+                    tma_2d(dst, map0, c * 128, mt * 128, full0 + 8 * s, pol);
+                    if (NMAT == 2) tma_2d(dst + kTileBytes, map1, c * 128, mt * 128, full0 + 8 * s, pol);
+                }
+                __syncwarp();
+            }
+        }
+    } else if (warp == kSfWarp) {
+        // -------------------------------------------------- scale loader --
+        // lane l takes rows l, l + 32, l + 64, l + 96 of the tile: their 8
+        // scale bytes (8 blocks of the chunk) become the l-th line of the
+        // chunk's two atoms; loads run two chunks ahead of the stores.
+        const long long nchunks = (end - beg) * KC;
+        // the unit of a chunk: scale pointers, tile row, alignment (one
+        // cache for the loads running ahead, one for the stores)
+        struct Loc {
+            long long item = -1;
+            const uint8_t *sc[NMAT];
+            int mt = 0;
+            bool ok = false;
+        };
+        auto locate = [&](Loc &l, long long i) {
+            const long long item = beg + i / KC;
+            if (item != l.item) {
+                const Unit u = unit_at(a, (int)(item / MT));
+                l.ok = u.ok;
+                l.sc[0] = PH == 0 ? u.ex.s1 : u.ex.s2;
+                if (NMAT == 2) l.sc[NMAT - 1] = u.ex.s3;
+                l.mt = (int)(item % MT);
+                l.item = item;
+            }
+        };
+        Loc lload, lstore;
+        uint2 r[3][NMAT][4];
+        auto load = [&](long long i, uint2 (&d)[NMAT][4]) {
+            if (i >= nchunks) return;
+            locate(lload, i);
+            if (!lload.ok) return;
+            const int c = (int)(i % KC);
+#pragma unroll
+            for (int m = 0; m < NMAT; m++)
+#pragma unroll
+                for (int j = 0; j < 4; j++)
+                    d[m][j] = ldg_u2(lload.sc[m] + (size_t)(lload.mt * 128 + lane + 32 * j) * G + c * 8);
+        };
+        load(0, r[0]);
+        load(1, r[1]);
+        uint32_t su = 0;
+        for (long long i = 0; i < nchunks && !*abort_flag; i += 3) {
+#pragma unroll
+            for (int k = 0; k < 3; k++) {
+                const long long ii = i + k;
+                if (ii < nchunks) {
+                    locate(lstore, ii);
+                    const bool skip = !lstore.ok;
+                    load(ii + 2, r[(k + 2) % 3]);
+                    if (!skip) {
+                        const int s = su % S;
+                        if (!mbar_wait(empty0 + 8 * s, ((su / S) & 1) ^ 1)) {
+                            if (lane == 0) fail(3);
+                            i = nchunks;
+                            break;
+                        }
+                        const uint32_t at0 = st0 + s * Sh::STAGE + NMAT * kTileBytes;
+#pragma unroll
+                        for (int m = 0; m < NMAT; m++) {
+                            sts128(at0 + (2 * m) * kAtomBytes + 16 * lane, drop_nan_scales(r[k][m][0].x),
+                                   drop_nan_scales(r[k][m][1].x), drop_nan_scales(r[k][m][2].x),
+                                   drop_nan_scales(r[k][m][3].x));
+                            sts128(at0 + (2 * m + 1) * kAtomBytes + 16 * lane, drop_nan_scales(r[k][m][0].y),
+                                   drop_nan_scales(r[k][m][1].y), drop_nan_scales(r[k][m][2].y),
+                                   drop_nan_scales(r[k][m][3].y));
+                        }
+                        fence_async_smem();
+                        mbar_arrive(full0 + 8 * s);
+                        su++;
+                    }
+                }
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ----------------------------------------------------- MMA issuer --
+        if (lane == 0) {
+            uint32_t su = 0, bu = 0, it = 0;
+            long long cur_key = -1;
+            bool run = true;
+            for (long long item = beg; item < end && run && !*abort_flag; item++) {
+                const Unit u = unit_at(a, (int)(item / MT));
+                if (!u.ok) continue;
+                const long long key = unit_key(u);
+                const int ntok = u.p1 - u.p0;
+                const int n = ntok <= 1 ? 8 : (ntok == 2 ? 16 : 32);
+                if (key != cur_key) {
+                    if (!mbar_wait(bfull, bu & 1)) {
+                        fail(4);
+                        break;
+                    }
+                    bu++;
+                    tc_fence_after();
+                    // one token: the atom's four 8-line groups all read its lines
+                    // (rows 8-31 are never used with N = 8)
+                    for (int at = 0; at < Sh::K / 128; at++)
+                        tmem_cp_atom(tmem + Sh::SFB_COL + 4 * at,
+                                     desc_atom(simg + at * 128, NTOK == 1 ? 0 : Sh::TOKS));
+                    cur_key = key;
+                }
+                const int b = it & 1;
+                if (!mbar_wait(acce0 + 8 * b, ((it >> 1) & 1) ^ 1)) {
+                    fail(5);
+                    break;
+                }
+                tc_fence_after();
+                for (int c = 0; c < KC; c++, su++) {
+                    const int s = su % S;
+                    if (!mbar_wait(full0 + 8 * s, (su / S) & 1)) {
+                        fail(6);
+                        run = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t stg = st0 + s * Sh::STAGE;
+                    const uint32_t sfa = tmem + Sh::SFA_COL + s * NMAT * 8;
+#pragma unroll
+                    for (int m = 0; m < NMAT; m++)
+#pragma unroll
+                        for (int at = 0; at < 2; at++)
+                            tmem_cp_atom(sfa + m * 8 + at * 4,
+                                         desc_atom(stg + NMAT * kTileBytes + (2 * m + at) * kAtomBytes, 128));
+#pragma unroll
+                    for (int m = 0; m < NMAT; m++)
+#pragma unroll
+                        for (int ks = 0; ks < 4; ks++) {
+                            const int id = 2 * (ks & 1);
+                            mma_mxf4(tmem + (b * NMAT + m) * NCOL, desc_sw128(stg + m * kTileBytes + 32 * ks, 1024),
+                                     desc_sw128(bimg + c * 1024 + 32 * ks, Sh::TOKB), idesc_mxf4(n, id),
+                                     sfa + m * 8 + (ks >> 1) * 4, tmem + Sh::SFB_COL + (c * 2 + (ks >> 1)) * 4,
+                                     (c | ks) != 0);
+                        }
+                    umma_commit(empty0 + 8 * s);
+                }
+                if (!run) break;
+                umma_commit(accf0 + 8 * b);
+                it++;
+                // release the unit's B images once its last MMA is done
+                bool last = true;
+                for (long long nx = item + 1; nx < end; nx++) {
+                    const Unit v = unit_at(a, (int)(nx / MT));
+                    if (!v.ok) continue;
+                    last = unit_key(v) != key;
+                    break;
+                }
+                if (last) umma_commit(bempty);
+            }
+            umma_commit(done);
+        }
+    } else {
+        // ------------------------------------------------------- epilogue --
+        const int q = warp & 3;
+        uint32_t it = 0;
+        for (long long item = beg; item < end && !*abort_flag; item++) {
+            const int unit = (int)(item / MT), mt = (int)(item % MT);
+            const Unit u = unit_at(a, unit);
+            if (!u.ok) continue;
+            const int b = it & 1;
+            if (!mbar_wait(accf0 + 8 * b, (it >> 1) & 1)) {
+                if (lane == 0) fail(7);
+                break;
+            }
+            tc_fence_after();
+            uint32_t v[NMAT][NCOL];
+#pragma unroll
+            for (int m = 0; m < NMAT; m++)
+                tmem_ld<NCOL>(tmem + ((uint32_t)(32 * q) << 16) + (b * NMAT + m) * NCOL, v[m]);
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(acce0 + 8 * b);
+            it++;
+            const int row = mt * 128 + 32 * q + lane;
+            const int ntok = u.p1 - u.p0;
+#pragma unroll
+            for (int j = 0; j < NTOK; j++) {
+                if (j < ntok) {
+                    float acc[NMAT];
+#pragma unroll
+                    for (int m = 0; m < NMAT; m++) {
+                        acc[m] = 0.f;
+#pragma unroll
+                        for (int p = 0; p < kPieces; p++) acc[m] += __uint_as_float(v[m][8 * j + p]);
+                    }
+                    const int pair = pair_at(a, u.p0 + j);
+                    if (PH == 0) {
+                        float *gu = a.gu + (size_t)pair * 2 * kF;
+                        gu[row] = acc[0];
+                        gu[kF + row] = acc[NMAT - 1];
+                        const float h = situ_glu(acc[0], acc[NMAT - 1]);
+                        uint8_t *ib = a.img_out + (size_t)pair * img_bytes(kF);
+                        store_pieces(h, ib, ib + img_b(kF), mt * 4 + q);
+                    } else {
+                        a.out[(size_t)pair * kD + row] = acc[0];
+                    }
+                }
+            }
+        }
+    }
+
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        // no MMA may still be running when TMEM is released
+        if (!mbar_wait(done, 0) && lane == 0) report_status(a.status, kStatusWaitTimeout, 8);
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------- launchers --
+
+// Tensor-map templates of the weight matrices (uint8 view of the packed
+// bytes, 128 x 128-byte boxes, 128-byte swizzle), encoded once per device.
+// The kernels replace the global address per expert; the templates point at
+// the library's own scratch array (larger than one matrix), so a map is
+// never left pointing at memory that is not allocated.
+bool weight_map_templates(CUtensorMap &w13, CUtensorMap &w2) {
+    constexpr int kDevs = 64;
+    static int state[kDevs];              // 0 not tried, 1 ok, 2 failed
+    static CUtensorMap t13[kDevs], t2[kDevs];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) return false;
+    if (state[dev] == 0) {
+        state[dev] = 2;
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        void *base = library_scratch();
+        if (base != nullptr && library_scratch_bytes() >= (size_t)kD / 2 * kF &&
+            library_scratch_bytes() >= (size_t)kF / 2 * kD &&
+            cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess && fn != nullptr) {
+            auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+            const cuuint32_t box[2] = {128, 128}, es[2] = {1, 1};
+            const cuuint64_t d13[2] = {(cuuint64_t)kD / 2, (cuuint64_t)kF}, s13[1] = {(cuuint64_t)kD / 2};
+            const cuuint64_t d2[2] = {(cuuint64_t)kF / 2, (cuuint64_t)kD}, s2[1] = {(cuuint64_t)kF / 2};
+            const CUresult r1 = enc(&t13[dev], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, d13, s13, box, es,
+                                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            const CUresult r2 = enc(&t2[dev], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, d2, s2, box, es,
+                                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r1 == CUDA_SUCCESS && r2 == CUDA_SUCCESS) state[dev] = 1;
+        }
+    }
+    if (state[dev] != 1) return false;
+    w13 = t13[dev];
+    w2 = t2[dev];
+    return true;
+}
+
+template <int PH, int NTOK>
+cudaError_t launch_mx_t(const Ctx &c, MxArgs a, bool pdl) {
+    using Sh = MxShape<PH, NTOK>;
+    CUtensorMap w13, w2;
+    if (!weight_map_templates(w13, w2)) return cudaErrorNotSupported;
+    static bool configured = false;
+    if (!configured) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(k_mx<PH, NTOK>, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    a.status = c.status;
+    int grid = c.num_sms < kMaxGrid ? c.num_sms : kMaxGrid;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Sh::SMEM;
+    cfg.stream = c.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k_mx<PH, NTOK>, a, PH == 0 ? w13 : w2, w13);
+}
+
+MxArgs mx_args(const DecodeExperts &d) {
+    MxArgs a{};
+    if (d.single) {
+        a.one = *d.single;
+    } else {
+        a.experts = d.experts;
+        a.units = d.units;
+        a.n_units = d.n_units;
+        a.perm = d.perm;
+    }
+    return a;
+}
+
+}  // namespace
+
+size_t mx_ximg_bytes(int n_tokens) { return (size_t)n_tokens * img_bytes(kD); }
+size_t mx_himg_bytes(int n_pairs) { return (size_t)n_pairs * img_bytes(kF); }
+size_t mx_maps_bytes() { return (size_t)kMaxGrid * 2 * (2 + 1) * 128; }
+
+cudaError_t launch_mx_ximg(const Ctx &c, const void *x, int x_bf16, int n_tokens, uint8_t *ximg) {
+    const long long warps = (long long)n_tokens * (kD / 32);
+    k_mx_ximg<<<(unsigned)((warps + 7) / 8), 256, 0, c.stream>>>(x, x_bf16, n_tokens, ximg);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mx_gate_up(const Ctx &c, const DecodeExperts &d, int max_pairs_per_unit,
+                              const uint8_t *ximg, uint8_t *himg, float *gu, uint8_t *maps) {
+    MxArgs a = mx_args(d);
+    a.img_in = ximg;
+    a.img_out = himg;
+    a.gu = gu;
+    a.maps = maps;
+    return max_pairs_per_unit <= 1 ? launch_mx_t<0, 1>(c, a, false) : launch_mx_t<0, kUnitPairs>(c, a, false);
+}
+
+cudaError_t launch_mx_down(const Ctx &c, const DecodeExperts &d, int max_pairs_per_unit,
+                           const uint8_t *himg, float *out, uint8_t *maps) {
+    MxArgs a = mx_args(d);
+    a.img_in = himg;
+    a.out = out;
+    a.maps = maps + (size_t)kMaxGrid * 2 * 2 * 128;
+    return max_pairs_per_unit <= 1 ? launch_mx_t<1, 1>(c, a, true) : launch_mx_t<1, kUnitPairs>(c, a, true);
+}
+
+}  // namespace k3mx

@@ -80,7 +80,8 @@ def test_workspace_sizes():
     assert k3mx.k3mx_moe_workspace_size(4096, 1, 0) == k3mx.k3mx_moe_workspace_size(4096, 1, 2)
     assert k3mx.k3mx_moe_workspace_size(4096, 1, 2) >= 4096 * 16 * 3072 * 2
     assert k3mx.k3mx_moe_host_workspace_size(64, 1, 1) > k3mx.k3mx_moe_workspace_size(64, 1, 1)
-    assert k3mx.k3mx_expert_ffn_workspace_size() == 2 * 3072 * 4
+    # g and u, then the MXFP4 pieces of x and h and the tensor-map slots
+    assert k3mx.k3mx_expert_ffn_workspace_size() >= 2 * 3072 * 4 + 8 * (3584 + 3072) // 2
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU behaviour only")
@@ -99,6 +100,6 @@ def test_noalloc_refuses_bad_arguments():
     assert call(1, dt=2) == 1
     assert call(1, x=FAKE + 2) == 2
     assert call(1, io=FAKE + 4) == 2
-    # the fixed 6 MiB array holds the decode layout of the largest batch, either dtype
+    # the fixed 8 MiB array holds the decode layout of the largest batch, either dtype
     for dt in (0, 1):
-        assert k3mx.k3mx_moe_workspace_size(k3mx.K3MX_NOALLOC_MAX_TOKENS, dt, 1) <= 6 << 20
+        assert k3mx.k3mx_moe_workspace_size(k3mx.K3MX_NOALLOC_MAX_TOKENS, dt, 1) <= 8 << 20
