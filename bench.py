@@ -46,7 +46,7 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
 # kernels per traced launch group
-KERNELS_PER_GROUP = {"route_group": 1, "route": 1, "group": 3, "bf16_to_f32": 1, "mx_pieces": 1,
+KERNELS_PER_GROUP = {"route": 1, "group_small": 1, "group": 3, "mx_pieces": 1,
                      "decode_gate_up": 1, "decode_down": 1, "combine": 1,
                      "prefill_prep": 2, "prefill_gate_up": 1, "prefill_down": 1}
 PARAMS_PER_EXPERT = 33030144
@@ -253,8 +253,9 @@ def time_workload(k3mx, wl, table, dev, steps, warmup, dist, flush):
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    k3mx.k3mx_trace_read()
-    k3mx.k3mx_trace_enable(True)
+    # timed steps: only the step's own kernels between the two events (the
+    # library chains them as programmatic dependents, which per-kernel
+    # events would serialise)
     for i in range(steps):
         flush.zero_()
         ev[i][0].record(stream)
@@ -262,10 +263,19 @@ def time_workload(k3mx, wl, table, dev, steps, warmup, dist, flush):
                              idx_out=idx[i], w_out=w)
         ev[i][1].record(stream)
     torch.cuda.synchronize(dev)
-    k3mx.k3mx_trace_enable(False)
-    trace = k3mx.k3mx_trace_read()
     if dist is not None:
         dist.barrier()
+    # the same steps again with an event pair around every kernel launch:
+    # per-kernel durations
+    k3mx.k3mx_trace_read()
+    k3mx.k3mx_trace_enable(True)
+    for i in range(steps):
+        flush.zero_()
+        k3mx.k3mx_moe_routed(y, xs[warmup + i], table, lgs[warmup + i], bias, ws, path=wl.path,
+                             idx_out=idx[i], w_out=w)
+    torch.cuda.synchronize(dev)
+    k3mx.k3mx_trace_enable(False)
+    trace = k3mx.k3mx_trace_read()
     st, det = k3mx.k3mx_device_status()
     if st != 0:
         raise RuntimeError(f"device status {st} ({det})")

@@ -209,9 +209,19 @@ k3mx_status run_moe(const Ctx &c, float *y, const void *x, int x_dtype, int n_to
                at<int32_t>(ws, L.act), at<int32_t>(ws, L.n_active), at<int32_t>(ws, L.units),
                at<int32_t>(ws, L.n_units)};
     cudaError_t err;
+    const bool decode = path == K3MX_PATH_DECODE;
+    uint8_t *ximg = decode ? at<uint8_t>(ws, L.ximg) : nullptr;
+    const int x_bf16 = x_dtype == K3MX_BF16 ? 1 : 0;
+    bool pieces_done = false;
     if (n_tokens * kK <= 1024) {
-        err = traced("route_group", c.stream,
-                     [&] { return launch_route_group_small(c, idx, w, logits, bias, n_tokens, g); });
+        // one CTA per token, the decode path's x pieces in the same launch;
+        // grouping as a programmatic dependent
+        err = traced("route", c.stream, [&] {
+            return launch_route_prep(c, idx, w, logits, bias, n_tokens, decode ? x : nullptr, x_bf16, ximg);
+        });
+        if (err == cudaSuccess)
+            err = traced("group_small", c.stream, [&] { return launch_group_small(c, idx, n_tokens, g); });
+        pieces_done = decode;
     } else {
         err = traced("route", c.stream,
                      [&] { return launch_route(c, idx, w, logits, bias, n_tokens); });
@@ -240,13 +250,12 @@ k3mx_status run_moe(const Ctx &c, float *y, const void *x, int x_dtype, int n_to
     }
 
     DecodeExperts d{experts, nullptr, g.units, g.n_units, g.perm, max_units(n_tokens)};
-    uint8_t *ximg = at<uint8_t>(ws, L.ximg), *himg = at<uint8_t>(ws, L.himg), *maps = at<uint8_t>(ws, L.maps);
+    uint8_t *himg = at<uint8_t>(ws, L.himg), *maps = at<uint8_t>(ws, L.maps);
     float *gu = at<float>(ws, L.h);
     float *stage = at<float>(ws, L.stage);
     const int upairs = n_tokens == 1 ? 1 : kUnitPairs;
-    err = traced("mx_pieces", c.stream, [&] {
-        return launch_mx_ximg(c, x, x_dtype == K3MX_BF16 ? 1 : 0, n_tokens, ximg);
-    });
+    if (!pieces_done)
+        err = traced("mx_pieces", c.stream, [&] { return launch_mx_ximg(c, x, x_bf16, n_tokens, ximg); });
     if (err == cudaSuccess)
         err = traced("decode_gate_up", c.stream,
                      [&] { return launch_mx_gate_up(c, d, upairs, ximg, himg, gu, maps); });

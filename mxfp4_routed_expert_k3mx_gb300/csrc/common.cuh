@@ -212,6 +212,25 @@ __device__ __forceinline__ void pdl_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// launch `kernel` as a programmatic dependent of the previous kernel in the
+// stream (it may start before that kernel ends and must call pdl_wait
+// before reading its results)
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ------------------------------------------------------------ tracing --
 // Launch tracing (k3mx_trace_enable): an event pair on the launch stream
 // around each traced launch.  Defined in abi.cu.
@@ -251,6 +270,13 @@ struct GroupOut {
 
 cudaError_t launch_route(const Ctx &c, int32_t *idx, float *w, const float *logits,
                          const float *bias, int n_tokens);
+// routing with one CTA per token (n_tokens <= 64) plus, when x is given, the
+// tokens' x piece images (mx path) in the same launch
+cudaError_t launch_route_prep(const Ctx &c, int32_t *idx, float *w, const float *logits,
+                              const float *bias, int n_tokens, const void *x, int x_bf16,
+                              uint8_t *ximg);
+// grouping of n_tokens * 16 <= 1024 pairs, programmatic dependent of the routing
+cudaError_t launch_group_small(const Ctx &c, const int32_t *idx, int n_tokens, const GroupOut &g);
 // route + group in one CTA (n_tokens * 16 <= 1024)
 cudaError_t launch_route_group_small(const Ctx &c, int32_t *idx, float *w, const float *logits,
                                      const float *bias, int n_tokens, const GroupOut &g);

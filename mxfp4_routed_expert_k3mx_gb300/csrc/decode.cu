@@ -553,6 +553,7 @@ __global__ void k_combine(float *__restrict__ y, const float *__restrict__ out,
                           const float *__restrict__ w, int n_tokens) {
     const int per_tok = kD / 4;
     const long long i4 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    pdl_wait();                                          // the per-pair rows come from the down pass
     if (i4 >= (long long)n_tokens * per_tok) return;
     const int t = (int)(i4 / per_tok), c = (int)(i4 % per_tok);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -711,8 +712,8 @@ cudaError_t launch_combine(const Ctx &c, float *y, const float *stage, const flo
                            int n_tokens) {
     const long long n4 = (long long)n_tokens * (kD / 4);
     const int threads = 256;
-    k_combine<<<(int)((n4 + threads - 1) / threads), threads, 0, c.stream>>>(y, stage, w, n_tokens);
-    return cudaGetLastError();
+    return launch_pdl(k_combine, dim3((unsigned)((n4 + threads - 1) / threads)), dim3(threads), 0, c.stream, y,
+                      stage, w, n_tokens);
 }
 
 cudaError_t launch_bf16_to_f32(const Ctx &c, float *out, const uint16_t *in, size_t n) {

@@ -36,12 +36,12 @@
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
+#include "pieces.cuh"
 
 namespace k3mx {
 namespace {
 
-constexpr int kPieces = 8;
-constexpr int kChunk = 256;                    // K columns per stage
+constexpr int kChunk = kPieceChunk;           // K columns per stage
 constexpr int kTileBytes = 128 * 128;          // 128 rows x 128 packed bytes
 constexpr int kAtomBytes = 512;                // scale-factor atom: 32 lines x 16 B
 constexpr int kThreads = 7 * 32;
@@ -49,13 +49,6 @@ constexpr int kProdWarp = 0, kSfWarp = 1, kMmaWarp = 2;   // warps 3-6: epilogue
 constexpr int kTmemCols = 512;
 constexpr int kMaxGrid = 256;
 constexpr int kSmemLimit = 227 * 1024;
-
-// piece image of a K-long vector: B part [K/256][8 rows][128 B] (128-byte
-// swizzle, 1024 B per chunk), scale part [K/128][8 lines][16 B] (bytes 0-3
-// of a line: the row's scales of the atom's 4 blocks)
-__host__ __device__ constexpr int img_b(int K) { return K / kChunk * 1024; }
-__host__ __device__ constexpr int img_s(int K) { return K / 128 * 128; }
-__host__ __device__ constexpr int img_bytes(int K) { return img_b(K) + img_s(K); }
 
 template <int PH> struct MxCfg;
 template <> struct MxCfg<0> { static constexpr int NMAT = 2, K = kD, M = kF; };   // gate/up
@@ -67,7 +60,8 @@ template <int PH, int NTOK> struct MxShape {
     static constexpr int NCOL = 8 * NTOK;                          // D columns per matrix
     static constexpr int STAGE = NMAT * (kTileBytes + 2 * kAtomBytes);
     static constexpr int TOKB = img_b(K), TOKS = img_s(K);
-    static constexpr int FIXED = 1024 + NTOK * (TOKB + TOKS);      // header + piece images
+    static constexpr int SRAW = NMAT * 128 * G;                    // one tile's scale rows
+    static constexpr int FIXED = 1024 + NTOK * (TOKB + TOKS) + SRAW;  // header, piece images, scales
     static constexpr int S_FIT = (kSmemLimit - 1024 - FIXED) / STAGE;
     static constexpr int S = S_FIT > 10 ? 10 : S_FIT;
     static constexpr int SMEM = 1024 + FIXED + S * STAGE;          // + 1024 alignment slack
@@ -93,7 +87,7 @@ struct MxArgs {
 };
 
 struct Hdr {
-    uint64_t full[10], empty[10], accf[2], acce[2], bfull, bempty, done;
+    uint64_t full[10], empty[10], accf[2], acce[2], bfull, bempty, sfull, done;
     uint32_t tmem;
     int abort;
 };
@@ -197,90 +191,17 @@ __device__ __forceinline__ uint64_t l2_evict_last_policy() {
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
     return pol;
 }
+// bytes [p, p + n) into L2 (n a multiple of 16, p 16-byte aligned)
+__device__ __forceinline__ void l2_prefetch_bulk(const void *p, uint32_t n) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(n) : "memory");
+}
 // scale byte 255 (a group that contributes nothing) -> 0 (2^-127)
 __device__ __forceinline__ uint32_t drop_nan_scales(uint32_t w) { return w & ~__vcmpeq4(w, 0xFFFFFFFFu); }
 
-// ----------------------------------------------------- activation pieces --
-
-// 2^k for -126 <= k <= 127
-__device__ __forceinline__ float exp2i(int k) { return __uint_as_float((uint32_t)(k + 127) << 23); }
-
-// index of the e2m1 magnitude nearest to a in [0, 6]: 0, .5, 1, 1.5, 2, 3, 4, 6
-__device__ __forceinline__ int e2m1_index(float a) {
-    return (a >= 0.25f) + (a >= 0.75f) + (a >= 1.25f) + (a >= 1.75f) + (a >= 2.5f) + (a >= 3.5f) +
-           (a >= 5.0f);
-}
-__device__ __forceinline__ float e2m1_mag(int i) {
-    return i < 2 ? 0.5f * (float)i : __uint_as_float((uint32_t)(126 + (i >> 1)) << 23 | (uint32_t)(i & 1) << 22);
-}
-// bits 0-7 of x to bits 0, 4, ..., 28
-__device__ __forceinline__ uint32_t spread_nibbles(uint32_t x) {
-    x = (x | (x << 12)) & 0x000F000Fu;
-    x = (x | (x << 6)) & 0x03030303u;
-    x = (x | (x << 3)) & 0x11111111u;
-    return x;
-}
-
-// The 32 values of a warp (lane = column of one 32-column block `kb` of a
-// vector) as kPieces MXFP4 pieces, stored into the vector's piece image
-// (B part `ib`, scale part `is`).  Whole warp.
-__device__ __forceinline__ void store_pieces(float r, uint8_t *ib, uint8_t *is, int kb) {
-    const int lane = threadIdx.x & 31;
-    uint32_t m0 = 0, m1 = 0, m2 = 0, m3 = 0, msb = 0;
-#pragma unroll
-    for (int p = 0; p < kPieces; p++) {
-        float mx = fabsf(r);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        const uint32_t mb = __float_as_uint(mx);
-        const int E = (int)(mb >> 23) - 127;
-        int code = 0;
-        uint32_t sb = 0;
-        if (E == 128) {
-            sb = 255;                                   // Inf or NaN in the block: NaN scale
-        } else if (E >= -124) {
-            const int e = (mb & 0x7FFFFFu) <= 0x400000u ? E - 2 : E - 1;   // max / 2^e in (3, 6]
-            const int i = e2m1_index(fabsf(r) * exp2i(-e));
-            const float v = e2m1_mag(i) * exp2i(e);
-            code = i | ((r < 0.f && i != 0) ? 8 : 0);
-            r -= copysignf(v, r);                       // exact
-            sb = (uint32_t)(e + 127);
-        }
-        const uint32_t b0 = __ballot_sync(0xffffffffu, code & 1), b1 = __ballot_sync(0xffffffffu, code & 2);
-        const uint32_t b2 = __ballot_sync(0xffffffffu, code & 4), b3 = __ballot_sync(0xffffffffu, code & 8);
-        if (lane == p) {
-            m0 = b0;
-            m1 = b1;
-            m2 = b2;
-            m3 = b3;
-            msb = sb;
-        }
-    }
-    if (lane < kPieces) {
-        uint32_t w[4];
-#pragma unroll
-        for (int q = 0; q < 4; q++)
-            w[q] = spread_nibbles((m0 >> (8 * q)) & 0xFFu) | spread_nibbles((m1 >> (8 * q)) & 0xFFu) << 1 |
-                   spread_nibbles((m2 >> (8 * q)) & 0xFFu) << 2 | spread_nibbles((m3 >> (8 * q)) & 0xFFu) << 3;
-        *reinterpret_cast<uint4 *>(ib + (kb >> 3) * 1024 + lane * 128 + (((kb & 7) ^ lane) << 4)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
-        is[(kb >> 2) * 128 + lane * 16 + (kb & 3)] = (uint8_t)msb;
-    }
-}
-
-// x (fp32 or bf16 bits) of every token -> its piece image; one warp per
-// 32-column block
+// x of every token -> its piece image; one warp per 32-column block
 __global__ void __launch_bounds__(256) k_mx_ximg(const void *__restrict__ x, int bf16, int n_tokens,
                                                  uint8_t *__restrict__ img) {
-    constexpr int NB = kD / 32;
-    const int w = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-    if (w >= n_tokens * NB) return;
-    const int t = w / NB, kb = w % NB;
-    const size_t i = (size_t)t * kD + (size_t)kb * 32 + lane;
-    const float v = bf16 ? __uint_as_float((uint32_t)static_cast<const uint16_t *>(x)[i] << 16)
-                         : static_cast<const float *>(x)[i];
-    uint8_t *ib = img + (size_t)t * img_bytes(kD);
-    store_pieces(v, ib, ib + img_b(kD), kb);
+    ximg_block(x, bf16, n_tokens, img, blockIdx.x * 8 + (threadIdx.x >> 5));
 }
 
 // ------------------------------------------------------------ work units --
@@ -335,10 +256,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t st0 = sbase + 1024;                            // stages
     const uint32_t bimg = st0 + S * Sh::STAGE;                    // unit's B images [NTOK][TOKB]
     const uint32_t simg = bimg + NTOK * Sh::TOKB;                 // unit's scale images [NTOK][TOKS]
+    const uint32_t sraw = simg + NTOK * Sh::TOKS;                 // tile's scale rows [NMAT][128][G]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t full0 = smem_addr(hd->full), empty0 = smem_addr(hd->empty);
     const uint32_t accf0 = smem_addr(hd->accf), acce0 = smem_addr(hd->acce);
     const uint32_t bfull = smem_addr(&hd->bfull), bempty = smem_addr(&hd->bempty);
+    const uint32_t sfull = smem_addr(&hd->sfull);
     const uint32_t done = smem_addr(&hd->done);
 
     if (tid == 0) {
@@ -352,6 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(bfull, 1);
         mbar_init(bempty, 1);
+        mbar_init(sfull, 1);
         mbar_init(done, 1);
         hd->abort = 0;
         fence_mbar_init();
@@ -362,7 +286,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = hd->tmem;
     volatile int *abort_flag = &hd->abort;
-    if (PH == 0) pdl_launch_dependents();
+    // Launched as a programmatic dependent: the prologue above overlapped
+    // the previous kernel.  gate/up reads the work units, so it waits here;
+    // down streams weights at once and waits (producer) only before the h
+    // pieces.  Either lets the next kernel launch after this point.
+    if (PH == 0) pdl_wait();
+    pdl_launch_dependents();
 
     const int n_units = a.experts == nullptr ? 1 : __ldg(a.n_units);
     const long long total = (long long)n_units * MT;
@@ -444,76 +373,80 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kSfWarp) {
         // -------------------------------------------------- scale loader --
-        // lane l takes rows l, l + 32, l + 64, l + 96 of the tile: their 8
-        // scale bytes (8 blocks of the chunk) become the l-th line of the
-        // chunk's two atoms; loads run two chunks ahead of the stores.
-        const long long nchunks = (end - beg) * KC;
-        // the unit of a chunk: scale pointers, tile row, alignment (one
-        // cache for the loads running ahead, one for the stores)
-        struct Loc {
-            long long item = -1;
-            const uint8_t *sc[NMAT];
-            int mt = 0;
-            bool ok = false;
+        // A tile's scale rows (128 x G bytes per matrix, contiguous in
+        // memory) arrive in one bulk copy per item, issued as soon as the
+        // previous item's last chunk is transposed.  Lane l turns rows l,
+        // l + 32, l + 64, l + 96 into the l-th line of each chunk's two atoms.
+        const uint64_t pol = l2_evict_first_policy();
+        auto next_valid = [&](long long from) {
+            while (from < end && !unit_at(a, (int)(from / MT)).ok) from++;
+            return from;
         };
-        auto locate = [&](Loc &l, long long i) {
-            const long long item = beg + i / KC;
-            if (item != l.item) {
+        auto issue = [&](long long item) {
+            if (lane == 0) {
                 const Unit u = unit_at(a, (int)(item / MT));
-                l.ok = u.ok;
-                l.sc[0] = PH == 0 ? u.ex.s1 : u.ex.s2;
-                if (NMAT == 2) l.sc[NMAT - 1] = u.ex.s3;
-                l.mt = (int)(item % MT);
-                l.item = item;
+                const size_t off = (size_t)(item % MT) * 128 * G;
+                mbar_arrive_expect_tx(sfull, Sh::SRAW);
+                bulk_g2s(sraw, (PH == 0 ? u.ex.s1 : u.ex.s2) + off, 128 * G, sfull, pol);
+                if (NMAT == 2) bulk_g2s(sraw + 128 * G, u.ex.s3 + off, 128 * G, sfull, pol);
             }
         };
-        Loc lload, lstore;
-        uint2 r[3][NMAT][4];
-        auto load = [&](long long i, uint2 (&d)[NMAT][4]) {
-            if (i >= nchunks) return;
-            locate(lload, i);
-            if (!lload.ok) return;
-            const int c = (int)(i % KC);
-#pragma unroll
-            for (int m = 0; m < NMAT; m++)
-#pragma unroll
-                for (int j = 0; j < 4; j++)
-                    d[m][j] = ldg_u2(lload.sc[m] + (size_t)(lload.mt * 128 + lane + 32 * j) * G + c * 8);
+        // the next item's scale rows into L2 while this item streams, so
+        // its copy at the item boundary does not wait on DRAM
+        auto prefetch = [&](long long item) {
+            if (lane == 0) {
+                const Unit u = unit_at(a, (int)(item / MT));
+                const size_t off = (size_t)(item % MT) * 128 * G;
+                l2_prefetch_bulk((PH == 0 ? u.ex.s1 : u.ex.s2) + off, 128 * G);
+                if (NMAT == 2) l2_prefetch_bulk(u.ex.s3 + off, 128 * G);
+            }
         };
-        load(0, r[0]);
-        load(1, r[1]);
-        uint32_t su = 0;
-        for (long long i = 0; i < nchunks && !*abort_flag; i += 3) {
-#pragma unroll
-            for (int k = 0; k < 3; k++) {
-                const long long ii = i + k;
-                if (ii < nchunks) {
-                    locate(lstore, ii);
-                    const bool skip = !lstore.ok;
-                    load(ii + 2, r[(k + 2) % 3]);
-                    if (!skip) {
-                        const int s = su % S;
-                        if (!mbar_wait(empty0 + 8 * s, ((su / S) & 1) ^ 1)) {
-                            if (lane == 0) fail(3);
-                            i = nchunks;
-                            break;
-                        }
-                        const uint32_t at0 = st0 + s * Sh::STAGE + NMAT * kTileBytes;
-#pragma unroll
-                        for (int m = 0; m < NMAT; m++) {
-                            sts128(at0 + (2 * m) * kAtomBytes + 16 * lane, drop_nan_scales(r[k][m][0].x),
-                                   drop_nan_scales(r[k][m][1].x), drop_nan_scales(r[k][m][2].x),
-                                   drop_nan_scales(r[k][m][3].x));
-                            sts128(at0 + (2 * m + 1) * kAtomBytes + 16 * lane, drop_nan_scales(r[k][m][0].y),
-                                   drop_nan_scales(r[k][m][1].y), drop_nan_scales(r[k][m][2].y),
-                                   drop_nan_scales(r[k][m][3].y));
-                        }
-                        fence_async_smem();
-                        mbar_arrive(full0 + 8 * s);
-                        su++;
-                    }
+        uint32_t su = 0, sl = 0;
+        long long item = next_valid(beg);
+        if (item < end) issue(item);
+        while (item < end && !*abort_flag) {
+            const long long nitem = next_valid(item + 1);
+            if (nitem < end) prefetch(nitem);
+            if (!mbar_wait(sfull, sl & 1)) {
+                if (lane == 0) fail(3);
+                break;
+            }
+            sl++;
+            bool ok = true;
+            for (int c = 0; c < KC; c++, su++) {
+                const int s = su % S;
+                if (!mbar_wait(empty0 + 8 * s, ((su / S) & 1) ^ 1)) {
+                    if (lane == 0) fail(9);
+                    ok = false;
+                    break;
                 }
+                uint2 w[NMAT][4];
+#pragma unroll
+                for (int m = 0; m < NMAT; m++)
+#pragma unroll
+                    for (int j = 0; j < 4; j++)
+                        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                                     : "=r"(w[m][j].x), "=r"(w[m][j].y)
+                                     : "r"(sraw + m * 128 * G + (lane + 32 * j) * G + c * 8));
+                const uint32_t at0 = st0 + s * Sh::STAGE + NMAT * kTileBytes;
+#pragma unroll
+                for (int m = 0; m < NMAT; m++) {
+                    sts128(at0 + (2 * m) * kAtomBytes + 16 * lane, drop_nan_scales(w[m][0].x),
+                           drop_nan_scales(w[m][1].x), drop_nan_scales(w[m][2].x), drop_nan_scales(w[m][3].x));
+                    sts128(at0 + (2 * m + 1) * kAtomBytes + 16 * lane, drop_nan_scales(w[m][0].y),
+                           drop_nan_scales(w[m][1].y), drop_nan_scales(w[m][2].y), drop_nan_scales(w[m][3].y));
+                }
+                fence_async_smem();
+                if (c == KC - 1 && nitem < end) {
+                    // every lane's reads of the scale rows are done (their
+                    // values were stored above) before the next copy lands
+                    __syncwarp();
+                    issue(nitem);
+                }
+                mbar_arrive(full0 + 8 * s);
             }
+            if (!ok) break;
+            item = nitem;
         }
     } else if (warp == kMmaWarp) {
         // ----------------------------------------------------- MMA issuer --
@@ -750,7 +683,7 @@ cudaError_t launch_mx_gate_up(const Ctx &c, const DecodeExperts &d, int max_pair
     a.img_out = himg;
     a.gu = gu;
     a.maps = maps;
-    return max_pairs_per_unit <= 1 ? launch_mx_t<0, 1>(c, a, false) : launch_mx_t<0, kUnitPairs>(c, a, false);
+    return max_pairs_per_unit <= 1 ? launch_mx_t<0, 1>(c, a, true) : launch_mx_t<0, kUnitPairs>(c, a, true);
 }
 
 cudaError_t launch_mx_down(const Ctx &c, const DecodeExperts &d, int max_pairs_per_unit,

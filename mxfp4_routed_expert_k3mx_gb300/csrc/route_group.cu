@@ -7,11 +7,12 @@
 //   - sigma is evaluated in double and rounded to fp32 once, so the fp32
 //     score, key and selection agree bit for bit with a CPU evaluation in the
 //     same precision;
-//   - equal keys go to the lower expert index: each key is packed with the
-//     complemented index into one 64-bit word and the warp takes maxima;
+//   - equal keys go to the lower expert index: a key is paired with its
+//     complemented index and the warp takes the lexicographic maximum;
 //   - -0 counts as +0 and a NaN key ranks below every number.
 // One warp per token: lane l holds experts l, l+32, ..., 28 keys in
-// registers; 16 rounds of a warp max pick the winners in key order.
+// registers; 16 rounds of a warp maximum (redux.sync) pick the winners in
+// key order.
 //
 // Grouping (Kimi K3 engine (c/kimi_k3.c), "Chunked prefill": every unique
 // expert of a chunk is loaded once for all its tokens): counts per expert,
@@ -19,6 +20,7 @@
 // counts come from shared-memory integer atomics (order-free); the placement
 // is a stable warp-sequential scatter, so the output is deterministic.
 #include "common.cuh"
+#include "pieces.cuh"
 
 namespace k3mx {
 namespace {
@@ -57,27 +59,32 @@ __device__ __forceinline__ float key_of_order(uint32_t o) {
     return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
 }
 
-// the lane's best remaining key packed with its complemented expert index
-__device__ __forceinline__ unsigned long long lane_best(const uint32_t (&ok)[kPer], int lane) {
-    uint32_t b = 0;
-    int bi = 0;
+// the lane's best remaining key (strictly greater wins, so among equal keys
+// the lower slot, i.e. the lower expert index, is kept) and its slot
+__device__ __forceinline__ uint32_t lane_best(const uint32_t (&ok)[kPer], int &slot) {
+    uint32_t b = ok[0];
+    slot = 0;
 #pragma unroll
-    for (int i = 0; i < kPer; i++) {
-        if (ok[i] > b) {            // strict: equal keys keep the lower index
+    for (int i = 1; i < kPer; i++)
+        if (ok[i] > b) {
             b = ok[i];
-            bi = i;
+            slot = i;
         }
-    }
-    return ((unsigned long long)b << 32) | (0xFFFFFFFFu - (uint32_t)(lane + 32 * bi));
+    return b;
 }
 
-__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long m) {
+__device__ __forceinline__ void clear_slot(uint32_t (&ok)[kPer], int slot) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const unsigned long long other = __shfl_xor_sync(0xffffffffu, m, o);
-        m = other > m ? other : m;
-    }
-    return m;
+    for (int i = 0; i < kPer; i++)
+        if (i == slot) ok[i] = 0;
+}
+
+// The warp's largest (key, complemented index) pair: the largest key first,
+// then among its holders the largest complemented index (lowest expert).
+// Each lane offers its best (hi, lo); returns both halves.
+__device__ __forceinline__ void warp_max_pair(uint32_t hi, uint32_t lo, uint32_t &mhi, uint32_t &mlo) {
+    mhi = __reduce_max_sync(0xffffffffu, hi);
+    mlo = __reduce_max_sync(0xffffffffu, hi == mhi ? lo : 0u);
 }
 
 __device__ __forceinline__ void write_routing(int32_t *idx_t, float *w_t, int lane, int my_e,
@@ -98,24 +105,21 @@ __device__ void route_warp_all(const float *__restrict__ lt, const float *__rest
         const int e = lane + 32 * i;
         ok[i] = order_key(exact_score(__ldg(lt + e)) + __ldg(bias + e));
     }
-    unsigned long long best = lane_best(ok, lane);
+    int slot;
+    uint32_t best = lane_best(ok, slot);
     float my_s = 0.f;
     int my_e = 0;
     double sum = 0.0;
 #pragma unroll 1
     for (int k = 0; k < kK; k++) {
-        const unsigned long long m = warp_max_u64(best);
-        const int e = (int)(0xFFFFFFFFu - (uint32_t)(m & 0xFFFFFFFFull));
-        const int owner = e & 31, slot = e >> 5;
-        float s_win = 0.f;
-        if (lane == owner) {
-#pragma unroll
-            for (int i = 0; i < kPer; i++)
-                if (i == slot) ok[i] = 0;
-            best = lane_best(ok, lane);
-            s_win = exact_score(__ldg(lt + e));
+        uint32_t mhi, mlo;
+        warp_max_pair(best, 0xFFFFFFFFu - (uint32_t)(lane + 32 * slot), mhi, mlo);
+        const int e = (int)(0xFFFFFFFFu - mlo);
+        if ((e & 31) == lane) {
+            clear_slot(ok, slot);
+            best = lane_best(ok, slot);
         }
-        s_win = __shfl_sync(0xffffffffu, s_win, owner);
+        const float s_win = exact_score(__ldg(lt + e));
         sum += (double)s_win;                       // slot order, as on the CPU
         if (lane == k) {
             my_s = s_win;
@@ -125,48 +129,48 @@ __device__ void route_warp_all(const float *__restrict__ lt, const float *__rest
     write_routing(idx_t, w_t, lane, my_e, my_s, sum);
 }
 
-// One token on one warp.  (1) fp32 estimates of all 896 keys; (2) the 16th
-// largest estimate a16; (3) every expert whose estimate is within
-// 2^-18 * max(1,|a16|) of a16 is a candidate: an expert of the exact top 16
-// cannot lie further below (each estimate is within 2^-20 * max(1,|key|) of
-// its exact key, and the 16th order statistic moves by no more than that);
-// (4) exact keys for the candidates only, and the exact top-16 among them.
-// `scratch` is 128 ints of shared memory for this warp.
+// One token on one warp.  (1) fp32 estimates of all 896 keys (28 per lane,
+// in registers); (2) the 16th largest estimate a16 by 16 rounds of a warp
+// maximum; (3) every expert whose estimate is within 2^-18 * max(1,|a16|)
+// of a16 is a candidate: an expert of the exact top 16 cannot lie further
+// below (each estimate is within 2^-20 * max(1,|key|) of its exact key, and
+// the 16th order statistic moves by no more than that); (4) exact keys for
+// the candidates only, and the exact top-16 among them.  `scratch` is 128
+// ints of shared memory for this warp.
 __device__ void route_warp(const float *__restrict__ lt, const float *__restrict__ bias,
                            int32_t *__restrict__ idx_t, float *__restrict__ w_t, int lane,
                            int *scratch) {
-    float ak[kPer];
     uint32_t ok[kPer];
 #pragma unroll
     for (int i = 0; i < kPer; i++) {
         const int e = lane + 32 * i;
-        ak[i] = canon_key(approx_score(__ldg(lt + e)) + __ldg(bias + e));
-        ok[i] = order_key(ak[i]);
+        ok[i] = order_key(canon_key(approx_score(__ldg(lt + e)) + __ldg(bias + e)));
     }
-    unsigned long long best = lane_best(ok, lane);
-    unsigned long long m16 = 0;
+    // the 16th largest estimate (equal estimates count once each)
+    uint32_t cand[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; i++) cand[i] = ok[i];
+    int slot;
+    uint32_t best = lane_best(cand, slot), m16 = 0;
 #pragma unroll 1
     for (int k = 0; k < kK; k++) {
-        const unsigned long long m = warp_max_u64(best);
-        const int e = (int)(0xFFFFFFFFu - (uint32_t)(m & 0xFFFFFFFFull));
-        if (lane == (e & 31)) {
-#pragma unroll
-            for (int i = 0; i < kPer; i++)
-                if (i == (e >> 5)) ok[i] = 0;
-            best = lane_best(ok, lane);
+        m16 = __reduce_max_sync(0xffffffffu, best);
+        const int owner = __ffs(__ballot_sync(0xffffffffu, best == m16)) - 1;
+        if (lane == owner) {
+            clear_slot(cand, slot);
+            best = lane_best(cand, slot);
         }
-        m16 = m;
     }
-    const float a16 = key_of_order((uint32_t)(m16 >> 32));
+    const float a16 = key_of_order(m16);
     // a non-finite a16 (infinite biases) keeps every expert: exact path
-    const float tau = isfinite(a16) ? a16 - 0x1p-18f * fmaxf(1.0f, fabsf(a16)) : -INFINITY;
+    const uint32_t tau = isfinite(a16) ? order_key(a16 - 0x1p-18f * fmaxf(1.0f, fabsf(a16))) : 0u;
 
     // candidates into a compact per-warp list (at most 64)
     const unsigned lt_mask = (1u << lane) - 1u;
     int n = 0;
 #pragma unroll
     for (int i = 0; i < kPer; i++) {
-        const bool c = ak[i] >= tau;
+        const bool c = ok[i] >= tau;
         const unsigned bm = __ballot_sync(0xffffffffu, c);
         const int pos = n + __popc(bm & lt_mask);
         if (c && pos < 64) scratch[pos] = lane + 32 * i;
@@ -178,18 +182,19 @@ __device__ void route_warp(const float *__restrict__ lt, const float *__restrict
         return;
     }
     // exact keys: lane holds candidates lane and lane + 32
-    unsigned long long ck[2];
+    uint32_t khi[2], klo[2];
     float cs[2];
 #pragma unroll
     for (int j = 0; j < 2; j++) {
         const int pos = lane + 32 * j;
-        ck[j] = 0;
+        khi[j] = 0;
+        klo[j] = 0;
         cs[j] = 0.f;
         if (pos < n) {
             const int e = scratch[pos];
             cs[j] = exact_score(__ldg(lt + e));
-            ck[j] = ((unsigned long long)order_key(cs[j] + __ldg(bias + e)) << 32) |
-                    (0xFFFFFFFFu - (uint32_t)e);
+            khi[j] = order_key(cs[j] + __ldg(bias + e));
+            klo[j] = 0xFFFFFFFFu - (uint32_t)e;
         }
     }
     __syncwarp();
@@ -198,18 +203,25 @@ __device__ void route_warp(const float *__restrict__ lt, const float *__restrict
     double sum = 0.0;
 #pragma unroll 1
     for (int k = 0; k < kK; k++) {
-        const unsigned long long mine = ck[0] > ck[1] ? ck[0] : ck[1];
-        const unsigned long long m = warp_max_u64(mine);
-        const int e = (int)(0xFFFFFFFFu - (uint32_t)(m & 0xFFFFFFFFull));
+        const bool first = khi[0] > khi[1] || (khi[0] == khi[1] && klo[0] > klo[1]);
+        const uint32_t bh = first ? khi[0] : khi[1], bl = first ? klo[0] : klo[1];
+        uint32_t mhi, mlo;
+        warp_max_pair(bh, bl, mhi, mlo);
+        const int e = (int)(0xFFFFFFFFu - mlo);
+        // packed pairs are unique (they carry the index): one lane owns it
+        const bool mine = bh == mhi && bl == mlo;
         float s_win = 0.f;
-#pragma unroll
-        for (int j = 0; j < 2; j++)
-            if (ck[j] == m) {
-                s_win = cs[j];
-                ck[j] = 0;
+        if (mine) {
+            s_win = first ? cs[0] : cs[1];
+            if (first) {
+                khi[0] = 0;
+                klo[0] = 0;
+            } else {
+                khi[1] = 0;
+                klo[1] = 0;
             }
-        // packed keys are unique (they carry the index): one lane owns m
-        const int owner = __ffs(__ballot_sync(0xffffffffu, mine == m)) - 1;
+        }
+        const int owner = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
         s_win = __shfl_sync(0xffffffffu, s_win, owner);
         sum += (double)s_win;                       // slot order, as on the CPU
         if (lane == k) {
@@ -328,6 +340,167 @@ __device__ void scatter_warp(const int32_t *idx, int p_begin, int p_end, int *ru
     }
 }
 
+// ------------------------------------------------- one token per CTA --
+//
+// For a few tokens the warp-per-token router leaves the GPU idle, so each
+// token gets a 256-thread CTA: thread t holds experts t, t+256, t+512,
+// t+768.  (1) fp32 estimates of the 896 keys; (2) each warp's 16 largest
+// estimates by rounds of a warp maximum, then the 16th largest of those 128,
+// a16; (3) candidates within 2^-18 * max(1,|a16|) of a16 (the same bound as
+// route_warp); (4) exact double scores for the candidates, each candidate's
+// rank among them by (key, lower index), and the sum of the 16 winners'
+// scores in slot order.
+
+constexpr int kRT = 256;                 // threads per routing CTA
+constexpr int kRS = 4;                   // expert slots per thread
+
+struct RouteSmem {
+    uint32_t top[8][kK];
+    uint32_t tau;
+    int n;
+    int cand[64];
+    uint32_t khi[64], klo[64];
+    float cs[64];
+    int sel_e[kK];
+    float sel_s[kK];
+    double sum;
+};
+
+__device__ void route_cta(const float *__restrict__ lt, const float *__restrict__ bias,
+                          int32_t *__restrict__ idx_t, float *__restrict__ w_t, RouteSmem &sm) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t ok[kRS], cand[kRS];
+#pragma unroll
+    for (int j = 0; j < kRS; j++) {
+        const int e = tid + kRT * j;
+        ok[j] = e < kE ? order_key(canon_key(approx_score(__ldg(lt + e)) + __ldg(bias + e))) : 0u;
+        cand[j] = ok[j];
+    }
+    auto best_of = [&](const uint32_t(&v)[kRS], int &slot) {
+        uint32_t b = v[0];
+        slot = 0;
+#pragma unroll
+        for (int j = 1; j < kRS; j++)
+            if (v[j] > b) {
+                b = v[j];
+                slot = j;
+            }
+        return b;
+    };
+    int slot;
+    uint32_t best = best_of(cand, slot);
+#pragma unroll 1
+    for (int k = 0; k < kK; k++) {
+        const uint32_t m = __reduce_max_sync(0xffffffffu, best);
+        const int owner = __ffs(__ballot_sync(0xffffffffu, best == m)) - 1;
+        if (lane == owner) {
+#pragma unroll
+            for (int j = 0; j < kRS; j++)
+                if (j == slot) cand[j] = 0;
+            best = best_of(cand, slot);
+        }
+        if (lane == 0) sm.top[warp][k] = m;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t v[kRS];
+#pragma unroll
+        for (int j = 0; j < kRS; j++) v[j] = (&sm.top[0][0])[lane + 32 * j];
+        uint32_t b = best_of(v, slot), m16 = 0;
+#pragma unroll 1
+        for (int k = 0; k < kK; k++) {
+            m16 = __reduce_max_sync(0xffffffffu, b);
+            const int owner = __ffs(__ballot_sync(0xffffffffu, b == m16)) - 1;
+            if (lane == owner) {
+#pragma unroll
+                for (int j = 0; j < kRS; j++)
+                    if (j == slot) v[j] = 0;
+                b = best_of(v, slot);
+            }
+        }
+        if (lane == 0) {
+            const float a16 = key_of_order(m16);
+            // a non-finite a16 (infinite biases) keeps every expert: exact path
+            sm.tau = isfinite(a16) ? order_key(a16 - 0x1p-18f * fmaxf(1.0f, fabsf(a16))) : 0u;
+            sm.n = 0;
+        }
+    }
+    __syncthreads();
+    const uint32_t tau = sm.tau;
+#pragma unroll
+    for (int j = 0; j < kRS; j++) {
+        const int e = tid + kRT * j;
+        if (e < kE && ok[j] >= tau) {
+            const int pos = atomicAdd(&sm.n, 1);       // list order is free: ranks decide
+            if (pos < 64) sm.cand[pos] = e;
+        }
+    }
+    __syncthreads();
+    const int n = sm.n;
+    if (n > 64) {
+        if (warp == 0) route_warp_all(lt, bias, idx_t, w_t, lane);
+        return;
+    }
+    if (tid < n) {
+        const int e = sm.cand[tid];
+        const float s = exact_score(__ldg(lt + e));
+        sm.cs[tid] = s;
+        sm.khi[tid] = order_key(s + __ldg(bias + e));
+        sm.klo[tid] = 0xFFFFFFFFu - (uint32_t)e;
+    }
+    __syncthreads();
+    if (tid < n) {
+        const uint32_t h = sm.khi[tid], l = sm.klo[tid];
+        int r = 0;
+        for (int u = 0; u < n; u++) r += (sm.khi[u] > h) || (sm.khi[u] == h && sm.klo[u] > l);
+        if (r < kK) {
+            sm.sel_e[r] = (int)(0xFFFFFFFFu - l);
+            sm.sel_s[r] = sm.cs[tid];
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        double sum = 0.0;
+        for (int r = 0; r < kK; r++) sum += (double)sm.sel_s[r];   // slot order, as on the CPU
+        sm.sum = sum;
+    }
+    __syncthreads();
+    if (tid < kK) {
+        idx_t[tid] = sm.sel_e[tid];
+        w_t[tid] = (float)((double)sm.sel_s[tid] / sm.sum) * kRoutedScale;
+    }
+}
+
+// CTAs 0..n_tokens-1 route one token each; the CTAs after them (when x is
+// given) write the tokens' x piece images, one warp per 32-column block.
+__global__ void __launch_bounds__(kRT)
+k_route_prep(int32_t *idx, float *w, const float *logits, const float *bias, int n_tokens,
+             const void *x, int x_bf16, uint8_t *ximg) {
+    __shared__ RouteSmem sm;
+    if ((int)blockIdx.x < n_tokens) {
+        const int t = blockIdx.x;
+        route_cta(logits + (size_t)t * kE, bias, idx + (size_t)t * kK, w + (size_t)t * kK, sm);
+    } else {
+        ximg_block(x, x_bf16, n_tokens, ximg, (blockIdx.x - n_tokens) * (kRT / 32) + (threadIdx.x >> 5));
+    }
+}
+
+// grouping of n_tokens * 16 <= 1024 pairs in one CTA, launched as a
+// programmatic dependent of the routing kernel
+__global__ void __launch_bounds__(512) k_group_small(const int32_t *idx, int n_tokens, GroupOut g) {
+    __shared__ int cnt[kE];
+    __shared__ int tmp[33];
+    for (int e = threadIdx.x; e < kE; e += blockDim.x) cnt[e] = 0;
+    pdl_wait();
+    pdl_launch_dependents();
+    __syncthreads();
+    const int n_pairs = n_tokens * kK;
+    for (int p = threadIdx.x; p < n_pairs; p += blockDim.x) atomicAdd(&cnt[idx[p]], 1);
+    __syncthreads();
+    finish_counts(cnt, g, tmp);
+    if (threadIdx.x < 32) scatter_warp(idx, 0, n_pairs, cnt, g.perm);
+}
+
 // route + group for n_tokens * 16 <= 1024 pairs, one 512-thread CTA
 __global__ void __launch_bounds__(512)
 k_route_group_small(int32_t *idx, float *w, const float *logits, const float *bias,
@@ -411,6 +584,19 @@ cudaError_t launch_route_group_small(const Ctx &c, int32_t *idx, float *w, const
                                      const float *bias, int n_tokens, const GroupOut &g) {
     k_route_group_small<<<1, 512, 0, c.stream>>>(idx, w, logits, bias, n_tokens, g);
     return cudaGetLastError();
+}
+
+cudaError_t launch_route_prep(const Ctx &c, int32_t *idx, float *w, const float *logits,
+                              const float *bias, int n_tokens, const void *x, int x_bf16,
+                              uint8_t *ximg) {
+    const int piece_ctas = x != nullptr ? (n_tokens * (kD / 32) + kRT / 32 - 1) / (kRT / 32) : 0;
+    k_route_prep<<<n_tokens + piece_ctas, kRT, 0, c.stream>>>(idx, w, logits, bias, n_tokens, x, x_bf16,
+                                                              ximg);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_group_small(const Ctx &c, const int32_t *idx, int n_tokens, const GroupOut &g) {
+    return launch_pdl(k_group_small, dim3(1), dim3(512), 0, c.stream, idx, n_tokens, g);
 }
 
 size_t group_scratch_bytes(int n_tokens) {
