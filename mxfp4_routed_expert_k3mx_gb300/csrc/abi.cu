@@ -127,7 +127,7 @@ namespace {
 // ------------------------------------------------------- workspace layout --
 
 struct MoeLayout {
-    size_t idx, w, counts, offsets, act, n_active, units, n_units, perm, hist, ximg, himg, maps, h,
+    size_t idx, w, counts, offsets, act, n_active, units, n_units, perm, hist, ximg, himg, maps, sk, h,
         stage, total;
     // prefill-only regions
     size_t pre;
@@ -165,6 +165,7 @@ MoeLayout moe_layout(int n_tokens, int x_dtype, int path) {
         L.ximg = take(mx_ximg_bytes(n_tokens));  // x of every token as MXFP4 pieces
         L.himg = take(mx_himg_bytes((int)P));    // h of every pair as MXFP4 pieces
         L.maps = take(mx_maps_bytes());
+        L.sk = n_tokens == 1 ? take(mx_streamk_bytes()) : 0;   // stream-K hand-over (one token)
         L.h = take(P * 2 * kF * 4);          // g and u per pair
         L.stage = take(P * kD * 4);
     } else {
@@ -211,15 +212,19 @@ k3mx_status run_moe(const Ctx &c, float *y, const void *x, int x_dtype, int n_to
     cudaError_t err;
     const bool decode = path == K3MX_PATH_DECODE;
     uint8_t *ximg = decode ? at<uint8_t>(ws, L.ximg) : nullptr;
+    uint8_t *sk = decode && n_tokens == 1 ? at<uint8_t>(ws, L.sk) : nullptr;
     const int x_bf16 = x_dtype == K3MX_BF16 ? 1 : 0;
     bool pieces_done = false;
     if (n_tokens * kK <= 1024) {
         // one CTA per token, the decode path's x pieces in the same launch;
         // grouping as a programmatic dependent
+        const bool one = n_tokens == 1 && g.units != nullptr;
         err = traced("route", c.stream, [&] {
-            return launch_route_prep(c, idx, w, logits, bias, n_tokens, decode ? x : nullptr, x_bf16, ximg);
+            return launch_route_prep(c, idx, w, logits, bias, n_tokens, decode ? x : nullptr, x_bf16, ximg,
+                                     one ? &g : nullptr, reinterpret_cast<int *>(sk), mx_streamk_flag_count(),
+                                     decode ? experts : nullptr);
         });
-        if (err == cudaSuccess)
+        if (err == cudaSuccess && !one)
             err = traced("group_small", c.stream, [&] { return launch_group_small(c, idx, n_tokens, g); });
         pieces_done = decode;
     } else {
@@ -255,12 +260,13 @@ k3mx_status run_moe(const Ctx &c, float *y, const void *x, int x_dtype, int n_to
     float *stage = at<float>(ws, L.stage);
     const int upairs = n_tokens == 1 ? 1 : kUnitPairs;
     if (!pieces_done)
-        err = traced("mx_pieces", c.stream, [&] { return launch_mx_ximg(c, x, x_bf16, n_tokens, ximg); });
+        err = traced("mx_pieces", c.stream, [&] { return launch_mx_ximg(c, x, x_bf16, n_tokens, ximg, sk); });
     if (err == cudaSuccess)
         err = traced("decode_gate_up", c.stream,
-                     [&] { return launch_mx_gate_up(c, d, upairs, ximg, himg, gu, maps); });
+                     [&] { return launch_mx_gate_up(c, d, upairs, ximg, himg, gu, maps, sk); });
     if (err == cudaSuccess)
-        err = traced("decode_down", c.stream, [&] { return launch_mx_down(c, d, upairs, himg, stage, maps); });
+        err = traced("decode_down", c.stream,
+                     [&] { return launch_mx_down(c, d, upairs, himg, stage, maps, sk); });
     if (err == cudaSuccess)
         err = traced("combine", c.stream, [&] { return launch_combine(c, y, stage, w, n_tokens); });
     return from_cuda(err);
@@ -304,7 +310,7 @@ k3mx_status k3mx_gemv(float *y, const float *x, const uint8_t *packed, const uin
 // expert_ffn workspace: g and u [2][F] fp32, x and h piece images, tensor-map slots
 size_t k3mx_expert_ffn_workspace_size(void) {
     return up256((size_t)2 * kF * sizeof(float)) + up256(mx_ximg_bytes(1)) + up256(mx_himg_bytes(1)) +
-           up256(mx_maps_bytes());
+           up256(mx_maps_bytes()) + up256(mx_streamk_bytes());
 }
 
 k3mx_status k3mx_expert_ffn(float *y, const float *x, const k3mx_expert *expert, void *workspace,
@@ -326,12 +332,13 @@ k3mx_status k3mx_expert_ffn(float *y, const float *x, const k3mx_expert *expert,
     uint8_t *ximg = reinterpret_cast<uint8_t *>(ws + up256((size_t)2 * kF * sizeof(float)));
     uint8_t *himg = ximg + up256(mx_ximg_bytes(1));
     uint8_t *maps = himg + up256(mx_himg_bytes(1));
-    cudaError_t err = traced("mx_pieces", c.stream, [&] { return launch_mx_ximg(c, x, 0, 1, ximg); });
+    uint8_t *sk = maps + up256(mx_maps_bytes());
+    cudaError_t err = traced("mx_pieces", c.stream, [&] { return launch_mx_ximg(c, x, 0, 1, ximg, sk); });
     if (err == cudaSuccess)
         err = traced("decode_gate_up", c.stream,
-                     [&] { return launch_mx_gate_up(c, d, 1, ximg, himg, gu, maps); });
+                     [&] { return launch_mx_gate_up(c, d, 1, ximg, himg, gu, maps, sk); });
     if (err == cudaSuccess)
-        err = traced("decode_down", c.stream, [&] { return launch_mx_down(c, d, 1, himg, y, maps); });
+        err = traced("decode_down", c.stream, [&] { return launch_mx_down(c, d, 1, himg, y, maps, sk); });
     return from_cuda(err);
 }
 

@@ -271,10 +271,12 @@ struct GroupOut {
 cudaError_t launch_route(const Ctx &c, int32_t *idx, float *w, const float *logits,
                          const float *bias, int n_tokens);
 // routing with one CTA per token (n_tokens <= 64) plus, when x is given, the
-// tokens' x piece images (mx path) in the same launch
+// tokens' x piece images (mx path) in the same launch; a single token with
+// `g_one` is also grouped there (else group with launch_group_small)
 cudaError_t launch_route_prep(const Ctx &c, int32_t *idx, float *w, const float *logits,
                               const float *bias, int n_tokens, const void *x, int x_bf16,
-                              uint8_t *ximg);
+                              uint8_t *ximg, const GroupOut *g_one, int *flags, int n_flags,
+                              const k3mx_expert *experts);
 // grouping of n_tokens * 16 <= 1024 pairs, programmatic dependent of the routing
 cudaError_t launch_group_small(const Ctx &c, const int32_t *idx, int n_tokens, const GroupOut &g);
 // route + group in one CTA (n_tokens * 16 <= 1024)
@@ -314,13 +316,18 @@ size_t library_scratch_bytes();
 size_t mx_ximg_bytes(int n_tokens);
 size_t mx_himg_bytes(int n_pairs);
 size_t mx_maps_bytes();
-cudaError_t launch_mx_ximg(const Ctx &c, const void *x, int x_bf16, int n_tokens, uint8_t *ximg);
+// stream-K hand-over region of single-token decode (flags + partials); the
+// step's first kernel zeroes the mx_streamk_flag_count() flags at its start
+size_t mx_streamk_bytes();
+int mx_streamk_flag_count();
+// x pieces of every token (and, with `sk`, the stream-K flags zeroed)
+cudaError_t launch_mx_ximg(const Ctx &c, const void *x, int x_bf16, int n_tokens, uint8_t *ximg, uint8_t *sk);
 // gate/up: g, u -> gu [pair][2][F]; h = SiTU(g, u) -> piece images himg
 cudaError_t launch_mx_gate_up(const Ctx &c, const DecodeExperts &d, int max_pairs_per_unit,
-                              const uint8_t *ximg, uint8_t *himg, float *gu, uint8_t *maps);
+                              const uint8_t *ximg, uint8_t *himg, float *gu, uint8_t *maps, uint8_t *sk);
 // down: W2 h of every pair -> out [pair][D] (launched as a dependent of gate/up)
 cudaError_t launch_mx_down(const Ctx &c, const DecodeExperts &d, int max_pairs_per_unit,
-                           const uint8_t *himg, float *out, uint8_t *maps);
+                           const uint8_t *himg, float *out, uint8_t *maps, uint8_t *sk);
 cudaError_t launch_bf16_to_f32(const Ctx &c, float *out, const uint16_t *in, size_t n);
 
 }  // namespace k3mx

@@ -61,7 +61,11 @@ template <int PH, int NTOK> struct MxShape {
     static constexpr int STAGE = NMAT * (kTileBytes + 2 * kAtomBytes);
     static constexpr int TOKB = img_b(K), TOKS = img_s(K);
     static constexpr int SRAW = NMAT * 128 * G;                    // one tile's scale rows
-    static constexpr int FIXED = 1024 + NTOK * (TOKB + TOKS) + SRAW;  // header, piece images, scales
+    // one token: two scale-row buffers, so the next part's rows load during
+    // the whole current part (a copy issued at the part boundary waits
+    // behind the weight stream); several tokens: one (shared memory)
+    static constexpr int SBUF = NTOK == 1 ? 2 : 1;
+    static constexpr int FIXED = 1024 + NTOK * (TOKB + TOKS) + SBUF * SRAW;  // header, images, scales
     static constexpr int S_FIT = (kSmemLimit - 1024 - FIXED) / STAGE;
     static constexpr int S = S_FIT > 10 ? 10 : S_FIT;
     static constexpr int SMEM = 1024 + FIXED + S * STAGE;          // + 1024 alignment slack
@@ -83,11 +87,13 @@ struct MxArgs {
     float *gu;                      // gate/up: [pair][2][F]
     float *out;                     // down: [pair][D]
     uint8_t *maps;                  // this pass's tensor-map slots [grid][2][NMAT][128 B]
+    float *partials;                // stream-K hand-over accumulators [grid][NMAT][NCOL][128], or null
+    int *flags;                     // [grid] hand-over flags, zeroed by the step's first kernel
     int *status;
 };
 
 struct Hdr {
-    uint64_t full[10], empty[10], accf[2], acce[2], bfull, bempty, sfull, done;
+    uint64_t full[10], empty[10], accf[2], acce[2], bfull, bempty, sfull[2], done;
     uint32_t tmem;
     int abort;
 };
@@ -191,16 +197,14 @@ __device__ __forceinline__ uint64_t l2_evict_last_policy() {
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
     return pol;
 }
-// bytes [p, p + n) into L2 (n a multiple of 16, p 16-byte aligned)
-__device__ __forceinline__ void l2_prefetch_bulk(const void *p, uint32_t n) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(n) : "memory");
-}
 // scale byte 255 (a group that contributes nothing) -> 0 (2^-127)
 __device__ __forceinline__ uint32_t drop_nan_scales(uint32_t w) { return w & ~__vcmpeq4(w, 0xFFFFFFFFu); }
 
 // x of every token -> its piece image; one warp per 32-column block
 __global__ void __launch_bounds__(256) k_mx_ximg(const void *__restrict__ x, int bf16, int n_tokens,
-                                                 uint8_t *__restrict__ img) {
+                                                 uint8_t *__restrict__ img, int *flags, int n_flags) {
+    if (flags != nullptr && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < n_flags; i += blockDim.x) flags[i] = 0;
     ximg_block(x, bf16, n_tokens, img, blockIdx.x * 8 + (threadIdx.x >> 5));
 }
 
@@ -256,12 +260,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t st0 = sbase + 1024;                            // stages
     const uint32_t bimg = st0 + S * Sh::STAGE;                    // unit's B images [NTOK][TOKB]
     const uint32_t simg = bimg + NTOK * Sh::TOKB;                 // unit's scale images [NTOK][TOKS]
-    const uint32_t sraw = simg + NTOK * Sh::TOKS;                 // tile's scale rows [NMAT][128][G]
+    const uint32_t sraw0 = simg + NTOK * Sh::TOKS;                // tile's scale rows [SBUF][NMAT][128][G]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t full0 = smem_addr(hd->full), empty0 = smem_addr(hd->empty);
     const uint32_t accf0 = smem_addr(hd->accf), acce0 = smem_addr(hd->acce);
     const uint32_t bfull = smem_addr(&hd->bfull), bempty = smem_addr(&hd->bempty);
-    const uint32_t sfull = smem_addr(&hd->sfull);
+    const uint32_t sfull0 = smem_addr(hd->sfull);
     const uint32_t done = smem_addr(&hd->done);
 
     if (tid == 0) {
@@ -275,7 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(bfull, 1);
         mbar_init(bempty, 1);
-        mbar_init(sfull, 1);
+        mbar_init(sfull0, 1);
+        mbar_init(sfull0 + 8, 1);
         mbar_init(done, 1);
         hd->abort = 0;
         fence_mbar_init();
@@ -294,9 +299,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_launch_dependents();
 
     const int n_units = a.experts == nullptr ? 1 : __ldg(a.n_units);
-    const long long total = (long long)n_units * MT;
-    const long long beg = total * blockIdx.x / gridDim.x;
-    const long long end = total * (blockIdx.x + 1) / gridDim.x;
+    // This CTA's work is a range of the pass's chunk sequence (item-major,
+    // KC chunks per item).  One token per unit: equal ranges (stream-K), an
+    // item cut between two neighbouring CTAs is finished by the one holding
+    // its first chunk, which adds the other's fp32 partial accumulators in
+    // a fixed order.  Otherwise (or for very little work): whole items.
+    const long long n_chunks = (long long)n_units * MT * KC;
+    const bool sk = NTOK == 1 && a.partials != nullptr && n_chunks >= (long long)gridDim.x * (KC + 1);
+    long long q0, q1;
+    if (sk) {
+        q0 = n_chunks * blockIdx.x / gridDim.x;
+        q1 = n_chunks * (blockIdx.x + 1) / gridDim.x;
+    } else {
+        const long long items = (long long)n_units * MT;
+        q0 = items * blockIdx.x / gridDim.x * KC;
+        q1 = items * (blockIdx.x + 1) / gridDim.x * KC;
+    }
     auto fail = [&](int detail) {
         report_status(a.status, kStatusWaitTimeout, detail);
         *abort_flag = 1;
@@ -307,6 +325,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (NTOK == 1 && PH == 0) return a.experts == nullptr ? 0 : __ldg(a.perm + u.p0) / kK;
         return (long long)u.p0 << 32 | (uint32_t)u.p1;
     };
+    // parts: the chunks [lo, hi) of one item inside [q, q1); `next` skips
+    // items of units with misaligned pointers (every role skips the same)
+    struct Part {
+        long long item;
+        int lo, hi;
+        Unit u;
+    };
+    auto next_part = [&](long long &q, Part &p) -> bool {
+        while (q < q1) {
+            p.item = q / KC;
+            p.lo = (int)(q % KC);
+            p.hi = (int)min((long long)KC, p.lo + (q1 - q));
+            q += p.hi - p.lo;
+            p.u = unit_at(a, (int)(p.item / MT));
+            if (p.u.ok) return true;
+            if (warp == kProdWarp && lane == 0 && p.lo == 0 && p.item % MT == 0)
+                report_status(a.status, kStatusBadPointer, p.u.e);
+        }
+        return false;
+    };
 
     if (warp == kProdWarp) {
         // ---------------------------------------------------- TMA producer --
@@ -314,16 +352,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t pol_img = l2_evict_last_policy();   // piece images: read by every CTA
         uint8_t *gmaps = a.maps + (size_t)blockIdx.x * (2 * NMAT * 128);
         int cur_e = -1, slot = 0;
-        long long cur_key = -1;
+        long long cur_key = -1, q = q0;
         uint32_t su = 0, bl = 0;
         bool waited = PH == 0;
-        for (long long item = beg; item < end && !*abort_flag; item++) {
-            const int unit = (int)(item / MT), mt = (int)(item % MT);
-            const Unit u = unit_at(a, unit);
-            if (!u.ok) {
-                if (lane == 0 && mt == 0) report_status(a.status, kStatusBadPointer, u.e);
-                continue;
-            }
+        Part p;
+        while (!*abort_flag && next_part(q, p)) {
+            const Unit &u = p.u;
+            const int mt = (int)(p.item % MT);
             if (u.e != cur_e) {
                 slot ^= 1;
                 publish_map(gmaps + (slot * NMAT + 0) * 128, smap0, tm0, PH == 0 ? u.ex.w1 : u.ex.w2);
@@ -356,10 +391,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const uint8_t *map0 = gmaps + (slot * NMAT + 0) * 128;
             const uint8_t *map1 = gmaps + (slot * NMAT + (NMAT - 1)) * 128;
-            for (int c = 0; c < KC; c++, su++) {
+            bool ok = true;
+            for (int c = p.lo; c < p.hi; c++, su++) {
                 const int s = su % S;
                 if (!mbar_wait(empty0 + 8 * s, ((su / S) & 1) ^ 1)) {
                     if (lane == 0) fail(2);
+                    ok = false;
                     break;
                 }
                 if (lane == 0) {
@@ -370,50 +407,51 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
             }
+            if (!ok) break;
         }
     } else if (warp == kSfWarp) {
         // -------------------------------------------------- scale loader --
         // A tile's scale rows (128 x G bytes per matrix, contiguous in
-        // memory) arrive in one bulk copy per item, issued as soon as the
-        // previous item's last chunk is transposed.  Lane l turns rows l,
-        // l + 32, l + 64, l + 96 into the l-th line of each chunk's two atoms.
+        // memory) arrive in one bulk copy per part into one of SBUF buffers:
+        // with two, the next part's copy is issued when the current part
+        // starts; with one, after its last chunk is transposed.  Lane l turns
+        // rows l, l + 32, l + 64, l + 96 into the l-th line of each chunk's
+        // two atoms.
+        constexpr int SB = Sh::SBUF;
         const uint64_t pol = l2_evict_first_policy();
-        auto next_valid = [&](long long from) {
-            while (from < end && !unit_at(a, (int)(from / MT)).ok) from++;
-            return from;
+        auto rows_of = [&](const Part &p, int m) {
+            const size_t off = (size_t)(p.item % MT) * 128 * G;
+            return (m == 0 ? (PH == 0 ? p.u.ex.s1 : p.u.ex.s2) : p.u.ex.s3) + off;
         };
-        auto issue = [&](long long item) {
+        auto issue = [&](const Part &p, int buf) {
+            // every lane's earlier reads of this buffer are done (their
+            // values were stored) before the copy may overwrite it
+            __syncwarp();
+            fence_async_smem();
             if (lane == 0) {
-                const Unit u = unit_at(a, (int)(item / MT));
-                const size_t off = (size_t)(item % MT) * 128 * G;
-                mbar_arrive_expect_tx(sfull, Sh::SRAW);
-                bulk_g2s(sraw, (PH == 0 ? u.ex.s1 : u.ex.s2) + off, 128 * G, sfull, pol);
-                if (NMAT == 2) bulk_g2s(sraw + 128 * G, u.ex.s3 + off, 128 * G, sfull, pol);
+                mbar_arrive_expect_tx(sfull0 + 8 * buf, Sh::SRAW);
+#pragma unroll
+                for (int m = 0; m < NMAT; m++)
+                    bulk_g2s(sraw0 + buf * Sh::SRAW + m * 128 * G, rows_of(p, m), 128 * G, sfull0 + 8 * buf, pol);
             }
         };
-        // the next item's scale rows into L2 while this item streams, so
-        // its copy at the item boundary does not wait on DRAM
-        auto prefetch = [&](long long item) {
-            if (lane == 0) {
-                const Unit u = unit_at(a, (int)(item / MT));
-                const size_t off = (size_t)(item % MT) * 128 * G;
-                l2_prefetch_bulk((PH == 0 ? u.ex.s1 : u.ex.s2) + off, 128 * G);
-                if (NMAT == 2) l2_prefetch_bulk(u.ex.s3 + off, 128 * G);
-            }
-        };
-        uint32_t su = 0, sl = 0;
-        long long item = next_valid(beg);
-        if (item < end) issue(item);
-        while (item < end && !*abort_flag) {
-            const long long nitem = next_valid(item + 1);
-            if (nitem < end) prefetch(nitem);
-            if (!mbar_wait(sfull, sl & 1)) {
+        uint32_t su = 0, np = 0;           // stage uses, parts taken
+        long long q = q0;
+        Part cur, nxt;
+        bool have = next_part(q, cur);
+        if (have) issue(cur, 0);
+        while (have && !*abort_flag) {
+            const int buf = np % SB;
+            long long qn = q;
+            const bool more = next_part(qn, nxt);
+            if (more && SB == 2) issue(nxt, (np + 1) % SB);
+            if (!mbar_wait(sfull0 + 8 * buf, (np / SB) & 1)) {
                 if (lane == 0) fail(3);
                 break;
             }
-            sl++;
+            const uint32_t sraw = sraw0 + buf * Sh::SRAW;
             bool ok = true;
-            for (int c = 0; c < KC; c++, su++) {
+            for (int c = cur.lo; c < cur.hi; c++, su++) {
                 const int s = su % S;
                 if (!mbar_wait(empty0 + 8 * s, ((su / S) & 1) ^ 1)) {
                     if (lane == 0) fail(9);
@@ -437,26 +475,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                            drop_nan_scales(w[m][1].y), drop_nan_scales(w[m][2].y), drop_nan_scales(w[m][3].y));
                 }
                 fence_async_smem();
-                if (c == KC - 1 && nitem < end) {
-                    // every lane's reads of the scale rows are done (their
-                    // values were stored above) before the next copy lands
-                    __syncwarp();
-                    issue(nitem);
-                }
+                if (SB == 1 && c == cur.hi - 1 && more) issue(nxt, 0);
                 mbar_arrive(full0 + 8 * s);
             }
             if (!ok) break;
-            item = nitem;
+            np++;
+            q = qn;
+            cur = nxt;
+            have = more;
         }
     } else if (warp == kMmaWarp) {
         // ----------------------------------------------------- MMA issuer --
         if (lane == 0) {
             uint32_t su = 0, bu = 0, it = 0;
-            long long cur_key = -1;
+            long long cur_key = -1, q = q0;
             bool run = true;
-            for (long long item = beg; item < end && run && !*abort_flag; item++) {
-                const Unit u = unit_at(a, (int)(item / MT));
-                if (!u.ok) continue;
+            Part p;
+            while (run && !*abort_flag && next_part(q, p)) {
+                const Unit &u = p.u;
                 const long long key = unit_key(u);
                 const int ntok = u.p1 - u.p0;
                 const int n = ntok <= 1 ? 8 : (ntok == 2 ? 16 : 32);
@@ -480,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                for (int c = 0; c < KC; c++, su++) {
+                for (int c = p.lo; c < p.hi; c++, su++) {
                     const int s = su % S;
                     if (!mbar_wait(full0 + 8 * s, (su / S) & 1)) {
                         fail(6);
@@ -504,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mma_mxf4(tmem + (b * NMAT + m) * NCOL, desc_sw128(stg + m * kTileBytes + 32 * ks, 1024),
                                      desc_sw128(bimg + c * 1024 + 32 * ks, Sh::TOKB), idesc_mxf4(n, id),
                                      sfa + m * 8 + (ks >> 1) * 4, tmem + Sh::SFB_COL + (c * 2 + (ks >> 1)) * 4,
-                                     (c | ks) != 0);
+                                     (c != p.lo || ks != 0) ? 1u : 0u);
                         }
                     umma_commit(empty0 + 8 * s);
                 }
@@ -512,25 +548,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 umma_commit(accf0 + 8 * b);
                 it++;
                 // release the unit's B images once its last MMA is done
-                bool last = true;
-                for (long long nx = item + 1; nx < end; nx++) {
-                    const Unit v = unit_at(a, (int)(nx / MT));
-                    if (!v.ok) continue;
-                    last = unit_key(v) != key;
-                    break;
-                }
-                if (last) umma_commit(bempty);
+                long long qn = q;
+                Part nx;
+                if (!next_part(qn, nx) || unit_key(nx.u) != key) umma_commit(bempty);
             }
             umma_commit(done);
         }
     } else {
         // ------------------------------------------------------- epilogue --
-        const int q = warp & 3;
+        const int q4 = warp & 3;
+        const int row_in_tile = 32 * q4 + lane;
+        constexpr int PARTIAL = NMAT * NCOL * 128;
         uint32_t it = 0;
-        for (long long item = beg; item < end && !*abort_flag; item++) {
-            const int unit = (int)(item / MT), mt = (int)(item % MT);
-            const Unit u = unit_at(a, unit);
-            if (!u.ok) continue;
+        long long q = q0;
+        Part p;
+        while (!*abort_flag && next_part(q, p)) {
+            const Unit &u = p.u;
+            const int mt = (int)(p.item % MT);
             const int b = it & 1;
             if (!mbar_wait(accf0 + 8 * b, (it >> 1) & 1)) {
                 if (lane == 0) fail(7);
@@ -540,12 +574,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t v[NMAT][NCOL];
 #pragma unroll
             for (int m = 0; m < NMAT; m++)
-                tmem_ld<NCOL>(tmem + ((uint32_t)(32 * q) << 16) + (b * NMAT + m) * NCOL, v[m]);
+                tmem_ld<NCOL>(tmem + ((uint32_t)(32 * q4) << 16) + (b * NMAT + m) * NCOL, v[m]);
             tmem_ld_wait();
             tc_fence_before();
             mbar_arrive(acce0 + 8 * b);
             it++;
-            const int row = mt * 128 + 32 * q + lane;
+            if (sk && p.lo > 0) {
+                // the tail of an item begun by the previous CTA: hand over
+                // the partial accumulators and move on
+                float *dst = a.partials + (size_t)blockIdx.x * PARTIAL;
+#pragma unroll
+                for (int m = 0; m < NMAT; m++)
+#pragma unroll
+                    for (int j = 0; j < NCOL; j++) dst[(m * NCOL + j) * 128 + row_in_tile] = __uint_as_float(v[m][j]);
+                __threadfence();
+                named_sync(1, 128);
+                if (q4 == 0 && lane == 0)
+                    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(a.flags + blockIdx.x), "r"(1) : "memory");
+                continue;
+            }
+            if (sk && p.hi < KC) {
+                // the head of an item the next CTA finishes: add its partial
+                const int *flag = a.flags + blockIdx.x + 1;
+                int f = 0;
+                for (uint32_t i = 0; i < kWaitLimit && f == 0; i++) {
+                    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(f) : "l"(flag) : "memory");
+                    if (f == 0) __nanosleep(64);
+                }
+                if (f == 0) fail(10);
+                const float *src = a.partials + (size_t)(blockIdx.x + 1) * PARTIAL;
+#pragma unroll
+                for (int m = 0; m < NMAT; m++)
+#pragma unroll
+                    for (int j = 0; j < NCOL; j++)
+                        v[m][j] = __float_as_uint(__uint_as_float(v[m][j]) + src[(m * NCOL + j) * 128 + row_in_tile]);
+            }
+            const int row = mt * 128 + row_in_tile;
             const int ntok = u.p1 - u.p0;
 #pragma unroll
             for (int j = 0; j < NTOK; j++) {
@@ -555,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int m = 0; m < NMAT; m++) {
                         acc[m] = 0.f;
 #pragma unroll
-                        for (int p = 0; p < kPieces; p++) acc[m] += __uint_as_float(v[m][8 * j + p]);
+                        for (int pc = 0; pc < kPieces; pc++) acc[m] += __uint_as_float(v[m][8 * j + pc]);
                     }
                     const int pair = pair_at(a, u.p0 + j);
                     if (PH == 0) {
@@ -564,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         gu[kF + row] = acc[NMAT - 1];
                         const float h = situ_glu(acc[0], acc[NMAT - 1]);
                         uint8_t *ib = a.img_out + (size_t)pair * img_bytes(kF);
-                        store_pieces(h, ib, ib + img_b(kF), mt * 4 + q);
+                        store_pieces(h, ib, ib + img_b(kF), mt * 4 + q4);
                     } else {
                         a.out[(size_t)pair * kD + row] = acc[0];
                     }
@@ -670,28 +734,48 @@ size_t mx_ximg_bytes(int n_tokens) { return (size_t)n_tokens * img_bytes(kD); }
 size_t mx_himg_bytes(int n_pairs) { return (size_t)n_pairs * img_bytes(kF); }
 size_t mx_maps_bytes() { return (size_t)kMaxGrid * 2 * (2 + 1) * 128; }
 
-cudaError_t launch_mx_ximg(const Ctx &c, const void *x, int x_bf16, int n_tokens, uint8_t *ximg) {
+// stream-K region (one token per unit): flags [2][kMaxGrid] ints, then the
+// gate/up and the down hand-over partials
+namespace {
+constexpr size_t kSkFlagBytes = (size_t)2 * kMaxGrid * sizeof(int);
+constexpr size_t kSkPart0 = (size_t)MxShape<0, 1>::NMAT * MxShape<0, 1>::NCOL * 128 * sizeof(float);
+constexpr size_t kSkPart1 = (size_t)MxShape<1, 1>::NMAT * MxShape<1, 1>::NCOL * 128 * sizeof(float);
+}  // namespace
+size_t mx_streamk_bytes() { return kSkFlagBytes + (size_t)kMaxGrid * (kSkPart0 + kSkPart1); }
+int mx_streamk_flag_count() { return 2 * kMaxGrid; }
+
+cudaError_t launch_mx_ximg(const Ctx &c, const void *x, int x_bf16, int n_tokens, uint8_t *ximg, uint8_t *sk) {
     const long long warps = (long long)n_tokens * (kD / 32);
-    k_mx_ximg<<<(unsigned)((warps + 7) / 8), 256, 0, c.stream>>>(x, x_bf16, n_tokens, ximg);
+    k_mx_ximg<<<(unsigned)((warps + 7) / 8), 256, 0, c.stream>>>(x, x_bf16, n_tokens, ximg,
+                                                                 reinterpret_cast<int *>(sk),
+                                                                 sk != nullptr ? 2 * kMaxGrid : 0);
     return cudaGetLastError();
 }
 
 cudaError_t launch_mx_gate_up(const Ctx &c, const DecodeExperts &d, int max_pairs_per_unit,
-                              const uint8_t *ximg, uint8_t *himg, float *gu, uint8_t *maps) {
+                              const uint8_t *ximg, uint8_t *himg, float *gu, uint8_t *maps, uint8_t *sk) {
     MxArgs a = mx_args(d);
     a.img_in = ximg;
     a.img_out = himg;
     a.gu = gu;
     a.maps = maps;
+    if (sk != nullptr && max_pairs_per_unit <= 1) {
+        a.flags = reinterpret_cast<int *>(sk);
+        a.partials = reinterpret_cast<float *>(sk + kSkFlagBytes);
+    }
     return max_pairs_per_unit <= 1 ? launch_mx_t<0, 1>(c, a, true) : launch_mx_t<0, kUnitPairs>(c, a, true);
 }
 
 cudaError_t launch_mx_down(const Ctx &c, const DecodeExperts &d, int max_pairs_per_unit,
-                           const uint8_t *himg, float *out, uint8_t *maps) {
+                           const uint8_t *himg, float *out, uint8_t *maps, uint8_t *sk) {
     MxArgs a = mx_args(d);
     a.img_in = himg;
     a.out = out;
     a.maps = maps + (size_t)kMaxGrid * 2 * 2 * 128;
+    if (sk != nullptr && max_pairs_per_unit <= 1) {
+        a.flags = reinterpret_cast<int *>(sk) + kMaxGrid;
+        a.partials = reinterpret_cast<float *>(sk + kSkFlagBytes + (size_t)kMaxGrid * kSkPart0);
+    }
     return max_pairs_per_unit <= 1 ? launch_mx_t<1, 1>(c, a, true) : launch_mx_t<1, kUnitPairs>(c, a, true);
 }
 

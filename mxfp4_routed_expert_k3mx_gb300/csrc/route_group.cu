@@ -344,12 +344,12 @@ __device__ void scatter_warp(const int32_t *idx, int p_begin, int p_end, int *ru
 //
 // For a few tokens the warp-per-token router leaves the GPU idle, so each
 // token gets a 256-thread CTA: thread t holds experts t, t+256, t+512,
-// t+768.  (1) fp32 estimates of the 896 keys; (2) each warp's 16 largest
-// estimates by rounds of a warp maximum, then the 16th largest of those 128,
-// a16; (3) candidates within 2^-18 * max(1,|a16|) of a16 (the same bound as
-// route_warp); (4) exact double scores for the candidates, each candidate's
-// rank among them by (key, lower index), and the sum of the 16 winners'
-// scores in slot order.
+// t+768.  (1) fp32 estimates of the 896 keys; (2) each warp sorts its 128
+// estimates (bitonic network in registers and shuffles), warp 0 sorts the
+// eight warps' 16 largest: a16 is the 16th; (3) candidates within
+// 2^-18 * max(1,|a16|) of a16 (the same bound as route_warp); (4) exact
+// double scores for the candidates, each candidate's rank among them by
+// (key, lower index), and the slot-order sum of the 16 winners' scores.
 
 constexpr int kRT = 256;                 // threads per routing CTA
 constexpr int kRS = 4;                   // expert slots per thread
@@ -363,63 +363,65 @@ struct RouteSmem {
     float cs[64];
     int sel_e[kK];
     float sel_s[kK];
+    int sorted_e[kK];
     double sum;
 };
+
+// 128 values of a warp (lane l holds positions 4l .. 4l+3) sorted in
+// descending order by a bitonic network
+__device__ __forceinline__ void warp_sort128_desc(uint32_t (&v)[kRS]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int k = 2; k <= 128; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            if (j >= kRS) {
+                const int lj = j / kRS;
+#pragma unroll
+                for (int r = 0; r < kRS; r++) {
+                    const int i = kRS * lane + r;
+                    const uint32_t o = __shfl_xor_sync(0xffffffffu, v[r], lj);
+                    const bool desc = (i & k) == 0, lower = (i & j) == 0;
+                    v[r] = (desc == lower) ? max(v[r], o) : min(v[r], o);
+                }
+            } else {
+#pragma unroll
+                for (int r = 0; r < kRS; r++) {
+                    const int q = r ^ j;
+                    if (q > r) {
+                        const int i = kRS * lane + r;
+                        const bool desc = (i & k) == 0;
+                        const uint32_t a = v[r], b = v[q];
+                        v[r] = desc ? max(a, b) : min(a, b);
+                        v[q] = desc ? min(a, b) : max(a, b);
+                    }
+                }
+            }
+        }
+    }
+}
 
 __device__ void route_cta(const float *__restrict__ lt, const float *__restrict__ bias,
                           int32_t *__restrict__ idx_t, float *__restrict__ w_t, RouteSmem &sm) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    uint32_t ok[kRS], cand[kRS];
+    uint32_t ok[kRS], v[kRS];
 #pragma unroll
     for (int j = 0; j < kRS; j++) {
         const int e = tid + kRT * j;
         ok[j] = e < kE ? order_key(canon_key(approx_score(__ldg(lt + e)) + __ldg(bias + e))) : 0u;
-        cand[j] = ok[j];
+        v[j] = ok[j];
     }
-    auto best_of = [&](const uint32_t(&v)[kRS], int &slot) {
-        uint32_t b = v[0];
-        slot = 0;
+    warp_sort128_desc(v);
+    if (lane < kK / kRS)
 #pragma unroll
-        for (int j = 1; j < kRS; j++)
-            if (v[j] > b) {
-                b = v[j];
-                slot = j;
-            }
-        return b;
-    };
-    int slot;
-    uint32_t best = best_of(cand, slot);
-#pragma unroll 1
-    for (int k = 0; k < kK; k++) {
-        const uint32_t m = __reduce_max_sync(0xffffffffu, best);
-        const int owner = __ffs(__ballot_sync(0xffffffffu, best == m)) - 1;
-        if (lane == owner) {
-#pragma unroll
-            for (int j = 0; j < kRS; j++)
-                if (j == slot) cand[j] = 0;
-            best = best_of(cand, slot);
-        }
-        if (lane == 0) sm.top[warp][k] = m;
-    }
+        for (int r = 0; r < kRS; r++) sm.top[warp][kRS * lane + r] = v[r];
     __syncthreads();
     if (warp == 0) {
-        uint32_t v[kRS];
 #pragma unroll
-        for (int j = 0; j < kRS; j++) v[j] = (&sm.top[0][0])[lane + 32 * j];
-        uint32_t b = best_of(v, slot), m16 = 0;
-#pragma unroll 1
-        for (int k = 0; k < kK; k++) {
-            m16 = __reduce_max_sync(0xffffffffu, b);
-            const int owner = __ffs(__ballot_sync(0xffffffffu, b == m16)) - 1;
-            if (lane == owner) {
-#pragma unroll
-                for (int j = 0; j < kRS; j++)
-                    if (j == slot) v[j] = 0;
-                b = best_of(v, slot);
-            }
-        }
-        if (lane == 0) {
-            const float a16 = key_of_order(m16);
+        for (int r = 0; r < kRS; r++) v[r] = (&sm.top[0][0])[kRS * lane + r];
+        warp_sort128_desc(v);
+        if (lane == (kK - 1) / kRS) {
+            const float a16 = key_of_order(v[(kK - 1) % kRS]);
             // a non-finite a16 (infinite biases) keeps every expert: exact path
             sm.tau = isfinite(a16) ? order_key(a16 - 0x1p-18f * fmaxf(1.0f, fabsf(a16))) : 0u;
             sm.n = 0;
@@ -439,6 +441,9 @@ __device__ void route_cta(const float *__restrict__ lt, const float *__restrict_
     const int n = sm.n;
     if (n > 64) {
         if (warp == 0) route_warp_all(lt, bias, idx_t, w_t, lane);
+        __syncthreads();
+        if (tid < kK) sm.sel_e[tid] = idx_t[tid];
+        __syncthreads();
         return;
     }
     if (tid < n) {
@@ -460,8 +465,22 @@ __device__ void route_cta(const float *__restrict__ lt, const float *__restrict_
     }
     __syncthreads();
     if (tid == 0) {
-        double sum = 0.0;
-        for (int r = 0; r < kK; r++) sum += (double)sm.sel_s[r];   // slot order, as on the CPU
+        // The slot-order double sum.  With every score in [2^-24, 1] each
+        // term is a multiple of 2^-47 and the sum stays below 2^5, so every
+        // partial sum is exact in double and the sum equals the integer
+        // sum of the scores in units of 2^-47 (no double adds needed).
+        bool fixed = true;
+        long long acc = 0;
+        for (int r = 0; r < kK; r++) {
+            const float sr = sm.sel_s[r];
+            fixed = fixed && sr >= 0x1p-24f && sr <= 1.0f;
+            acc += (long long)__float2ll_rz(sr * 0x1p47f);
+        }
+        double sum = (double)acc * 0x1p-47;
+        if (!fixed) {
+            sum = 0.0;
+            for (int r = 0; r < kK; r++) sum += (double)sm.sel_s[r];
+        }
         sm.sum = sum;
     }
     __syncthreads();
@@ -471,15 +490,62 @@ __device__ void route_cta(const float *__restrict__ lt, const float *__restrict_
     }
 }
 
-// CTAs 0..n_tokens-1 route one token each; the CTAs after them (when x is
-// given) write the tokens' x piece images, one warp per 32-column block.
+// Grouping of a single token's 16 pairs (pair p = slot p) inside its
+// routing CTA: the 16 experts are distinct, so each has one pair and one
+// work unit; units and perm follow increasing expert index.
+__device__ void group_one_token(const int32_t *__restrict__ idx_t, const GroupOut &g, RouteSmem &sm) {
+    const int tid = threadIdx.x;
+    if (tid < kK) {
+        const int e = idx_t[tid];
+        int rank = 0;
+        for (int u = 0; u < kK; u++) rank += idx_t[u] < e;
+        sm.sorted_e[rank] = e;
+        g.perm[rank] = tid;
+        g.act[rank] = e;
+        g.units[3 * rank + 0] = e;
+        g.units[3 * rank + 1] = rank;
+        g.units[3 * rank + 2] = rank + 1;
+    }
+    __syncthreads();
+    for (int e = tid; e <= kE; e += kRT) {
+        int below = 0, hit = 0;
+        for (int u = 0; u < kK; u++) {
+            below += sm.sorted_e[u] < e;
+            hit |= sm.sorted_e[u] == e;
+        }
+        g.offsets[e] = below;
+        if (e < kE) g.counts[e] = hit;
+    }
+    if (tid == 0) {
+        *g.n_active = kK;
+        *g.n_units = kK;
+    }
+}
+
+// CTAs 0..n_tokens-1 route one token each (and, for a single token with a
+// work-unit list, group it); the CTAs after them (when x is given) write
+// the tokens' x piece images, one warp per 32-column block.
 __global__ void __launch_bounds__(kRT)
 k_route_prep(int32_t *idx, float *w, const float *logits, const float *bias, int n_tokens,
-             const void *x, int x_bf16, uint8_t *ximg) {
+             const void *x, int x_bf16, uint8_t *ximg, GroupOut g, int *flags, int n_flags,
+             const k3mx_expert *experts) {
     __shared__ RouteSmem sm;
+    // the expert passes may launch now: their prologues overlap this kernel
+    pdl_launch_dependents();
+    if (blockIdx.x == 0) {
+        for (int i = threadIdx.x; i < n_flags; i += blockDim.x) flags[i] = 0;
+        // the expert pointer table into L2 for the passes' first lookups
+        if (experts != nullptr)
+            for (int i = threadIdx.x; i < (int)(kE * sizeof(k3mx_expert) / 128); i += blockDim.x)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const uint8_t *>(experts) + 128 * i));
+    }
     if ((int)blockIdx.x < n_tokens) {
         const int t = blockIdx.x;
         route_cta(logits + (size_t)t * kE, bias, idx + (size_t)t * kK, w + (size_t)t * kK, sm);
+        if (n_tokens == 1 && g.units != nullptr) {
+            __syncthreads();
+            group_one_token(idx, g, sm);
+        }
     } else {
         ximg_block(x, x_bf16, n_tokens, ximg, (blockIdx.x - n_tokens) * (kRT / 32) + (threadIdx.x >> 5));
     }
@@ -588,10 +654,13 @@ cudaError_t launch_route_group_small(const Ctx &c, int32_t *idx, float *w, const
 
 cudaError_t launch_route_prep(const Ctx &c, int32_t *idx, float *w, const float *logits,
                               const float *bias, int n_tokens, const void *x, int x_bf16,
-                              uint8_t *ximg) {
+                              uint8_t *ximg, const GroupOut *g_one, int *flags, int n_flags,
+                              const k3mx_expert *experts) {
     const int piece_ctas = x != nullptr ? (n_tokens * (kD / 32) + kRT / 32 - 1) / (kRT / 32) : 0;
+    GroupOut g{};
+    if (g_one != nullptr && n_tokens == 1) g = *g_one;
     k_route_prep<<<n_tokens + piece_ctas, kRT, 0, c.stream>>>(idx, w, logits, bias, n_tokens, x, x_bf16,
-                                                              ximg);
+                                                              ximg, g, flags, flags ? n_flags : 0, experts);
     return cudaGetLastError();
 }
 

@@ -73,7 +73,8 @@ def test_moe_refuses_bad_arguments():
 
 def test_workspace_sizes():
     d = [k3mx.k3mx_moe_workspace_size(t, 0, 1) for t in (1, 2, 64, 1000)]
-    assert all(a < b for a, b in zip(d, d[1:]))
+    # grows with the batch (one token also holds the split-item hand-over region)
+    assert all(a < b for a, b in zip(d[1:], d[2:])) and d[0] > 0
     # the decode path keeps h and the per-pair outputs in fp32
     assert k3mx.k3mx_moe_workspace_size(64, 0, 1) >= 64 * 16 * (2 * 3072 + 3584) * 4
     # AUTO picks prefill for bf16 and many tokens; its h is f16
