@@ -164,7 +164,7 @@ MoeLayout moe_layout(int n_tokens, int x_dtype, int path) {
     if (path == K3MX_PATH_DECODE) {
         L.ximg = take(mx_ximg_bytes(n_tokens));  // x of every token as MXFP4 pieces
         L.himg = take(mx_himg_bytes((int)P));    // h of every pair as MXFP4 pieces
-        L.maps = take(mx_maps_bytes());
+        L.maps = take(mx_maps_bytes(kE));          // weight tensor maps of the expert table
         L.sk = n_tokens == 1 ? take(mx_streamk_bytes()) : 0;   // stream-K hand-over (one token)
         L.h = take(P * 2 * kF * 4);          // g and u per pair
         L.stage = take(P * kD * 4);
@@ -222,7 +222,7 @@ k3mx_status run_moe(const Ctx &c, float *y, const void *x, int x_dtype, int n_to
         err = traced("route", c.stream, [&] {
             return launch_route_prep(c, idx, w, logits, bias, n_tokens, decode ? x : nullptr, x_bf16, ximg,
                                      one ? &g : nullptr, reinterpret_cast<int *>(sk), mx_streamk_flag_count(),
-                                     decode ? experts : nullptr);
+                                     decode ? experts : nullptr, decode ? at<uint8_t>(ws, L.maps) : nullptr);
         });
         if (err == cudaSuccess && !one)
             err = traced("group_small", c.stream, [&] { return launch_group_small(c, idx, n_tokens, g); });
@@ -260,7 +260,8 @@ k3mx_status run_moe(const Ctx &c, float *y, const void *x, int x_dtype, int n_to
     float *stage = at<float>(ws, L.stage);
     const int upairs = n_tokens == 1 ? 1 : kUnitPairs;
     if (!pieces_done)
-        err = traced("mx_pieces", c.stream, [&] { return launch_mx_ximg(c, x, x_bf16, n_tokens, ximg, sk); });
+        err = traced("mx_pieces", c.stream,
+                     [&] { return launch_mx_ximg(c, x, x_bf16, n_tokens, ximg, sk, maps, experts, nullptr); });
     if (err == cudaSuccess)
         err = traced("decode_gate_up", c.stream,
                      [&] { return launch_mx_gate_up(c, d, upairs, ximg, himg, gu, maps, sk); });
@@ -310,7 +311,7 @@ k3mx_status k3mx_gemv(float *y, const float *x, const uint8_t *packed, const uin
 // expert_ffn workspace: g and u [2][F] fp32, x and h piece images, tensor-map slots
 size_t k3mx_expert_ffn_workspace_size(void) {
     return up256((size_t)2 * kF * sizeof(float)) + up256(mx_ximg_bytes(1)) + up256(mx_himg_bytes(1)) +
-           up256(mx_maps_bytes()) + up256(mx_streamk_bytes());
+           up256(mx_maps_bytes(1)) + up256(mx_streamk_bytes());
 }
 
 k3mx_status k3mx_expert_ffn(float *y, const float *x, const k3mx_expert *expert, void *workspace,
@@ -332,8 +333,9 @@ k3mx_status k3mx_expert_ffn(float *y, const float *x, const k3mx_expert *expert,
     uint8_t *ximg = reinterpret_cast<uint8_t *>(ws + up256((size_t)2 * kF * sizeof(float)));
     uint8_t *himg = ximg + up256(mx_ximg_bytes(1));
     uint8_t *maps = himg + up256(mx_himg_bytes(1));
-    uint8_t *sk = maps + up256(mx_maps_bytes());
-    cudaError_t err = traced("mx_pieces", c.stream, [&] { return launch_mx_ximg(c, x, 0, 1, ximg, sk); });
+    uint8_t *sk = maps + up256(mx_maps_bytes(1));
+    cudaError_t err = traced("mx_pieces", c.stream,
+                             [&] { return launch_mx_ximg(c, x, 0, 1, ximg, sk, maps, nullptr, expert); });
     if (err == cudaSuccess)
         err = traced("decode_gate_up", c.stream,
                      [&] { return launch_mx_gate_up(c, d, 1, ximg, himg, gu, maps, sk); });

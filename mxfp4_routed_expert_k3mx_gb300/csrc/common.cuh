@@ -271,12 +271,13 @@ struct GroupOut {
 cudaError_t launch_route(const Ctx &c, int32_t *idx, float *w, const float *logits,
                          const float *bias, int n_tokens);
 // routing with one CTA per token (n_tokens <= 64) plus, when x is given, the
-// tokens' x piece images (mx path) in the same launch; a single token with
-// `g_one` is also grouped there (else group with launch_group_small)
+// tokens' x piece images and the weight tensor maps of the expert table
+// (mx path) in the same launch; a single token with `g_one` is also
+// grouped there (else group with launch_group_small)
 cudaError_t launch_route_prep(const Ctx &c, int32_t *idx, float *w, const float *logits,
                               const float *bias, int n_tokens, const void *x, int x_bf16,
                               uint8_t *ximg, const GroupOut *g_one, int *flags, int n_flags,
-                              const k3mx_expert *experts);
+                              const k3mx_expert *experts, uint8_t *maps);
 // grouping of n_tokens * 16 <= 1024 pairs, programmatic dependent of the routing
 cudaError_t launch_group_small(const Ctx &c, const int32_t *idx, int n_tokens, const GroupOut &g);
 // route + group in one CTA (n_tokens * 16 <= 1024)
@@ -315,13 +316,15 @@ size_t library_scratch_bytes();
 // MMA reads; tensor-map slots: per-CTA copies of the weight tensor maps.
 size_t mx_ximg_bytes(int n_tokens);
 size_t mx_himg_bytes(int n_pairs);
-size_t mx_maps_bytes();
+size_t mx_maps_bytes(int n_experts);
 // stream-K hand-over region of single-token decode (flags + partials); the
 // step's first kernel zeroes the mx_streamk_flag_count() flags at its start
 size_t mx_streamk_bytes();
 int mx_streamk_flag_count();
-// x pieces of every token (and, with `sk`, the stream-K flags zeroed)
-cudaError_t launch_mx_ximg(const Ctx &c, const void *x, int x_bf16, int n_tokens, uint8_t *ximg, uint8_t *sk);
+// x pieces of every token, the weight tensor maps of the expert table (or
+// of the single expert `one`), and, with `sk`, the stream-K flags zeroed
+cudaError_t launch_mx_ximg(const Ctx &c, const void *x, int x_bf16, int n_tokens, uint8_t *ximg, uint8_t *sk,
+                           uint8_t *maps, const k3mx_expert *table, const k3mx_expert *one);
 // gate/up: g, u -> gu [pair][2][F]; h = SiTU(g, u) -> piece images himg
 cudaError_t launch_mx_gate_up(const Ctx &c, const DecodeExperts &d, int max_pairs_per_unit,
                               const uint8_t *ximg, uint8_t *himg, float *gu, uint8_t *maps, uint8_t *sk);

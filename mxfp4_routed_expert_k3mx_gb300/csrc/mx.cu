@@ -32,11 +32,11 @@
 // Two accumulator buffers let the epilogue of one item overlap the MMAs of
 // the next.  Every wait is bounded; a timeout is reported on the device
 // status word and every role leaves its loop.
-#include <cuda.h>
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
 #include "pieces.cuh"
+#include "tmaps.cuh"
 
 namespace k3mx {
 namespace {
@@ -65,7 +65,11 @@ template <int PH, int NTOK> struct MxShape {
     // the whole current part (a copy issued at the part boundary waits
     // behind the weight stream); several tokens: one (shared memory)
     static constexpr int SBUF = NTOK == 1 ? 2 : 1;
-    static constexpr int FIXED = 1024 + NTOK * (TOKB + TOKS) + SBUF * SRAW;  // header, images, scales
+    // down with one token per unit: two piece-image buffers, so the next
+    // pair's h images load while the current unit's MMAs run (gate/up keeps
+    // the token's x images for every unit)
+    static constexpr int BBUF = PH == 1 && NTOK == 1 ? 2 : 1;
+    static constexpr int FIXED = 1024 + BBUF * NTOK * (TOKB + TOKS) + SBUF * SRAW;  // header, images, scales
     static constexpr int S_FIT = (kSmemLimit - 1024 - FIXED) / STAGE;
     static constexpr int S = S_FIT > 10 ? 10 : S_FIT;
     static constexpr int SMEM = 1024 + FIXED + S * STAGE;          // + 1024 alignment slack
@@ -86,14 +90,14 @@ struct MxArgs {
     uint8_t *img_out;               // gate/up: per-pair h images
     float *gu;                      // gate/up: [pair][2][F]
     float *out;                     // down: [pair][D]
-    uint8_t *maps;                  // this pass's tensor-map slots [grid][2][NMAT][128 B]
+    const uint8_t *maps;            // per-expert weight tensor maps [expert][w1, w3, w2]
     float *partials;                // stream-K hand-over accumulators [grid][NMAT][NCOL][128], or null
     int *flags;                     // [grid] hand-over flags, zeroed by the step's first kernel
     int *status;
 };
 
 struct Hdr {
-    uint64_t full[10], empty[10], accf[2], acce[2], bfull, bempty, sfull[2], done;
+    uint64_t full[10], empty[10], accf[2], acce[2], bfull[2], bempty[2], sfull[2], done;
     uint32_t tmem;
     int abort;
 };
@@ -139,30 +143,6 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const void *map, int x, int
         "l"(map), "r"(x), "r"(y), "r"(bar), "l"(policy)
         : "memory");
 }
-// a copy of a tensor map (staged in shared memory) with its global address
-// replaced, published to `gmap` for the tensor-map proxy (whole warp)
-__device__ __forceinline__ void publish_map(void *gmap, uint32_t smap, const CUtensorMap &tmpl,
-                                            const void *addr) {
-    const int lane = threadIdx.x & 31;
-    if (lane < 8) {
-        const uint4 v = reinterpret_cast<const uint4 *>(&tmpl)[lane];
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(smap + 16 * lane), "r"(v.x),
-                     "r"(v.y), "r"(v.z), "r"(v.w)
-                     : "memory");
-    }
-    __syncwarp();
-    if (lane == 0)
-        asm volatile("tensormap.replace.tile.global_address.shared::cta.b1024.b64 [%0], %1;" ::"r"(smap),
-                     "l"(reinterpret_cast<uint64_t>(addr))
-                     : "memory");
-    __syncwarp();
-    asm volatile(
-        "tensormap.cp_fenceproxy.global.shared::cta.tensormap::generic.release.cta.sync.aligned "
-        "[%0], [%1], 128;" ::"l"(gmap),
-        "r"(smap)
-        : "memory");
-    asm volatile("fence.proxy.tensormap::generic.acquire.cta [%0], 128;" ::"l"(gmap) : "memory");
-}
 template <int N>
 __device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&v)[N]);
 template <>
@@ -201,11 +181,21 @@ __device__ __forceinline__ uint64_t l2_evict_last_policy() {
 __device__ __forceinline__ uint32_t drop_nan_scales(uint32_t w) { return w & ~__vcmpeq4(w, 0xFFFFFFFFu); }
 
 // x of every token -> its piece image; one warp per 32-column block
+// x of every token -> its piece image (one warp per 32-column block); the
+// CTAs after those build the weight tensor maps of the expert table (or of
+// the single expert `one`); CTA 0 zeroes the stream-K flags
 __global__ void __launch_bounds__(256) k_mx_ximg(const void *__restrict__ x, int bf16, int n_tokens,
-                                                 uint8_t *__restrict__ img, int *flags, int n_flags) {
+                                                 uint8_t *__restrict__ img, int *flags, int n_flags,
+                                                 int piece_ctas, uint8_t *maps, int n_map_experts,
+                                                 const k3mx_expert *table, k3mx_expert one,
+                                                 const __grid_constant__ CUtensorMap w13,
+                                                 const __grid_constant__ CUtensorMap w2) {
     if (flags != nullptr && blockIdx.x == 0)
         for (int i = threadIdx.x; i < n_flags; i += blockDim.x) flags[i] = 0;
-    ximg_block(x, bf16, n_tokens, img, blockIdx.x * 8 + (threadIdx.x >> 5));
+    if ((int)blockIdx.x < piece_ctas)
+        ximg_block(x, bf16, n_tokens, img, blockIdx.x * 8 + (threadIdx.x >> 5));
+    else
+        build_maps_cta(maps, n_map_experts, table, one, w13, w2, blockIdx.x - piece_ctas);
 }
 
 // ------------------------------------------------------------ work units --
@@ -248,7 +238,7 @@ __device__ __forceinline__ int pair_at(const MxArgs &a, int slot) {
 
 template <int PH, int NTOK>
 __global__ void __launch_bounds__(kThreads, 1)
-    k_mx(const MxArgs a, const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1) {
+    k_mx(const MxArgs a) {
     using Sh = MxShape<PH, NTOK>;
     constexpr int NMAT = Sh::NMAT, KC = Sh::KC, MT = Sh::MT, G = Sh::G, S = Sh::S, NCOL = Sh::NCOL;
 
@@ -256,15 +246,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Hdr *hd = reinterpret_cast<Hdr *>(smem);
     const uint32_t sbase = smem_addr(smem);
-    const uint32_t smap0 = sbase + 512;                           // 2 x 128 B tensor-map staging
     const uint32_t st0 = sbase + 1024;                            // stages
-    const uint32_t bimg = st0 + S * Sh::STAGE;                    // unit's B images [NTOK][TOKB]
-    const uint32_t simg = bimg + NTOK * Sh::TOKB;                 // unit's scale images [NTOK][TOKS]
-    const uint32_t sraw0 = simg + NTOK * Sh::TOKS;                // tile's scale rows [SBUF][NMAT][128][G]
+    constexpr int BB = Sh::BBUF;
+    const uint32_t bimg0 = st0 + S * Sh::STAGE;                   // unit's B images [BBUF][NTOK][TOKB]
+    const uint32_t simg0 = bimg0 + BB * NTOK * Sh::TOKB;          // unit's scale images [BBUF][NTOK][TOKS]
+    const uint32_t sraw0 = simg0 + BB * NTOK * Sh::TOKS;          // tile's scale rows [SBUF][NMAT][128][G]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t full0 = smem_addr(hd->full), empty0 = smem_addr(hd->empty);
     const uint32_t accf0 = smem_addr(hd->accf), acce0 = smem_addr(hd->acce);
-    const uint32_t bfull = smem_addr(&hd->bfull), bempty = smem_addr(&hd->bempty);
+    const uint32_t bfull0 = smem_addr(hd->bfull), bempty0 = smem_addr(hd->bempty);
     const uint32_t sfull0 = smem_addr(hd->sfull);
     const uint32_t done = smem_addr(&hd->done);
 
@@ -277,8 +267,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(accf0 + 8 * i, 1);
             mbar_init(acce0 + 8 * i, 128);
         }
-        mbar_init(bfull, 1);
-        mbar_init(bempty, 1);
+        for (int i = 0; i < 2; i++) {
+            mbar_init(bfull0 + 8 * i, 1);
+            mbar_init(bempty0 + 8 * i, 1);
+        }
         mbar_init(sfull0, 1);
         mbar_init(sfull0 + 8, 1);
         mbar_init(done, 1);
@@ -350,8 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------- TMA producer --
         const uint64_t pol = l2_evict_first_policy();     // weights: read once
         const uint64_t pol_img = l2_evict_last_policy();   // piece images: read by every CTA
-        uint8_t *gmaps = a.maps + (size_t)blockIdx.x * (2 * NMAT * 128);
-        int cur_e = -1, slot = 0;
+        int cur_e = -1;
+        const uint8_t *map0 = nullptr, *map1 = nullptr;
         long long cur_key = -1, q = q0;
         uint32_t su = 0, bl = 0;
         bool waited = PH == 0;
@@ -360,44 +352,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Unit &u = p.u;
             const int mt = (int)(p.item % MT);
             if (u.e != cur_e) {
-                slot ^= 1;
-                publish_map(gmaps + (slot * NMAT + 0) * 128, smap0, tm0, PH == 0 ? u.ex.w1 : u.ex.w2);
-                if (NMAT == 2) publish_map(gmaps + (slot * NMAT + 1) * 128, smap0 + 128, tm1, u.ex.w3);
+                const uint8_t *em = a.maps + (size_t)u.e * kMapsPerExpert * kMapBytes;
+                map0 = em + (PH == 0 ? 0 : 2) * kMapBytes;
+                map1 = em + 1 * kMapBytes;
+                acquire_map(map0);
+                if (NMAT == 2) acquire_map(map1);
                 cur_e = u.e;
             }
-            const long long key = unit_key(u);
-            if (key != cur_key) {
-                if (!waited) {
-                    pdl_wait();
-                    waited = true;
-                }
-                if (bl > 0 && !mbar_wait(bempty, (bl - 1) & 1)) {
-                    if (lane == 0) fail(1);
-                    break;
-                }
-                const int ntok = u.p1 - u.p0;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(bfull, (uint32_t)(ntok * (Sh::TOKB + Sh::TOKS)));
-                    for (int j = 0; j < ntok; j++) {
-                        const int pair = pair_at(a, u.p0 + j);
-                        const int src = PH == 0 ? pair / kK : pair;
-                        const uint8_t *img = a.img_in + (size_t)src * img_bytes(Sh::K);
-                        bulk_g2s(bimg + j * Sh::TOKB, img, Sh::TOKB, bfull, pol_img);
-                        bulk_g2s(simg + j * Sh::TOKS, img + Sh::TOKB, Sh::TOKS, bfull, pol_img);
-                    }
-                }
-                bl++;
-                cur_key = key;
-            }
-            const uint8_t *map0 = gmaps + (slot * NMAT + 0) * 128;
-            const uint8_t *map1 = gmaps + (slot * NMAT + (NMAT - 1)) * 128;
-            bool ok = true;
-            for (int c = p.lo; c < p.hi; c++, su++) {
+            // the first weight tile goes out before the piece-image lookups
+            auto issue_stage = [&](int c) -> bool {
                 const int s = su % S;
                 if (!mbar_wait(empty0 + 8 * s, ((su / S) & 1) ^ 1)) {
                     if (lane == 0) fail(2);
-                    ok = false;
-                    break;
+                    return false;
                 }
                 if (lane == 0) {
                     const uint32_t dst = st0 + s * Sh::STAGE;
@@ -406,7 +373,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (NMAT == 2) tma_2d(dst + kTileBytes, map1, c * 128, mt * 128, full0 + 8 * s, pol);
                 }
                 __syncwarp();
+                su++;
+                return true;
+            };
+            if (!issue_stage(p.lo)) break;
+            const long long key = unit_key(u);
+            if (key != cur_key) {
+                if (!waited) {
+                    pdl_wait();
+                    waited = true;
+                }
+                // B buffer bl % BB: wait until the MMAs of its previous fill are done
+                const int bb = bl % BB;
+                if (bl >= (uint32_t)BB && !mbar_wait(bempty0 + 8 * bb, (bl / BB - 1) & 1)) {
+                    if (lane == 0) fail(1);
+                    break;
+                }
+                const int ntok = u.p1 - u.p0;
+                if (lane == 0) {
+                    const uint32_t bfull = bfull0 + 8 * bb;
+                    mbar_arrive_expect_tx(bfull, (uint32_t)(ntok * (Sh::TOKB + Sh::TOKS)));
+                    for (int j = 0; j < ntok; j++) {
+                        const int pair = pair_at(a, u.p0 + j);
+                        const int src = PH == 0 ? pair / kK : pair;
+                        const uint8_t *img = a.img_in + (size_t)src * img_bytes(Sh::K);
+                        bulk_g2s(bimg0 + (bb * NTOK + j) * Sh::TOKB, img, Sh::TOKB, bfull, pol_img);
+                        bulk_g2s(simg0 + (bb * NTOK + j) * Sh::TOKS, img + Sh::TOKB, Sh::TOKS, bfull, pol_img);
+                    }
+                }
+                bl++;
+                cur_key = key;
             }
+            bool ok = true;
+            for (int c = p.lo + 1; c < p.hi && ok; c++) ok = issue_stage(c);
             if (!ok) break;
         }
     } else if (warp == kSfWarp) {
@@ -487,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kMmaWarp) {
         // ----------------------------------------------------- MMA issuer --
         if (lane == 0) {
-            uint32_t su = 0, bu = 0, it = 0;
+            uint32_t su = 0, bu = 0, it = 0, bcur = 0;
             long long cur_key = -1, q = q0;
             bool run = true;
             Part p;
@@ -497,7 +496,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int ntok = u.p1 - u.p0;
                 const int n = ntok <= 1 ? 8 : (ntok == 2 ? 16 : 32);
                 if (key != cur_key) {
-                    if (!mbar_wait(bfull, bu & 1)) {
+                    bcur = bu % BB;
+                    if (!mbar_wait(bfull0 + 8 * bcur, (bu / BB) & 1)) {
                         fail(4);
                         break;
                     }
@@ -505,6 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     // one token: the atom's four 8-line groups all read its lines
                     // (rows 8-31 are never used with N = 8)
+                    const uint32_t simg = simg0 + bcur * NTOK * Sh::TOKS;
                     for (int at = 0; at < Sh::K / 128; at++)
                         tmem_cp_atom(tmem + Sh::SFB_COL + 4 * at,
                                      desc_atom(simg + at * 128, NTOK == 1 ? 0 : Sh::TOKS));
@@ -538,7 +539,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int ks = 0; ks < 4; ks++) {
                             const int id = 2 * (ks & 1);
                             mma_mxf4(tmem + (b * NMAT + m) * NCOL, desc_sw128(stg + m * kTileBytes + 32 * ks, 1024),
-                                     desc_sw128(bimg + c * 1024 + 32 * ks, Sh::TOKB), idesc_mxf4(n, id),
+                                     desc_sw128(bimg0 + bcur * NTOK * Sh::TOKB + c * 1024 + 32 * ks, Sh::TOKB),
+                                     idesc_mxf4(n, id),
                                      sfa + m * 8 + (ks >> 1) * 4, tmem + Sh::SFB_COL + (c * 2 + (ks >> 1)) * 4,
                                      (c != p.lo || ks != 0) ? 1u : 0u);
                         }
@@ -550,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // release the unit's B images once its last MMA is done
                 long long qn = q;
                 Part nx;
-                if (!next_part(qn, nx) || unit_key(nx.u) != key) umma_commit(bempty);
+                if (!next_part(qn, nx) || unit_key(nx.u) != key) umma_commit(bempty0 + 8 * bcur);
             }
             umma_commit(done);
         }
@@ -648,9 +650,47 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------- launchers --
 
-// Tensor-map templates of the weight matrices (uint8 view of the packed
-// bytes, 128 x 128-byte boxes, 128-byte swizzle), encoded once per device.
-// The kernels replace the global address per expert; the templates point at
+template <int PH, int NTOK>
+cudaError_t launch_mx_t(const Ctx &c, MxArgs a, bool pdl) {
+    using Sh = MxShape<PH, NTOK>;
+    static bool configured = false;
+    if (!configured) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(k_mx<PH, NTOK>, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    a.status = c.status;
+    int grid = c.num_sms < kMaxGrid ? c.num_sms : kMaxGrid;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Sh::SMEM;
+    cfg.stream = c.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k_mx<PH, NTOK>, a);
+}
+
+MxArgs mx_args(const DecodeExperts &d) {
+    MxArgs a{};
+    if (d.single) {
+        a.one = *d.single;
+    } else {
+        a.experts = d.experts;
+        a.units = d.units;
+        a.n_units = d.n_units;
+        a.perm = d.perm;
+    }
+    return a;
+}
+
+}  // namespace
+
+// Tensor-map templates (tmaps.cuh), encoded once per device.  They point at
 // the library's own scratch array (larger than one matrix), so a map is
 // never left pointing at memory that is not allocated.
 bool weight_map_templates(CUtensorMap &w13, CUtensorMap &w2) {
@@ -688,51 +728,9 @@ bool weight_map_templates(CUtensorMap &w13, CUtensorMap &w2) {
     return true;
 }
 
-template <int PH, int NTOK>
-cudaError_t launch_mx_t(const Ctx &c, MxArgs a, bool pdl) {
-    using Sh = MxShape<PH, NTOK>;
-    CUtensorMap w13, w2;
-    if (!weight_map_templates(w13, w2)) return cudaErrorNotSupported;
-    static bool configured = false;
-    if (!configured) {
-        const cudaError_t e =
-            cudaFuncSetAttribute(k_mx<PH, NTOK>, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
-    a.status = c.status;
-    int grid = c.num_sms < kMaxGrid ? c.num_sms : kMaxGrid;
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = Sh::SMEM;
-    cfg.stream = c.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, k_mx<PH, NTOK>, a, PH == 0 ? w13 : w2, w13);
-}
-
-MxArgs mx_args(const DecodeExperts &d) {
-    MxArgs a{};
-    if (d.single) {
-        a.one = *d.single;
-    } else {
-        a.experts = d.experts;
-        a.units = d.units;
-        a.n_units = d.n_units;
-        a.perm = d.perm;
-    }
-    return a;
-}
-
-}  // namespace
-
 size_t mx_ximg_bytes(int n_tokens) { return (size_t)n_tokens * img_bytes(kD); }
 size_t mx_himg_bytes(int n_pairs) { return (size_t)n_pairs * img_bytes(kF); }
-size_t mx_maps_bytes() { return (size_t)kMaxGrid * 2 * (2 + 1) * 128; }
+size_t mx_maps_bytes(int n_experts) { return expert_maps_bytes(n_experts); }
 
 // stream-K region (one token per unit): flags [2][kMaxGrid] ints, then the
 // gate/up and the down hand-over partials
@@ -744,11 +742,18 @@ constexpr size_t kSkPart1 = (size_t)MxShape<1, 1>::NMAT * MxShape<1, 1>::NCOL * 
 size_t mx_streamk_bytes() { return kSkFlagBytes + (size_t)kMaxGrid * (kSkPart0 + kSkPart1); }
 int mx_streamk_flag_count() { return 2 * kMaxGrid; }
 
-cudaError_t launch_mx_ximg(const Ctx &c, const void *x, int x_bf16, int n_tokens, uint8_t *ximg, uint8_t *sk) {
+cudaError_t launch_mx_ximg(const Ctx &c, const void *x, int x_bf16, int n_tokens, uint8_t *ximg, uint8_t *sk,
+                           uint8_t *maps, const k3mx_expert *table, const k3mx_expert *one) {
+    CUtensorMap w13, w2;
+    if (!weight_map_templates(w13, w2)) return cudaErrorNotSupported;
     const long long warps = (long long)n_tokens * (kD / 32);
-    k_mx_ximg<<<(unsigned)((warps + 7) / 8), 256, 0, c.stream>>>(x, x_bf16, n_tokens, ximg,
-                                                                 reinterpret_cast<int *>(sk),
-                                                                 sk != nullptr ? 2 * kMaxGrid : 0);
+    const int piece_ctas = (int)((warps + 7) / 8);
+    const int n_map_experts = one != nullptr ? 1 : kE;
+    const int map_ctas = (n_map_experts * kMapsPerExpert + 7) / 8;
+    const k3mx_expert single = one != nullptr ? *one : k3mx_expert{};
+    k_mx_ximg<<<(unsigned)(piece_ctas + map_ctas), 256, 0, c.stream>>>(
+        x, x_bf16, n_tokens, ximg, reinterpret_cast<int *>(sk), sk != nullptr ? 2 * kMaxGrid : 0, piece_ctas,
+        maps, n_map_experts, one != nullptr ? nullptr : table, single, w13, w2);
     return cudaGetLastError();
 }
 
@@ -771,7 +776,7 @@ cudaError_t launch_mx_down(const Ctx &c, const DecodeExperts &d, int max_pairs_p
     MxArgs a = mx_args(d);
     a.img_in = himg;
     a.out = out;
-    a.maps = maps + (size_t)kMaxGrid * 2 * 2 * 128;
+    a.maps = maps;
     if (sk != nullptr && max_pairs_per_unit <= 1) {
         a.flags = reinterpret_cast<int *>(sk) + kMaxGrid;
         a.partials = reinterpret_cast<float *>(sk + kSkFlagBytes + (size_t)kMaxGrid * kSkPart0);

@@ -21,6 +21,7 @@
 // is a stable warp-sequential scatter, so the output is deterministic.
 #include "common.cuh"
 #include "pieces.cuh"
+#include "tmaps.cuh"
 
 namespace k3mx {
 namespace {
@@ -402,7 +403,8 @@ __device__ __forceinline__ void warp_sort128_desc(uint32_t (&v)[kRS]) {
 }
 
 __device__ void route_cta(const float *__restrict__ lt, const float *__restrict__ bias,
-                          int32_t *__restrict__ idx_t, float *__restrict__ w_t, RouteSmem &sm) {
+                          int32_t *__restrict__ idx_t, float *__restrict__ w_t,
+                          const k3mx_expert *__restrict__ experts, RouteSmem &sm) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint32_t ok[kRS], v[kRS];
 #pragma unroll
@@ -528,7 +530,8 @@ __device__ void group_one_token(const int32_t *__restrict__ idx_t, const GroupOu
 __global__ void __launch_bounds__(kRT)
 k_route_prep(int32_t *idx, float *w, const float *logits, const float *bias, int n_tokens,
              const void *x, int x_bf16, uint8_t *ximg, GroupOut g, int *flags, int n_flags,
-             const k3mx_expert *experts) {
+             const k3mx_expert *experts, int piece_ctas, uint8_t *maps,
+             const __grid_constant__ CUtensorMap w13, const __grid_constant__ CUtensorMap w2) {
     __shared__ RouteSmem sm;
     // the expert passes may launch now: their prologues overlap this kernel
     pdl_launch_dependents();
@@ -541,13 +544,15 @@ k_route_prep(int32_t *idx, float *w, const float *logits, const float *bias, int
     }
     if ((int)blockIdx.x < n_tokens) {
         const int t = blockIdx.x;
-        route_cta(logits + (size_t)t * kE, bias, idx + (size_t)t * kK, w + (size_t)t * kK, sm);
+        route_cta(logits + (size_t)t * kE, bias, idx + (size_t)t * kK, w + (size_t)t * kK, experts, sm);
         if (n_tokens == 1 && g.units != nullptr) {
             __syncthreads();
             group_one_token(idx, g, sm);
         }
-    } else {
+    } else if ((int)blockIdx.x < n_tokens + piece_ctas) {
         ximg_block(x, x_bf16, n_tokens, ximg, (blockIdx.x - n_tokens) * (kRT / 32) + (threadIdx.x >> 5));
+    } else {
+        build_maps_cta(maps, kE, experts, k3mx_expert{}, w13, w2, blockIdx.x - n_tokens - piece_ctas);
     }
 }
 
@@ -655,12 +660,19 @@ cudaError_t launch_route_group_small(const Ctx &c, int32_t *idx, float *w, const
 cudaError_t launch_route_prep(const Ctx &c, int32_t *idx, float *w, const float *logits,
                               const float *bias, int n_tokens, const void *x, int x_bf16,
                               uint8_t *ximg, const GroupOut *g_one, int *flags, int n_flags,
-                              const k3mx_expert *experts) {
+                              const k3mx_expert *experts, uint8_t *maps) {
     const int piece_ctas = x != nullptr ? (n_tokens * (kD / 32) + kRT / 32 - 1) / (kRT / 32) : 0;
+    CUtensorMap w13{}, w2{};
+    int map_ctas = 0;
+    if (maps != nullptr && experts != nullptr) {
+        if (!weight_map_templates(w13, w2)) return cudaErrorNotSupported;
+        map_ctas = (kE * kMapsPerExpert + 7) / 8;
+    }
     GroupOut g{};
     if (g_one != nullptr && n_tokens == 1) g = *g_one;
-    k_route_prep<<<n_tokens + piece_ctas, kRT, 0, c.stream>>>(idx, w, logits, bias, n_tokens, x, x_bf16,
-                                                              ximg, g, flags, flags ? n_flags : 0, experts);
+    k_route_prep<<<n_tokens + piece_ctas + map_ctas, kRT, 0, c.stream>>>(
+        idx, w, logits, bias, n_tokens, x, x_bf16, ximg, g, flags, flags ? n_flags : 0, experts, piece_ctas, maps,
+        w13, w2);
     return cudaGetLastError();
 }
 
