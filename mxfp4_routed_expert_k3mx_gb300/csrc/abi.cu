@@ -262,6 +262,12 @@ k3mx_status run_moe(const Ctx &c, float *y, const void *x, int x_dtype, int n_to
     if (!pieces_done)
         err = traced("mx_pieces", c.stream,
                      [&] { return launch_mx_ximg(c, x, x_bf16, n_tokens, ximg, sk, maps, experts, nullptr); });
+    if (err == cudaSuccess && n_tokens == 1) {
+        // one token: gate/up, down and the weighted sum in one launch
+        err = traced("decode_expert", c.stream,
+                     [&] { return launch_mx_fused1(c, d, ximg, himg, gu, stage, w, y, maps, sk); });
+        return from_cuda(err);
+    }
     if (err == cudaSuccess)
         err = traced("decode_gate_up", c.stream,
                      [&] { return launch_mx_gate_up(c, d, upairs, ximg, himg, gu, maps, sk); });
@@ -337,10 +343,8 @@ k3mx_status k3mx_expert_ffn(float *y, const float *x, const k3mx_expert *expert,
     cudaError_t err = traced("mx_pieces", c.stream,
                              [&] { return launch_mx_ximg(c, x, 0, 1, ximg, sk, maps, nullptr, expert); });
     if (err == cudaSuccess)
-        err = traced("decode_gate_up", c.stream,
-                     [&] { return launch_mx_gate_up(c, d, 1, ximg, himg, gu, maps, sk); });
-    if (err == cudaSuccess)
-        err = traced("decode_down", c.stream, [&] { return launch_mx_down(c, d, 1, himg, y, maps, sk); });
+        err = traced("decode_expert", c.stream,
+                     [&] { return launch_mx_fused1(c, d, ximg, himg, gu, nullptr, nullptr, y, maps, sk); });
     return from_cuda(err);
 }
 

@@ -94,6 +94,10 @@ struct MxArgs {
     float *partials;                // stream-K hand-over accumulators [grid][NMAT][NCOL][128], or null
     int *flags;                     // [grid] hand-over flags, zeroed by the step's first kernel
     int *status;
+    // fused single-token pass only
+    const float *w;                 // routing weights [16] of the token (null: one expert, no sum)
+    float *y;                       // [D]: the weighted sum (or the one expert's output)
+    int *sync;                      // flags [256], h blocks done per pair [16], y tiles done [28]
 };
 
 struct Hdr {
@@ -648,6 +652,498 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+
+// ----------------------------------------------- fused single-token pass --
+//
+// One token (a batch of one, or one expert): gate/up, down and the weighted
+// sum of the token's expert outputs in one persistent launch, so no pass
+// waits for another to drain and the weight stream does not pause between
+// them.  Stages are 32 KB: a gate/up stage is one 256-column chunk of W1
+// and of W3, a down stage two consecutive 256-column chunks of W2.  The
+// sequence of stages (every gate/up item, then every down item) is cut in
+// equal ranges over the CTAs (stream-K); an item split between two CTAs
+// is finished by the one holding its first stage, which adds the other's
+// fp32 partial in a fixed order.  A down item starts its MMAs once every
+// gate/up item of its pair has written its block of h (a per-pair count);
+// the last down item of a 128-row tile of y (a per-tile count) adds the
+// 16 pairs' rows with their routing weights in slot order.
+
+namespace f1 {
+constexpr int KCG = kD / kChunk;                 // 14 gate/up stages per item
+constexpr int KCD = kF / (2 * kChunk);           // 6 down stages per item
+constexpr int MTG = kF / 128, MTD = kD / 128;    // 24 gate/up, 28 down items per unit
+constexpr int GG = kD / 32, GD = kF / 32;        // scale bytes per weight row: 112, 96
+constexpr int PER_UNIT = MTG * KCG + MTD * KCD;  // 504 stages per unit
+constexpr int STAGE = 2 * kTileBytes + 4 * kAtomBytes;
+constexpr int XB = img_b(kD), XS = img_s(kD);    // the token's x pieces
+constexpr int HB = img_b(kF), HS = img_s(kF);    // a pair's h pieces
+constexpr int SOFF = 2 * HB;                     // scale parts after the two h B parts
+constexpr int BREG = 2 * HB + 2 * HS;            // x's image overlaps both h buffers
+constexpr int SRAW = 2 * 128 * GG;               // a gate/up tile's scale rows (the larger)
+constexpr int FIXED = 1024 + BREG + 2 * SRAW;
+constexpr int S = (kSmemLimit - 1024 - FIXED) / STAGE;
+constexpr int SMEM = 1024 + FIXED + S * STAGE;
+constexpr int SFA_COL = 2 * 2 * 8;               // accumulators [2][2][8] first
+constexpr int SFB_COL = SFA_COL + S * 16;
+constexpr int TMEM_COLS = 256;
+constexpr int PARTIAL = 2 * 8 * 128;             // floats per hand-over slot
+constexpr int SYNC_HDONE = 2 * kMaxGrid, SYNC_TILE = 2 * kMaxGrid + kK;   // after the two passes' flags
+static_assert(XB <= 2 * HB && XS <= 2 * HS, "x image must fit the h buffers");
+static_assert(S >= 3 && S <= 10, "pipeline depth");
+static_assert(SFB_COL + (kD / 128) * 4 <= TMEM_COLS, "TMEM budget");
+static_assert(SMEM <= kSmemLimit, "shared memory budget");
+}  // namespace f1
+
+__global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
+    using namespace f1;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Hdr *hd = reinterpret_cast<Hdr *>(smem);
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t st0 = sbase + 1024;
+    const uint32_t breg = st0 + S * STAGE;
+    const uint32_t sraw0 = breg + BREG;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t full0 = smem_addr(hd->full), empty0 = smem_addr(hd->empty);
+    const uint32_t accf0 = smem_addr(hd->accf), acce0 = smem_addr(hd->acce);
+    const uint32_t bfull0 = smem_addr(hd->bfull), bempty0 = smem_addr(hd->bempty);
+    const uint32_t sfull0 = smem_addr(hd->sfull), done = smem_addr(&hd->done);
+    if (tid == 0) {
+        for (int i = 0; i < S; i++) {
+            mbar_init(full0 + 8 * i, 1 + 32);
+            mbar_init(empty0 + 8 * i, 1);
+        }
+        for (int i = 0; i < 2; i++) {
+            mbar_init(accf0 + 8 * i, 1);
+            mbar_init(acce0 + 8 * i, 128);
+            mbar_init(bfull0 + 8 * i, 1);
+            mbar_init(bempty0 + 8 * i, 1);
+            mbar_init(sfull0 + 8 * i, 1);
+        }
+        mbar_init(done, 1);
+        hd->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) tmem_alloc(smem_addr(&hd->tmem), TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = hd->tmem;
+    volatile int *abort_flag = &hd->abort;
+    pdl_wait();
+    pdl_launch_dependents();
+
+    const int n_units = a.experts == nullptr ? 1 : __ldg(a.n_units);
+    // Every CTA takes an equal share of the gate/up stages, then of the down
+    // stages (so both passes run on every SM).  Shares are equal stage
+    // ranges when there is enough work (stream-K), else whole items.
+    const long long GU = (long long)n_units * MTG * KCG, GDn = (long long)n_units * MTD * KCD;
+    const long long G = gridDim.x, B = blockIdx.x;
+    const bool sk = a.partials != nullptr && GU >= G * (KCG + 1) && GDn >= G * (KCD + 1);
+    long long qg0, qg1, qd0, qd1;
+    if (sk) {
+        qg0 = GU * B / G;
+        qg1 = GU * (B + 1) / G;
+        qd0 = GU + GDn * B / G;
+        qd1 = GU + GDn * (B + 1) / G;
+    } else {
+        const long long ig = (long long)n_units * MTG, id = (long long)n_units * MTD;
+        qg0 = ig * B / G * KCG;
+        qg1 = ig * (B + 1) / G * KCG;
+        qd0 = GU + id * B / G * KCD;
+        qd1 = GU + id * (B + 1) / G * KCD;
+    }
+    const long long q0 = qg0;
+    auto fail = [&](int detail) {
+        report_status(a.status, kStatusWaitTimeout, detail);
+        *abort_flag = 1;
+    };
+    struct Part {
+        int ph;          // 0 gate/up, 1 down
+        long long item;  // within the phase
+        int lo, hi;      // stages of the item
+        int mt;          // 128-row tile
+        Unit u;
+    };
+    auto next_part = [&](long long &q, Part &p) -> bool {
+        for (;;) {
+            if (q >= qg1 && q < qd0) q = qd0;              // gate/up share done: the down share
+            if (q >= qd1) return false;
+            const bool up = q < GU;
+            const int kc = up ? KCG : KCD;
+            const long long r = q - (up ? 0 : GU), lim = up ? qg1 : qd1;
+            p.ph = up ? 0 : 1;
+            p.item = r / kc;
+            p.lo = (int)(r % kc);
+            p.hi = (int)min((long long)kc, p.lo + (lim - q));
+            q += p.hi - p.lo;
+            const int mts = up ? MTG : MTD;
+            p.mt = (int)(p.item % mts);
+            p.u = unit_at(a, (int)(p.item / mts));
+            if (p.u.ok) return true;
+            if (warp == kProdWarp && lane == 0 && p.lo == 0 && p.mt == 0)
+                report_status(a.status, kStatusBadPointer, p.u.e);
+        }
+    };
+    // B epoch of a part: the token's x for gate/up, the pair's h for down
+    auto b_key = [&](const Part &p) -> long long {
+        return p.ph == 0 ? -1 : (long long)pair_at(a, p.u.p0);
+    };
+    // B buffer of epoch n: epoch 0 is x (overlapping both h buffers)
+    auto b_off = [&](uint32_t n) { return (uint32_t)((n & 1) * HB); };
+    auto s_off = [&](uint32_t n) { return (uint32_t)(SOFF + (n & 1) * HS); };
+
+    if (warp == kProdWarp) {
+        // ---------------------------------------------------- TMA producer --
+        const uint64_t pol = l2_evict_first_policy();
+        const uint64_t pol_img = l2_evict_last_policy();
+        int cur_e = -1, cur_ph = -1;
+        const uint8_t *map0 = nullptr, *map1 = nullptr;
+        long long cur_key = -2, q = q0;
+        uint32_t su = 0, bl = 0;
+        bool x_first = false;            // epoch 0 held x (which overlaps both h buffers)
+        Part p;
+        while (!*abort_flag && next_part(q, p)) {
+            const Unit &u = p.u;
+            if (u.e != cur_e || p.ph != cur_ph) {
+                const uint8_t *em = a.maps + (size_t)u.e * kMapsPerExpert * kMapBytes;
+                map0 = em + (p.ph == 0 ? 0 : 2) * kMapBytes;
+                map1 = em + (p.ph == 0 ? 1 : 2) * kMapBytes;
+                acquire_map(map0);
+                if (p.ph == 0) acquire_map(map1);
+                cur_e = u.e;
+                cur_ph = p.ph;
+            }
+            auto issue_stage = [&](int c) -> bool {
+                const int s = su % S;
+                if (!mbar_wait(empty0 + 8 * s, ((su / S) & 1) ^ 1)) {
+                    if (lane == 0) fail(2);
+                    return false;
+                }
+                if (lane == 0) {
+                    const uint32_t dst = st0 + s * STAGE;
+                    mbar_arrive_expect_tx(full0 + 8 * s, 2 * kTileBytes);
+                    if (p.ph == 0) {
+                        tma_2d(dst, map0, c * 128, p.mt * 128, full0 + 8 * s, pol);
+                        tma_2d(dst + kTileBytes, map1, c * 128, p.mt * 128, full0 + 8 * s, pol);
+                    } else {
+                        tma_2d(dst, map0, (2 * c) * 128, p.mt * 128, full0 + 8 * s, pol);
+                        tma_2d(dst + kTileBytes, map0, (2 * c + 1) * 128, p.mt * 128, full0 + 8 * s, pol);
+                    }
+                }
+                __syncwarp();
+                su++;
+                return true;
+            };
+            // weight tiles first (they need nothing from the gate/up pass),
+            // then the part's B images
+            const int pre = min(S, p.hi - p.lo);
+            bool ok = true;
+            for (int c = p.lo; c < p.lo + pre && ok; c++) ok = issue_stage(c);
+            if (!ok) break;
+            const long long key = b_key(p);
+            if (key != cur_key) {
+                // epoch bl: x (bl = 0) or a pair's h; wait for the epoch that
+                // used its buffer (x overlaps both h buffers)
+                if (bl >= 2 || (bl == 1 && x_first)) {
+                    const uint32_t wb = bl == 1 ? 0 : (bl & 1), par = bl == 1 ? 0 : ((bl / 2 - 1) & 1);
+                    if (!mbar_wait(bempty0 + 8 * wb, par)) {
+                        if (lane == 0) fail(1);
+                        break;
+                    }
+                }
+                if (bl == 0) x_first = p.ph == 0;
+                const uint8_t *src;
+                uint32_t nb, ns;
+                if (p.ph == 0) {
+                    src = a.img_in + (size_t)(a.experts == nullptr ? 0 : pair_at(a, u.p0) / kK) * img_bytes(kD);
+                    nb = XB;
+                    ns = XS;
+                } else {
+                    // the pair's h: every gate/up item of the pair has written its block
+                    const int pair = (int)key;
+                    const int *cnt = a.sync + SYNC_HDONE + (a.experts == nullptr ? 0 : pair % kK);
+                    int f = 0;
+                    for (uint32_t i = 0; i < kWaitLimit && f < MTG; i++) {
+                        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(f) : "l"(cnt) : "memory");
+                        if (f < MTG) __nanosleep(128);
+                    }
+                    if (f < MTG) {
+                        if (lane == 0) fail(11);
+                        break;
+                    }
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    src = a.img_out + (size_t)pair * img_bytes(kF);
+                    nb = HB;
+                    ns = HS;
+                }
+                if (lane == 0) {
+                    const uint32_t bf = bfull0 + 8 * (bl & 1);
+                    mbar_arrive_expect_tx(bf, nb + ns);
+                    bulk_g2s(breg + b_off(bl), src, nb, bf, pol_img);
+                    bulk_g2s(breg + s_off(bl), src + nb, ns, bf, pol_img);
+                }
+                __syncwarp();
+                bl++;
+                cur_key = key;
+            }
+            for (int c = p.lo + pre; c < p.hi && ok; c++) ok = issue_stage(c);
+            if (!ok) break;
+        }
+    } else if (warp == kSfWarp) {
+        // -------------------------------------------------- scale loader --
+        // a part's tile scale rows in one bulk copy into one of two buffers
+        // (the next part's copy goes out when the current part starts);
+        // per stage, the 4 atoms: gate/up W1 and W3 of the chunk, down the
+        // two chunks of W2
+        const uint64_t pol = l2_evict_first_policy();
+        auto issue = [&](const Part &p, int buf) {
+            __syncwarp();
+            fence_async_smem();
+            if (lane == 0) {
+                const int G = p.ph == 0 ? GG : GD;
+                const size_t off = (size_t)p.mt * 128 * G;
+                const uint32_t dst = sraw0 + buf * SRAW;
+                mbar_arrive_expect_tx(sfull0 + 8 * buf, (p.ph == 0 ? 2 : 1) * 128 * G);
+                if (p.ph == 0) {
+                    bulk_g2s(dst, p.u.ex.s1 + off, 128 * G, sfull0 + 8 * buf, pol);
+                    bulk_g2s(dst + 128 * G, p.u.ex.s3 + off, 128 * G, sfull0 + 8 * buf, pol);
+                } else {
+                    bulk_g2s(dst, p.u.ex.s2 + off, 128 * G, sfull0 + 8 * buf, pol);
+                }
+            }
+        };
+        uint32_t su = 0, np = 0;
+        long long q = q0;
+        Part cur, nxt;
+        bool have = next_part(q, cur);
+        if (have) issue(cur, 0);
+        while (have && !*abort_flag) {
+            const int buf = np & 1;
+            long long qn = q;
+            const bool more = next_part(qn, nxt);
+            if (more) issue(nxt, (np + 1) & 1);
+            if (!mbar_wait(sfull0 + 8 * buf, (np / 2) & 1)) {
+                if (lane == 0) fail(3);
+                break;
+            }
+            const uint32_t sraw = sraw0 + buf * SRAW;
+            const int G = cur.ph == 0 ? GG : GD;
+            bool ok = true;
+            for (int c = cur.lo; c < cur.hi; c++, su++) {
+                const int s = su % S;
+                if (!mbar_wait(empty0 + 8 * s, ((su / S) & 1) ^ 1)) {
+                    if (lane == 0) fail(9);
+                    ok = false;
+                    break;
+                }
+                uint2 wv[2][4];
+#pragma unroll
+                for (int t = 0; t < 2; t++) {
+                    // sub-tile t: gate/up matrix t of chunk c; down chunk 2c + t
+                    const uint32_t base = cur.ph == 0 ? sraw + t * 128 * G + c * 8 : sraw + (2 * c + t) * 8;
+#pragma unroll
+                    for (int j = 0; j < 4; j++)
+                        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                                     : "=r"(wv[t][j].x), "=r"(wv[t][j].y)
+                                     : "r"(base + (lane + 32 * j) * G));
+                }
+                const uint32_t at0 = st0 + s * STAGE + 2 * kTileBytes;
+#pragma unroll
+                for (int t = 0; t < 2; t++) {
+                    sts128(at0 + (2 * t) * kAtomBytes + 16 * lane, drop_nan_scales(wv[t][0].x),
+                           drop_nan_scales(wv[t][1].x), drop_nan_scales(wv[t][2].x), drop_nan_scales(wv[t][3].x));
+                    sts128(at0 + (2 * t + 1) * kAtomBytes + 16 * lane, drop_nan_scales(wv[t][0].y),
+                           drop_nan_scales(wv[t][1].y), drop_nan_scales(wv[t][2].y), drop_nan_scales(wv[t][3].y));
+                }
+                fence_async_smem();
+                mbar_arrive(full0 + 8 * s);
+            }
+            if (!ok) break;
+            np++;
+            q = qn;
+            cur = nxt;
+            have = more;
+        }
+    } else if (warp == kMmaWarp) {
+        // ----------------------------------------------------- MMA issuer --
+        if (lane == 0) {
+            uint32_t su = 0, bu = 0, it = 0, bcur = 0;
+            long long cur_key = -2, q = q0;
+            bool run = true;
+            Part p;
+            while (run && !*abort_flag && next_part(q, p)) {
+                const long long key = b_key(p);
+                if (key != cur_key) {
+                    bcur = bu;
+                    if (!mbar_wait(bfull0 + 8 * (bu & 1), (bu / 2) & 1)) {
+                        fail(4);
+                        break;
+                    }
+                    bu++;
+                    tc_fence_after();
+                    // scale atoms of the epoch's B (one token: the four 8-line
+                    // groups all read its lines)
+                    const int atoms = p.ph == 0 ? kD / 128 : kF / 128;
+                    for (int at = 0; at < atoms; at++)
+                        tmem_cp_atom(tmem + SFB_COL + 4 * at, desc_atom(breg + s_off(bcur) + at * 128, 0));
+                    cur_key = key;
+                }
+                const uint32_t bimg = breg + b_off(bcur);
+                const int b = it & 1;
+                if (!mbar_wait(acce0 + 8 * b, ((it >> 1) & 1) ^ 1)) {
+                    fail(5);
+                    break;
+                }
+                tc_fence_after();
+                for (int c = p.lo; c < p.hi; c++, su++) {
+                    const int s = su % S;
+                    if (!mbar_wait(full0 + 8 * s, (su / S) & 1)) {
+                        fail(6);
+                        run = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t stg = st0 + s * STAGE;
+                    const uint32_t sfa = tmem + SFA_COL + s * 16;
+#pragma unroll
+                    for (int at = 0; at < 4; at++)
+                        tmem_cp_atom(sfa + at * 4, desc_atom(stg + 2 * kTileBytes + at * kAtomBytes, 128));
+#pragma unroll
+                    for (int t = 0; t < 2; t++) {
+                        // gate/up: matrix t into accumulator t; down: chunk 2c + t into accumulator 0
+                        const int bc = p.ph == 0 ? c : 2 * c + t;          // B's 256-column chunk
+                        const uint32_t d = tmem + (b * 2 + (p.ph == 0 ? t : 0)) * 8;
+#pragma unroll
+                        for (int ks = 0; ks < 4; ks++) {
+                            const int id = 2 * (ks & 1);
+                            const bool fresh = c == p.lo && ks == 0 && (p.ph == 0 || t == 0);
+                            mma_mxf4(d, desc_sw128(stg + t * kTileBytes + 32 * ks, 1024),
+                                     desc_sw128(bimg + bc * 1024 + 32 * ks, 1024), idesc_mxf4(8, id),
+                                     sfa + t * 8 + (ks >> 1) * 4, tmem + SFB_COL + (bc * 2 + (ks >> 1)) * 4,
+                                     fresh ? 0u : 1u);
+                        }
+                    }
+                    umma_commit(empty0 + 8 * s);
+                }
+                if (!run) break;
+                umma_commit(accf0 + 8 * b);
+                it++;
+                long long qn = q;
+                Part nx;
+                if (!next_part(qn, nx) || b_key(nx) != key) umma_commit(bempty0 + 8 * (bcur & 1));
+            }
+            umma_commit(done);
+        }
+    } else {
+        // ------------------------------------------------------- epilogue --
+        const int q4 = warp & 3;
+        const int row_in_tile = 32 * q4 + lane;
+        __shared__ int last_tile;
+        uint32_t it = 0;
+        long long q = q0;
+        Part p;
+        while (!*abort_flag && next_part(q, p)) {
+            const Unit &u = p.u;
+            const int kc = p.ph == 0 ? KCG : KCD;
+            const int b = it & 1;
+            if (!mbar_wait(accf0 + 8 * b, (it >> 1) & 1)) {
+                if (lane == 0) fail(7);
+                break;
+            }
+            tc_fence_after();
+            uint32_t v[2][8];
+#pragma unroll
+            for (int m = 0; m < 2; m++) tmem_ld<8>(tmem + ((uint32_t)(32 * q4) << 16) + (b * 2 + m) * 8, v[m]);
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(acce0 + 8 * b);
+            it++;
+            const int nm = p.ph == 0 ? 2 : 1;
+            if (sk && p.lo > 0) {
+                // the tail of an item begun by the previous CTA: hand over
+                float *dst = a.partials + ((size_t)p.ph * kMaxGrid + blockIdx.x) * PARTIAL;
+#pragma unroll
+                for (int m = 0; m < 2; m++)
+                    if (m < nm)
+#pragma unroll
+                        for (int j = 0; j < 8; j++) dst[(m * 8 + j) * 128 + row_in_tile] = __uint_as_float(v[m][j]);
+                __threadfence();
+                named_sync(1, 128);
+                if (q4 == 0 && lane == 0)
+                    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(a.sync + p.ph * kMaxGrid + blockIdx.x),
+                                 "r"(1)
+                                 : "memory");
+                continue;
+            }
+            if (sk && p.hi < kc) {
+                // the head of an item the next CTA finishes: add its partial
+                const int *flag = a.sync + p.ph * kMaxGrid + blockIdx.x + 1;
+                int f = 0;
+                for (uint32_t i = 0; i < kWaitLimit && f == 0; i++) {
+                    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(f) : "l"(flag) : "memory");
+                    if (f == 0) __nanosleep(64);
+                }
+                if (f == 0) fail(10);
+                const float *src = a.partials + ((size_t)p.ph * kMaxGrid + blockIdx.x + 1) * PARTIAL;
+#pragma unroll
+                for (int m = 0; m < 2; m++)
+                    if (m < nm)
+#pragma unroll
+                        for (int j = 0; j < 8; j++)
+                            v[m][j] = __float_as_uint(__uint_as_float(v[m][j]) + __ldcg(src + (m * 8 + j) * 128 + row_in_tile));
+            }
+            float acc[2] = {0.f, 0.f};
+#pragma unroll
+            for (int m = 0; m < 2; m++)
+#pragma unroll
+                for (int pc = 0; pc < kPieces; pc++) acc[m] += __uint_as_float(v[m][pc]);
+            const int pair = pair_at(a, u.p0);
+            const int row = p.mt * 128 + row_in_tile;
+            if (p.ph == 0) {
+                float *gu = a.gu + (size_t)pair * 2 * kF;
+                gu[row] = acc[0];
+                gu[kF + row] = acc[1];
+                uint8_t *ib = a.img_out + (size_t)pair * img_bytes(kF);
+                store_pieces(situ_glu(acc[0], acc[1]), ib, ib + img_b(kF), p.mt * 4 + q4);
+                // this item's block of h is written: count it for the pair
+                __threadfence();
+                named_sync(1, 128);
+                if (q4 == 0 && lane == 0)
+                    atomicAdd(a.sync + SYNC_HDONE + (a.experts == nullptr ? 0 : pair % kK), 1);
+            } else if (a.w == nullptr) {
+                a.y[row] = acc[0];                      // one expert: its output is y
+            } else {
+                a.out[(size_t)pair * kD + row] = acc[0];
+                // the last of the token's 16 pairs to finish this tile forms y
+                __threadfence();
+                named_sync(1, 128);
+                if (q4 == 0 && lane == 0) {
+                    const int done_pairs = atomicAdd(a.sync + SYNC_TILE + p.mt, 1) + 1;
+                    __threadfence();
+                    last_tile = done_pairs == kK;
+                }
+                named_sync(1, 128);
+                if (last_tile) {
+                    const int t = pair / kK;
+                    float yv = 0.f;
+#pragma unroll 4
+                    for (int k = 0; k < kK; k++)
+                        yv = fmaf(__ldg(a.w + (size_t)t * kK + k), __ldcg(a.out + ((size_t)t * kK + k) * kD + row), yv);
+                    a.y[(size_t)t * kD + row] = yv;
+                }
+            }
+        }
+    }
+
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        if (!mbar_wait(done, 0) && lane == 0) report_status(a.status, kStatusWaitTimeout, 8);
+        tc_fence_after();
+        tmem_dealloc(tmem, f1::TMEM_COLS);
+    }
+}
+
 // ------------------------------------------------------------- launchers --
 
 template <int PH, int NTOK>
@@ -728,19 +1224,42 @@ bool weight_map_templates(CUtensorMap &w13, CUtensorMap &w2) {
     return true;
 }
 
+// stream-K region (one token per unit): flags [2][kMaxGrid] ints, then the
+// gate/up and the down hand-over partials
+namespace {
+constexpr size_t kSkFlagBytes = (size_t)4 * kMaxGrid * sizeof(int);
+constexpr size_t kSkPart0 = (size_t)MxShape<0, 1>::NMAT * MxShape<0, 1>::NCOL * 128 * sizeof(float);
+constexpr size_t kSkPart1 = (size_t)MxShape<1, 1>::NMAT * MxShape<1, 1>::NCOL * 128 * sizeof(float);
+}  // namespace
+cudaError_t launch_mx_fused1(const Ctx &c, const DecodeExperts &d, const uint8_t *ximg, uint8_t *himg, float *gu,
+                             float *stage, const float *w, float *y, const uint8_t *maps, uint8_t *sk) {
+    static bool configured = false;
+    if (!configured) {
+        const cudaError_t e = cudaFuncSetAttribute(k_mx1, cudaFuncAttributeMaxDynamicSharedMemorySize, f1::SMEM);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    MxArgs a = mx_args(d);
+    a.img_in = ximg;
+    a.img_out = himg;
+    a.gu = gu;
+    a.out = stage;
+    a.maps = maps;
+    a.w = w;
+    a.y = y;
+    a.status = c.status;
+    a.sync = reinterpret_cast<int *>(sk);
+    a.partials = reinterpret_cast<float *>(sk + kSkFlagBytes);
+    const int grid = c.num_sms < kMaxGrid ? c.num_sms : kMaxGrid;
+    return launch_pdl(k_mx1, dim3(grid), dim3(kThreads), f1::SMEM, c.stream, a);
+}
+
 size_t mx_ximg_bytes(int n_tokens) { return (size_t)n_tokens * img_bytes(kD); }
 size_t mx_himg_bytes(int n_pairs) { return (size_t)n_pairs * img_bytes(kF); }
 size_t mx_maps_bytes(int n_experts) { return expert_maps_bytes(n_experts); }
 
-// stream-K region (one token per unit): flags [2][kMaxGrid] ints, then the
-// gate/up and the down hand-over partials
-namespace {
-constexpr size_t kSkFlagBytes = (size_t)2 * kMaxGrid * sizeof(int);
-constexpr size_t kSkPart0 = (size_t)MxShape<0, 1>::NMAT * MxShape<0, 1>::NCOL * 128 * sizeof(float);
-constexpr size_t kSkPart1 = (size_t)MxShape<1, 1>::NMAT * MxShape<1, 1>::NCOL * 128 * sizeof(float);
-}  // namespace
-size_t mx_streamk_bytes() { return kSkFlagBytes + (size_t)kMaxGrid * (kSkPart0 + kSkPart1); }
-int mx_streamk_flag_count() { return 2 * kMaxGrid; }
+size_t mx_streamk_bytes() { return kSkFlagBytes + (size_t)2 * kMaxGrid * kSkPart0; }
+int mx_streamk_flag_count() { return (int)(kSkFlagBytes / sizeof(int)); }
 
 cudaError_t launch_mx_ximg(const Ctx &c, const void *x, int x_bf16, int n_tokens, uint8_t *ximg, uint8_t *sk,
                            uint8_t *maps, const k3mx_expert *table, const k3mx_expert *one) {
@@ -752,7 +1271,7 @@ cudaError_t launch_mx_ximg(const Ctx &c, const void *x, int x_bf16, int n_tokens
     const int map_ctas = (n_map_experts * kMapsPerExpert + 7) / 8;
     const k3mx_expert single = one != nullptr ? *one : k3mx_expert{};
     k_mx_ximg<<<(unsigned)(piece_ctas + map_ctas), 256, 0, c.stream>>>(
-        x, x_bf16, n_tokens, ximg, reinterpret_cast<int *>(sk), sk != nullptr ? 2 * kMaxGrid : 0, piece_ctas,
+        x, x_bf16, n_tokens, ximg, reinterpret_cast<int *>(sk), sk != nullptr ? mx_streamk_flag_count() : 0, piece_ctas,
         maps, n_map_experts, one != nullptr ? nullptr : table, single, w13, w2);
     return cudaGetLastError();
 }

@@ -49,7 +49,9 @@ __device__ __forceinline__ uint32_t spread_nibbles(uint32_t x) {
 __device__ __forceinline__ void store_pieces(float r, uint8_t *ib, uint8_t *is, int kb) {
     const int lane = threadIdx.x & 31;
     uint32_t m0 = 0, m1 = 0, m2 = 0, m3 = 0, msb = 0;
-#pragma unroll
+    // rolled: the body runs in epilogues while the weight stream keeps
+    // memory busy, and a short body keeps its first instruction fetches few
+#pragma unroll 1
     for (int p = 0; p < kPieces; p++) {
         float mx = fabsf(r);
 #pragma unroll
