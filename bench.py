@@ -47,7 +47,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 
 # kernels per traced launch group
 KERNELS_PER_GROUP = {"route": 1, "group_small": 1, "group": 3, "mx_pieces": 1,
-                     "decode_gate_up": 1, "decode_down": 1, "combine": 1,
+                     "decode_expert": 1, "decode_gate_up": 1, "decode_down": 1, "combine": 1,
                      "prefill_prep": 2, "prefill_gate_up": 1, "prefill_down": 1}
 PARAMS_PER_EXPERT = 33030144
 X_IMAGE_BYTES = 8 * 3584 // 2 + 3584          # 8 MXFP4 pieces of x and their scale lines
@@ -360,15 +360,29 @@ def run_ours(args):
     total_ms_max, bytes_all = reduce_over_ranks(dist, total_ms, bytes_total, dev)
     value = bytes_all / (total_ms_max / 1e3) / 1e9
 
-    # dominant kernel: the fused gate/up + SiTU pass (two thirds of the bytes)
+    # dominant kernel: one token per step runs gate/up, down and the weighted
+    # sum in one persistent launch (decode_expert); batches run the fused
+    # gate/up + SiTU pass (decode_gate_up, two thirds of the bytes)
     tr = res["trace"]
-    n_launch, ms_gu = tr.get("decode_gate_up", (0, 0.0))
-    gu_bytes = sum(d * GATE_UP_BYTES for d in res["distinct"]) / max(1, len(res["distinct"]))
-    # x pieces read; per pair g, u (fp32) and the pieces of h written
-    gu_bytes += primary.T * X_IMAGE_BYTES + primary.T * K * (H_IMAGE_BYTES + 2 * F * 4)
-    achieved = gu_bytes / (ms_gu / max(1, n_launch) / 1e3) / 1e9 if n_launch else None
-    src_hash = kernel_source_hash(["mx.cu", "common.cuh"])
-    traffic = profiled_traffic("decode_gate_up", primary.name, src_hash)
+    avg_distinct = sum(res["distinct"]) / max(1, len(res["distinct"]))
+    pairs = primary.T * K
+    if "decode_expert" in tr:
+        dom = "decode_expert"
+        # weights of every selected expert, the x pieces, per pair g and u
+        # written, h pieces written and read, the pair's output row written
+        # and read, y written
+        dom_bytes = (avg_distinct * EXPERT_BYTES + primary.T * X_IMAGE_BYTES
+                     + pairs * (2 * F * 4 + 2 * H_IMAGE_BYTES + 2 * D * 4) + primary.T * D * 4)
+    else:
+        dom = "decode_gate_up"
+        # w1, w3 of every selected expert, the x pieces, per pair g and u
+        # (fp32) and the h pieces written
+        dom_bytes = (avg_distinct * GATE_UP_BYTES + primary.T * X_IMAGE_BYTES
+                     + pairs * (H_IMAGE_BYTES + 2 * F * 4))
+    n_launch, ms_dom = tr.get(dom, (0, 0.0))
+    achieved = dom_bytes / (ms_dom / max(1, n_launch) / 1e3) / 1e9 if n_launch else None
+    src_hash = kernel_source_hash(["mx.cu", "common.cuh", "pieces.cuh"])
+    traffic = profiled_traffic(dom, primary.name, src_hash)
     launches = sum(KERNELS_PER_GROUP.get(k, 1) * v[0] for k, v in tr.items())
 
     line = {
@@ -384,10 +398,10 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}"},
         "hbm_frac": round(value / world / hbm_peak, 4),
         "hbm_frac_nominal_8tbs": round(value / world / 8000.0, 4),
-        "roofline": {"kernel": "decode_gate_up", "bound": "hbm",
+        "roofline": {"kernel": dom, "bound": "hbm",
                      "achieved": round(achieved, 1) if achieved else None, "peak": hbm_peak,
                      "unit": "GB/s", "frac": round(achieved / hbm_peak, 4) if achieved else None,
-                     "traffic": traffic, "algorithmic_bytes_per_launch": int(gu_bytes),
+                     "traffic": traffic, "algorithmic_bytes_per_launch": int(dom_bytes),
                      "peak_source": f"{peak_src} HBM copy"},
         "kernels": {k: {"launches": v[0], "avg_us": round(1e3 * v[1] / max(1, v[0]), 2)} for k, v in tr.items()},
         "gpu_launches": launches,

@@ -345,18 +345,23 @@ __device__ void scatter_warp(const int32_t *idx, int p_begin, int p_end, int *ru
 //
 // For a few tokens the warp-per-token router leaves the GPU idle, so each
 // token gets a 256-thread CTA: thread t holds experts t, t+256, t+512,
-// t+768.  (1) fp32 estimates of the 896 keys; (2) each warp sorts its 128
-// estimates (bitonic network in registers and shuffles), warp 0 sorts the
-// eight warps' 16 largest: a16 is the 16th; (3) candidates within
-// 2^-18 * max(1,|a16|) of a16 (the same bound as route_warp); (4) exact
-// double scores for the candidates, each candidate's rank among them by
-// (key, lower index), and the slot-order sum of the 16 winners' scores.
+// t+768.  (1) fp32 estimates of the 896 keys; (2) a two-pass radix select
+// (8 bits per pass, shared-memory histograms) finds the 16-bit prefix of
+// the 16th largest estimate a16, whose lowest value stands in for a16 in
+// the candidate bound; (3) candidates within 2^-18 * max(1,|v|) below that
+// value v (the bound of route_warp, applied to a value no larger than a16);
+// (4) exact double scores for the candidates, each candidate's rank among
+// them by (key, lower index); (5) warp 0 forms the slot-order sum of the 16
+// winners' scores and the weights.  Every phase is a few dozen
+// instructions: a single token's step waits for this CTA alone.
 
 constexpr int kRT = 256;                 // threads per routing CTA
 constexpr int kRS = 4;                   // expert slots per thread
 
 struct RouteSmem {
-    uint32_t top[8][kK];
+    int hist[256];
+    uint32_t prefix;                     // selected bin of the pass
+    int above;                           // estimates in higher bins
     uint32_t tau;
     int n;
     int cand[64];
@@ -364,69 +369,79 @@ struct RouteSmem {
     float cs[64];
     int sel_e[kK];
     float sel_s[kK];
-    int sorted_e[kK];
-    double sum;
 };
 
-// 128 values of a warp (lane l holds positions 4l .. 4l+3) sorted in
-// descending order by a bitonic network
-__device__ __forceinline__ void warp_sort128_desc(uint32_t (&v)[kRS]) {
+// Warp 0, after a histogram pass: the bin (scanning from the top) that
+// holds the `need`-th largest value, and how many values lie in the bins
+// above it; clears the histogram for the next pass.
+__device__ __forceinline__ void radix_pick(RouteSmem &sm, int need) {
     const int lane = threadIdx.x & 31;
+    int c[8], tot = 0;
 #pragma unroll
-    for (int k = 2; k <= 128; k <<= 1) {
+    for (int i = 0; i < 8; i++) {
+        c[i] = sm.hist[255 - 8 * lane - i];      // lane 0 holds the top bins
+        sm.hist[255 - 8 * lane - i] = 0;
+        tot += c[i];
+    }
+    int incl = tot;
 #pragma unroll
-        for (int j = k >> 1; j > 0; j >>= 1) {
-            if (j >= kRS) {
-                const int lj = j / kRS;
-#pragma unroll
-                for (int r = 0; r < kRS; r++) {
-                    const int i = kRS * lane + r;
-                    const uint32_t o = __shfl_xor_sync(0xffffffffu, v[r], lj);
-                    const bool desc = (i & k) == 0, lower = (i & j) == 0;
-                    v[r] = (desc == lower) ? max(v[r], o) : min(v[r], o);
-                }
-            } else {
-#pragma unroll
-                for (int r = 0; r < kRS; r++) {
-                    const int q = r ^ j;
-                    if (q > r) {
-                        const int i = kRS * lane + r;
-                        const bool desc = (i & k) == 0;
-                        const uint32_t a = v[r], b = v[q];
-                        v[r] = desc ? max(a, b) : min(a, b);
-                        v[q] = desc ? min(a, b) : max(a, b);
-                    }
-                }
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    int before = incl - tot;                       // values in the bins of lower lanes
+    if (before < need && incl >= need) {
+#pragma unroll 1
+        for (int i = 0; i < 8; i++) {
+            if (before + c[i] >= need) {
+                sm.prefix = (uint32_t)(255 - 8 * lane - i);
+                sm.above = before;
+                break;
             }
+            before += c[i];
         }
     }
 }
 
 __device__ void route_cta(const float *__restrict__ lt, const float *__restrict__ bias,
-                          int32_t *__restrict__ idx_t, float *__restrict__ w_t,
-                          const k3mx_expert *__restrict__ experts, RouteSmem &sm) {
+                          int32_t *__restrict__ idx_t, float *__restrict__ w_t, RouteSmem &sm) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    uint32_t ok[kRS], v[kRS];
+    float lv[kRS], bv[kRS];
 #pragma unroll
     for (int j = 0; j < kRS; j++) {
         const int e = tid + kRT * j;
-        ok[j] = e < kE ? order_key(canon_key(approx_score(__ldg(lt + e)) + __ldg(bias + e))) : 0u;
-        v[j] = ok[j];
+        lv[j] = e < kE ? __ldg(lt + e) : 0.f;
+        bv[j] = e < kE ? __ldg(bias + e) : 0.f;
     }
-    warp_sort128_desc(v);
-    if (lane < kK / kRS)
+    sm.hist[tid] = 0;
+    if (tid == 0) sm.n = 0;
+    uint32_t ok[kRS];
 #pragma unroll
-        for (int r = 0; r < kRS; r++) sm.top[warp][kRS * lane + r] = v[r];
+    for (int j = 0; j < kRS; j++)
+        ok[j] = tid + kRT * j < kE ? order_key(canon_key(approx_score(lv[j]) + bv[j])) : 0u;
+    __syncthreads();
+    // pass 1: the top 8 bits of the order keys
+#pragma unroll
+    for (int j = 0; j < kRS; j++)
+        if (tid + kRT * j < kE) atomicAdd(&sm.hist[ok[j] >> 24], 1);
+    __syncthreads();
+    if (warp == 0) radix_pick(sm, kK);
+    __syncthreads();
+    const uint32_t p1 = sm.prefix;
+    const int need = kK - sm.above;
+    // pass 2: the next 8 bits of the keys in that bin
+#pragma unroll
+    for (int j = 0; j < kRS; j++)
+        if (tid + kRT * j < kE && (ok[j] >> 24) == p1) atomicAdd(&sm.hist[(ok[j] >> 16) & 255u], 1);
     __syncthreads();
     if (warp == 0) {
-#pragma unroll
-        for (int r = 0; r < kRS; r++) v[r] = (&sm.top[0][0])[kRS * lane + r];
-        warp_sort128_desc(v);
-        if (lane == (kK - 1) / kRS) {
-            const float a16 = key_of_order(v[(kK - 1) % kRS]);
-            // a non-finite a16 (infinite biases) keeps every expert: exact path
-            sm.tau = isfinite(a16) ? order_key(a16 - 0x1p-18f * fmaxf(1.0f, fabsf(a16))) : 0u;
-            sm.n = 0;
+        radix_pick(sm, need);
+        __syncwarp();
+        if (lane == 0) {
+            // the lowest value with a16's 16-bit prefix; a non-finite one
+            // (infinite keys) keeps every expert: exact path
+            const float lo = key_of_order((p1 << 24) | (sm.prefix << 16));
+            sm.tau = isfinite(lo) ? order_key(lo - 0x1p-18f * fmaxf(1.0f, fabsf(lo))) : 0u;
         }
     }
     __syncthreads();
@@ -459,6 +474,7 @@ __device__ void route_cta(const float *__restrict__ lt, const float *__restrict_
     if (tid < n) {
         const uint32_t h = sm.khi[tid], l = sm.klo[tid];
         int r = 0;
+#pragma unroll 1
         for (int u = 0; u < n; u++) r += (sm.khi[u] > h) || (sm.khi[u] == h && sm.klo[u] > l);
         if (r < kK) {
             sm.sel_e[r] = (int)(0xFFFFFFFFu - l);
@@ -466,67 +482,53 @@ __device__ void route_cta(const float *__restrict__ lt, const float *__restrict_
         }
     }
     __syncthreads();
-    if (tid == 0) {
+    if (warp == 0) {
         // The slot-order double sum.  With every score in [2^-24, 1] each
         // term is a multiple of 2^-47 and the sum stays below 2^5, so every
         // partial sum is exact in double and the sum equals the integer
-        // sum of the scores in units of 2^-47 (no double adds needed).
-        bool fixed = true;
-        long long acc = 0;
-        for (int r = 0; r < kK; r++) {
-            const float sr = sm.sel_s[r];
-            fixed = fixed && sr >= 0x1p-24f && sr <= 1.0f;
-            acc += (long long)__float2ll_rz(sr * 0x1p47f);
-        }
+        // sum of the scores in units of 2^-47, whatever the order of adds.
+        const float sr = lane < kK ? sm.sel_s[lane] : 0.f;
+        const bool fixed = __all_sync(0xffffffffu, lane >= kK || (sr >= 0x1p-24f && sr <= 1.0f));
+        long long acc = lane < kK ? (long long)__float2ll_rz(sr * 0x1p47f) : 0ll;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
         double sum = (double)acc * 0x1p-47;
         if (!fixed) {
             sum = 0.0;
             for (int r = 0; r < kK; r++) sum += (double)sm.sel_s[r];
         }
-        sm.sum = sum;
-    }
-    __syncthreads();
-    if (tid < kK) {
-        idx_t[tid] = sm.sel_e[tid];
-        w_t[tid] = (float)((double)sm.sel_s[tid] / sm.sum) * kRoutedScale;
+        if (lane < kK) {
+            idx_t[lane] = sm.sel_e[lane];
+            w_t[lane] = (float)((double)sr / sum) * kRoutedScale;
+        }
     }
 }
 
 // Grouping of a single token's 16 pairs (pair p = slot p) inside its
-// routing CTA: the 16 experts are distinct, so each has one pair and one
-// work unit; units and perm follow increasing expert index.
-__device__ void group_one_token(const int32_t *__restrict__ idx_t, const GroupOut &g, RouteSmem &sm) {
-    const int tid = threadIdx.x;
-    if (tid < kK) {
-        const int e = idx_t[tid];
-        int rank = 0;
-        for (int u = 0; u < kK; u++) rank += idx_t[u] < e;
-        sm.sorted_e[rank] = e;
-        g.perm[rank] = tid;
-        g.act[rank] = e;
+// routing CTA, warp 0: the 16 experts are distinct, so each has one pair
+// and one work unit; units and perm follow increasing expert index.  The
+// decode passes read only the units and perm; counts, offsets and the
+// active list are not written.
+__device__ void group_one_token(const GroupOut &g, const RouteSmem &sm) {
+    const int lane = threadIdx.x & 31;
+    const int e = lane < kK ? sm.sel_e[lane] : 0x7FFFFFFF;
+    int rank = 0;
+#pragma unroll
+    for (int u = 0; u < kK; u++) rank += __shfl_sync(0xffffffffu, e, u) < e;
+    if (lane < kK) {
+        g.perm[rank] = lane;
         g.units[3 * rank + 0] = e;
         g.units[3 * rank + 1] = rank;
         g.units[3 * rank + 2] = rank + 1;
     }
-    __syncthreads();
-    for (int e = tid; e <= kE; e += kRT) {
-        int below = 0, hit = 0;
-        for (int u = 0; u < kK; u++) {
-            below += sm.sorted_e[u] < e;
-            hit |= sm.sorted_e[u] == e;
-        }
-        g.offsets[e] = below;
-        if (e < kE) g.counts[e] = hit;
-    }
-    if (tid == 0) {
-        *g.n_active = kK;
-        *g.n_units = kK;
-    }
+    if (lane == 0) *g.n_units = kK;
 }
 
 // CTAs 0..n_tokens-1 route one token each (and, for a single token with a
 // work-unit list, group it); the CTAs after them (when x is given) write
-// the tokens' x piece images, one warp per 32-column block.
+// the tokens' x piece images, one warp per 32-column block; the rest build
+// the weight tensor maps of the expert table.  The last CTA zeroes the
+// stream-K flags and pulls the expert table into L2.
 __global__ void __launch_bounds__(kRT)
 k_route_prep(int32_t *idx, float *w, const float *logits, const float *bias, int n_tokens,
              const void *x, int x_bf16, uint8_t *ximg, GroupOut g, int *flags, int n_flags,
@@ -535,25 +537,26 @@ k_route_prep(int32_t *idx, float *w, const float *logits, const float *bias, int
     __shared__ RouteSmem sm;
     // the expert passes may launch now: their prologues overlap this kernel
     pdl_launch_dependents();
-    if (blockIdx.x == 0) {
+    if ((int)blockIdx.x < n_tokens) {
+        const int t = blockIdx.x;
+        route_cta(logits + (size_t)t * kE, bias, idx + (size_t)t * kK, w + (size_t)t * kK, sm);
+        if (n_tokens == 1 && g.units != nullptr) {
+            __syncthreads();
+            if (threadIdx.x < 32) group_one_token(g, sm);
+        }
+        return;
+    }
+    if (blockIdx.x == gridDim.x - 1) {
         for (int i = threadIdx.x; i < n_flags; i += blockDim.x) flags[i] = 0;
         // the expert pointer table into L2 for the passes' first lookups
         if (experts != nullptr)
             for (int i = threadIdx.x; i < (int)(kE * sizeof(k3mx_expert) / 128); i += blockDim.x)
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const uint8_t *>(experts) + 128 * i));
     }
-    if ((int)blockIdx.x < n_tokens) {
-        const int t = blockIdx.x;
-        route_cta(logits + (size_t)t * kE, bias, idx + (size_t)t * kK, w + (size_t)t * kK, experts, sm);
-        if (n_tokens == 1 && g.units != nullptr) {
-            __syncthreads();
-            group_one_token(idx, g, sm);
-        }
-    } else if ((int)blockIdx.x < n_tokens + piece_ctas) {
+    if ((int)blockIdx.x < n_tokens + piece_ctas)
         ximg_block(x, x_bf16, n_tokens, ximg, (blockIdx.x - n_tokens) * (kRT / 32) + (threadIdx.x >> 5));
-    } else {
+    else
         build_maps_cta(maps, kE, experts, k3mx_expert{}, w13, w2, blockIdx.x - n_tokens - piece_ctas);
-    }
 }
 
 // grouping of n_tokens * 16 <= 1024 pairs in one CTA, launched as a

@@ -97,3 +97,26 @@ def test_decode_experts_shared_by_many_tokens(arena, cuda_dev):
     assert sorted(set(ir.ravel().tolist())) == list(range(100, 116))
     yr, bound = moe_oracle(x, ir, wr, list(range(T)))
     assert_within(y, yr, 1e-5 * bound, "shared experts")
+
+
+def test_decode_routing_ties_and_crowded_keys(arena, cuda_dev):
+    """The layer's one-CTA-per-token router on hard key sets, bit-exact
+    against the oracle: every key equal (more than 64 candidates, the exact
+    fallback), 40 equal keys around the 16th place, keys one ulp apart, and
+    a bias that lifts a block of experts to the top."""
+    _, table = arena
+    T = 4
+    x = synth.token_inputs(T, seed=31)
+    logits, bias = synth.router_inputs(T, seed=31)
+    logits[0, :] = 0.25                                   # all 896 keys tie
+    logits[1, 300:340] = 3.0                              # 40-way tie for the top 16
+    base = np.float32(1.5)
+    logits[2, 500:540] = np.nextafter(base, np.float32(10), dtype=np.float32) * 0 + base
+    logits[2, 500:540:2] = np.nextafter(base, np.float32(10), dtype=np.float32)
+    bias = bias.copy()
+    bias[700:716] = 2.0                                   # token 3's winners come from the bias
+    y, idx, w = run_moe(cuda_dev, table, torch.from_numpy(x), logits, bias, k3mx.K3MX_PATH_DECODE)
+    ir, wr = oracle.route(logits, bias)
+    assert np.array_equal(idx, ir) and np.array_equal(w, wr)
+    yr, bound = moe_oracle(x, ir, wr, list(range(T)))
+    assert_within(y, yr, 1e-5 * bound, "routing ties")
