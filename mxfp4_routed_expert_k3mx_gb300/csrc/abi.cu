@@ -258,7 +258,6 @@ k3mx_status run_moe(const Ctx &c, float *y, const void *x, int x_dtype, int n_to
     uint8_t *himg = at<uint8_t>(ws, L.himg), *maps = at<uint8_t>(ws, L.maps);
     float *gu = at<float>(ws, L.h);
     float *stage = at<float>(ws, L.stage);
-    const int upairs = n_tokens == 1 ? 1 : kUnitPairs;
     if (!pieces_done)
         err = traced("mx_pieces", c.stream,
                      [&] { return launch_mx_ximg(c, x, x_bf16, n_tokens, ximg, sk, maps, experts, nullptr); });
@@ -270,10 +269,10 @@ k3mx_status run_moe(const Ctx &c, float *y, const void *x, int x_dtype, int n_to
     }
     if (err == cudaSuccess)
         err = traced("decode_gate_up", c.stream,
-                     [&] { return launch_mx_gate_up(c, d, upairs, ximg, himg, gu, maps, sk); });
+                     [&] { return launch_mx_gate_up(c, d, ximg, himg, gu, maps); });
     if (err == cudaSuccess)
         err = traced("decode_down", c.stream,
-                     [&] { return launch_mx_down(c, d, upairs, himg, stage, maps, sk); });
+                     [&] { return launch_mx_down(c, d, himg, stage, maps); });
     if (err == cudaSuccess)
         err = traced("combine", c.stream, [&] { return launch_combine(c, y, stage, w, n_tokens); });
     return from_cuda(err);

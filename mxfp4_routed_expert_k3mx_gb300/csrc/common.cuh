@@ -326,16 +326,16 @@ int mx_streamk_flag_count();
 cudaError_t launch_mx_ximg(const Ctx &c, const void *x, int x_bf16, int n_tokens, uint8_t *ximg, uint8_t *sk,
                            uint8_t *maps, const k3mx_expert *table, const k3mx_expert *one);
 // gate/up: g, u -> gu [pair][2][F]; h = SiTU(g, u) -> piece images himg
-cudaError_t launch_mx_gate_up(const Ctx &c, const DecodeExperts &d, int max_pairs_per_unit,
-                              const uint8_t *ximg, uint8_t *himg, float *gu, uint8_t *maps, uint8_t *sk);
+cudaError_t launch_mx_gate_up(const Ctx &c, const DecodeExperts &d, const uint8_t *ximg, uint8_t *himg,
+                              float *gu, uint8_t *maps);
 // one token (a batch of one, or one expert with w = null): gate/up, down and
 // the weighted sum in one persistent launch; y [D] written, per-pair rows
 // in `stage` (with w), g and u in `gu`; a dependent of the step's first kernel
 cudaError_t launch_mx_fused1(const Ctx &c, const DecodeExperts &d, const uint8_t *ximg, uint8_t *himg, float *gu,
                              float *stage, const float *w, float *y, const uint8_t *maps, uint8_t *sk);
 // down: W2 h of every pair -> out [pair][D] (launched as a dependent of gate/up)
-cudaError_t launch_mx_down(const Ctx &c, const DecodeExperts &d, int max_pairs_per_unit,
-                           const uint8_t *himg, float *out, uint8_t *maps, uint8_t *sk);
+cudaError_t launch_mx_down(const Ctx &c, const DecodeExperts &d, const uint8_t *himg, float *out,
+                           uint8_t *maps);
 cudaError_t launch_bf16_to_f32(const Ctx &c, float *out, const uint16_t *in, size_t n);
 
 }  // namespace k3mx

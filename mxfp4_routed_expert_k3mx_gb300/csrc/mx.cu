@@ -91,13 +91,13 @@ struct MxArgs {
     float *gu;                      // gate/up: [pair][2][F]
     float *out;                     // down: [pair][D]
     const uint8_t *maps;            // per-expert weight tensor maps [expert][w1, w3, w2]
-    float *partials;                // stream-K hand-over accumulators [grid][NMAT][NCOL][128], or null
-    int *flags;                     // [grid] hand-over flags, zeroed by the step's first kernel
+    float *partials;                // fused pass: stream-K hand-over sums [segment][grid][2][128], or null
     int *status;
     // fused single-token pass only
     const float *w;                 // routing weights [16] of the token (null: one expert, no sum)
     float *y;                       // [D]: the weighted sum (or the one expert's output)
-    int *sync;                      // flags [256], h blocks done per pair [16], y tiles done [28]
+    int *sync;                      // hand-over flags [segment][grid], h blocks done per pair [16],
+                                    // y tiles done [28]; zeroed by the step's first kernel
 };
 
 struct Hdr {
@@ -166,11 +166,6 @@ __device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, uint32_t (&v)[32]) {
           "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
           "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
         : "r"(taddr));
-}
-__device__ __forceinline__ uint2 ldg_u2(const uint8_t *p) {
-    uint2 v;
-    asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-    return v;
 }
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
@@ -295,22 +290,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_launch_dependents();
 
     const int n_units = a.experts == nullptr ? 1 : __ldg(a.n_units);
-    // This CTA's work is a range of the pass's chunk sequence (item-major,
-    // KC chunks per item).  One token per unit: equal ranges (stream-K), an
-    // item cut between two neighbouring CTAs is finished by the one holding
-    // its first chunk, which adds the other's fp32 partial accumulators in
-    // a fixed order.  Otherwise (or for very little work): whole items.
-    const long long n_chunks = (long long)n_units * MT * KC;
-    const bool sk = NTOK == 1 && a.partials != nullptr && n_chunks >= (long long)gridDim.x * (KC + 1);
-    long long q0, q1;
-    if (sk) {
-        q0 = n_chunks * blockIdx.x / gridDim.x;
-        q1 = n_chunks * (blockIdx.x + 1) / gridDim.x;
-    } else {
-        const long long items = (long long)n_units * MT;
-        q0 = items * blockIdx.x / gridDim.x * KC;
-        q1 = items * (blockIdx.x + 1) / gridDim.x * KC;
-    }
+    // This CTA's work is a contiguous range of whole items (item-major, KC
+    // chunks per item).
+    const long long items = (long long)n_units * MT;
+    const long long q0 = items * blockIdx.x / gridDim.x * KC;
+    const long long q1 = items * (blockIdx.x + 1) / gridDim.x * KC;
     auto fail = [&](int detail) {
         report_status(a.status, kStatusWaitTimeout, detail);
         *abort_flag = 1;
@@ -564,7 +548,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------- epilogue --
         const int q4 = warp & 3;
         const int row_in_tile = 32 * q4 + lane;
-        constexpr int PARTIAL = NMAT * NCOL * 128;
         uint32_t it = 0;
         long long q = q0;
         Part p;
@@ -585,36 +568,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(acce0 + 8 * b);
             it++;
-            if (sk && p.lo > 0) {
-                // the tail of an item begun by the previous CTA: hand over
-                // the partial accumulators and move on
-                float *dst = a.partials + (size_t)blockIdx.x * PARTIAL;
-#pragma unroll
-                for (int m = 0; m < NMAT; m++)
-#pragma unroll
-                    for (int j = 0; j < NCOL; j++) dst[(m * NCOL + j) * 128 + row_in_tile] = __uint_as_float(v[m][j]);
-                __threadfence();
-                named_sync(1, 128);
-                if (q4 == 0 && lane == 0)
-                    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(a.flags + blockIdx.x), "r"(1) : "memory");
-                continue;
-            }
-            if (sk && p.hi < KC) {
-                // the head of an item the next CTA finishes: add its partial
-                const int *flag = a.flags + blockIdx.x + 1;
-                int f = 0;
-                for (uint32_t i = 0; i < kWaitLimit && f == 0; i++) {
-                    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(f) : "l"(flag) : "memory");
-                    if (f == 0) __nanosleep(64);
-                }
-                if (f == 0) fail(10);
-                const float *src = a.partials + (size_t)(blockIdx.x + 1) * PARTIAL;
-#pragma unroll
-                for (int m = 0; m < NMAT; m++)
-#pragma unroll
-                    for (int j = 0; j < NCOL; j++)
-                        v[m][j] = __float_as_uint(__uint_as_float(v[m][j]) + src[(m * NCOL + j) * 128 + row_in_tile]);
-            }
             const int row = mt * 128 + row_in_tile;
             const int ntok = u.p1 - u.p0;
 #pragma unroll
@@ -663,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // sequence of stages (every gate/up item, then every down item) is cut in
 // equal ranges over the CTAs (stream-K); an item split between two CTAs
 // is finished by the one holding its first stage, which adds the other's
-// fp32 partial in a fixed order.  A down item starts its MMAs once every
+// summed pieces in a fixed order.  A down item starts its MMAs once every
 // gate/up item of its pair has written its block of h (a per-pair count);
 // the last down item of a 128-row tile of y (a per-tile count) adds the
 // 16 pairs' rows with their routing weights in slot order.
@@ -673,7 +626,6 @@ constexpr int KCG = kD / kChunk;                 // 14 gate/up stages per item
 constexpr int KCD = kF / (2 * kChunk);           // 6 down stages per item
 constexpr int MTG = kF / 128, MTD = kD / 128;    // 24 gate/up, 28 down items per unit
 constexpr int GG = kD / 32, GD = kF / 32;        // scale bytes per weight row: 112, 96
-constexpr int PER_UNIT = MTG * KCG + MTD * KCD;  // 504 stages per unit
 constexpr int STAGE = 2 * kTileBytes + 4 * kAtomBytes;
 constexpr int XB = img_b(kD), XS = img_s(kD);    // the token's x pieces
 constexpr int HB = img_b(kF), HS = img_s(kF);    // a pair's h pieces
@@ -686,8 +638,12 @@ constexpr int SMEM = 1024 + FIXED + S * STAGE;
 constexpr int SFA_COL = 2 * 2 * 8;               // accumulators [2][2][8] first
 constexpr int SFB_COL = SFA_COL + S * 16;
 constexpr int TMEM_COLS = 256;
-constexpr int PARTIAL = 2 * 8 * 128;             // floats per hand-over slot
-constexpr int SYNC_HDONE = 2 * kMaxGrid, SYNC_TILE = 2 * kMaxGrid + kK;   // after the two passes' flags
+constexpr int NSEG = 2;                          // work segments: gate/up, down
+constexpr int PARTIAL = 2 * 128;                 // floats per hand-over slot: the summed pieces
+constexpr int SYNC_HDONE = NSEG * kMaxGrid, SYNC_TILE = SYNC_HDONE + kK;   // after the segments' flags
+constexpr int SYNC_INTS = SYNC_TILE + 64;
+static_assert(MTD <= 64, "tile counts");
+constexpr int MAX_UNITS = kK;                    // one token: at most 16 units
 static_assert(XB <= 2 * HB && XS <= 2 * HS, "x image must fit the h buffers");
 static_assert(S >= 3 && S <= 10, "pipeline depth");
 static_assert(SFB_COL + (kD / 128) * 4 <= TMEM_COLS, "TMEM budget");
@@ -733,53 +689,88 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
     pdl_wait();
     pdl_launch_dependents();
 
-    const int n_units = a.experts == nullptr ? 1 : __ldg(a.n_units);
-    // Every CTA takes an equal share of the gate/up stages, then of the down
-    // stages (so both passes run on every SM).  Shares are equal stage
-    // ranges when there is enough work (stream-K), else whole items.
+    // the token's work units (at most 16), read once into shared memory
+    __shared__ Unit s_unit[MAX_UNITS];
+    __shared__ int s_pair[MAX_UNITS];
+    __shared__ int s_nunits;
+    if (warp == kProdWarp) {
+        const int nu = a.experts == nullptr ? 1 : min(__ldg(a.n_units), MAX_UNITS);
+        if (lane < nu) {
+            s_unit[lane] = unit_at(a, lane);
+            s_pair[lane] = pair_at(a, s_unit[lane].p0);
+        }
+        if (lane == 0) s_nunits = nu;
+    }
+    __syncthreads();
+    const int n_units = s_nunits;
+
+    // Two work segments, every gate/up stage (unit-major) and then every
+    // down stage, each cut in equal stage ranges over the CTAs (stream-K)
+    // when there is enough work, else in whole items: every CTA runs its
+    // gate/up share, then its down share.  (Splitting the units into two
+    // halves run as gate/up A, gate/up B, down A, down B measured no faster:
+    // the extra short parts cost what the shorter wait for h saved.)
     const long long GU = (long long)n_units * MTG * KCG, GDn = (long long)n_units * MTD * KCD;
     const long long G = gridDim.x, B = blockIdx.x;
     const bool sk = a.partials != nullptr && GU >= G * (KCG + 1) && GDn >= G * (KCD + 1);
-    long long qg0, qg1, qd0, qd1;
-    if (sk) {
-        qg0 = GU * B / G;
-        qg1 = GU * (B + 1) / G;
-        qd0 = GU + GDn * B / G;
-        qd1 = GU + GDn * (B + 1) / G;
-    } else {
-        const long long ig = (long long)n_units * MTG, id = (long long)n_units * MTD;
-        qg0 = ig * B / G * KCG;
-        qg1 = ig * (B + 1) / G * KCG;
-        qd0 = GU + id * B / G * KCD;
-        qd1 = GU + id * (B + 1) / G * KCD;
+    const int nseg = 2;
+    long long r0[NSEG], r1[NSEG], cum[NSEG + 1];
+    {
+        const long long st[NSEG] = {0, GU}, len[NSEG] = {GU, GDn};
+        const int kc[NSEG] = {KCG, KCD};
+        cum[0] = 0;
+#pragma unroll
+        for (int i = 0; i < NSEG; i++) {
+            if (sk) {
+                r0[i] = st[i] + len[i] * B / G;
+                r1[i] = st[i] + len[i] * (B + 1) / G;
+            } else {
+                const long long items = len[i] / kc[i];
+                r0[i] = st[i] + items * B / G * kc[i];
+                r1[i] = st[i] + items * (B + 1) / G * kc[i];
+            }
+            cum[i + 1] = cum[i] + (r1[i] - r0[i]);
+        }
     }
-    const long long q0 = qg0;
     auto fail = [&](int detail) {
         report_status(a.status, kStatusWaitTimeout, detail);
         *abort_flag = 1;
     };
     struct Part {
         int ph;          // 0 gate/up, 1 down
+        int seg;         // work segment
         long long item;  // within the phase
         int lo, hi;      // stages of the item
         int mt;          // 128-row tile
+        int pair;        // the unit's pair
         Unit u;
     };
-    auto next_part = [&](long long &q, Part &p) -> bool {
+    // parts in order: `t` walks this CTA's stages, segment after segment
+    auto next_part = [&](long long &t, Part &p) -> bool {
         for (;;) {
-            if (q >= qg1 && q < qd0) q = qd0;              // gate/up share done: the down share
-            if (q >= qd1) return false;
+            int sg = 0;
+#pragma unroll
+            for (int i = 1; i < NSEG; i++) sg += (i < nseg && t >= cum[i]) ? 1 : 0;
+            if (t >= cum[nseg]) return false;
+            long long q0s = r0[0], q1s = r1[0], c0 = cum[0];
+#pragma unroll
+            for (int i = 1; i < NSEG; i++)
+                if (sg == i) q0s = r0[i], q1s = r1[i], c0 = cum[i];
+            const long long q = q0s + (t - c0);
             const bool up = q < GU;
             const int kc = up ? KCG : KCD;
-            const long long r = q - (up ? 0 : GU), lim = up ? qg1 : qd1;
+            const long long r = q - (up ? 0 : GU);
             p.ph = up ? 0 : 1;
+            p.seg = sg;
             p.item = r / kc;
             p.lo = (int)(r % kc);
-            p.hi = (int)min((long long)kc, p.lo + (lim - q));
-            q += p.hi - p.lo;
+            p.hi = (int)min((long long)kc, p.lo + (q1s - q));
+            t += p.hi - p.lo;
             const int mts = up ? MTG : MTD;
             p.mt = (int)(p.item % mts);
-            p.u = unit_at(a, (int)(p.item / mts));
+            const int ui = (int)(p.item / mts);
+            p.u = s_unit[ui];
+            p.pair = s_pair[ui];
             if (p.u.ok) return true;
             if (warp == kProdWarp && lane == 0 && p.lo == 0 && p.mt == 0)
                 report_status(a.status, kStatusBadPointer, p.u.e);
@@ -787,7 +778,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
     };
     // B epoch of a part: the token's x for gate/up, the pair's h for down
     auto b_key = [&](const Part &p) -> long long {
-        return p.ph == 0 ? -1 : (long long)pair_at(a, p.u.p0);
+        return p.ph == 0 ? -1 : (long long)p.pair;
     };
     // B buffer of epoch n: epoch 0 is x (overlapping both h buffers)
     auto b_off = [&](uint32_t n) { return (uint32_t)((n & 1) * HB); };
@@ -799,7 +790,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
         const uint64_t pol_img = l2_evict_last_policy();
         int cur_e = -1, cur_ph = -1;
         const uint8_t *map0 = nullptr, *map1 = nullptr;
-        long long cur_key = -2, q = q0;
+        long long cur_key = -2, q = 0;
         uint32_t su = 0, bl = 0;
         bool x_first = false;            // epoch 0 held x (which overlaps both h buffers)
         Part p;
@@ -856,7 +847,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
                 const uint8_t *src;
                 uint32_t nb, ns;
                 if (p.ph == 0) {
-                    src = a.img_in + (size_t)(a.experts == nullptr ? 0 : pair_at(a, u.p0) / kK) * img_bytes(kD);
+                    src = a.img_in + (size_t)(p.pair / kK) * img_bytes(kD);
                     nb = XB;
                     ns = XS;
                 } else {
@@ -914,7 +905,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
             }
         };
         uint32_t su = 0, np = 0;
-        long long q = q0;
+        long long q = 0;
         Part cur, nxt;
         bool have = next_part(q, cur);
         if (have) issue(cur, 0);
@@ -969,7 +960,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
         // ----------------------------------------------------- MMA issuer --
         if (lane == 0) {
             uint32_t su = 0, bu = 0, it = 0, bcur = 0;
-            long long cur_key = -2, q = q0;
+            long long cur_key = -2, q = 0;
             bool run = true;
             Part p;
             while (run && !*abort_flag && next_part(q, p)) {
@@ -1041,10 +1032,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
         const int row_in_tile = 32 * q4 + lane;
         __shared__ int last_tile;
         uint32_t it = 0;
-        long long q = q0;
+        long long q = 0;
         Part p;
         while (!*abort_flag && next_part(q, p)) {
-            const Unit &u = p.u;
             const int kc = p.ph == 0 ? KCG : KCD;
             const int b = it & 1;
             if (!mbar_wait(accf0 + 8 * b, (it >> 1) & 1)) {
@@ -1060,45 +1050,41 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
             mbar_arrive(acce0 + 8 * b);
             it++;
             const int nm = p.ph == 0 ? 2 : 1;
+            float acc[2] = {0.f, 0.f};
+#pragma unroll
+            for (int m = 0; m < 2; m++)
+#pragma unroll
+                for (int pc = 0; pc < kPieces; pc++) acc[m] += __uint_as_float(v[m][pc]);
+            const size_t slot = (size_t)p.seg * kMaxGrid + blockIdx.x;
             if (sk && p.lo > 0) {
                 // the tail of an item begun by the previous CTA: hand over
-                float *dst = a.partials + ((size_t)p.ph * kMaxGrid + blockIdx.x) * PARTIAL;
+                // the summed pieces and move on
+                float *dst = a.partials + slot * PARTIAL;
 #pragma unroll
                 for (int m = 0; m < 2; m++)
-                    if (m < nm)
-#pragma unroll
-                        for (int j = 0; j < 8; j++) dst[(m * 8 + j) * 128 + row_in_tile] = __uint_as_float(v[m][j]);
-                __threadfence();
+                    if (m < nm) dst[m * 128 + row_in_tile] = acc[m];
                 named_sync(1, 128);
-                if (q4 == 0 && lane == 0)
-                    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(a.sync + p.ph * kMaxGrid + blockIdx.x),
-                                 "r"(1)
-                                 : "memory");
+                if (q4 == 0 && lane == 0) {
+                    __threadfence();
+                    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(a.sync + slot), "r"(1) : "memory");
+                }
                 continue;
             }
             if (sk && p.hi < kc) {
-                // the head of an item the next CTA finishes: add its partial
-                const int *flag = a.sync + p.ph * kMaxGrid + blockIdx.x + 1;
+                // the head of an item the next CTA finishes: add its sums
+                const int *flag = a.sync + slot + 1;
                 int f = 0;
                 for (uint32_t i = 0; i < kWaitLimit && f == 0; i++) {
                     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(f) : "l"(flag) : "memory");
                     if (f == 0) __nanosleep(64);
                 }
                 if (f == 0) fail(10);
-                const float *src = a.partials + ((size_t)p.ph * kMaxGrid + blockIdx.x + 1) * PARTIAL;
+                const float *src = a.partials + (slot + 1) * PARTIAL;
 #pragma unroll
                 for (int m = 0; m < 2; m++)
-                    if (m < nm)
-#pragma unroll
-                        for (int j = 0; j < 8; j++)
-                            v[m][j] = __float_as_uint(__uint_as_float(v[m][j]) + __ldcg(src + (m * 8 + j) * 128 + row_in_tile));
+                    if (m < nm) acc[m] += __ldcg(src + m * 128 + row_in_tile);
             }
-            float acc[2] = {0.f, 0.f};
-#pragma unroll
-            for (int m = 0; m < 2; m++)
-#pragma unroll
-                for (int pc = 0; pc < kPieces; pc++) acc[m] += __uint_as_float(v[m][pc]);
-            const int pair = pair_at(a, u.p0);
+            const int pair = p.pair;
             const int row = p.mt * 128 + row_in_tile;
             if (p.ph == 0) {
                 float *gu = a.gu + (size_t)pair * 2 * kF;
@@ -1107,18 +1093,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
                 uint8_t *ib = a.img_out + (size_t)pair * img_bytes(kF);
                 store_pieces(situ_glu(acc[0], acc[1]), ib, ib + img_b(kF), p.mt * 4 + q4);
                 // this item's block of h is written: count it for the pair
-                __threadfence();
+                // (the barrier orders the four warps' writes before one
+                // thread's fence and count)
                 named_sync(1, 128);
-                if (q4 == 0 && lane == 0)
+                if (q4 == 0 && lane == 0) {
+                    __threadfence();
                     atomicAdd(a.sync + SYNC_HDONE + (a.experts == nullptr ? 0 : pair % kK), 1);
+                }
             } else if (a.w == nullptr) {
                 a.y[row] = acc[0];                      // one expert: its output is y
             } else {
                 a.out[(size_t)pair * kD + row] = acc[0];
                 // the last of the token's 16 pairs to finish this tile forms y
-                __threadfence();
                 named_sync(1, 128);
                 if (q4 == 0 && lane == 0) {
+                    __threadfence();
                     const int done_pairs = atomicAdd(a.sync + SYNC_TILE + p.mt, 1) + 1;
                     __threadfence();
                     last_tile = done_pairs == kK;
@@ -1224,12 +1213,12 @@ bool weight_map_templates(CUtensorMap &w13, CUtensorMap &w2) {
     return true;
 }
 
-// stream-K region (one token per unit): flags [2][kMaxGrid] ints, then the
-// gate/up and the down hand-over partials
+// stream-K region of the fused single-token pass: the hand-over flags
+// [4 segments][kMaxGrid], the per-pair h counts and the per-tile y counts
+// (ints), then the hand-over partials [4 segments][kMaxGrid][2][128] fp32
 namespace {
-constexpr size_t kSkFlagBytes = (size_t)4 * kMaxGrid * sizeof(int);
-constexpr size_t kSkPart0 = (size_t)MxShape<0, 1>::NMAT * MxShape<0, 1>::NCOL * 128 * sizeof(float);
-constexpr size_t kSkPart1 = (size_t)MxShape<1, 1>::NMAT * MxShape<1, 1>::NCOL * 128 * sizeof(float);
+constexpr size_t kSkFlagBytes = (size_t)f1::SYNC_INTS * sizeof(int);
+constexpr size_t kSkPartBytes = (size_t)f1::NSEG * kMaxGrid * f1::PARTIAL * sizeof(float);
 }  // namespace
 cudaError_t launch_mx_fused1(const Ctx &c, const DecodeExperts &d, const uint8_t *ximg, uint8_t *himg, float *gu,
                              float *stage, const float *w, float *y, const uint8_t *maps, uint8_t *sk) {
@@ -1258,7 +1247,7 @@ size_t mx_ximg_bytes(int n_tokens) { return (size_t)n_tokens * img_bytes(kD); }
 size_t mx_himg_bytes(int n_pairs) { return (size_t)n_pairs * img_bytes(kF); }
 size_t mx_maps_bytes(int n_experts) { return expert_maps_bytes(n_experts); }
 
-size_t mx_streamk_bytes() { return kSkFlagBytes + (size_t)2 * kMaxGrid * kSkPart0; }
+size_t mx_streamk_bytes() { return kSkFlagBytes + kSkPartBytes; }
 int mx_streamk_flag_count() { return (int)(kSkFlagBytes / sizeof(int)); }
 
 cudaError_t launch_mx_ximg(const Ctx &c, const void *x, int x_bf16, int n_tokens, uint8_t *ximg, uint8_t *sk,
@@ -1276,31 +1265,23 @@ cudaError_t launch_mx_ximg(const Ctx &c, const void *x, int x_bf16, int n_tokens
     return cudaGetLastError();
 }
 
-cudaError_t launch_mx_gate_up(const Ctx &c, const DecodeExperts &d, int max_pairs_per_unit,
-                              const uint8_t *ximg, uint8_t *himg, float *gu, uint8_t *maps, uint8_t *sk) {
+cudaError_t launch_mx_gate_up(const Ctx &c, const DecodeExperts &d, const uint8_t *ximg, uint8_t *himg,
+                              float *gu, uint8_t *maps) {
     MxArgs a = mx_args(d);
     a.img_in = ximg;
     a.img_out = himg;
     a.gu = gu;
     a.maps = maps;
-    if (sk != nullptr && max_pairs_per_unit <= 1) {
-        a.flags = reinterpret_cast<int *>(sk);
-        a.partials = reinterpret_cast<float *>(sk + kSkFlagBytes);
-    }
-    return max_pairs_per_unit <= 1 ? launch_mx_t<0, 1>(c, a, true) : launch_mx_t<0, kUnitPairs>(c, a, true);
+    return launch_mx_t<0, kUnitPairs>(c, a, true);
 }
 
-cudaError_t launch_mx_down(const Ctx &c, const DecodeExperts &d, int max_pairs_per_unit,
-                           const uint8_t *himg, float *out, uint8_t *maps, uint8_t *sk) {
+cudaError_t launch_mx_down(const Ctx &c, const DecodeExperts &d, const uint8_t *himg, float *out,
+                           uint8_t *maps) {
     MxArgs a = mx_args(d);
     a.img_in = himg;
     a.out = out;
     a.maps = maps;
-    if (sk != nullptr && max_pairs_per_unit <= 1) {
-        a.flags = reinterpret_cast<int *>(sk) + kMaxGrid;
-        a.partials = reinterpret_cast<float *>(sk + kSkFlagBytes + (size_t)kMaxGrid * kSkPart0);
-    }
-    return max_pairs_per_unit <= 1 ? launch_mx_t<1, 1>(c, a, true) : launch_mx_t<1, kUnitPairs>(c, a, true);
+    return launch_mx_t<1, kUnitPairs>(c, a, true);
 }
 
 }  // namespace k3mx
