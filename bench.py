@@ -11,7 +11,7 @@ streamed per second (GB/s); the line also carries the batch-64 decode and
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference]
   python bench.py --profile-case decode|prefill --tokens T [--resident R]
-                  [--confine] [--iters I]
+                  [--confine] [--mx] [--iters I]
 
 The --profile-case form runs a small case of one path for Nsight Compute
 captures (a few GB on the device): R experts (default 64, 1.1 GB, larger
@@ -48,7 +48,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # kernels per traced launch group
 KERNELS_PER_GROUP = {"route": 1, "group_small": 1, "group": 3, "mx_pieces": 1,
                      "decode_expert": 1, "decode_gate_up": 1, "decode_down": 1, "combine": 1,
-                     "prefill_prep": 2, "prefill_gate_up": 1, "prefill_down": 1}
+                     "prefill_prep": 3, "prefill_gate_up": 1, "prefill_down": 1}
 PARAMS_PER_EXPERT = 33030144
 X_IMAGE_BYTES = 8 * 3584 // 2 + 3584          # 8 MXFP4 pieces of x and their scale lines
 H_IMAGE_BYTES = 8 * 3072 // 2 + 3072
@@ -429,31 +429,38 @@ def run_ours(args):
                                      "hbm_frac": round(b / (ms / 1e3) / 1e9 / hbm_peak, 4),
                                      "kernels": {k: {"launches": v[0], "avg_us": round(1e3 * v[1] / max(1, v[0]), 2)}
                                                  for k, v in r["trace"].items()}}
-            # prefill, 4096 bf16 tokens, flat routing: tcgen05 grouped GEMMs
-            wl = Workload("moe_prefill_4096", 4096, True, k3mx.K3MX_PATH_PREFILL)
-            r = time_workload(k3mx, wl, table, dev, max(3, args.steps // 4), args.warmup, None, flush)
-            ms = sum(r["ms"]) / len(r["ms"])
-            pairs = 4096 * K
-            flops = 2.0 * PARAMS_PER_EXPERT * pairs
-            tr = r["trace"]
-            kern = {}
-            pf_hash = kernel_source_hash(["prefill.cu", "prefill.cuh", "common.cuh"])
-            for name, params in (("prefill_gate_up", GATE_UP_PARAMS), ("prefill_down", PARAMS_PER_EXPERT - GATE_UP_PARAMS)):
-                if name in tr:
-                    kms = tr[name][1] / tr[name][0]
-                    tf = 2.0 * params * pairs / (kms / 1e3) / 1e12
-                    kern[name] = {"avg_ms": round(kms, 4), "TFLOP_s": round(tf, 1),
-                                  "frac_bf16_peak": round(tf / bf16_peak, 4),
-                                  "traffic": profiled_traffic(name, wl.name, pf_hash)}
-            sec["moe_prefill_4096"] = {
-                "tokens_per_s": round(4096 / (ms / 1e3), 1), "ms_per_step": round(ms, 4),
-                "TFLOP_s": round(flops / (ms / 1e3) / 1e12, 1),
-                "frac_bf16_peak": round(flops / (ms / 1e3) / 1e12 / bf16_peak, 4),
-                "expert_GB_s": round(E * EXPERT_BYTES / (ms / 1e3) / 1e9, 1),
-                "peak_source": f"{peak_src} bf16 burst {bf16_peak} TFLOP/s (f16 MMA, same rate)",
-                "tensor_kernels": kern,
-                "kernels": {k: {"launches": v[0], "avg_us": round(1e3 * v[1] / max(1, v[0]), 2)}
-                            for k, v in tr.items()}}
+            # prefill, 4096 bf16 tokens, flat routing: tcgen05 grouped GEMMs,
+            # weights dequantised to f16 (PREFILL) or fed as stored to the
+            # block-scaled MMAs with x and h as MXFP4 pieces (PREFILL_MX)
+            for wname, wpath, srcs in (("moe_prefill_4096", k3mx.K3MX_PATH_PREFILL,
+                                        ["prefill.cu", "prefill.cuh", "common.cuh"]),
+                                       ("moe_prefill_4096_mx", k3mx.K3MX_PATH_PREFILL_MX,
+                                        ["px.cu", "tc.cuh", "pieces.cuh", "common.cuh"])):
+                wl = Workload(wname, 4096, True, wpath)
+                r = time_workload(k3mx, wl, table, dev, max(3, args.steps // 4), args.warmup, None, flush)
+                ms = sum(r["ms"]) / len(r["ms"])
+                pairs = 4096 * K
+                flops = 2.0 * PARAMS_PER_EXPERT * pairs
+                tr = r["trace"]
+                kern = {}
+                pf_hash = kernel_source_hash(srcs)
+                for name, params in (("prefill_gate_up", GATE_UP_PARAMS),
+                                     ("prefill_down", PARAMS_PER_EXPERT - GATE_UP_PARAMS)):
+                    if name in tr:
+                        kms = tr[name][1] / tr[name][0]
+                        tf = 2.0 * params * pairs / (kms / 1e3) / 1e12
+                        kern[name] = {"avg_ms": round(kms, 4), "TFLOP_s": round(tf, 1),
+                                      "frac_bf16_peak": round(tf / bf16_peak, 4),
+                                      "traffic": profiled_traffic(name, wl.name, pf_hash)}
+                sec[wname] = {
+                    "tokens_per_s": round(4096 / (ms / 1e3), 1), "ms_per_step": round(ms, 4),
+                    "TFLOP_s": round(flops / (ms / 1e3) / 1e12, 1),
+                    "frac_bf16_peak": round(flops / (ms / 1e3) / 1e12 / bf16_peak, 4),
+                    "expert_GB_s": round(E * EXPERT_BYTES / (ms / 1e3) / 1e9, 1),
+                    "peak_source": f"{peak_src} bf16 burst {bf16_peak} TFLOP/s (algorithmic FLOPs)",
+                    "tensor_kernels": kern,
+                    "kernels": {k: {"launches": v[0], "avg_us": round(1e3 * v[1] / max(1, v[0]), 2)}
+                                for k, v in tr.items()}}
         line["secondary"] = sec
         if not args.no_cpu_baseline:
             steps_in = [decode_inputs(i, 1) for i in range(64)]
@@ -482,7 +489,7 @@ def run_profile_case(args):
     if args.confine:
         bias[R:] = -100.0
     prefill = args.profile_case == "prefill"
-    path = k3mx.K3MX_PATH_PREFILL if prefill else k3mx.K3MX_PATH_DECODE
+    path = (k3mx.K3MX_PATH_PREFILL_MX if args.mx else k3mx.K3MX_PATH_PREFILL) if prefill else k3mx.K3MX_PATH_DECODE
     dt = k3mx.K3MX_BF16 if prefill else k3mx.K3MX_F32
     ws = torch.empty(k3mx.k3mx_moe_workspace_size(T, dt, path), dtype=torch.uint8, device=dev)
     y = torch.empty((T, D), dtype=torch.float32, device=dev)
@@ -495,7 +502,7 @@ def run_profile_case(args):
         k3mx.k3mx_moe_routed(y, xt, table, torch.from_numpy(logits).to(dev), bias, ws, path=path)
     torch.cuda.synchronize(dev)
     st = k3mx.k3mx_device_status()
-    print(json.dumps({"profile_case": args.profile_case, "tokens": T, "resident": R,
+    print(json.dumps({"profile_case": args.profile_case, "mx": args.mx, "tokens": T, "resident": R,
                       "confine": args.confine, "iters": args.iters, "status": st,
                       "y_abs_sum": float(y.abs().sum())}), flush=True)
     if st[0] != 0:
@@ -515,6 +522,7 @@ def main():
     ap.add_argument("--tokens", type=int, default=1)
     ap.add_argument("--resident", type=int, default=64)
     ap.add_argument("--confine", action="store_true")
+    ap.add_argument("--mx", action="store_true", help="prefill profile case on the block-scaled path")
     ap.add_argument("--iters", type=int, default=4)
     args = ap.parse_args()
     if args.profile_case:

@@ -63,9 +63,10 @@ enum { K3MX_F32 = 0, K3MX_BF16 = 1 };
 
 /* execution path of k3mx_moe_routed */
 enum {
-    K3MX_PATH_AUTO = 0,     /* PREFILL when x is bf16 and n_tokens >= K3MX_PREFILL_MIN_TOKENS, else DECODE */
-    K3MX_PATH_DECODE = 1,   /* fp32 activations, grouped CUDA-core GEMV, fp32 h      */
-    K3MX_PATH_PREFILL = 2   /* bf16 activations, grouped tcgen05 GEMM, bf16 h        */
+    K3MX_PATH_AUTO = 0,       /* PREFILL_MX when x is bf16 and n_tokens >= K3MX_PREFILL_MIN_TOKENS, else DECODE */
+    K3MX_PATH_DECODE = 1,     /* fp32 activations; x and h as 8 MXFP4 pieces, kind::mxf4 MMAs   */
+    K3MX_PATH_PREFILL = 2,    /* bf16 activations; weights dequantised to f16, kind::f16 MMAs   */
+    K3MX_PATH_PREFILL_MX = 3  /* bf16 activations; x and h as 4 MXFP4 pieces, kind::mxf4 MMAs   */
 };
 #define K3MX_PREFILL_MIN_TOKENS 256
 #define K3MX_MAX_TOKENS         65536
@@ -159,7 +160,7 @@ k3mx_status k3mx_group(int32_t *counts, int32_t *offsets, int32_t *perm,
  *   x        [n_tokens][3584], fp32 (x_dtype K3MX_F32) or bf16 bits (K3MX_BF16)
  *   experts  DEVICE array of 896 k3mx_expert
  *   logits   [n_tokens][896] fp32, bias [896] fp32
- *   path     K3MX_PATH_*; PREFILL requires bf16 x
+ *   path     K3MX_PATH_*; PREFILL and PREFILL_MX require bf16 x
  *   idx_out, w_out: optional DEVICE arrays [n_tokens][16] (NULL to skip)
  *            receiving the routing result
  *   workspace: device, 256-byte aligned, >= k3mx_moe_workspace_size(...)
@@ -168,9 +169,15 @@ k3mx_status k3mx_group(int32_t *counts, int32_t *offsets, int32_t *perm,
  * abs-weighted sums.
  * PREFILL converts x (bf16) to f16, dequantises the
  * weights to f16, rounds h to f16 and multiplies f16 x f16 on the tensor
- * cores with fp32 accumulation: per-token relative L2 error within 1e-2.  DECODE is deterministic; PREFILL adds the 16 expert
- * contributions of a token with fp32 atomics, so the order of those adds,
- * and the last bits of y, may vary between runs.
+ * cores with fp32 accumulation: per-token relative L2 error within 1e-2.
+ * PREFILL_MX splits x and h (h from a hardware-tanh SiTU) into four MXFP4
+ * pieces per 32-column block (residual below 4^-4 of the block's largest
+ * value) and multiplies them with the weights as stored on the
+ * block-scaled tensor cores with fp32 accumulation: per-token relative L2
+ * error within 1e-2 (about 3e-4 on the synthetic workload).  DECODE is
+ * deterministic; both prefill paths add the 16 expert contributions of a
+ * token with fp32 atomics, so the order of those adds, and the last bits
+ * of y, may vary between runs.
  */
 size_t k3mx_moe_workspace_size(int n_tokens, int x_dtype, int path);
 k3mx_status k3mx_moe_routed(float *y, const void *x, int x_dtype, int n_tokens,

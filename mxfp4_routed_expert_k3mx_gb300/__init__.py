@@ -23,7 +23,7 @@ K3MX_LATENT = 3584
 K3MX_INTER = 3072
 K3MX_EXPERT_BYTES = 17547264
 K3MX_F32, K3MX_BF16 = 0, 1
-K3MX_PATH_AUTO, K3MX_PATH_DECODE, K3MX_PATH_PREFILL = 0, 1, 2
+K3MX_PATH_AUTO, K3MX_PATH_DECODE, K3MX_PATH_PREFILL, K3MX_PATH_PREFILL_MX = 0, 1, 2, 3
 K3MX_PREFILL_MIN_TOKENS = 256
 K3MX_MAX_TOKENS = 65536
 K3MX_NOALLOC_MAX_TOKENS = 8

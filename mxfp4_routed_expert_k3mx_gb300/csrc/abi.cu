@@ -137,7 +137,7 @@ struct MoeLayout {
 
 int resolve_path(int n_tokens, int x_dtype, int path) {
     if (path == K3MX_PATH_AUTO)
-        return (x_dtype == K3MX_BF16 && n_tokens >= K3MX_PREFILL_MIN_TOKENS) ? K3MX_PATH_PREFILL
+        return (x_dtype == K3MX_BF16 && n_tokens >= K3MX_PREFILL_MIN_TOKENS) ? K3MX_PATH_PREFILL_MX
                                                                              : K3MX_PATH_DECODE;
     return path;
 }
@@ -168,6 +168,8 @@ MoeLayout moe_layout(int n_tokens, int x_dtype, int path) {
         L.sk = n_tokens == 1 ? take(mx_streamk_bytes()) : 0;   // stream-K hand-over (one token)
         L.h = take(P * 2 * kF * 4);          // g and u per pair
         L.stage = take(P * kD * 4);
+    } else if (path == K3MX_PATH_PREFILL_MX) {
+        L.pre = take(prefill_mx_scratch_bytes(n_tokens));
     } else {
         L.pre = take(prefill_scratch_bytes(n_tokens));
     }
@@ -190,9 +192,9 @@ k3mx_status check_moe_args(const void *y, const void *x, int x_dtype, int n_toke
                            int path) {
     if (!y || !x || !experts || !logits || !bias) return K3MX_EINVAL;
     if (x_dtype != K3MX_F32 && x_dtype != K3MX_BF16) return K3MX_EINVAL;
-    if (path < K3MX_PATH_AUTO || path > K3MX_PATH_PREFILL) return K3MX_EINVAL;
+    if (path < K3MX_PATH_AUTO || path > K3MX_PATH_PREFILL_MX) return K3MX_EINVAL;
     if (n_tokens < 1 || n_tokens > K3MX_MAX_TOKENS) return K3MX_ESHAPE;
-    if (resolve_path(n_tokens, x_dtype, path) == K3MX_PATH_PREFILL && x_dtype != K3MX_BF16)
+    if (resolve_path(n_tokens, x_dtype, path) >= K3MX_PATH_PREFILL && x_dtype != K3MX_BF16)
         return K3MX_EINVAL;
     if (!aligned16(y) || !aligned16(x) || !aligned16(logits) || !aligned16(bias) ||
         !aligned16(experts))
@@ -237,7 +239,7 @@ k3mx_status run_moe(const Ctx &c, float *y, const void *x, int x_dtype, int n_to
     if (err != cudaSuccess) return K3MX_ECUDA;
     const int max_active = n_tokens * kK < kE ? n_tokens * kK : kE;
 
-    if (path == K3MX_PATH_PREFILL) {
+    if (path == K3MX_PATH_PREFILL || path == K3MX_PATH_PREFILL_MX) {
         PrefillArgs a{};
         a.y = y;
         a.x = static_cast<const uint16_t *>(x);
@@ -251,7 +253,8 @@ k3mx_status run_moe(const Ctx &c, float *y, const void *x, int x_dtype, int n_to
         a.n_active = g.n_active;
         a.max_active = max_active;
         a.scratch = at<void>(ws, L.pre);
-        return from_cuda(launch_prefill(c, a));  // traced per kernel inside
+        // traced per kernel inside
+        return from_cuda(path == K3MX_PATH_PREFILL_MX ? launch_prefill_mx(c, a) : launch_prefill(c, a));
     }
 
     DecodeExperts d{experts, nullptr, g.units, g.n_units, g.perm, max_units(n_tokens)};
@@ -441,10 +444,10 @@ k3mx_status k3mx_moe_routed_host(float *y_host, const void *x_host, int x_dtype,
                                  size_t ws_bytes, k3mx_stream_t stream) {
     if (!y_host || !x_host || !logits_host || !bias_host || !experts) return K3MX_EINVAL;
     if (x_dtype != K3MX_F32 && x_dtype != K3MX_BF16) return K3MX_EINVAL;
-    if (path < K3MX_PATH_AUTO || path > K3MX_PATH_PREFILL) return K3MX_EINVAL;
+    if (path < K3MX_PATH_AUTO || path > K3MX_PATH_PREFILL_MX) return K3MX_EINVAL;
     if (n_tokens < 1 || n_tokens > K3MX_MAX_TOKENS) return K3MX_ESHAPE;
     path = resolve_path(n_tokens, x_dtype, path);
-    if (path == K3MX_PATH_PREFILL && x_dtype != K3MX_BF16) return K3MX_EINVAL;
+    if (path >= K3MX_PATH_PREFILL && x_dtype != K3MX_BF16) return K3MX_EINVAL;
     if (!aligned16(experts)) return K3MX_EALIGN;
     const MoeLayout L = moe_layout(n_tokens, x_dtype, path);
     if (!workspace || ws_bytes < L.total_host) return K3MX_EWORKSPACE;

@@ -37,6 +37,7 @@
 #include "common.cuh"
 #include "pieces.cuh"
 #include "tmaps.cuh"
+#include "tc.cuh"
 
 namespace k3mx {
 namespace {
@@ -105,79 +106,6 @@ struct Hdr {
     uint32_t tmem;
     int abort;
 };
-
-// ------------------------------------------------------------ PTX helpers --
-
-// K-major operand in the 128-byte swizzle with a given stride between
-// 8-row groups
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t sbo) {
-    return (uint64_t)((saddr >> 4) & 0x3FFFu) | (uint64_t)(16u >> 4) << 16 |
-           (uint64_t)((sbo >> 4) & 0x3FFFu) << 32 | (uint64_t)1 << 46 | (uint64_t)2 << 61;
-}
-// tcgen05.cp source: 32 lines of 16 B in four 8-line groups `sbo` apart, no swizzle
-__device__ __forceinline__ uint64_t desc_atom(uint32_t saddr, uint32_t sbo) {
-    return (uint64_t)((saddr >> 4) & 0x3FFFu) | (uint64_t)((sbo >> 4) & 0x3FFFu) << 32 |
-           (uint64_t)1 << 46;
-}
-// one scale-factor atom (32 lines x 16 B) into 4 TMEM columns of all 128
-// lanes (each lane quarter gets the same copy); scale of row m, block kb of
-// the atom: column m / 32, byte kb, line m % 32
-__device__ __forceinline__ void tmem_cp_atom(uint32_t taddr, uint64_t desc) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
-}
-// instruction descriptor, kind::mxf4: e2m1 A and B, ue8m0 scales, K-major,
-// M = 128, N = n; sf_id picks the byte pair of the scale columns
-__device__ __forceinline__ uint32_t idesc_mxf4(int n, int sf_id) {
-    return ((uint32_t)sf_id << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | (1u << 23) |
-           ((uint32_t)(128 >> 4) << 24) | ((uint32_t)sf_id << 29);
-}
-__device__ __forceinline__ void mma_mxf4(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t sfa, uint32_t sfb, uint32_t acc) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
-        : "memory");
-}
-__device__ __forceinline__ void tma_2d(uint32_t dst, const void *map, int x, int y, uint32_t bar,
-                                       uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
-        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(map), "r"(x), "r"(y), "r"(bar), "l"(policy)
-        : "memory");
-}
-template <int N>
-__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&v)[N]);
-template <>
-__device__ __forceinline__ void tmem_ld<8>(uint32_t taddr, uint32_t (&v)[8]) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
-                 : "r"(taddr));
-}
-template <>
-__device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, uint32_t (&v)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
-          "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
-          "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
-          "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-        : "r"(taddr));
-}
-__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-                 : "memory");
-}
-__device__ __forceinline__ uint64_t l2_evict_last_policy() {
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-// scale byte 255 (a group that contributes nothing) -> 0 (2^-127)
-__device__ __forceinline__ uint32_t drop_nan_scales(uint32_t w) { return w & ~__vcmpeq4(w, 0xFFFFFFFFu); }
 
 // x of every token -> its piece image; one warp per 32-column block
 // x of every token -> its piece image (one warp per 32-column block); the

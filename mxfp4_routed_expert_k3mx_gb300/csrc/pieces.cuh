@@ -43,20 +43,20 @@ __device__ __forceinline__ uint32_t spread_nibbles(uint32_t x) {
     return x;
 }
 
-// The 32 values of a warp (lane = column of one 32-column block `kb` of a
-// vector) as kPieces MXFP4 pieces, stored into the vector's piece image
-// (B part `ib`, scale part `is`).  Whole warp.
-__device__ __forceinline__ void store_pieces(float r, uint8_t *ib, uint8_t *is, int kb) {
+// The 32 values of a warp (lane = column of one 32-column block) split
+// into NP MXFP4 pieces.  Lane p < NP receives piece p: its 16 packed bytes
+// (`words`, the low nibble of byte i is lane 2i's code) and its ue8m0 scale
+// byte.  Whole warp.  ROLLED keeps the loop body short (few instruction
+// fetches where the body runs once per launch); otherwise it is unrolled.
+template <int NP, bool ROLLED>
+__device__ __forceinline__ void split_pieces(float r, uint4 &words, uint32_t &scale) {
     const int lane = threadIdx.x & 31;
     uint32_t m0 = 0, m1 = 0, m2 = 0, m3 = 0, msb = 0;
-    // rolled: the body runs in epilogues while the weight stream keeps
-    // memory busy, and a short body keeps its first instruction fetches few
-#pragma unroll 1
-    for (int p = 0; p < kPieces; p++) {
-        float mx = fabsf(r);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        const uint32_t mb = __float_as_uint(mx);
+#pragma unroll(ROLLED ? 1 : NP)
+    for (int p = 0; p < NP; p++) {
+        // the block's largest residual magnitude (non-negative floats order
+        // as their bit patterns)
+        const uint32_t mb = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(r)));
         const int E = (int)(mb >> 23) - 127;
         int code = 0;
         uint32_t sb = 0;
@@ -80,15 +80,28 @@ __device__ __forceinline__ void store_pieces(float r, uint8_t *ib, uint8_t *is, 
             msb = sb;
         }
     }
-    if (lane < kPieces) {
-        uint32_t w[4];
+    uint32_t w[4];
 #pragma unroll
-        for (int q = 0; q < 4; q++)
-            w[q] = spread_nibbles((m0 >> (8 * q)) & 0xFFu) | spread_nibbles((m1 >> (8 * q)) & 0xFFu) << 1 |
-                   spread_nibbles((m2 >> (8 * q)) & 0xFFu) << 2 | spread_nibbles((m3 >> (8 * q)) & 0xFFu) << 3;
-        *reinterpret_cast<uint4 *>(ib + (kb >> 3) * 1024 + lane * 128 + (((kb & 7) ^ lane) << 4)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
-        is[(kb >> 2) * 128 + lane * 16 + (kb & 3)] = (uint8_t)msb;
+    for (int q = 0; q < 4; q++)
+        w[q] = spread_nibbles((m0 >> (8 * q)) & 0xFFu) | spread_nibbles((m1 >> (8 * q)) & 0xFFu) << 1 |
+               spread_nibbles((m2 >> (8 * q)) & 0xFFu) << 2 | spread_nibbles((m3 >> (8 * q)) & 0xFFu) << 3;
+    words = make_uint4(w[0], w[1], w[2], w[3]);
+    scale = msb;
+}
+
+// The 32 values of a warp (lane = column of one 32-column block `kb` of a
+// vector) as kPieces MXFP4 pieces, stored into the vector's piece image
+// (B part `ib`, scale part `is`).  Whole warp.
+__device__ __forceinline__ void store_pieces(float r, uint8_t *ib, uint8_t *is, int kb) {
+    const int lane = threadIdx.x & 31;
+    uint4 w;
+    uint32_t sb;
+    // rolled: the body runs in epilogues while the weight stream keeps
+    // memory busy, and a short body keeps its first instruction fetches few
+    split_pieces<kPieces, true>(r, w, sb);
+    if (lane < kPieces) {
+        *reinterpret_cast<uint4 *>(ib + (kb >> 3) * 1024 + lane * 128 + (((kb & 7) ^ lane) << 4)) = w;
+        is[(kb >> 2) * 128 + lane * 16 + (kb & 3)] = (uint8_t)sb;
     }
 }
 

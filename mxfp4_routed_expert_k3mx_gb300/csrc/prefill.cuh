@@ -21,4 +21,11 @@ int prefill_max_units(int n_tokens);
 size_t prefill_scratch_bytes(int n_tokens);
 cudaError_t launch_prefill(const Ctx &c, const PrefillArgs &a);
 
+// Block-scaled variant (px.cu): x and h as four MXFP4 pieces, the weights
+// fed to kind::mxf4 MMAs as stored.  `scratch` holds
+// prefill_mx_scratch_bytes(n_tokens) bytes, 256-byte aligned.
+int prefill_mx_max_units(int n_tokens);
+size_t prefill_mx_scratch_bytes(int n_tokens);
+cudaError_t launch_prefill_mx(const Ctx &c, const PrefillArgs &a);
+
 }  // namespace k3mx

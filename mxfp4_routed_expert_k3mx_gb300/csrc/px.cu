@@ -1,0 +1,822 @@
+// px.cu - prefill on block-scaled 5th-generation tensor-core MMAs
+// (tcgen05 kind::mxf4): the grouped expert GEMMs of many tokens with the
+// packed MXFP4 weights and their ue8m0 group scales fed to the tensor cores
+// exactly as stored (Kimi K3 engine (c/kimi_k3.c), "Weights"), with no
+// per-weight work in registers.
+//
+// Activations.  kind::mxf4 multiplies e2m1 by e2m1, so every activation
+// row (x of a token for gate/up, h of a pair for down) is split into kPP
+// MXFP4 pieces per 32-column block (pieces.cuh: piece i takes the scale
+// that maps the block's largest residual into (3, 6] and the nearest e2m1
+// value of every residual).  Four pieces leave a residual below 4^-4 of the
+// block's largest value (the layer's relative L2 error is about 2e-4).  The
+// MMA sums the pieces itself: piece p of every token of a work unit is one
+// B operand, and the kPP MMAs of a K step accumulate into the same columns.
+//
+// Work.  A unit is one expert and at most kUT of its (token, slot) pairs,
+// contiguous in the grouped order (Kimi K3 engine (c/kimi_k3.c), "Chunked
+// prefill": each unique expert is loaded once for all its tokens).  Item =
+// (unit, 128-row tile); a CTA per SM takes every grid-th item.  Per
+// item K streams in 128-column stages:
+//   warp 0      A producer: TMA of the weight tiles (128 rows x 64 B, 64-byte
+//               swizzle) through per-expert tensor maps into an A ring
+//   warp 1      scale loader: the tile's scale bytes (16 per row, four
+//               stages ahead) from global into registers, then per stage the
+//               32-line scale-factor atoms tcgen05.cp reads (255 -> 0)
+//   warp 2      TMEM owner; lane 0 copies the scale atoms to TMEM and issues,
+//               per stage, 2 K steps x kPP pieces x NMAT MMAs (M = 128,
+//               N = the unit's tokens rounded up to 16, K = 64)
+//   warp 3      B producer: one 3-D TMA per stage for all pieces of the
+//               unit's rows (box of 32, 64 or 96 rows) and one bulk copy of
+//               the stage's B scale atoms into a B ring
+//   warps 4-11  epilogue, two warps per TMEM lane quarter, each half the
+//               unit's tokens: gate/up h = SiTU(g, u) split into pieces
+//               (rows of the grouped h planes + the unit's B scale atoms for
+//               down); down y[t] += w_tk * Y (fp32 atomics)
+// Two accumulator buffers let the epilogue of one item overlap the MMAs of
+// the next.  Every wait is bounded; a timeout is reported on the device
+// status word and every role leaves its loop.
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "pieces.cuh"
+#include "prefill.cuh"
+#include "tc.cuh"
+#include "tmaps.cuh"
+
+namespace k3mx {
+namespace {
+
+constexpr int kPP = 4;                  // activation pieces
+constexpr int kUT = 96;                 // pairs per unit (MMA N <= 96)
+constexpr int kKS = 128;                // K columns per stage (64 packed bytes per row)
+constexpr int kATile = 128 * 64;        // A tile: 128 rows x 64 B
+constexpr int kBPiece = kUT * 64;       // one piece of the unit's B: 96 rows x 64 B
+__host__ __device__ constexpr int b_rows(int i) { return 32 * (i + 1); }   // B box heights: 32, 64, 96
+// the B box of a unit of n pairs: the smallest height holding them
+__host__ __device__ constexpr int b_sel(int n) { return n <= 32 ? 0 : n <= 64 ? 1 : 2; }
+constexpr int kAtomB = 512;             // scale-factor atom: 32 lines x 16 B
+constexpr int kPxThreads = 12 * 32;
+constexpr int kAProd = 0, kSfW = 1, kMmaW = 2, kBProd = 3, kEpi0 = 4;
+constexpr int kEpiThreads = 8 * 32;
+constexpr int kPxSmemLimit = 227 * 1024;
+
+template <int PH> struct PxCfg;
+template <> struct PxCfg<0> {           // gate/up: g = W1 x, u = W3 x
+    static constexpr int NMAT = 2, K = kD, M = kF, SA = 5, SB = 4;
+};
+template <> struct PxCfg<1> {           // down: Y = W2 h
+    static constexpr int NMAT = 1, K = kF, M = kD, SA = 6, SB = 6;
+};
+
+template <int PH> struct PxShape {
+    using C = PxCfg<PH>;
+    static constexpr int NMAT = C::NMAT, K = C::K, M = C::M, SA = C::SA, SB = C::SB;
+    static constexpr int KC = K / kKS, MT = M / 128, G = K / 32;
+    static constexpr int ASTAGE = ((NMAT * (kATile + kAtomB)) + 1023) / 1024 * 1024;
+    static constexpr int BSTAGE = kPP * kBPiece + kPP * kAtomB;          // 26 KB
+    // gate/up: per epilogue warp a 32 x 33 fp32 tile to turn (feature, token)
+    // into (token, feature)
+    static constexpr int TRANS = PH == 0 ? 8 * 32 * 33 * 4 : 0;
+    static constexpr int SMEM = 1024 + 1024 + SA * ASTAGE + SB * BSTAGE + TRANS;  // alignment slack, header
+    // TMEM: accumulators [2][NMAT][kUT], A scales [SA][NMAT][4], B scales [SB][kPP][4]
+    static constexpr int ACC = 2 * NMAT * kUT;
+    static constexpr int SFA_COL = ACC;
+    static constexpr int SFB_COL = SFA_COL + SA * NMAT * 4;
+    static constexpr int TMEM_COLS = 512;
+    static_assert(SFB_COL + SB * kPP * 4 <= TMEM_COLS, "TMEM budget");
+    static_assert(SMEM <= kPxSmemLimit, "shared memory budget");
+    static_assert(K % (4 * kKS) == 0, "scale rows load in 16-byte groups of four stages");
+    static_assert(ASTAGE % 1024 == 0 && BSTAGE % 1024 == 0, "stage alignment");
+};
+
+struct PxArgs {
+    const int32_t *units;          // [unit][3]: expert, first slot, pairs
+    const int32_t *n_units;
+    const int32_t *perm;           // slot -> pair t * 16 + k
+    const float *w;                // routing weights by pair
+    const uint8_t *maps;           // per-expert weight tensor maps [expert][w1, w3, w2]
+    const k3mx_expert *experts;    // device table [896]
+    const uint8_t *b_atoms;        // B scale atoms of the pass's input [unit][KC][kPP][512]
+    uint8_t *h_planes;             // gate/up: h pieces [kPP][slots][F / 2]
+    uint8_t *h_atoms;              // gate/up: down's B scale atoms [unit][F / 128][kPP][512]
+    size_t slots;                  // 16 T: rows of one piece plane
+    float *y;                      // down: [T][D], accumulated
+    int *status;
+};
+
+struct PxHdr {
+    uint64_t afull[16], aempty[16], bfull[8], bempty[8], accf[2], acce[2], done;
+    uint32_t tmem;
+    int abort;
+};
+
+// SiTU-GLU for the prefill epilogue (Kimi K3 engine (c/kimi_k3.c),
+// "Architecture notes": 4 tanh(g/4) sigma(g) 25 tanh(u/25)) with the
+// hardware tanh (relative error about 2^-11), sigma(g) = (1 + tanh(g/2)) / 2
+__device__ __forceinline__ float tanh_hw(float v) {
+    float r;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+__device__ __forceinline__ float situ_fast(float g, float u) {
+    const float sg = 0.5f + 0.5f * tanh_hw(0.5f * g);
+    return (4.0f * tanh_hw(0.25f * g) * sg) * (25.0f * tanh_hw(u * 0.04f));
+}
+
+// The kPP pieces of 32 values held by one lane (v, column order): piece p
+// takes the scale 2^e that maps the largest remaining |v| into (3, 6] and the
+// nearest e2m1 code of every v / 2^e (hardware conversion, two columns per
+// byte, the even column in the low nibble); v keeps the exact residual.
+// words[p] are the piece's 16 packed bytes, scale[p] its ue8m0 byte (255
+// when the values hold Inf or NaN; 0, with nothing taken, below 2^-124).
+__device__ __forceinline__ void lane_pieces(float (&v)[32], uint4 (&words)[kPP], uint32_t (&scale)[kPP]) {
+#pragma unroll
+    for (int p = 0; p < kPP; p++) {
+        // the largest |v| (non-negative floats order as their bit patterns;
+        // Inf and NaN lie above every finite value)
+        uint32_t mb = 0;
+#pragma unroll
+        for (int j = 0; j < 32; j++) mb = max(mb, __float_as_uint(fabsf(v[j])));
+        const int E = (int)(mb >> 23) - 127;
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        uint32_t sb = 0;
+        if (E == 128) {
+            sb = 255;
+        } else if (E >= -124) {
+            const int e = (mb & 0x7FFFFFu) <= 0x400000u ? E - 2 : E - 1;   // max / 2^e in (3, 6]
+            const float down = exp2i(-e), up = exp2i(e);
+#pragma unroll
+            for (int j = 0; j < 16; j++) {
+                uint32_t byte, h2;
+                asm("{\n\t.reg .b8 t;\n\t"
+                    "cvt.rn.satfinite.e2m1x2.f32 t, %2, %3;\n\t"
+                    "cvt.u32.u8 %0, t;\n\t"
+                    "cvt.rn.f16x2.e2m1x2 %1, t;\n\t}"
+                    : "=r"(byte), "=r"(h2)
+                    : "f"(v[2 * j + 1] * down), "f"(v[2 * j] * down));
+                const float2 q = __half22float2(*reinterpret_cast<const __half2 *>(&h2));
+                v[2 * j] = fmaf(-q.x, up, v[2 * j]);             // exact
+                v[2 * j + 1] = fmaf(-q.y, up, v[2 * j + 1]);
+                w[j >> 2] |= (byte & 0xFFu) << (8 * (j & 3));
+            }
+            sb = (uint32_t)(e + 127);
+        }
+        words[p] = make_uint4(w[0], w[1], w[2], w[3]);
+        scale[p] = sb;
+    }
+}
+
+// byte of a unit's B scale atoms: stage c (128 columns), piece p, row n of
+// the unit, 32-column block kb % 4 of the stage
+__device__ __forceinline__ size_t atom_byte(int unit, int kc_total, int c, int p, int n, int kb4) {
+    return (((size_t)unit * kc_total + c) * kPP + p) * kAtomB + (size_t)(n & 31) * 16 + (n >> 5) * 4 + kb4;
+}
+
+// an item's unit and whether its expert's pointers are usable (16-byte
+// aligned; the maps of another expert are never used)
+struct PxItem {
+    int unit, mt, e, off, ntok;
+    bool ok;
+};
+template <int MT>
+__device__ __forceinline__ PxItem px_item(const PxArgs &a, long long item) {
+    PxItem r;
+    r.unit = (int)(item / MT);
+    r.mt = (int)(item % MT);
+    r.e = __ldg(a.units + 3 * r.unit);
+    r.off = __ldg(a.units + 3 * r.unit + 1);
+    r.ntok = __ldg(a.units + 3 * r.unit + 2);
+    const uint4 *q = reinterpret_cast<const uint4 *>(a.experts + r.e);
+    const uint4 v0 = __ldg(q), v1 = __ldg(q + 1), v2 = __ldg(q + 2);
+    r.ok = ((v0.x | v0.z | v1.x | v1.z | v2.x | v2.z) & 15u) == 0 && r.ntok >= 1 && r.ntok <= kUT;
+    return r;
+}
+__device__ __forceinline__ const uint8_t *px_scales(const PxArgs &a, int e, int m, int ph) {
+    // k3mx_expert fields in order: w1, s1, w3, s3, w2, s2
+    const unsigned long long *q = reinterpret_cast<const unsigned long long *>(a.experts + e);
+    return reinterpret_cast<const uint8_t *>(__ldg(q + (ph == 1 ? 5 : (m == 0 ? 1 : 3))));
+}
+
+__device__ __forceinline__ uint64_t l2_evict_normal_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+template <int PH>
+__global__ void __launch_bounds__(kPxThreads, 1)
+    k_px(const PxArgs a, const __grid_constant__ CUtensorMap bmap32, const __grid_constant__ CUtensorMap bmap64,
+         const __grid_constant__ CUtensorMap bmap96) {
+    using Sh = PxShape<PH>;
+    constexpr int NMAT = Sh::NMAT, KC = Sh::KC, MT = Sh::MT, G = Sh::G, SA = Sh::SA, SB = Sh::SB;
+    static_assert(SA <= 16 && SB <= 8, "barrier slots");
+
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    PxHdr *hd = reinterpret_cast<PxHdr *>(smem);
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t ar0 = sbase + 1024;                      // A ring [SA][ASTAGE]
+    const uint32_t br0 = ar0 + SA * Sh::ASTAGE;             // B ring [SB][BSTAGE]
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t afull0 = smem_addr(hd->afull), aempty0 = smem_addr(hd->aempty);
+    const uint32_t bfull0 = smem_addr(hd->bfull), bempty0 = smem_addr(hd->bempty);
+    const uint32_t accf0 = smem_addr(hd->accf), acce0 = smem_addr(hd->acce);
+    const uint32_t done = smem_addr(&hd->done);
+
+    if (tid == 0) {
+        for (int i = 0; i < SA; i++) {
+            mbar_init(afull0 + 8 * i, 1 + 32);     // producer's expect_tx + the scale loader's lanes
+            mbar_init(aempty0 + 8 * i, 1);
+        }
+        for (int i = 0; i < SB; i++) {
+            mbar_init(bfull0 + 8 * i, 1);
+            mbar_init(bempty0 + 8 * i, 1);
+        }
+        for (int i = 0; i < 2; i++) {
+            mbar_init(accf0 + 8 * i, 1);
+            mbar_init(acce0 + 8 * i, kEpiThreads);
+        }
+        mbar_init(done, 1);
+        hd->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaW) tmem_alloc(smem_addr(&hd->tmem), Sh::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = hd->tmem;
+    volatile int *abort_flag = &hd->abort;
+    // gate/up reads the prep kernels' results everywhere; down reads gate/up's
+    // h only in the B producer (the weights and work units were ready before
+    // gate/up started), so its weight stream starts as gate/up CTAs retire
+    if (PH == 0) pdl_wait();
+    pdl_launch_dependents();
+
+    // Items are dealt round robin (item = CTA + k * grid): at any time the
+    // CTAs work on a few consecutive units, so each unit's activation rows
+    // come from HBM once and from L2 for its other row tiles.
+    const long long items = (long long)__ldg(a.n_units) * MT;
+    const long long i0 = blockIdx.x, istep = gridDim.x;
+    auto fail = [&](int detail) {
+        report_status(a.status, kStatusWaitTimeout, detail);
+        *abort_flag = 1;
+    };
+
+    if (warp == kAProd) {
+        // ------------------------------------------------- A producer --
+        const uint64_t pol = l2_evict_first_policy();       // weights: read once
+        uint32_t sa = 0;
+        int cur_e = -1;
+        const uint8_t *map0 = nullptr, *map1 = nullptr;
+        for (long long item = i0; item < items && !*abort_flag; item += istep) {
+            const PxItem it = px_item<MT>(a, item);
+            if (!it.ok) {
+                if (lane == 0 && it.mt == 0) report_status(a.status, kStatusBadPointer, it.e);
+                continue;
+            }
+            if (it.e != cur_e) {
+                const uint8_t *em = a.maps + (size_t)it.e * kMapsPerExpert * kMapBytes;
+                map0 = em + (PH == 0 ? 0 : 2) * kMapBytes;
+                map1 = em + 1 * kMapBytes;
+                if (lane == 0) {
+                    acquire_map(map0);
+                    if (NMAT == 2) acquire_map(map1);
+                }
+                cur_e = it.e;
+            }
+            bool ok = true;
+            for (int c = 0; c < KC; c++, sa++) {
+                const int s = sa % SA;
+                if (!mbar_wait(aempty0 + 8 * s, ((sa / SA) & 1) ^ 1)) {
+                    if (lane == 0) fail(300 + PH);
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    const uint32_t dst = ar0 + s * Sh::ASTAGE;
+                    mbar_arrive_expect_tx(afull0 + 8 * s, NMAT * kATile);
+                    tma_2d(dst, map0, c * 64, it.mt * 128, afull0 + 8 * s, pol);
+                    if (NMAT == 2) tma_2d(dst + kATile, map1, c * 64, it.mt * 128, afull0 + 8 * s, pol);
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+        }
+    } else if (warp == kSfW) {
+        // ----------------------------------------------- scale loader --
+        // Each weight row's scale bytes load 16 at a time (four stages) into
+        // registers two groups ahead; per stage, lane l writes line l of
+        // each matrix's atom: rows l, l + 32, l + 64, l + 96, four bytes each
+        constexpr int NG = KC / 4;                            // 16-byte groups per row
+        uint4 cur[NMAT][4], n1[NMAT][4], n2[NMAT][4];
+        // the group sequence: (item, group) for every item of the range
+        auto advance = [&](long long &item, int &g) -> bool {
+            if (++g == NG) {
+                g = 0;
+                item += istep;
+            }
+            return item < items;
+        };
+        auto load_group = [&](long long item, int g, uint4 (&dst)[NMAT][4]) {
+            const PxItem it = px_item<MT>(a, item);
+            if (!it.ok) return;
+#pragma unroll
+            for (int m = 0; m < NMAT; m++) {
+                const uint8_t *base = px_scales(a, it.e, m, PH) + (size_t)(it.mt * 128 + lane) * G + 16 * g;
+#pragma unroll
+                for (int i = 0; i < 4; i++)
+                    dst[m][i] = __ldg(reinterpret_cast<const uint4 *>(base + (size_t)32 * i * G));
+            }
+        };
+        long long la_item = i0;
+        int la_g = 0;
+        bool have2 = la_item < items;
+        if (have2) load_group(la_item, la_g, cur);
+        have2 = have2 && advance(la_item, la_g);
+        if (have2) load_group(la_item, la_g, n1);
+        have2 = have2 && advance(la_item, la_g);
+        if (have2) load_group(la_item, la_g, n2);
+        uint32_t sa = 0;
+        for (long long item = i0; item < items && !*abort_flag; item += istep) {
+            const PxItem it = px_item<MT>(a, item);
+            bool ok = true;
+            for (int g = 0; g < NG && ok; g++) {
+                if (it.ok) {
+#pragma unroll
+                    for (int j = 0; j < 4; j++) {
+                        const int s = (int)(sa % SA);
+                        if (!mbar_wait(aempty0 + 8 * s, ((sa / SA) & 1) ^ 1)) {
+                            if (lane == 0) fail(310 + PH);
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t at0 = ar0 + s * Sh::ASTAGE + NMAT * kATile;
+#pragma unroll
+                        for (int m = 0; m < NMAT; m++) {
+                            const uint32_t w0 = j == 0 ? cur[m][0].x : j == 1 ? cur[m][0].y : j == 2 ? cur[m][0].z : cur[m][0].w;
+                            const uint32_t w1 = j == 0 ? cur[m][1].x : j == 1 ? cur[m][1].y : j == 2 ? cur[m][1].z : cur[m][1].w;
+                            const uint32_t w2 = j == 0 ? cur[m][2].x : j == 1 ? cur[m][2].y : j == 2 ? cur[m][2].z : cur[m][2].w;
+                            const uint32_t w3 = j == 0 ? cur[m][3].x : j == 1 ? cur[m][3].y : j == 2 ? cur[m][3].z : cur[m][3].w;
+                            sts128(at0 + m * kAtomB + 16 * lane, drop_nan_scales(w0), drop_nan_scales(w1),
+                                   drop_nan_scales(w2), drop_nan_scales(w3));
+                        }
+                        fence_async_smem();
+                        mbar_arrive(afull0 + 8 * s);
+                        sa++;
+                    }
+                }
+                // rotate the register groups and load two ahead
+#pragma unroll
+                for (int m = 0; m < NMAT; m++)
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        cur[m][i] = n1[m][i];
+                        n1[m][i] = n2[m][i];
+                    }
+                if (have2) {
+                    have2 = advance(la_item, la_g);
+                    if (have2) load_group(la_item, la_g, n2);
+                }
+            }
+            if (!ok) break;
+        }
+    } else if (warp == kBProd) {
+        // ------------------------------------------------- B producer --
+        if (PH == 1) pdl_wait();                               // h of every pair is written
+        const uint64_t pol = l2_evict_normal_policy();
+        uint32_t sb = 0;
+        for (long long item = i0; item < items && !*abort_flag; item += istep) {
+            const PxItem it = px_item<MT>(a, item);
+            if (!it.ok) continue;
+            const int hsel = b_sel(it.ntok);
+            const void *bm = hsel == 0 ? (const void *)&bmap32 : hsel == 1 ? (const void *)&bmap64 : (const void *)&bmap96;
+            const int rows = b_rows(hsel);
+            bool ok = true;
+            for (int c = 0; c < KC; c++, sb++) {
+                const int s = sb % SB;
+                if (!mbar_wait(bempty0 + 8 * s, ((sb / SB) & 1) ^ 1)) {
+                    if (lane == 0) fail(320 + PH);
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    const uint32_t dst = br0 + s * Sh::BSTAGE;
+                    const uint32_t bf = bfull0 + 8 * s;
+                    mbar_arrive_expect_tx(bf, (uint32_t)(kPP * rows * 64 + kPP * kAtomB));
+                    // pieces land `rows` rows apart: [piece][rows][64 B]
+                    tma_3d(dst, bm, c * 64, it.off, 0, bf, pol);
+                    bulk_g2s(dst + kPP * kBPiece, a.b_atoms + ((size_t)it.unit * KC + c) * kPP * kAtomB,
+                             kPP * kAtomB, bf, pol);
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+        }
+    } else if (warp == kMmaW) {
+        // ------------------------------------------------- MMA issuer --
+        if (lane == 0) {
+            uint32_t sa = 0, sb = 0, itn = 0;
+            bool run = true;
+            for (long long item = i0; item < items && run && !*abort_flag; item += istep) {
+                const PxItem it = px_item<MT>(a, item);
+                if (!it.ok) continue;
+                const int npad = (it.ntok + 15) & ~15;
+                const uint32_t id0 = idesc_mxf4(npad, 0), id1 = idesc_mxf4(npad, 2);
+                const uint32_t pstride =
+                    64u * (uint32_t)b_rows(b_sel(it.ntok));
+                const int b = itn & 1;
+                if (!mbar_wait(acce0 + 8 * b, ((itn >> 1) & 1) ^ 1)) {
+                    fail(330 + PH);
+                    break;
+                }
+                tc_fence_after();
+                for (int c = 0; c < KC; c++, sa++, sb++) {
+                    const int s_a = sa % SA, s_b = sb % SB;
+                    if (!mbar_wait(afull0 + 8 * s_a, (sa / SA) & 1) || !mbar_wait(bfull0 + 8 * s_b, (sb / SB) & 1)) {
+                        fail(340 + PH);
+                        run = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t ast = ar0 + s_a * Sh::ASTAGE, bst = br0 + s_b * Sh::BSTAGE;
+                    const uint32_t sfa = tmem + Sh::SFA_COL + s_a * NMAT * 4;
+                    const uint32_t sfb = tmem + Sh::SFB_COL + s_b * kPP * 4;
+#pragma unroll
+                    for (int m = 0; m < NMAT; m++)
+                        tmem_cp_atom(sfa + m * 4, desc_atom(ast + NMAT * kATile + m * kAtomB, 128));
+#pragma unroll
+                    for (int p = 0; p < kPP; p++)
+                        tmem_cp_atom(sfb + p * 4, desc_atom(bst + kPP * kBPiece + p * kAtomB, 128));
+#pragma unroll
+                    for (int m = 0; m < NMAT; m++)
+#pragma unroll
+                        for (int ks = 0; ks < 2; ks++)
+#pragma unroll
+                            for (int p = 0; p < kPP; p++)
+                                mma_mxf4(tmem + (b * NMAT + m) * kUT, desc_sw64(ast + m * kATile + 32 * ks),
+                                         desc_sw64(bst + p * pstride + 32 * ks), ks ? id1 : id0, sfa + m * 4,
+                                         sfb + p * 4, (c | ks | p) != 0 ? 1u : 0u);
+                    umma_commit(aempty0 + 8 * s_a);
+                    umma_commit(bempty0 + 8 * s_b);
+                }
+                if (!run) break;
+                umma_commit(accf0 + 8 * b);
+                itn++;
+            }
+            umma_commit(done);
+        }
+        __syncwarp();
+    } else {
+        // --------------------------------------------------- epilogue --
+        const int q4 = warp & 3, half = (warp - kEpi0) >> 2;
+        (void)half;
+        const int row_in_tile = 32 * q4 + lane;
+        const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+        uint32_t itn = 0;
+        for (long long item = i0; item < items && !*abort_flag; item += istep) {
+            const PxItem it = px_item<MT>(a, item);
+            if (!it.ok) continue;
+            const int b = itn & 1;
+            if (!mbar_wait(accf0 + 8 * b, (itn >> 1) & 1)) {
+                if (lane == 0) fail(350 + PH);
+                break;
+            }
+            tc_fence_after();
+            const int n0 = half * (kUT / 2), n1 = min(it.ntok, n0 + kUT / 2);
+            const int row = it.mt * 128 + row_in_tile;
+            if (PH == 0) {
+                // rounds of 32 tokens (this warp: rounds half, half + 2, ...):
+                // h of the warp's 32 features x 32 tokens through shared
+                // memory, then each lane splits one token's 32 features
+                const int kb = it.mt * 4 + q4;                   // the warp's 32-feature block of h
+                float *tile = reinterpret_cast<float *>(smem + 1024 + SA * Sh::ASTAGE + SB * Sh::BSTAGE) +
+                              (warp - kEpi0) * 32 * 33;
+                const size_t plane = a.slots * (kF / 2);
+                for (int nb = 32 * half; nb < it.ntok; nb += 64) {
+#pragma unroll
+                    for (int hh = 0; hh < 2; hh++) {
+                        uint32_t gv[16], uv[16];
+                        tmem_ld16(tmem + lane_base + (uint32_t)(b * 2 + 0) * kUT + nb + 16 * hh, gv);
+                        tmem_ld16(tmem + lane_base + (uint32_t)(b * 2 + 1) * kUT + nb + 16 * hh, uv);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 16; j++)
+                            tile[(16 * hh + j) * 33 + lane] = situ_fast(__uint_as_float(gv[j]), __uint_as_float(uv[j]));
+                    }
+                    __syncwarp();
+                    float v[32];
+#pragma unroll
+                    for (int f = 0; f < 32; f++) v[f] = tile[lane * 33 + f];
+                    __syncwarp();
+                    const int n = nb + lane;
+                    if (n < it.ntok) {
+                        uint4 wds[kPP];
+                        uint32_t sc[kPP];
+                        lane_pieces(v, wds, sc);
+                        uint8_t *dst = a.h_planes + ((size_t)it.off + n) * (kF / 2) + (size_t)kb * 16;
+#pragma unroll
+                        for (int p = 0; p < kPP; p++) {
+                            *reinterpret_cast<uint4 *>(dst + p * plane) = wds[p];
+                            a.h_atoms[atom_byte(it.unit, kF / kKS, it.mt, p, n, q4)] = (uint8_t)sc[p];
+                        }
+                    }
+                }
+            } else {
+                for (int nb = n0; nb < n1; nb += 16) {
+                    uint32_t dv[16];
+                    tmem_ld16(tmem + lane_base + (uint32_t)b * kUT + nb, dv);
+                    tmem_ld_wait();
+                    const int nn = min(16, n1 - nb);
+                    for (int j = 0; j < nn; j++) {
+                        const int pair = __ldg(a.perm + it.off + nb + j);
+                        atomicAdd(a.y + (size_t)(pair / kK) * kD + row, __ldg(a.w + pair) * __uint_as_float(dv[j]));
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(acce0 + 8 * b);
+            itn++;
+        }
+    }
+
+    __syncthreads();
+    if (warp == kMmaW) {
+        // no MMA may still be running when TMEM is released
+        if (!mbar_wait(done, 0) && lane == 0) report_status(a.status, kStatusWaitTimeout, 360 + PH);
+        tc_fence_after();
+        tmem_dealloc(tmem, Sh::TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------ preparation --
+
+// Work units: every active expert's pairs cut into ceil(n / kUT) runs of
+// nearly equal length (one 1024-thread CTA, expert e on thread e).
+__global__ void __launch_bounds__(1024) k_px_units(const int32_t *counts, const int32_t *offsets,
+                                                   int32_t *units, int32_t *n_units) {
+    __shared__ int tmp[33];
+    const int e = threadIdx.x, lane = e & 31, wp = e >> 5;
+    const int cnt = e < kE ? counts[e] : 0;
+    const int nu = (cnt + kUT - 1) / kUT;
+    int incl = nu;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) tmp[wp] = incl;
+    __syncthreads();
+    if (wp == 0) {
+        const int ws = tmp[lane];
+        int wi = ws;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += v;
+        }
+        tmp[lane] = wi - ws;
+        if (lane == 31) tmp[32] = wi;
+    }
+    __syncthreads();
+    const int pos = incl - nu + tmp[wp];
+    if (e < kE && nu > 0) {
+        const int o0 = offsets[e];
+        for (int k = 0; k < nu; k++) {
+            const int lo = (int)((long long)cnt * k / nu), hi = (int)((long long)cnt * (k + 1) / nu);
+            units[3 * (pos + k) + 0] = e;
+            units[3 * (pos + k) + 1] = o0 + lo;
+            units[3 * (pos + k) + 2] = hi - lo;
+        }
+    }
+    if (e == 0) *n_units = tmp[32];
+}
+
+// CTAs below max_units: unit u's slots -> (unit, row) and each pair's slot;
+// the CTAs after them build the weight tensor maps of the expert table.
+__global__ void __launch_bounds__(256)
+k_px_slots(const int32_t *units, const int32_t *n_units, const int32_t *perm, int32_t *slot_un,
+           int32_t *slot_of_pair, int max_units, uint8_t *maps, const k3mx_expert *table,
+           const __grid_constant__ CUtensorMap w13, const __grid_constant__ CUtensorMap w2) {
+    if ((int)blockIdx.x < max_units) {
+        const int u = blockIdx.x;
+        if (u >= __ldg(n_units)) return;
+        const int off = units[3 * u + 1], ntok = units[3 * u + 2];
+        for (int n = threadIdx.x; n < ntok; n += blockDim.x) {
+            const int slot = off + n;
+            slot_un[slot] = (u << 8) | n;
+            slot_of_pair[perm[slot]] = slot;
+        }
+        return;
+    }
+    build_maps_cta(maps, kE, table, k3mx_expert{}, w13, w2, blockIdx.x - max_units);
+}
+
+// One thread per (token, 32-column block): x (bf16) -> kPP pieces, written
+// to the token's 16 slots (rows of the piece planes and bytes of the units'
+// B scale atoms); y of the token's block zeroed for the down pass's sums.
+__global__ void __launch_bounds__(256)
+k_px_xprep(const uint16_t *__restrict__ x, int n_tokens, const int32_t *__restrict__ slot_of_pair,
+           const int32_t *__restrict__ slot_un, uint8_t *__restrict__ planes, uint8_t *__restrict__ atoms,
+           size_t slots, float *__restrict__ y) {
+    constexpr int NB = kD / 32, KC = kD / kKS;
+    const long long w = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (w >= (long long)n_tokens * NB) return;
+    const int t = (int)(w / NB), kb = (int)(w % NB);
+    const size_t i0 = (size_t)t * kD + (size_t)kb * 32;
+    float v[32];
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + i0);
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        const uint4 u = __ldg(src + q);
+        const uint32_t ws[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            v[8 * q + 2 * k] = __uint_as_float(ws[k] << 16);
+            v[8 * q + 2 * k + 1] = __uint_as_float(ws[k] & 0xFFFF0000u);
+        }
+    }
+    float4 *yz = reinterpret_cast<float4 *>(y + i0);
+#pragma unroll
+    for (int q = 0; q < 8; q++) yz[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    uint4 wds[kPP];
+    uint32_t sc[kPP];
+    lane_pieces(v, wds, sc);
+#pragma unroll 4
+    for (int k = 0; k < kK; k++) {
+        const int slot = __ldg(slot_of_pair + (size_t)t * kK + k);
+        const int un = __ldg(slot_un + slot);
+        uint8_t *dst = planes + (size_t)slot * (kD / 2) + (size_t)kb * 16;
+#pragma unroll
+        for (int p = 0; p < kPP; p++) {
+            *reinterpret_cast<uint4 *>(dst + (size_t)p * slots * (kD / 2)) = wds[p];
+            atoms[atom_byte(un >> 8, KC, kb >> 2, p, un & 255, kb & 3)] = (uint8_t)sc[p];
+        }
+    }
+}
+
+// ------------------------------------------------------------- launchers --
+
+template <int PH>
+cudaError_t launch_px_t(const Ctx &c, const PxArgs &a, const CUtensorMap (&bmaps)[3], long long max_items) {
+    using Sh = PxShape<PH>;
+    static bool configured = false;
+    if (!configured) {
+        const cudaError_t e = cudaFuncSetAttribute(k_px<PH>, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    long long grid = c.num_sms;
+    if (grid > max_items) grid = max_items;
+    if (grid < 1) grid = 1;
+    return launch_pdl(k_px<PH>, dim3((unsigned)grid), dim3(kPxThreads), (size_t)Sh::SMEM, c.stream, a, bmaps[0],
+                      bmaps[1], bmaps[2]);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }
+    return fn;
+}
+
+// 2-D uint8 map: rows x row_bytes, boxes of box_rows x 64 bytes, 64-byte swizzle
+bool encode_sw64(CUtensorMap &m, const void *base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
+    auto enc = tmap_encoder();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {row_bytes, rows}, strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {64, box_rows}, es[2] = {1, 1};
+    return enc(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// weight map templates of the prefill path (128 rows x 64 B boxes), encoded
+// once per device over the library's scratch array (any address works for
+// a template; the device replaces it per expert)
+bool px_weight_templates(CUtensorMap &w13, CUtensorMap &w2) {
+    constexpr int kDevs = 64;
+    static int state[kDevs];
+    static CUtensorMap t13[kDevs], t2[kDevs];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) return false;
+    if (state[dev] == 0) {
+        state[dev] = 2;
+        void *base = library_scratch();
+        if (base != nullptr && library_scratch_bytes() >= (size_t)kD / 2 * kF &&
+            encode_sw64(t13[dev], base, kD / 2, kF, 128) && encode_sw64(t2[dev], base, kF / 2, kD, 128))
+            state[dev] = 1;
+    }
+    if (state[dev] != 1) return false;
+    w13 = t13[dev];
+    w2 = t2[dev];
+    return true;
+}
+
+// 3-D uint8 map over kPP planes of `rows` rows of row_bytes: boxes of 64
+// bytes x box_rows rows x kPP planes, 64-byte swizzle
+bool encode_planes(CUtensorMap &m, const void *base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
+    auto enc = tmap_encoder();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[3] = {row_bytes, rows, (cuuint64_t)kPP}, strides[2] = {row_bytes, row_bytes * rows};
+    const cuuint32_t box[3] = {64, box_rows, (cuuint32_t)kPP}, es[3] = {1, 1, 1};
+    return enc(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline size_t up256(size_t n) { return (n + 255) & ~size_t(255); }
+
+struct PxLayout {
+    size_t xplanes, hplanes, xatoms, hatoms, units, n_units, slot_un, slot_of_pair, maps, total;
+};
+PxLayout px_layout(int n_tokens) {
+    PxLayout L{};
+    const size_t S = (size_t)n_tokens * kK, U = (size_t)prefill_mx_max_units(n_tokens);
+    size_t o = 0;
+    auto take = [&](size_t b) {
+        const size_t at = o;
+        o += up256(b);
+        return at;
+    };
+    L.xplanes = take(kPP * S * (kD / 2));
+    L.hplanes = take(kPP * S * (kF / 2));
+    L.xatoms = take(U * (kD / kKS) * kPP * kAtomB);
+    L.hatoms = take(U * (kF / kKS) * kPP * kAtomB);
+    L.units = take(U * 3 * 4);
+    L.n_units = take(4);
+    L.slot_un = take(S * 4);
+    L.slot_of_pair = take(S * 4);
+    L.maps = take(expert_maps_bytes(kE));
+    L.total = o;
+    return L;
+}
+
+}  // namespace
+
+int prefill_mx_max_units(int n_tokens) {
+    const int pairs = n_tokens * kK;
+    return pairs / kUT + (pairs < kE ? pairs : kE);
+}
+
+size_t prefill_mx_scratch_bytes(int n_tokens) { return px_layout(n_tokens).total; }
+
+cudaError_t launch_prefill_mx(const Ctx &c, const PrefillArgs &p) {
+    const PxLayout L = px_layout(p.n_tokens);
+    char *ws = static_cast<char *>(p.scratch);
+    auto at = [&](size_t off) { return ws + off; };
+    const size_t S = (size_t)p.n_tokens * kK;
+    const int U = prefill_mx_max_units(p.n_tokens);
+    int32_t *units = reinterpret_cast<int32_t *>(at(L.units));
+    int32_t *n_units = reinterpret_cast<int32_t *>(at(L.n_units));
+    int32_t *slot_un = reinterpret_cast<int32_t *>(at(L.slot_un));
+    int32_t *slot_of_pair = reinterpret_cast<int32_t *>(at(L.slot_of_pair));
+    uint8_t *xplanes = reinterpret_cast<uint8_t *>(at(L.xplanes));
+    uint8_t *hplanes = reinterpret_cast<uint8_t *>(at(L.hplanes));
+    uint8_t *maps = reinterpret_cast<uint8_t *>(at(L.maps));
+
+    CUtensorMap w13, w2, xmap[3], hmap[3];
+    if (!px_weight_templates(w13, w2)) return cudaErrorNotSupported;
+    for (int i = 0; i < 3; i++)
+        if (!encode_planes(xmap[i], xplanes, kD / 2, S, b_rows(i)) ||
+            !encode_planes(hmap[i], hplanes, kF / 2, S, b_rows(i)))
+            return cudaErrorNotSupported;
+
+    cudaError_t err = traced("prefill_prep", c.stream, [&] {
+        k_px_units<<<1, 1024, 0, c.stream>>>(p.counts, p.offsets, units, n_units);
+        const int map_ctas = (kE * kMapsPerExpert + 7) / 8;
+        k_px_slots<<<(unsigned)(U + map_ctas), 256, 0, c.stream>>>(units, n_units, p.perm, slot_un, slot_of_pair, U,
+                                                                     maps, p.experts, w13, w2);
+        const long long threads = (long long)p.n_tokens * (kD / 32);
+        k_px_xprep<<<(unsigned)((threads + 255) / 256), 256, 0, c.stream>>>(
+            p.x, p.n_tokens, slot_of_pair, slot_un, xplanes, reinterpret_cast<uint8_t *>(at(L.xatoms)), S, p.y);
+        return cudaGetLastError();
+    });
+    if (err != cudaSuccess) return err;
+
+    PxArgs a{};
+    a.units = units;
+    a.n_units = n_units;
+    a.perm = p.perm;
+    a.w = p.w;
+    a.maps = maps;
+    a.experts = p.experts;
+    a.h_planes = hplanes;
+    a.h_atoms = reinterpret_cast<uint8_t *>(at(L.hatoms));
+    a.slots = S;
+    a.y = p.y;
+    a.status = c.status;
+    a.b_atoms = reinterpret_cast<const uint8_t *>(at(L.xatoms));
+    err = traced("prefill_gate_up", c.stream, [&] { return launch_px_t<0>(c, a, xmap, (long long)U * (kF / 128)); });
+    if (err != cudaSuccess) return err;
+    a.b_atoms = reinterpret_cast<const uint8_t *>(at(L.hatoms));
+    return traced("prefill_down", c.stream, [&] { return launch_px_t<1>(c, a, hmap, (long long)U * (kD / 128)); });
+}
+
+}  // namespace k3mx

@@ -63,8 +63,9 @@ def test_moe_refuses_bad_arguments():
                                        a["path"], a["io"], a["wo"], a["ws"], a["wsb"], None)
     assert call(args(ex=None)) == 1
     assert call(args(dt=2)) == 1                     # unknown dtype
-    assert call(args(path=3)) == 1                   # unknown path
+    assert call(args(path=4)) == 1                   # unknown path
     assert call(args(path=2)) == 1                   # prefill needs bf16 x
+    assert call(args(path=3)) == 1                   # so does the block-scaled prefill
     assert call(args(T=0)) == 3
     assert call(args(x=FAKE + 2)) == 2
     assert call(args(wsb=ws - 1)) == 4
@@ -78,7 +79,7 @@ def test_workspace_sizes():
     # the decode path keeps h and the per-pair outputs in fp32
     assert k3mx.k3mx_moe_workspace_size(64, 0, 1) >= 64 * 16 * (2 * 3072 + 3584) * 4
     # AUTO picks prefill for bf16 and many tokens; its h is f16
-    assert k3mx.k3mx_moe_workspace_size(4096, 1, 0) == k3mx.k3mx_moe_workspace_size(4096, 1, 2)
+    assert k3mx.k3mx_moe_workspace_size(4096, 1, 0) == k3mx.k3mx_moe_workspace_size(4096, 1, 3)
     assert k3mx.k3mx_moe_workspace_size(4096, 1, 2) >= 4096 * 16 * 3072 * 2
     assert k3mx.k3mx_moe_host_workspace_size(64, 1, 1) > k3mx.k3mx_moe_workspace_size(64, 1, 1)
     # g and u, then the MXFP4 pieces of x and h and the tensor-map slots

@@ -1,6 +1,8 @@
-"""The routed-expert layer on the prefill path (bf16 activations, grouped
-tcgen05 GEMMs) against the oracle.  Routing bit-exact; per sampled token the
-relative L2 error of y is at most 1e-2 (the bf16-activation tolerance)."""
+"""The routed-expert layer on the two prefill paths (bf16 activations,
+grouped tcgen05 GEMMs: weights dequantised to f16, or x and h as four MXFP4
+pieces on the block-scaled MMAs) against the oracle.  Routing bit-exact;
+per sampled token the relative L2 error of y is at most 1e-2 (the
+bf16-activation tolerance)."""
 import numpy as np
 import pytest
 import torch
@@ -13,16 +15,18 @@ from helpers import moe_oracle
 pytestmark = pytest.mark.gpu
 
 
-def run_prefill(dev, table, xb, logits, bias):
+PATHS = [pytest.param(k3mx.K3MX_PATH_PREFILL, id="f16"), pytest.param(k3mx.K3MX_PATH_PREFILL_MX, id="mx")]
+
+
+def run_prefill(dev, table, xb, logits, bias, path):
     T = xb.shape[0]
     x_t = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).to(dev)
     y = torch.full((T, 3584), float("nan"), dtype=torch.float32, device=dev)
     idx = torch.empty((T, 16), dtype=torch.int32, device=dev)
     w = torch.empty((T, 16), dtype=torch.float32, device=dev)
-    ws = torch.empty(k3mx.k3mx_moe_workspace_size(T, k3mx.K3MX_BF16, k3mx.K3MX_PATH_PREFILL),
-                     dtype=torch.uint8, device=dev)
+    ws = torch.empty(k3mx.k3mx_moe_workspace_size(T, k3mx.K3MX_BF16, path), dtype=torch.uint8, device=dev)
     k3mx.k3mx_moe_routed(y, x_t, table, torch.from_numpy(logits).to(dev), torch.from_numpy(bias).to(dev),
-                         ws, path=k3mx.K3MX_PATH_PREFILL, idx_out=idx, w_out=w)
+                         ws, path=path, idx_out=idx, w_out=w)
     st, det = k3mx.k3mx_device_status()
     assert st == 0, (st, det)
     return y.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy()
@@ -37,7 +41,8 @@ def check_tokens(y, x, ir, wr, tokens, what):
                for i, t in enumerate(tokens))
 
 
-def test_prefill_4096_tokens(arena, cuda_dev):
+@pytest.mark.parametrize("path", PATHS)
+def test_prefill_4096_tokens(arena, cuda_dev, path):
     """x bf16 [4096 x 3584] ~ N(0,1), top-16 of 896 with flat routing
     (about 73 tokens per expert)."""
     _, table = arena
@@ -46,7 +51,7 @@ def test_prefill_4096_tokens(arena, cuda_dev):
     x = synth.bf16_to_f32(xb)
     logits, _ = synth.router_inputs(T, seed=0)
     bias = np.zeros(896, np.float32)
-    y, idx, w = run_prefill(cuda_dev, table, xb, logits, bias)
+    y, idx, w = run_prefill(cuda_dev, table, xb, logits, bias, path)
     ir, wr = oracle.route(logits, bias)
     assert np.array_equal(idx, ir) and np.array_equal(w, wr)
     counts = np.bincount(ir.ravel(), minlength=896)
@@ -56,22 +61,25 @@ def test_prefill_4096_tokens(arena, cuda_dev):
     assert worst < 5e-3
 
 
-def test_prefill_small_batch_and_padding(arena, cuda_dev):
+@pytest.mark.parametrize("path", PATHS)
+def test_prefill_small_batch_and_padding(arena, cuda_dev, path):
     """300 tokens: about 5 tokens per expert, so every tile pads N to 16."""
     _, table = arena
     T = 300
     xb = synth.f32_to_bf16(synth.token_inputs(T, seed=4))
     x = synth.bf16_to_f32(xb)
     logits, bias = synth.router_inputs(T, seed=4)
-    y, idx, w = run_prefill(cuda_dev, table, xb, logits, bias)
+    y, idx, w = run_prefill(cuda_dev, table, xb, logits, bias, path)
     ir, wr = oracle.route(logits, bias)
     assert np.array_equal(idx, ir)
     check_tokens(y, x, ir, wr, [0, 150, 299], "prefill 300")
 
 
-def test_prefill_expert_with_more_than_128_tokens(arena, cuda_dev):
-    """200 tokens on the same 16 experts: each expert's list splits into a
-    128-token and a 72-token work unit."""
+@pytest.mark.parametrize("path", PATHS)
+def test_prefill_expert_with_more_than_128_tokens(arena, cuda_dev, path):
+    """200 tokens on the same 16 experts: each expert's list splits into
+    several work units (128 + 72 pairs on the f16 path, 3 x 66-67 on the
+    block-scaled path)."""
     _, table = arena
     T = 200
     xb = synth.f32_to_bf16(synth.token_inputs(T, seed=8))
@@ -79,8 +87,25 @@ def test_prefill_expert_with_more_than_128_tokens(arena, cuda_dev):
     logits, _ = synth.router_inputs(T, seed=8)
     bias = np.zeros(896, np.float32)
     logits[:, 300:316] += 8.0
-    y, idx, w = run_prefill(cuda_dev, table, xb, logits, bias)
+    y, idx, w = run_prefill(cuda_dev, table, xb, logits, bias, path)
     ir, wr = oracle.route(logits, bias)
     assert np.array_equal(idx, ir)
     assert np.all(np.bincount(ir.ravel(), minlength=896)[300:316] == T)
     check_tokens(y, x, ir, wr, [0, 127, 128, 199], "prefill skewed")
+
+
+def test_prefill_paths_agree(arena, cuda_dev):
+    """The two prefill paths on the same 1024 tokens: every token's outputs
+    agree to the sum of their error bounds (relative L2 within 2e-2), and
+    the default path for bf16 batches is the block-scaled one."""
+    _, table = arena
+    T = 1024
+    xb = synth.f32_to_bf16(synth.token_inputs(T, seed=12))
+    logits, bias = synth.router_inputs(T, seed=12)
+    a, _, _ = run_prefill(cuda_dev, table, xb, logits, bias, k3mx.K3MX_PATH_PREFILL)
+    b, _, _ = run_prefill(cuda_dev, table, xb, logits, bias, k3mx.K3MX_PATH_PREFILL_MX)
+    c, _, _ = run_prefill(cuda_dev, table, xb, logits, bias, k3mx.K3MX_PATH_AUTO)
+    rel = np.linalg.norm(a - b, axis=1) / np.linalg.norm(a, axis=1)
+    assert rel.max() <= 2e-2, rel.max()
+    relc = np.linalg.norm(c - b, axis=1) / np.linalg.norm(b, axis=1)
+    assert relc.max() <= 1e-5, relc.max()                 # same kernels; only the atomic order differs
