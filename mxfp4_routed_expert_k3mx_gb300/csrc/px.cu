@@ -79,8 +79,14 @@ template <int PH> struct PxShape {
     // into (token, feature)
     static constexpr int TRANS = PH == 0 ? 8 * 32 * 33 * 4 : 0;
     static constexpr int SMEM = 1024 + 1024 + SA * ASTAGE + SB * BSTAGE + TRANS;  // alignment slack, header
-    // TMEM: accumulators [2][NMAT][kUT], A scales [SA][NMAT][4], B scales [SB][kPP][4]
-    static constexpr int ACC = 2 * NMAT * kUT;
+    // Down puts two pieces side by side in one B operand (N = 2 x the box
+    // rows): MMAs per K step halve, and each accumulator holds an even-piece
+    // and an odd-piece half that the epilogue adds.  (Gate/up has no TMEM
+    // for the wider accumulators of two matrices.)
+    static constexpr bool PAIR = PH == 1;
+    static constexpr int NACC = PAIR ? 2 * kUT : kUT;         // accumulator columns per matrix
+    // TMEM: accumulators [2][NMAT][NACC], A scales [SA][NMAT][4], B scales [SB][kPP][4]
+    static constexpr int ACC = 2 * NMAT * NACC;
     static constexpr int SFA_COL = ACC;
     static constexpr int SFB_COL = SFA_COL + SA * NMAT * 4;
     static constexpr int TMEM_COLS = 512;
@@ -171,6 +177,16 @@ __device__ __forceinline__ void lane_pieces(float (&v)[32], uint4 (&words)[kPP],
 // the unit, 32-column block kb % 4 of the stage
 __device__ __forceinline__ size_t atom_byte(int unit, int kc_total, int c, int p, int n, int kb4) {
     return (((size_t)unit * kc_total + c) * kPP + p) * kAtomB + (size_t)(n & 31) * 16 + (n >> 5) * 4 + kb4;
+}
+
+// byte of the down pass's B scale atoms, pieces side by side: piece pair
+// p / 2 of stage c holds two atoms over the combined rows r = (p % 2) *
+// rows + n (rows = the unit's box height); atom r / 128, line r % 32,
+// column (r / 32) % 4
+__device__ __forceinline__ size_t atom_byte_pair(int unit, int kc_total, int c, int p, int n, int rows, int kb4) {
+    const int r = (p & 1) * rows + n;
+    return (((size_t)unit * kc_total + c) * (kPP / 2) + (p >> 1)) * (2 * kAtomB) + (size_t)(r >> 7) * kAtomB +
+           (size_t)(r & 31) * 16 + ((r >> 5) & 3) * 4 + kb4;
 }
 
 // an item's unit and whether its expert's pointers are usable (16-byte
@@ -422,9 +438,10 @@ __global__ void __launch_bounds__(kPxThreads, 1)
                 const PxItem it = px_item<MT>(a, item);
                 if (!it.ok) continue;
                 const int npad = (it.ntok + 15) & ~15;
-                const uint32_t id0 = idesc_mxf4(npad, 0), id1 = idesc_mxf4(npad, 2);
-                const uint32_t pstride =
-                    64u * (uint32_t)b_rows(b_sel(it.ntok));
+                const uint32_t pstride = 64u * (uint32_t)b_rows(b_sel(it.ntok));
+                // paired pieces: N covers two box heights (both pieces' rows)
+                const int nmma = Sh::PAIR ? 2 * b_rows(b_sel(it.ntok)) : npad;
+                const uint32_t id0 = idesc_mxf4(nmma, 0), id1 = idesc_mxf4(nmma, 2);
                 const int b = itn & 1;
                 if (!mbar_wait(acce0 + 8 * b, ((itn >> 1) & 1) ^ 1)) {
                     fail(330 + PH);
@@ -445,18 +462,23 @@ __global__ void __launch_bounds__(kPxThreads, 1)
 #pragma unroll
                     for (int m = 0; m < NMAT; m++)
                         tmem_cp_atom(sfa + m * 4, desc_atom(ast + NMAT * kATile + m * kAtomB, 128));
+                    // B scales: per piece one atom of 128 rows, or per piece
+                    // pair two atoms of 256 combined rows (4 columns each)
 #pragma unroll
                     for (int p = 0; p < kPP; p++)
                         tmem_cp_atom(sfb + p * 4, desc_atom(bst + kPP * kBPiece + p * kAtomB, 128));
+                    constexpr int NB = Sh::PAIR ? kPP / 2 : kPP;        // B operands per K step
 #pragma unroll
                     for (int m = 0; m < NMAT; m++)
 #pragma unroll
                         for (int ks = 0; ks < 2; ks++)
 #pragma unroll
-                            for (int p = 0; p < kPP; p++)
-                                mma_mxf4(tmem + (b * NMAT + m) * kUT, desc_sw64(ast + m * kATile + 32 * ks),
-                                         desc_sw64(bst + p * pstride + 32 * ks), ks ? id1 : id0, sfa + m * 4,
-                                         sfb + p * 4, (c | ks | p) != 0 ? 1u : 0u);
+                            for (int q = 0; q < NB; q++) {
+                                const int p0 = Sh::PAIR ? 2 * q : q;       // first piece of the operand
+                                mma_mxf4(tmem + (b * NMAT + m) * Sh::NACC, desc_sw64(ast + m * kATile + 32 * ks),
+                                         desc_sw64(bst + p0 * pstride + 32 * ks), ks ? id1 : id0, sfa + m * 4,
+                                         sfb + (Sh::PAIR ? 8 * q : 4 * q), (c | ks | q) != 0 ? 1u : 0u);
+                            }
                     umma_commit(aempty0 + 8 * s_a);
                     umma_commit(bempty0 + 8 * s_b);
                 }
@@ -490,6 +512,7 @@ __global__ void __launch_bounds__(kPxThreads, 1)
                 // h of the warp's 32 features x 32 tokens through shared
                 // memory, then each lane splits one token's 32 features
                 const int kb = it.mt * 4 + q4;                   // the warp's 32-feature block of h
+                const int hrows = b_rows(b_sel(it.ntok));         // the down pass's B box of this unit
                 float *tile = reinterpret_cast<float *>(smem + 1024 + SA * Sh::ASTAGE + SB * Sh::BSTAGE) +
                               (warp - kEpi0) * 32 * 33;
                 const size_t plane = a.slots * (kF / 2);
@@ -518,19 +541,24 @@ __global__ void __launch_bounds__(kPxThreads, 1)
 #pragma unroll
                         for (int p = 0; p < kPP; p++) {
                             *reinterpret_cast<uint4 *>(dst + p * plane) = wds[p];
-                            a.h_atoms[atom_byte(it.unit, kF / kKS, it.mt, p, n, q4)] = (uint8_t)sc[p];
+                            a.h_atoms[atom_byte_pair(it.unit, kF / kKS, it.mt, p, n, hrows, q4)] = (uint8_t)sc[p];
                         }
                     }
                 }
             } else {
+                // token n's sum: the even-piece column n plus the odd-piece
+                // column rows + n
+                const int rows = b_rows(b_sel(it.ntok));
                 for (int nb = n0; nb < n1; nb += 16) {
-                    uint32_t dv[16];
-                    tmem_ld16(tmem + lane_base + (uint32_t)b * kUT + nb, dv);
+                    uint32_t dv[16], dw[16];
+                    tmem_ld16(tmem + lane_base + (uint32_t)b * Sh::NACC + nb, dv);
+                    tmem_ld16(tmem + lane_base + (uint32_t)b * Sh::NACC + rows + nb, dw);
                     tmem_ld_wait();
                     const int nn = min(16, n1 - nb);
                     for (int j = 0; j < nn; j++) {
                         const int pair = __ldg(a.perm + it.off + nb + j);
-                        atomicAdd(a.y + (size_t)(pair / kK) * kD + row, __ldg(a.w + pair) * __uint_as_float(dv[j]));
+                        const float yv = __uint_as_float(dv[j]) + __uint_as_float(dw[j]);
+                        atomicAdd(a.y + (size_t)(pair / kK) * kD + row, __ldg(a.w + pair) * yv);
                     }
                 }
             }
