@@ -75,18 +75,21 @@ template <int PH> struct PxShape {
     static constexpr int KC = K / kKS, MT = M / 128, G = K / 32;
     static constexpr int ASTAGE = ((NMAT * (kATile + kAtomB)) + 1023) / 1024 * 1024;
     static constexpr int BSTAGE = kPP * kBPiece + kPP * kAtomB;          // 26 KB
-    // gate/up: per epilogue warp a 32 x 33 fp32 tile to turn (feature, token)
-    // into (token, feature)
-    static constexpr int TRANS = PH == 0 ? 8 * 32 * 33 * 4 : 0;
+    // gate/up: per epilogue warp two rounds of h, 32 tokens x 32 features
+    // in f16 (rows of 17 words: conflict-free both ways), to turn (feature,
+    // token) into (token, feature)
+    static constexpr int TROW = 68;
+    static constexpr int TRANS = PH == 0 ? 8 * 2 * 32 * TROW : 0;
     static constexpr int SMEM = 1024 + 1024 + SA * ASTAGE + SB * BSTAGE + TRANS;  // alignment slack, header
-    // Down puts two pieces side by side in one B operand (N = 2 x the box
-    // rows): MMAs per K step halve, and each accumulator holds an even-piece
-    // and an odd-piece half that the epilogue adds.  (Gate/up has no TMEM
-    // for the wider accumulators of two matrices.)
-    static constexpr bool PAIR = PH == 1;
-    static constexpr int NACC = PAIR ? 2 * kUT : kUT;         // accumulator columns per matrix
-    // TMEM: accumulators [2][NMAT][NACC], A scales [SA][NMAT][4], B scales [SB][kPP][4]
-    static constexpr int ACC = 2 * NMAT * NACC;
+    // Two pieces side by side in one B operand (N = 2 x the box rows): MMAs
+    // per K step halve, and each accumulator holds an even-piece and an
+    // odd-piece half that the epilogue adds.  Gate/up's two matrices leave
+    // TMEM for one accumulator buffer: its epilogue releases the buffer as
+    // soon as h is staged in shared memory.
+    static constexpr int NACC = 2 * kUT;                       // accumulator columns per matrix
+    static constexpr int NBUF = PH == 0 ? 1 : 2;
+    // TMEM: accumulators [NBUF][NMAT][NACC], A scales [SA][NMAT][4], B scales [SB][kPP][4]
+    static constexpr int ACC = NBUF * NMAT * NACC;
     static constexpr int SFA_COL = ACC;
     static constexpr int SFB_COL = SFA_COL + SA * NMAT * 4;
     static constexpr int TMEM_COLS = 512;
@@ -440,10 +443,11 @@ __global__ void __launch_bounds__(kPxThreads, 1)
                 const int npad = (it.ntok + 15) & ~15;
                 const uint32_t pstride = 64u * (uint32_t)b_rows(b_sel(it.ntok));
                 // paired pieces: N covers two box heights (both pieces' rows)
-                const int nmma = Sh::PAIR ? 2 * b_rows(b_sel(it.ntok)) : npad;
+                const int nmma = 2 * b_rows(b_sel(it.ntok));
+                (void)npad;
                 const uint32_t id0 = idesc_mxf4(nmma, 0), id1 = idesc_mxf4(nmma, 2);
-                const int b = itn & 1;
-                if (!mbar_wait(acce0 + 8 * b, ((itn >> 1) & 1) ^ 1)) {
+                const int b = itn % Sh::NBUF;
+                if (!mbar_wait(acce0 + 8 * b, ((itn / Sh::NBUF) & 1) ^ 1)) {
                     fail(330 + PH);
                     break;
                 }
@@ -467,17 +471,17 @@ __global__ void __launch_bounds__(kPxThreads, 1)
 #pragma unroll
                     for (int p = 0; p < kPP; p++)
                         tmem_cp_atom(sfb + p * 4, desc_atom(bst + kPP * kBPiece + p * kAtomB, 128));
-                    constexpr int NB = Sh::PAIR ? kPP / 2 : kPP;        // B operands per K step
+                    constexpr int NB = kPP / 2;                        // B operands per K step
 #pragma unroll
                     for (int m = 0; m < NMAT; m++)
 #pragma unroll
                         for (int ks = 0; ks < 2; ks++)
 #pragma unroll
                             for (int q = 0; q < NB; q++) {
-                                const int p0 = Sh::PAIR ? 2 * q : q;       // first piece of the operand
+                                const int p0 = 2 * q;                      // first piece of the operand
                                 mma_mxf4(tmem + (b * NMAT + m) * Sh::NACC, desc_sw64(ast + m * kATile + 32 * ks),
                                          desc_sw64(bst + p0 * pstride + 32 * ks), ks ? id1 : id0, sfa + m * 4,
-                                         sfb + (Sh::PAIR ? 8 * q : 4 * q), (c | ks | q) != 0 ? 1u : 0u);
+                                         sfb + 8 * q, (c | ks | q) != 0 ? 1u : 0u);
                             }
                     umma_commit(aempty0 + 8 * s_a);
                     umma_commit(bempty0 + 8 * s_b);
@@ -499,8 +503,8 @@ __global__ void __launch_bounds__(kPxThreads, 1)
         for (long long item = i0; item < items && !*abort_flag; item += istep) {
             const PxItem it = px_item<MT>(a, item);
             if (!it.ok) continue;
-            const int b = itn & 1;
-            if (!mbar_wait(accf0 + 8 * b, (itn >> 1) & 1)) {
+            const int b = itn % Sh::NBUF;
+            if (!mbar_wait(accf0 + 8 * b, (itn / Sh::NBUF) & 1)) {
                 if (lane == 0) fail(350 + PH);
                 break;
             }
@@ -508,31 +512,48 @@ __global__ void __launch_bounds__(kPxThreads, 1)
             const int n0 = half * (kUT / 2), n1 = min(it.ntok, n0 + kUT / 2);
             const int row = it.mt * 128 + row_in_tile;
             if (PH == 0) {
-                // rounds of 32 tokens (this warp: rounds half, half + 2, ...):
-                // h of the warp's 32 features x 32 tokens through shared
-                // memory, then each lane splits one token's 32 features
+                // Rounds of 32 tokens (this warp: tokens 32 half + 64 k ...).
+                // First every round's h (g and u: even-piece plus odd-piece
+                // columns) into the warp's f16 tiles, then the accumulator is
+                // released, then each lane splits one token's 32 features.
                 const int kb = it.mt * 4 + q4;                   // the warp's 32-feature block of h
-                const int hrows = b_rows(b_sel(it.ntok));         // the down pass's B box of this unit
-                float *tile = reinterpret_cast<float *>(smem + 1024 + SA * Sh::ASTAGE + SB * Sh::BSTAGE) +
-                              (warp - kEpi0) * 32 * 33;
+                const int hrows = b_rows(b_sel(it.ntok));         // the unit's B box height
+                uint8_t *tiles = smem + 1024 + SA * Sh::ASTAGE + SB * Sh::BSTAGE + (warp - kEpi0) * 2 * 32 * Sh::TROW;
                 const size_t plane = a.slots * (kF / 2);
-                for (int nb = 32 * half; nb < it.ntok; nb += 64) {
+                int nr = 0;
+                for (int nb = 32 * half; nb < it.ntok; nb += 64, nr++) {
+                    uint8_t *tile = tiles + nr * 32 * Sh::TROW;
 #pragma unroll
                     for (int hh = 0; hh < 2; hh++) {
-                        uint32_t gv[16], uv[16];
-                        tmem_ld16(tmem + lane_base + (uint32_t)(b * 2 + 0) * kUT + nb + 16 * hh, gv);
-                        tmem_ld16(tmem + lane_base + (uint32_t)(b * 2 + 1) * kUT + nb + 16 * hh, uv);
+                        uint32_t g0[16], g1[16], u0[16], u1[16];
+                        const uint32_t cg = tmem + lane_base + (uint32_t)nb + 16 * hh, cu = cg + Sh::NACC;
+                        tmem_ld16(cg, g0);
+                        tmem_ld16(cg + hrows, g1);
+                        tmem_ld16(cu, u0);
+                        tmem_ld16(cu + hrows, u1);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int j = 0; j < 16; j++)
-                            tile[(16 * hh + j) * 33 + lane] = situ_fast(__uint_as_float(gv[j]), __uint_as_float(uv[j]));
+                        for (int j = 0; j < 16; j++) {
+                            const float g = __uint_as_float(g0[j]) + __uint_as_float(g1[j]);
+                            const float u = __uint_as_float(u0[j]) + __uint_as_float(u1[j]);
+                            *reinterpret_cast<__half *>(tile + (16 * hh + j) * Sh::TROW + 2 * lane) =
+                                __float2half_rn(situ_fast(g, u));
+                        }
                     }
-                    __syncwarp();
+                }
+                tc_fence_before();
+                mbar_arrive(acce0 + 8 * b);
+                __syncwarp();
+                for (int r = 0; r < nr; r++) {
+                    const int n = 32 * half + 64 * r + lane;
+                    const uint8_t *row = tiles + (r * 32 + lane) * Sh::TROW;
                     float v[32];
 #pragma unroll
-                    for (int f = 0; f < 32; f++) v[f] = tile[lane * 33 + f];
-                    __syncwarp();
-                    const int n = nb + lane;
+                    for (int wd = 0; wd < 16; wd++) {
+                        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(row + 4 * wd));
+                        v[2 * wd] = f.x;
+                        v[2 * wd + 1] = f.y;
+                    }
                     if (n < it.ntok) {
                         uint4 wds[kPP];
                         uint32_t sc[kPP];
@@ -545,6 +566,7 @@ __global__ void __launch_bounds__(kPxThreads, 1)
                         }
                     }
                 }
+                __syncwarp();
             } else {
                 // token n's sum: the even-piece column n plus the odd-piece
                 // column rows + n
@@ -552,7 +574,7 @@ __global__ void __launch_bounds__(kPxThreads, 1)
                 for (int nb = n0; nb < n1; nb += 16) {
                     uint32_t dv[16], dw[16];
                     tmem_ld16(tmem + lane_base + (uint32_t)b * Sh::NACC + nb, dv);
-                    tmem_ld16(tmem + lane_base + (uint32_t)b * Sh::NACC + rows + nb, dw);
+                    tmem_ld16(tmem + lane_base + (uint32_t)b * Sh::NACC + rows + nb, dw);   // NMAT = 1
                     tmem_ld_wait();
                     const int nn = min(16, n1 - nb);
                     for (int j = 0; j < nn; j++) {
@@ -562,8 +584,10 @@ __global__ void __launch_bounds__(kPxThreads, 1)
                     }
                 }
             }
-            tc_fence_before();
-            mbar_arrive(acce0 + 8 * b);
+            if (PH == 1) {
+                tc_fence_before();
+                mbar_arrive(acce0 + 8 * b);
+            }
             itn++;
         }
     }
@@ -645,8 +669,8 @@ k_px_slots(const int32_t *units, const int32_t *n_units, const int32_t *perm, in
 // B scale atoms); y of the token's block zeroed for the down pass's sums.
 __global__ void __launch_bounds__(256)
 k_px_xprep(const uint16_t *__restrict__ x, int n_tokens, const int32_t *__restrict__ slot_of_pair,
-           const int32_t *__restrict__ slot_un, uint8_t *__restrict__ planes, uint8_t *__restrict__ atoms,
-           size_t slots, float *__restrict__ y) {
+           const int32_t *__restrict__ slot_un, const int32_t *__restrict__ units, uint8_t *__restrict__ planes,
+           uint8_t *__restrict__ atoms, size_t slots, float *__restrict__ y) {
     constexpr int NB = kD / 32, KC = kD / kKS;
     const long long w = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (w >= (long long)n_tokens * NB) return;
@@ -674,11 +698,12 @@ k_px_xprep(const uint16_t *__restrict__ x, int n_tokens, const int32_t *__restri
     for (int k = 0; k < kK; k++) {
         const int slot = __ldg(slot_of_pair + (size_t)t * kK + k);
         const int un = __ldg(slot_un + slot);
+        const int rows = b_rows(b_sel(__ldg(units + 3 * (un >> 8) + 2)));
         uint8_t *dst = planes + (size_t)slot * (kD / 2) + (size_t)kb * 16;
 #pragma unroll
         for (int p = 0; p < kPP; p++) {
             *reinterpret_cast<uint4 *>(dst + (size_t)p * slots * (kD / 2)) = wds[p];
-            atoms[atom_byte(un >> 8, KC, kb >> 2, p, un & 255, kb & 3)] = (uint8_t)sc[p];
+            atoms[atom_byte_pair(un >> 8, KC, kb >> 2, p, un & 255, rows, kb & 3)] = (uint8_t)sc[p];
         }
     }
 }
@@ -823,7 +848,7 @@ cudaError_t launch_prefill_mx(const Ctx &c, const PrefillArgs &p) {
                                                                      maps, p.experts, w13, w2);
         const long long threads = (long long)p.n_tokens * (kD / 32);
         k_px_xprep<<<(unsigned)((threads + 255) / 256), 256, 0, c.stream>>>(
-            p.x, p.n_tokens, slot_of_pair, slot_un, xplanes, reinterpret_cast<uint8_t *>(at(L.xatoms)), S, p.y);
+            p.x, p.n_tokens, slot_of_pair, slot_un, units, xplanes, reinterpret_cast<uint8_t *>(at(L.xatoms)), S, p.y);
         return cudaGetLastError();
     });
     if (err != cudaSuccess) return err;
