@@ -27,8 +27,8 @@
 //               per stage, 2 K steps x kPP pieces x NMAT MMAs (M = 128,
 //               N = the unit's tokens rounded up to 16, K = 64)
 //   warp 3      B producer: one 3-D TMA per stage for all pieces of the
-//               unit's rows (box of 32, 64 or 96 rows) and one bulk copy of
-//               the stage's B scale atoms into a B ring
+//               unit's rows (box of 16, 32, ..., 96 rows) and one bulk copy
+//               of the stage's B scale atoms into a B ring
 //   warps 4-11  epilogue, two warps per TMEM lane quarter, each half the
 //               unit's tokens: gate/up h = SiTU(g, u) split into pieces
 //               (rows of the grouped h planes + the unit's B scale atoms for
@@ -52,9 +52,15 @@ constexpr int kUT = 96;                 // pairs per unit (MMA N <= 96)
 constexpr int kKS = 128;                // K columns per stage (64 packed bytes per row)
 constexpr int kATile = 128 * 64;        // A tile: 128 rows x 64 B
 constexpr int kBPiece = kUT * 64;       // one piece of the unit's B: 96 rows x 64 B
-__host__ __device__ constexpr int b_rows(int i) { return 32 * (i + 1); }   // B box heights: 32, 64, 96
+constexpr int kBoxes = kUT / 16;
+__host__ __device__ constexpr int b_rows(int i) { return 16 * (i + 1); }   // B box heights: 16, 32, ..., 96
 // the B box of a unit of n pairs: the smallest height holding them
-__host__ __device__ constexpr int b_sel(int n) { return n <= 32 ? 0 : n <= 64 ? 1 : 2; }
+__host__ __device__ constexpr int b_sel(int n) { return n <= 16 ? 0 : (n + 15) / 16 - 1; }
+
+// the B tensor maps of one pass, one per box height
+struct PxBMaps {
+    CUtensorMap m[kBoxes];
+};
 constexpr int kAtomB = 512;             // scale-factor atom: 32 lines x 16 B
 constexpr int kPxThreads = 12 * 32;
 constexpr int kAProd = 0, kSfW = 1, kMmaW = 2, kBProd = 3, kEpi0 = 4;
@@ -225,8 +231,7 @@ __device__ __forceinline__ uint64_t l2_evict_normal_policy() {
 
 template <int PH>
 __global__ void __launch_bounds__(kPxThreads, 1)
-    k_px(const PxArgs a, const __grid_constant__ CUtensorMap bmap32, const __grid_constant__ CUtensorMap bmap64,
-         const __grid_constant__ CUtensorMap bmap96) {
+    k_px(const PxArgs a, const __grid_constant__ PxBMaps bmaps) {
     using Sh = PxShape<PH>;
     constexpr int NMAT = Sh::NMAT, KC = Sh::KC, MT = Sh::MT, G = Sh::G, SA = Sh::SA, SB = Sh::SB;
     static_assert(SA <= 16 && SB <= 8, "barrier slots");
@@ -409,7 +414,7 @@ __global__ void __launch_bounds__(kPxThreads, 1)
             const PxItem it = px_item<MT>(a, item);
             if (!it.ok) continue;
             const int hsel = b_sel(it.ntok);
-            const void *bm = hsel == 0 ? (const void *)&bmap32 : hsel == 1 ? (const void *)&bmap64 : (const void *)&bmap96;
+            const void *bm = &bmaps.m[hsel];
             const int rows = b_rows(hsel);
             bool ok = true;
             for (int c = 0; c < KC; c++, sb++) {
@@ -711,7 +716,7 @@ k_px_xprep(const uint16_t *__restrict__ x, int n_tokens, const int32_t *__restri
 // ------------------------------------------------------------- launchers --
 
 template <int PH>
-cudaError_t launch_px_t(const Ctx &c, const PxArgs &a, const CUtensorMap (&bmaps)[3], long long max_items) {
+cudaError_t launch_px_t(const Ctx &c, const PxArgs &a, const PxBMaps &bmaps, long long max_items) {
     using Sh = PxShape<PH>;
     static bool configured = false;
     if (!configured) {
@@ -722,8 +727,7 @@ cudaError_t launch_px_t(const Ctx &c, const PxArgs &a, const CUtensorMap (&bmaps
     long long grid = c.num_sms;
     if (grid > max_items) grid = max_items;
     if (grid < 1) grid = 1;
-    return launch_pdl(k_px<PH>, dim3((unsigned)grid), dim3(kPxThreads), (size_t)Sh::SMEM, c.stream, a, bmaps[0],
-                      bmaps[1], bmaps[2]);
+    return launch_pdl(k_px<PH>, dim3((unsigned)grid), dim3(kPxThreads), (size_t)Sh::SMEM, c.stream, a, bmaps);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
@@ -834,11 +838,12 @@ cudaError_t launch_prefill_mx(const Ctx &c, const PrefillArgs &p) {
     uint8_t *hplanes = reinterpret_cast<uint8_t *>(at(L.hplanes));
     uint8_t *maps = reinterpret_cast<uint8_t *>(at(L.maps));
 
-    CUtensorMap w13, w2, xmap[3], hmap[3];
+    CUtensorMap w13, w2;
+    PxBMaps xmap, hmap;
     if (!px_weight_templates(w13, w2)) return cudaErrorNotSupported;
-    for (int i = 0; i < 3; i++)
-        if (!encode_planes(xmap[i], xplanes, kD / 2, S, b_rows(i)) ||
-            !encode_planes(hmap[i], hplanes, kF / 2, S, b_rows(i)))
+    for (int i = 0; i < kBoxes; i++)
+        if (!encode_planes(xmap.m[i], xplanes, kD / 2, S, b_rows(i)) ||
+            !encode_planes(hmap.m[i], hplanes, kF / 2, S, b_rows(i)))
             return cudaErrorNotSupported;
 
     cudaError_t err = traced("prefill_prep", c.stream, [&] {
