@@ -55,6 +55,13 @@ H_IMAGE_BYTES = 8 * 3072 // 2 + 3072
 GATE_UP_PARAMS = 2 * 3072 * 3584
 
 
+# the sources of each profiled kernel: a committed DRAM-traffic figure is
+# reported only while these are unchanged
+DECODE_SOURCES = ["mx.cu", "common.cuh", "pieces.cuh", "tc.cuh", "tmaps.cuh"]
+PREFILL_SOURCES = ["prefill.cu", "prefill.cuh", "common.cuh"]
+PREFILL_MX_SOURCES = ["px.cu", "prefill.cuh", "tc.cuh", "pieces.cuh", "common.cuh", "tmaps.cuh"]
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -381,7 +388,7 @@ def run_ours(args):
                      + pairs * (H_IMAGE_BYTES + 2 * F * 4))
     n_launch, ms_dom = tr.get(dom, (0, 0.0))
     achieved = dom_bytes / (ms_dom / max(1, n_launch) / 1e3) / 1e9 if n_launch else None
-    src_hash = kernel_source_hash(["mx.cu", "common.cuh", "pieces.cuh"])
+    src_hash = kernel_source_hash(DECODE_SOURCES)
     traffic = profiled_traffic(dom, primary.name, src_hash)
     launches = sum(KERNELS_PER_GROUP.get(k, 1) * v[0] for k, v in tr.items())
 
@@ -432,10 +439,8 @@ def run_ours(args):
             # prefill, 4096 bf16 tokens, flat routing: tcgen05 grouped GEMMs,
             # weights dequantised to f16 (PREFILL) or fed as stored to the
             # block-scaled MMAs with x and h as MXFP4 pieces (PREFILL_MX)
-            for wname, wpath, srcs in (("moe_prefill_4096", k3mx.K3MX_PATH_PREFILL,
-                                        ["prefill.cu", "prefill.cuh", "common.cuh"]),
-                                       ("moe_prefill_4096_mx", k3mx.K3MX_PATH_PREFILL_MX,
-                                        ["px.cu", "tc.cuh", "pieces.cuh", "common.cuh"])):
+            for wname, wpath, srcs in (("moe_prefill_4096", k3mx.K3MX_PATH_PREFILL, PREFILL_SOURCES),
+                                       ("moe_prefill_4096_mx", k3mx.K3MX_PATH_PREFILL_MX, PREFILL_MX_SOURCES)):
                 wl = Workload(wname, 4096, True, wpath)
                 r = time_workload(k3mx, wl, table, dev, max(3, args.steps // 4), args.warmup, None, flush)
                 ms = sum(r["ms"]) / len(r["ms"])

@@ -300,9 +300,6 @@ struct DecodeExperts {
     const int32_t *units, *n_units, *perm;
     int max_units;                // upper bound of *n_units
 };
-cudaError_t launch_decode_phase_a(const Ctx &c, const DecodeExperts &d, const float *x, float *gu);
-cudaError_t launch_decode_phase_b(const Ctx &c, const DecodeExperts &d, const float *gu,
-                                  float *stage);
 cudaError_t launch_combine(const Ctx &c, float *y, const float *stage, const float *w,
                            int n_tokens);
 
@@ -336,7 +333,6 @@ cudaError_t launch_mx_fused1(const Ctx &c, const DecodeExperts &d, const uint8_t
 // down: W2 h of every pair -> out [pair][D] (launched as a dependent of gate/up)
 cudaError_t launch_mx_down(const Ctx &c, const DecodeExperts &d, const uint8_t *himg, float *out,
                            uint8_t *maps);
-cudaError_t launch_bf16_to_f32(const Ctx &c, float *out, const uint16_t *in, size_t n);
 
 }  // namespace k3mx
 

@@ -13,13 +13,13 @@
 // one scaled group sum per row, and the CTA adds the G group sums of a row
 // in shared memory in a fixed order (deterministic).
 //
-// Expert kernels:
-//   phase A: rows j of W1 and W3 together, h_j = SiTU(g_j, u_j), fp32 h
-//   phase B: rows i of W2 times h, one fp32 output per (token, slot) pair
-//   combine: y_t = sum_k w_tk * out_(t,k) in slot order
-// Work items are (active expert, row tile), handed out in contiguous runs
-// so a CTA mostly stays on one expert; all tokens routed to an expert reuse
-// the weights it loaded (Kimi K3 engine (c/kimi_k3.c), "Chunked prefill").
+// The tensor-core GEMV (`k_mma`, GEMV mode) streams 16-row tiles through a
+// bulk-copy ring and runs mma.sync against the activation split into two
+// exact f16 pieces; `k_gemv` takes the shapes the streaming path does not.
+// The `k_mma` template also holds expert modes (gate/up and down over
+// grouped pairs); the layer runs its experts on the block-scaled kernels of
+// mx.cu, so only the GEMV mode is instantiated.  `k_combine` forms
+// y_t = sum_k w_tk * out_(t,k) in slot order for the batched decode passes.
 #include "common.cuh"
 
 namespace k3mx {
@@ -569,10 +569,6 @@ __global__ void k_combine(float *__restrict__ y, const float *__restrict__ out,
     reinterpret_cast<float4 *>(y + (size_t)t * kD)[c] = acc;
 }
 
-__global__ void k_bf16_to_f32(float *__restrict__ out, const uint16_t *__restrict__ in, size_t n) {
-    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i < n) out[i] = __uint_as_float((uint32_t)in[i] << 16);
-}
 
 int occupancy(const void *fn, int threads, size_t smem) {
     int n = 0;
@@ -581,18 +577,6 @@ int occupancy(const void *fn, int threads, size_t smem) {
     return n;
 }
 
-ExpertsDev make_dev(const DecodeExperts &d) {
-    ExpertsDev e{};
-    e.experts = d.experts;
-    e.units = d.units;
-    e.n_units = d.n_units;
-    e.perm = d.perm;
-    if (d.single) {
-        e.one = *d.single;
-        e.single = 1;
-    }
-    return e;
-}
 
 constexpr size_t kSmemBudget = 224 * 1024;
 
@@ -675,51 +659,12 @@ cudaError_t launch_gemv(const Ctx &c, float *y, const float *x, const uint8_t *p
     return cudaGetLastError();
 }
 
-// gate/up: W1 and W3 (3072 x 3584) as separate 16-row tiles, K over 14 warps
-// (8 groups each); writes g and u, [pair][2][F]
-cudaError_t launch_decode_phase_a(const Ctx &c, const DecodeExperts &d, const float *x, float *gu) {
-    MmaArgs a{};
-    a.d = make_dev(d);
-    a.rows = kF;
-    a.in = kD;
-    a.ncw = 14;
-    a.gpw = 8;
-    a.stages = stages_for(mma_smem_bytes(1, 1, 4, kD, 14, 8, 0), (size_t)16 * (kD / 2 + kD / 32));
-    a.xin = x;
-    a.out = gu;
-    const long long items = (long long)(d.single ? 1 : d.max_units) * 2 * (kF / 16);
-    return launch_mma<1, 1, 8, 4, kModeGateUp, 15 * 32>(c, a, items, false);
-}
-
-// down: W2 (3584 x 3072), 16-row tiles, K over 12 warps (8 groups each); the
-// activation is h = SiTU(g, u) formed while building the pieces
-cudaError_t launch_decode_phase_b(const Ctx &c, const DecodeExperts &d, const float *gu,
-                                  float *stage) {
-    MmaArgs a{};
-    a.d = make_dev(d);
-    a.rows = kD;
-    a.in = kF;
-    a.ncw = 12;
-    a.gpw = 8;
-    a.stages = stages_for(mma_smem_bytes(1, 1, 4, kF, 12, 8, 0), (size_t)16 * (kF / 2 + kF / 32));
-    a.xin = gu;
-    a.out = stage;
-    const long long items = (long long)(d.single ? 1 : d.max_units) * (kD / 16);
-    return launch_mma<1, 1, 8, 4, kModeDown, 13 * 32>(c, a, items, true);
-}
-
 cudaError_t launch_combine(const Ctx &c, float *y, const float *stage, const float *w,
                            int n_tokens) {
     const long long n4 = (long long)n_tokens * (kD / 4);
     const int threads = 256;
     return launch_pdl(k_combine, dim3((unsigned)((n4 + threads - 1) / threads)), dim3(threads), 0, c.stream, y,
                       stage, w, n_tokens);
-}
-
-cudaError_t launch_bf16_to_f32(const Ctx &c, float *out, const uint16_t *in, size_t n) {
-    const int threads = 256;
-    k_bf16_to_f32<<<(unsigned)((n + threads - 1) / threads), threads, 0, c.stream>>>(out, in, n);
-    return cudaGetLastError();
 }
 
 }  // namespace k3mx
