@@ -191,7 +191,10 @@ k3mx_status k3mx_moe_routed(float *y, const void *x, int x_dtype, int n_tokens,
  * k3mx_moe_routed with HOST activations, logits, bias and output: copies
  * x, logits and bias to the workspace, runs the layer, copies y back, and
  * waits for the stream.  Weights (experts) stay DEVICE-resident.  Host
- * buffers may be pageable; page-locked buffers copy faster.
+ * buffers may be pageable.  On the DECODE path, when all four buffers are
+ * page-locked, mapped into the device's address space and 16-byte aligned,
+ * the kernels read x, logits and bias and write y in place instead (no
+ * copies; the same results).
  *   workspace: >= k3mx_moe_host_workspace_size(...) bytes.
  */
 size_t k3mx_moe_host_workspace_size(int n_tokens, int x_dtype, int path);

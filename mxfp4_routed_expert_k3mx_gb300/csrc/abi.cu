@@ -87,6 +87,17 @@ bool expert_ok(const k3mx_expert *e) {
 
 k3mx_status from_cuda(cudaError_t err) { return err == cudaSuccess ? K3MX_OK : K3MX_ECUDA; }
 
+// the device address of a page-locked host buffer mapped into the device's
+// address space, or nullptr (pageable or unknown memory)
+const void *mapped_host(const void *p) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();                       // clear the sticky-free error state
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
 // ---------------------------------------------------------------- tracing --
 
 constexpr int kTracePool = 8192;
@@ -455,6 +466,20 @@ k3mx_status k3mx_moe_routed_host(float *y_host, const void *x_host, int x_dtype,
     Ctx c;
     k3mx_status st = device_ctx(reinterpret_cast<cudaStream_t>(stream), c);
     if (st != K3MX_OK) return st;
+    // Page-locked host buffers mapped into the device's address space are
+    // read and written in place by the decode kernels (over the CPU-GPU
+    // link); other buffers, and the prefill paths (whose y is summed with
+    // atomics), go through copies.
+    if (path == K3MX_PATH_DECODE) {
+        const void *xm = mapped_host(x_host), *lm = mapped_host(logits_host), *bm = mapped_host(bias_host);
+        void *ym = const_cast<void *>(mapped_host(y_host));
+        if (xm && lm && bm && ym && aligned16(xm) && aligned16(lm) && aligned16(bm) && aligned16(ym)) {
+            st = run_moe(c, static_cast<float *>(ym), xm, x_dtype, n_tokens, experts, static_cast<const float *>(lm),
+                         static_cast<const float *>(bm), path, nullptr, nullptr, workspace, L);
+            if (st != K3MX_OK) return st;
+            return cudaStreamSynchronize(c.stream) == cudaSuccess ? K3MX_OK : K3MX_ECUDA;
+        }
+    }
     const size_t xb = (size_t)n_tokens * kD * (x_dtype == K3MX_BF16 ? 2 : 4);
     void *x_dev = at<void>(workspace, L.x_in);
     float *logits_dev = at<float>(workspace, L.logits_in);

@@ -73,6 +73,25 @@ def test_decode_host_entry_matches_device_entry(arena, cuda_dev):
     assert np.array_equal(y_host.numpy(), y_dev)      # same kernels, deterministic
 
 
+@pytest.mark.parametrize("T", [1, 3])
+def test_decode_host_entry_in_place_buffers(arena, cuda_dev, T):
+    """All four host buffers page-locked (the kernels may use them in place)
+    and one of them pageable (copies): both equal the device entry bit for
+    bit."""
+    _, table = arena
+    x = synth.token_inputs(T, seed=17)
+    logits, bias = synth.router_inputs(T, seed=17)
+    y_dev, _, _ = run_moe(cuda_dev, table, torch.from_numpy(x), logits, bias, k3mx.K3MX_PATH_DECODE)
+    ws = torch.empty(k3mx.k3mx_moe_host_workspace_size(T, 0, 1), dtype=torch.uint8, device=cuda_dev)
+    for pageable_bias in (False, True):
+        y_host = torch.full((T, 3584), float("nan"), dtype=torch.float32).pin_memory()
+        b = torch.from_numpy(bias)
+        k3mx.k3mx_moe_routed_host(y_host, torch.from_numpy(x).pin_memory(), table,
+                                  torch.from_numpy(logits).pin_memory(), b if pageable_bias else b.pin_memory(),
+                                  ws, path=k3mx.K3MX_PATH_DECODE)
+        assert np.array_equal(y_host.numpy(), y_dev), pageable_bias
+
+
 def test_decode_is_deterministic(arena, cuda_dev):
     _, table = arena
     x = synth.token_inputs(5, seed=9)
