@@ -60,6 +60,7 @@ def _load():
             lib.orc_expert.argtypes = [vp] * 5 + [vp] + [vp] * 6 + [i, i]
             lib.orc_expert_bound.argtypes = [vp, vp, vp, vp] + [vp] * 6 + [i, i]
             lib.orc_route.argtypes = [vp, vp, vp, vp, vp, i, i, i, ctypes.c_float]
+            lib.orc_topp.argtypes = [vp, vp, vp, i, i, i, ctypes.c_float, ctypes.c_double]
             lib.orc_group.argtypes = [vp, vp, vp, vp, i, i, i]
             lib.orc_group.restype = i
             lib.orc_moe.argtypes = [vp, vp, i, vp, vp, vp, i, i, i, vp]
@@ -158,8 +159,20 @@ def route(logits, bias, k=16, routed_scale=1.0, return_scores=False):
     return (idx, w, s) if return_scores else (idx, w)
 
 
+def route_topp(logits, bias, p, k=16, routed_scale=1.0):
+    """route(), then the top-p truncation: of the k experts in order of
+    decreasing raw score (ties: lower index), keep the shortest prefix whose
+    scores reach p times their total; kept weights renormalised over the
+    kept scores; dropped slots get index -1 and weight 0 (p <= 0: all kept)."""
+    idx, w, s = route(logits, bias, k, routed_scale, return_scores=True)
+    T, E = s.shape
+    _load().orc_topp(_p(idx), _p(w), _p(s), T, E, k, routed_scale, float(p))
+    return idx, w
+
+
 def group(idx, n_experts=896):
-    """counts [E], offsets [E+1], perm [T*K] (stable by pair index t*K+k)."""
+    """counts [E], offsets [E+1], perm [sum(counts)] (stable by pair index
+    t*K+k); index -1 (a slot dropped by top-p) is not grouped."""
     idx = np.ascontiguousarray(idx, np.int32)
     T, K = idx.shape
     counts = np.empty(n_experts, np.int32)
@@ -168,7 +181,7 @@ def group(idx, n_experts=896):
     rc = _load().orc_group(_p(counts), _p(offsets), _p(perm), _p(idx), T, n_experts, K)
     if rc != 0:
         raise ValueError("expert index out of range")
-    return counts, offsets, perm
+    return counts, offsets, perm[:int(offsets[-1])]
 
 
 def moe(x, idx, w, experts):
@@ -180,7 +193,7 @@ def moe(x, idx, w, experts):
     T, D = x.shape
     K = idx.shape[1]
     assert D <= 8192
-    ids = sorted(set(int(e) for e in idx.ravel()))
+    ids = sorted(set(int(e) for e in idx.ravel() if e >= 0))     # -1: a slot dropped by top-p
     some = experts[ids[0]]
     F = some[0].shape[0]
     E = int(idx.max()) + 1

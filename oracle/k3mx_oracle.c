@@ -33,6 +33,10 @@
  *        routed_scale 1.0, moe_renorm 1, situ_b1 4.0, situ_b2 25.0.
  *   [P]  Kimi K3 engine (c/kimi_k3.c), "Chunked prefill": within a chunk every
  *        unique expert is loaded once for all the tokens that chose it.
+ *   [TP] Kimi K3 engine (c/kimi_k3.c), "Streaming design" (K3_TOPP) and the
+ *        environment table: optionally keep the routed experts only up to a
+ *        cumulative weight p, dropping the low-weight tail of the top-16 and
+ *        renormalising the rest (0 = off).
  *
  * Readings where the pages are silent (each listed in the design notes):
  *   - sigma is evaluated in double with libm exp and rounded to fp32 once;
@@ -44,6 +48,11 @@
  *   - g = W1 x and u = W3 x (W1 is the gate).  g and u are the fp32 outputs
  *     of the GEMV; h is evaluated in double and rounded to fp32.
  *   - tokens are grouped by expert with a stable order (token, slot).
+ *   - [TP]: the 16 are taken in order of decreasing raw score (ties: lower
+ *     expert index); an expert is kept while the scores before it sum to
+ *     less than p times the sum of all 16 (so the kept set is the shortest
+ *     prefix reaching p); kept weights are raw scores over the kept sum;
+ *     a dropped slot has index -1 and weight 0 and runs no expert.
  */
 #include <math.h>
 #include <stddef.h>
@@ -238,12 +247,51 @@ void orc_route(int32_t *idx, float *w, float *s_out, const float *logits,
  *                 expert in increasing p (stable).
  * Returns 0, or -1 if an index lies outside 0..E-1.
  */
+/* [TP] on the result of orc_route (idx, w and the scores s [T][E]): drops
+ * the low-weight tail of each token's K experts.  p <= 0 keeps all K.  The
+ * sums are of at most K floats in [2^-24, 1] (multiples of 2^-47 below 2^5),
+ * so every one is exact in double. */
+void orc_topp(int32_t *idx, float *w, const float *s, int T, int E, int K, float routed_scale, double p)
+{
+    if (p <= 0.0) return;
+    for (int t = 0; t < T; t++) {
+        int32_t *it = idx + (size_t)t * K;
+        float *wt = w + (size_t)t * K;
+        const float *st = s + (size_t)t * E;
+        double total = 0.0;
+        for (int k = 0; k < K; k++) total += (double)st[it[k]];
+        const double limit = p * total;
+        unsigned char keep[64];
+        double kept = 0.0;
+        for (int k = 0; k < K; k++) {
+            /* the scores ranked before slot k: larger, or equal with a lower index */
+            double before = 0.0;
+            for (int j = 0; j < K; j++) {
+                const float sj = st[it[j]], sk = st[it[k]];
+                if (sj > sk || (sj == sk && it[j] < it[k])) before += (double)sj;
+            }
+            keep[k] = before < limit;
+            if (keep[k]) kept += (double)st[it[k]];
+        }
+        for (int k = 0; k < K; k++) {
+            if (keep[k]) {
+                wt[k] = (float)((double)st[it[k]] / kept) * routed_scale;
+            } else {
+                it[k] = -1;
+                wt[k] = 0.0f;
+            }
+        }
+    }
+}
+
+/* Grouping ([P]): index -1 marks a slot dropped by [TP]; it is not grouped. */
 int orc_group(int32_t *counts, int32_t *offsets, int32_t *perm,
               const int32_t *idx, int T, int E, int K)
 {
     const long long n = (long long)T * K;
     for (int e = 0; e < E; e++) counts[e] = 0;
     for (long long p = 0; p < n; p++) {
+        if (idx[p] == -1) continue;
         if (idx[p] < 0 || idx[p] >= E) return -1;
         counts[idx[p]]++;
     }
@@ -253,6 +301,7 @@ int orc_group(int32_t *counts, int32_t *offsets, int32_t *perm,
     for (int e = 0; e < E; e++) counts[e] = 0;
     for (long long p = 0; p < n; p++) {
         const int e = idx[p];
+        if (e < 0) continue;
         perm[offsets[e] + counts[e]] = (int32_t)p;
         counts[e]++;
     }
@@ -277,6 +326,7 @@ void orc_moe(float *y, const float *x, int T, const uint8_t *const *ptrs,
         for (int i = 0; i < D; i++) acc[i] = 0.0;
         for (int k = 0; k < K; k++) {
             const int e = idx[(size_t)t * K + k];
+            if (e < 0) continue;                  /* dropped by [TP] */
             const uint8_t *const *p = ptrs + (size_t)6 * e;
             orc_expert(ye, NULL, NULL, NULL, tmp, x + (size_t)t * D,
                        p[0], p[1], p[2], p[3], p[4], p[5], D, F);

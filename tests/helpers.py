@@ -21,6 +21,8 @@ def moe_oracle(x, idx, w, tokens):
         bnd = np.zeros(x.shape[1])
         for k in range(idx.shape[1]):
             e = int(idx[t, k])
+            if e < 0:                                     # dropped by top-p
+                continue
             if e not in ex:
                 ex[e] = arena_expert(e)
             _, _, _, h = oracle.expert(x[t], *ex[e], intermediates=True)

@@ -364,3 +364,77 @@ def test_moe_is_weighted_sum_of_experts_tiny():
     y1 = oracle.moe(x, idx, w1, experts)
     assert np.array_equal(y1[0], oracle.expert(x[0], *experts[4]))
     assert np.array_equal(y1[1], oracle.expert(x[1], *experts[2]))
+
+
+# ------------------------------------------------------------ top-p routing --
+# K3_TOPP (Kimi K3 engine (c/kimi_k3.c), "Streaming design"; environment
+# table): keep the routed experts up to cumulative weight p, drop the
+# low-weight tail of the top-16 and renormalise the rest.
+
+def _topp_brute(logits, bias, p):
+    """The truncation from its definition on the full-precision route result:
+    sort the 16 by raw score (ties: lower index), keep the shortest prefix
+    whose scores reach p of their total, renormalise over the kept."""
+    idx, w, s = oracle.route(logits, bias, return_scores=True)
+    out_i, out_w = idx.copy(), w.copy()
+    for t in range(idx.shape[0]):
+        sc = [(float(s[t, e]), int(e)) for e in idx[t]]
+        order = sorted(range(16), key=lambda k: (-sc[k][0], sc[k][1]))
+        total = sum(v for v, _ in sc)
+        kept, cum = set(), 0.0
+        for k in order:
+            if cum < p * total:
+                kept.add(k)
+            cum += sc[k][0]
+        ks = sum(sc[k][0] for k in kept)
+        for k in range(16):
+            if k in kept:
+                out_w[t, k] = np.float32(sc[k][0] / ks)
+            else:
+                out_i[t, k], out_w[t, k] = -1, 0.0
+    return out_i, out_w
+
+
+def test_topp_matches_its_definition():
+    logits, bias = synth.router_inputs(40, seed=51)
+    for p in (0.3, 0.5, 0.8, 0.9, 0.99):
+        i1, w1 = oracle.route_topp(logits, bias, p)
+        i2, w2 = _topp_brute(logits, bias, p)
+        assert np.array_equal(i1, i2) and np.array_equal(w1, w2), p
+
+
+def test_topp_special_cases():
+    logits, bias = synth.router_inputs(12, seed=52)
+    i0, w0 = oracle.route(logits, bias)
+    for p in (0.0, -1.0, 1.0, 2.0):                   # off, and p >= 1 keeps everything
+        i, w = oracle.route_topp(logits, bias, p)
+        assert np.array_equal(i, i0) and np.array_equal(w, w0), p
+    i, w = oracle.route_topp(logits, bias, 1e-9)      # only the heaviest expert survives
+    assert np.all((i >= 0).sum(1) == 1)
+    assert np.all(w[i >= 0] == 1.0)
+    _, _, s = oracle.route(logits, bias, return_scores=True)
+    for t in range(12):                               # ... and it is the largest raw score
+        e = i[t][i[t] >= 0][0]
+        assert s[t, e] == s[t, i0[t]].max()
+
+
+def test_topp_invariants():
+    logits, bias = synth.router_inputs(64, seed=53)
+    for p in (0.4, 0.7, 0.95):
+        i, w = oracle.route_topp(logits, bias, p)
+        i0, _, s = oracle.route(logits, bias, return_scores=True)
+        kept = i >= 0
+        assert np.all(kept.sum(1) >= 1)
+        assert np.all(np.abs(w.sum(1, dtype=np.float64) - 1.0) <= 16 * 2.0 ** -24)
+        assert np.all(w[~kept] == 0.0)
+        assert np.array_equal(i[kept], i0[kept])      # kept slots keep their expert and place
+        for t in range(64):
+            ks = s[t, i[t][kept[t]]].astype(np.float64)
+            ds = s[t, i0[t][~kept[t]]].astype(np.float64)
+            tot = s[t, i0[t]].astype(np.float64).sum()
+            assert ks.sum() >= p * tot                        # the kept part reaches p
+            assert ks.sum() - ks.min() < p * tot              # and no kept expert is spare
+            if ds.size:
+                assert ds.max() <= ks.min()                   # only the lightest are dropped
+        counts, offsets, perm = oracle.group(i)
+        assert offsets[-1] == kept.sum() and len(perm) == kept.sum()
