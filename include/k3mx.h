@@ -135,14 +135,35 @@ k3mx_status k3mx_route_topk(int32_t *idx, float *w, const float *logits,
                             k3mx_stream_t stream);
 
 /*
+ * k3mx_route_topk followed by the top-p truncation (Kimi K3 engine
+ * (c/kimi_k3.c), "Streaming design": K3_TOPP keeps the routed experts up to
+ * a cumulative weight p, dropping the low-weight tail of the top-16 and
+ * renormalising the rest).  Per token, the 16 selected experts are taken in
+ * order of decreasing raw score s (ties: lower expert index); an expert is
+ * kept while the scores ahead of it sum to less than top_p times the sum of
+ * all 16 (the shortest prefix reaching top_p); a kept slot's weight is
+ * s / (sum of the kept scores) (double, rounded to fp32) * routed_scale; a
+ * dropped slot gets index -1 and weight 0 and keeps its place.  The sums
+ * are exact (scores in [2^-24, 1]) or slot-order double sums.
+ *   top_p: finite; top_p <= 0 keeps all 16 (the same result as
+ *          k3mx_route_topk), top_p >= 1 keeps all 16; NaN or Inf is
+ *          refused (K3MX_EINVAL).  Other arguments as k3mx_route_topk.
+ * Index results are bit-identical to a CPU evaluation in the same precision.
+ */
+k3mx_status k3mx_route_topp(int32_t *idx, float *w, const float *logits,
+                            const float *bias, int n_tokens, float top_p,
+                            k3mx_stream_t stream);
+
+/*
  * Token-to-expert grouping (Kimi K3 engine (c/kimi_k3.c), "Chunked prefill":
  * each unique expert of a chunk is loaded once for all its tokens):
  *   counts [896]          pairs routed to each expert
  *   offsets [897]         exclusive prefix sum of counts, offsets[896] = 16 T
  *   perm [16 T]           pair indices p = t*16 + k sorted by (expert, p)
- *   idx [n_tokens][16]    int32 expert ids in 0..895 (entries outside that
- *                         range are clamped out: they are not counted and
- *                         the device status reports K3MX_EINVAL)
+ *   idx [n_tokens][16]    int32 expert ids in 0..895, or -1 for a slot
+ *                         dropped by top-p (not grouped); other entries are
+ *                         clamped out: they are not counted and the device
+ *                         status reports K3MX_EINVAL
  * Bit-exact and deterministic.  workspace: device, 16-byte aligned,
  * >= k3mx_group_workspace_size(n_tokens) bytes.
  */
@@ -186,6 +207,18 @@ k3mx_status k3mx_moe_routed(float *y, const void *x, int x_dtype, int n_tokens,
                             int32_t *idx_out, float *w_out,
                             void *workspace, size_t ws_bytes,
                             k3mx_stream_t stream);
+
+/*
+ * k3mx_moe_routed with the top-p routing of k3mx_route_topp: dropped slots
+ * run no expert (idx_out -1, w_out 0).  top_p <= 0 or >= 1: the same result
+ * as k3mx_moe_routed.  Workspace: k3mx_moe_workspace_size(...).
+ */
+k3mx_status k3mx_moe_routed_topp(float *y, const void *x, int x_dtype, int n_tokens,
+                                 const k3mx_expert *experts, const float *logits,
+                                 const float *bias, int path, float top_p,
+                                 int32_t *idx_out, float *w_out,
+                                 void *workspace, size_t ws_bytes,
+                                 k3mx_stream_t stream);
 
 /*
  * k3mx_moe_routed with HOST activations, logits, bias and output: copies

@@ -64,10 +64,12 @@ def lib():
             "k3mx_expert_ffn_workspace_size": ([], sz),
             "k3mx_expert_ffn": ([vp, vp, ctypes.POINTER(Expert), vp, sz, vp], i),
             "k3mx_route_topk": ([vp, vp, vp, vp, i, vp], i),
+            "k3mx_route_topp": ([vp, vp, vp, vp, i, ctypes.c_float, vp], i),
             "k3mx_group_workspace_size": ([i], sz),
             "k3mx_group": ([vp, vp, vp, vp, i, vp, sz, vp], i),
             "k3mx_moe_workspace_size": ([i, i, i], sz),
             "k3mx_moe_routed": ([vp, vp, i, i, vp, vp, vp, i, vp, vp, vp, sz, vp], i),
+            "k3mx_moe_routed_topp": ([vp, vp, i, i, vp, vp, vp, i, ctypes.c_float, vp, vp, vp, sz, vp], i),
             "k3mx_moe_host_workspace_size": ([i, i, i], sz),
             "k3mx_moe_routed_host": ([vp, vp, i, i, vp, vp, vp, i, vp, sz, vp], i),
             "k3mx_moe_decode_noalloc": ([vp, vp, i, i, vp, vp, vp, vp, vp, vp], i),
@@ -167,6 +169,18 @@ def k3mx_route_topk(idx, w, logits, bias, stream=None):
     return idx, w
 
 
+def k3mx_route_topp(idx, w, logits, bias, top_p, stream=None):
+    """k3mx_route_topk with the top-p truncation (dropped slots: -1, 0)."""
+    _dev(idx, torch.int32, "idx")
+    _dev(w, torch.float32, "w")
+    _dev(logits, torch.float32, "logits")
+    _dev(bias, torch.float32, "bias")
+    T = logits.shape[0]
+    _check("k3mx_route_topp", lib().k3mx_route_topp(_ptr(idx), _ptr(w), _ptr(logits), _ptr(bias), T,
+                                                     float(top_p), _stream(stream)))
+    return idx, w
+
+
 def k3mx_group_workspace_size(n_tokens):
     return int(lib().k3mx_group_workspace_size(n_tokens))
 
@@ -209,6 +223,23 @@ def k3mx_moe_routed(y, x, experts, logits, bias, workspace, path=K3MX_PATH_AUTO,
     T = x.shape[0]
     _check("k3mx_moe_routed", lib().k3mx_moe_routed(
         _ptr(y), _ptr(x), _x_dtype(x), T, _ptr(experts), _ptr(logits), _ptr(bias), path,
+        _ptr(idx_out), _ptr(w_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+    return y
+
+
+def k3mx_moe_routed_topp(y, x, experts, logits, bias, workspace, top_p, path=K3MX_PATH_AUTO,
+                         idx_out=None, w_out=None, stream=None):
+    """k3mx_moe_routed with top-p routing: the low-weight tail of each
+    token's 16 experts is dropped and runs no expert."""
+    _dev(y, torch.float32, "y")
+    if not (x.is_cuda and x.is_contiguous()):
+        raise TypeError("x: contiguous CUDA tensor expected")
+    _dev(logits, torch.float32, "logits")
+    _dev(bias, torch.float32, "bias")
+    T = x.shape[0]
+    _check("k3mx_moe_routed_topp", lib().k3mx_moe_routed_topp(
+        _ptr(y), _ptr(x), _x_dtype(x), T, _ptr(experts), _ptr(logits), _ptr(bias), path, float(top_p),
         _ptr(idx_out), _ptr(w_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)))
     return y

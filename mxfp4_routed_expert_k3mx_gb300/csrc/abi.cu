@@ -1,6 +1,7 @@
 // abi.cu - the extern "C" entry points of libk3mx.so: argument checks,
 // workspace layout and kernel launches.  No entry point allocates device
 // memory; scratch lives in the caller's workspace.
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 
@@ -216,7 +217,7 @@ k3mx_status check_moe_args(const void *y, const void *x, int x_dtype, int n_toke
 // The layer on device buffers; `ws` is already checked.
 k3mx_status run_moe(const Ctx &c, float *y, const void *x, int x_dtype, int n_tokens,
                     const k3mx_expert *experts, const float *logits, const float *bias, int path,
-                    int32_t *idx_out, float *w_out, void *ws, const MoeLayout &L) {
+                    int32_t *idx_out, float *w_out, void *ws, const MoeLayout &L, double top_p = 0.0) {
     int32_t *idx = idx_out ? idx_out : at<int32_t>(ws, L.idx);
     float *w = w_out ? w_out : at<float>(ws, L.w);
     GroupOut g{at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.perm),
@@ -235,14 +236,14 @@ k3mx_status run_moe(const Ctx &c, float *y, const void *x, int x_dtype, int n_to
         err = traced("route", c.stream, [&] {
             return launch_route_prep(c, idx, w, logits, bias, n_tokens, decode ? x : nullptr, x_bf16, ximg,
                                      one ? &g : nullptr, reinterpret_cast<int *>(sk), mx_streamk_flag_count(),
-                                     decode ? experts : nullptr, decode ? at<uint8_t>(ws, L.maps) : nullptr);
+                                     decode ? experts : nullptr, decode ? at<uint8_t>(ws, L.maps) : nullptr, top_p);
         });
         if (err == cudaSuccess && !one)
             err = traced("group_small", c.stream, [&] { return launch_group_small(c, idx, n_tokens, g); });
         pieces_done = decode;
     } else {
         err = traced("route", c.stream,
-                     [&] { return launch_route(c, idx, w, logits, bias, n_tokens); });
+                     [&] { return launch_route(c, idx, w, logits, bias, n_tokens, top_p); });
         if (err == cudaSuccess)
             err = traced("group", c.stream,
                          [&] { return launch_group(c, idx, n_tokens, g, at<void>(ws, L.hist)); });
@@ -371,7 +372,21 @@ k3mx_status k3mx_route_topk(int32_t *idx, float *w, const float *logits, const f
     k3mx_status st = device_ctx(reinterpret_cast<cudaStream_t>(stream), c);
     if (st != K3MX_OK) return st;
     return from_cuda(traced("route", c.stream,
-                            [&] { return launch_route(c, idx, w, logits, bias, n_tokens); }));
+                            [&] { return launch_route(c, idx, w, logits, bias, n_tokens, 0.0); }));
+}
+
+k3mx_status k3mx_route_topp(int32_t *idx, float *w, const float *logits, const float *bias,
+                            int n_tokens, float top_p, k3mx_stream_t stream) {
+    if (!idx || !w || !logits || !bias) return K3MX_EINVAL;
+    if (!(top_p == top_p) || top_p == INFINITY || top_p == -INFINITY) return K3MX_EINVAL;
+    if (n_tokens < 1 || n_tokens > K3MX_MAX_TOKENS) return K3MX_ESHAPE;
+    if (!aligned16(idx) || !aligned16(w) || !aligned16(logits) || !aligned16(bias))
+        return K3MX_EALIGN;
+    Ctx c;
+    k3mx_status st = device_ctx(reinterpret_cast<cudaStream_t>(stream), c);
+    if (st != K3MX_OK) return st;
+    return from_cuda(traced("route", c.stream,
+                            [&] { return launch_route(c, idx, w, logits, bias, n_tokens, (double)top_p); }));
 }
 
 size_t k3mx_group_workspace_size(int n_tokens) {
@@ -447,6 +462,25 @@ k3mx_status k3mx_moe_routed(float *y, const void *x, int x_dtype, int n_tokens,
     if (st != K3MX_OK) return st;
     return run_moe(c, y, x, x_dtype, n_tokens, experts, logits, bias, path, idx_out, w_out,
                    workspace, L);
+}
+
+k3mx_status k3mx_moe_routed_topp(float *y, const void *x, int x_dtype, int n_tokens,
+                                 const k3mx_expert *experts, const float *logits, const float *bias,
+                                 int path, float top_p, int32_t *idx_out, float *w_out, void *workspace,
+                                 size_t ws_bytes, k3mx_stream_t stream) {
+    if (!(top_p == top_p) || top_p == INFINITY || top_p == -INFINITY) return K3MX_EINVAL;
+    k3mx_status st = check_moe_args(y, x, x_dtype, n_tokens, experts, logits, bias, path);
+    if (st != K3MX_OK) return st;
+    if ((idx_out && !aligned16(idx_out)) || (w_out && !aligned16(w_out))) return K3MX_EALIGN;
+    path = resolve_path(n_tokens, x_dtype, path);
+    const MoeLayout L = moe_layout(n_tokens, x_dtype, path);
+    if (!workspace || ws_bytes < L.total) return K3MX_EWORKSPACE;
+    if (!aligned256(workspace)) return K3MX_EALIGN;
+    Ctx c;
+    st = device_ctx(reinterpret_cast<cudaStream_t>(stream), c);
+    if (st != K3MX_OK) return st;
+    return run_moe(c, y, x, x_dtype, n_tokens, experts, logits, bias, path, idx_out, w_out, workspace, L,
+                   (double)top_p);
 }
 
 k3mx_status k3mx_moe_routed_host(float *y_host, const void *x_host, int x_dtype, int n_tokens,

@@ -560,6 +560,7 @@ __global__ void k_combine(float *__restrict__ y, const float *__restrict__ out,
 #pragma unroll
     for (int k = 0; k < kK; k++) {
         const float wk = __ldg(w + (size_t)t * kK + k);
+        if (wk == 0.f) continue;                         // a slot dropped by top-p has no row
         const float4 v = __ldg(reinterpret_cast<const float4 *>(out + ((size_t)t * kK + k) * kD) + c);
         acc.x = fmaf(wk, v.x, acc.x);
         acc.y = fmaf(wk, v.y, acc.y);

@@ -1038,15 +1038,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
                     __threadfence();
                     const int done_pairs = atomicAdd(a.sync + SYNC_TILE + p.mt, 1) + 1;
                     __threadfence();
-                    last_tile = done_pairs == kK;
+                    last_tile = done_pairs == n_units;     // the token's pairs (top-p may keep fewer than 16)
                 }
                 named_sync(1, 128);
                 if (last_tile) {
                     const int t = pair / kK;
                     float yv = 0.f;
 #pragma unroll 4
-                    for (int k = 0; k < kK; k++)
-                        yv = fmaf(__ldg(a.w + (size_t)t * kK + k), __ldcg(a.out + ((size_t)t * kK + k) * kD + row), yv);
+                    for (int k = 0; k < kK; k++) {
+                        const float wk = __ldg(a.w + (size_t)t * kK + k);
+                        if (wk != 0.f)                     // a slot dropped by top-p has no row
+                            yv = fmaf(wk, __ldcg(a.out + ((size_t)t * kK + k) * kD + row), yv);
+                    }
                     a.y[(size_t)t * kD + row] = yv;
                 }
             }

@@ -611,7 +611,8 @@ __global__ void __launch_bounds__(kPxThreads, 1)
 // Work units: every active expert's pairs cut into ceil(n / kUT) runs of
 // nearly equal length (one 1024-thread CTA, expert e on thread e).
 __global__ void __launch_bounds__(1024) k_px_units(const int32_t *counts, const int32_t *offsets,
-                                                   int32_t *units, int32_t *n_units) {
+                                                   int32_t *units, int32_t *n_units, int32_t *slot_of_pair,
+                                                   int n_pairs) {
     __shared__ int tmp[33];
     const int e = threadIdx.x, lane = e & 31, wp = e >> 5;
     const int cnt = e < kE ? counts[e] : 0;
@@ -637,6 +638,8 @@ __global__ void __launch_bounds__(1024) k_px_units(const int32_t *counts, const 
     }
     __syncthreads();
     const int pos = incl - nu + tmp[wp];
+    // every pair's slot starts as "not grouped" (a slot dropped by top-p)
+    for (int i = threadIdx.x; i < n_pairs; i += blockDim.x) slot_of_pair[i] = -1;
     if (e < kE && nu > 0) {
         const int o0 = offsets[e];
         for (int k = 0; k < nu; k++) {
@@ -702,6 +705,7 @@ k_px_xprep(const uint16_t *__restrict__ x, int n_tokens, const int32_t *__restri
 #pragma unroll 4
     for (int k = 0; k < kK; k++) {
         const int slot = __ldg(slot_of_pair + (size_t)t * kK + k);
+        if (slot < 0) continue;                          // dropped by top-p
         const int un = __ldg(slot_un + slot);
         const int rows = b_rows(b_sel(__ldg(units + 3 * (un >> 8) + 2)));
         uint8_t *dst = planes + (size_t)slot * (kD / 2) + (size_t)kb * 16;
@@ -847,7 +851,7 @@ cudaError_t launch_prefill_mx(const Ctx &c, const PrefillArgs &p) {
             return cudaErrorNotSupported;
 
     cudaError_t err = traced("prefill_prep", c.stream, [&] {
-        k_px_units<<<1, 1024, 0, c.stream>>>(p.counts, p.offsets, units, n_units);
+        k_px_units<<<1, 1024, 0, c.stream>>>(p.counts, p.offsets, units, n_units, slot_of_pair, (int)S);
         const int map_ctas = (kE * kMapsPerExpert + 7) / 8;
         k_px_slots<<<(unsigned)(U + map_ctas), 256, 0, c.stream>>>(units, n_units, p.perm, slot_un, slot_of_pair, U,
                                                                      maps, p.experts, w13, w2);

@@ -88,8 +88,50 @@ __device__ __forceinline__ void warp_max_pair(uint32_t hi, uint32_t lo, uint32_t
     mlo = __reduce_max_sync(0xffffffffu, hi == mhi ? lo : 0u);
 }
 
+// The token's routing result; lane k < 16 holds slot k's expert e and raw
+// score s, `sum` is the slot-order double sum of the 16 scores.  With
+// top_p > 0 the low-weight tail is dropped (Kimi K3 engine (c/kimi_k3.c),
+// "Streaming design", K3_TOPP): in order of decreasing score (ties: lower
+// index) an expert is kept while the scores ahead of it sum to less than
+// top_p * sum; kept weights are raw scores over the kept sum, a dropped slot
+// gets index -1 and weight 0.  The sums are slot-order double sums, or, with
+// every score in [2^-24, 1], exact sums in units of 2^-47 (the same values).
+// Whole warp.
 __device__ __forceinline__ void write_routing(int32_t *idx_t, float *w_t, int lane, int my_e,
-                                              float my_s, double sum) {
+                                              float my_s, double sum, double top_p) {
+    if (top_p > 0.0) {
+        const float s = my_s;
+        const int e = my_e;
+        const bool fixed = __all_sync(0xffffffffu, lane >= kK || (s >= 0x1p-24f && s <= 1.0f));
+        double before = 0.0, kept = 0.0;
+        long long bfx = 0, kfx = 0;
+#pragma unroll 1
+        for (int j = 0; j < kK; j++) {
+            const float sj = __shfl_sync(0xffffffffu, s, j);
+            const int ej = __shfl_sync(0xffffffffu, e, j);
+            if (sj > s || (sj == s && ej < e)) {
+                if (fixed) bfx += (long long)__float2ll_rz(sj * 0x1p47f);
+                else before += (double)sj;
+            }
+        }
+        if (fixed) before = (double)bfx * 0x1p-47;
+        const bool keep = lane < kK && before < top_p * sum;
+#pragma unroll 1
+        for (int j = 0; j < kK; j++) {
+            const int kj = __shfl_sync(0xffffffffu, keep ? 1 : 0, j);
+            const float sj = __shfl_sync(0xffffffffu, s, j);
+            if (kj) {
+                if (fixed) kfx += (long long)__float2ll_rz(sj * 0x1p47f);
+                else kept += (double)sj;
+            }
+        }
+        if (fixed) kept = (double)kfx * 0x1p-47;
+        if (lane < kK) {
+            idx_t[lane] = keep ? e : -1;
+            w_t[lane] = keep ? (float)((double)s / kept) * kRoutedScale : 0.f;
+        }
+        return;
+    }
     if (lane < kK) {
         idx_t[lane] = my_e;
         w_t[lane] = (float)((double)my_s / sum) * kRoutedScale;
@@ -99,7 +141,7 @@ __device__ __forceinline__ void write_routing(int32_t *idx_t, float *w_t, int la
 // Exact selection over all 896 experts (used when the candidate filter
 // below would keep more than 64 experts, e.g. with many equal or NaN keys).
 __device__ void route_warp_all(const float *__restrict__ lt, const float *__restrict__ bias,
-                               int32_t *__restrict__ idx_t, float *__restrict__ w_t, int lane) {
+                               int32_t *__restrict__ idx_t, float *__restrict__ w_t, int lane, double top_p) {
     uint32_t ok[kPer];
 #pragma unroll
     for (int i = 0; i < kPer; i++) {
@@ -127,7 +169,7 @@ __device__ void route_warp_all(const float *__restrict__ lt, const float *__rest
             my_e = e;
         }
     }
-    write_routing(idx_t, w_t, lane, my_e, my_s, sum);
+    write_routing(idx_t, w_t, lane, my_e, my_s, sum, top_p);
 }
 
 // One token on one warp.  (1) fp32 estimates of all 896 keys (28 per lane,
@@ -140,7 +182,7 @@ __device__ void route_warp_all(const float *__restrict__ lt, const float *__rest
 // ints of shared memory for this warp.
 __device__ void route_warp(const float *__restrict__ lt, const float *__restrict__ bias,
                            int32_t *__restrict__ idx_t, float *__restrict__ w_t, int lane,
-                           int *scratch) {
+                           int *scratch, double top_p) {
     uint32_t ok[kPer];
 #pragma unroll
     for (int i = 0; i < kPer; i++) {
@@ -179,7 +221,7 @@ __device__ void route_warp(const float *__restrict__ lt, const float *__restrict
     }
     __syncwarp();
     if (n > 64) {
-        route_warp_all(lt, bias, idx_t, w_t, lane);
+        route_warp_all(lt, bias, idx_t, w_t, lane, top_p);
         return;
     }
     // exact keys: lane holds candidates lane and lane + 32
@@ -230,17 +272,17 @@ __device__ void route_warp(const float *__restrict__ lt, const float *__restrict
             my_e = e;
         }
     }
-    write_routing(idx_t, w_t, lane, my_e, my_s, sum);
+    write_routing(idx_t, w_t, lane, my_e, my_s, sum, top_p);
 }
 
 __global__ void __launch_bounds__(256) k_route(int32_t *idx, float *w, const float *logits,
-                                               const float *bias, int n_tokens) {
+                                               const float *bias, int n_tokens, double top_p) {
     __shared__ int scratch[8][128];
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int t = blockIdx.x * (blockDim.x / 32) + warp;
     if (t >= n_tokens) return;
     route_warp(logits + (size_t)t * kE, bias, idx + (size_t)t * kK, w + (size_t)t * kK, lane,
-               scratch[warp]);
+               scratch[warp], top_p);
 }
 
 // exclusive scan of one int per thread over the block (up to 32 warps);
@@ -404,7 +446,7 @@ __device__ __forceinline__ void radix_pick(RouteSmem &sm, int need) {
 }
 
 __device__ void route_cta(const float *__restrict__ lt, const float *__restrict__ bias,
-                          int32_t *__restrict__ idx_t, float *__restrict__ w_t, RouteSmem &sm) {
+                          int32_t *__restrict__ idx_t, float *__restrict__ w_t, RouteSmem &sm, double top_p) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float lv[kRS], bv[kRS];
 #pragma unroll
@@ -457,7 +499,7 @@ __device__ void route_cta(const float *__restrict__ lt, const float *__restrict_
     __syncthreads();
     const int n = sm.n;
     if (n > 64) {
-        if (warp == 0) route_warp_all(lt, bias, idx_t, w_t, lane);
+        if (warp == 0) route_warp_all(lt, bias, idx_t, w_t, lane, top_p);
         __syncthreads();
         if (tid < kK) sm.sel_e[tid] = idx_t[tid];
         __syncthreads();
@@ -497,31 +539,33 @@ __device__ void route_cta(const float *__restrict__ lt, const float *__restrict_
             sum = 0.0;
             for (int r = 0; r < kK; r++) sum += (double)sm.sel_s[r];
         }
-        if (lane < kK) {
-            idx_t[lane] = sm.sel_e[lane];
-            w_t[lane] = (float)((double)sr / sum) * kRoutedScale;
-        }
+        write_routing(idx_t, w_t, lane, lane < kK ? sm.sel_e[lane] : 0, sr, sum, top_p);
+        // the grouping of a single token reads the (possibly dropped) slots
+        __syncwarp();
+        if (lane < kK) sm.sel_e[lane] = idx_t[lane];
     }
 }
 
 // Grouping of a single token's 16 pairs (pair p = slot p) inside its
-// routing CTA, warp 0: the 16 experts are distinct, so each has one pair
-// and one work unit; units and perm follow increasing expert index.  The
-// decode passes read only the units and perm; counts, offsets and the
-// active list are not written.
+// routing CTA, warp 0: the experts are distinct, so each kept slot (index
+// >= 0; top-p may drop some) has one pair and one work unit; units and perm
+// follow increasing expert index.  The decode passes read only the units and
+// perm; counts, offsets and the active list are not written.
 __device__ void group_one_token(const GroupOut &g, const RouteSmem &sm) {
     const int lane = threadIdx.x & 31;
-    const int e = lane < kK ? sm.sel_e[lane] : 0x7FFFFFFF;
+    const int ei = lane < kK ? sm.sel_e[lane] : -1;
+    const int e = ei >= 0 ? ei : 0x7FFFFFFF;
     int rank = 0;
 #pragma unroll
     for (int u = 0; u < kK; u++) rank += __shfl_sync(0xffffffffu, e, u) < e;
-    if (lane < kK) {
+    if (ei >= 0) {
         g.perm[rank] = lane;
         g.units[3 * rank + 0] = e;
         g.units[3 * rank + 1] = rank;
         g.units[3 * rank + 2] = rank + 1;
     }
-    if (lane == 0) *g.n_units = kK;
+    const int kept = __popc(__ballot_sync(0xffffffffu, ei >= 0));
+    if (lane == 0) *g.n_units = kept;
 }
 
 // CTAs 0..n_tokens-1 route one token each (and, for a single token with a
@@ -532,14 +576,14 @@ __device__ void group_one_token(const GroupOut &g, const RouteSmem &sm) {
 __global__ void __launch_bounds__(kRT)
 k_route_prep(int32_t *idx, float *w, const float *logits, const float *bias, int n_tokens,
              const void *x, int x_bf16, uint8_t *ximg, GroupOut g, int *flags, int n_flags,
-             const k3mx_expert *experts, int piece_ctas, uint8_t *maps,
+             const k3mx_expert *experts, int piece_ctas, uint8_t *maps, double top_p,
              const __grid_constant__ CUtensorMap w13, const __grid_constant__ CUtensorMap w2) {
     __shared__ RouteSmem sm;
     // the expert passes may launch now: their prologues overlap this kernel
     pdl_launch_dependents();
     if ((int)blockIdx.x < n_tokens) {
         const int t = blockIdx.x;
-        route_cta(logits + (size_t)t * kE, bias, idx + (size_t)t * kK, w + (size_t)t * kK, sm);
+        route_cta(logits + (size_t)t * kE, bias, idx + (size_t)t * kK, w + (size_t)t * kK, sm, top_p);
         if (n_tokens == 1 && g.units != nullptr) {
             __syncthreads();
             if (threadIdx.x < 32) group_one_token(g, sm);
@@ -569,30 +613,13 @@ __global__ void __launch_bounds__(512) k_group_small(const int32_t *idx, int n_t
     pdl_launch_dependents();
     __syncthreads();
     const int n_pairs = n_tokens * kK;
-    for (int p = threadIdx.x; p < n_pairs; p += blockDim.x) atomicAdd(&cnt[idx[p]], 1);
+    for (int p = threadIdx.x; p < n_pairs; p += blockDim.x) {
+        const int e = idx[p];
+        if (e >= 0 && e < kE) atomicAdd(&cnt[e], 1);     // -1: a slot dropped by top-p
+    }
     __syncthreads();
     finish_counts(cnt, g, tmp);
     if (threadIdx.x < 32) scatter_warp(idx, 0, n_pairs, cnt, g.perm);
-}
-
-// route + group for n_tokens * 16 <= 1024 pairs, one 512-thread CTA
-__global__ void __launch_bounds__(512)
-k_route_group_small(int32_t *idx, float *w, const float *logits, const float *bias,
-                    int n_tokens, GroupOut g) {
-    __shared__ int cnt[kE];
-    __shared__ int tmp[33];
-    __shared__ int scratch[16][128];
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nwarps = blockDim.x / 32;
-    for (int t = warp; t < n_tokens; t += nwarps)
-        route_warp(logits + (size_t)t * kE, bias, idx + (size_t)t * kK, w + (size_t)t * kK, lane,
-                   scratch[warp]);
-    for (int e = threadIdx.x; e < kE; e += blockDim.x) cnt[e] = 0;
-    __syncthreads();                         // idx written by this block is visible
-    const int n_pairs = n_tokens * kK;
-    for (int p = threadIdx.x; p < n_pairs; p += blockDim.x) atomicAdd(&cnt[idx[p]], 1);
-    __syncthreads();
-    finish_counts(cnt, g, tmp);
-    if (warp == 0) scatter_warp(idx, 0, n_pairs, cnt, g.perm);
 }
 
 // per-segment histograms: hist[seg][e]
@@ -607,7 +634,7 @@ k_group_count(const int32_t *idx, int n_pairs, int *hist, int *status) {
         const int e = idx[p];
         if (e >= 0 && e < kE)
             atomicAdd(&cnt[e], 1);
-        else
+        else if (e != -1)                                 // -1: a slot dropped by top-p
             report_status(status, kStatusBadIndex, p);
     }
     __syncthreads();
@@ -647,23 +674,17 @@ k_group_scatter(const int32_t *idx, int n_pairs, const int *base, int32_t *perm)
 }  // namespace
 
 cudaError_t launch_route(const Ctx &c, int32_t *idx, float *w, const float *logits,
-                         const float *bias, int n_tokens) {
+                         const float *bias, int n_tokens, double top_p) {
     const int per_block = 8;
     k_route<<<(n_tokens + per_block - 1) / per_block, 32 * per_block, 0, c.stream>>>(
-        idx, w, logits, bias, n_tokens);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_route_group_small(const Ctx &c, int32_t *idx, float *w, const float *logits,
-                                     const float *bias, int n_tokens, const GroupOut &g) {
-    k_route_group_small<<<1, 512, 0, c.stream>>>(idx, w, logits, bias, n_tokens, g);
+        idx, w, logits, bias, n_tokens, top_p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_route_prep(const Ctx &c, int32_t *idx, float *w, const float *logits,
                               const float *bias, int n_tokens, const void *x, int x_bf16,
                               uint8_t *ximg, const GroupOut *g_one, int *flags, int n_flags,
-                              const k3mx_expert *experts, uint8_t *maps) {
+                              const k3mx_expert *experts, uint8_t *maps, double top_p) {
     const int piece_ctas = x != nullptr ? (n_tokens * (kD / 32) + kRT / 32 - 1) / (kRT / 32) : 0;
     CUtensorMap w13{}, w2{};
     int map_ctas = 0;
@@ -675,7 +696,7 @@ cudaError_t launch_route_prep(const Ctx &c, int32_t *idx, float *w, const float 
     if (g_one != nullptr && n_tokens == 1) g = *g_one;
     k_route_prep<<<n_tokens + piece_ctas + map_ctas, kRT, 0, c.stream>>>(
         idx, w, logits, bias, n_tokens, x, x_bf16, ximg, g, flags, flags ? n_flags : 0, experts, piece_ctas, maps,
-        w13, w2);
+        top_p, w13, w2);
     return cudaGetLastError();
 }
 

@@ -15,7 +15,7 @@ FAKE = 0x10000          # an aligned, non-null address that is never dereference
 def test_library_exports_every_declared_symbol():
     L = k3mx.lib()
     declared = k3mx.declared_symbols()
-    assert len(declared) == 16
+    assert len(declared) == 18
     out = subprocess.run(["nm", "-D", "--defined-only", k3mx.LIB_PATH],
                          capture_output=True, text=True, check=True).stdout
     exported = set(re.findall(r"\sT\s(k3mx_\w+)", out))
@@ -48,6 +48,11 @@ def test_route_group_refuse_bad_arguments():
     assert L.k3mx_route_topk(FAKE, FAKE, FAKE, FAKE, 0, None) == 3
     assert L.k3mx_route_topk(FAKE, FAKE, FAKE, FAKE, 65537, None) == 3
     assert L.k3mx_route_topk(FAKE, FAKE + 4, FAKE, FAKE, 1, None) == 2
+    for p in (float("nan"), float("inf"), float("-inf")):                 # top_p not finite
+        assert L.k3mx_route_topp(FAKE, FAKE, FAKE, FAKE, 1, p, None) == 1
+    assert L.k3mx_route_topp(FAKE, FAKE, FAKE, None, 1, 0.5, None) == 1
+    assert L.k3mx_route_topp(FAKE, FAKE, FAKE, FAKE, 0, 0.5, None) == 3
+    assert L.k3mx_route_topp(FAKE, FAKE + 4, FAKE, FAKE, 1, 0.5, None) == 2
     ws = k3mx.k3mx_group_workspace_size(64)
     assert ws > 0 and k3mx.k3mx_group_workspace_size(0) == 0
     assert L.k3mx_group(FAKE, FAKE, FAKE, FAKE, 64, FAKE, ws - 1, None) == 4
