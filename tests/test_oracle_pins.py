@@ -438,3 +438,15 @@ def test_topp_invariants():
                 assert ds.max() <= ks.min()                   # only the lightest are dropped
         counts, offsets, perm = oracle.group(i)
         assert offsets[-1] == kept.sum() and len(perm) == kept.sum()
+
+
+def test_topp_equal_scores_keep_the_lowest_indices():
+    """16 equal scores: each carries 1/16, so the shortest prefix reaching p
+    has ceil(16 p) experts, and ties rank the lower expert index first."""
+    logits = np.full((3, 896), 0.25, np.float32)
+    bias = np.zeros(896, np.float32)
+    for p, n in ((0.25, 4), (0.26, 5), (0.75, 12), (0.999, 16)):
+        i, w = oracle.route_topp(logits, bias, p)
+        assert np.all((i >= 0).sum(1) == n), p
+        assert sorted(i[0][i[0] >= 0]) == list(range(n))
+        assert np.all(w[i >= 0] == np.float32(1.0 / n))
