@@ -576,6 +576,8 @@ static_assert(XB <= 2 * HB && XS <= 2 * HS, "x image must fit the h buffers");
 static_assert(S >= 3 && S <= 10, "pipeline depth");
 static_assert(SFB_COL + (kD / 128) * 4 <= TMEM_COLS, "TMEM budget");
 static_assert(SMEM <= kSmemLimit, "shared memory budget");
+static_assert(kE * (int)sizeof(k3mx_expert) <= S * STAGE, "the expert table is staged in the ring");
+constexpr int PREFETCH = 12;                     // down stages pulled into L2 while h is pending
 }  // namespace f1
 
 __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
@@ -614,23 +616,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
     tc_fence_after();
     const uint32_t tmem = hd->tmem;
     volatile int *abort_flag = &hd->abort;
-    pdl_wait();
-    pdl_launch_dependents();
-
-    // the token's work units (at most 16), read once into shared memory
-    __shared__ Unit s_unit[MAX_UNITS];
-    __shared__ int s_pair[MAX_UNITS];
-    __shared__ int s_nunits;
-    if (warp == kProdWarp) {
-        const int nu = a.experts == nullptr ? 1 : min(__ldg(a.n_units), MAX_UNITS);
-        if (lane < nu) {
-            s_unit[lane] = unit_at(a, lane);
-            s_pair[lane] = pair_at(a, s_unit[lane].p0);
-        }
-        if (lane == 0) s_nunits = nu;
-    }
-    __syncthreads();
-    const int n_units = s_nunits;
 
     // Two work segments, every gate/up stage (unit-major) and then every
     // down stage, each cut in equal stage ranges over the CTAs (stream-K)
@@ -638,28 +623,103 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
     // gate/up share, then its down share.  (Splitting the units into two
     // halves run as gate/up A, gate/up B, down A, down B measured no faster:
     // the extra short parts cost what the shorter wait for h saved.)
-    const long long GU = (long long)n_units * MTG * KCG, GDn = (long long)n_units * MTD * KCD;
-    const long long G = gridDim.x, B = blockIdx.x;
-    const bool sk = a.partials != nullptr && GU >= G * (KCG + 1) && GDn >= G * (KCD + 1);
-    const int nseg = 2;
-    long long r0[NSEG], r1[NSEG], cum[NSEG + 1];
-    {
-        const long long st[NSEG] = {0, GU}, len[NSEG] = {GU, GDn};
-        const int kc[NSEG] = {KCG, KCD};
-        cum[0] = 0;
+    struct Sched {
+        int gu, r0[NSEG], r1[NSEG], cum[NSEG + 1];
+        bool sk;
+    };
+    auto plan = [&](int nu) {
+        Sched sc;
+        const int GU = nu * MTG * KCG, GDn = nu * MTD * KCD;
+        const int G = gridDim.x, B = blockIdx.x;
+        sc.gu = GU;
+        sc.sk = a.partials != nullptr && GU >= G * (KCG + 1) && GDn >= G * (KCD + 1);
+        const int st[NSEG] = {0, GU}, len[NSEG] = {GU, GDn}, kc[NSEG] = {KCG, KCD};
+        sc.cum[0] = 0;
 #pragma unroll
         for (int i = 0; i < NSEG; i++) {
-            if (sk) {
-                r0[i] = st[i] + len[i] * B / G;
-                r1[i] = st[i] + len[i] * (B + 1) / G;
+            if (sc.sk) {
+                sc.r0[i] = st[i] + len[i] * B / G;
+                sc.r1[i] = st[i] + len[i] * (B + 1) / G;
             } else {
-                const long long items = len[i] / kc[i];
-                r0[i] = st[i] + items * B / G * kc[i];
-                r1[i] = st[i] + items * (B + 1) / G * kc[i];
+                const int items = len[i] / kc[i];
+                sc.r0[i] = st[i] + items * B / G * kc[i];
+                sc.r1[i] = st[i] + items * (B + 1) / G * kc[i];
             }
-            cum[i + 1] = cum[i] + (r1[i] - r0[i]);
+            sc.cum[i + 1] = sc.cum[i] + (sc.r1[i] - sc.r0[i]);
+        }
+        return sc;
+    };
+    // A token keeps all 16 experts unless top-p drops some: the partition
+    // for 16 units is made while the routing kernel runs.  The expert table
+    // is an input of the call that no kernel of the step writes, so it is
+    // staged now in the stage ring (unused until the first weight copy),
+    // and a unit's pointers become a shared-memory lookup.
+    Sched sc = plan(MAX_UNITS);
+    const uint2 *tab = reinterpret_cast<const uint2 *>(smem + 1024);
+    if (a.experts != nullptr) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(a.experts);   // 16-byte aligned (checked)
+        uint4 *dst = reinterpret_cast<uint4 *>(smem + 1024);
+        for (int i = tid; i < kE * 3; i += kThreads) dst[i] = __ldg(src + i);
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+    __syncthreads();                     // every warp's share of the table is staged
+
+    // the token's work units (at most 16): the unit count, the unit list
+    // and perm in one round of loads (all 16 entries lie in the workspace)
+    __shared__ Unit s_unit[MAX_UNITS];
+    __shared__ int s_pair[MAX_UNITS];
+    __shared__ int s_nunits;
+    if (warp == kProdWarp) {
+        if (a.experts == nullptr) {
+            if (lane == 0) {
+                s_unit[0] = unit_at(a, 0);
+                s_pair[0] = 0;
+                s_nunits = 1;
+            }
+        } else {
+            const int n_raw = __ldg(a.n_units);
+            int e = 0, p0 = 0, p1 = 0, pr = 0;
+            if (lane < MAX_UNITS) {
+                e = __ldg(a.units + 3 * lane);
+                p0 = __ldg(a.units + 3 * lane + 1);
+                p1 = __ldg(a.units + 3 * lane + 2);
+                pr = __ldg(a.perm + lane);
+            }
+            const int nu = min(max(n_raw, 0), MAX_UNITS);
+            const int pair = __shfl_sync(0xffffffffu, pr, p0 & (MAX_UNITS - 1));
+            if (lane < nu) {
+                Unit u;
+                u.e = e;
+                u.p0 = p0;
+                u.p1 = p1;
+                const bool in = (unsigned)e < (unsigned)kE;
+                const uint2 *t = tab + 6 * (in ? e : 0);
+                uint64_t w[6], orp = 0;
+#pragma unroll
+                for (int i = 0; i < 6; i++) {
+                    w[i] = (uint64_t)t[i].y << 32 | t[i].x;
+                    orp |= w[i];
+                }
+                u.ex.w1 = reinterpret_cast<const uint8_t *>(w[0]);
+                u.ex.s1 = reinterpret_cast<const uint8_t *>(w[1]);
+                u.ex.w3 = reinterpret_cast<const uint8_t *>(w[2]);
+                u.ex.s3 = reinterpret_cast<const uint8_t *>(w[3]);
+                u.ex.w2 = reinterpret_cast<const uint8_t *>(w[4]);
+                u.ex.s2 = reinterpret_cast<const uint8_t *>(w[5]);
+                u.ok = in && (orp & 15u) == 0;
+                s_unit[lane] = u;
+                s_pair[lane] = pair;
+            }
+            if (lane == 0) s_nunits = nu;
         }
     }
+    // the table reads before the ring's first asynchronous writes
+    fence_async_smem();
+    __syncthreads();
+    const int n_units = s_nunits;
+    if (n_units != MAX_UNITS) sc = plan(n_units);
+    const int nseg = 2;
     auto fail = [&](int detail) {
         report_status(a.status, kStatusWaitTimeout, detail);
         *abort_flag = 1;
@@ -667,36 +727,36 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
     struct Part {
         int ph;          // 0 gate/up, 1 down
         int seg;         // work segment
-        long long item;  // within the phase
+        int item;        // within the phase
         int lo, hi;      // stages of the item
         int mt;          // 128-row tile
         int pair;        // the unit's pair
         Unit u;
     };
     // parts in order: `t` walks this CTA's stages, segment after segment
-    auto next_part = [&](long long &t, Part &p) -> bool {
+    auto next_part = [&](int &t, Part &p) -> bool {
         for (;;) {
             int sg = 0;
 #pragma unroll
-            for (int i = 1; i < NSEG; i++) sg += (i < nseg && t >= cum[i]) ? 1 : 0;
-            if (t >= cum[nseg]) return false;
-            long long q0s = r0[0], q1s = r1[0], c0 = cum[0];
+            for (int i = 1; i < NSEG; i++) sg += (i < nseg && t >= sc.cum[i]) ? 1 : 0;
+            if (t >= sc.cum[nseg]) return false;
+            int q0s = sc.r0[0], q1s = sc.r1[0], c0 = sc.cum[0];
 #pragma unroll
             for (int i = 1; i < NSEG; i++)
-                if (sg == i) q0s = r0[i], q1s = r1[i], c0 = cum[i];
-            const long long q = q0s + (t - c0);
-            const bool up = q < GU;
+                if (sg == i) q0s = sc.r0[i], q1s = sc.r1[i], c0 = sc.cum[i];
+            const int q = q0s + (t - c0);
+            const bool up = q < sc.gu;
             const int kc = up ? KCG : KCD;
-            const long long r = q - (up ? 0 : GU);
+            const int r = q - (up ? 0 : sc.gu);
             p.ph = up ? 0 : 1;
             p.seg = sg;
             p.item = r / kc;
-            p.lo = (int)(r % kc);
-            p.hi = (int)min((long long)kc, p.lo + (q1s - q));
+            p.lo = r % kc;
+            p.hi = min(kc, p.lo + (q1s - q));
             t += p.hi - p.lo;
             const int mts = up ? MTG : MTD;
-            p.mt = (int)(p.item % mts);
-            const int ui = (int)(p.item / mts);
+            p.mt = p.item % mts;
+            const int ui = p.item / mts;
             p.u = s_unit[ui];
             p.pair = s_pair[ui];
             if (p.u.ok) return true;
@@ -718,9 +778,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
         const uint64_t pol_img = l2_evict_last_policy();
         int cur_e = -1, cur_ph = -1;
         const uint8_t *map0 = nullptr, *map1 = nullptr;
-        long long cur_key = -2, q = 0;
+        long long cur_key = -2;
+        int q = 0;
         uint32_t su = 0, bl = 0;
         bool x_first = false;            // epoch 0 held x (which overlaps both h buffers)
+        bool prefetched = false;
+        auto prefetch_down = [&](const uint8_t *m, int c, int mt) {
+            tma_prefetch_2d(m, (2 * c) * 128, mt * 128);
+            tma_prefetch_2d(m, (2 * c + 1) * 128, mt * 128);
+        };
         Part p;
         while (!*abort_flag && next_part(q, p)) {
             const Unit &u = p.u;
@@ -754,13 +820,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
                 su++;
                 return true;
             };
-            // weight tiles first (they need nothing from the gate/up pass),
-            // then the part's B images
-            const int pre = min(S, p.hi - p.lo);
+            // A new B image: the token's x is ready, so it goes out before
+            // the part's weight tiles (which would queue ahead of it); a
+            // pair's h waits for the gate/up pass, so up to a ring of weight
+            // tiles (which need nothing) goes out first.
+            const long long key = b_key(p);
+            const int pre = key != cur_key && p.ph == 0 ? 0 : min(S, p.hi - p.lo);
             bool ok = true;
             for (int c = p.lo; c < p.lo + pre && ok; c++) ok = issue_stage(c);
             if (!ok) break;
-            const long long key = b_key(p);
             if (key != cur_key) {
                 // epoch bl: x (bl = 0) or a pair's h; wait for the epoch that
                 // used its buffer (x overlaps both h buffers)
@@ -779,6 +847,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
                     nb = XB;
                     ns = XS;
                 } else {
+                    if (!prefetched) {
+                        // The pair's h may still be pending (the gate/up pass
+                        // drains unevenly over the CTAs): the next down
+                        // stages of this CTA, after those in the ring, go
+                        // into L2 meanwhile, so the weight stream does not
+                        // pause.
+                        prefetched = true;
+                        if (lane == 0) {
+                            int budget = PREFETCH, t = q;
+                            for (int c = p.lo + pre; c < p.hi && budget > 0; c++, budget--)
+                                prefetch_down(map0, c, p.mt);
+                            Part np;
+                            while (budget > 0 && next_part(t, np)) {
+                                if (np.ph != 1) continue;
+                                const uint8_t *m = a.maps + ((size_t)np.u.e * kMapsPerExpert + 2) * kMapBytes;
+                                acquire_map(m);
+                                for (int c = np.lo; c < np.hi && budget > 0; c++, budget--) prefetch_down(m, c, np.mt);
+                            }
+                        }
+                        __syncwarp();
+                    }
                     // the pair's h: every gate/up item of the pair has written its block
                     const int pair = (int)key;
                     const int *cnt = a.sync + SYNC_HDONE + (a.experts == nullptr ? 0 : pair % kK);
@@ -833,13 +922,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
             }
         };
         uint32_t su = 0, np = 0;
-        long long q = 0;
+        int q = 0;
         Part cur, nxt;
         bool have = next_part(q, cur);
         if (have) issue(cur, 0);
         while (have && !*abort_flag) {
             const int buf = np & 1;
-            long long qn = q;
+            int qn = q;
             const bool more = next_part(qn, nxt);
             if (more) issue(nxt, (np + 1) & 1);
             if (!mbar_wait(sfull0 + 8 * buf, (np / 2) & 1)) {
@@ -888,7 +977,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
         // ----------------------------------------------------- MMA issuer --
         if (lane == 0) {
             uint32_t su = 0, bu = 0, it = 0, bcur = 0;
-            long long cur_key = -2, q = 0;
+            long long cur_key = -2;
+            int q = 0;
             bool run = true;
             Part p;
             while (run && !*abort_flag && next_part(q, p)) {
@@ -948,7 +1038,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
                 if (!run) break;
                 umma_commit(accf0 + 8 * b);
                 it++;
-                long long qn = q;
+                int qn = q;
                 Part nx;
                 if (!next_part(qn, nx) || b_key(nx) != key) umma_commit(bempty0 + 8 * (bcur & 1));
             }
@@ -960,7 +1050,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
         const int row_in_tile = 32 * q4 + lane;
         __shared__ int last_tile;
         uint32_t it = 0;
-        long long q = 0;
+        int q = 0;
         Part p;
         while (!*abort_flag && next_part(q, p)) {
             const int kc = p.ph == 0 ? KCG : KCD;
@@ -984,7 +1074,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
 #pragma unroll
                 for (int pc = 0; pc < kPieces; pc++) acc[m] += __uint_as_float(v[m][pc]);
             const size_t slot = (size_t)p.seg * kMaxGrid + blockIdx.x;
-            if (sk && p.lo > 0) {
+            if (sc.sk && p.lo > 0) {
                 // the tail of an item begun by the previous CTA: hand over
                 // the summed pieces and move on
                 float *dst = a.partials + slot * PARTIAL;
@@ -998,7 +1088,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
                 }
                 continue;
             }
-            if (sk && p.hi < kc) {
+            if (sc.sk && p.hi < kc) {
                 // the head of an item the next CTA finishes: add its sums
                 const int *flag = a.sync + slot + 1;
                 int f = 0;

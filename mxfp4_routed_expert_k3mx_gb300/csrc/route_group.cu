@@ -50,6 +50,23 @@ __device__ __forceinline__ float approx_score(float l) {
     return 1.0f / (1.0f + expf(-l));
 }
 
+// A score s in [2^-24, 1] in units of 2^-47: its significand shifted by the
+// exponent, integer operations only (exact: s = M 2^(E-150), E >= 103).
+__device__ __forceinline__ long long score_fx(float s) {
+    const uint32_t u = __float_as_uint(s);
+    const uint32_t E = (u >> 23) & 0xFFu, M = (u & 0x7FFFFFu) | 0x800000u;
+    return (long long)((unsigned long long)M << (E - 103u));
+}
+
+// A sum of at most 16 such values (0 < v < 2^52) times 2^-47 as a double,
+// built from its bits: exact, since v has at most 52 significant bits.
+__device__ __forceinline__ double fx_to_double(long long v) {
+    const unsigned long long x = (unsigned long long)v;
+    const int t = 63 - __clzll(x);                    // leading bit, t <= 51
+    const unsigned long long frac = (x << (52 - t)) & 0xFFFFFFFFFFFFFull;
+    return __longlong_as_double((long long)(((unsigned long long)(1023 + t - 47) << 52) | frac));
+}
+
 __device__ __forceinline__ float canon_key(float k) {
     if (k != k) return -INFINITY;        // NaN ranks last
     if (k == 0.0f) return 0.0f;          // -0 -> +0
@@ -97,8 +114,8 @@ __device__ __forceinline__ void warp_max_pair(uint32_t hi, uint32_t lo, uint32_t
 // gets index -1 and weight 0.  The sums are slot-order double sums, or, with
 // every score in [2^-24, 1], exact sums in units of 2^-47 (the same values).
 // Whole warp.
-__device__ __forceinline__ void write_routing(int32_t *idx_t, float *w_t, int lane, int my_e,
-                                              float my_s, double sum, double top_p) {
+__device__ __forceinline__ int write_routing(int32_t *idx_t, float *w_t, int lane, int my_e,
+                                             float my_s, double sum, double top_p) {
     if (top_p > 0.0) {
         const float s = my_s;
         const int e = my_e;
@@ -110,32 +127,33 @@ __device__ __forceinline__ void write_routing(int32_t *idx_t, float *w_t, int la
             const float sj = __shfl_sync(0xffffffffu, s, j);
             const int ej = __shfl_sync(0xffffffffu, e, j);
             if (sj > s || (sj == s && ej < e)) {
-                if (fixed) bfx += (long long)__float2ll_rz(sj * 0x1p47f);
+                if (fixed) bfx += score_fx(sj);
                 else before += (double)sj;
             }
         }
-        if (fixed) before = (double)bfx * 0x1p-47;
+        if (fixed) before = bfx > 0 ? fx_to_double(bfx) : 0.0;
         const bool keep = lane < kK && before < top_p * sum;
 #pragma unroll 1
         for (int j = 0; j < kK; j++) {
             const int kj = __shfl_sync(0xffffffffu, keep ? 1 : 0, j);
             const float sj = __shfl_sync(0xffffffffu, s, j);
             if (kj) {
-                if (fixed) kfx += (long long)__float2ll_rz(sj * 0x1p47f);
+                if (fixed) kfx += score_fx(sj);
                 else kept += (double)sj;
             }
         }
-        if (fixed) kept = (double)kfx * 0x1p-47;
+        if (fixed) kept = fx_to_double(kfx);
         if (lane < kK) {
             idx_t[lane] = keep ? e : -1;
             w_t[lane] = keep ? (float)((double)s / kept) * kRoutedScale : 0.f;
         }
-        return;
+        return keep ? e : -1;
     }
     if (lane < kK) {
         idx_t[lane] = my_e;
         w_t[lane] = (float)((double)my_s / sum) * kRoutedScale;
     }
+    return my_e;
 }
 
 // Exact selection over all 896 experts (used when the candidate filter
@@ -407,7 +425,7 @@ struct RouteSmem {
     uint32_t tau;
     int n;
     int cand[64];
-    uint32_t khi[64], klo[64];
+    unsigned long long ck[64];           // exact key << 32 | complemented expert index
     float cs[64];
     int sel_e[kK];
     float sel_s[kK];
@@ -509,17 +527,18 @@ __device__ void route_cta(const float *__restrict__ lt, const float *__restrict_
         const int e = sm.cand[tid];
         const float s = exact_score(__ldg(lt + e));
         sm.cs[tid] = s;
-        sm.khi[tid] = order_key(s + __ldg(bias + e));
-        sm.klo[tid] = 0xFFFFFFFFu - (uint32_t)e;
+        sm.ck[tid] = (unsigned long long)order_key(s + __ldg(bias + e)) << 32 | (0xFFFFFFFFu - (uint32_t)e);
     }
     __syncthreads();
     if (tid < n) {
-        const uint32_t h = sm.khi[tid], l = sm.klo[tid];
+        // rank = the candidates ahead (larger key, or equal key and lower
+        // index); the comparisons are independent, so they are unrolled
+        const unsigned long long me = sm.ck[tid];
         int r = 0;
-#pragma unroll 1
-        for (int u = 0; u < n; u++) r += (sm.khi[u] > h) || (sm.khi[u] == h && sm.klo[u] > l);
+#pragma unroll 16
+        for (int u = 0; u < n; u++) r += sm.ck[u] > me;
         if (r < kK) {
-            sm.sel_e[r] = (int)(0xFFFFFFFFu - l);
+            sm.sel_e[r] = (int)(0xFFFFFFFFu - (uint32_t)me);
             sm.sel_s[r] = sm.cs[tid];
         }
     }
@@ -531,18 +550,18 @@ __device__ void route_cta(const float *__restrict__ lt, const float *__restrict_
         // sum of the scores in units of 2^-47, whatever the order of adds.
         const float sr = lane < kK ? sm.sel_s[lane] : 0.f;
         const bool fixed = __all_sync(0xffffffffu, lane >= kK || (sr >= 0x1p-24f && sr <= 1.0f));
-        long long acc = lane < kK ? (long long)__float2ll_rz(sr * 0x1p47f) : 0ll;
+        long long acc = lane < kK && fixed ? score_fx(sr) : 0ll;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        double sum = (double)acc * 0x1p-47;
+        double sum = fixed ? fx_to_double(acc) : 0.0;
         if (!fixed) {
             sum = 0.0;
             for (int r = 0; r < kK; r++) sum += (double)sm.sel_s[r];
         }
-        write_routing(idx_t, w_t, lane, lane < kK ? sm.sel_e[lane] : 0, sr, sum, top_p);
+        const int kept_e = write_routing(idx_t, w_t, lane, lane < kK ? sm.sel_e[lane] : 0, sr, sum, top_p);
         // the grouping of a single token reads the (possibly dropped) slots
         __syncwarp();
-        if (lane < kK) sm.sel_e[lane] = idx_t[lane];
+        if (lane < kK) sm.sel_e[lane] = kept_e;
     }
 }
 

@@ -53,6 +53,11 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const void *map, int x, int
         "l"(map), "r"(x), "r"(y), "r"(bar), "l"(policy)
         : "memory");
 }
+// a box of a tensor map into L2 only (no shared memory, no barrier)
+__device__ __forceinline__ void tma_prefetch_2d(const void *map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
+                 : "memory");
+}
 __device__ __forceinline__ void tma_3d(uint32_t dst, const void *map, int x, int y, int z, uint32_t bar,
                                        uint64_t policy) {
     asm volatile(
