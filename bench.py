@@ -20,8 +20,13 @@ calls with fresh logits, then prints the device status.  With --confine the
 bias keeps routing on the R resident experts, so each expert a launch
 touches is a distinct one, as in the full workload.
 
-Timing: CUDA events on the launching stream around each step; L2 (129 MB)
-is flushed by a 256 MB write between timed steps, outside the events.
+Timing: CUDA events on the launching stream around each step.  The inputs
+of every step are larger than L2 (129 MB): a decode step streams 16 experts
+it has not just used (280.8 MB; 10.7 GB at batch 64), a prefill step all
+15.7 GB, so L2 is not flushed between timed steps; the batch-1 line also
+reports the same steps with L2 flushed by a 256 MB write between them
+("l2_flushed"), which adds the write-back of that buffer's dirty lines and
+cold instruction and table fetches to every step.
 N > 1 runs independent replicas, one per GPU (weak scaling), timed between
 barriers; rank 0 reports the maximum over ranks.
 """
@@ -264,7 +269,8 @@ def time_workload(k3mx, wl, table, dev, steps, warmup, dist, flush):
     # library chains them as programmatic dependents, which per-kernel
     # events would serialise)
     for i in range(steps):
-        flush.zero_()
+        if flush is not None:
+            flush.zero_()
         ev[i][0].record(stream)
         k3mx.k3mx_moe_routed(y, xs[warmup + i], table, lgs[warmup + i], bias, ws, path=wl.path,
                              idx_out=idx[i], w_out=w)
@@ -277,7 +283,8 @@ def time_workload(k3mx, wl, table, dev, steps, warmup, dist, flush):
     k3mx.k3mx_trace_read()
     k3mx.k3mx_trace_enable(True)
     for i in range(steps):
-        flush.zero_()
+        if flush is not None:
+            flush.zero_()
         k3mx.k3mx_moe_routed(y, xs[warmup + i], table, lgs[warmup + i], bias, ws, path=wl.path,
                              idx_out=idx[i], w_out=w)
     torch.cuda.synchronize(dev)
@@ -316,7 +323,8 @@ def time_e2e(k3mx, wl, table, dev, steps, warmup, flush):
     stream = torch.cuda.current_stream(dev)
     ms = []
     for i in range(steps):
-        flush.zero_()
+        if flush is not None:
+            flush.zero_()
         torch.cuda.synchronize(dev)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -359,8 +367,12 @@ def run_ours(args):
     uuid = getattr(props, "uuid", None)
     clocks = ClockSampler(f"GPU-{uuid}" if uuid is not None else str(local))
     clocks.start()
-    res = time_workload(k3mx, primary, table, dev, args.steps, args.warmup, dist, flush)
+    res = time_workload(k3mx, primary, table, dev, args.steps, args.warmup, dist, None)
     clk = clocks.stop()
+    # the same workload with L2 flushed between steps (reported beside it)
+    res_fl = time_workload(k3mx, primary, table, dev, args.steps, args.warmup, dist, flush)
+    fl_ms = sum(res_fl["ms"])
+    fl_bytes = sum(d * EXPERT_BYTES for d in res_fl["distinct"])
 
     total_ms = sum(res["ms"])
     bytes_total = sum(d * EXPERT_BYTES for d in res["distinct"])
@@ -401,8 +413,12 @@ def run_ours(args):
                    "latent": D, "inter": F, "arena_gb": round(E * EXPERT_BYTES / 1e9, 2),
                    "expert_bytes_per_step": 16 * EXPERT_BYTES, "x": "fp32 N(0,1)",
                    "logits": "fresh seeded N(0,1) per step", "bias": "N(0,0.1)",
-                   "l2": "flushed between timed steps (256 MB write, outside the events)",
+                   "l2": "not flushed: every step streams 280.8 MB of experts it has not just used "
+                         "(2.2x the 129 MB L2)",
                    "parallelism": f"replicas x{world}"},
+        "l2_flushed": {"value": round(fl_bytes / (fl_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+                       "ms_per_step": round(fl_ms / len(res_fl["ms"]), 4),
+                       "flush": "256 MB write between timed steps, outside the events"},
         "hbm_frac": round(value / world / hbm_peak, 4),
         "hbm_frac_nominal_8tbs": round(value / world / 8000.0, 4),
         "roofline": {"kernel": dom, "bound": "hbm",
@@ -418,7 +434,7 @@ def run_ours(args):
 
     if rank == 0:
         # end to end through the host-buffer entry point
-        e2e_ms, h2d, d2h = time_e2e(k3mx, primary, table, dev, args.steps, args.warmup, flush)
+        e2e_ms, h2d, d2h = time_e2e(k3mx, primary, table, dev, args.steps, args.warmup, None)
         e2e_gbs = 16 * EXPERT_BYTES * len(e2e_ms) / (sum(e2e_ms) / 1e3) / 1e9 * world
         line["e2e"] = {"value": round(e2e_gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h, "ms_per_step": round(sum(e2e_ms) / len(e2e_ms), 4)}
@@ -426,7 +442,7 @@ def run_ours(args):
         sec = {}
         if not args.primary_only:
             wl = Workload("moe_decode_b64", 64, True, k3mx.K3MX_PATH_DECODE)
-            r = time_workload(k3mx, wl, table, dev, max(3, args.steps // 2), args.warmup, None, flush)
+            r = time_workload(k3mx, wl, table, dev, max(3, args.steps // 2), args.warmup, None, None)
             ms = sum(r["ms"])
             b = sum(d * EXPERT_BYTES for d in r["distinct"])
             sec["moe_decode_b64"] = {"GB_s": round(b / (ms / 1e3) / 1e9, 2),
@@ -442,7 +458,7 @@ def run_ours(args):
             for wname, wpath, srcs in (("moe_prefill_4096", k3mx.K3MX_PATH_PREFILL, PREFILL_SOURCES),
                                        ("moe_prefill_4096_mx", k3mx.K3MX_PATH_PREFILL_MX, PREFILL_MX_SOURCES)):
                 wl = Workload(wname, 4096, True, wpath)
-                r = time_workload(k3mx, wl, table, dev, max(3, args.steps // 4), args.warmup, None, flush)
+                r = time_workload(k3mx, wl, table, dev, max(3, args.steps // 4), args.warmup, None, None)
                 ms = sum(r["ms"]) / len(r["ms"])
                 pairs = 4096 * K
                 flops = 2.0 * PARAMS_PER_EXPERT * pairs

@@ -293,6 +293,10 @@ int k3mx_trace_read(k3mx_trace_entry *out, int max_entries);
 /* a static string naming a status code */
 const char *k3mx_status_str(k3mx_status status);
 
+/* the name of the last CUDA error that a call made on this host thread
+ * reported as K3MX_ECUDA ("cudaSuccess" if none); a static string */
+const char *k3mx_last_cuda_error(void);
+
 /* version of this ABI, (major << 16) | minor */
 int k3mx_abi_version(void);
 

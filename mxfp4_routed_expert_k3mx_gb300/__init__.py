@@ -35,7 +35,10 @@ STATUS = {0: "K3MX_OK", 1: "K3MX_EINVAL", 2: "K3MX_EALIGN", 3: "K3MX_ESHAPE",
 class K3mxError(RuntimeError):
     def __init__(self, func, status):
         self.status = status
-        super().__init__(f"{func} failed: {STATUS.get(status, status)} ({lib().k3mx_status_str(status).decode()})")
+        msg = f"{func} failed: {STATUS.get(status, status)} ({lib().k3mx_status_str(status).decode()})"
+        if status == 5:
+            msg += f": {lib().k3mx_last_cuda_error().decode()}"
+        super().__init__(msg)
 
 
 class Expert(ctypes.Structure):
@@ -75,6 +78,7 @@ def lib():
             "k3mx_moe_decode_noalloc": ([vp, vp, i, i, vp, vp, vp, vp, vp, vp], i),
             "k3mx_device_status": ([vp, ctypes.POINTER(ctypes.c_int)], i),
             "k3mx_status_str": ([i], ctypes.c_char_p),
+            "k3mx_last_cuda_error": ([], ctypes.c_char_p),
             "k3mx_abi_version": ([], i),
             "k3mx_trace_enable": ([i], i),
             "k3mx_trace_read": ([ctypes.POINTER(TraceEntry), i], i),

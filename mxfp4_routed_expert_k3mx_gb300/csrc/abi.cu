@@ -86,7 +86,14 @@ bool expert_ok(const k3mx_expert *e) {
            aligned16(e->s2);
 }
 
-k3mx_status from_cuda(cudaError_t err) { return err == cudaSuccess ? K3MX_OK : K3MX_ECUDA; }
+// the last CUDA error a call of this thread reported as K3MX_ECUDA
+thread_local cudaError_t g_last_cuda = cudaSuccess;
+
+k3mx_status from_cuda(cudaError_t err) {
+    if (err == cudaSuccess) return K3MX_OK;
+    g_last_cuda = err;
+    return K3MX_ECUDA;
+}
 
 // the device address of a page-locked host buffer mapped into the device's
 // address space, or nullptr (pageable or unknown memory)
@@ -248,7 +255,7 @@ k3mx_status run_moe(const Ctx &c, float *y, const void *x, int x_dtype, int n_to
             err = traced("group", c.stream,
                          [&] { return launch_group(c, idx, n_tokens, g, at<void>(ws, L.hist)); });
     }
-    if (err != cudaSuccess) return K3MX_ECUDA;
+    if (err != cudaSuccess) return from_cuda(err);
     const int max_active = n_tokens * kK < kE ? n_tokens * kK : kE;
 
     if (path == K3MX_PATH_PREFILL || path == K3MX_PATH_PREFILL_MX) {
@@ -301,6 +308,10 @@ using namespace k3mx;
 extern "C" {
 
 int k3mx_abi_version(void) { return (1 << 16) | 0; }
+
+const char *k3mx_last_cuda_error(void) {
+    return g_last_cuda == cudaSuccess ? "cudaSuccess" : cudaGetErrorName(g_last_cuda);
+}
 
 const char *k3mx_status_str(k3mx_status s) {
     switch (s) {

@@ -15,7 +15,7 @@ FAKE = 0x10000          # an aligned, non-null address that is never dereference
 def test_library_exports_every_declared_symbol():
     L = k3mx.lib()
     declared = k3mx.declared_symbols()
-    assert len(declared) == 18
+    assert len(declared) == 19
     out = subprocess.run(["nm", "-D", "--defined-only", k3mx.LIB_PATH],
                          capture_output=True, text=True, check=True).stdout
     exported = set(re.findall(r"\sT\s(k3mx_\w+)", out))
@@ -29,6 +29,7 @@ def test_status_strings_and_version():
     for code in range(8):
         assert k3mx.k3mx_status_str(code)
     assert k3mx.k3mx_status_str(99) == "unknown status"
+    assert k3mx.lib().k3mx_last_cuda_error() in (b"cudaSuccess", b"cudaErrorNoDevice", b"cudaErrorInsufficientDriver")
 
 
 def test_gemv_refuses_bad_arguments():
