@@ -62,6 +62,10 @@ def _load():
             lib.orc_route.argtypes = [vp, vp, vp, vp, vp, i, i, i, ctypes.c_float]
             lib.orc_topp.argtypes = [vp, vp, vp, i, i, i, ctypes.c_float, ctypes.c_double]
             lib.orc_group.argtypes = [vp, vp, vp, vp, i, i, i]
+            lib.orc_bf16.restype = ctypes.c_double
+            lib.orc_bf16.argtypes = [ctypes.c_uint16]
+            lib.orc_router_logits.argtypes = [vp, vp, vp, i, i, i, i]
+            lib.orc_router_absdot.argtypes = [vp, vp, vp, i, i, i, i]
             lib.orc_group.restype = i
             lib.orc_moe.argtypes = [vp, vp, i, vp, vp, vp, i, i, i, vp]
             lib.orc_num_threads.restype = i
@@ -168,6 +172,40 @@ def route_topp(logits, bias, p, k=16, routed_scale=1.0):
     T, E = s.shape
     _load().orc_topp(_p(idx), _p(w), _p(s), T, E, k, routed_scale, float(p))
     return idx, w
+
+
+def bf16(bits):
+    """A bf16 bit pattern as a float."""
+    return float(_load().orc_bf16(int(bits)))
+
+
+def _router_args(W, h):
+    W = np.ascontiguousarray(W, np.uint16)
+    if h.dtype == np.uint16:
+        hb, h = 1, np.ascontiguousarray(h, np.uint16)
+    else:
+        hb, h = 0, np.ascontiguousarray(h, np.float32)
+    E, C = W.shape
+    T = h.shape[0]
+    assert h.shape == (T, C)
+    return W, h, hb, T, E, C
+
+
+def router_logits(W, h):
+    """Router logits [T, E] fp32 from bf16 router weights W [E, C] (uint16
+    bit patterns) and the hidden state h [T, C] (fp32, or uint16 bf16)."""
+    W, h, hb, T, E, C = _router_args(W, h)
+    out = np.empty((T, E), np.float32)
+    _load().orc_router_logits(_p(out), _p(W), _p(h), hb, T, E, C)
+    return out
+
+
+def router_absdot(W, h):
+    """sum_c |W[e,c] h[t,c]| [T, E] in double: the scale of a logit's tolerance."""
+    W, h, hb, T, E, C = _router_args(W, h)
+    out = np.empty((T, E), np.float64)
+    _load().orc_router_absdot(_p(out), _p(W), _p(h), hb, T, E, C)
+    return out
 
 
 def group(idx, n_experts=896):

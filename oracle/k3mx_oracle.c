@@ -33,6 +33,11 @@
  *        routed_scale 1.0, moe_renorm 1, situ_b1 4.0, situ_b2 25.0.
  *   [P]  Kimi K3 engine (c/kimi_k3.c), "Chunked prefill": within a chunk every
  *        unique expert is loaded once for all the tokens that chose it.
+ *   [RG] Kimi K3 engine (c/kimi_k3.c), "Architecture notes", Stable
+ *        LatentMoE bullet: the sigmoid router is a [896, 7168] matrix applied
+ *        to the 7168-wide hidden state; its outputs are the logits [A] takes.
+ *        The trunk (router included) is bf16 (kimi-k3-in-c README, the
+ *        resident set of budget.py: "norms, router gates, biases").
  *   [TP] Kimi K3 engine (c/kimi_k3.c), "Streaming design" (K3_TOPP) and the
  *        environment table: optionally keep the routed experts only up to a
  *        cumulative weight p, dropping the low-weight tail of the top-16 and
@@ -236,6 +241,56 @@ void orc_route(int32_t *idx, float *w, float *s_out, const float *logits,
         for (int k = 0; k < K; k++)
             w[(size_t)t * K + k] =
                 (float)((double)s[idx[(size_t)t * K + k]] / sum) * routed_scale;
+    }
+}
+
+/* a bf16 bit pattern as a double: the upper half of an fp32 */
+double orc_bf16(uint16_t b)
+{
+    const uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/*
+ * Router logits [RG]:  logits[t][e] = (float) sum_c W[e][c] * h[t][c]
+ * W: [E][C] bf16 row-major; h: [T][C] fp32 (h_bf16 = 0) or bf16 (h_bf16 = 1).
+ * Every product is exact in double (8 + 24 significant bits); the sum runs
+ * over c in ascending order in double and is rounded to fp32 once.
+ */
+void orc_router_logits(float *logits, const uint16_t *W, const void *h, int h_bf16, int T, int E, int C)
+{
+    #pragma omp parallel for collapse(2) schedule(static)
+    for (int t = 0; t < T; t++) {
+        for (int e = 0; e < E; e++) {
+            const uint16_t *we = W + (size_t)e * C;
+            double acc = 0.0;
+            for (int c = 0; c < C; c++) {
+                const double hv = h_bf16 ? orc_bf16(((const uint16_t *)h)[(size_t)t * C + c])
+                                         : (double)((const float *)h)[(size_t)t * C + c];
+                acc += orc_bf16(we[c]) * hv;
+            }
+            logits[(size_t)t * E + e] = (float)acc;
+        }
+    }
+}
+
+/* The tolerance scale of a logit: sum_c |W[e][c] h[t][c]| in double. */
+void orc_router_absdot(double *b, const uint16_t *W, const void *h, int h_bf16, int T, int E, int C)
+{
+    #pragma omp parallel for collapse(2) schedule(static)
+    for (int t = 0; t < T; t++) {
+        for (int e = 0; e < E; e++) {
+            const uint16_t *we = W + (size_t)e * C;
+            double acc = 0.0;
+            for (int c = 0; c < C; c++) {
+                const double hv = h_bf16 ? orc_bf16(((const uint16_t *)h)[(size_t)t * C + c])
+                                         : (double)((const float *)h)[(size_t)t * C + c];
+                acc += fabs(orc_bf16(we[c]) * hv);
+            }
+            b[(size_t)t * E + e] = acc;
+        }
     }
 }
 

@@ -9,6 +9,7 @@ Stream numbering (seed is the workload seed, 0 unless stated):
   STREAM_W_PACKED / STREAM_W_SCALES : the single GEMV matrix W
   STREAM_X                          : token activations
   STREAM_LOGITS / STREAM_BIAS       : router logits and score-correction bias
+  STREAM_ROUTER_W / STREAM_HIDDEN   : router weights and the hidden state
   expert e, tensor t                : 0x100000 + 8 e + t  (inside synth_expert)
 """
 import ctypes
@@ -29,12 +30,15 @@ STREAM_W_SCALES = 2
 STREAM_X = 10
 STREAM_LOGITS = 11
 STREAM_BIAS = 12
+STREAM_ROUTER_W = 13
+STREAM_HIDDEN = 14
 
 # Kimi-K3 routed-expert shape: latent width D, expert inter width F.
 D_LATENT = 3584
 F_INTER = 3072
 N_EXPERTS = 896
 TOP_K = 16
+H_MODEL = 7168          # hidden width the router reads
 
 
 def build(force=False):
@@ -162,6 +166,18 @@ def router_inputs(n_tokens, seed=0, E=N_EXPERTS, bias_std=0.1):
     logits = normal_f32(n_tokens * E, seed, STREAM_LOGITS).reshape(n_tokens, E)
     bias = normal_f32(E, seed, STREAM_BIAS, 0.0, bias_std)
     return logits, bias
+
+
+def router_weights(seed=0, E=N_EXPERTS, C=H_MODEL):
+    """Router weights ~ N(0, 1/C) rounded to bf16: uint16 bit patterns [E, C]
+    (with unit-variance hidden states the logits come out about N(0, 1))."""
+    w = normal_f32(E * C, seed, STREAM_ROUTER_W, 0.0, float(C) ** -0.5)
+    return f32_to_bf16(w).reshape(E, C)
+
+
+def hidden_inputs(n_tokens, seed=0, C=H_MODEL):
+    """Hidden states ~ N(0,1): fp32 [T, C]."""
+    return normal_f32(n_tokens * C, seed, STREAM_HIDDEN).reshape(n_tokens, C)
 
 
 def expert_arena_device(device, seed=0, lo=118, hi=128, n_experts=N_EXPERTS, chunk=16):

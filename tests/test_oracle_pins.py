@@ -450,3 +450,64 @@ def test_topp_equal_scores_keep_the_lowest_indices():
         assert np.all((i >= 0).sum(1) == n), p
         assert sorted(i[0][i[0] >= 0]) == list(range(n))
         assert np.all(w[i >= 0] == np.float32(1.0 / n))
+
+
+# ---- router logits (Kimi K3 engine (c/kimi_k3.c), "Architecture notes":
+# the sigmoid router [896, 7168] over the hidden state; bf16 trunk)
+
+def test_bf16_patterns():
+    """bf16 = the upper half of an fp32: sign, 8 exponent bits, 7 fraction bits."""
+    assert oracle.bf16(0x3F80) == 1.0
+    assert oracle.bf16(0xC000) == -2.0
+    assert oracle.bf16(0x3F81) == 1.0 + 2.0 ** -7
+    assert oracle.bf16(0x0001) == 2.0 ** -133            # smallest subnormal
+    assert oracle.bf16(0x7F80) == float("inf")
+    z = oracle.bf16(0x8000)
+    assert z == 0.0 and np.copysign(1.0, z) == -1.0
+
+
+def test_router_logits_one_hot_and_integers():
+    """A one-hot hidden state reads one column of W exactly; integer weights
+    and states give exact integer logits."""
+    rng = np.random.default_rng(61)
+    E, C = 5, 96
+    W = synth.f32_to_bf16(rng.standard_normal((E, C)).astype(np.float32))
+    for c in (0, 17, 95):
+        h = np.zeros((1, C), np.float32)
+        h[0, c] = 1.0
+        lg = oracle.router_logits(W, h)
+        assert [lg[0, e] for e in range(E)] == [oracle.bf16(W[e, c]) for e in range(E)]
+    Wi = rng.integers(-8, 9, (E, C)).astype(np.float32)       # small integers: exact in bf16
+    hi = rng.integers(-100, 101, (3, C)).astype(np.float32)
+    lg = oracle.router_logits(synth.f32_to_bf16(Wi), hi)
+    exact = hi.astype(np.int64) @ Wi.astype(np.int64).T        # integer arithmetic
+    assert np.array_equal(lg.astype(np.int64), exact) and np.all(lg == exact)
+
+
+def test_router_logits_linear_and_dtype_paths():
+    """Linear in h up to one fp32 rounding per logit; a bf16 hidden state
+    gives the same logits as its exact fp32 widening."""
+    W = synth.router_weights(seed=62, E=32, C=7168)
+    h1 = synth.hidden_inputs(2, seed=63)
+    h2 = synth.hidden_inputs(2, seed=64)
+    l1, l2, l12 = (oracle.router_logits(W, h) for h in (h1, h2, (h1 + h2).astype(np.float32)))
+    scale = oracle.router_absdot(W, h1) + oracle.router_absdot(W, h2)
+    assert np.all(np.abs(l12.astype(np.float64) - l1 - l2) <= 1e-6 * scale)
+    hb = synth.f32_to_bf16(h1)
+    assert np.array_equal(oracle.router_logits(W, hb), oracle.router_logits(W, synth.bf16_to_f32(hb)))
+
+
+def test_router_logits_brute_force_small():
+    """Against a numpy dot in float64 on tiny shapes (a different summation
+    order): equal within 1e-12 of sum |w h|, and the workload's scale gives
+    unit-variance logits."""
+    rng = np.random.default_rng(65)
+    for E, C in ((3, 32), (7, 100), (2, 7168)):
+        W = synth.f32_to_bf16(rng.standard_normal((E, C)).astype(np.float32))
+        h = rng.standard_normal((4, C)).astype(np.float32)
+        Wd = (W.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        ref = h.astype(np.float64) @ Wd.T
+        lg = oracle.router_logits(W, h)
+        assert np.all(np.abs(lg - ref) <= 1e-12 * (np.abs(h) @ np.abs(Wd).T) + np.abs(ref) * 2.0 ** -24)
+    lg = oracle.router_logits(synth.router_weights(seed=0, E=64), synth.hidden_inputs(8, seed=0))
+    assert 0.8 < lg.std() < 1.2
