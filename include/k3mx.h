@@ -155,6 +155,26 @@ k3mx_status k3mx_route_topp(int32_t *idx, float *w, const float *logits,
                             k3mx_stream_t stream);
 
 /*
+ * The router and its top-16 (Kimi K3 engine (c/kimi_k3.c), "Architecture
+ * notes", Stable LatentMoE: a sigmoid router [896, 7168] over the hidden
+ * state; the trunk, router included, is bf16):
+ *   logits[t][e] = sum_c router_w[e][c] * hidden[t][c]        (fp32 sums)
+ * followed by the routing of k3mx_route_topk (top_p > 0: k3mx_route_topp)
+ * on those logits.
+ *   logits [n_tokens][896] fp32 (written)
+ *   idx [n_tokens][16] int32, w [n_tokens][16] fp32 (written)
+ *   hidden [n_tokens][7168], h_dtype K3MX_F32 or K3MX_BF16
+ *   router_w [896][7168] bf16 bit patterns, row-major; bias [896] fp32
+ *   top_p: finite (<= 0: off); 1 <= n_tokens <= K3MX_MAX_TOKENS
+ * All pointers device, 16-byte aligned.  Each logit is within
+ * 1e-5 * sum_c |router_w[e][c] hidden[t][c]| of the exact sum; idx and w
+ * are exactly the routing of the logits written.
+ */
+k3mx_status k3mx_router(float *logits, int32_t *idx, float *w, const void *hidden, int h_dtype,
+                        const uint16_t *router_w, const float *bias, int n_tokens, float top_p,
+                        k3mx_stream_t stream);
+
+/*
  * Token-to-expert grouping (Kimi K3 engine (c/kimi_k3.c), "Chunked prefill":
  * each unique expert of a chunk is loaded once for all its tokens):
  *   counts [896]          pairs routed to each expert

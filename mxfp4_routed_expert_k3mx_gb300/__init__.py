@@ -68,6 +68,7 @@ def lib():
             "k3mx_expert_ffn": ([vp, vp, ctypes.POINTER(Expert), vp, sz, vp], i),
             "k3mx_route_topk": ([vp, vp, vp, vp, i, vp], i),
             "k3mx_route_topp": ([vp, vp, vp, vp, i, ctypes.c_float, vp], i),
+            "k3mx_router": ([vp, vp, vp, vp, i, vp, vp, i, ctypes.c_float, vp], i),
             "k3mx_group_workspace_size": ([i], sz),
             "k3mx_group": ([vp, vp, vp, vp, i, vp, sz, vp], i),
             "k3mx_moe_workspace_size": ([i, i, i], sz),
@@ -171,6 +172,23 @@ def k3mx_route_topk(idx, w, logits, bias, stream=None):
     _check("k3mx_route_topk", lib().k3mx_route_topk(_ptr(idx), _ptr(w), _ptr(logits), _ptr(bias), T,
                                                      _stream(stream)))
     return idx, w
+
+
+def k3mx_router(logits, idx, w, hidden, router_w, bias, top_p=0.0, stream=None):
+    """Router logits from the hidden state (fp32 or bf16 [T, 7168]) and the
+    bf16 router weights (int16 or uint16-viewed [896, 7168]), then the top-16."""
+    _dev(logits, torch.float32, "logits")
+    _dev(idx, torch.int32, "idx")
+    _dev(w, torch.float32, "w")
+    _dev(bias, torch.float32, "bias")
+    if not (router_w.is_cuda and router_w.is_contiguous() and router_w.element_size() == 2):
+        raise ValueError("router_w: contiguous 16-bit device tensor expected")
+    if not (hidden.is_cuda and hidden.is_contiguous()):
+        raise ValueError("hidden: contiguous device tensor expected")
+    T = hidden.shape[0]
+    _check("k3mx_router", lib().k3mx_router(_ptr(logits), _ptr(idx), _ptr(w), _ptr(hidden), _x_dtype(hidden),
+                                            _ptr(router_w), _ptr(bias), T, float(top_p), _stream(stream)))
+    return logits, idx, w
 
 
 def k3mx_route_topp(idx, w, logits, bias, top_p, stream=None):

@@ -400,6 +400,33 @@ k3mx_status k3mx_route_topp(int32_t *idx, float *w, const float *logits, const f
                             [&] { return launch_route(c, idx, w, logits, bias, n_tokens, (double)top_p); }));
 }
 
+k3mx_status k3mx_router(float *logits, int32_t *idx, float *w, const void *hidden, int h_dtype,
+                        const uint16_t *router_w, const float *bias, int n_tokens, float top_p,
+                        k3mx_stream_t stream) {
+    if (!logits || !idx || !w || !hidden || !router_w || !bias) return K3MX_EINVAL;
+    if (h_dtype != K3MX_F32 && h_dtype != K3MX_BF16) return K3MX_EINVAL;
+    if (!(top_p == top_p) || top_p == INFINITY || top_p == -INFINITY) return K3MX_EINVAL;
+    if (n_tokens < 1 || n_tokens > K3MX_MAX_TOKENS) return K3MX_ESHAPE;
+    if (!aligned16(logits) || !aligned16(idx) || !aligned16(w) || !aligned16(hidden) || !aligned16(router_w) ||
+        !aligned16(bias))
+        return K3MX_EALIGN;
+    Ctx c;
+    k3mx_status st = device_ctx(reinterpret_cast<cudaStream_t>(stream), c);
+    if (st != K3MX_OK) return st;
+    cudaError_t err = traced("router", c.stream, [&] {
+        return launch_router_logits(c, logits, hidden, h_dtype == K3MX_BF16 ? 1 : 0, router_w, n_tokens);
+    });
+    if (err != cudaSuccess) return from_cuda(err);
+    // the top-16 as a programmatic dependent of the logits
+    err = traced("route", c.stream, [&] {
+        return n_tokens * kK <= 1024
+                   ? launch_route_prep(c, idx, w, logits, bias, n_tokens, nullptr, 0, nullptr, nullptr, nullptr, 0,
+                                       nullptr, nullptr, (double)top_p, true)
+                   : launch_route(c, idx, w, logits, bias, n_tokens, (double)top_p, true);
+    });
+    return from_cuda(err);
+}
+
 size_t k3mx_group_workspace_size(int n_tokens) {
     if (n_tokens < 1 || n_tokens > K3MX_MAX_TOKENS) return 0;
     return up256((kE + 1) * 4) + up256(kE * 4) + up256(group_scratch_bytes(n_tokens));

@@ -271,7 +271,12 @@ struct GroupOut {
 // top_p > 0: the low-weight tail of each token's 16 experts is dropped
 // (index -1, weight 0), the kept weights renormalised
 cudaError_t launch_route(const Ctx &c, int32_t *idx, float *w, const float *logits,
-                         const float *bias, int n_tokens, double top_p);
+                         const float *bias, int n_tokens, double top_p,
+                         bool pdl = false);
+// router logits [T][896] = W [896][7168] (bf16) times hidden [T][7168] (fp32
+// or bf16), launched as a programmatic dependent
+cudaError_t launch_router_logits(const Ctx &c, float *logits, const void *h, int h_bf16, const uint16_t *W,
+                                 int n_tokens);
 // routing with one CTA per token (n_tokens <= 64) plus, when x is given, the
 // tokens' x piece images and the weight tensor maps of the expert table
 // (mx path) in the same launch; a single token with `g_one` is also
@@ -279,7 +284,8 @@ cudaError_t launch_route(const Ctx &c, int32_t *idx, float *w, const float *logi
 cudaError_t launch_route_prep(const Ctx &c, int32_t *idx, float *w, const float *logits,
                               const float *bias, int n_tokens, const void *x, int x_bf16,
                               uint8_t *ximg, const GroupOut *g_one, int *flags, int n_flags,
-                              const k3mx_expert *experts, uint8_t *maps, double top_p);
+                              const k3mx_expert *experts, uint8_t *maps, double top_p,
+                              bool pdl = false);
 // grouping of n_tokens * 16 <= 1024 pairs, programmatic dependent of the routing
 cudaError_t launch_group_small(const Ctx &c, const int32_t *idx, int n_tokens, const GroupOut &g);
 size_t group_scratch_bytes(int n_tokens);

@@ -296,6 +296,7 @@ __device__ void route_warp(const float *__restrict__ lt, const float *__restrict
 __global__ void __launch_bounds__(256) k_route(int32_t *idx, float *w, const float *logits,
                                                const float *bias, int n_tokens, double top_p) {
     __shared__ int scratch[8][128];
+    pdl_wait();                          // the logits, when a router pass writes them
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int t = blockIdx.x * (blockDim.x / 32) + warp;
     if (t >= n_tokens) return;
@@ -600,6 +601,7 @@ k_route_prep(int32_t *idx, float *w, const float *logits, const float *bias, int
     __shared__ RouteSmem sm;
     // the expert passes may launch now: their prologues overlap this kernel
     pdl_launch_dependents();
+    pdl_wait();                          // the logits, when a router pass writes them
     if ((int)blockIdx.x < n_tokens) {
         const int t = blockIdx.x;
         route_cta(logits + (size_t)t * kE, bias, idx + (size_t)t * kK, w + (size_t)t * kK, sm, top_p);
@@ -693,17 +695,18 @@ k_group_scatter(const int32_t *idx, int n_pairs, const int *base, int32_t *perm)
 }  // namespace
 
 cudaError_t launch_route(const Ctx &c, int32_t *idx, float *w, const float *logits,
-                         const float *bias, int n_tokens, double top_p) {
+                         const float *bias, int n_tokens, double top_p, bool pdl) {
     const int per_block = 8;
-    k_route<<<(n_tokens + per_block - 1) / per_block, 32 * per_block, 0, c.stream>>>(
-        idx, w, logits, bias, n_tokens, top_p);
+    const dim3 grid((n_tokens + per_block - 1) / per_block);
+    if (pdl) return launch_pdl(k_route, grid, dim3(32 * per_block), 0, c.stream, idx, w, logits, bias, n_tokens, top_p);
+    k_route<<<grid, 32 * per_block, 0, c.stream>>>(idx, w, logits, bias, n_tokens, top_p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_route_prep(const Ctx &c, int32_t *idx, float *w, const float *logits,
                               const float *bias, int n_tokens, const void *x, int x_bf16,
                               uint8_t *ximg, const GroupOut *g_one, int *flags, int n_flags,
-                              const k3mx_expert *experts, uint8_t *maps, double top_p) {
+                              const k3mx_expert *experts, uint8_t *maps, double top_p, bool pdl) {
     const int piece_ctas = x != nullptr ? (n_tokens * (kD / 32) + kRT / 32 - 1) / (kRT / 32) : 0;
     CUtensorMap w13{}, w2{};
     int map_ctas = 0;
@@ -713,9 +716,12 @@ cudaError_t launch_route_prep(const Ctx &c, int32_t *idx, float *w, const float 
     }
     GroupOut g{};
     if (g_one != nullptr && n_tokens == 1) g = *g_one;
-    k_route_prep<<<n_tokens + piece_ctas + map_ctas, kRT, 0, c.stream>>>(
-        idx, w, logits, bias, n_tokens, x, x_bf16, ximg, g, flags, flags ? n_flags : 0, experts, piece_ctas, maps,
-        top_p, w13, w2);
+    const dim3 grid(n_tokens + piece_ctas + map_ctas);
+    if (pdl)
+        return launch_pdl(k_route_prep, grid, dim3(kRT), 0, c.stream, idx, w, logits, bias, n_tokens, x, x_bf16,
+                          ximg, g, flags, flags ? n_flags : 0, experts, piece_ctas, maps, top_p, w13, w2);
+    k_route_prep<<<grid, kRT, 0, c.stream>>>(idx, w, logits, bias, n_tokens, x, x_bf16, ximg, g, flags,
+                                             flags ? n_flags : 0, experts, piece_ctas, maps, top_p, w13, w2);
     return cudaGetLastError();
 }
 

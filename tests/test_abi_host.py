@@ -15,7 +15,7 @@ FAKE = 0x10000          # an aligned, non-null address that is never dereference
 def test_library_exports_every_declared_symbol():
     L = k3mx.lib()
     declared = k3mx.declared_symbols()
-    assert len(declared) == 19
+    assert len(declared) == 20
     out = subprocess.run(["nm", "-D", "--defined-only", k3mx.LIB_PATH],
                          capture_output=True, text=True, check=True).stdout
     exported = set(re.findall(r"\sT\s(k3mx_\w+)", out))
@@ -58,6 +58,18 @@ def test_route_group_refuse_bad_arguments():
     assert ws > 0 and k3mx.k3mx_group_workspace_size(0) == 0
     assert L.k3mx_group(FAKE, FAKE, FAKE, FAKE, 64, FAKE, ws - 1, None) == 4
     assert L.k3mx_group(FAKE, FAKE, FAKE, FAKE, 64, None, ws, None) == 4
+
+
+def test_router_refuses_bad_arguments():
+    L = k3mx.lib()
+    ok = dict(lg=FAKE, idx=FAKE, w=FAKE, h=FAKE, dt=0, W=FAKE, b=FAKE, T=1, p=0.0)
+    call = lambda **kw: L.k3mx_router(*(dict(ok, **kw)[k] for k in ("lg", "idx", "w", "h", "dt", "W", "b", "T", "p")),
+                                      None)
+    assert call(W=None) == 1
+    assert call(dt=2) == 1                           # unknown hidden dtype
+    assert call(p=float("nan")) == 1
+    assert call(T=0) == 3 and call(T=65537) == 3
+    assert call(h=FAKE + 4) == 2 and call(W=FAKE + 8) == 2
 
 
 def test_moe_refuses_bad_arguments():
