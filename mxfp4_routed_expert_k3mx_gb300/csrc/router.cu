@@ -7,8 +7,14 @@
 // are fp32.  The top-16 of the logits is the routing kernels' work
 // (route_group.cu), launched right behind as programmatic dependents.
 //
-// Few tokens (decode): k_router_gemv, one warp per router row with the row
-// held in registers, HBM-bound on the 12.8 MB of weights.
+// Few tokens (decode), or fp32 states: k_router_gemv, one warp per router
+// row with the row held in registers, HBM-bound on the 12.8 MB of weights.
+// Many bf16 states (prefill): k_router_gemm, the tcgen05 tensor cores
+// (kind::f16 with bf16 A and B, fp32 accumulators in TMEM); a CTA computes
+// 128 router rows x 256 tokens over the whole 7168-deep sum, its operands
+// streamed by TMA (128-byte swizzle) through a 4-stage ring.
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 
 namespace k3mx {
@@ -105,10 +111,172 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1)
     }
 }
 
+// ----------------------------------------------------- tensor-core GEMM --
+
+constexpr int kGM = 128, kGN = 256, kGK = 64;    // tile: router rows x tokens x K per stage
+constexpr int kGStages = 4;
+constexpr int kGABytes = kGM * kGK * 2, kGBBytes = kGN * kGK * 2;
+constexpr int kGStage = kGABytes + kGBBytes;
+constexpr int kGKSteps = kH / kGK;               // 112
+constexpr int kGThreads = 192;                   // warp 0 TMA, 1 MMA, 2-5 epilogue
+constexpr int kGSmem = 1024 + 1024 + kGStages * kGStage;
+constexpr int kGemmMinTokens = 17;               // from here on the tensor cores
+static_assert(kE % kGM == 0 && kH % kGK == 0, "router tiles");
+
+struct GHdr {
+    uint64_t full[kGStages], empty[kGStages], accf;
+    uint32_t tmem;
+};
+
+// bf16 A and B, f32 accumulator, both K-major, M x N
+__device__ __forceinline__ uint32_t idesc_bf16(int m, int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void tma_2d_plain(uint32_t dst, const void *map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(dst),
+        "l"(map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__global__ void __launch_bounds__(kGThreads, 1)
+    k_router_gemm(float *__restrict__ logits, int n_tokens, int *status, const __grid_constant__ CUtensorMap wmap,
+                  const __grid_constant__ CUtensorMap hmap) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    GHdr *hd = reinterpret_cast<GHdr *>(smem);
+    const uint32_t st0 = smem_addr(smem) + 1024;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t full0 = smem_addr(hd->full), empty0 = smem_addr(hd->empty), accf = smem_addr(&hd->accf);
+    const int m0 = blockIdx.x * kGM, n0 = blockIdx.y * kGN;
+    if (tid == 0) {
+        for (int i = 0; i < kGStages; i++) {
+            mbar_init(full0 + 8 * i, 1);
+            mbar_init(empty0 + 8 * i, 1);
+        }
+        mbar_init(accf, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(smem_addr(&hd->tmem), kGN);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = hd->tmem;
+    pdl_launch_dependents();
+    bool ok = true;
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer --
+        if (lane == 0) {
+            pdl_wait();                               // the hidden states, if a kernel before writes them
+            for (int k = 0; k < kGKSteps; k++) {
+                const int s = k % kGStages;
+                if (k >= kGStages && !mbar_wait(empty0 + 8 * s, ((k / kGStages) - 1) & 1)) {
+                    report_status(status, kStatusWaitTimeout, 300);
+                    ok = false;
+                    break;
+                }
+                const uint32_t dst = st0 + s * kGStage;
+                mbar_arrive_expect_tx(full0 + 8 * s, kGStage);
+                tma_2d_plain(dst, &wmap, k * kGK, m0, full0 + 8 * s);
+                tma_2d_plain(dst + kGABytes, &hmap, k * kGK, n0, full0 + 8 * s);
+            }
+        }
+    } else if (warp == 1) {
+        // -------------------------------------------------- MMA issuer --
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16(kGM, kGN);
+            for (int k = 0; k < kGKSteps; k++) {
+                const int s = k % kGStages;
+                if (!mbar_wait(full0 + 8 * s, (k / kGStages) & 1)) {
+                    report_status(status, kStatusWaitTimeout, 301);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a = st0 + s * kGStage, b = a + kGABytes;
+#pragma unroll
+                for (int k16 = 0; k16 < kGK / 16; k16++)
+                    umma_f16(tmem, umma_desc_sw128(a + 32 * k16), umma_desc_sw128(b + 32 * k16), idesc,
+                             (k > 0 || k16 > 0) ? 1u : 0u);
+                umma_commit(empty0 + 8 * s);          // the stage is free once these finish
+            }
+            umma_commit(accf);                        // every MMA issued so far has finished
+        }
+    } else {
+        // --------------------------------------------------- epilogue --
+        const int q = warp & 3;                       // TMEM lane quarter of this warp
+        const int e = m0 + 32 * q + lane;
+        if (mbar_wait(accf, 0)) {
+            tc_fence_after();
+            const uint32_t base = tmem + ((uint32_t)(32 * q) << 16);
+            for (int c0 = 0; c0 < kGN; c0 += 16) {
+                if (n0 + c0 >= n_tokens) break;
+                uint32_t v[16];
+                tmem_ld16(base + c0, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; j++) {
+                    const int t = n0 + c0 + j;
+                    if (t < n_tokens) logits[(size_t)t * kE + e] = __uint_as_float(v[j]);
+                }
+            }
+        } else if (lane == 0) {
+            report_status(status, kStatusWaitTimeout, 302);
+        }
+    }
+    (void)ok;
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kGN);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 router_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }
+    return fn;
+}
+
+// bf16 [rows][kH] row-major, boxes of box_rows x 64 (128 bytes, 128-byte swizzle)
+bool encode_bf16_rows(CUtensorMap &m, const void *base, uint64_t rows, uint32_t box_rows) {
+    auto enc = router_encoder();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)kH, rows}, strides[1] = {(cuuint64_t)kH * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kGK, box_rows}, es[2] = {1, 1};
+    return enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 cudaError_t launch_router_logits(const Ctx &c, float *logits, const void *h, int h_bf16, const uint16_t *W,
                                  int n_tokens) {
+    if (h_bf16 && n_tokens >= kGemmMinTokens) {
+        static bool gconf = false;
+        if (!gconf) {
+            const cudaError_t e = cudaFuncSetAttribute(k_router_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmem);
+            if (e != cudaSuccess) return e;
+            gconf = true;
+        }
+        CUtensorMap wm, hm;
+        if (!encode_bf16_rows(wm, W, kE, kGM) || !encode_bf16_rows(hm, h, (uint64_t)n_tokens, kGN))
+            return cudaErrorInvalidValue;
+        const dim3 grid(kE / kGM, (n_tokens + kGN - 1) / kGN);
+        return launch_pdl(k_router_gemm, grid, dim3(kGThreads), (size_t)kGSmem, c.stream, logits, n_tokens,
+                          c.status, wm, hm);
+    }
     static bool configured = false;
     if (!configured) {
         const cudaError_t e =

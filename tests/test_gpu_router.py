@@ -58,13 +58,31 @@ def test_router_fp32_hidden(cuda_dev, router_w, T):
     assert 0.8 < lg.std() < 1.2                      # unit-variance logits by construction
 
 
-@pytest.mark.parametrize("T", [1, 5, 300])
+@pytest.mark.parametrize("T", [1, 5, 16, 17, 300])
 def test_router_bf16_hidden(cuda_dev, router_w, T):
+    """bf16 states: CUDA cores up to 16 tokens, tensor cores from 17 (a
+    ragged last tile of 256 tokens)."""
     W, Wt = router_w
     hb = synth.f32_to_bf16(synth.hidden_inputs(T, seed=40 + T))
     _, bias = synth.router_inputs(1, seed=40 + T)
     lg, idx, w = run_router(cuda_dev, Wt, hb, bias)
     check(W, hb, lg, idx, w, bias)
+
+
+def test_router_bf16_prefill_4096(cuda_dev, router_w):
+    """The prefill batch (16 token tiles x 7 router-row tiles): sampled
+    tokens against the oracle, the routing of every token bit-exact."""
+    W, Wt = router_w
+    T = 4096
+    hb = synth.f32_to_bf16(synth.hidden_inputs(T, seed=4096))
+    _, bias = synth.router_inputs(1, seed=4096)
+    lg, idx, w = run_router(cuda_dev, Wt, hb, bias)
+    tokens = np.array([0, 1, 255, 256, 1000, 2047, 3840, 4095])
+    ref = oracle.router_logits(W, hb[tokens])
+    scale = oracle.router_absdot(W, hb[tokens])
+    assert np.all(np.abs(lg[tokens].astype(np.float64) - ref) <= 1e-5 * scale)
+    ir, wr = oracle.route(lg, bias)
+    assert np.array_equal(idx, ir) and np.array_equal(w.view(np.uint32), wr.view(np.uint32))
 
 
 def test_router_top_p(cuda_dev, router_w):
