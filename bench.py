@@ -10,7 +10,7 @@ streamed per second (GB/s); the line also carries the batch-64 decode and
 4096-token prefill workloads under "secondary".
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference]
-  python bench.py --profile-case decode|prefill --tokens T [--resident R]
+  python bench.py --profile-case decode|prefill|router --tokens T [--resident R]
                   [--confine] [--mx] [--iters I]
 
 The --profile-case form runs a small case of one path for Nsight Compute
@@ -51,7 +51,7 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
 # kernels per traced launch group
-KERNELS_PER_GROUP = {"route": 1, "group_small": 1, "group": 3, "mx_pieces": 1,
+KERNELS_PER_GROUP = {"router": 1, "route": 1, "group_small": 1, "group": 3, "mx_pieces": 1,
                      "decode_expert": 1, "decode_gate_up": 1, "decode_down": 1, "combine": 1,
                      "prefill_prep": 3, "prefill_gate_up": 1, "prefill_down": 1}
 PARAMS_PER_EXPERT = 33030144
@@ -337,6 +337,59 @@ def time_e2e(k3mx, wl, table, dev, steps, warmup, flush):
     return ms, h2d, d2h
 
 
+def time_router(k3mx, dev, flush, steps, warmup, bf16_peak, hbm_peak):
+    """The router (logits of the bf16 [896, 7168] router, then the top-16)
+    at one fp32 decode token and at 4096 bf16 prefill tokens.  Its inputs fit
+    in L2, so L2 is flushed (256 MB write) before every timed call."""
+    import numpy as np
+    import torch
+    import synth
+    W = torch.from_numpy(synth.router_weights(seed=0).view(np.int16)).to(dev)
+    _, bias_np = synth.router_inputs(1, seed=0)
+    bias = torch.from_numpy(bias_np).to(dev)
+    out = {}
+    stream = torch.cuda.current_stream(dev)
+    for name, T, bf16 in (("router_b1", 1, False), ("router_4096", 4096, True)):
+        h = synth.hidden_inputs(T, seed=1)
+        ht = (torch.from_numpy(synth.f32_to_bf16(h).view(np.int16)).view(torch.bfloat16) if bf16
+              else torch.from_numpy(h)).to(dev)
+        lg = torch.empty((T, E), dtype=torch.float32, device=dev)
+        idx = torch.empty((T, K), dtype=torch.int32, device=dev)
+        w = torch.empty((T, K), dtype=torch.float32, device=dev)
+        for _ in range(warmup):
+            k3mx.k3mx_router(lg, idx, w, ht, W, bias)
+        ms = []
+        k3mx.k3mx_trace_read()
+        k3mx.k3mx_trace_enable(True)
+        for _ in range(steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            k3mx.k3mx_router(lg, idx, w, ht, W, bias)
+            b.record(stream)
+            b.synchronize()
+            ms.append(a.elapsed_time(b))
+        k3mx.k3mx_trace_enable(False)
+        tr = k3mx.k3mx_trace_read()
+        m = statistics.median(ms)
+        wbytes = E * 7168 * 2
+        flops = 2.0 * T * E * 7168
+        r = {"us_per_call": round(1e3 * m, 2), "tokens_per_s": round(T / (m / 1e3), 1),
+             "kernels": {k: {"launches": v[0], "avg_us": round(1e3 * v[1] / max(1, v[0]), 2)} for k, v in tr.items()},
+             "l2": "flushed before every call (256 MB write, outside the events)"}
+        if "router" in tr:
+            kus = 1e3 * tr["router"][1] / tr["router"][0]
+            if T == 1:
+                gbs = (wbytes + T * 7168 * 4 + T * E * 4) / (kus / 1e6) / 1e9
+                r["logits_kernel"] = {"us": round(kus, 2), "GB_s": round(gbs, 1), "hbm_frac": round(gbs / hbm_peak, 4)}
+            else:
+                tf = flops / (kus / 1e6) / 1e12
+                r["logits_kernel"] = {"us": round(kus, 2), "TFLOP_s": round(tf, 1),
+                                      "frac_bf16_peak": round(tf / bf16_peak, 4)}
+        out[name] = r
+    return out
+
+
 def run_ours(args):
     import torch
     rank = int(os.environ.get("RANK", "0"))
@@ -482,6 +535,7 @@ def run_ours(args):
                     "tensor_kernels": kern,
                     "kernels": {k: {"launches": v[0], "avg_us": round(1e3 * v[1] / max(1, v[0]), 2)}
                                 for k, v in tr.items()}}
+            sec.update(time_router(k3mx, dev, flush, max(5, args.steps // 2), args.warmup, bf16_peak, hbm_peak))
         line["secondary"] = sec
         if not args.no_cpu_baseline:
             steps_in = [decode_inputs(i, 1) for i in range(64)]
@@ -503,6 +557,25 @@ def run_profile_case(args):
     import mxfp4_routed_expert_k3mx_gb300 as k3mx
     import synth
     dev = torch.device("cuda:0")
+    if args.profile_case == "router":
+        # the router alone: fp32 states up to 16 tokens, bf16 beyond
+        T = args.tokens
+        W = torch.from_numpy(synth.router_weights(seed=0).view(np.int16)).to(dev)
+        _, bias = synth.router_inputs(1, seed=0)
+        h = synth.hidden_inputs(T, seed=1)
+        ht = (torch.from_numpy(h) if T <= 16 else
+              torch.from_numpy(synth.f32_to_bf16(h).view(np.int16)).view(torch.bfloat16)).to(dev)
+        lg = torch.empty((T, E), dtype=torch.float32, device=dev)
+        idx = torch.empty((T, K), dtype=torch.int32, device=dev)
+        w = torch.empty((T, K), dtype=torch.float32, device=dev)
+        for _ in range(args.iters):
+            k3mx.k3mx_router(lg, idx, w, ht, W, torch.from_numpy(bias).to(dev))
+        torch.cuda.synchronize(dev)
+        st = k3mx.k3mx_device_status()
+        print(json.dumps({"profile_case": "router", "tokens": T, "iters": args.iters, "status": st}), flush=True)
+        if st[0] != 0:
+            sys.exit(1)
+        return
     T, R = args.tokens, args.resident
     arena = synth.expert_arena_device(dev, seed=0, lo=118, hi=128, n_experts=R)
     table = k3mx.expert_table(arena, n_experts=R)[torch.arange(E, device=dev) % R].contiguous()
@@ -539,7 +612,7 @@ def main():
     ap.add_argument("--primary-only", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
-    ap.add_argument("--profile-case", choices=["decode", "prefill"])
+    ap.add_argument("--profile-case", choices=["decode", "prefill", "router"])
     ap.add_argument("--tokens", type=int, default=1)
     ap.add_argument("--resident", type=int, default=64)
     ap.add_argument("--confine", action="store_true")

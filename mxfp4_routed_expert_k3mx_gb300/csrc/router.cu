@@ -8,7 +8,8 @@
 // (route_group.cu), launched right behind as programmatic dependents.
 //
 // Few tokens (decode), or fp32 states: k_router_gemv, one warp per router
-// row with the row held in registers, HBM-bound on the 12.8 MB of weights.
+// row, the rows brought in by bulk copies; HBM-bound on the 12.8 MB of
+// weights.
 // Many bf16 states (prefill): k_router_gemm, the tcgen05 tensor cores
 // (kind::f16 with bf16 A and B, fp32 accumulators in TMEM); a CTA computes
 // 128 router rows x 256 tokens over the whole 7168-deep sum, its operands
@@ -23,87 +24,119 @@ namespace {
 constexpr int kH = 7168;                         // hidden width
 constexpr int kRowVec = kH / 8;                  // 16-byte vectors per router row
 constexpr int kVecPerLane = kRowVec / 32;        // 28
-constexpr int kGemvTok = 4;                      // hidden states per shared-memory chunk
-constexpr int kGemvWarps = 8;
-constexpr int kGemvSmem = kGemvTok * kH * 4;
-static_assert(kE % kGemvWarps == 0 && kRowVec % 32 == 0, "router shape");
+constexpr int kGemvTok = 3;                      // hidden states per shared-memory chunk
+constexpr int kGemvWarps = 7;                    // one router row per warp: 128 CTAs
+constexpr int kRowBytes = kH * 2;                // 14336
+constexpr int kGemvSmem = 1024 + kGemvWarps * kRowBytes + kGemvTok * kH * 4;
+static_assert(kE % kGemvWarps == 0 && kRowVec % 32 == 0 && kRowBytes % 16 == 0, "router shape");
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
-// read once: no L1 allocation
-__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
-// One warp per router row: the row's 14 KB sit in registers (28 16-byte
-// vectors per lane, vector v = lane + 32 i holds columns 8v..8v+7); the
-// hidden states pass through shared memory in chunks of 4, laid out so that
-// the lanes read consecutive 16-byte words (columns 8v..8v+3 at slot v,
-// 8v+4..8v+7 at slot kRowVec + v).  Per lane, 8-term sums per vector are
-// added over its 28 vectors; the warp adds its lanes: a logit is at most 41
-// fp32 roundings deep.
+// One warp per router row.  The CTA's 8 rows (112 KB, contiguous) come in
+// by bulk copies, one per row, issued before anything else; the hidden
+// states pass through shared memory in chunks of 3, laid out so that the
+// lanes read consecutive 16-byte words (columns 8v..8v+3 at slot v,
+// 8v+4..8v+7 at slot kRowVec + v, vector v = lane + 32 i).  Per lane, a
+// vector's 8 products are two 4-term sums added, the vectors go to four
+// running sums (7 each) added pairwise, and the warp adds its lanes: a
+// logit is at most 4 + 1 + 7 + 2 + 5 = 19 fp32 roundings deep.
 __global__ void __launch_bounds__(kGemvWarps * 32, 1)
     k_router_gemv(float *__restrict__ logits, const void *__restrict__ h, int h_bf16,
-                  const uint16_t *__restrict__ W, int n_tokens) {
-    extern __shared__ float4 hs[];                // [kGemvTok][2 * kRowVec]
+                  const uint16_t *__restrict__ W, int n_tokens, int *status) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
+    const uint8_t *rows = smem + 1024;
+    float4 *hs = reinterpret_cast<float4 *>(smem + 1024 + kGemvWarps * kRowBytes);   // [kGemvTok][2 * kRowVec]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = blockIdx.x * kGemvWarps + warp;
+    const uint32_t b = smem_addr(bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(b, kGemvWarps * kRowBytes);
+        const uint8_t *src = reinterpret_cast<const uint8_t *>(W) + (size_t)blockIdx.x * kGemvWarps * kRowBytes;
+        for (int r = 0; r < kGemvWarps; r++)
+            bulk_g2s(smem_addr(rows) + r * kRowBytes, src + (size_t)r * kRowBytes, kRowBytes, b,
+                     l2_evict_first_policy());
+    }
     // the routing kernel behind may start its prologue
     pdl_launch_dependents();
-    const uint4 *wr = reinterpret_cast<const uint4 *>(W + (size_t)e * kH);
-    uint4 wv[kVecPerLane];
-#pragma unroll
-    for (int i = 0; i < kVecPerLane; i++) wv[i] = ld_stream(wr + lane + 32 * i);
     pdl_wait();                                   // the hidden states, if a kernel before writes them
+    const uint4 *wr = reinterpret_cast<const uint4 *>(rows + warp * kRowBytes);
+    bool have_rows = false;
     for (int t0 = 0; t0 < n_tokens; t0 += kGemvTok) {
         const int nt = min(kGemvTok, n_tokens - t0);
-        __syncthreads();                          // the previous chunk is consumed
-        for (int i = threadIdx.x; i < nt * (kH / 4); i += blockDim.x) {
-            const int t = i / (kH / 4), c4 = i % (kH / 4);
-            float4 v;
-            if (h_bf16) {
-                const uint2 b = reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(h) +
+        __syncthreads();                          // the barrier is set up; the previous chunk is consumed
+        // 8 loads in flight per thread before the stores
+        const int n4 = nt * (kH / 4);
+        for (int i0 = threadIdx.x; i0 < n4; i0 += 8 * (int)blockDim.x) {
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; u++) {
+                const int i = i0 + u * (int)blockDim.x;
+                if (i < n4) {
+                    const int t = i / (kH / 4), c4 = i % (kH / 4);
+                    if (h_bf16) {
+                        const uint2 q = reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(h) +
+                                                                        (size_t)(t0 + t) * kH)[c4];
+                        v[u] = make_float4(bf16_lo(q.x), bf16_hi(q.x), bf16_lo(q.y), bf16_hi(q.y));
+                    } else {
+                        v[u] = reinterpret_cast<const float4 *>(static_cast<const float *>(h) +
                                                                 (size_t)(t0 + t) * kH)[c4];
-                v = make_float4(bf16_lo(b.x), bf16_hi(b.x), bf16_lo(b.y), bf16_hi(b.y));
-            } else {
-                v = reinterpret_cast<const float4 *>(static_cast<const float *>(h) + (size_t)(t0 + t) * kH)[c4];
+                    }
+                }
             }
-            hs[t * (2 * kRowVec) + (c4 & 1) * kRowVec + (c4 >> 1)] = v;
+#pragma unroll
+            for (int u = 0; u < 8; u++) {
+                const int i = i0 + u * (int)blockDim.x;
+                if (i < n4) {
+                    const int t = i / (kH / 4), c4 = i % (kH / 4);
+                    hs[t * (2 * kRowVec) + (c4 & 1) * kRowVec + (c4 >> 1)] = v[u];
+                }
+            }
         }
         __syncthreads();
-        float acc[kGemvTok];
+        if (!have_rows) {
+            if (!mbar_wait(b, 0)) {
+                if (lane == 0) report_status(status, kStatusWaitTimeout, 310);
+                return;                           // every warp leaves: no barrier follows
+            }
+            have_rows = true;
+        }
+        // four independent running sums per token (vectors i mod 4), each
+        // vector's 8 products as two 4-term chains: the iterations overlap
+        float acc[kGemvTok][4];
 #pragma unroll
-        for (int j = 0; j < kGemvTok; j++) acc[j] = 0.f;
+        for (int j = 0; j < kGemvTok; j++)
 #pragma unroll
+            for (int r = 0; r < 4; r++) acc[j][r] = 0.f;
+        static_assert(kVecPerLane % 4 == 0, "vectors per lane");
+#pragma unroll 4
         for (int i = 0; i < kVecPerLane; i++) {
             const int v = lane + 32 * i;
-            const uint4 q = wv[i];
+            const uint4 q = wr[v];
             const float w0 = bf16_lo(q.x), w1 = bf16_hi(q.x), w2 = bf16_lo(q.y), w3 = bf16_hi(q.y);
             const float w4 = bf16_lo(q.z), w5 = bf16_hi(q.z), w6 = bf16_lo(q.w), w7 = bf16_hi(q.w);
 #pragma unroll
             for (int j = 0; j < kGemvTok; j++) {
                 if (j < nt) {
-                    const float4 a = hs[j * (2 * kRowVec) + v], b = hs[j * (2 * kRowVec) + kRowVec + v];
-                    float s8 = w0 * a.x;
-                    s8 = fmaf(w1, a.y, s8);
-                    s8 = fmaf(w2, a.z, s8);
-                    s8 = fmaf(w3, a.w, s8);
-                    s8 = fmaf(w4, b.x, s8);
-                    s8 = fmaf(w5, b.y, s8);
-                    s8 = fmaf(w6, b.z, s8);
-                    s8 = fmaf(w7, b.w, s8);
-                    acc[j] += s8;
+                    const float4 a = hs[j * (2 * kRowVec) + v], c = hs[j * (2 * kRowVec) + kRowVec + v];
+                    float s0 = w0 * a.x, s1 = w4 * c.x;
+                    s0 = fmaf(w1, a.y, s0);
+                    s1 = fmaf(w5, c.y, s1);
+                    s0 = fmaf(w2, a.z, s0);
+                    s1 = fmaf(w6, c.z, s1);
+                    s0 = fmaf(w3, a.w, s0);
+                    s1 = fmaf(w7, c.w, s1);
+                    acc[j][i & 3] += s0 + s1;
                 }
             }
         }
 #pragma unroll
         for (int j = 0; j < kGemvTok; j++) {
-            float a = acc[j];
+            float a = (acc[j][0] + acc[j][1]) + (acc[j][2] + acc[j][3]);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
             if (lane == 0 && j < nt) logits[(size_t)(t0 + j) * kE + e] = a;
@@ -285,7 +318,7 @@ cudaError_t launch_router_logits(const Ctx &c, float *logits, const void *h, int
         configured = true;
     }
     return launch_pdl(k_router_gemv, dim3(kE / kGemvWarps), dim3(kGemvWarps * 32), (size_t)kGemvSmem, c.stream,
-                      logits, h, h_bf16, W, n_tokens);
+                      logits, h, h_bf16, W, n_tokens, c.status);
 }
 
 }  // namespace k3mx
