@@ -28,7 +28,8 @@ namespace {
 
 constexpr float kRoutedScale = 1.0f;     // K3Cfg routed_scale
 constexpr int kPer = kE / 32;            // 28 experts per lane
-constexpr int kSeg = 4096;               // pairs per grouping segment
+constexpr int kSeg = 1024;               // pairs per grouping segment (one warp scatters one)
+constexpr int kRouteWarpMax = 64;        // more tokens: one routing CTA per token
 
 __device__ __forceinline__ uint32_t order_key(float k) {
     if (k != k) k = -INFINITY;           // NaN ranks last
@@ -384,18 +385,28 @@ __device__ void finish_counts(int *cnt_sm, const GroupOut &g, int *tmp) {
 // pairs in order, 32 at a time.
 __device__ void scatter_warp(const int32_t *idx, int p_begin, int p_end, int *running,
                              int32_t *perm) {
+    constexpr int kChunks = kSeg / 32;
     const int lane = threadIdx.x % 32;
     const unsigned lt_mask = (1u << lane) - 1u;
-    for (int base = p_begin; base < p_end; base += 32) {
-        const int p = base + lane;
+    // the segment's expert indices first (independent loads), then the
+    // placement chunk by chunk
+    int ev[kChunks];
+#pragma unroll
+    for (int k = 0; k < kChunks; k++) {
+        const int p = p_begin + 32 * k + lane;
         int e = -1;
         if (p < p_end) {
             e = idx[p];
             if (e < 0 || e >= kE) e = -1;
         }
+        ev[k] = e;
+    }
+#pragma unroll
+    for (int k = 0; k < kChunks; k++) {
+        const int e = ev[k];
         const unsigned peers = __match_any_sync(0xffffffffu, e);
         const int rank = __popc(peers & lt_mask);
-        if (e >= 0) perm[running[e] + rank] = p;
+        if (e >= 0) perm[running[e] + rank] = p_begin + 32 * k + lane;
         __syncwarp();
         if (e >= 0 && rank == 0) running[e] += __popc(peers);
         __syncwarp();
@@ -668,19 +679,35 @@ k_group_scan(int *hist, int n_seg, GroupOut g) {
     __shared__ int cnt[kE];
     __shared__ int tmp[33];
     const int e = threadIdx.x;
+    constexpr int B = 16;                            // segments per batch of independent loads
     if (e < kE) {
         int c = 0;
-        for (int s = 0; s < n_seg; s++) {
-            const int h = hist[(size_t)s * kE + e];
-            hist[(size_t)s * kE + e] = c;            // within-expert start of segment s
-            c += h;
+        for (int s0 = 0; s0 < n_seg; s0 += B) {
+            int h[B];
+#pragma unroll
+            for (int j = 0; j < B; j++) h[j] = s0 + j < n_seg ? hist[(size_t)(s0 + j) * kE + e] : 0;
+#pragma unroll
+            for (int j = 0; j < B; j++)
+                if (s0 + j < n_seg) {
+                    hist[(size_t)(s0 + j) * kE + e] = c;   // within-expert start of segment s0 + j
+                    c += h[j];
+                }
         }
         cnt[e] = c;
     }
     __syncthreads();
     finish_counts(cnt, g, tmp);
-    if (e < kE)
-        for (int s = 0; s < n_seg; s++) hist[(size_t)s * kE + e] += cnt[e];
+    if (e < kE) {
+        const int off = cnt[e];
+        for (int s0 = 0; s0 < n_seg; s0 += B) {
+            int h[B];
+#pragma unroll
+            for (int j = 0; j < B; j++) h[j] = s0 + j < n_seg ? hist[(size_t)(s0 + j) * kE + e] : 0;
+#pragma unroll
+            for (int j = 0; j < B; j++)
+                if (s0 + j < n_seg) hist[(size_t)(s0 + j) * kE + e] = h[j] + off;
+        }
+    }
 }
 
 __global__ void __launch_bounds__(32)
@@ -696,6 +723,20 @@ k_group_scatter(const int32_t *idx, int n_pairs, const int *base, int32_t *perm)
 
 cudaError_t launch_route(const Ctx &c, int32_t *idx, float *w, const float *logits,
                          const float *bias, int n_tokens, double top_p, bool pdl) {
+    if (n_tokens > kRouteWarpMax) {
+        // many tokens: a CTA per token (its phases are a few dozen
+        // instructions each; a warp per token runs 16 dependent rounds)
+        const dim3 grid(n_tokens);
+        const GroupOut g{};
+        if (pdl)
+            return launch_pdl(k_route_prep, grid, dim3(kRT), 0, c.stream, idx, w, logits, bias, n_tokens,
+                              (const void *)nullptr, 0, (uint8_t *)nullptr, g, (int *)nullptr, 0,
+                              (const k3mx_expert *)nullptr, 0, (uint8_t *)nullptr, top_p, CUtensorMap{},
+                              CUtensorMap{});
+        k_route_prep<<<grid, kRT, 0, c.stream>>>(idx, w, logits, bias, n_tokens, nullptr, 0, nullptr, g, nullptr,
+                                                 0, nullptr, 0, nullptr, top_p, CUtensorMap{}, CUtensorMap{});
+        return cudaGetLastError();
+    }
     const int per_block = 8;
     const dim3 grid((n_tokens + per_block - 1) / per_block);
     if (pdl) return launch_pdl(k_route, grid, dim3(32 * per_block), 0, c.stream, idx, w, logits, bias, n_tokens, top_p);
