@@ -66,6 +66,8 @@ def _load():
             lib.orc_bf16.argtypes = [ctypes.c_uint16]
             lib.orc_router_logits.argtypes = [vp, vp, vp, i, i, i, i]
             lib.orc_router_absdot.argtypes = [vp, vp, vp, i, i, i, i]
+            lib.orc_rmsnorm.argtypes = [vp, vp, vp, i, i, ctypes.c_double]
+            lib.orc_situ_vec.argtypes = [vp, vp, vp, ctypes.c_longlong]
             lib.orc_group.restype = i
             lib.orc_moe.argtypes = [vp, vp, i, vp, vp, vp, i, i, i, vp]
             lib.orc_num_threads.restype = i
@@ -206,6 +208,54 @@ def router_absdot(W, h):
     out = np.empty((T, E), np.float64)
     _load().orc_router_absdot(_p(out), _p(W), _p(h), hb, T, E, C)
     return out
+
+
+def bf16_matvec(W, x):
+    """y [T, R] fp32 = bf16 W [R, C] times x [T, C] (fp32 or bf16), double
+    sums in ascending column order, one rounding (the router's product)."""
+    return router_logits(W, x)
+
+
+def rmsnorm(x, g, eps=1e-5):
+    """x [T, D] fp32 / sqrt(mean(x^2) + eps) * g (bf16 [D]), in double."""
+    x = np.ascontiguousarray(x, np.float32)
+    g = np.ascontiguousarray(g, np.uint16)
+    T, D = x.shape
+    out = np.empty_like(x)
+    _load().orc_rmsnorm(_p(out), _p(x), _p(g), T, D, float(eps))
+    return out
+
+
+def situ_vec(g, u):
+    """SiTU-GLU elementwise, fp32 in, double inside, fp32 out."""
+    g = np.ascontiguousarray(g, np.float32)
+    u = np.ascontiguousarray(u, np.float32)
+    out = np.empty_like(g)
+    _load().orc_situ_vec(_p(out), _p(g), _p(u), g.size)
+    return out
+
+
+def latent_block(h, blk, idx, w, experts, tokens=None):
+    """The Stable LatentMoE block [LM] for hidden states h [T, 7168] (fp32
+    or bf16) given the routing (idx, w) of the router logits:
+        x  = W_dn h                            (7168 -> 3584)
+        yr = sum_k w_k expert_k(x)             (the routed experts)
+        y  = W_up rmsnorm(yr) + W2s situ(W1s h, W3s h)
+    `blk` maps "w_dn", "w_up", "g_norm", "w1s", "w3s", "w2s" to bf16 arrays;
+    `experts` is the list of per-expert (w1p, w1s, w3p, w3s, w2p, w2s).
+    Every product step returns fp32; the final sum is taken in double and
+    rounded once.  `tokens` restricts the work to those rows of h.  Returns
+    y [T', 7168] and the intermediates (x, yr, z, a)."""
+    if tokens is not None:
+        h, idx, w = h[tokens], idx[tokens], w[tokens]
+    x = bf16_matvec(blk["w_dn"], h)
+    yr = moe(x, idx, w, experts)
+    z = rmsnorm(yr, blk["g_norm"])
+    y_up = bf16_matvec(blk["w_up"], z)
+    a = situ_vec(bf16_matvec(blk["w1s"], h), bf16_matvec(blk["w3s"], h))
+    y_sh = bf16_matvec(blk["w2s"], a)
+    y = (y_up.astype(np.float64) + y_sh.astype(np.float64)).astype(np.float32)
+    return y, (x, yr, z, a)
 
 
 def group(idx, n_experts=896):

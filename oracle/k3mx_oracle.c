@@ -38,6 +38,13 @@
  *        to the 7168-wide hidden state; its outputs are the logits [A] takes.
  *        The trunk (router included) is bf16 (kimi-k3-in-c README, the
  *        resident set of budget.py: "norms, router gates, biases").
+ *   [LM] Kimi K3 engine (c/kimi_k3.c), "Architecture notes", Stable
+ *        LatentMoE bullet: the token is projected 7168 -> 3584, the experts
+ *        run in that latent, the aggregate is RMSNorm-ed and projected back
+ *        3584 -> 7168, and two fused full-width shared experts (inter 6144)
+ *        are added; K3Cfg (kimi-k3-in-c README, "2. The config reader that
+ *        refuses to guess"): n_shared 2 "full width, added UNWEIGHTED",
+ *        latent_norm 1 "RMSNorm on the AGGREGATE", rms_eps 1e-5.
  *   [TP] Kimi K3 engine (c/kimi_k3.c), "Streaming design" (K3_TOPP) and the
  *        environment table: optionally keep the routed experts only up to a
  *        cumulative weight p, dropping the low-weight tail of the top-16 and
@@ -292,6 +299,28 @@ void orc_router_absdot(double *b, const uint16_t *W, const void *h, int h_bf16, 
             b[(size_t)t * E + e] = acc;
         }
     }
+}
+
+/*
+ * RMSNorm [LM]: y[t][i] = x[t][i] / sqrt(mean_i x[t][i]^2 + eps) * g[i],
+ * g bf16; in double, rounded to fp32 once.
+ */
+void orc_rmsnorm(float *y, const float *x, const uint16_t *g, int T, int D, double eps)
+{
+    for (int t = 0; t < T; t++) {
+        const float *xt = x + (size_t)t * D;
+        double ss = 0.0;
+        for (int i = 0; i < D; i++) ss += (double)xt[i] * (double)xt[i];
+        const double r = 1.0 / sqrt(ss / (double)D + eps);
+        for (int i = 0; i < D; i++) y[(size_t)t * D + i] = (float)((double)xt[i] * r * orc_bf16(g[i]));
+    }
+}
+
+/* SiTU-GLU elementwise [A][LM]: a[i] = (float) SiTU(g[i], u[i]) */
+void orc_situ_vec(float *a, const float *g, const float *u, long long n)
+{
+    #pragma omp parallel for schedule(static)
+    for (long long i = 0; i < n; i++) a[i] = (float)orc_situ((double)g[i], (double)u[i]);
 }
 
 /*

@@ -32,6 +32,7 @@ STREAM_LOGITS = 11
 STREAM_BIAS = 12
 STREAM_ROUTER_W = 13
 STREAM_HIDDEN = 14
+STREAM_BLOCK = 20       # + 0..5: the LatentMoE block's bf16 matrices and norm weight
 
 # Kimi-K3 routed-expert shape: latent width D, expert inter width F.
 D_LATENT = 3584
@@ -39,6 +40,7 @@ F_INTER = 3072
 N_EXPERTS = 896
 TOP_K = 16
 H_MODEL = 7168          # hidden width the router reads
+F_SHARED = 6144         # inter width of the fused shared experts
 
 
 def build(force=False):
@@ -178,6 +180,19 @@ def router_weights(seed=0, E=N_EXPERTS, C=H_MODEL):
 def hidden_inputs(n_tokens, seed=0, C=H_MODEL):
     """Hidden states ~ N(0,1): fp32 [T, C]."""
     return normal_f32(n_tokens * C, seed, STREAM_HIDDEN).reshape(n_tokens, C)
+
+
+def latent_block_weights(seed=0, H=H_MODEL, D=D_LATENT, FS=F_SHARED):
+    """The LatentMoE block's bf16 tensors (uint16 bit patterns): the latent
+    projections w_dn [D, H] ~ N(0, 1/H) and w_up [H, D] ~ N(0, 1/D), the
+    aggregate's RMSNorm weight g_norm [D] ~ N(1, 0.1^2), and the fused shared
+    experts w1s, w3s [FS, H] ~ N(0, 1/H), w2s [H, FS] ~ N(0, 1/FS): unit-scale
+    activations in, unit-scale activations out."""
+    def mat(k, rows, cols):
+        return f32_to_bf16(normal_f32(rows * cols, seed, STREAM_BLOCK + k, 0.0, float(cols) ** -0.5)).reshape(rows, cols)
+    return {"w_dn": mat(0, D, H), "w_up": mat(1, H, D),
+            "g_norm": f32_to_bf16(normal_f32(D, seed, STREAM_BLOCK + 2, 1.0, 0.1)),
+            "w1s": mat(3, FS, H), "w3s": mat(4, FS, H), "w2s": mat(5, H, FS)}
 
 
 def expert_arena_device(device, seed=0, lo=118, hi=128, n_experts=N_EXPERTS, chunk=16):

@@ -511,3 +511,64 @@ def test_router_logits_brute_force_small():
         assert np.all(np.abs(lg - ref) <= 1e-12 * (np.abs(h) @ np.abs(Wd).T) + np.abs(ref) * 2.0 ** -24)
     lg = oracle.router_logits(synth.router_weights(seed=0, E=64), synth.hidden_inputs(8, seed=0))
     assert 0.8 < lg.std() < 1.2
+
+
+# ---- the LatentMoE block around the routed experts (Kimi K3 engine
+# (c/kimi_k3.c), "Architecture notes": latent projections, RMSNorm on the
+# aggregate, fused shared experts added unweighted)
+
+def test_rmsnorm_closed_forms():
+    D = 3584
+    one = np.full(D, 0x3F80, np.uint16)                     # g = 1
+    for c in (0.5, -3.0, 1e3):
+        y = oracle.rmsnorm(np.full((1, D), c, np.float32), one)
+        assert np.allclose(y, np.sign(c) * abs(c) / np.sqrt(c * c + 1e-5), rtol=1e-7)
+    assert np.all(oracle.rmsnorm(np.zeros((1, D), np.float32), one) == 0.0)
+    x = synth.token_inputs(3, seed=71)
+    y1 = oracle.rmsnorm(x, one, eps=0.0)
+    assert np.array_equal(y1, oracle.rmsnorm(4.0 * x, one, eps=0.0))   # scale-free without eps
+    assert np.all(np.abs(np.sqrt(np.mean(y1.astype(np.float64) ** 2, axis=1)) - 1.0) < 1e-6)
+    g = synth.f32_to_bf16(np.linspace(0.5, 2.0, D).astype(np.float32))
+    assert np.allclose(oracle.rmsnorm(x, g, eps=0.0), y1 * synth.bf16_to_f32(g), rtol=1e-6)
+
+
+def test_situ_vec_is_the_activation():
+    g = np.array([0.0, 1.5, -2.0, 40.0], np.float32)
+    u = np.array([3.0, 0.0, -1.0, 2.0], np.float32)
+    a = oracle.situ_vec(g, u)
+    assert a[0] == 0.0 and a[1] == 0.0
+    assert a[2] == np.float32(oracle.situ(-2.0, -1.0)) and a[3] == np.float32(oracle.situ(40.0, 2.0))
+
+
+def _identity_bf16(rows, cols):
+    W = np.zeros((rows, cols), np.uint16)
+    n = min(rows, cols)
+    W[np.arange(n), np.arange(n)] = 0x3F80
+    return W
+
+
+def test_latent_block_wiring():
+    """Identity projections and a silent shared expert expose each stage:
+    x = h[:3584], the routed sum of x, its RMSNorm, the shared expert's
+    unweighted add."""
+    from helpers import arena_expert
+    H, D, FS = 7168, 3584, 64
+    h = synth.hidden_inputs(1, seed=72)
+    logits, bias = synth.router_inputs(1, seed=72)
+    idx, w = oracle.route(logits, bias)
+    experts = {int(e): arena_expert(int(e)) for e in idx[0]}
+    g_norm = synth.f32_to_bf16(np.full(D, 2.0, np.float32))
+    blk = {"w_dn": _identity_bf16(D, H), "w_up": _identity_bf16(H, D), "g_norm": g_norm,
+           "w1s": np.zeros((FS, H), np.uint16), "w3s": synth.router_weights(seed=73, E=FS, C=H),
+           "w2s": synth.router_weights(seed=74, E=H, C=FS)}
+    y, (x, yr, z, a) = oracle.latent_block(h, blk, idx, w, experts)
+    assert np.array_equal(x, h[:, :D])                     # W_dn = [I 0]
+    assert np.array_equal(yr, oracle.moe(h[:, :D], idx, w, experts))
+    assert np.array_equal(z, oracle.rmsnorm(yr, g_norm))
+    assert np.all(a == 0.0)                                # W1s = 0: SiTU(0, u) = 0
+    assert np.array_equal(y[:, :D], z) and np.all(y[:, D:] == 0.0)
+    blk["w1s"] = synth.router_weights(seed=75, E=FS, C=H)    # the shared expert on
+    y2, (_, _, _, a2) = oracle.latent_block(h, blk, idx, w, experts)
+    ysh = oracle.bf16_matvec(blk["w2s"], a2)
+    assert np.any(a2 != 0.0)
+    assert np.array_equal(y2, (z.astype(np.float64) @ np.eye(D, H) + ysh.astype(np.float64)).astype(np.float32))
