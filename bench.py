@@ -51,7 +51,8 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
 # kernels per traced launch group
-KERNELS_PER_GROUP = {"router": 1, "route": 1, "group_small": 1, "group": 3, "mx_pieces": 1,
+KERNELS_PER_GROUP = {"router": 1, "latent_down": 1, "shared_gate_up": 2, "shared_down": 2, "latent_up": 2,
+                     "route": 1, "group_small": 1, "group": 3, "mx_pieces": 1,
                      "decode_expert": 1, "decode_gate_up": 1, "decode_down": 1, "combine": 1,
                      "prefill_prep": 3, "prefill_gate_up": 1, "prefill_down": 1}
 PARAMS_PER_EXPERT = 33030144
@@ -390,6 +391,66 @@ def time_router(k3mx, dev, flush, steps, warmup, bf16_peak, hbm_peak):
     return out
 
 
+def time_latent_block(k3mx, dev, table, steps, warmup, bf16_peak, hbm_peak):
+    """The whole Stable LatentMoE block (router, latent projections, routed
+    experts, RMSNorm, fused shared experts) at one fp32 decode token and at
+    4096 bf16 prefill tokens.  Its inputs exceed L2 (the block's 379 MB of
+    bf16 matrices plus 280.8 MB of experts per decode token), so L2 is not
+    flushed."""
+    import numpy as np
+    import torch
+    import synth
+    host = synth.latent_block_weights(seed=0)
+    host["router_w"] = synth.router_weights(seed=0)
+    dblk = {k: torch.from_numpy(v.view(np.int16)).to(dev) for k, v in host.items()}
+    _, bias = synth.router_inputs(1, seed=0)
+    dblk["bias"] = torch.from_numpy(bias).to(dev)
+    blk = k3mx.latent_block(dblk)
+    dense_bytes = sum(v.size * 2 for k, v in host.items())
+    out = {}
+    stream = torch.cuda.current_stream(dev)
+    for name, T, bf16 in (("latent_block_b1", 1, False), ("latent_block_4096", 4096, True)):
+        hs = [synth.hidden_inputs(T, seed=200 + i) for i in range(warmup + steps)]
+        dt = k3mx.K3MX_BF16 if bf16 else k3mx.K3MX_F32
+        hts = [(torch.from_numpy(synth.f32_to_bf16(h).view(np.int16)).view(torch.bfloat16) if bf16
+                else torch.from_numpy(h)).to(dev) for h in hs]
+        y = torch.empty((T, 7168), dtype=torch.float32, device=dev)
+        idx = torch.empty((T, K), dtype=torch.int32, device=dev)
+        ws = torch.empty(k3mx.k3mx_latent_moe_workspace_size(T, dt), dtype=torch.uint8, device=dev)
+        for i in range(warmup):
+            k3mx.k3mx_latent_moe(y, hts[i], blk, table, ws, idx_out=idx)
+        torch.cuda.synchronize(dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        distinct = []
+        for i in range(steps):
+            ev[i][0].record(stream)
+            k3mx.k3mx_latent_moe(y, hts[warmup + i], blk, table, ws, idx_out=idx)
+            ev[i][1].record(stream)
+            if T == 1:
+                distinct.append(16)
+        torch.cuda.synchronize(dev)
+        k3mx.k3mx_trace_read()
+        k3mx.k3mx_trace_enable(True)
+        k3mx.k3mx_latent_moe(y, hts[-1], blk, table, ws, idx_out=idx)
+        torch.cuda.synchronize(dev)
+        k3mx.k3mx_trace_enable(False)
+        tr = k3mx.k3mx_trace_read()
+        ms = statistics.median([a.elapsed_time(b) for a, b in ev])
+        r = {"us_per_call": round(1e3 * ms, 2), "tokens_per_s": round(T / (ms / 1e3), 1),
+             "kernels": {k: {"launches": v[0], "avg_us": round(1e3 * v[1] / max(1, v[0]), 2)} for k, v in tr.items()},
+             "l2": "not flushed (inputs exceed L2)"}
+        if T == 1:
+            gbs = (dense_bytes + 16 * EXPERT_BYTES) / (ms / 1e3) / 1e9
+            r["weight_GB_s"] = round(gbs, 1)
+            r["hbm_frac"] = round(gbs / hbm_peak, 4)
+        else:
+            flops = 2.0 * T * (dense_bytes / 2 - 3584) + 2.0 * PARAMS_PER_EXPERT * T * K
+            r["TFLOP_s"] = round(flops / (ms / 1e3) / 1e12, 1)
+            r["frac_bf16_peak"] = round(flops / (ms / 1e3) / 1e12 / bf16_peak, 4)
+        out[name] = r
+    return out
+
+
 def run_ours(args):
     import torch
     rank = int(os.environ.get("RANK", "0"))
@@ -536,6 +597,7 @@ def run_ours(args):
                     "kernels": {k: {"launches": v[0], "avg_us": round(1e3 * v[1] / max(1, v[0]), 2)}
                                 for k, v in tr.items()}}
             sec.update(time_router(k3mx, dev, flush, max(5, args.steps // 2), args.warmup, bf16_peak, hbm_peak))
+            sec.update(time_latent_block(k3mx, dev, table, max(3, args.steps // 4), args.warmup, bf16_peak, hbm_peak))
         line["secondary"] = sec
         if not args.no_cpu_baseline:
             steps_in = [decode_inputs(i, 1) for i in range(64)]

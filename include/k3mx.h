@@ -175,6 +175,46 @@ k3mx_status k3mx_router(float *logits, int32_t *idx, float *w, const void *hidde
                         k3mx_stream_t stream);
 
 /*
+ * The Stable LatentMoE block around the routed experts (Kimi K3 engine
+ * (c/kimi_k3.c), "Architecture notes"; K3Cfg n_shared 2 "full width, added
+ * UNWEIGHTED", latent_norm 1 "RMSNorm on the AGGREGATE", rms_eps 1e-5):
+ *   logits = router h                          (k3mx_router's product)
+ *   x      = w_dn h                            (7168 -> 3584)
+ *   r      = sum_k w_k expert_k(x)             (k3mx_moe_routed on x, logits)
+ *   y      = w_up (RMSNorm(r) * g_norm) + w2s SiTU-GLU(w1s h, w3s h)
+ * All matrices bf16 (bit patterns), row-major; the structure holds device
+ * pointers and lives on the host.
+ */
+typedef struct {
+    const uint16_t *router_w;    /* [896][7168] */
+    const float *bias;           /* [896] score-correction bias */
+    const uint16_t *w_dn;        /* [3584][7168] */
+    const uint16_t *w_up;        /* [7168][3584] */
+    const uint16_t *g_norm;      /* [3584] RMSNorm weight of the routed sum */
+    const uint16_t *w1s, *w3s;   /* [6144][7168] fused shared experts: gate, up */
+    const uint16_t *w2s;         /* [7168][6144] fused shared experts: down */
+} k3mx_latent_block;
+
+/*
+ *   y [n_tokens][7168] fp32 (written); hidden [n_tokens][7168], h_dtype
+ *   K3MX_F32 or K3MX_BF16; experts as for k3mx_moe_routed; top_p as for
+ *   k3mx_route_topp (<= 0: off); idx_out, w_out optional [n_tokens][16].
+ * fp32 states or up to 16 bf16 ones run in fp32 on CUDA cores (the routed
+ * part on the DECODE path); from 17 bf16 states the products run on the
+ * tensor cores with bf16 operands (x, SiTU(g, u) and the normalised sum
+ * rounded to bf16) and the routed part takes its bf16 default path.
+ * Numerics: per token, |y - exact| / |exact| (L2) is at most 1e-4 with fp32
+ * states (measured ~5e-7) and 1e-2 with bf16 batches (measured ~7e-3, the
+ * bf16 rounding of the intermediates).  workspace: device,
+ * 256-byte aligned, >= k3mx_latent_moe_workspace_size(n_tokens, h_dtype).
+ */
+size_t k3mx_latent_moe_workspace_size(int n_tokens, int h_dtype);
+k3mx_status k3mx_latent_moe(float *y, const void *hidden, int h_dtype, int n_tokens,
+                            const k3mx_latent_block *blk, const k3mx_expert *experts, float top_p,
+                            int32_t *idx_out, float *w_out, void *workspace, size_t ws_bytes,
+                            k3mx_stream_t stream);
+
+/*
  * Token-to-expert grouping (Kimi K3 engine (c/kimi_k3.c), "Chunked prefill":
  * each unique expert of a chunk is loaded once for all its tokens):
  *   counts [896]          pairs routed to each expert

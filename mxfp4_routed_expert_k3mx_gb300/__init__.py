@@ -46,6 +46,11 @@ class Expert(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("w1", "s1", "w3", "s3", "w2", "s2")]
 
 
+class LatentBlock(ctypes.Structure):
+    """k3mx_latent_block: device pointers of the LatentMoE block's tensors."""
+    _fields_ = [(n, ctypes.c_void_p) for n in ("router_w", "bias", "w_dn", "w_up", "g_norm", "w1s", "w3s", "w2s")]
+
+
 class TraceEntry(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_int), ("total_ms", ctypes.c_double)]
 
@@ -69,6 +74,8 @@ def lib():
             "k3mx_route_topk": ([vp, vp, vp, vp, i, vp], i),
             "k3mx_route_topp": ([vp, vp, vp, vp, i, ctypes.c_float, vp], i),
             "k3mx_router": ([vp, vp, vp, vp, i, vp, vp, i, ctypes.c_float, vp], i),
+            "k3mx_latent_moe_workspace_size": ([i, i], sz),
+            "k3mx_latent_moe": ([vp, vp, i, i, ctypes.POINTER(LatentBlock), vp, ctypes.c_float, vp, vp, vp, sz, vp], i),
             "k3mx_group_workspace_size": ([i], sz),
             "k3mx_group": ([vp, vp, vp, vp, i, vp, sz, vp], i),
             "k3mx_moe_workspace_size": ([i, i, i], sz),
@@ -189,6 +196,38 @@ def k3mx_router(logits, idx, w, hidden, router_w, bias, top_p=0.0, stream=None):
     _check("k3mx_router", lib().k3mx_router(_ptr(logits), _ptr(idx), _ptr(w), _ptr(hidden), _x_dtype(hidden),
                                             _ptr(router_w), _ptr(bias), T, float(top_p), _stream(stream)))
     return logits, idx, w
+
+
+LATENT_BLOCK_FIELDS = ("router_w", "bias", "w_dn", "w_up", "g_norm", "w1s", "w3s", "w2s")
+
+
+def latent_block(tensors):
+    """A k3mx_latent_block from a dict of contiguous device tensors (bf16
+    matrices as int16/uint16/bfloat16, the bias fp32)."""
+    for n in LATENT_BLOCK_FIELDS:
+        t = tensors[n]
+        if not (t.is_cuda and t.is_contiguous()):
+            raise ValueError(f"{n}: contiguous device tensor expected")
+    return LatentBlock(*[tensors[n].data_ptr() for n in LATENT_BLOCK_FIELDS])
+
+
+def k3mx_latent_moe_workspace_size(n_tokens, h_dtype):
+    return int(lib().k3mx_latent_moe_workspace_size(n_tokens, h_dtype))
+
+
+def k3mx_latent_moe(y, hidden, block, experts, workspace, top_p=0.0, idx_out=None, w_out=None, stream=None):
+    """The LatentMoE block: y [T, 7168] fp32 from hidden [T, 7168] (fp32 or
+    bf16).  `block` is a LatentBlock (see latent_block), `experts` the
+    device expert table."""
+    _dev(y, torch.float32, "y")
+    if not (hidden.is_cuda and hidden.is_contiguous()):
+        raise ValueError("hidden: contiguous device tensor expected")
+    T = hidden.shape[0]
+    _check("k3mx_latent_moe", lib().k3mx_latent_moe(
+        _ptr(y), _ptr(hidden), _x_dtype(hidden), T, ctypes.byref(block), _ptr(experts), float(top_p),
+        _ptr(idx_out), _ptr(w_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+    return y
 
 
 def k3mx_route_topp(idx, w, logits, bias, top_p, stream=None):

@@ -6,6 +6,7 @@
 #include <cstring>
 
 #include "common.cuh"
+#include "dense.cuh"
 #include "prefill.cuh"
 
 namespace k3mx {
@@ -300,6 +301,42 @@ k3mx_status run_moe(const Ctx &c, float *y, const void *x, int x_dtype, int n_to
     return from_cuda(err);
 }
 
+// ------------------------------------------------ the LatentMoE block --
+
+constexpr int kHid = 7168, kFs = 6144;           // hidden width, fused shared experts' inter width
+
+struct LatentLayout {
+    size_t logits, xlat, ylat, gu, ysh, act, z, moe, total;
+    bool batched;
+    int moe_path;
+    MoeLayout moe_l;
+};
+
+LatentLayout latent_layout(int n_tokens, int h_dtype) {
+    LatentLayout L{};
+    const size_t T = (size_t)n_tokens;
+    L.batched = h_dtype == K3MX_BF16 && n_tokens >= kDenseGemmMinTokens;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off += up256(bytes);
+        return o;
+    };
+    L.logits = take(T * kE * 4);
+    L.xlat = take(T * kD * (L.batched ? 2 : 4));
+    L.ylat = take(T * kD * 4);
+    L.gu = take(T * 2 * kFs * 4);
+    L.ysh = take(T * kHid * 4);
+    L.act = L.batched ? take(T * kFs * 2) : 0;
+    L.z = L.batched ? take(T * kD * 2) : 0;
+    const int x_dtype = L.batched ? K3MX_BF16 : K3MX_F32;
+    L.moe_path = resolve_path(n_tokens, x_dtype, K3MX_PATH_AUTO);
+    L.moe_l = moe_layout(n_tokens, x_dtype, L.moe_path);
+    L.moe = take(L.moe_l.total);
+    L.total = off;
+    return L;
+}
+
 }  // namespace
 }  // namespace k3mx
 
@@ -424,6 +461,106 @@ k3mx_status k3mx_router(float *logits, int32_t *idx, float *w, const void *hidde
                                        nullptr, nullptr, (double)top_p, true)
                    : launch_route(c, idx, w, logits, bias, n_tokens, (double)top_p, true);
     });
+    return from_cuda(err);
+}
+
+size_t k3mx_latent_moe_workspace_size(int n_tokens, int h_dtype) {
+    if (n_tokens < 1 || n_tokens > K3MX_MAX_TOKENS) return 0;
+    if (h_dtype != K3MX_F32 && h_dtype != K3MX_BF16) return 0;
+    return latent_layout(n_tokens, h_dtype).total;
+}
+
+k3mx_status k3mx_latent_moe(float *y, const void *hidden, int h_dtype, int n_tokens, const k3mx_latent_block *blk,
+                            const k3mx_expert *experts, float top_p, int32_t *idx_out, float *w_out,
+                            void *workspace, size_t ws_bytes, k3mx_stream_t stream) {
+    if (!y || !hidden || !blk || !experts) return K3MX_EINVAL;
+    if (!blk->router_w || !blk->bias || !blk->w_dn || !blk->w_up || !blk->g_norm || !blk->w1s || !blk->w3s ||
+        !blk->w2s)
+        return K3MX_EINVAL;
+    if (h_dtype != K3MX_F32 && h_dtype != K3MX_BF16) return K3MX_EINVAL;
+    if (!(top_p == top_p) || top_p == INFINITY || top_p == -INFINITY) return K3MX_EINVAL;
+    if (n_tokens < 1 || n_tokens > K3MX_MAX_TOKENS) return K3MX_ESHAPE;
+    if (!aligned16(y) || !aligned16(hidden) || !aligned16(experts) || !aligned16(blk->router_w) ||
+        !aligned16(blk->bias) || !aligned16(blk->w_dn) || !aligned16(blk->w_up) || !aligned16(blk->g_norm) ||
+        !aligned16(blk->w1s) || !aligned16(blk->w3s) || !aligned16(blk->w2s) ||
+        (idx_out && !aligned16(idx_out)) || (w_out && !aligned16(w_out)))
+        return K3MX_EALIGN;
+    const LatentLayout L = latent_layout(n_tokens, h_dtype);
+    if (!workspace || ws_bytes < L.total) return K3MX_EWORKSPACE;
+    if (!aligned256(workspace)) return K3MX_EALIGN;
+    Ctx c;
+    k3mx_status st = device_ctx(reinterpret_cast<cudaStream_t>(stream), c);
+    if (st != K3MX_OK) return st;
+    const int T = n_tokens;
+    const int h_bf16 = h_dtype == K3MX_BF16 ? 1 : 0;
+    float *logits = at<float>(workspace, L.logits), *ylat = at<float>(workspace, L.ylat);
+    float *gu = at<float>(workspace, L.gu), *ysh = at<float>(workspace, L.ysh);
+    void *xlat = at<void>(workspace, L.xlat);
+    auto gemv = [&](float *out, int ldy, int col0, const float *add, const void *x, int x_bf16, int ldx,
+                    const uint16_t *W0, const uint16_t *W1, int r_split, int rows, int K, int xf) {
+        GemvArgs a{};
+        a.y = out;
+        a.ldy = ldy;
+        a.col0 = col0;
+        a.add = add;
+        a.x = x;
+        a.x_bf16 = x_bf16;
+        a.ldx = ldx;
+        a.g = blk->g_norm;
+        a.W0 = W0;
+        a.W1 = W1;
+        a.r_split = r_split;
+        a.rows = rows;
+        a.n_tokens = T;
+        a.status = c.status;
+        return launch_dense_gemv(c, K, xf, a);
+    };
+    const uint16_t *hb = static_cast<const uint16_t *>(hidden);
+    // 1. the router's logits
+    cudaError_t err = traced("router", c.stream,
+                             [&] { return launch_router_logits(c, logits, hidden, h_bf16, blk->router_w, T); });
+    // 2. the latent: x = W_dn h (7168 -> 3584)
+    if (err == cudaSuccess)
+        err = traced("latent_down", c.stream, [&] {
+            return L.batched ? launch_dense_gemm(c, kHid, blk->w_dn, kD, hb, T, nullptr, static_cast<uint16_t *>(xlat),
+                                                 kD, 0, nullptr)
+                             : gemv(static_cast<float *>(xlat), kD, 0, nullptr, hidden, h_bf16, kHid, blk->w_dn,
+                                    blk->w_dn, kD, kD, kHid, kXfPlain);
+        });
+    if (err != cudaSuccess) return from_cuda(err);
+    // 3. the routed experts on the latent: route, group, experts, weighted sum
+    st = run_moe(c, ylat, xlat, L.batched ? K3MX_BF16 : K3MX_F32, T, experts, logits, blk->bias,
+                 L.moe_path, idx_out, w_out, at<void>(workspace, L.moe), L.moe_l, (double)top_p);
+    if (st != K3MX_OK) return st;
+    // 4. the fused shared experts' g | u on the hidden state
+    err = traced("shared_gate_up", c.stream, [&] {
+        if (!L.batched)
+            return gemv(gu, 2 * kFs, 0, nullptr, hidden, h_bf16, kHid, blk->w1s, blk->w3s, kFs, 2 * kFs, kHid,
+                        kXfPlain);
+        cudaError_t e = launch_dense_gemm(c, kHid, blk->w1s, kFs, hb, T, gu, nullptr, 2 * kFs, 0, nullptr);
+        if (e == cudaSuccess) e = launch_dense_gemm(c, kHid, blk->w3s, kFs, hb, T, gu, nullptr, 2 * kFs, kFs, nullptr);
+        return e;
+    });
+    // 5. their down projection of SiTU-GLU(g, u)
+    if (err == cudaSuccess)
+        err = traced("shared_down", c.stream, [&] {
+            if (!L.batched)
+                return gemv(ysh, kHid, 0, nullptr, gu, 0, 2 * kFs, blk->w2s, blk->w2s, kHid, kHid, kFs, kXfSitu);
+            uint16_t *act = at<uint16_t>(workspace, L.act);
+            cudaError_t e = launch_situ_bf16(c, gu, kFs, T, act);
+            if (e == cudaSuccess) e = launch_dense_gemm(c, kFs, blk->w2s, kHid, act, T, ysh, nullptr, kHid, 0, nullptr);
+            return e;
+        });
+    // 6. y = W_up RMSNorm(routed sum) + shared (3584 -> 7168)
+    if (err == cudaSuccess)
+        err = traced("latent_up", c.stream, [&] {
+            if (!L.batched)
+                return gemv(y, kHid, 0, ysh, ylat, 0, kD, blk->w_up, blk->w_up, kHid, kHid, kD, kXfRmsNorm);
+            uint16_t *z = at<uint16_t>(workspace, L.z);
+            cudaError_t e = launch_rmsnorm_bf16(c, ylat, blk->g_norm, kD, T, z);
+            if (e == cudaSuccess) e = launch_dense_gemm(c, kD, blk->w_up, kHid, z, T, y, nullptr, kHid, 0, ysh);
+            return e;
+        });
     return from_cuda(err);
 }
 

@@ -1,0 +1,41 @@
+// dense.cuh - the bf16 matrix products of the LatentMoE block (dense.cu).
+#pragma once
+#include "common.cuh"
+
+namespace k3mx {
+
+constexpr int kXfPlain = 0;      // the input as given (fp32 or bf16)
+constexpr int kXfSitu = 1;       // SiTU-GLU(g, u) of an fp32 [g | u] row pair (u at +K)
+constexpr int kXfRmsNorm = 2;    // RMSNorm (eps 1e-5) of an fp32 row times a bf16 weight
+constexpr int kDenseGemmMinTokens = 17;   // bf16 inputs from here on: the tensor cores
+
+// y[t * ldy + col0 + r] = sum_c W[r][c] xin[t][c] (+ add at the same place)
+struct GemvArgs {
+    float *y;
+    int ldy, col0;
+    const float *add;            // or null
+    const void *x;               // input rows [T][ldx]
+    int x_bf16, ldx;
+    const uint16_t *g;           // RMSNorm weight [K] (kXfRmsNorm)
+    const uint16_t *W0, *W1;     // weight rows [0, r_split) of W0, the rest of W1
+    int r_split, rows;
+    int n_tokens;
+    int *status;
+};
+
+// CUDA cores, any token count; K in {7168, 6144, 3584}; r_split a multiple of 8
+cudaError_t launch_dense_gemv(const Ctx &c, int K, int xf, const GemvArgs &a);
+
+// tcgen05 tensor cores: x bf16 [T][K] (row stride K), W bf16 [rows][K],
+// rows a multiple of 128, K in {7168, 6144, 3584}; the output fp32 (y) or
+// bf16 (y_bf16), y[t * ldy + col0 + r] (+ add, fp32 output only)
+cudaError_t launch_dense_gemm(const Ctx &c, int K, const uint16_t *W, int rows, const uint16_t *x, int n_tokens,
+                              float *y, uint16_t *y_bf16, int ldy, int col0, const float *add);
+
+// SiTU-GLU of fp32 [T][2F] (g | u) rows into bf16 [T][F]
+cudaError_t launch_situ_bf16(const Ctx &c, const float *gu, int F, int n_tokens, uint16_t *out);
+// RMSNorm (eps 1e-5) of fp32 [T][D] rows times a bf16 weight, into bf16
+cudaError_t launch_rmsnorm_bf16(const Ctx &c, const float *x, const uint16_t *g, int D, int n_tokens,
+                                uint16_t *out);
+
+}  // namespace k3mx

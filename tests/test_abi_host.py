@@ -15,7 +15,7 @@ FAKE = 0x10000          # an aligned, non-null address that is never dereference
 def test_library_exports_every_declared_symbol():
     L = k3mx.lib()
     declared = k3mx.declared_symbols()
-    assert len(declared) == 20
+    assert len(declared) == 22
     out = subprocess.run(["nm", "-D", "--defined-only", k3mx.LIB_PATH],
                          capture_output=True, text=True, check=True).stdout
     exported = set(re.findall(r"\sT\s(k3mx_\w+)", out))
