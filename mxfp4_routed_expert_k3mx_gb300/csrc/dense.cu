@@ -8,8 +8,8 @@
 // RMSNorm of the input times its weight.  Every product of a bf16 weight
 // and an fp32 value is exact in fp32; the sums are fp32.
 //
-// Few tokens, or fp32 inputs: k_gemv, one warp per weight row, the CTA's 8
-// rows brought in by bulk copies first; HBM-bound on the weights.  Many bf16
+// Few tokens, or fp32 inputs: k_gemv, persistent CTAs streaming their rows
+// through a ring of bulk copies, one warp per row; HBM-bound on the weights.  Many bf16
 // inputs: k_gemm on the tcgen05 tensor cores (kind::f16 with bf16 A and B,
 // fp32 accumulators in TMEM); a CTA computes 128 weight rows x 256 tokens
 // over the whole sum, its operands streamed by TMA (128-byte swizzle)
@@ -23,7 +23,9 @@ namespace k3mx {
 namespace {
 
 constexpr int kGemvTok = 3;                      // inputs per shared-memory chunk
-constexpr int kGemvRows = 8;                     // one weight row per warp
+constexpr int kGemvWarps = 8;                    // consumer warps, one weight row each at a time
+constexpr int kGemvThreads = (kGemvWarps + 1) * 32;   // + the producer warp
+constexpr int kGemvMaxSlots = 16;
 constexpr float kRmsEps = 1e-5f;                 // K3Cfg rms_eps
 
 template <int K>
@@ -31,8 +33,12 @@ struct GemvShape {
     static constexpr int VEC = K / 8;            // 16-byte vectors per row
     static constexpr int VPL = VEC / 32;         // per lane
     static constexpr int ROWB = K * 2;
-    static constexpr int SMEM = 1024 + kGemvRows * ROWB + kGemvTok * K * 4;
-    static_assert(VEC % 32 == 0, "row length");
+    static constexpr int HDR = 2048;             // barriers and partial sums
+    static constexpr int STAGE = kGemvTok * K * 4;
+    static constexpr int FIT = (227 * 1024 - 1024 - HDR - STAGE) / ROWB;
+    static constexpr int SLOTS = FIT > kGemvMaxSlots ? kGemvMaxSlots : FIT;
+    static constexpr int SMEM = 1024 + HDR + STAGE + SLOTS * ROWB;   // + the 1024-byte alignment slack
+    static_assert(VEC % 32 == 0 && SLOTS >= 4, "row length");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
@@ -63,48 +69,56 @@ __device__ __forceinline__ float4 input4(const GemvArgs &a, int t, int c4, float
     return v;
 }
 
-// One warp per weight row: the CTA's rows (up to 8 x 2K bytes, contiguous in
-// one matrix) come in by bulk copies issued first; the inputs pass through
-// shared memory in chunks of 3 (loads batched 8 per thread), laid out so
-// that lanes read consecutive 16-byte words (columns 8v..8v+3 at slot v,
-// 8v+4..8v+7 at slot K/8 + v, vector v = lane + 32 i).  Per lane, a vector's
-// 8 products are two 4-term sums added, the vectors go to four running sums
-// added pairwise, and the warp adds its lanes (about 20 fp32 roundings deep
-// at K = 7168).  RMSNorm inputs first reduce each token's sum of squares over
-// the CTA.
+// Persistent, one CTA per SM over a contiguous range of weight rows.  The
+// inputs (3 at a time) are staged in shared memory first, laid out so that
+// lanes read consecutive 16-byte words (columns 8v..8v+3 at slot v,
+// 8v+4..8v+7 at slot K/8 + v, vector v = lane + 32 i); then a producer warp
+// streams the range's rows by bulk copies through a ring of up to 16 row
+// slots while 8 consumer warps take one row each at a time.  Per lane, a
+// vector's 8 products are two 4-term sums added, the vectors go to four
+// running sums added pairwise, and the warp adds its lanes (about 20 fp32
+// roundings deep at K = 7168).  RMSNorm inputs first reduce each token's
+// sum of squares over the CTA.
 template <int K, int XF>
-__global__ void __launch_bounds__(kGemvRows * 32, 1) k_gemv(const GemvArgs a) {
+__global__ void __launch_bounds__(kGemvThreads, 1) k_gemv(const GemvArgs a) {
     using Sh = GemvShape<K>;
-    constexpr int VEC = Sh::VEC, VPL = Sh::VPL;
+    constexpr int VEC = Sh::VEC, VPL = Sh::VPL, SLOTS = Sh::SLOTS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
-    float *red = reinterpret_cast<float *>(smem + 64);          // [kGemvTok][8] partial sums of squares
-    const uint8_t *rows = smem + 1024;
-    float4 *hs = reinterpret_cast<float4 *>(smem + 1024 + kGemvRows * Sh::ROWB);   // [kGemvTok][2 VEC]
+    const uint32_t full0 = smem_addr(smem), empty0 = full0 + 8 * kGemvMaxSlots;
+    float *red = reinterpret_cast<float *>(smem + 16 * kGemvMaxSlots);   // [kGemvTok][kGemvWarps + 1]
+    float4 *hs = reinterpret_cast<float4 *>(smem + Sh::HDR);             // [kGemvTok][2 VEC]
+    const uint32_t ring = smem_addr(smem) + Sh::HDR + Sh::STAGE;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r0 = blockIdx.x * kGemvRows;
-    const int nrows = min(kGemvRows, a.rows - r0);
-    const uint32_t b = smem_addr(bar);
+    constexpr int NW = kGemvWarps + 1;
+    const int G = gridDim.x, b = blockIdx.x;
+    const int rb = (int)((long long)a.rows * b / G), nr = (int)((long long)a.rows * (b + 1) / G) - rb;
+    const int prefilled = min(nr, SLOTS);         // rows whose copies go out before anything else
+    auto row_src = [&](int i) {
+        const int gr = rb + i;
+        return gr < a.r_split ? a.W0 + (size_t)gr * K : a.W1 + (size_t)(gr - a.r_split) * K;
+    };
     if (threadIdx.x == 0) {
-        mbar_init(b, 1);
+        for (int i = 0; i < SLOTS; i++) {
+            mbar_init(full0 + 8 * i, 1);
+            mbar_init(empty0 + 8 * i, 1);
+        }
         fence_mbar_init();
-        mbar_arrive_expect_tx(b, (uint32_t)(nrows * Sh::ROWB));
+        // the weights are the call's own: the ring fills while the kernel
+        // before finishes and the inputs are staged
         const uint64_t pol = l2_evict_first_policy();
-        for (int r = 0; r < nrows; r++) {
-            const int gr = r0 + r;
-            const uint16_t *src = gr < a.r_split ? a.W0 + (size_t)gr * K : a.W1 + (size_t)(gr - a.r_split) * K;
-            bulk_g2s(smem_addr(rows) + r * Sh::ROWB, src, Sh::ROWB, b, pol);
+        for (int i = 0; i < prefilled; i++) {
+            mbar_arrive_expect_tx(full0 + 8 * i, Sh::ROWB);
+            bulk_g2s(ring + i * Sh::ROWB, row_src(i), Sh::ROWB, full0 + 8 * i, pol);
         }
     }
     // the kernel behind may start its prologue
     pdl_launch_dependents();
     pdl_wait();                                   // the inputs, if a kernel before writes them
-    const uint4 *wr = reinterpret_cast<const uint4 *>(rows + warp * Sh::ROWB);
-    bool have_rows = false;
-    for (int t0 = 0; t0 < a.n_tokens; t0 += kGemvTok) {
+    int gbase = 0;                                // rows this CTA streamed in earlier chunks
+    for (int t0 = 0; t0 < a.n_tokens; t0 += kGemvTok, gbase += nr) {
         const int nt = min(kGemvTok, a.n_tokens - t0);
-        __syncthreads();                          // the barrier is set up; the previous chunk is consumed
+        __syncthreads();                          // barriers set up; the previous chunk is consumed
         float scale[kGemvTok] = {1.f, 1.f, 1.f};
         if (XF == kXfRmsNorm) {
             for (int j = 0; j < nt; j++) {
@@ -116,13 +130,12 @@ __global__ void __launch_bounds__(kGemvRows * 32, 1) k_gemv(const GemvArgs a) {
                 }
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-                if (lane == 0) red[j * 8 + warp] = ss;
+                if (lane == 0) red[j * NW + warp] = ss;
             }
             __syncthreads();
             for (int j = 0; j < nt; j++) {
                 float ss = 0.f;
-#pragma unroll
-                for (int w = 0; w < kGemvRows; w++) ss += red[j * 8 + w];
+                for (int w = 0; w < NW; w++) ss += red[j * NW + w];
                 scale[j] = 1.0f / sqrtf(ss / (float)K + kRmsEps);
             }
         }
@@ -135,8 +148,7 @@ __global__ void __launch_bounds__(kGemvRows * 32, 1) k_gemv(const GemvArgs a) {
                 const int i = i0 + u * (int)blockDim.x;
                 if (i < n4) {
                     const int t = i / (K / 4), c4 = i % (K / 4);
-                    float sc = scale[0];
-                    if (XF == kXfRmsNorm) sc = t == 0 ? scale[0] : (t == 1 ? scale[1] : scale[2]);
+                    const float sc = t == 0 ? scale[0] : (t == 1 ? scale[1] : scale[2]);
                     v[u] = input4<K, XF>(a, t0 + t, c4, sc);
                 }
             }
@@ -150,55 +162,72 @@ __global__ void __launch_bounds__(kGemvRows * 32, 1) k_gemv(const GemvArgs a) {
             }
         }
         __syncthreads();
-        if (!have_rows) {
-            if (!mbar_wait(b, 0)) {
-                if (lane == 0) report_status(a.status, kStatusWaitTimeout, 310);
-                return;                           // every warp leaves: no barrier follows
-            }
-            have_rows = true;
-        }
-        if (warp >= nrows) continue;
-        // four independent running sums per input (vectors i mod 4), each
-        // vector's 8 products as two 4-term chains: the iterations overlap
-        float acc[kGemvTok][4];
-#pragma unroll
-        for (int j = 0; j < kGemvTok; j++)
-#pragma unroll
-            for (int r = 0; r < 4; r++) acc[j][r] = 0.f;
-#pragma unroll 2
-        for (int i0 = 0; i0 < VPL; i0 += 4)
-#pragma unroll
-        for (int r = 0; r < 4; r++) {
-            const int i = i0 + r;
-            if (i >= VPL) break;
-            const int v = lane + 32 * i;
-            const uint4 q = wr[v];
-            const float w0 = bf16_lo(q.x), w1 = bf16_hi(q.x), w2 = bf16_lo(q.y), w3 = bf16_hi(q.y);
-            const float w4 = bf16_lo(q.z), w5 = bf16_hi(q.z), w6 = bf16_lo(q.w), w7 = bf16_hi(q.w);
-#pragma unroll
-            for (int j = 0; j < kGemvTok; j++) {
-                if (j < nt) {
-                    const float4 x0 = hs[j * (2 * VEC) + v], x1 = hs[j * (2 * VEC) + VEC + v];
-                    float s0 = w0 * x0.x, s1 = w4 * x1.x;
-                    s0 = fmaf(w1, x0.y, s0);
-                    s1 = fmaf(w5, x1.y, s1);
-                    s0 = fmaf(w2, x0.z, s0);
-                    s1 = fmaf(w6, x1.z, s1);
-                    s0 = fmaf(w3, x0.w, s0);
-                    s1 = fmaf(w7, x1.w, s1);
-                    acc[j][r] += s0 + s1;
+        if (warp == kGemvWarps) {
+            // ---------------------------------------------------- producer --
+            if (lane == 0) {
+                const uint64_t pol = l2_evict_first_policy();
+                for (int i = gbase == 0 ? prefilled : 0; i < nr; i++) {
+                    const int g = gbase + i, s = g % SLOTS;
+                    if (g >= SLOTS && !mbar_wait(empty0 + 8 * s, ((g / SLOTS) - 1) & 1)) {
+                        report_status(a.status, kStatusWaitTimeout, 311);
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full0 + 8 * s, Sh::ROWB);
+                    bulk_g2s(ring + s * Sh::ROWB, row_src(i), Sh::ROWB, full0 + 8 * s, pol);
                 }
             }
+            continue;
         }
+        // ------------------------------------------------------ consumers --
+        for (int i = warp; i < nr; i += kGemvWarps) {
+            const int g = gbase + i, s = g % SLOTS;
+            const bool ok = mbar_wait(full0 + 8 * s, (g / SLOTS) & 1);
+            if (!ok && lane == 0) report_status(a.status, kStatusWaitTimeout, 310);
+            const uint4 *wr = reinterpret_cast<const uint4 *>(smem + Sh::HDR + Sh::STAGE + s * Sh::ROWB);
+            // four independent running sums per input (vectors i mod 4),
+            // each vector's 8 products as two 4-term chains
+            float acc[kGemvTok][4];
 #pragma unroll
-        for (int j = 0; j < kGemvTok; j++) {
-            float s = (acc[j][0] + acc[j][1]) + (acc[j][2] + acc[j][3]);
+            for (int j = 0; j < kGemvTok; j++)
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-            if (lane == 0 && j < nt) {
-                const size_t o = (size_t)(t0 + j) * a.ldy + a.col0 + r0 + warp;
-                if (a.add != nullptr) s += a.add[o];
-                a.y[o] = s;
+                for (int r = 0; r < 4; r++) acc[j][r] = 0.f;
+#pragma unroll 2
+            for (int v0 = 0; v0 < VPL; v0 += 4)
+#pragma unroll
+                for (int r = 0; r < 4; r++) {
+                    const int vi = v0 + r;
+                    if (vi >= VPL) break;
+                    const int v = lane + 32 * vi;
+                    const uint4 q = wr[v];
+                    const float w0 = bf16_lo(q.x), w1 = bf16_hi(q.x), w2 = bf16_lo(q.y), w3 = bf16_hi(q.y);
+                    const float w4 = bf16_lo(q.z), w5 = bf16_hi(q.z), w6 = bf16_lo(q.w), w7 = bf16_hi(q.w);
+#pragma unroll
+                    for (int j = 0; j < kGemvTok; j++) {
+                        if (j < nt) {
+                            const float4 x0 = hs[j * (2 * VEC) + v], x1 = hs[j * (2 * VEC) + VEC + v];
+                            float s0 = w0 * x0.x, s1 = w4 * x1.x;
+                            s0 = fmaf(w1, x0.y, s0);
+                            s1 = fmaf(w5, x1.y, s1);
+                            s0 = fmaf(w2, x0.z, s0);
+                            s1 = fmaf(w6, x1.z, s1);
+                            s0 = fmaf(w3, x0.w, s0);
+                            s1 = fmaf(w7, x1.w, s1);
+                            acc[j][r] += s0 + s1;
+                        }
+                    }
+                }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * s);      // the slot's row is read
+#pragma unroll
+            for (int j = 0; j < kGemvTok; j++) {
+                float sum = (acc[j][0] + acc[j][1]) + (acc[j][2] + acc[j][3]);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+                if (lane == 0 && j < nt && ok) {
+                    const size_t o = (size_t)(t0 + j) * a.ldy + a.col0 + rb + i;
+                    if (a.add != nullptr) sum += a.add[o];
+                    a.y[o] = sum;
+                }
             }
         }
     }
@@ -431,8 +460,11 @@ cudaError_t gemv_t(const Ctx &c, const GemvArgs &a) {
     static bool done = false;
     const cudaError_t e = configure_once(k_gemv<K, XF>, GemvShape<K>::SMEM, done);
     if (e != cudaSuccess) return e;
-    return launch_pdl(k_gemv<K, XF>, dim3((a.rows + kGemvRows - 1) / kGemvRows), dim3(kGemvRows * 32),
-                      (size_t)GemvShape<K>::SMEM, c.stream, a);
+    // one CTA per SM, at least 4 rows each
+    int grid = c.num_sms;
+    if (grid > (a.rows + 3) / 4) grid = (a.rows + 3) / 4;
+    if (grid < 1) grid = 1;
+    return launch_pdl(k_gemv<K, XF>, dim3(grid), dim3(kGemvThreads), (size_t)GemvShape<K>::SMEM, c.stream, a);
 }
 
 template <int K>
@@ -450,7 +482,6 @@ cudaError_t gemm_t(const Ctx &c, const uint16_t *W, int rows, const uint16_t *x,
 }  // namespace
 
 cudaError_t launch_dense_gemv(const Ctx &c, int K, int xf, const GemvArgs &a) {
-    if (a.r_split % kGemvRows != 0) return cudaErrorInvalidValue;
     if (K == 7168 && xf == kXfPlain) return gemv_t<7168, kXfPlain>(c, a);
     if (K == 6144 && xf == kXfSitu) return gemv_t<6144, kXfSitu>(c, a);
     if (K == 3584 && xf == kXfRmsNorm) return gemv_t<3584, kXfRmsNorm>(c, a);

@@ -23,7 +23,7 @@ struct GemvArgs {
     int *status;
 };
 
-// CUDA cores, any token count; K in {7168, 6144, 3584}; r_split a multiple of 8
+// CUDA cores, any token count; K in {7168, 6144, 3584}
 cudaError_t launch_dense_gemv(const Ctx &c, int K, int xf, const GemvArgs &a);
 
 // tcgen05 tensor cores: x bf16 [T][K] (row stride K), W bf16 [rows][K],
