@@ -345,6 +345,14 @@ __global__ void __launch_bounds__(kGThreads, 1)
             const uint32_t base = tmem + ((uint32_t)(32 * q) << 16);
             for (int c0 = 0; c0 < kGN; c0 += 16) {
                 if (n0 + c0 >= o.n_tokens) break;
+                // the addends first, all 16 loads in flight (the output
+                // stores cannot then hold them back)
+                float ad[16];
+#pragma unroll
+                for (int j = 0; j < 16; j++) {
+                    const int t = n0 + c0 + j;
+                    ad[j] = o.add != nullptr && t < o.n_tokens ? __ldg(o.add + (size_t)t * o.ldy + o.col0 + r) : 0.f;
+                }
                 uint32_t v[16];
                 tmem_ld16(base + c0, v);
                 tmem_ld_wait();
@@ -353,8 +361,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
                     const int t = n0 + c0 + j;
                     if (t < o.n_tokens) {
                         const size_t at = (size_t)t * o.ldy + o.col0 + r;
-                        float val = __uint_as_float(v[j]);
-                        if (o.add != nullptr) val += o.add[at];
+                        const float val = __uint_as_float(v[j]) + ad[j];
                         if (o.y_bf16 != nullptr) o.y_bf16[at] = f32_to_bf16_rn(val);
                         else o.y[at] = val;
                     }
