@@ -275,7 +275,7 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
     return (uint16_t)((u + 0x7FFFu + ((u >> 16) & 1u)) >> 16);
 }
 
-template <int K>
+template <int K, bool ADD>
 __global__ void __launch_bounds__(kGThreads, 1)
     k_gemm(const GemmOut o, const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap) {
     constexpr int KSTEPS = K / kGK;
@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 16; j++) {
                     const int t = n0 + c0 + j;
-                    ad[j] = o.add != nullptr && t < o.n_tokens ? __ldg(o.add + (size_t)t * o.ldy + o.col0 + r) : 0.f;
+                    ad[j] = ADD && t < o.n_tokens ? __ldg(o.add + (size_t)t * o.ldy + o.col0 + r) : 0.f;
                 }
                 uint32_t v[16];
                 tmem_ld16(base + c0, v);
@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
                     const int t = n0 + c0 + j;
                     if (t < o.n_tokens) {
                         const size_t at = (size_t)t * o.ldy + o.col0 + r;
-                        const float val = __uint_as_float(v[j]) + ad[j];
+                        const float val = ADD ? __uint_as_float(v[j]) + ad[j] : __uint_as_float(v[j]);
                         if (o.y_bf16 != nullptr) o.y_bf16[at] = f32_to_bf16_rn(val);
                         else o.y[at] = val;
                     }
@@ -474,16 +474,16 @@ cudaError_t gemv_t(const Ctx &c, const GemvArgs &a) {
     return launch_pdl(k_gemv<K, XF>, dim3(grid), dim3(kGemvThreads), (size_t)GemvShape<K>::SMEM, c.stream, a);
 }
 
-template <int K>
+template <int K, bool ADD>
 cudaError_t gemm_t(const Ctx &c, const uint16_t *W, int rows, const uint16_t *x, const GemmOut &o) {
     static bool done = false;
-    const cudaError_t e = configure_once(k_gemm<K>, kGSmem, done);
+    const cudaError_t e = configure_once(k_gemm<K, ADD>, kGSmem, done);
     if (e != cudaSuccess) return e;
     CUtensorMap wm, xm;
     if (!encode_bf16_rows(wm, W, K, (uint64_t)rows, kGM) || !encode_bf16_rows(xm, x, K, (uint64_t)o.n_tokens, kGN))
         return cudaErrorInvalidValue;
     const dim3 grid(rows / kGM, (o.n_tokens + kGN - 1) / kGN);
-    return launch_pdl(k_gemm<K>, grid, dim3(kGThreads), (size_t)kGSmem, c.stream, o, wm, xm);
+    return launch_pdl(k_gemm<K, ADD>, grid, dim3(kGThreads), (size_t)kGSmem, c.stream, o, wm, xm);
 }
 
 }  // namespace
@@ -499,9 +499,13 @@ cudaError_t launch_dense_gemm(const Ctx &c, int K, const uint16_t *W, int rows, 
                               float *y, uint16_t *y_bf16, int ldy, int col0, const float *add) {
     if (rows % kGM != 0 || n_tokens < 1) return cudaErrorInvalidValue;
     const GemmOut o{y, y_bf16, ldy, col0, add, n_tokens, c.status};
-    if (K == 7168) return gemm_t<7168>(c, W, rows, x, o);
-    if (K == 6144) return gemm_t<6144>(c, W, rows, x, o);
-    if (K == 3584) return gemm_t<3584>(c, W, rows, x, o);
+    if (add != nullptr) {
+        if (K == 3584) return gemm_t<3584, true>(c, W, rows, x, o);
+        return cudaErrorInvalidValue;
+    }
+    if (K == 7168) return gemm_t<7168, false>(c, W, rows, x, o);
+    if (K == 6144) return gemm_t<6144, false>(c, W, rows, x, o);
+    if (K == 3584) return gemm_t<3584, false>(c, W, rows, x, o);
     return cudaErrorInvalidValue;
 }
 
