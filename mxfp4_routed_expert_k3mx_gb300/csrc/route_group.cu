@@ -674,6 +674,7 @@ k_group_count(const int32_t *idx, int n_pairs, int *hist, int *status) {
 }
 
 // column sums, offsets, active list, and per-segment starting positions
+// within each expert (the scatter adds the expert offsets)
 __global__ void __launch_bounds__(1024)
 k_group_scan(int *hist, int n_seg, GroupOut g) {
     __shared__ int cnt[kE];
@@ -696,24 +697,13 @@ k_group_scan(int *hist, int n_seg, GroupOut g) {
         cnt[e] = c;
     }
     __syncthreads();
-    finish_counts(cnt, g, tmp);
-    if (e < kE) {
-        const int off = cnt[e];
-        for (int s0 = 0; s0 < n_seg; s0 += B) {
-            int h[B];
-#pragma unroll
-            for (int j = 0; j < B; j++) h[j] = s0 + j < n_seg ? hist[(size_t)(s0 + j) * kE + e] : 0;
-#pragma unroll
-            for (int j = 0; j < B; j++)
-                if (s0 + j < n_seg) hist[(size_t)(s0 + j) * kE + e] = h[j] + off;
-        }
-    }
+    finish_counts(cnt, g, tmp);                      // offsets: the scatter adds them
 }
 
 __global__ void __launch_bounds__(32)
-k_group_scatter(const int32_t *idx, int n_pairs, const int *base, int32_t *perm) {
+k_group_scatter(const int32_t *idx, int n_pairs, const int *base, const int32_t *offsets, int32_t *perm) {
     __shared__ int running[kE];
-    for (int e = threadIdx.x; e < kE; e += 32) running[e] = base[(size_t)blockIdx.x * kE + e];
+    for (int e = threadIdx.x; e < kE; e += 32) running[e] = base[(size_t)blockIdx.x * kE + e] + offsets[e];
     __syncwarp();
     const int p0 = blockIdx.x * kSeg;
     scatter_warp(idx, p0, min(p0 + kSeg, n_pairs), running, perm);
@@ -782,7 +772,7 @@ cudaError_t launch_group(const Ctx &c, const int32_t *idx, int n_tokens, const G
     int *hist = static_cast<int *>(scratch);
     k_group_count<<<n_seg, 256, 0, c.stream>>>(idx, n_pairs, hist, c.status);
     k_group_scan<<<1, 1024, 0, c.stream>>>(hist, n_seg, g);
-    k_group_scatter<<<n_seg, 32, 0, c.stream>>>(idx, n_pairs, hist, g.perm);
+    k_group_scatter<<<n_seg, 32, 0, c.stream>>>(idx, n_pairs, hist, g.offsets, g.perm);
     return cudaGetLastError();
 }
 

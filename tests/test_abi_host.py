@@ -1,6 +1,7 @@
 """Host-side checks of the C ABI that need no GPU: the library loads, exports
 every function include/k3mx.h declares, and refuses bad arguments before it
 touches the device."""
+import ctypes
 import re
 import subprocess
 
@@ -70,6 +71,30 @@ def test_router_refuses_bad_arguments():
     assert call(p=float("nan")) == 1
     assert call(T=0) == 3 and call(T=65537) == 3
     assert call(h=FAKE + 4) == 2 and call(W=FAKE + 8) == 2
+
+
+def test_latent_block_refuses_bad_arguments():
+    L = k3mx.lib()
+    blk = k3mx.LatentBlock(*([FAKE] * 8))
+    ws = k3mx.k3mx_latent_moe_workspace_size(1, k3mx.K3MX_F32)
+    assert ws > k3mx.k3mx_moe_workspace_size(1, k3mx.K3MX_F32, k3mx.K3MX_PATH_DECODE)
+    assert k3mx.k3mx_latent_moe_workspace_size(0, 0) == 0 and k3mx.k3mx_latent_moe_workspace_size(1, 2) == 0
+    # bf16 batches keep bf16 intermediates: a 4096-token workspace holds the
+    # shared experts' g | u in fp32 and their activation in bf16
+    assert k3mx.k3mx_latent_moe_workspace_size(4096, 1) >= 4096 * (2 * 6144 * 4 + 6144 * 2)
+    call = lambda **kw: L.k3mx_latent_moe(*(dict(dict(y=FAKE, h=FAKE, dt=0, T=1, b=ctypes.byref(blk), ex=FAKE, p=0.0,
+                                                      io=None, wo=None, ws=FAKE, wsb=ws), **kw)[k]
+                                            for k in ("y", "h", "dt", "T", "b", "ex", "p", "io", "wo", "ws", "wsb")),
+                                          None)
+    assert call(b=None) == 1 and call(ex=None) == 1
+    assert call(dt=2) == 1 and call(p=float("nan")) == 1
+    assert call(T=0) == 3
+    assert call(h=FAKE + 4) == 2
+    assert call(wsb=ws - 1) == 4
+    bad = k3mx.LatentBlock(*([FAKE] * 7 + [None]))
+    assert call(b=ctypes.byref(bad)) == 1                      # every tensor of the block is required
+    bad = k3mx.LatentBlock(*([FAKE] * 4 + [FAKE + 2] + [FAKE] * 3))
+    assert call(b=ctypes.byref(bad)) == 2                      # g_norm misaligned
 
 
 def test_moe_refuses_bad_arguments():
