@@ -10,7 +10,7 @@ streamed per second (GB/s); the line also carries the batch-64 decode and
 4096-token prefill workloads under "secondary".
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference]
-  python bench.py --profile-case decode|prefill|router --tokens T [--resident R]
+  python bench.py --profile-case decode|prefill|router|latent --tokens T [--resident R]
                   [--confine] [--mx] [--iters I]
 
 The --profile-case form runs a small case of one path for Nsight Compute
@@ -619,6 +619,33 @@ def run_profile_case(args):
     import mxfp4_routed_expert_k3mx_gb300 as k3mx
     import synth
     dev = torch.device("cuda:0")
+    if args.profile_case == "latent":
+        # the whole LatentMoE block over R resident experts (entry e -> e mod R)
+        T, R = args.tokens, args.resident
+        arena = synth.expert_arena_device(dev, seed=0, lo=118, hi=128, n_experts=R)
+        table = k3mx.expert_table(arena, n_experts=R)[torch.arange(E, device=dev) % R].contiguous()
+        host = synth.latent_block_weights(seed=0)
+        host["router_w"] = synth.router_weights(seed=0)
+        dblk = {k: torch.from_numpy(v.view(np.int16)).to(dev) for k, v in host.items()}
+        _, bias = synth.router_inputs(1, seed=0)
+        dblk["bias"] = torch.from_numpy(bias).to(dev)
+        blk = k3mx.latent_block(dblk)
+        h = synth.hidden_inputs(T, seed=1)
+        bf16 = T > 16
+        ht = (torch.from_numpy(synth.f32_to_bf16(h).view(np.int16)).view(torch.bfloat16) if bf16
+              else torch.from_numpy(h)).to(dev)
+        dt = k3mx.K3MX_BF16 if bf16 else k3mx.K3MX_F32
+        y = torch.empty((T, 7168), dtype=torch.float32, device=dev)
+        ws = torch.empty(k3mx.k3mx_latent_moe_workspace_size(T, dt), dtype=torch.uint8, device=dev)
+        for _ in range(args.iters):
+            k3mx.k3mx_latent_moe(y, ht, blk, table, ws)
+        torch.cuda.synchronize(dev)
+        st = k3mx.k3mx_device_status()
+        print(json.dumps({"profile_case": "latent", "tokens": T, "resident": R, "iters": args.iters, "status": st}),
+              flush=True)
+        if st[0] != 0:
+            sys.exit(1)
+        return
     if args.profile_case == "router":
         # the router alone: fp32 states up to 16 tokens, bf16 beyond
         T = args.tokens
@@ -674,7 +701,7 @@ def main():
     ap.add_argument("--primary-only", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
-    ap.add_argument("--profile-case", choices=["decode", "prefill", "router"])
+    ap.add_argument("--profile-case", choices=["decode", "prefill", "router", "latent"])
     ap.add_argument("--tokens", type=int, default=1)
     ap.add_argument("--resident", type=int, default=64)
     ap.add_argument("--confine", action="store_true")

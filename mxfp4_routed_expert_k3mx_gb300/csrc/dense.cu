@@ -34,12 +34,16 @@ struct GemvShape {
     static constexpr int VPL = VEC / 32;         // per lane
     static constexpr int ROWB = K * 2;
     static constexpr int HDR = 2048;             // barriers and partial sums
-    static constexpr int STAGE = kGemvTok * K * 4;
-    static constexpr int FIT = (227 * 1024 - 1024 - HDR - STAGE) / ROWB;
-    static constexpr int SLOTS = FIT > kGemvMaxSlots ? kGemvMaxSlots : FIT;
-    static constexpr int SMEM = 1024 + HDR + STAGE + SLOTS * ROWB;   // + the 1024-byte alignment slack
-    static_assert(VEC % 32 == 0 && SLOTS >= 4, "row length");
-    static_assert(SMEM <= 227 * 1024, "shared memory budget");
+    static constexpr int SMEM_MAX = 227 * 1024;
+    // inputs per chunk (1..3) and row slots: the chunk takes what it needs,
+    // the ring the rest (fewer inputs, more rows in flight)
+    static constexpr int slots(int chunk) {
+        const int fit = (SMEM_MAX - 1024 - HDR - chunk * K * 4) / ROWB;
+        return fit > kGemvMaxSlots ? kGemvMaxSlots : fit;
+    }
+    static constexpr int smem(int chunk) { return 1024 + HDR + chunk * K * 4 + slots(chunk) * ROWB; }
+    static_assert(VEC % 32 == 0 && slots(kGemvTok) >= 4, "row length");
+    static_assert(smem(kGemvTok) <= SMEM_MAX && smem(1) <= SMEM_MAX, "shared memory budget");
 };
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
@@ -82,13 +86,16 @@ __device__ __forceinline__ float4 input4(const GemvArgs &a, int t, int c4, float
 template <int K, int XF>
 __global__ void __launch_bounds__(kGemvThreads, 1) k_gemv(const GemvArgs a) {
     using Sh = GemvShape<K>;
-    constexpr int VEC = Sh::VEC, VPL = Sh::VPL, SLOTS = Sh::SLOTS;
+    constexpr int VEC = Sh::VEC, VPL = Sh::VPL;
+    const int chunk = min(kGemvTok, a.n_tokens);  // inputs staged at a time
+    const int SLOTS = Sh::slots(chunk);
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t full0 = smem_addr(smem), empty0 = full0 + 8 * kGemvMaxSlots;
     float *red = reinterpret_cast<float *>(smem + 16 * kGemvMaxSlots);   // [kGemvTok][kGemvWarps + 1]
-    float4 *hs = reinterpret_cast<float4 *>(smem + Sh::HDR);             // [kGemvTok][2 VEC]
-    const uint32_t ring = smem_addr(smem) + Sh::HDR + Sh::STAGE;
+    float4 *hs = reinterpret_cast<float4 *>(smem + Sh::HDR);             // [chunk][2 VEC]
+    const int stage_b = chunk * K * 4;
+    const uint32_t ring = smem_addr(smem) + Sh::HDR + stage_b;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int NW = kGemvWarps + 1;
     const int G = gridDim.x, b = blockIdx.x;
@@ -116,8 +123,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gemv(const GemvArgs a) {
     pdl_launch_dependents();
     pdl_wait();                                   // the inputs, if a kernel before writes them
     int gbase = 0;                                // rows this CTA streamed in earlier chunks
-    for (int t0 = 0; t0 < a.n_tokens; t0 += kGemvTok, gbase += nr) {
-        const int nt = min(kGemvTok, a.n_tokens - t0);
+    for (int t0 = 0; t0 < a.n_tokens; t0 += chunk, gbase += nr) {
+        const int nt = min(chunk, a.n_tokens - t0);
         __syncthreads();                          // barriers set up; the previous chunk is consumed
         float scale[kGemvTok] = {1.f, 1.f, 1.f};
         if (XF == kXfRmsNorm) {
@@ -183,7 +190,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gemv(const GemvArgs a) {
             const int g = gbase + i, s = g % SLOTS;
             const bool ok = mbar_wait(full0 + 8 * s, (g / SLOTS) & 1);
             if (!ok && lane == 0) report_status(a.status, kStatusWaitTimeout, 310);
-            const uint4 *wr = reinterpret_cast<const uint4 *>(smem + Sh::HDR + Sh::STAGE + s * Sh::ROWB);
+            const uint4 *wr = reinterpret_cast<const uint4 *>(smem + Sh::HDR + stage_b + s * Sh::ROWB);
             // four independent running sums per input (vectors i mod 4),
             // each vector's 8 products as two 4-term chains
             float acc[kGemvTok][4];
@@ -465,13 +472,14 @@ cudaError_t configure_once(F kernel, int smem, bool &done) {
 template <int K, int XF>
 cudaError_t gemv_t(const Ctx &c, const GemvArgs &a) {
     static bool done = false;
-    const cudaError_t e = configure_once(k_gemv<K, XF>, GemvShape<K>::SMEM, done);
+    const cudaError_t e = configure_once(k_gemv<K, XF>, GemvShape<K>::SMEM_MAX, done);
     if (e != cudaSuccess) return e;
+    const int chunk = a.n_tokens < kGemvTok ? a.n_tokens : kGemvTok;
     // one CTA per SM, at least 4 rows each
     int grid = c.num_sms;
     if (grid > (a.rows + 3) / 4) grid = (a.rows + 3) / 4;
     if (grid < 1) grid = 1;
-    return launch_pdl(k_gemv<K, XF>, dim3(grid), dim3(kGemvThreads), (size_t)GemvShape<K>::SMEM, c.stream, a);
+    return launch_pdl(k_gemv<K, XF>, dim3(grid), dim3(kGemvThreads), (size_t)GemvShape<K>::smem(chunk), c.stream, a);
 }
 
 template <int K, bool ADD>
