@@ -70,8 +70,9 @@ def check(host, h, y, idx, w, lg, tokens, tol, top_p=0.0):
     return worst
 
 
-@pytest.mark.parametrize("T", [1, 3])
+@pytest.mark.parametrize("T", [1, 3, 5])
 def test_latent_block_fp32(arena, cuda_dev, block, T):
+    """5 states: two input chunks (3 + 2) through every CUDA-core product."""
     host, dblk, blk = block
     _, table = arena
     h = synth.hidden_inputs(T, seed=90 + T)
@@ -88,6 +89,15 @@ def test_latent_block_fp32_top_p(arena, cuda_dev, block):
     y, idx, w, ht = run_block(cuda_dev, table, blk, h, top_p=0.8)
     assert np.any(idx < 0)
     check(host, h, y, idx, w, gpu_logits(cuda_dev, dblk, ht), [0, 1], 1e-4, top_p=0.8)
+
+
+def test_latent_block_bf16_small(arena, cuda_dev, block):
+    """16 bf16 states stay on the CUDA cores (fp32 intermediates)."""
+    host, dblk, blk = block
+    _, table = arena
+    hb = synth.f32_to_bf16(synth.hidden_inputs(16, seed=116))
+    y, idx, w, ht = run_block(cuda_dev, table, blk, hb)
+    check(host, hb, y, idx, w, gpu_logits(cuda_dev, dblk, ht), [0, 7, 15], 1e-4)
 
 
 @pytest.mark.parametrize("T", [20, 300])
