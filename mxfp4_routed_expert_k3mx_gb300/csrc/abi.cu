@@ -1,6 +1,7 @@
 // abi.cu - the extern "C" entry points of libk3mx.so: argument checks,
 // workspace layout and kernel launches.  No entry point allocates device
 // memory; scratch lives in the caller's workspace.
+#include <initializer_list>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -239,12 +240,15 @@ k3mx_status run_moe(const Ctx &c, float *y, const void *x, int x_dtype, int n_to
     bool pieces_done = false;
     if (n_tokens * kK <= 1024) {
         // one CTA per token, the decode path's x pieces in the same launch;
-        // grouping as a programmatic dependent
+        // grouping as a programmatic dependent.  Every block of the routing
+        // kernel waits for the kernel before it first thing, so it too is
+        // launched as a programmatic dependent (of whatever came before).
         const bool one = n_tokens == 1 && g.units != nullptr;
         err = traced("route", c.stream, [&] {
             return launch_route_prep(c, idx, w, logits, bias, n_tokens, decode ? x : nullptr, x_bf16, ximg,
                                      one ? &g : nullptr, reinterpret_cast<int *>(sk), mx_streamk_flag_count(),
-                                     decode ? experts : nullptr, decode ? at<uint8_t>(ws, L.maps) : nullptr, top_p);
+                                     decode ? experts : nullptr, decode ? at<uint8_t>(ws, L.maps) : nullptr, top_p,
+                                     true);
         });
         if (err == cudaSuccess && !one)
             err = traced("group_small", c.stream, [&] { return launch_group_small(c, idx, n_tokens, g); });
@@ -496,66 +500,81 @@ k3mx_status k3mx_latent_moe(float *y, const void *hidden, int h_dtype, int n_tok
     float *logits = at<float>(workspace, L.logits), *ylat = at<float>(workspace, L.ylat);
     float *gu = at<float>(workspace, L.gu), *ysh = at<float>(workspace, L.ysh);
     void *xlat = at<void>(workspace, L.xlat);
-    auto gemv = [&](float *out, int ldy, int col0, const float *add, const void *x, int x_bf16, int ldx,
-                    const uint16_t *W0, const uint16_t *W1, int r_split, int rows, int K, int xf) {
+    // a CUDA-core product over up to four weight matrices sharing one input
+    auto gemv = [&](std::initializer_list<GemvSeg> segs, const void *x, int x_bf16, int ldx, int K, int xf,
+                    const int *rows) {
         GemvArgs a{};
-        a.y = out;
-        a.ldy = ldy;
-        a.col0 = col0;
-        a.add = add;
+        int r = 0, k = 0;
+        for (const GemvSeg &sg : segs) {
+            a.seg[k] = sg;
+            a.seg[k].r0 = r;
+            r += rows[k++];
+        }
+        a.n_seg = k;
+        a.rows = r;
         a.x = x;
         a.x_bf16 = x_bf16;
         a.ldx = ldx;
         a.g = blk->g_norm;
-        a.W0 = W0;
-        a.W1 = W1;
-        a.r_split = r_split;
-        a.rows = rows;
         a.n_tokens = T;
         a.status = c.status;
         return launch_dense_gemv(c, K, xf, a);
     };
     const uint16_t *hb = static_cast<const uint16_t *>(hidden);
-    // 1. the router's logits
-    cudaError_t err = traced("router", c.stream,
-                             [&] { return launch_router_logits(c, logits, hidden, h_bf16, blk->router_w, T); });
-    // 2. the latent: x = W_dn h (7168 -> 3584)
-    if (err == cudaSuccess)
-        err = traced("latent_down", c.stream, [&] {
-            return L.batched ? launch_dense_gemm(c, kHid, blk->w_dn, kD, hb, T, nullptr, static_cast<uint16_t *>(xlat),
-                                                 kD, 0, nullptr)
-                             : gemv(static_cast<float *>(xlat), kD, 0, nullptr, hidden, h_bf16, kHid, blk->w_dn,
-                                    blk->w_dn, kD, kD, kHid, kXfPlain);
+    cudaError_t err = cudaSuccess;
+    if (!L.batched) {
+        // 1. every product over the hidden state in one launch: the router's
+        // logits, the latent x = W_dn h (7168 -> 3584) and the fused shared
+        // experts' g | u
+        const int rows[4] = {kE, kD, kFs, kFs};
+        err = traced("hidden_products", c.stream, [&] {
+            return gemv({GemvSeg{blk->router_w, logits, nullptr, kE, 0},
+                         GemvSeg{blk->w_dn, static_cast<float *>(xlat), nullptr, kD, 0},
+                         GemvSeg{blk->w1s, gu, nullptr, 2 * kFs, 0}, GemvSeg{blk->w3s, gu + kFs, nullptr, 2 * kFs, 0}},
+                        hidden, h_bf16, kHid, kHid, kXfPlain, rows);
         });
+    } else {
+        // 1. the router's logits, the latent x = W_dn h (7168 -> 3584) in bf16
+        err = traced("router", c.stream,
+                     [&] { return launch_router_logits(c, logits, hidden, h_bf16, blk->router_w, T); });
+        if (err == cudaSuccess)
+            err = traced("latent_down", c.stream, [&] {
+                return launch_dense_gemm(c, kHid, blk->w_dn, kD, hb, T, nullptr, static_cast<uint16_t *>(xlat), kD,
+                                         0, nullptr);
+            });
+    }
     if (err != cudaSuccess) return from_cuda(err);
-    // 3. the routed experts on the latent: route, group, experts, weighted sum
+    // 2. the routed experts on the latent: route, group, experts, weighted sum
     st = run_moe(c, ylat, xlat, L.batched ? K3MX_BF16 : K3MX_F32, T, experts, logits, blk->bias,
                  L.moe_path, idx_out, w_out, at<void>(workspace, L.moe), L.moe_l, (double)top_p);
     if (st != K3MX_OK) return st;
-    // 4. the fused shared experts' g | u on the hidden state
-    err = traced("shared_gate_up", c.stream, [&] {
-        if (!L.batched)
-            return gemv(gu, 2 * kFs, 0, nullptr, hidden, h_bf16, kHid, blk->w1s, blk->w3s, kFs, 2 * kFs, kHid,
-                        kXfPlain);
-        cudaError_t e = launch_dense_gemm(c, kHid, blk->w1s, kFs, hb, T, gu, nullptr, 2 * kFs, 0, nullptr);
-        if (e == cudaSuccess) e = launch_dense_gemm(c, kHid, blk->w3s, kFs, hb, T, gu, nullptr, 2 * kFs, kFs, nullptr);
-        return e;
-    });
-    // 5. their down projection of SiTU-GLU(g, u)
+    // 3. the fused shared experts' g | u on the hidden state (tensor cores)
+    if (L.batched)
+        err = traced("shared_gate_up", c.stream, [&] {
+            cudaError_t e = launch_dense_gemm(c, kHid, blk->w1s, kFs, hb, T, gu, nullptr, 2 * kFs, 0, nullptr);
+            if (e == cudaSuccess)
+                e = launch_dense_gemm(c, kHid, blk->w3s, kFs, hb, T, gu, nullptr, 2 * kFs, kFs, nullptr);
+            return e;
+        });
+    // 4. their down projection of SiTU-GLU(g, u)
     if (err == cudaSuccess)
         err = traced("shared_down", c.stream, [&] {
-            if (!L.batched)
-                return gemv(ysh, kHid, 0, nullptr, gu, 0, 2 * kFs, blk->w2s, blk->w2s, kHid, kHid, kFs, kXfSitu);
+            if (!L.batched) {
+                const int rows[1] = {kHid};
+                return gemv({GemvSeg{blk->w2s, ysh, nullptr, kHid, 0}}, gu, 0, 2 * kFs, kFs, kXfSitu, rows);
+            }
             uint16_t *act = at<uint16_t>(workspace, L.act);
             cudaError_t e = launch_situ_bf16(c, gu, kFs, T, act);
             if (e == cudaSuccess) e = launch_dense_gemm(c, kFs, blk->w2s, kHid, act, T, ysh, nullptr, kHid, 0, nullptr);
             return e;
         });
-    // 6. y = W_up RMSNorm(routed sum) + shared (3584 -> 7168)
+    // 5. y = W_up RMSNorm(routed sum) + shared (3584 -> 7168)
     if (err == cudaSuccess)
         err = traced("latent_up", c.stream, [&] {
-            if (!L.batched)
-                return gemv(y, kHid, 0, ysh, ylat, 0, kD, blk->w_up, blk->w_up, kHid, kHid, kD, kXfRmsNorm);
+            if (!L.batched) {
+                const int rows[1] = {kHid};
+                return gemv({GemvSeg{blk->w_up, y, ysh, kHid, 0}}, ylat, 0, kD, kD, kXfRmsNorm, rows);
+            }
             uint16_t *z = at<uint16_t>(workspace, L.z);
             cudaError_t e = launch_rmsnorm_bf16(c, ylat, blk->g_norm, kD, T, z);
             if (e == cudaSuccess) e = launch_dense_gemm(c, kD, blk->w_up, kHid, z, T, y, nullptr, kHid, 0, ysh);

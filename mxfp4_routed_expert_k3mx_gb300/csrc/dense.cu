@@ -73,6 +73,32 @@ __device__ __forceinline__ float4 input4(const GemvArgs &a, int t, int c4, float
     return v;
 }
 
+// The weight row of product row gr (the segments are in row order, the
+// first at row 0)
+template <int K>
+__device__ __forceinline__ const uint16_t *row_weights(const GemvArgs &a, int gr) {
+    const uint16_t *w = a.seg[0].W + (size_t)gr * K;
+#pragma unroll
+    for (int k = 1; k < kGemvMaxSeg; k++)
+        if (k < a.n_seg && gr >= a.seg[k].r0) w = a.seg[k].W + (size_t)(gr - a.seg[k].r0) * K;
+    return w;
+}
+
+// Where product row gr of input t goes, and its addend (or null)
+__device__ __forceinline__ float *row_out(const GemvArgs &a, int gr, int t, const float *&add) {
+    size_t o = (size_t)t * a.seg[0].ldy + gr;
+    float *y = a.seg[0].y + o;
+    add = a.seg[0].add != nullptr ? a.seg[0].add + o : nullptr;
+#pragma unroll
+    for (int k = 1; k < kGemvMaxSeg; k++)
+        if (k < a.n_seg && gr >= a.seg[k].r0) {
+            o = (size_t)t * a.seg[k].ldy + (gr - a.seg[k].r0);
+            y = a.seg[k].y + o;
+            add = a.seg[k].add != nullptr ? a.seg[k].add + o : nullptr;
+        }
+    return y;
+}
+
 // Persistent, one CTA per SM over a contiguous range of weight rows.  The
 // inputs (3 at a time) are staged in shared memory first, laid out so that
 // lanes read consecutive 16-byte words (columns 8v..8v+3 at slot v,
@@ -101,10 +127,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gemv(const GemvArgs a) {
     const int G = gridDim.x, b = blockIdx.x;
     const int rb = (int)((long long)a.rows * b / G), nr = (int)((long long)a.rows * (b + 1) / G) - rb;
     const int prefilled = min(nr, SLOTS);         // rows whose copies go out before anything else
-    auto row_src = [&](int i) {
-        const int gr = rb + i;
-        return gr < a.r_split ? a.W0 + (size_t)gr * K : a.W1 + (size_t)(gr - a.r_split) * K;
-    };
+    auto row_src = [&](int i) { return row_weights<K>(a, rb + i); };
     if (threadIdx.x == 0) {
         for (int i = 0; i < SLOTS; i++) {
             mbar_init(full0 + 8 * i, 1);
@@ -231,9 +254,10 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gemv(const GemvArgs a) {
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
                 if (lane == 0 && j < nt && ok) {
-                    const size_t o = (size_t)(t0 + j) * a.ldy + a.col0 + rb + i;
-                    if (a.add != nullptr) sum += a.add[o];
-                    a.y[o] = sum;
+                    const float *ad;
+                    float *o = row_out(a, rb + i, t0 + j, ad);
+                    if (ad != nullptr) sum += *ad;
+                    *o = sum;
                 }
             }
         }
@@ -536,15 +560,12 @@ cudaError_t launch_router_logits(const Ctx &c, float *logits, const void *h, int
         return launch_dense_gemm(c, kH, W, kE, static_cast<const uint16_t *>(h), n_tokens, logits, nullptr, kE, 0,
                                  nullptr);
     GemvArgs a{};
-    a.y = logits;
-    a.ldy = kE;
+    a.seg[0] = GemvSeg{W, logits, nullptr, kE, 0};
+    a.n_seg = 1;
+    a.rows = kE;
     a.x = h;
     a.x_bf16 = h_bf16;
     a.ldx = kH;
-    a.W0 = W;
-    a.W1 = W;
-    a.r_split = kE;
-    a.rows = kE;
     a.n_tokens = n_tokens;
     a.status = c.status;
     return launch_dense_gemv(c, kH, kXfPlain, a);

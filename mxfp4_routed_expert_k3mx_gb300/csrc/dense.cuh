@@ -9,16 +9,23 @@ constexpr int kXfSitu = 1;       // SiTU-GLU(g, u) of an fp32 [g | u] row pair (
 constexpr int kXfRmsNorm = 2;    // RMSNorm (eps 1e-5) of an fp32 row times a bf16 weight
 constexpr int kDenseGemmMinTokens = 17;   // bf16 inputs from here on: the tensor cores
 
-// y[t * ldy + col0 + r] = sum_c W[r][c] xin[t][c] (+ add at the same place)
-struct GemvArgs {
+// One weight matrix of a CUDA-core product: rows [r0, next segment's r0)
+// of the product are the rows of W, written y[t * ldy + (r - r0)] (+ add at
+// the same place).  Several matrices over the same input run in one launch.
+constexpr int kGemvMaxSeg = 4;
+struct GemvSeg {
+    const uint16_t *W;           // weight rows [rows][K]
     float *y;
-    int ldy, col0;
     const float *add;            // or null
+    int ldy, r0;
+};
+
+struct GemvArgs {
+    GemvSeg seg[kGemvMaxSeg];
+    int n_seg, rows;             // segments in row order, their rows in all
     const void *x;               // input rows [T][ldx]
     int x_bf16, ldx;
     const uint16_t *g;           // RMSNorm weight [K] (kXfRmsNorm)
-    const uint16_t *W0, *W1;     // weight rows [0, r_split) of W0, the rest of W1
-    int r_split, rows;
     int n_tokens;
     int *status;
 };

@@ -417,11 +417,14 @@ __device__ void scatter_warp(const int32_t *idx, int p_begin, int p_end, int *ru
 //
 // For a few tokens the warp-per-token router leaves the GPU idle, so each
 // token gets a 256-thread CTA: thread t holds experts t, t+256, t+512,
-// t+768.  (1) fp32 estimates of the 896 keys; (2) a two-pass radix select
-// (8 bits per pass, shared-memory histograms) finds the 16-bit prefix of
-// the 16th largest estimate a16, whose lowest value stands in for a16 in
-// the candidate bound; (3) candidates within 2^-18 * max(1,|v|) below that
-// value v (the bound of route_warp, applied to a value no larger than a16);
+// t+768.  (1) fp32 estimates of the 896 keys; (2) the experts fall into 64
+// groups (group g: the experts of threads g, g+64, g+128, g+192), and v,
+// the 16th largest of the 64 group maxima, stands in for a16, the 16th
+// largest estimate: 16 distinct experts (the maxima of 16 groups) have
+// estimates >= v, so v <= a16, and v = a16 unless two of the top 16 share
+// a group; (3) candidates within 2^-18 * max(1,|v|) below v (the bound of
+// route_warp; the bound grows with v, so it keeps every expert that the
+// bound at a16 keeps);
 // (4) exact double scores for the candidates, each candidate's rank among
 // them by (key, lower index); (5) warp 0 forms the slot-order sum of the 16
 // winners' scores and the weights.  Every phase is a few dozen
@@ -431,9 +434,7 @@ constexpr int kRT = 256;                 // threads per routing CTA
 constexpr int kRS = 4;                   // expert slots per thread
 
 struct RouteSmem {
-    int hist[256];
-    uint32_t prefix;                     // selected bin of the pass
-    int above;                           // estimates in higher bins
+    uint32_t tmax[kRT];                  // each thread's largest key
     uint32_t tau;
     int n;
     int cand[64];
@@ -442,38 +443,6 @@ struct RouteSmem {
     int sel_e[kK];
     float sel_s[kK];
 };
-
-// Warp 0, after a histogram pass: the bin (scanning from the top) that
-// holds the `need`-th largest value, and how many values lie in the bins
-// above it; clears the histogram for the next pass.
-__device__ __forceinline__ void radix_pick(RouteSmem &sm, int need) {
-    const int lane = threadIdx.x & 31;
-    int c[8], tot = 0;
-#pragma unroll
-    for (int i = 0; i < 8; i++) {
-        c[i] = sm.hist[255 - 8 * lane - i];      // lane 0 holds the top bins
-        sm.hist[255 - 8 * lane - i] = 0;
-        tot += c[i];
-    }
-    int incl = tot;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-    }
-    int before = incl - tot;                       // values in the bins of lower lanes
-    if (before < need && incl >= need) {
-#pragma unroll 1
-        for (int i = 0; i < 8; i++) {
-            if (before + c[i] >= need) {
-                sm.prefix = (uint32_t)(255 - 8 * lane - i);
-                sm.above = before;
-                break;
-            }
-            before += c[i];
-        }
-    }
-}
 
 __device__ void route_cta(const float *__restrict__ lt, const float *__restrict__ bias,
                           int32_t *__restrict__ idx_t, float *__restrict__ w_t, RouteSmem &sm, double top_p) {
@@ -485,35 +454,39 @@ __device__ void route_cta(const float *__restrict__ lt, const float *__restrict_
         lv[j] = e < kE ? __ldg(lt + e) : 0.f;
         bv[j] = e < kE ? __ldg(bias + e) : 0.f;
     }
-    sm.hist[tid] = 0;
     if (tid == 0) sm.n = 0;
-    uint32_t ok[kRS];
+    uint32_t ok[kRS], mx = 0;
 #pragma unroll
-    for (int j = 0; j < kRS; j++)
+    for (int j = 0; j < kRS; j++) {
         ok[j] = tid + kRT * j < kE ? order_key(canon_key(approx_score(lv[j]) + bv[j])) : 0u;
-    __syncthreads();
-    // pass 1: the top 8 bits of the order keys
-#pragma unroll
-    for (int j = 0; j < kRS; j++)
-        if (tid + kRT * j < kE) atomicAdd(&sm.hist[ok[j] >> 24], 1);
-    __syncthreads();
-    if (warp == 0) radix_pick(sm, kK);
-    __syncthreads();
-    const uint32_t p1 = sm.prefix;
-    const int need = kK - sm.above;
-    // pass 2: the next 8 bits of the keys in that bin
-#pragma unroll
-    for (int j = 0; j < kRS; j++)
-        if (tid + kRT * j < kE && (ok[j] >> 24) == p1) atomicAdd(&sm.hist[(ok[j] >> 16) & 255u], 1);
+        mx = max(mx, ok[j]);
+    }
+    sm.tmax[tid] = mx;
     __syncthreads();
     if (warp == 0) {
-        radix_pick(sm, need);
-        __syncwarp();
+        // groups lane and lane + 32, then the 16th largest of the 64 maxima
+        // (equal maxima count once each)
+        uint32_t g0 = 0, g1 = 0;
+#pragma unroll
+        for (int q = 0; q < kRT / 64; q++) {
+            g0 = max(g0, sm.tmax[lane + 64 * q]);
+            g1 = max(g1, sm.tmax[lane + 32 + 64 * q]);
+        }
+        uint32_t m16 = 0;
+#pragma unroll 1
+        for (int k = 0; k < kK; k++) {
+            const uint32_t best = max(g0, g1);
+            m16 = __reduce_max_sync(0xffffffffu, best);
+            const int owner = __ffs(__ballot_sync(0xffffffffu, best == m16)) - 1;
+            if (lane == owner) {
+                if (g0 == m16) g0 = 0;
+                else g1 = 0;
+            }
+        }
         if (lane == 0) {
-            // the lowest value with a16's 16-bit prefix; a non-finite one
-            // (infinite keys) keeps every expert: exact path
-            const float lo = key_of_order((p1 << 24) | (sm.prefix << 16));
-            sm.tau = isfinite(lo) ? order_key(lo - 0x1p-18f * fmaxf(1.0f, fabsf(lo))) : 0u;
+            // a non-finite v (infinite keys) keeps every expert: exact path
+            const float v = key_of_order(m16);
+            sm.tau = isfinite(v) ? order_key(v - 0x1p-18f * fmaxf(1.0f, fabsf(v))) : 0u;
         }
     }
     __syncthreads();
