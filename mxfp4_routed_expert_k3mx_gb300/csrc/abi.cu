@@ -308,6 +308,7 @@ k3mx_status run_moe(const Ctx &c, float *y, const void *x, int x_dtype, int n_to
 // ------------------------------------------------ the LatentMoE block --
 
 constexpr int kHid = 7168, kFs = 6144;           // hidden width, fused shared experts' inter width
+static_assert(kLatentOutK1 == kD && kLatentOutK == kD + kFs, "the output product's two parts");
 
 struct LatentLayout {
     size_t logits, xlat, ylat, gu, ysh, act, z, moe, total;
@@ -556,13 +557,31 @@ k3mx_status k3mx_latent_moe(float *y, const void *hidden, int h_dtype, int n_tok
                 e = launch_dense_gemm(c, kHid, blk->w3s, kFs, hb, T, gu, nullptr, 2 * kFs, kFs, nullptr);
             return e;
         });
-    // 4. their down projection of SiTU-GLU(g, u)
+    if (!L.batched) {
+        // 4. y = W_up (RMSNorm(routed sum) * g_norm) + W2s SiTU-GLU(g, u) as
+        // one product over the two inputs side by side (3584 -> 7168 and
+        // the shared experts' 6144 -> 7168)
+        if (err == cudaSuccess)
+            err = traced("latent_out", c.stream, [&] {
+                GemvArgs a{};
+                a.seg[0] = GemvSeg{blk->w_up, y, nullptr, kHid, 0};
+                a.n_seg = 1;
+                a.rows = kHid;
+                a.x = ylat;
+                a.ldx = kD;
+                a.g = blk->g_norm;
+                a.x2 = gu;
+                a.ldx2 = 2 * kFs;
+                a.Wt = blk->w2s;
+                a.n_tokens = T;
+                a.status = c.status;
+                return launch_dense_gemv(c, kLatentOutK, kXfLatentOut, a);
+            });
+        return from_cuda(err);
+    }
+    // 4. the shared experts' down projection of SiTU-GLU(g, u)
     if (err == cudaSuccess)
         err = traced("shared_down", c.stream, [&] {
-            if (!L.batched) {
-                const int rows[1] = {kHid};
-                return gemv({GemvSeg{blk->w2s, ysh, nullptr, kHid, 0}}, gu, 0, 2 * kFs, kFs, kXfSitu, rows);
-            }
             uint16_t *act = at<uint16_t>(workspace, L.act);
             cudaError_t e = launch_situ_bf16(c, gu, kFs, T, act);
             if (e == cudaSuccess) e = launch_dense_gemm(c, kFs, blk->w2s, kHid, act, T, ysh, nullptr, kHid, 0, nullptr);
@@ -571,10 +590,6 @@ k3mx_status k3mx_latent_moe(float *y, const void *hidden, int h_dtype, int n_tok
     // 5. y = W_up RMSNorm(routed sum) + shared (3584 -> 7168)
     if (err == cudaSuccess)
         err = traced("latent_up", c.stream, [&] {
-            if (!L.batched) {
-                const int rows[1] = {kHid};
-                return gemv({GemvSeg{blk->w_up, y, ysh, kHid, 0}}, ylat, 0, kD, kD, kXfRmsNorm, rows);
-            }
             uint16_t *z = at<uint16_t>(workspace, L.z);
             cudaError_t e = launch_rmsnorm_bf16(c, ylat, blk->g_norm, kD, T, z);
             if (e == cudaSuccess) e = launch_dense_gemm(c, kD, blk->w_up, kHid, z, T, y, nullptr, kHid, 0, ysh);

@@ -4,8 +4,9 @@
 // 7168 -> 3584 into the experts' latent and 3584 -> 7168 back, and the two
 // fused full-width shared experts, inter 6144; the trunk is bf16):
 //   y[t][col0 + r] = sum_c W[r][c] xin[t][c]  (+ add[t][col0 + r])
-// with xin the input as given, SiTU-GLU of a (g | u) pair of rows, or the
-// RMSNorm of the input times its weight.  Every product of a bf16 weight
+// with xin the input as given, SiTU-GLU of a (g | u) pair of rows, the
+// RMSNorm of the input times its weight, or (the block's output product)
+// both side by side against W_up's and W2s's rows side by side.  Every product of a bf16 weight
 // and an fp32 value is exact in fp32; the sums are fp32.
 //
 // Few tokens, or fp32 inputs: k_gemv, persistent CTAs streaming their rows
@@ -52,6 +53,13 @@ __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v 
 // four consecutive input values c4*4 .. c4*4+3 of token row `t`
 template <int K, int XF>
 __device__ __forceinline__ float4 input4(const GemvArgs &a, int t, int c4, float scale) {
+    if (XF == kXfLatentOut && c4 >= kLatentOutK1 / 4) {
+        constexpr int K2 = K - kLatentOutK1;
+        const float *row = a.x2 + (size_t)t * a.ldx2;
+        const float4 g = reinterpret_cast<const float4 *>(row)[c4 - kLatentOutK1 / 4];
+        const float4 u = reinterpret_cast<const float4 *>(row + K2)[c4 - kLatentOutK1 / 4];
+        return make_float4(situ_glu(g.x, u.x), situ_glu(g.y, u.y), situ_glu(g.z, u.z), situ_glu(g.w, u.w));
+    }
     if (XF == kXfSitu) {
         const float *row = static_cast<const float *>(a.x) + (size_t)t * a.ldx;
         const float4 g = reinterpret_cast<const float4 *>(row)[c4];
@@ -65,7 +73,7 @@ __device__ __forceinline__ float4 input4(const GemvArgs &a, int t, int c4, float
     } else {
         v = reinterpret_cast<const float4 *>(static_cast<const float *>(a.x) + (size_t)t * a.ldx)[c4];
     }
-    if (XF == kXfRmsNorm) {
+    if (XF == kXfRmsNorm || XF == kXfLatentOut) {
         const uint2 q = reinterpret_cast<const uint2 *>(a.g)[c4];
         v = make_float4(v.x * scale * bf16_lo(q.x), v.y * scale * bf16_hi(q.x), v.z * scale * bf16_lo(q.y),
                         v.w * scale * bf16_hi(q.y));
@@ -119,6 +127,12 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gemv(const GemvArgs a) {
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t full0 = smem_addr(smem), empty0 = full0 + 8 * kGemvMaxSlots;
     float *red = reinterpret_cast<float *>(smem + 16 * kGemvMaxSlots);   // [kGemvTok][kGemvWarps + 1]
+    // the row each ring slot holds, set by the producer before the row's
+    // copies: a consumer waits for its row's number first, so that its
+    // parity wait is never two phases ahead of the slot (the consumer
+    // warps take rows round robin, and the ring may hold fewer slots than
+    // there are consumers)
+    volatile int *seq = reinterpret_cast<volatile int *>(smem + 512);
     float4 *hs = reinterpret_cast<float4 *>(smem + Sh::HDR);             // [chunk][2 VEC]
     const int stage_b = chunk * K * 4;
     const uint32_t ring = smem_addr(smem) + Sh::HDR + stage_b;
@@ -127,7 +141,19 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gemv(const GemvArgs a) {
     const int G = gridDim.x, b = blockIdx.x;
     const int rb = (int)((long long)a.rows * b / G), nr = (int)((long long)a.rows * (b + 1) / G) - rb;
     const int prefilled = min(nr, SLOTS);         // rows whose copies go out before anything else
-    auto row_src = [&](int i) { return row_weights<K>(a, rb + i); };
+    // a row's copies into ring slot `dst`: one bulk copy, or the two parts
+    // of an output-product row
+    auto issue_row = [&](int i, uint32_t dst, uint32_t bar, uint64_t pol) {
+        mbar_arrive_expect_tx(bar, Sh::ROWB);
+        if (XF == kXfLatentOut) {
+            constexpr int K2 = K - kLatentOutK1;
+            const size_t gr = (size_t)(rb + i);
+            bulk_g2s(dst, a.seg[0].W + gr * kLatentOutK1, kLatentOutK1 * 2, bar, pol);
+            bulk_g2s(dst + kLatentOutK1 * 2, a.Wt + gr * K2, K2 * 2, bar, pol);
+        } else {
+            bulk_g2s(dst, row_weights<K>(a, rb + i), Sh::ROWB, bar, pol);
+        }
+    };
     if (threadIdx.x == 0) {
         for (int i = 0; i < SLOTS; i++) {
             mbar_init(full0 + 8 * i, 1);
@@ -137,9 +163,10 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gemv(const GemvArgs a) {
         // the weights are the call's own: the ring fills while the kernel
         // before finishes and the inputs are staged
         const uint64_t pol = l2_evict_first_policy();
+        for (int i = prefilled; i < kGemvMaxSlots; i++) seq[i] = -1;
         for (int i = 0; i < prefilled; i++) {
-            mbar_arrive_expect_tx(full0 + 8 * i, Sh::ROWB);
-            bulk_g2s(ring + i * Sh::ROWB, row_src(i), Sh::ROWB, full0 + 8 * i, pol);
+            seq[i] = i;
+            issue_row(i, ring + i * Sh::ROWB, full0 + 8 * i, pol);
         }
     }
     // the kernel behind may start its prologue
@@ -150,11 +177,13 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gemv(const GemvArgs a) {
         const int nt = min(chunk, a.n_tokens - t0);
         __syncthreads();                          // barriers set up; the previous chunk is consumed
         float scale[kGemvTok] = {1.f, 1.f, 1.f};
-        if (XF == kXfRmsNorm) {
+        // the normalised part's length
+        constexpr int KN = XF == kXfLatentOut ? kLatentOutK1 : K;
+        if (XF == kXfRmsNorm || XF == kXfLatentOut) {
             for (int j = 0; j < nt; j++) {
                 const float *row = static_cast<const float *>(a.x) + (size_t)(t0 + j) * a.ldx;
                 float ss = 0.f;
-                for (int c4 = threadIdx.x; c4 < K / 4; c4 += blockDim.x) {
+                for (int c4 = threadIdx.x; c4 < KN / 4; c4 += blockDim.x) {
                     const float4 v = reinterpret_cast<const float4 *>(row)[c4];
                     ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
                 }
@@ -166,7 +195,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gemv(const GemvArgs a) {
             for (int j = 0; j < nt; j++) {
                 float ss = 0.f;
                 for (int w = 0; w < NW; w++) ss += red[j * NW + w];
-                scale[j] = 1.0f / sqrtf(ss / (float)K + kRmsEps);
+                scale[j] = 1.0f / sqrtf(ss / (float)KN + kRmsEps);
             }
         }
         // 8 loads in flight per thread before the stores
@@ -202,8 +231,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gemv(const GemvArgs a) {
                         report_status(a.status, kStatusWaitTimeout, 311);
                         break;
                     }
-                    mbar_arrive_expect_tx(full0 + 8 * s, Sh::ROWB);
-                    bulk_g2s(ring + s * Sh::ROWB, row_src(i), Sh::ROWB, full0 + 8 * s, pol);
+                    seq[s] = g;
+                    issue_row(i, ring + s * Sh::ROWB, full0 + 8 * s, pol);
                 }
             }
             continue;
@@ -211,7 +240,13 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gemv(const GemvArgs a) {
         // ------------------------------------------------------ consumers --
         for (int i = warp; i < nr; i += kGemvWarps) {
             const int g = gbase + i, s = g % SLOTS;
-            const bool ok = mbar_wait(full0 + 8 * s, (g / SLOTS) & 1);
+            bool ok = true;
+            for (uint32_t n = 0; seq[s] != g; n++)
+                if (n >= kWaitLimit) {
+                    ok = false;
+                    break;
+                }
+            ok = ok && mbar_wait(full0 + 8 * s, (g / SLOTS) & 1);
             if (!ok && lane == 0) report_status(a.status, kStatusWaitTimeout, 310);
             const uint4 *wr = reinterpret_cast<const uint4 *>(smem + Sh::HDR + stage_b + s * Sh::ROWB);
             // four independent running sums per input (vectors i mod 4),
@@ -524,6 +559,10 @@ cudaError_t launch_dense_gemv(const Ctx &c, int K, int xf, const GemvArgs &a) {
     if (K == 7168 && xf == kXfPlain) return gemv_t<7168, kXfPlain>(c, a);
     if (K == 6144 && xf == kXfSitu) return gemv_t<6144, kXfSitu>(c, a);
     if (K == 3584 && xf == kXfRmsNorm) return gemv_t<3584, kXfRmsNorm>(c, a);
+    if (K == kLatentOutK && xf == kXfLatentOut) {
+        if (a.n_seg != 1 || a.x_bf16 || a.Wt == nullptr || a.x2 == nullptr) return cudaErrorInvalidValue;
+        return gemv_t<kLatentOutK, kXfLatentOut>(c, a);
+    }
     return cudaErrorInvalidValue;
 }
 

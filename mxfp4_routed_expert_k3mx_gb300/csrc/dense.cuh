@@ -7,6 +7,11 @@ namespace k3mx {
 constexpr int kXfPlain = 0;      // the input as given (fp32 or bf16)
 constexpr int kXfSitu = 1;       // SiTU-GLU(g, u) of an fp32 [g | u] row pair (u at +K)
 constexpr int kXfRmsNorm = 2;    // RMSNorm (eps 1e-5) of an fp32 row times a bf16 weight
+// [RMSNorm(x) * g | SiTU-GLU(x2)]: the block's output product, W_up's
+// 3584 columns and W2s's 6144 side by side (K = 9728), each row's two
+// parts copied from the two matrices
+constexpr int kXfLatentOut = 3;
+constexpr int kLatentOutK1 = 3584, kLatentOutK = 3584 + 6144;
 constexpr int kDenseGemmMinTokens = 17;   // bf16 inputs from here on: the tensor cores
 
 // One weight matrix of a CUDA-core product: rows [r0, next segment's r0)
@@ -25,12 +30,15 @@ struct GemvArgs {
     int n_seg, rows;             // segments in row order, their rows in all
     const void *x;               // input rows [T][ldx]
     int x_bf16, ldx;
-    const uint16_t *g;           // RMSNorm weight [K] (kXfRmsNorm)
+    const uint16_t *g;           // RMSNorm weight (kXfRmsNorm, kXfLatentOut)
+    const float *x2;             // kXfLatentOut: the g | u rows [T][ldx2] of the SiTU-GLU part
+    int ldx2;
+    const uint16_t *Wt;          // kXfLatentOut: the rows' second parts [rows][K - kLatentOutK1]
     int n_tokens;
     int *status;
 };
 
-// CUDA cores, any token count; K in {7168, 6144, 3584}
+// CUDA cores, any token count; K in {7168, 6144, 3584, 9728 (kXfLatentOut)}
 cudaError_t launch_dense_gemv(const Ctx &c, int K, int xf, const GemvArgs &a);
 
 // tcgen05 tensor cores: x bf16 [T][K] (row stride K), W bf16 [rows][K],
