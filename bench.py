@@ -51,7 +51,7 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
 # kernels per traced launch group
-KERNELS_PER_GROUP = {"router": 1, "hidden_products": 1, "latent_out": 1, "latent_down": 1, "shared_gate_up": 2, "shared_down": 2, "latent_up": 2,
+KERNELS_PER_GROUP = {"router": 1, "hidden_products": 1, "latent_out": 1, "latent_down": 1, "shared_gate_up": 1, "shared_down": 2, "latent_up": 2,
                      "route": 1, "group_small": 1, "group": 3, "mx_pieces": 1,
                      "decode_expert": 1, "decode_gate_up": 1, "decode_down": 1, "combine": 1,
                      "prefill_prep": 3, "prefill_gate_up": 1, "prefill_down": 1}

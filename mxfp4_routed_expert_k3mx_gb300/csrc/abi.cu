@@ -552,10 +552,7 @@ k3mx_status k3mx_latent_moe(float *y, const void *hidden, int h_dtype, int n_tok
     // 3. the fused shared experts' g | u on the hidden state (tensor cores)
     if (L.batched)
         err = traced("shared_gate_up", c.stream, [&] {
-            cudaError_t e = launch_dense_gemm(c, kHid, blk->w1s, kFs, hb, T, gu, nullptr, 2 * kFs, 0, nullptr);
-            if (e == cudaSuccess)
-                e = launch_dense_gemm(c, kHid, blk->w3s, kFs, hb, T, gu, nullptr, 2 * kFs, kFs, nullptr);
-            return e;
+            return launch_dense_gemm2(c, kHid, blk->w1s, blk->w3s, kFs, hb, T, gu, 2 * kFs, 0, kFs);
         });
     if (!L.batched) {
         // 4. y = W_up (RMSNorm(routed sum) * g_norm) + W2s SiTU-GLU(g, u) as

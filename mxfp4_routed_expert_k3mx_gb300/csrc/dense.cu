@@ -320,6 +320,10 @@ struct GemmOut {
     const float *add;
     int n_tokens;
     int *status;
+    // rows from m_split on come from the second weight map and go to
+    // columns col1 + (row - m_split) (two matrices over one input in a
+    // launch; m_split = all rows for one matrix)
+    int m_split, col1;
 };
 
 // bf16 A and B, f32 accumulator, both K-major, M x N
@@ -343,7 +347,8 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
 
 template <int K, bool ADD>
 __global__ void __launch_bounds__(kGThreads, 1)
-    k_gemm(const GemmOut o, const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap) {
+    k_gemm(const GemmOut o, const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap wmap2,
+           const __grid_constant__ CUtensorMap xmap) {
     constexpr int KSTEPS = K / kGK;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -351,7 +356,11 @@ __global__ void __launch_bounds__(kGThreads, 1)
     const uint32_t st0 = smem_addr(smem) + 1024;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t full0 = smem_addr(hd->full), empty0 = smem_addr(hd->empty), accf = smem_addr(&hd->accf);
-    const int m0 = blockIdx.x * kGM, n0 = blockIdx.y * kGN;
+    // token tiles vary fastest: the CTAs that share a weight tile run
+    // together, and the input (at most 58.7 MB at 4096 tokens) stays in L2
+    const int m0 = blockIdx.y * kGM, n0 = blockIdx.x * kGN;
+    const bool second = m0 >= o.m_split;          // a tile of the second matrix
+    const int ma = second ? m0 - o.m_split : m0;  // its first row there
     if (tid == 0) {
         for (int i = 0; i < kGStages; i++) {
             mbar_init(full0 + 8 * i, 1);
@@ -369,6 +378,14 @@ __global__ void __launch_bounds__(kGThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------ TMA producer --
         if (lane == 0) {
+            const CUtensorMap *wm = second ? &wmap2 : &wmap;
+            // the weights are the call's own: the first stages' weight
+            // tiles go out before the wait for the inputs
+            const int pre = KSTEPS < kGStages ? KSTEPS : kGStages;
+            for (int k = 0; k < pre; k++) {
+                mbar_arrive_expect_tx(full0 + 8 * k, kGStage);
+                tma_2d_plain(st0 + k * kGStage, wm, k * kGK, ma, full0 + 8 * k);
+            }
             pdl_wait();                               // the inputs, if a kernel before writes them
             for (int k = 0; k < KSTEPS; k++) {
                 const int s = k % kGStages;
@@ -377,8 +394,10 @@ __global__ void __launch_bounds__(kGThreads, 1)
                     break;
                 }
                 const uint32_t dst = st0 + s * kGStage;
-                mbar_arrive_expect_tx(full0 + 8 * s, kGStage);
-                tma_2d_plain(dst, &wmap, k * kGK, m0, full0 + 8 * s);
+                if (k >= pre) {
+                    mbar_arrive_expect_tx(full0 + 8 * s, kGStage);
+                    tma_2d_plain(dst, wm, k * kGK, ma, full0 + 8 * s);
+                }
                 tma_2d_plain(dst + kGABytes, &xmap, k * kGK, n0, full0 + 8 * s);
             }
         }
@@ -405,7 +424,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     } else {
         // --------------------------------------------------- epilogue --
         const int q = warp & 3;                       // TMEM lane quarter of this warp
-        const int r = m0 + 32 * q + lane;             // weight row = TMEM lane
+        const int r = (second ? o.col1 : o.col0) + ma + 32 * q + lane;   // output column of this TMEM lane
         if (mbar_wait(accf, 0)) {
             tc_fence_after();
             const uint32_t base = tmem + ((uint32_t)(32 * q) << 16);
@@ -417,7 +436,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 16; j++) {
                     const int t = n0 + c0 + j;
-                    ad[j] = ADD && t < o.n_tokens ? __ldg(o.add + (size_t)t * o.ldy + o.col0 + r) : 0.f;
+                    ad[j] = ADD && t < o.n_tokens ? __ldg(o.add + (size_t)t * o.ldy + r) : 0.f;
                 }
                 uint32_t v[16];
                 tmem_ld16(base + c0, v);
@@ -426,7 +445,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 for (int j = 0; j < 16; j++) {
                     const int t = n0 + c0 + j;
                     if (t < o.n_tokens) {
-                        const size_t at = (size_t)t * o.ldy + o.col0 + r;
+                        const size_t at = (size_t)t * o.ldy + r;
                         const float val = ADD ? __uint_as_float(v[j]) + ad[j] : __uint_as_float(v[j]);
                         if (o.y_bf16 != nullptr) o.y_bf16[at] = f32_to_bf16_rn(val);
                         else o.y[at] = val;
@@ -541,16 +560,21 @@ cudaError_t gemv_t(const Ctx &c, const GemvArgs &a) {
     return launch_pdl(k_gemv<K, XF>, dim3(grid), dim3(kGemvThreads), (size_t)GemvShape<K>::smem(chunk), c.stream, a);
 }
 
+// rows of W, then (o.m_split < rows) rows - o.m_split rows of W2
 template <int K, bool ADD>
-cudaError_t gemm_t(const Ctx &c, const uint16_t *W, int rows, const uint16_t *x, const GemmOut &o) {
+cudaError_t gemm_t(const Ctx &c, const uint16_t *W, const uint16_t *W2, int rows, const uint16_t *x,
+                   const GemmOut &o) {
     static bool done = false;
     const cudaError_t e = configure_once(k_gemm<K, ADD>, kGSmem, done);
     if (e != cudaSuccess) return e;
-    CUtensorMap wm, xm;
-    if (!encode_bf16_rows(wm, W, K, (uint64_t)rows, kGM) || !encode_bf16_rows(xm, x, K, (uint64_t)o.n_tokens, kGN))
+    CUtensorMap wm, wm2, xm;
+    const int rows2 = rows - o.m_split;
+    if (!encode_bf16_rows(wm, W, K, (uint64_t)o.m_split, kGM) ||
+        !encode_bf16_rows(wm2, rows2 > 0 ? W2 : W, K, (uint64_t)(rows2 > 0 ? rows2 : o.m_split), kGM) ||
+        !encode_bf16_rows(xm, x, K, (uint64_t)o.n_tokens, kGN))
         return cudaErrorInvalidValue;
-    const dim3 grid(rows / kGM, (o.n_tokens + kGN - 1) / kGN);
-    return launch_pdl(k_gemm<K, ADD>, grid, dim3(kGThreads), (size_t)kGSmem, c.stream, o, wm, xm);
+    const dim3 grid((o.n_tokens + kGN - 1) / kGN, rows / kGM);
+    return launch_pdl(k_gemm<K, ADD>, grid, dim3(kGThreads), (size_t)kGSmem, c.stream, o, wm, wm2, xm);
 }
 
 }  // namespace
@@ -569,15 +593,22 @@ cudaError_t launch_dense_gemv(const Ctx &c, int K, int xf, const GemvArgs &a) {
 cudaError_t launch_dense_gemm(const Ctx &c, int K, const uint16_t *W, int rows, const uint16_t *x, int n_tokens,
                               float *y, uint16_t *y_bf16, int ldy, int col0, const float *add) {
     if (rows % kGM != 0 || n_tokens < 1) return cudaErrorInvalidValue;
-    const GemmOut o{y, y_bf16, ldy, col0, add, n_tokens, c.status};
+    const GemmOut o{y, y_bf16, ldy, col0, add, n_tokens, c.status, rows, 0};
     if (add != nullptr) {
-        if (K == 3584) return gemm_t<3584, true>(c, W, rows, x, o);
+        if (K == 3584) return gemm_t<3584, true>(c, W, W, rows, x, o);
         return cudaErrorInvalidValue;
     }
-    if (K == 7168) return gemm_t<7168, false>(c, W, rows, x, o);
-    if (K == 6144) return gemm_t<6144, false>(c, W, rows, x, o);
-    if (K == 3584) return gemm_t<3584, false>(c, W, rows, x, o);
+    if (K == 7168) return gemm_t<7168, false>(c, W, W, rows, x, o);
+    if (K == 6144) return gemm_t<6144, false>(c, W, W, rows, x, o);
+    if (K == 3584) return gemm_t<3584, false>(c, W, W, rows, x, o);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_dense_gemm2(const Ctx &c, int K, const uint16_t *W1, const uint16_t *W2, int rows, const uint16_t *x,
+                               int n_tokens, float *y, int ldy, int col1, int col2) {
+    if (rows % kGM != 0 || n_tokens < 1 || K != 7168) return cudaErrorInvalidValue;
+    const GemmOut o{y, nullptr, ldy, col1, nullptr, n_tokens, c.status, rows, col2};
+    return gemm_t<7168, false>(c, W1, W2, 2 * rows, x, o);
 }
 
 cudaError_t launch_situ_bf16(const Ctx &c, const float *gu, int F, int n_tokens, uint16_t *out) {

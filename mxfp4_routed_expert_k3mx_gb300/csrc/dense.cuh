@@ -47,6 +47,11 @@ cudaError_t launch_dense_gemv(const Ctx &c, int K, int xf, const GemvArgs &a);
 cudaError_t launch_dense_gemm(const Ctx &c, int K, const uint16_t *W, int rows, const uint16_t *x, int n_tokens,
                               float *y, uint16_t *y_bf16, int ldy, int col0, const float *add);
 
+// two matrices W1, W2 [rows][K] (K = 7168, rows a multiple of 128) over one
+// bf16 input in one launch: y[t * ldy + col1 + r] = W1 x, y[t * ldy + col2 +
+// r] = W2 x (fp32)
+cudaError_t launch_dense_gemm2(const Ctx &c, int K, const uint16_t *W1, const uint16_t *W2, int rows, const uint16_t *x,
+                               int n_tokens, float *y, int ldy, int col1, int col2);
 // SiTU-GLU of fp32 [T][2F] (g | u) rows into bf16 [T][F]
 cudaError_t launch_situ_bf16(const Ctx &c, const float *gu, int F, int n_tokens, uint16_t *out);
 // RMSNorm (eps 1e-5) of fp32 [T][D] rows times a bf16 weight, into bf16
