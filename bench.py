@@ -338,6 +338,208 @@ def time_e2e(k3mx, wl, table, dev, steps, warmup, flush):
     return ms, h2d, d2h
 
 
+GEMV_ROWS, GEMV_IN = 3072, 3584
+GEMV_W_BYTES = GEMV_ROWS * GEMV_IN // 2 + GEMV_ROWS * GEMV_IN // 32      # 5,849,088
+GEMV_BYTES = GEMV_W_BYTES + GEMV_IN * 4 + GEMV_ROWS * 4                  # + x + y: 5,875,712
+
+
+def graph_of(k3mx, dev, calls):
+    """A CUDA graph of the given library calls (each a no-argument function
+    issuing its launches on the current stream)."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            for c in calls:
+                c()
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize(dev)
+    return g
+
+
+def time_graph(g, dev, reps, warmup):
+    import torch
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize(dev)
+    ms = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    return ms
+
+
+def time_gemv(k3mx, dev, flush, steps, warmup, hbm_peak, cpu_budget_s):
+    """The single MXFP4 GEMV, W [3072 x 3584] (scales U{120..130}, 1% set to
+    255), x fp32 N(0,1): 64 calls over 64 distinct copies of W (374 MB, 2.9x
+    L2) in one CUDA graph, replayed; GB/s = 64 x 5,875,712 B / graph time.
+    Also one call alone after an L2 flush (latency), the kernel's own
+    duration from the launch trace, and the oracle on the host cores."""
+    import numpy as np
+    import torch
+    import synth
+    p, s, x = synth.gemv_inputs(seed=0)
+    n_copies = 64
+    P = torch.from_numpy(p).to(dev)
+    S = torch.from_numpy(s).to(dev)
+    Ps = [P.clone() for _ in range(n_copies)]
+    Ss = [S.clone() for _ in range(n_copies)]
+    xd = torch.from_numpy(x).to(dev)
+    ys = torch.empty((n_copies, GEMV_ROWS), dtype=torch.float32, device=dev)
+    for i in range(n_copies):
+        k3mx.k3mx_gemv(ys[i], xd, Ps[i], Ss[i])
+    torch.cuda.synchronize(dev)
+    calls = [lambda i=i: k3mx.k3mx_gemv(ys[i], xd, Ps[i], Ss[i]) for i in range(n_copies)]
+    g = graph_of(k3mx, dev, calls)
+    ms = time_graph(g, dev, max(3, steps // 2), warmup)
+    per_call_ms = statistics.median(ms) / n_copies
+    gbs = GEMV_BYTES / (per_call_ms / 1e3) / 1e9
+    # one call after an L2 flush (write outside the events), and the trace
+    stream = torch.cuda.current_stream(dev)
+    lat = []
+    for i in range(max(5, steps // 2)):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        k3mx.k3mx_gemv(ys[i % n_copies], xd, Ps[i % n_copies], Ss[i % n_copies])
+        b.record(stream)
+        b.synchronize()
+        lat.append(a.elapsed_time(b))
+    k3mx.k3mx_trace_read()
+    k3mx.k3mx_trace_enable(True)
+    for i in range(n_copies):
+        k3mx.k3mx_gemv(ys[i], xd, Ps[i], Ss[i])
+    torch.cuda.synchronize(dev)
+    k3mx.k3mx_trace_enable(False)
+    tr = k3mx.k3mx_trace_read()
+    kus = 1e3 * tr["gemv"][1] / tr["gemv"][0] if "gemv" in tr else None
+    out = {"GB_s": round(gbs, 1), "hbm_frac": round(gbs / hbm_peak, 4),
+           "us_per_gemv": round(1e3 * per_call_ms, 3),
+           "timing": f"{n_copies} GEMVs over distinct weight copies ({n_copies * GEMV_W_BYTES / 1e6:.0f} MB) "
+                     "in one CUDA graph, median of replays",
+           "single_call_us_l2_flushed": round(1e3 * statistics.median(lat), 2),
+           "roofline": {"kernel": "gemv", "bound": "hbm", "unit": "GB/s", "peak": hbm_peak,
+                        "algorithmic_bytes_per_launch": GEMV_BYTES,
+                        "achieved": round(GEMV_BYTES / (kus / 1e6) / 1e9, 1) if kus else None,
+                        "frac": round(GEMV_BYTES / (kus / 1e6) / 1e9 / hbm_peak, 4) if kus else None,
+                        "kernel_us": round(kus, 3) if kus else None}}
+    # the oracle on the host cores: the same GEMV, repeated for ~1/4 of the budget
+    import oracle
+    oracle.gemv(x, p, s)
+    n, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < cpu_budget_s / 4 or n < 2:
+        oracle.gemv(x, p, s)
+        n += 1
+    secs = time.perf_counter() - t0
+    out["cpu_baseline"] = {"value": round(n * GEMV_W_BYTES / secs / 1e9, 3), "unit": "GB/s",
+                           "cores": oracle.num_threads(), "kind": "oracle",
+                           "sample": f"{n} GEMVs of the same 3072 x 3584 matrix"}
+    del Ps, Ss, g
+    torch.cuda.empty_cache()
+    return out
+
+
+def time_expert(k3mx, dev, arena, steps, warmup, hbm_peak, cpu_budget_s):
+    """One full routed expert at one token (k3mx_expert_ffn): 32 calls over
+    32 distinct experts of the arena (561 MB, 4.4x L2), x fp32 N(0,1), in
+    one CUDA graph, replayed; GB/s = 32 x 17,547,264 B / graph time.  Also
+    the fused kernel's own duration and the oracle on the host cores."""
+    import torch
+    import synth
+    n_exp = 32
+    offs = k3mx.expert_offsets()
+    exs = [k3mx.expert_struct(*[arena.data_ptr() + e * EXPERT_BYTES + o for o in offs]) for e in range(n_exp)]
+    xs = torch.from_numpy(synth.token_inputs(n_exp, seed=77)).to(dev)
+    ys = torch.empty((n_exp, D), dtype=torch.float32, device=dev)
+    ws = torch.empty(k3mx.k3mx_expert_ffn_workspace_size(), dtype=torch.uint8, device=dev)
+    for e in range(n_exp):
+        k3mx.k3mx_expert_ffn(ys[e], xs[e], exs[e], ws)
+    torch.cuda.synchronize(dev)
+    calls = [lambda e=e: k3mx.k3mx_expert_ffn(ys[e], xs[e], exs[e], ws) for e in range(n_exp)]
+    g = graph_of(k3mx, dev, calls)
+    ms = time_graph(g, dev, max(3, steps // 2), warmup)
+    per_call_ms = statistics.median(ms) / n_exp
+    gbs = EXPERT_BYTES / (per_call_ms / 1e3) / 1e9
+    k3mx.k3mx_trace_read()
+    k3mx.k3mx_trace_enable(True)
+    for e in range(n_exp):
+        k3mx.k3mx_expert_ffn(ys[e], xs[e], exs[e], ws)
+    torch.cuda.synchronize(dev)
+    k3mx.k3mx_trace_enable(False)
+    tr = k3mx.k3mx_trace_read()
+    # the fused kernel's bytes: the expert's weights, the x pieces, g and u
+    # written, h pieces written and read, y written
+    kbytes = EXPERT_BYTES + X_IMAGE_BYTES + 2 * F * 4 + 2 * H_IMAGE_BYTES + D * 4
+    kus = 1e3 * tr["decode_expert"][1] / tr["decode_expert"][0] if "decode_expert" in tr else None
+    out = {"GB_s": round(gbs, 1), "hbm_frac": round(gbs / hbm_peak, 4),
+           "us_per_expert": round(1e3 * per_call_ms, 3),
+           "timing": f"{n_exp} calls over distinct experts ({n_exp * EXPERT_BYTES / 1e6:.0f} MB) in one CUDA "
+                     "graph, median of replays",
+           "kernels": {k: {"launches": v[0], "avg_us": round(1e3 * v[1] / max(1, v[0]), 2)} for k, v in tr.items()},
+           "roofline": {"kernel": "decode_expert", "bound": "hbm", "unit": "GB/s", "peak": hbm_peak,
+                        "algorithmic_bytes_per_launch": kbytes,
+                        "achieved": round(kbytes / (kus / 1e6) / 1e9, 1) if kus else None,
+                        "frac": round(kbytes / (kus / 1e6) / 1e9 / hbm_peak, 4) if kus else None}}
+    import oracle
+    w = synth.split_expert(synth.expert(0, seed=0))
+    x0 = synth.token_inputs(1, seed=77)[0]
+    oracle.expert(x0, *w)
+    n, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < cpu_budget_s / 4 or n < 2:
+        oracle.expert(x0, *w)
+        n += 1
+    secs = time.perf_counter() - t0
+    out["cpu_baseline"] = {"value": round(n * EXPERT_BYTES / secs / 1e9, 3), "unit": "GB/s",
+                           "cores": oracle.num_threads(), "kind": "oracle",
+                           "sample": f"{n} evaluations of one expert at one token"}
+    del g
+    return out
+
+
+def oracle_batch_sample(T, budget_s, seed_base=1000, flops=False):
+    """The oracle on tokens of a batched workload (T tokens per step, flat
+    routing), token after token until ~budget_s: tokens/s, expert GB/s
+    (each selected expert's bytes once per token) and GFLOP/s (2 x 33,030,144
+    per token and expert)."""
+    import numpy as np
+    import oracle
+    import synth
+    x, logits, bias = decode_inputs(0, T, seed_base)
+    if T > 64:
+        x = synth.bf16_to_f32(synth.f32_to_bf16(x))
+    idx, w = oracle.route(logits, bias)
+    total_s, toks, pairs = 0.0, 0, 0
+    cache = {}
+    for t in range(T):
+        if total_s >= budget_s:
+            break
+        ids = [int(e) for e in idx[t]]
+        ex = {}
+        for e in ids:
+            if e not in cache:
+                if len(cache) > 64:
+                    cache.clear()
+                cache[e] = synth.split_expert(synth.expert(e, seed=0))
+            ex[e] = cache[e]
+        t0 = time.perf_counter()
+        oracle.moe(x[t:t + 1], idx[t:t + 1], w[t:t + 1], ex)
+        total_s += time.perf_counter() - t0
+        toks += 1
+        pairs += len(ids)
+    return {"tokens_per_s": round(toks / total_s, 3),
+            "GB_s": round(pairs * EXPERT_BYTES / total_s / 1e9, 3),
+            "GFLOP_s": round(2.0 * PARAMS_PER_EXPERT * pairs / total_s / 1e9, 2),
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{toks} of the {T} tokens of one step, token by token (16 experts each)"}
+
+
 def time_router(k3mx, dev, flush, steps, warmup, bf16_peak, hbm_peak):
     """The router (logits of the bf16 [896, 7168] router, then the top-16)
     at one fp32 decode token and at 4096 bf16 prefill tokens.  Its inputs fit
@@ -555,6 +757,12 @@ def run_ours(args):
         # secondary workloads: batch 64 decode (bf16 -> fp32)
         sec = {}
         if not args.primary_only:
+            cb = 0.0 if args.no_cpu_baseline else args.cpu_budget_s
+            sec["gemv_3072x3584"] = time_gemv(k3mx, dev, flush, args.steps, args.warmup, hbm_peak, cb)
+            sec["expert_ffn_1tok"] = time_expert(k3mx, dev, arena, args.steps, args.warmup, hbm_peak, cb)
+            if args.no_cpu_baseline:
+                for k in ("gemv_3072x3584", "expert_ffn_1tok"):
+                    sec[k].pop("cpu_baseline", None)
             wl = Workload("moe_decode_b64", 64, True, k3mx.K3MX_PATH_DECODE)
             r = time_workload(k3mx, wl, table, dev, max(3, args.steps // 2), args.warmup, None, None)
             ms = sum(r["ms"])
@@ -566,6 +774,8 @@ def run_ours(args):
                                      "hbm_frac": round(b / (ms / 1e3) / 1e9 / hbm_peak, 4),
                                      "kernels": {k: {"launches": v[0], "avg_us": round(1e3 * v[1] / max(1, v[0]), 2)}
                                                  for k, v in r["trace"].items()}}
+            if not args.no_cpu_baseline:
+                sec["moe_decode_b64"]["cpu_baseline"] = oracle_batch_sample(64, args.cpu_budget_s / 2)
             # prefill, 4096 bf16 tokens, flat routing: tcgen05 grouped GEMMs,
             # weights dequantised to f16 (PREFILL) or fed as stored to the
             # block-scaled MMAs with x and h as MXFP4 pieces (PREFILL_MX)
@@ -596,6 +806,8 @@ def run_ours(args):
                     "tensor_kernels": kern,
                     "kernels": {k: {"launches": v[0], "avg_us": round(1e3 * v[1] / max(1, v[0]), 2)}
                                 for k, v in tr.items()}}
+            if not args.no_cpu_baseline:
+                sec["moe_prefill_4096_mx"]["cpu_baseline"] = oracle_batch_sample(4096, args.cpu_budget_s / 2)
             sec.update(time_router(k3mx, dev, flush, max(5, args.steps // 2), args.warmup, bf16_peak, hbm_peak))
             sec.update(time_latent_block(k3mx, dev, table, max(3, args.steps // 4), args.warmup, bf16_peak, hbm_peak))
         line["secondary"] = sec

@@ -332,6 +332,20 @@ k3mx_status k3mx_moe_decode_noalloc(float *y, const void *x, int x_dtype,
 k3mx_status k3mx_device_status(k3mx_stream_t stream, int *detail);
 
 /*
+ * The limit of the library's bounded device-side waits, a diagnostic aid
+ * with no counterpart on the pages.  Every kernel's waits for work (on a
+ * pipeline barrier, or on a flag another CTA sets) give up after `polls`
+ * polls (each at most a few microseconds) and report K3MX_ETIMEOUT through
+ * k3mx_device_status; the CTA then waits for its own copies in flight and
+ * its MMAs with the default limit, frees its tensor memory and returns, so
+ * the context stays usable and the next call runs normally.  polls = 0
+ * restores the default (2^22 polls, seconds); larger values are clamped to
+ * it.  Applies to the current device, from the next launch on; outputs of a
+ * call whose wait gave up are unspecified.  Waits for the device.
+ */
+k3mx_status k3mx_set_wait_limit(unsigned int polls);
+
+/*
  * Launch tracing, a measurement aid with no counterpart on the pages.  While
  * enabled, every kernel launch group the library issues is bracketed by a
  * pair of CUDA events recorded on the caller's stream, so durations are

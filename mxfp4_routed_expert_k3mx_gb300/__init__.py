@@ -85,6 +85,7 @@ def lib():
             "k3mx_moe_routed_host": ([vp, vp, i, i, vp, vp, vp, i, vp, sz, vp], i),
             "k3mx_moe_decode_noalloc": ([vp, vp, i, i, vp, vp, vp, vp, vp, vp], i),
             "k3mx_device_status": ([vp, ctypes.POINTER(ctypes.c_int)], i),
+            "k3mx_set_wait_limit": ([ctypes.c_uint], i),
             "k3mx_status_str": ([i], ctypes.c_char_p),
             "k3mx_last_cuda_error": ([], ctypes.c_char_p),
             "k3mx_abi_version": ([], i),
@@ -137,10 +138,44 @@ def _elems(t):
     return t.numel()
 
 
+# Shape checks run before any device check or library call: the C ABI gets
+# raw pointers and sizes only, so a tensor smaller than the sizes passed
+# would let a kernel read or write past its end.
+
+def _tokens(x, width, name):
+    """Token count of a [T, width] activation tensor."""
+    if not isinstance(x, torch.Tensor) or x.dim() != 2 or x.shape[1] != width or x.shape[0] < 1:
+        shape = tuple(x.shape) if isinstance(x, torch.Tensor) else type(x).__name__
+        raise TypeError(f"{name}: shape [T, {width}] with T >= 1 expected, got {shape}")
+    return int(x.shape[0])
+
+
+def _numel(t, n, name, optional=False):
+    if t is None and optional:
+        return
+    if not isinstance(t, torch.Tensor) or t.numel() != n:
+        got = t.numel() if isinstance(t, torch.Tensor) else type(t).__name__
+        raise TypeError(f"{name}: {n} elements expected (shape), got {got}")
+
+
+def _table(experts, name="experts"):
+    if not isinstance(experts, torch.Tensor) or experts.dtype != torch.int64 or \
+            tuple(experts.shape) != (K3MX_N_EXPERTS, 6):
+        got = (tuple(experts.shape), experts.dtype) if isinstance(experts, torch.Tensor) else type(experts).__name__
+        raise TypeError(f"{name}: int64 table of shape [{K3MX_N_EXPERTS}, 6] expected, got {got}")
+
+
 # ------------------------------------------------------------------ calls --
 
 def k3mx_gemv(y, x, packed, scales, stream=None):
     """y[rows] = W x with W given as packed [rows, in/2] uint8 and scales [rows, in/32] uint8."""
+    if not isinstance(packed, torch.Tensor) or packed.dim() != 2:
+        raise TypeError("packed: shape [rows, in/2] expected")
+    rows, half = packed.shape
+    if not isinstance(scales, torch.Tensor) or tuple(scales.shape) != (rows, 2 * half // 32):
+        raise TypeError(f"scales: shape [{rows}, {2 * half // 32}] expected")
+    _numel(x, 2 * half, "x")
+    _numel(y, rows, "y")
     _dev(y, torch.float32, "y")
     _dev(x, torch.float32, "x")
     _dev(packed, torch.uint8, "packed")
@@ -162,6 +197,8 @@ def k3mx_expert_ffn_workspace_size():
 
 def k3mx_expert_ffn(y, x, expert, workspace, stream=None):
     """y = W2 SiTU(W1 x, W3 x) for one expert (an Expert struct) and one token."""
+    _numel(x, K3MX_LATENT, "x")
+    _numel(y, K3MX_LATENT, "y")
     _dev(y, torch.float32, "y")
     _dev(x, torch.float32, "x")
     _check("k3mx_expert_ffn", lib().k3mx_expert_ffn(
@@ -171,6 +208,10 @@ def k3mx_expert_ffn(y, x, expert, workspace, stream=None):
 
 
 def k3mx_route_topk(idx, w, logits, bias, stream=None):
+    T = _tokens(logits, K3MX_N_EXPERTS, "logits")
+    _numel(idx, T * K3MX_TOPK, "idx")
+    _numel(w, T * K3MX_TOPK, "w")
+    _numel(bias, K3MX_N_EXPERTS, "bias")
     _dev(idx, torch.int32, "idx")
     _dev(w, torch.float32, "w")
     _dev(logits, torch.float32, "logits")
@@ -184,6 +225,12 @@ def k3mx_route_topk(idx, w, logits, bias, stream=None):
 def k3mx_router(logits, idx, w, hidden, router_w, bias, top_p=0.0, stream=None):
     """Router logits from the hidden state (fp32 or bf16 [T, 7168]) and the
     bf16 router weights (int16 or uint16-viewed [896, 7168]), then the top-16."""
+    T = _tokens(hidden, 7168, "hidden")
+    _numel(logits, T * K3MX_N_EXPERTS, "logits")
+    _numel(idx, T * K3MX_TOPK, "idx")
+    _numel(w, T * K3MX_TOPK, "w")
+    _numel(bias, K3MX_N_EXPERTS, "bias")
+    _numel(router_w, K3MX_N_EXPERTS * 7168, "router_w")
     _dev(logits, torch.float32, "logits")
     _dev(idx, torch.int32, "idx")
     _dev(w, torch.float32, "w")
@@ -219,10 +266,14 @@ def k3mx_latent_moe(y, hidden, block, experts, workspace, top_p=0.0, idx_out=Non
     """The LatentMoE block: y [T, 7168] fp32 from hidden [T, 7168] (fp32 or
     bf16).  `block` is a LatentBlock (see latent_block), `experts` the
     device expert table."""
+    T = _tokens(hidden, 7168, "hidden")
+    _numel(y, T * 7168, "y")
+    _numel(idx_out, T * K3MX_TOPK, "idx_out", optional=True)
+    _numel(w_out, T * K3MX_TOPK, "w_out", optional=True)
+    _table(experts)
     _dev(y, torch.float32, "y")
     if not (hidden.is_cuda and hidden.is_contiguous()):
         raise ValueError("hidden: contiguous device tensor expected")
-    T = hidden.shape[0]
     _check("k3mx_latent_moe", lib().k3mx_latent_moe(
         _ptr(y), _ptr(hidden), _x_dtype(hidden), T, ctypes.byref(block), _ptr(experts), float(top_p),
         _ptr(idx_out), _ptr(w_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
@@ -232,6 +283,10 @@ def k3mx_latent_moe(y, hidden, block, experts, workspace, top_p=0.0, idx_out=Non
 
 def k3mx_route_topp(idx, w, logits, bias, top_p, stream=None):
     """k3mx_route_topk with the top-p truncation (dropped slots: -1, 0)."""
+    T = _tokens(logits, K3MX_N_EXPERTS, "logits")
+    _numel(idx, T * K3MX_TOPK, "idx")
+    _numel(w, T * K3MX_TOPK, "w")
+    _numel(bias, K3MX_N_EXPERTS, "bias")
     _dev(idx, torch.int32, "idx")
     _dev(w, torch.float32, "w")
     _dev(logits, torch.float32, "logits")
@@ -247,6 +302,10 @@ def k3mx_group_workspace_size(n_tokens):
 
 
 def k3mx_group(counts, offsets, perm, idx, workspace, stream=None):
+    T = _tokens(idx, K3MX_TOPK, "idx")
+    _numel(counts, K3MX_N_EXPERTS, "counts")
+    _numel(offsets, K3MX_N_EXPERTS + 1, "offsets")
+    _numel(perm, T * K3MX_TOPK, "perm")
     for t, n in ((counts, "counts"), (offsets, "offsets"), (perm, "perm"), (idx, "idx")):
         _dev(t, torch.int32, n)
     T = idx.shape[0]
@@ -272,15 +331,36 @@ def _x_dtype(x):
     raise TypeError("x must be float32 or bfloat16")
 
 
+def _moe_shapes(y, x, experts, logits, bias, idx_out, w_out):
+    """The routed layer's tensors against the token count of x [T, 3584]."""
+    T = _tokens(x, K3MX_LATENT, "x")
+    _numel(y, T * K3MX_LATENT, "y")
+    _numel(logits, T * K3MX_N_EXPERTS, "logits")
+    _numel(bias, K3MX_N_EXPERTS, "bias")
+    _numel(idx_out, T * K3MX_TOPK, "idx_out", optional=True)
+    _numel(w_out, T * K3MX_TOPK, "w_out", optional=True)
+    _table(experts)
+    return T
+
+
+def _dev_opt(t, dtype, name):
+    if t is not None:
+        _dev(t, dtype, name)
+
+
 def k3mx_moe_routed(y, x, experts, logits, bias, workspace, path=K3MX_PATH_AUTO,
                     idx_out=None, w_out=None, stream=None):
     """The routed-expert layer on device tensors.  experts: device int64 [896, 6]
     table of pointers (see expert_table)."""
+    _moe_shapes(y, x, experts, logits, bias, idx_out, w_out)
     _dev(y, torch.float32, "y")
     if not (x.is_cuda and x.is_contiguous()):
         raise TypeError("x: contiguous CUDA tensor expected")
     _dev(logits, torch.float32, "logits")
     _dev(bias, torch.float32, "bias")
+    _dev(experts, torch.int64, "experts")
+    _dev_opt(idx_out, torch.int32, "idx_out")
+    _dev_opt(w_out, torch.float32, "w_out")
     T = x.shape[0]
     _check("k3mx_moe_routed", lib().k3mx_moe_routed(
         _ptr(y), _ptr(x), _x_dtype(x), T, _ptr(experts), _ptr(logits), _ptr(bias), path,
@@ -293,11 +373,15 @@ def k3mx_moe_routed_topp(y, x, experts, logits, bias, workspace, top_p, path=K3M
                          idx_out=None, w_out=None, stream=None):
     """k3mx_moe_routed with top-p routing: the low-weight tail of each
     token's 16 experts is dropped and runs no expert."""
+    _moe_shapes(y, x, experts, logits, bias, idx_out, w_out)
     _dev(y, torch.float32, "y")
     if not (x.is_cuda and x.is_contiguous()):
         raise TypeError("x: contiguous CUDA tensor expected")
     _dev(logits, torch.float32, "logits")
     _dev(bias, torch.float32, "bias")
+    _dev(experts, torch.int64, "experts")
+    _dev_opt(idx_out, torch.int32, "idx_out")
+    _dev_opt(w_out, torch.float32, "w_out")
     T = x.shape[0]
     _check("k3mx_moe_routed_topp", lib().k3mx_moe_routed_topp(
         _ptr(y), _ptr(x), _x_dtype(x), T, _ptr(experts), _ptr(logits), _ptr(bias), path, float(top_p),
@@ -309,11 +393,15 @@ def k3mx_moe_routed_topp(y, x, experts, logits, bias, workspace, top_p, path=K3M
 def k3mx_moe_decode_noalloc(y, x, experts, logits, bias, idx_out=None, w_out=None, stream=None):
     """The decode path on device tensors with the library's fixed scratch
     instead of a workspace (at most K3MX_NOALLOC_MAX_TOKENS tokens)."""
+    _moe_shapes(y, x, experts, logits, bias, idx_out, w_out)
     _dev(y, torch.float32, "y")
     if not (x.is_cuda and x.is_contiguous()):
         raise TypeError("x: contiguous CUDA tensor expected")
     _dev(logits, torch.float32, "logits")
     _dev(bias, torch.float32, "bias")
+    _dev(experts, torch.int64, "experts")
+    _dev_opt(idx_out, torch.int32, "idx_out")
+    _dev_opt(w_out, torch.float32, "w_out")
     _check("k3mx_moe_decode_noalloc", lib().k3mx_moe_decode_noalloc(
         _ptr(y), _ptr(x), _x_dtype(x), x.shape[0], _ptr(experts), _ptr(logits), _ptr(bias),
         _ptr(idx_out), _ptr(w_out), _stream(stream)))
@@ -324,6 +412,7 @@ def k3mx_moe_routed_host(y_host, x_host, experts, logits_host, bias_host, worksp
                          path=K3MX_PATH_AUTO, stream=None):
     """The layer with host (CPU tensor) activations, logits, bias and output;
     weights and workspace on the device.  Returns after y_host is written."""
+    _moe_shapes(y_host, x_host, experts, logits_host, bias_host, None, None)
     for t, n in ((y_host, "y"), (x_host, "x"), (logits_host, "logits"), (bias_host, "bias")):
         if t.is_cuda or not t.is_contiguous():
             raise TypeError(f"{n}: contiguous host tensor expected")
@@ -340,6 +429,11 @@ def k3mx_device_status(stream=None):
     d = ctypes.c_int(0)
     st = lib().k3mx_device_status(_stream(stream), ctypes.byref(d))
     return st, d.value
+
+
+def k3mx_set_wait_limit(polls):
+    """Polls after which a device-side wait gives up (0: the default)."""
+    _check("k3mx_set_wait_limit", lib().k3mx_set_wait_limit(int(polls)))
 
 
 def k3mx_trace_enable(on):

@@ -769,6 +769,19 @@ int k3mx_trace_read(k3mx_trace_entry *out, int max_entries) {
     return n;
 }
 
+k3mx_status k3mx_set_wait_limit(unsigned int polls) {
+    Ctx c;
+    k3mx_status st = device_ctx(nullptr, c);
+    if (st != K3MX_OK) return st;
+    const uint32_t p = polls == 0 ? kWaitLimit : (polls > kWaitLimit ? kWaitLimit : polls);
+    for (cudaError_t (*set)(uint32_t) : {set_wait_polls_mx, set_wait_polls_px, set_wait_polls_prefill,
+                                         set_wait_polls_decode, set_wait_polls_dense}) {
+        const cudaError_t e = set(p);
+        if (e != cudaSuccess) return from_cuda(e);
+    }
+    return K3MX_OK;
+}
+
 k3mx_status k3mx_device_status(k3mx_stream_t stream, int *detail) {
     Ctx c;
     k3mx_status st = device_ctx(reinterpret_cast<cudaStream_t>(stream), c);

@@ -128,10 +128,23 @@ __device__ __forceinline__ void report_status(int *status, int code, int detail)
 // --------------------------------------------- async copies and barriers --
 //
 // Hand-written PTX for the bulk-copy engine (cp.async.bulk) and mbarriers.
-// Every wait is bounded: after kWaitLimit polls it gives up and the caller
-// reports kStatusWaitTimeout instead of spinning forever.
+// Every wait is bounded: after a number of polls it gives up and the caller
+// reports kStatusWaitTimeout instead of spinning forever.  Waits for work
+// take g_wait_polls polls (kWaitLimit unless k3mx_set_wait_limit changed it
+// on this device); the waits a CTA makes on its way out (its copies in
+// flight, its last MMAs before TMEM is freed) always take kWaitLimit, so a
+// short limit never frees TMEM under a running MMA or leaves a copy landing
+// in a finished CTA's shared memory.
 
 constexpr uint32_t kWaitLimit = 1u << 22;
+
+// One copy per translation unit (device code is not linked across files);
+// every copy is set by k3mx_set_wait_limit through set_wait_polls_here().
+static __device__ uint32_t g_wait_polls = kWaitLimit;
+__device__ __forceinline__ uint32_t wait_polls() { return __ldg(&g_wait_polls); }
+static inline cudaError_t set_wait_polls_here(uint32_t polls) {
+    return cudaMemcpyToSymbol(g_wait_polls, &polls, sizeof(polls));
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -170,11 +183,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// true when the phase of parity `parity` completed, false after kWaitLimit polls
+// true when the phase of parity `parity` completed, false after wait_polls()
+// polls (the limit is read only when the first poll fails)
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint32_t lim = wait_polls();
+    for (uint32_t i = 1; i < lim; i++)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+// the same with kWaitLimit polls: for the waits on a CTA's way out
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
     for (uint32_t i = 0; i < kWaitLimit; i++)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
+}
+
+// On a CTA's way out: wait until the last copy issued into each of the `n`
+// slots of a ring has landed.  Uses are counted from 0, use u goes to slot
+// u % n and completes one phase of that slot's barrier.  False if a wait
+// gave up.
+__device__ __forceinline__ bool drain_ring(uint32_t bar0, uint32_t n, uint32_t issued) {
+    bool ok = true;
+    for (uint32_t s = 0; s < n && s < issued; s++) {
+        const uint32_t last = s + n * ((issued - 1 - s) / n);
+        ok = mbar_wait_drain(bar0 + 8 * s, (last / n) & 1) && ok;
+    }
+    return ok;
 }
 
 // L2 policy for data read exactly once (weights): evict first
@@ -307,6 +342,14 @@ struct DecodeExperts {
 };
 cudaError_t launch_combine(const Ctx &c, float *y, const float *stage, const float *w,
                            int n_tokens);
+
+// The poll limit of the bounded waits in each kernel file, on the current
+// device (k3mx_set_wait_limit).
+cudaError_t set_wait_polls_mx(uint32_t polls);
+cudaError_t set_wait_polls_px(uint32_t polls);
+cudaError_t set_wait_polls_prefill(uint32_t polls);
+cudaError_t set_wait_polls_decode(uint32_t polls);
+cudaError_t set_wait_polls_dense(uint32_t polls);
 
 // The library's fixed device scratch array (abi.cu): its address on the
 // current device, looked up on first use, and its size.

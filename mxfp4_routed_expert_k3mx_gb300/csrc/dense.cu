@@ -133,6 +133,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gemv(const GemvArgs a) {
     // warps take rows round robin, and the ring may hold fewer slots than
     // there are consumers)
     volatile int *seq = reinterpret_cast<volatile int *>(smem + 512);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 640);   // a wait gave up
     float4 *hs = reinterpret_cast<float4 *>(smem + Sh::HDR);             // [chunk][2 VEC]
     const int stage_b = chunk * K * 4;
     const uint32_t ring = smem_addr(smem) + Sh::HDR + stage_b;
@@ -159,6 +160,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gemv(const GemvArgs a) {
             mbar_init(full0 + 8 * i, 1);
             mbar_init(empty0 + 8 * i, 1);
         }
+        *abort_flag = 0;
         fence_mbar_init();
         // the weights are the call's own: the ring fills while the kernel
         // before finishes and the inputs are staged
@@ -173,6 +175,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gemv(const GemvArgs a) {
     pdl_launch_dependents();
     pdl_wait();                                   // the inputs, if a kernel before writes them
     int gbase = 0;                                // rows this CTA streamed in earlier chunks
+    int g_next = prefilled;                       // producer: rows whose copies went out
     for (int t0 = 0; t0 < a.n_tokens; t0 += chunk, gbase += nr) {
         const int nt = min(chunk, a.n_tokens - t0);
         __syncthreads();                          // barriers set up; the previous chunk is consumed
@@ -225,29 +228,45 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gemv(const GemvArgs a) {
             // ---------------------------------------------------- producer --
             if (lane == 0) {
                 const uint64_t pol = l2_evict_first_policy();
-                for (int i = gbase == 0 ? prefilled : 0; i < nr; i++) {
+                for (int i = gbase == 0 ? prefilled : 0; i < nr && !*abort_flag; i++) {
                     const int g = gbase + i, s = g % SLOTS;
                     if (g >= SLOTS && !mbar_wait(empty0 + 8 * s, ((g / SLOTS) - 1) & 1)) {
                         report_status(a.status, kStatusWaitTimeout, 311);
+                        *abort_flag = 1;
                         break;
                     }
                     seq[s] = g;
                     issue_row(i, ring + s * Sh::ROWB, full0 + 8 * s, pol);
+                    g_next = g + 1;
                 }
             }
             continue;
         }
         // ------------------------------------------------------ consumers --
-        for (int i = warp; i < nr; i += kGemvWarps) {
+        for (int i = warp; i < nr && !*abort_flag; i += kGemvWarps) {
             const int g = gbase + i, s = g % SLOTS;
+            // the slot carries this row once the producer has claimed it for
+            // the row (polls back off like an mbarrier wait's suspend)
             bool ok = true;
-            for (uint32_t n = 0; seq[s] != g; n++)
-                if (n >= kWaitLimit) {
+            const uint32_t lim = wait_polls();
+            for (uint32_t n = 0; seq[s] != g; n++) {
+                if (n >= lim) {
                     ok = false;
                     break;
                 }
+                __nanosleep(256);
+            }
             ok = ok && mbar_wait(full0 + 8 * s, (g / SLOTS) & 1);
-            if (!ok && lane == 0) report_status(a.status, kStatusWaitTimeout, 310);
+            if (!ok) {
+                // give up on this row and the rest: reading the slot or
+                // arriving on its barrier would advance a phase that belongs
+                // to another row
+                if (lane == 0) {
+                    report_status(a.status, kStatusWaitTimeout, 310);
+                    *abort_flag = 1;
+                }
+                break;
+            }
             const uint4 *wr = reinterpret_cast<const uint4 *>(smem + Sh::HDR + stage_b + s * Sh::ROWB);
             // four independent running sums per input (vectors i mod 4),
             // each vector's 8 products as two 4-term chains
@@ -288,7 +307,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gemv(const GemvArgs a) {
                 float sum = (acc[j][0] + acc[j][1]) + (acc[j][2] + acc[j][3]);
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-                if (lane == 0 && j < nt && ok) {
+                if (lane == 0 && j < nt) {
                     const float *ad;
                     float *o = row_out(a, rb + i, t0 + j, ad);
                     if (ad != nullptr) sum += *ad;
@@ -297,6 +316,14 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gemv(const GemvArgs a) {
             }
         }
     }
+    // after a wait gave up, the ring's copies still in flight land before
+    // the CTA leaves (the last row issued into each slot)
+    __syncthreads();
+    if (warp == kGemvWarps && lane == 0 && *abort_flag)
+        for (int sl = 0; sl < SLOTS && sl < g_next; sl++) {
+            const int gl = sl + SLOTS * ((g_next - 1 - sl) / SLOTS);
+            mbar_wait_drain(full0 + 8 * sl, (gl / SLOTS) & 1);
+        }
 }
 
 // ----------------------------------------------------- tensor-core GEMM --
@@ -640,5 +667,7 @@ cudaError_t launch_router_logits(const Ctx &c, float *logits, const void *h, int
     a.status = c.status;
     return launch_dense_gemv(c, kH, kXfPlain, a);
 }
+
+cudaError_t set_wait_polls_dense(uint32_t polls) { return set_wait_polls_here(polls); }
 
 }  // namespace k3mx

@@ -22,8 +22,9 @@
 //               replaced on the device for each expert; bulk copies of the
 //               unit's piece images (B operand and its scales) once per unit
 //   warp 1      scale loader: the tile's 128 x 8 scale bytes per matrix into
-//               the 32-row scale-factor atoms tcgen05.cp reads (scale 255,
-//               "contributes nothing", becomes 0, i.e. 2^-127)
+//               the 32-row scale-factor atoms tcgen05.cp reads; a group of
+//               scale 255 ("contributes nothing") gets scale 0 and, once the
+//               tile has landed, its 32 codes are zeroed, so it adds exactly 0
 //   warp 2      TMEM owner; lane 0 copies the scale atoms to TMEM and issues
 //               four K=64 MMAs per matrix and chunk, M=128, N = 8 per token
 //   warps 3-6   epilogue (TMEM lane quarter = warp % 4): adds the pieces;
@@ -102,7 +103,9 @@ struct MxArgs {
 };
 
 struct Hdr {
-    uint64_t full[10], empty[10], accf[2], acce[2], bfull[2], bempty[2], sfull[2], done;
+    // full: the stage's scale atoms (32 scale-loader lanes); tfull: its weight
+    // tiles (the producer's expect_tx and the copies' bytes)
+    uint64_t full[10], tfull[10], empty[10], accf[2], acce[2], bfull[2], bempty[2], sfull[2], done;
     uint32_t tmem;
     int abort;
 };
@@ -180,6 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sraw0 = simg0 + BB * NTOK * Sh::TOKS;          // tile's scale rows [SBUF][NMAT][128][G]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t full0 = smem_addr(hd->full), empty0 = smem_addr(hd->empty);
+    const uint32_t tfull0 = smem_addr(hd->tfull);
     const uint32_t accf0 = smem_addr(hd->accf), acce0 = smem_addr(hd->acce);
     const uint32_t bfull0 = smem_addr(hd->bfull), bempty0 = smem_addr(hd->bempty);
     const uint32_t sfull0 = smem_addr(hd->sfull);
@@ -187,7 +191,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         for (int i = 0; i < S; i++) {
-            mbar_init(full0 + 8 * i, 1 + 32);      // producer's expect_tx + the scale loader's lanes
+            mbar_init(full0 + 8 * i, 32);          // the scale loader's lanes
+            mbar_init(tfull0 + 8 * i, 1);          // the producer's expect_tx
             mbar_init(empty0 + 8 * i, 1);
         }
         for (int i = 0; i < 2; i++) {
@@ -284,9 +289,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (lane == 0) {
                     const uint32_t dst = st0 + s * Sh::STAGE;
-                    mbar_arrive_expect_tx(full0 + 8 * s, NMAT * kTileBytes);
-                    tma_2d(dst, map0, c * 128, mt * 128, full0 + 8 * s, pol);
-                    if (NMAT == 2) tma_2d(dst + kTileBytes, map1, c * 128, mt * 128, full0 + 8 * s, pol);
+                    mbar_arrive_expect_tx(tfull0 + 8 * s, NMAT * kTileBytes);
+                    tma_2d(dst, map0, c * 128, mt * 128, tfull0 + 8 * s, pol);
+                    if (NMAT == 2) tma_2d(dst + kTileBytes, map1, c * 128, mt * 128, tfull0 + 8 * s, pol);
                 }
                 __syncwarp();
                 su++;
@@ -324,6 +329,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = p.lo + 1; c < p.hi && ok; c++) ok = issue_stage(c);
             if (!ok) break;
         }
+        // copies still in flight (after a wait gave up) land before the CTA leaves
+        if (lane == 0 && (!drain_ring(tfull0, S, su) || !drain_ring(bfull0, BB, bl)))
+            report_status(a.status, kStatusWaitTimeout, 13);
     } else if (warp == kSfWarp) {
         // -------------------------------------------------- scale loader --
         // A tile's scale rows (128 x G bytes per matrix, contiguous in
@@ -338,9 +346,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const size_t off = (size_t)(p.item % MT) * 128 * G;
             return (m == 0 ? (PH == 0 ? p.u.ex.s1 : p.u.ex.s2) : p.u.ex.s3) + off;
         };
+        uint32_t ni = 0;                   // parts whose scale rows were issued
         auto issue = [&](const Part &p, int buf) {
             // every lane's earlier reads of this buffer are done (their
             // values were stored) before the copy may overwrite it
+            ni++;
             __syncwarp();
             fence_async_smem();
             if (lane == 0) {
@@ -381,7 +391,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                         asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
                                      : "=r"(w[m][j].x), "=r"(w[m][j].y)
                                      : "r"(sraw + m * 128 * G + (lane + 32 * j) * G + c * 8));
-                const uint32_t at0 = st0 + s * Sh::STAGE + NMAT * kTileBytes;
+                const uint32_t stg = st0 + s * Sh::STAGE, at0 = stg + NMAT * kTileBytes;
+                // groups with scale 255 contribute nothing: once the stage's
+                // weight tiles landed, their codes are zeroed (rare; most
+                // stages skip this)
+                uint32_t nan = 0;
+#pragma unroll
+                for (int m = 0; m < NMAT; m++)
+#pragma unroll
+                    for (int j = 0; j < 4; j++) nan |= nan_scale_mask(w[m][j].x) | nan_scale_mask(w[m][j].y);
+                if (__any_sync(0xffffffffu, nan != 0)) {
+                    if (!mbar_wait(tfull0 + 8 * s, (su / S) & 1)) {
+                        if (lane == 0) fail(12);
+                        ok = false;
+                        break;
+                    }
+#pragma unroll
+                    for (int m = 0; m < NMAT; m++)
+#pragma unroll
+                        for (int j = 0; j < 4; j++) zero_nan_groups_sw128(stg + m * kTileBytes, lane + 32 * j, w[m][j]);
+                }
 #pragma unroll
                 for (int m = 0; m < NMAT; m++) {
                     sts128(at0 + (2 * m) * kAtomBytes + 16 * lane, drop_nan_scales(w[m][0].x),
@@ -399,6 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             cur = nxt;
             have = more;
         }
+        if (lane == 0 && !drain_ring(sfull0, SB, ni)) report_status(a.status, kStatusWaitTimeout, 14);
     } else if (warp == kMmaWarp) {
         // ----------------------------------------------------- MMA issuer --
         if (lane == 0) {
@@ -435,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 for (int c = p.lo; c < p.hi; c++, su++) {
                     const int s = su % S;
-                    if (!mbar_wait(full0 + 8 * s, (su / S) & 1)) {
+                    if (!mbar_wait(tfull0 + 8 * s, (su / S) & 1) || !mbar_wait(full0 + 8 * s, (su / S) & 1)) {
                         fail(6);
                         run = false;
                         break;
@@ -527,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == kMmaWarp) {
         // no MMA may still be running when TMEM is released
-        if (!mbar_wait(done, 0) && lane == 0) report_status(a.status, kStatusWaitTimeout, 8);
+        if (!mbar_wait_drain(done, 0) && lane == 0) report_status(a.status, kStatusWaitTimeout, 8);
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -591,12 +621,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
     const uint32_t sraw0 = breg + BREG;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t full0 = smem_addr(hd->full), empty0 = smem_addr(hd->empty);
+    const uint32_t tfull0 = smem_addr(hd->tfull);
     const uint32_t accf0 = smem_addr(hd->accf), acce0 = smem_addr(hd->acce);
     const uint32_t bfull0 = smem_addr(hd->bfull), bempty0 = smem_addr(hd->bempty);
     const uint32_t sfull0 = smem_addr(hd->sfull), done = smem_addr(&hd->done);
     if (tid == 0) {
         for (int i = 0; i < S; i++) {
-            mbar_init(full0 + 8 * i, 1 + 32);
+            mbar_init(full0 + 8 * i, 32);
+            mbar_init(tfull0 + 8 * i, 1);
             mbar_init(empty0 + 8 * i, 1);
         }
         for (int i = 0; i < 2; i++) {
@@ -807,13 +839,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
                 }
                 if (lane == 0) {
                     const uint32_t dst = st0 + s * STAGE;
-                    mbar_arrive_expect_tx(full0 + 8 * s, 2 * kTileBytes);
+                    const uint32_t tf = tfull0 + 8 * s;
+                    mbar_arrive_expect_tx(tf, 2 * kTileBytes);
                     if (p.ph == 0) {
-                        tma_2d(dst, map0, c * 128, p.mt * 128, full0 + 8 * s, pol);
-                        tma_2d(dst + kTileBytes, map1, c * 128, p.mt * 128, full0 + 8 * s, pol);
+                        tma_2d(dst, map0, c * 128, p.mt * 128, tf, pol);
+                        tma_2d(dst + kTileBytes, map1, c * 128, p.mt * 128, tf, pol);
                     } else {
-                        tma_2d(dst, map0, (2 * c) * 128, p.mt * 128, full0 + 8 * s, pol);
-                        tma_2d(dst + kTileBytes, map0, (2 * c + 1) * 128, p.mt * 128, full0 + 8 * s, pol);
+                        tma_2d(dst, map0, (2 * c) * 128, p.mt * 128, tf, pol);
+                        tma_2d(dst + kTileBytes, map0, (2 * c + 1) * 128, p.mt * 128, tf, pol);
                     }
                 }
                 __syncwarp();
@@ -872,7 +905,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
                     const int pair = (int)key;
                     const int *cnt = a.sync + SYNC_HDONE + (a.experts == nullptr ? 0 : pair % kK);
                     int f = 0;
-                    for (uint32_t i = 0; i < kWaitLimit && f < MTG; i++) {
+                    const uint32_t lim = wait_polls();
+                    for (uint32_t i = 0; i < lim && f < MTG; i++) {
                         asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(f) : "l"(cnt) : "memory");
                         if (f < MTG) __nanosleep(128);
                     }
@@ -898,6 +932,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
             for (int c = p.lo + pre; c < p.hi && ok; c++) ok = issue_stage(c);
             if (!ok) break;
         }
+        // copies still in flight (after a wait gave up) land before the CTA leaves
+        if (lane == 0 && (!drain_ring(tfull0, S, su) || !drain_ring(bfull0, 2, bl)))
+            report_status(a.status, kStatusWaitTimeout, 13);
     } else if (warp == kSfWarp) {
         // -------------------------------------------------- scale loader --
         // a part's tile scale rows in one bulk copy into one of two buffers
@@ -905,7 +942,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
         // per stage, the 4 atoms: gate/up W1 and W3 of the chunk, down the
         // two chunks of W2
         const uint64_t pol = l2_evict_first_policy();
+        uint32_t ni = 0;                   // parts whose scale rows were issued
         auto issue = [&](const Part &p, int buf) {
+            ni++;
             __syncwarp();
             fence_async_smem();
             if (lane == 0) {
@@ -956,7 +995,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
                                      : "=r"(wv[t][j].x), "=r"(wv[t][j].y)
                                      : "r"(base + (lane + 32 * j) * G));
                 }
-                const uint32_t at0 = st0 + s * STAGE + 2 * kTileBytes;
+                const uint32_t stg = st0 + s * STAGE, at0 = stg + 2 * kTileBytes;
+                // groups with scale 255 contribute nothing: once the stage's
+                // weight tiles landed, their codes are zeroed (rare)
+                uint32_t nan = 0;
+#pragma unroll
+                for (int t = 0; t < 2; t++)
+#pragma unroll
+                    for (int j = 0; j < 4; j++) nan |= nan_scale_mask(wv[t][j].x) | nan_scale_mask(wv[t][j].y);
+                if (__any_sync(0xffffffffu, nan != 0)) {
+                    if (!mbar_wait(tfull0 + 8 * s, (su / S) & 1)) {
+                        if (lane == 0) fail(12);
+                        ok = false;
+                        break;
+                    }
+#pragma unroll
+                    for (int t = 0; t < 2; t++)
+#pragma unroll
+                        for (int j = 0; j < 4; j++) zero_nan_groups_sw128(stg + t * kTileBytes, lane + 32 * j, wv[t][j]);
+                }
 #pragma unroll
                 for (int t = 0; t < 2; t++) {
                     sts128(at0 + (2 * t) * kAtomBytes + 16 * lane, drop_nan_scales(wv[t][0].x),
@@ -973,6 +1030,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
             cur = nxt;
             have = more;
         }
+        if (lane == 0 && !drain_ring(sfull0, 2, ni)) report_status(a.status, kStatusWaitTimeout, 14);
     } else if (warp == kMmaWarp) {
         // ----------------------------------------------------- MMA issuer --
         if (lane == 0) {
@@ -1007,7 +1065,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
                 tc_fence_after();
                 for (int c = p.lo; c < p.hi; c++, su++) {
                     const int s = su % S;
-                    if (!mbar_wait(full0 + 8 * s, (su / S) & 1)) {
+                    if (!mbar_wait(tfull0 + 8 * s, (su / S) & 1) || !mbar_wait(full0 + 8 * s, (su / S) & 1)) {
                         fail(6);
                         run = false;
                         break;
@@ -1092,7 +1150,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
                 // the head of an item the next CTA finishes: add its sums
                 const int *flag = a.sync + slot + 1;
                 int f = 0;
-                for (uint32_t i = 0; i < kWaitLimit && f == 0; i++) {
+                const uint32_t lim = wait_polls();
+                for (uint32_t i = 0; i < lim && f == 0; i++) {
                     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(f) : "l"(flag) : "memory");
                     if (f == 0) __nanosleep(64);
                 }
@@ -1148,7 +1207,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
 
     __syncthreads();
     if (warp == kMmaWarp) {
-        if (!mbar_wait(done, 0) && lane == 0) report_status(a.status, kStatusWaitTimeout, 8);
+        if (!mbar_wait_drain(done, 0) && lane == 0) report_status(a.status, kStatusWaitTimeout, 8);
         tc_fence_after();
         tmem_dealloc(tmem, f1::TMEM_COLS);
     }
@@ -1263,6 +1322,8 @@ cudaError_t launch_mx_fused1(const Ctx &c, const DecodeExperts &d, const uint8_t
     const int grid = c.num_sms < kMaxGrid ? c.num_sms : kMaxGrid;
     return launch_pdl(k_mx1, dim3(grid), dim3(kThreads), f1::SMEM, c.stream, a);
 }
+
+cudaError_t set_wait_polls_mx(uint32_t polls) { return set_wait_polls_here(polls); }
 
 size_t mx_ximg_bytes(int n_tokens) { return (size_t)n_tokens * img_bytes(kD); }
 size_t mx_himg_bytes(int n_pairs) { return (size_t)n_pairs * img_bytes(kF); }

@@ -9,13 +9,19 @@
 //   down:    Y = W2 H^T over K = 3072, y[t] += w_tk * Y (fp32 atomics)
 //
 // MXFP4 -> f16 in shared memory.  tcgen05 kind::f16 takes A and B of one
-// type; the weights are dequantised to f16 and the activations are f16 too
-// (x is converted once; it is bf16 N(0,1) and every such value is exact in
-// f16 down to 2^-24).  An e2m1 code is exact in f16 (cvt.rn.f16x2.e2m1x2);
+// type; the weights are dequantised to f16 and the activations are f16 too:
+// x is converted once, each token scaled by a power of two 2^-k_t that puts
+// its largest |x| in [2^13, 2^14), so no bf16 value overflows f16 and every
+// value within 2^-11 of the token's largest is exact (bf16 keeps 8
+// significant bits, f16 11); the gate/up epilogue multiplies g and u by
+// 2^k_t.  An e2m1 code is exact in f16 (cvt.rn.f16x2.e2m1x2);
 // its group scale 2^(s - 127) is split into a per-row reference 2^(sref-127),
 // sref the row's largest scale, applied to the fp32 accumulator in the
 // epilogue, and 2^(s - sref) <= 1 multiplied into the f16 value (exact while
-// s - sref >= -24; smaller groups, 2^24 below the row's largest, round).
+// s - sref >= -24; smaller groups, 2^24 below the row's largest, round).  In
+// a row whose scales span more than 24 binades, sref is the largest scale of
+// a group with a nonzero code (a group of zero codes adds nothing whatever
+// its scale, so it does not push the row's other groups out of range).
 //
 // Warp roles in a persistent CTA (one per SM):
 //   warps 0-7   dequant: global packed bytes -> registers (4 chunks ahead)
@@ -59,7 +65,8 @@ struct PArgs {
     const k3mx_expert *experts;
     const int32_t *units, *n_units, *perm;
     const float *w;            // routing weights by pair
-    const __half *xh;          // [T][D] f16 activations
+    const __half *xh;          // [T][D] f16 activations, token t scaled by 2^-xexp[t]
+    const int *xexp;           // [T]
     __half *H;                 // [16T][F] f16 h rows in grouped order
     float *y;                  // [T][D]
     int *status;
@@ -75,9 +82,26 @@ __device__ __forceinline__ __half2 pow2_h2(int k) {
     return *reinterpret_cast<__half2 *>(&b);
 }
 
-// the largest non-NaN scale byte of a scale row (127 when every group is NaN)
-__device__ __forceinline__ int row_sref(const uint8_t *srow, int ngroups) {
-    int mx = -1;
+// v * 2^e: one multiply when 2^e is a normal float, else ldexpf
+__device__ __forceinline__ float scale_pow2(float v, int e) {
+    return (e >= -126 && e <= 127) ? v * __int_as_float((e + 127) << 23) : ldexpf(v, e);
+}
+
+// spread of the f16 dequantisation below the row's reference scale
+constexpr int kRefSpan = 24;
+
+// a group of 16 packed bytes holds a nonzero code (codes 0 and 8 are +-0)
+__device__ __forceinline__ bool group_nonzero(const uint8_t *g16) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(g16));
+    return ((v.x | v.y | v.z | v.w) & 0x77777777u) != 0;
+}
+
+// The reference scale byte of a weight row (srow: its G scale bytes, prow:
+// its packed bytes): the largest non-NaN scale, or, when the non-NaN scales
+// span more than kRefSpan binades, the largest scale of a group with a
+// nonzero code; 127 when no group qualifies.  One thread.
+__device__ __forceinline__ int row_sref(const uint8_t *srow, const uint8_t *prow, int ngroups) {
+    int mx = -1, mn = 256;
     for (int i = 0; i < ngroups; i += 16) {
         const uint4 v = __ldg(reinterpret_cast<const uint4 *>(srow + i));
         const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
@@ -86,8 +110,18 @@ __device__ __forceinline__ int row_sref(const uint8_t *srow, int ngroups) {
 #pragma unroll
             for (int k = 0; k < 4; k++) {
                 const int b = (ws[q] >> (8 * k)) & 0xFF;
-                if (b != 255 && b > mx) mx = b;
+                if (b != 255) {
+                    mx = max(mx, b);
+                    mn = min(mn, b);
+                }
             }
+    }
+    if (mx - mn > kRefSpan) {
+        mx = -1;
+        for (int g = 0; g < ngroups; g++) {
+            const int b = srow[g];
+            if (b != 255 && b > mx && group_nonzero(prow + 16 * g)) mx = b;
+        }
     }
     return mx < 0 ? 127 : mx;
 }
@@ -176,9 +210,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_prefill(PArgs a) {
                 const int row = mt * kBM + rb + 64 * i;
                 rowp[i] = W + (size_t)row * ROWB + 16 * half;
                 srow[i] = Sc + (size_t)row * G;
-                // the row's largest non-NaN scale: the lane pair scans
+                // the row's reference scale (row_sref): the lane pair scans
                 // alternate 16-byte blocks of the row's G scale bytes
-                int mx = -1;
+                int mx = -1, mn = 256;
                 for (int blk = half; blk < G / 16; blk += 2) {
                     const uint4 v = __ldg(reinterpret_cast<const uint4 *>(srow[i] + 16 * blk));
                     const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
@@ -187,10 +221,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_prefill(PArgs a) {
 #pragma unroll
                         for (int k = 0; k < 4; k++) {
                             const int bb = (ws[q] >> (8 * k)) & 0xFF;
-                            if (bb != 255 && bb > mx) mx = bb;
+                            if (bb != 255) {
+                                mx = max(mx, bb);
+                                mn = min(mn, bb);
+                            }
                         }
                 }
                 mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
+                if (mx - mn > kRefSpan) {
+                    // a wide row (rare): the largest scale of a group with a
+                    // nonzero code, the pair taking alternate groups
+                    const unsigned pair = 3u << (lane & 30);
+                    int m2 = -1;
+                    const uint8_t *prow = W + (size_t)row * ROWB;
+                    for (int gq = half; gq < G; gq += 2) {
+                        const int b = srow[i][gq];
+                        if (b != 255 && b > m2 && group_nonzero(prow + 16 * gq)) m2 = b;
+                    }
+                    mx = max(m2, __shfl_xor_sync(pair, m2, 1));
+                }
                 sref[i] = mx < 0 ? 127 : mx;
             }
             // packed bytes and the group's scale byte, kPF chunks ahead
@@ -273,25 +323,37 @@ __global__ void __launch_bounds__(kThreads, 1) k_prefill(PArgs a) {
             const k3mx_expert ex = a.experts[e];
             const int row = mt * kBM + r;
             if (PH == kPhaseGateUp) {
-                const float f1 = ldexpf(1.f, row_sref(ex.s1 + (size_t)row * G, G) - 127);
-                const float f3 = ldexpf(1.f, row_sref(ex.s3 + (size_t)row * G, G) - 127);
+                const int e1 = row_sref(ex.s1 + (size_t)row * G, ex.w1 + (size_t)row * (K / 2), G) - 127;
+                const int e3 = row_sref(ex.s3 + (size_t)row * G, ex.w3 + (size_t)row * (K / 2), G) - 127;
                 const uint32_t tg = tmem + lane_base + (uint32_t)(ab * 256);
+                // the unit's token exponents k_t, lane l holding tokens l, l + 32, l + 64, l + 96
+                int ktv[kUnitTokens / 32];
+#pragma unroll
+                for (int qq = 0; qq < kUnitTokens / 32; qq++) {
+                    const int n = lane + 32 * qq;
+                    ktv[qq] = n < ntok ? __ldg(a.xexp + __ldg(a.perm + off + n) / kK) : 0;
+                }
                 for (int n0 = 0; n0 < npad; n0 += 16) {
                     uint32_t gv[16], uv[16];
                     tmem_ld16(tg + n0, gv);
                     tmem_ld16(tg + 128 + n0, uv);
                     tmem_ld_wait();
+                    const int qsel = n0 >> 5;
+                    const int kreg = qsel == 0 ? ktv[0] : qsel == 1 ? ktv[1] : qsel == 2 ? ktv[2] : ktv[3];
 #pragma unroll
                     for (int j = 0; j < 16; j++) {
                         const int n = n0 + j;
+                        const int kt = __shfl_sync(0xffffffffu, kreg, n & 31);
                         if (n < ntok) {
-                            const float h = situ_glu(__uint_as_float(gv[j]) * f1, __uint_as_float(uv[j]) * f3);
+                            // the row's reference scale and the token's 2^k_t, one rounding
+                            const float h = situ_glu(scale_pow2(__uint_as_float(gv[j]), e1 + kt),
+                                                     scale_pow2(__uint_as_float(uv[j]), e3 + kt));
                             a.H[(size_t)(off + n) * kF + row] = __float2half_rn(h);
                         }
                     }
                 }
             } else {
-                const float f2 = ldexpf(1.f, row_sref(ex.s2 + (size_t)row * G, G) - 127);
+                const float f2 = ldexpf(1.f, row_sref(ex.s2 + (size_t)row * G, ex.w2 + (size_t)row * (K / 2), G) - 127);
                 const uint32_t td = tmem + lane_base + (uint32_t)(ab * 128);
                 for (int n0 = 0; n0 < npad; n0 += 16) {
                     uint32_t dv[16];
@@ -388,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_prefill(PArgs a) {
             }
             // every MMA issued so far has completed before TMEM is released
             umma_commit(smem_addr(&hd->done));
-            if (!mbar_wait(smem_addr(&hd->done), 0)) report_status(a.status, kStatusWaitTimeout, 250 + PH);
+            if (!mbar_wait_drain(smem_addr(&hd->done), 0)) report_status(a.status, kStatusWaitTimeout, 250 + PH);
         }
         __syncwarp();
     }
@@ -401,18 +463,39 @@ __global__ void __launch_bounds__(kThreads, 1) k_prefill(PArgs a) {
     }
 }
 
-// x (bf16 bits) -> f16 activations; y = 0
-__global__ void k_prefill_prep(__half *xh, float *y, const uint16_t *x, size_t n) {
-    const size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
-    if (i + 3 < n) {
-        const uint2 v = *reinterpret_cast<const uint2 *>(x + i);
-        const float f0 = __uint_as_float(v.x << 16), f1 = __uint_as_float(v.x & 0xFFFF0000u);
-        const float f2 = __uint_as_float(v.y << 16), f3 = __uint_as_float(v.y & 0xFFFF0000u);
-        __half2 h01 = __floats2half2_rn(f0, f1), h23 = __floats2half2_rn(f2, f3);
-        *reinterpret_cast<uint2 *>(xh + i) =
-            make_uint2(*reinterpret_cast<uint32_t *>(&h01), *reinterpret_cast<uint32_t *>(&h23));
-        *reinterpret_cast<float4 *>(y + i) = make_float4(0.f, 0.f, 0.f, 0.f);
+// x (bf16 bits) -> f16 activations, token t scaled by 2^-k_t (k_t = the
+// exponent of its largest |x| minus 13; 0 for a token of zeros or one
+// holding Inf or NaN); y = 0.  One warp per token.
+__global__ void __launch_bounds__(256) k_prefill_prep(__half *xh, int *xexp, float *y, const uint16_t *x,
+                                                      int n_tokens) {
+    const int t = (int)(((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
+    if (t >= n_tokens) return;
+    const uint2 *src = reinterpret_cast<const uint2 *>(x + (size_t)t * kD);
+    constexpr int NV = kD / 4 / 32;                 // 28 four-value words per lane
+    uint2 v[NV];
+    uint32_t mb = 0;
+#pragma unroll
+    for (int i = 0; i < NV; i++) {
+        v[i] = __ldg(src + lane + 32 * i);
+        mb = max(mb, max(max(v[i].x & 0x7FFFu, (v[i].x >> 16) & 0x7FFFu), max(v[i].y & 0x7FFFu, (v[i].y >> 16) & 0x7FFFu)));
     }
+    mb = __reduce_max_sync(0xffffffffu, mb);
+    // the largest |x| as bf16 bits: biased exponent in bits 7-14 (0: zero or subnormal)
+    int k = 0;
+    if (mb != 0 && mb < 0x7F80u) k = (mb >= 0x80u ? (int)(mb >> 7) - 127 : -133 + (31 - __clz((int)mb))) - 13;
+    __half *dst = xh + (size_t)t * kD;
+    float *yz = y + (size_t)t * kD;
+#pragma unroll
+    for (int i = 0; i < NV; i++) {
+        const int c = 4 * (lane + 32 * i);
+        const float f0 = ldexpf(__uint_as_float(v[i].x << 16), -k), f1 = ldexpf(__uint_as_float(v[i].x & 0xFFFF0000u), -k);
+        const float f2 = ldexpf(__uint_as_float(v[i].y << 16), -k), f3 = ldexpf(__uint_as_float(v[i].y & 0xFFFF0000u), -k);
+        __half2 h01 = __floats2half2_rn(f0, f1), h23 = __floats2half2_rn(f2, f3);
+        *reinterpret_cast<uint2 *>(dst + c) =
+            make_uint2(*reinterpret_cast<uint32_t *>(&h01), *reinterpret_cast<uint32_t *>(&h23));
+        *reinterpret_cast<float4 *>(yz + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (lane == 0) xexp[t] = k;
 }
 
 // Work units: every active expert's pair list cut into runs of at most 128
@@ -479,6 +562,8 @@ inline size_t up256(size_t n) { return (n + 255) & ~size_t(255); }
 
 }  // namespace
 
+cudaError_t set_wait_polls_prefill(uint32_t polls) { return set_wait_polls_here(polls); }
+
 int prefill_max_units(int n_tokens) {
     const int pairs = n_tokens * kK;
     return pairs / kUnitTokens + (pairs < kE ? pairs : kE);
@@ -486,7 +571,8 @@ int prefill_max_units(int n_tokens) {
 
 size_t prefill_scratch_bytes(int n_tokens) {
     const size_t T = n_tokens;
-    return up256(T * kD * 2) + up256(T * kK * kF * 2) + up256((size_t)prefill_max_units(n_tokens) * 3 * 4) + 256;
+    return up256(T * kD * 2) + up256(T * kK * kF * 2) + up256((size_t)prefill_max_units(n_tokens) * 3 * 4) + 256 +
+           up256(T * 4);
 }
 
 cudaError_t launch_prefill(const Ctx &c, const PrefillArgs &p) {
@@ -496,10 +582,10 @@ cudaError_t launch_prefill(const Ctx &c, const PrefillArgs &p) {
     __half *H = reinterpret_cast<__half *>(ws + up256(T * kD * 2));
     int32_t *units = reinterpret_cast<int32_t *>(ws + up256(T * kD * 2) + up256(T * kK * kF * 2));
     int32_t *n_units = units + up256((size_t)prefill_max_units(p.n_tokens) * 3 * 4) / 4;
+    int *xexp = reinterpret_cast<int *>(reinterpret_cast<char *>(n_units) + 256);
 
-    const size_t n = T * kD;
     cudaError_t err = traced("prefill_prep", c.stream, [&] {
-        k_prefill_prep<<<(unsigned)((n / 4 + 255) / 256), 256, 0, c.stream>>>(xh, p.y, p.x, n);
+        k_prefill_prep<<<(unsigned)((T * 32 + 255) / 256), 256, 0, c.stream>>>(xh, xexp, p.y, p.x, (int)T);
         k_prefill_units<<<1, 1024, 0, c.stream>>>(p.counts, p.offsets, units, n_units);
         return cudaGetLastError();
     });
@@ -512,6 +598,7 @@ cudaError_t launch_prefill(const Ctx &c, const PrefillArgs &p) {
     a.perm = p.perm;
     a.w = p.w;
     a.xh = xh;
+    a.xexp = xexp;
     a.H = H;
     a.y = p.y;
     a.status = c.status;

@@ -5,13 +5,18 @@
 // per-weight work in registers.
 //
 // Activations.  kind::mxf4 multiplies e2m1 by e2m1, so every activation
-// row (x of a token for gate/up, h of a pair for down) is split into kPP
+// row (x of a token for gate/up, h of a pair for down) is split into PP
 // MXFP4 pieces per 32-column block (pieces.cuh: piece i takes the scale
 // that maps the block's largest residual into (3, 6] and the nearest e2m1
-// value of every residual).  Four pieces leave a residual below 4^-4 of the
-// block's largest value (the layer's relative L2 error is about 2e-4).  The
-// MMA sums the pieces itself: piece p of every token of a work unit is one
-// B operand, and the kPP MMAs of a K step accumulate into the same columns.
+// value of every residual); PP pieces leave a residual below 4^-PP of the
+// block's largest value.  x takes six pieces: SiTU-GLU's gate turns an
+// absolute error of g into a large change of h where g is near 0, and with
+// four pieces a block holding one value 10^2-10^3 times the others leaves its
+// small values with two pieces' precision (layer errors up to 2e-2 in
+// simulation, below 4e-5 with six).  h (|h| <= 100, read linearly) takes
+// four.  The MMA sums the pieces itself: piece p of every token of a work
+// unit is one B operand, and the MMAs of a K step accumulate into the same
+// columns.
 //
 // Work.  A unit is one expert and at most kUT of its (token, slot) pairs,
 // contiguous in the grouped order (Kimi K3 engine (c/kimi_k3.c), "Chunked
@@ -22,9 +27,11 @@
 //               swizzle) through per-expert tensor maps into an A ring
 //   warp 1      scale loader: the tile's scale bytes (16 per row, four
 //               stages ahead) from global into registers, then per stage the
-//               32-line scale-factor atoms tcgen05.cp reads (255 -> 0)
+//               32-line scale-factor atoms tcgen05.cp reads; a group of scale
+//               255 gets scale 0 and its codes are zeroed once the tile has
+//               landed, so it adds exactly 0
 //   warp 2      TMEM owner; lane 0 copies the scale atoms to TMEM and issues,
-//               per stage, 2 K steps x kPP pieces x NMAT MMAs (M = 128,
+//               per stage, 2 K steps x PP / 2 piece pairs x NMAT MMAs (M = 128,
 //               N = the unit's tokens rounded up to 16, K = 64)
 //   warp 3      B producer: one 3-D TMA per stage for all pieces of the
 //               unit's rows (box of 16, 32, ..., 96 rows) and one bulk copy
@@ -47,7 +54,8 @@
 namespace k3mx {
 namespace {
 
-constexpr int kPP = 4;                  // activation pieces
+constexpr int kPPx = 6;                 // pieces of x (gate/up's B)
+constexpr int kPPh = 4;                 // pieces of h (down's B)
 constexpr int kUT = 96;                 // pairs per unit (MMA N <= 96)
 constexpr int kKS = 128;                // K columns per stage (64 packed bytes per row)
 constexpr int kATile = 128 * 64;        // A tile: 128 rows x 64 B
@@ -69,21 +77,24 @@ constexpr int kPxSmemLimit = 227 * 1024;
 
 template <int PH> struct PxCfg;
 template <> struct PxCfg<0> {           // gate/up: g = W1 x, u = W3 x
-    static constexpr int NMAT = 2, K = kD, M = kF, SA = 5, SB = 4;
+    static constexpr int NMAT = 2, K = kD, M = kF, SA = 4, SB = 3, PP = kPPx;
 };
 template <> struct PxCfg<1> {           // down: Y = W2 h
-    static constexpr int NMAT = 1, K = kF, M = kD, SA = 6, SB = 6;
+    static constexpr int NMAT = 1, K = kF, M = kD, SA = 6, SB = 6, PP = kPPh;
 };
 
 template <int PH> struct PxShape {
     using C = PxCfg<PH>;
-    static constexpr int NMAT = C::NMAT, K = C::K, M = C::M, SA = C::SA, SB = C::SB;
+    static constexpr int NMAT = C::NMAT, K = C::K, M = C::M, SA = C::SA, SB = C::SB, PP = C::PP;
     static constexpr int KC = K / kKS, MT = M / 128, G = K / 32;
     static constexpr int ASTAGE = ((NMAT * (kATile + kAtomB)) + 1023) / 1024 * 1024;
-    static constexpr int BSTAGE = kPP * kBPiece + kPP * kAtomB;          // 26 KB
+    static constexpr int BSTAGE = PP * kBPiece + PP * kAtomB;            // 39 KB (x), 26 KB (h)
     // gate/up: per epilogue warp two rounds of h, 32 tokens x 32 features
     // in f16 (rows of 17 words: conflict-free both ways), to turn (feature,
-    // token) into (token, feature)
+    // token) into (token, feature); a token's 32 values are scaled by a
+    // power of two that puts their largest magnitude in [2^14, 2^15), its
+    // exponent kept in the row's 17th word, so h keeps 11 bits whatever
+    // its size
     static constexpr int TROW = 68;
     static constexpr int TRANS = PH == 0 ? 8 * 2 * 32 * TROW : 0;
     static constexpr int SMEM = 1024 + 1024 + SA * ASTAGE + SB * BSTAGE + TRANS;  // alignment slack, header
@@ -94,12 +105,13 @@ template <int PH> struct PxShape {
     // soon as h is staged in shared memory.
     static constexpr int NACC = 2 * kUT;                       // accumulator columns per matrix
     static constexpr int NBUF = PH == 0 ? 1 : 2;
-    // TMEM: accumulators [NBUF][NMAT][NACC], A scales [SA][NMAT][4], B scales [SB][kPP][4]
+    // TMEM: accumulators [NBUF][NMAT][NACC], A scales [SA][NMAT][4], B scales [SB][PP][4]
     static constexpr int ACC = NBUF * NMAT * NACC;
     static constexpr int SFA_COL = ACC;
     static constexpr int SFB_COL = SFA_COL + SA * NMAT * 4;
     static constexpr int TMEM_COLS = 512;
-    static_assert(SFB_COL + SB * kPP * 4 <= TMEM_COLS, "TMEM budget");
+    static_assert(SFB_COL + SB * PP * 4 <= TMEM_COLS, "TMEM budget");
+    static_assert(PP % 2 == 0, "pieces go two to an operand");
     static_assert(SMEM <= kPxSmemLimit, "shared memory budget");
     static_assert(K % (4 * kKS) == 0, "scale rows load in 16-byte groups of four stages");
     static_assert(ASTAGE % 1024 == 0 && BSTAGE % 1024 == 0, "stage alignment");
@@ -112,16 +124,18 @@ struct PxArgs {
     const float *w;                // routing weights by pair
     const uint8_t *maps;           // per-expert weight tensor maps [expert][w1, w3, w2]
     const k3mx_expert *experts;    // device table [896]
-    const uint8_t *b_atoms;        // B scale atoms of the pass's input [unit][KC][kPP][512]
-    uint8_t *h_planes;             // gate/up: h pieces [kPP][slots][F / 2]
-    uint8_t *h_atoms;              // gate/up: down's B scale atoms [unit][F / 128][kPP][512]
+    const uint8_t *b_atoms;        // B scale atoms of the pass's input [unit][KC][PP][512]
+    uint8_t *h_planes;             // gate/up: h pieces [kPPh][slots][F / 2]
+    uint8_t *h_atoms;              // gate/up: down's B scale atoms [unit][F / 128][kPPh][512]
     size_t slots;                  // 16 T: rows of one piece plane
     float *y;                      // down: [T][D], accumulated
     int *status;
 };
 
 struct PxHdr {
-    uint64_t afull[16], aempty[16], bfull[8], bempty[8], accf[2], acce[2], done;
+    // afull: the A stage's scale atoms (32 scale-loader lanes); atfull: its
+    // weight tiles (the producer's expect_tx and the copies' bytes)
+    uint64_t afull[16], atfull[16], aempty[16], bfull[8], bempty[8], accf[2], acce[2], done;
     uint32_t tmem;
     int abort;
 };
@@ -139,15 +153,16 @@ __device__ __forceinline__ float situ_fast(float g, float u) {
     return (4.0f * tanh_hw(0.25f * g) * sg) * (25.0f * tanh_hw(u * 0.04f));
 }
 
-// The kPP pieces of 32 values held by one lane (v, column order): piece p
+// The NP pieces of 32 values held by one lane (v, column order): piece p
 // takes the scale 2^e that maps the largest remaining |v| into (3, 6] and the
 // nearest e2m1 code of every v / 2^e (hardware conversion, two columns per
 // byte, the even column in the low nibble); v keeps the exact residual.
 // words[p] are the piece's 16 packed bytes, scale[p] its ue8m0 byte (255
 // when the values hold Inf or NaN; 0, with nothing taken, below 2^-124).
-__device__ __forceinline__ void lane_pieces(float (&v)[32], uint4 (&words)[kPP], uint32_t (&scale)[kPP]) {
+template <int NP>
+__device__ __forceinline__ void lane_pieces(float (&v)[32], uint4 (&words)[NP], uint32_t (&scale)[NP]) {
 #pragma unroll
-    for (int p = 0; p < kPP; p++) {
+    for (int p = 0; p < NP; p++) {
         // the largest |v| (non-negative floats order as their bit patterns;
         // Inf and NaN lie above every finite value)
         uint32_t mb = 0;
@@ -182,19 +197,14 @@ __device__ __forceinline__ void lane_pieces(float (&v)[32], uint4 (&words)[kPP],
     }
 }
 
-// byte of a unit's B scale atoms: stage c (128 columns), piece p, row n of
-// the unit, 32-column block kb % 4 of the stage
-__device__ __forceinline__ size_t atom_byte(int unit, int kc_total, int c, int p, int n, int kb4) {
-    return (((size_t)unit * kc_total + c) * kPP + p) * kAtomB + (size_t)(n & 31) * 16 + (n >> 5) * 4 + kb4;
-}
-
-// byte of the down pass's B scale atoms, pieces side by side: piece pair
-// p / 2 of stage c holds two atoms over the combined rows r = (p % 2) *
+// byte of a pass's B scale atoms (PP pieces), pieces side by side: piece
+// pair p / 2 of stage c holds two atoms over the combined rows r = (p % 2) *
 // rows + n (rows = the unit's box height); atom r / 128, line r % 32,
 // column (r / 32) % 4
+template <int PP>
 __device__ __forceinline__ size_t atom_byte_pair(int unit, int kc_total, int c, int p, int n, int rows, int kb4) {
     const int r = (p & 1) * rows + n;
-    return (((size_t)unit * kc_total + c) * (kPP / 2) + (p >> 1)) * (2 * kAtomB) + (size_t)(r >> 7) * kAtomB +
+    return (((size_t)unit * kc_total + c) * (PP / 2) + (p >> 1)) * (2 * kAtomB) + (size_t)(r >> 7) * kAtomB +
            (size_t)(r & 31) * 16 + ((r >> 5) & 3) * 4 + kb4;
 }
 
@@ -244,13 +254,15 @@ __global__ void __launch_bounds__(kPxThreads, 1)
     const uint32_t br0 = ar0 + SA * Sh::ASTAGE;             // B ring [SB][BSTAGE]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t afull0 = smem_addr(hd->afull), aempty0 = smem_addr(hd->aempty);
+    const uint32_t atfull0 = smem_addr(hd->atfull);
     const uint32_t bfull0 = smem_addr(hd->bfull), bempty0 = smem_addr(hd->bempty);
     const uint32_t accf0 = smem_addr(hd->accf), acce0 = smem_addr(hd->acce);
     const uint32_t done = smem_addr(&hd->done);
 
     if (tid == 0) {
         for (int i = 0; i < SA; i++) {
-            mbar_init(afull0 + 8 * i, 1 + 32);     // producer's expect_tx + the scale loader's lanes
+            mbar_init(afull0 + 8 * i, 32);         // the scale loader's lanes
+            mbar_init(atfull0 + 8 * i, 1);         // the producer's expect_tx
             mbar_init(aempty0 + 8 * i, 1);
         }
         for (int i = 0; i < SB; i++) {
@@ -319,14 +331,16 @@ __global__ void __launch_bounds__(kPxThreads, 1)
                 }
                 if (lane == 0) {
                     const uint32_t dst = ar0 + s * Sh::ASTAGE;
-                    mbar_arrive_expect_tx(afull0 + 8 * s, NMAT * kATile);
-                    tma_2d(dst, map0, c * 64, it.mt * 128, afull0 + 8 * s, pol);
-                    if (NMAT == 2) tma_2d(dst + kATile, map1, c * 64, it.mt * 128, afull0 + 8 * s, pol);
+                    mbar_arrive_expect_tx(atfull0 + 8 * s, NMAT * kATile);
+                    tma_2d(dst, map0, c * 64, it.mt * 128, atfull0 + 8 * s, pol);
+                    if (NMAT == 2) tma_2d(dst + kATile, map1, c * 64, it.mt * 128, atfull0 + 8 * s, pol);
                 }
                 __syncwarp();
             }
             if (!ok) break;
         }
+        // copies still in flight (after a wait gave up) land before the CTA leaves
+        if (lane == 0 && !drain_ring(atfull0, SA, sa)) report_status(a.status, kStatusWaitTimeout, 370 + PH);
     } else if (warp == kSfW) {
         // ----------------------------------------------- scale loader --
         // Each weight row's scale bytes load 16 at a time (four stages) into
@@ -375,16 +389,36 @@ __global__ void __launch_bounds__(kPxThreads, 1)
                             ok = false;
                             break;
                         }
-                        const uint32_t at0 = ar0 + s * Sh::ASTAGE + NMAT * kATile;
+                        const uint32_t ast = ar0 + s * Sh::ASTAGE, at0 = ast + NMAT * kATile;
+                        uint32_t wq[NMAT][4];
 #pragma unroll
-                        for (int m = 0; m < NMAT; m++) {
-                            const uint32_t w0 = j == 0 ? cur[m][0].x : j == 1 ? cur[m][0].y : j == 2 ? cur[m][0].z : cur[m][0].w;
-                            const uint32_t w1 = j == 0 ? cur[m][1].x : j == 1 ? cur[m][1].y : j == 2 ? cur[m][1].z : cur[m][1].w;
-                            const uint32_t w2 = j == 0 ? cur[m][2].x : j == 1 ? cur[m][2].y : j == 2 ? cur[m][2].z : cur[m][2].w;
-                            const uint32_t w3 = j == 0 ? cur[m][3].x : j == 1 ? cur[m][3].y : j == 2 ? cur[m][3].z : cur[m][3].w;
-                            sts128(at0 + m * kAtomB + 16 * lane, drop_nan_scales(w0), drop_nan_scales(w1),
-                                   drop_nan_scales(w2), drop_nan_scales(w3));
+                        for (int m = 0; m < NMAT; m++)
+#pragma unroll
+                            for (int i = 0; i < 4; i++)
+                                wq[m][i] = j == 0 ? cur[m][i].x : j == 1 ? cur[m][i].y : j == 2 ? cur[m][i].z : cur[m][i].w;
+                        // groups with scale 255 contribute nothing: once the
+                        // stage's weight tiles landed, their codes are zeroed
+                        // (rare; most stages skip this)
+                        uint32_t nan = 0;
+#pragma unroll
+                        for (int m = 0; m < NMAT; m++)
+#pragma unroll
+                            for (int i = 0; i < 4; i++) nan |= nan_scale_mask(wq[m][i]);
+                        if (__any_sync(0xffffffffu, nan != 0)) {
+                            if (!mbar_wait(atfull0 + 8 * s, (sa / SA) & 1)) {
+                                if (lane == 0) fail(315 + PH);
+                                ok = false;
+                                break;
+                            }
+#pragma unroll
+                            for (int m = 0; m < NMAT; m++)
+#pragma unroll
+                                for (int i = 0; i < 4; i++) zero_nan_groups_sw64(ast + m * kATile, lane + 32 * i, wq[m][i]);
                         }
+#pragma unroll
+                        for (int m = 0; m < NMAT; m++)
+                            sts128(at0 + m * kAtomB + 16 * lane, drop_nan_scales(wq[m][0]), drop_nan_scales(wq[m][1]),
+                                   drop_nan_scales(wq[m][2]), drop_nan_scales(wq[m][3]));
                         fence_async_smem();
                         mbar_arrive(afull0 + 8 * s);
                         sa++;
@@ -427,16 +461,17 @@ __global__ void __launch_bounds__(kPxThreads, 1)
                 if (lane == 0) {
                     const uint32_t dst = br0 + s * Sh::BSTAGE;
                     const uint32_t bf = bfull0 + 8 * s;
-                    mbar_arrive_expect_tx(bf, (uint32_t)(kPP * rows * 64 + kPP * kAtomB));
+                    mbar_arrive_expect_tx(bf, (uint32_t)(Sh::PP * rows * 64 + Sh::PP * kAtomB));
                     // pieces land `rows` rows apart: [piece][rows][64 B]
                     tma_3d(dst, bm, c * 64, it.off, 0, bf, pol);
-                    bulk_g2s(dst + kPP * kBPiece, a.b_atoms + ((size_t)it.unit * KC + c) * kPP * kAtomB,
-                             kPP * kAtomB, bf, pol);
+                    bulk_g2s(dst + Sh::PP * kBPiece, a.b_atoms + ((size_t)it.unit * KC + c) * Sh::PP * kAtomB,
+                             Sh::PP * kAtomB, bf, pol);
                 }
                 __syncwarp();
             }
             if (!ok) break;
         }
+        if (lane == 0 && !drain_ring(bfull0, SB, sb)) report_status(a.status, kStatusWaitTimeout, 372 + PH);
     } else if (warp == kMmaW) {
         // ------------------------------------------------- MMA issuer --
         if (lane == 0) {
@@ -459,7 +494,8 @@ __global__ void __launch_bounds__(kPxThreads, 1)
                 tc_fence_after();
                 for (int c = 0; c < KC; c++, sa++, sb++) {
                     const int s_a = sa % SA, s_b = sb % SB;
-                    if (!mbar_wait(afull0 + 8 * s_a, (sa / SA) & 1) || !mbar_wait(bfull0 + 8 * s_b, (sb / SB) & 1)) {
+                    if (!mbar_wait(atfull0 + 8 * s_a, (sa / SA) & 1) || !mbar_wait(afull0 + 8 * s_a, (sa / SA) & 1) ||
+                        !mbar_wait(bfull0 + 8 * s_b, (sb / SB) & 1)) {
                         fail(340 + PH);
                         run = false;
                         break;
@@ -467,16 +503,16 @@ __global__ void __launch_bounds__(kPxThreads, 1)
                     tc_fence_after();
                     const uint32_t ast = ar0 + s_a * Sh::ASTAGE, bst = br0 + s_b * Sh::BSTAGE;
                     const uint32_t sfa = tmem + Sh::SFA_COL + s_a * NMAT * 4;
-                    const uint32_t sfb = tmem + Sh::SFB_COL + s_b * kPP * 4;
+                    const uint32_t sfb = tmem + Sh::SFB_COL + s_b * Sh::PP * 4;
 #pragma unroll
                     for (int m = 0; m < NMAT; m++)
                         tmem_cp_atom(sfa + m * 4, desc_atom(ast + NMAT * kATile + m * kAtomB, 128));
                     // B scales: per piece one atom of 128 rows, or per piece
                     // pair two atoms of 256 combined rows (4 columns each)
 #pragma unroll
-                    for (int p = 0; p < kPP; p++)
-                        tmem_cp_atom(sfb + p * 4, desc_atom(bst + kPP * kBPiece + p * kAtomB, 128));
-                    constexpr int NB = kPP / 2;                        // B operands per K step
+                    for (int p = 0; p < Sh::PP; p++)
+                        tmem_cp_atom(sfb + p * 4, desc_atom(bst + Sh::PP * kBPiece + p * kAtomB, 128));
+                    constexpr int NB = Sh::PP / 2;                     // B operands per K step
 #pragma unroll
                     for (int m = 0; m < NMAT; m++)
 #pragma unroll
@@ -519,8 +555,9 @@ __global__ void __launch_bounds__(kPxThreads, 1)
             if (PH == 0) {
                 // Rounds of 32 tokens (this warp: tokens 32 half + 64 k ...).
                 // First every round's h (g and u: even-piece plus odd-piece
-                // columns) into the warp's f16 tiles, then the accumulator is
-                // released, then each lane splits one token's 32 features.
+                // columns) into the warp's f16 tiles, scaled per token, then
+                // the accumulator is released, then each lane splits one
+                // token's 32 features.
                 const int kb = it.mt * 4 + q4;                   // the warp's 32-feature block of h
                 const int hrows = b_rows(b_sel(it.ntok));         // the unit's B box height
                 uint8_t *tiles = smem + 1024 + SA * Sh::ASTAGE + SB * Sh::BSTAGE + (warp - kEpi0) * 2 * 32 * Sh::TROW;
@@ -537,12 +574,25 @@ __global__ void __launch_bounds__(kPxThreads, 1)
                         tmem_ld16(cu, u0);
                         tmem_ld16(cu + hrows, u1);
                         tmem_ld_wait();
+                        float hv[16];
 #pragma unroll
                         for (int j = 0; j < 16; j++) {
                             const float g = __uint_as_float(g0[j]) + __uint_as_float(g1[j]);
                             const float u = __uint_as_float(u0[j]) + __uint_as_float(u1[j]);
-                            *reinterpret_cast<__half *>(tile + (16 * hh + j) * Sh::TROW + 2 * lane) =
-                                __float2half_rn(situ_fast(g, u));
+                            hv[j] = situ_fast(g, u);
+                        }
+                        // each token's block of 32 features: its largest |h| sets the scale
+                        uint32_t mb[16];
+#pragma unroll
+                        for (int j = 0; j < 16; j++) mb[j] = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv[j])));
+#pragma unroll
+                        for (int j = 0; j < 16; j++) {
+                            const int E = (int)(mb[j] >> 23);
+                            const int es = (E == 0 || E == 255) ? 0 : max(-100, min(100, E - 127 - 14));
+                            uint8_t *trow = tile + (16 * hh + j) * Sh::TROW;
+                            *reinterpret_cast<__half *>(trow + 2 * lane) =
+                                __float2half_rn(hv[j] * __int_as_float((127 - es) << 23));
+                            if (lane == j) *reinterpret_cast<int *>(trow + 64) = es;
                         }
                     }
                 }
@@ -552,22 +602,23 @@ __global__ void __launch_bounds__(kPxThreads, 1)
                 for (int r = 0; r < nr; r++) {
                     const int n = 32 * half + 64 * r + lane;
                     const uint8_t *row = tiles + (r * 32 + lane) * Sh::TROW;
+                    const float up = __int_as_float((127 + *reinterpret_cast<const int *>(row + 64)) << 23);
                     float v[32];
 #pragma unroll
                     for (int wd = 0; wd < 16; wd++) {
                         const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(row + 4 * wd));
-                        v[2 * wd] = f.x;
-                        v[2 * wd + 1] = f.y;
+                        v[2 * wd] = f.x * up;
+                        v[2 * wd + 1] = f.y * up;
                     }
                     if (n < it.ntok) {
-                        uint4 wds[kPP];
-                        uint32_t sc[kPP];
-                        lane_pieces(v, wds, sc);
+                        uint4 wds[kPPh];
+                        uint32_t sc[kPPh];
+                        lane_pieces<kPPh>(v, wds, sc);
                         uint8_t *dst = a.h_planes + ((size_t)it.off + n) * (kF / 2) + (size_t)kb * 16;
 #pragma unroll
-                        for (int p = 0; p < kPP; p++) {
+                        for (int p = 0; p < kPPh; p++) {
                             *reinterpret_cast<uint4 *>(dst + p * plane) = wds[p];
-                            a.h_atoms[atom_byte_pair(it.unit, kF / kKS, it.mt, p, n, hrows, q4)] = (uint8_t)sc[p];
+                            a.h_atoms[atom_byte_pair<kPPh>(it.unit, kF / kKS, it.mt, p, n, hrows, q4)] = (uint8_t)sc[p];
                         }
                     }
                 }
@@ -600,7 +651,7 @@ __global__ void __launch_bounds__(kPxThreads, 1)
     __syncthreads();
     if (warp == kMmaW) {
         // no MMA may still be running when TMEM is released
-        if (!mbar_wait(done, 0) && lane == 0) report_status(a.status, kStatusWaitTimeout, 360 + PH);
+        if (!mbar_wait_drain(done, 0) && lane == 0) report_status(a.status, kStatusWaitTimeout, 360 + PH);
         tc_fence_after();
         tmem_dealloc(tmem, Sh::TMEM_COLS);
     }
@@ -672,7 +723,7 @@ k_px_slots(const int32_t *units, const int32_t *n_units, const int32_t *perm, in
     build_maps_cta(maps, kE, table, k3mx_expert{}, w13, w2, blockIdx.x - max_units);
 }
 
-// One thread per (token, 32-column block): x (bf16) -> kPP pieces, written
+// One thread per (token, 32-column block): x (bf16) -> kPPx pieces, written
 // to the token's 16 slots (rows of the piece planes and bytes of the units'
 // B scale atoms); y of the token's block zeroed for the down pass's sums.
 __global__ void __launch_bounds__(256)
@@ -699,9 +750,9 @@ k_px_xprep(const uint16_t *__restrict__ x, int n_tokens, const int32_t *__restri
     float4 *yz = reinterpret_cast<float4 *>(y + i0);
 #pragma unroll
     for (int q = 0; q < 8; q++) yz[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-    uint4 wds[kPP];
-    uint32_t sc[kPP];
-    lane_pieces(v, wds, sc);
+    uint4 wds[kPPx];
+    uint32_t sc[kPPx];
+    lane_pieces<kPPx>(v, wds, sc);
 #pragma unroll 4
     for (int k = 0; k < kK; k++) {
         const int slot = __ldg(slot_of_pair + (size_t)t * kK + k);
@@ -710,9 +761,9 @@ k_px_xprep(const uint16_t *__restrict__ x, int n_tokens, const int32_t *__restri
         const int rows = b_rows(b_sel(__ldg(units + 3 * (un >> 8) + 2)));
         uint8_t *dst = planes + (size_t)slot * (kD / 2) + (size_t)kb * 16;
 #pragma unroll
-        for (int p = 0; p < kPP; p++) {
+        for (int p = 0; p < kPPx; p++) {
             *reinterpret_cast<uint4 *>(dst + (size_t)p * slots * (kD / 2)) = wds[p];
-            atoms[atom_byte_pair(un >> 8, KC, kb >> 2, p, un & 255, rows, kb & 3)] = (uint8_t)sc[p];
+            atoms[atom_byte_pair<kPPx>(un >> 8, KC, kb >> 2, p, un & 255, rows, kb & 3)] = (uint8_t)sc[p];
         }
     }
 }
@@ -780,13 +831,14 @@ bool px_weight_templates(CUtensorMap &w13, CUtensorMap &w2) {
     return true;
 }
 
-// 3-D uint8 map over kPP planes of `rows` rows of row_bytes: boxes of 64
-// bytes x box_rows rows x kPP planes, 64-byte swizzle
-bool encode_planes(CUtensorMap &m, const void *base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
+// 3-D uint8 map over `planes` planes of `rows` rows of row_bytes: boxes of
+// 64 bytes x box_rows rows x all planes, 64-byte swizzle
+bool encode_planes(CUtensorMap &m, const void *base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows,
+                   int planes) {
     auto enc = tmap_encoder();
     if (enc == nullptr) return false;
-    const cuuint64_t dims[3] = {row_bytes, rows, (cuuint64_t)kPP}, strides[2] = {row_bytes, row_bytes * rows};
-    const cuuint32_t box[3] = {64, box_rows, (cuuint32_t)kPP}, es[3] = {1, 1, 1};
+    const cuuint64_t dims[3] = {row_bytes, rows, (cuuint64_t)planes}, strides[2] = {row_bytes, row_bytes * rows};
+    const cuuint32_t box[3] = {64, box_rows, (cuuint32_t)planes}, es[3] = {1, 1, 1};
     return enc(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -806,10 +858,10 @@ PxLayout px_layout(int n_tokens) {
         o += up256(b);
         return at;
     };
-    L.xplanes = take(kPP * S * (kD / 2));
-    L.hplanes = take(kPP * S * (kF / 2));
-    L.xatoms = take(U * (kD / kKS) * kPP * kAtomB);
-    L.hatoms = take(U * (kF / kKS) * kPP * kAtomB);
+    L.xplanes = take(kPPx * S * (kD / 2));
+    L.hplanes = take(kPPh * S * (kF / 2));
+    L.xatoms = take(U * (kD / kKS) * kPPx * kAtomB);
+    L.hatoms = take(U * (kF / kKS) * kPPh * kAtomB);
     L.units = take(U * 3 * 4);
     L.n_units = take(4);
     L.slot_un = take(S * 4);
@@ -820,6 +872,8 @@ PxLayout px_layout(int n_tokens) {
 }
 
 }  // namespace
+
+cudaError_t set_wait_polls_px(uint32_t polls) { return set_wait_polls_here(polls); }
 
 int prefill_mx_max_units(int n_tokens) {
     const int pairs = n_tokens * kK;
@@ -846,8 +900,8 @@ cudaError_t launch_prefill_mx(const Ctx &c, const PrefillArgs &p) {
     PxBMaps xmap, hmap;
     if (!px_weight_templates(w13, w2)) return cudaErrorNotSupported;
     for (int i = 0; i < kBoxes; i++)
-        if (!encode_planes(xmap.m[i], xplanes, kD / 2, S, b_rows(i)) ||
-            !encode_planes(hmap.m[i], hplanes, kF / 2, S, b_rows(i)))
+        if (!encode_planes(xmap.m[i], xplanes, kD / 2, S, b_rows(i), kPPx) ||
+            !encode_planes(hmap.m[i], hplanes, kF / 2, S, b_rows(i), kPPh))
             return cudaErrorNotSupported;
 
     cudaError_t err = traced("prefill_prep", c.stream, [&] {

@@ -95,8 +95,36 @@ __device__ __forceinline__ uint64_t l2_evict_last_policy() {
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
     return pol;
 }
-// scale byte 255 (a group that contributes nothing) -> 0 (2^-127)
+// scale byte 255 (a group that contributes nothing) -> 0 (2^-127); the
+// group's codes are zeroed in shared memory as well (zero_nan_groups_*), so
+// the group adds exactly 0
 __device__ __forceinline__ uint32_t drop_nan_scales(uint32_t w) { return w & ~__vcmpeq4(w, 0xFFFFFFFFu); }
+
+// bytes 0xFF of a scale word (four groups) as 0xFF lanes, else 0
+__device__ __forceinline__ uint32_t nan_scale_mask(uint32_t w) { return __vcmpeq4(w, 0xFFFFFFFFu); }
+
+// Zero the 16 packed bytes (32 codes) of every group whose scale byte is 255,
+// for row r of a weight tile of 128-byte rows in the 128-byte swizzle (a
+// 256-column chunk: groups 0-3 from sc.x, 4-7 from sc.y).  Called after the
+// tile's copy landed and before the tensor core reads it.
+__device__ __forceinline__ void zero_nan_groups_sw128(uint32_t tile, int r, uint2 sc) {
+    const uint32_t m[2] = {nan_scale_mask(sc.x), nan_scale_mask(sc.y)};
+#pragma unroll
+    for (int g = 0; g < 8; g++)
+        if ((m[g >> 2] >> (8 * (g & 3))) & 1u)
+            sts128(tile + (uint32_t)(r * 128) + (uint32_t)(((g ^ (r & 7)) & 7) << 4), 0u, 0u, 0u, 0u);
+}
+
+// The same for a tile of 64-byte rows in the 64-byte swizzle (a 128-column
+// stage: groups 0-3 from the bytes of sc); chunk j of row r sits at
+// j ^ ((r / 2) % 4)
+__device__ __forceinline__ void zero_nan_groups_sw64(uint32_t tile, int r, uint32_t sc) {
+    const uint32_t m = nan_scale_mask(sc);
+#pragma unroll
+    for (int g = 0; g < 4; g++)
+        if ((m >> (8 * g)) & 1u)
+            sts128(tile + (uint32_t)(r * 64) + (uint32_t)(((g ^ (r >> 1)) & 3) << 4), 0u, 0u, 0u, 0u);
+}
 
 
 }  // namespace

@@ -16,7 +16,7 @@ FAKE = 0x10000          # an aligned, non-null address that is never dereference
 def test_library_exports_every_declared_symbol():
     L = k3mx.lib()
     declared = k3mx.declared_symbols()
-    assert len(declared) == 22
+    assert len(declared) == 23
     out = subprocess.run(["nm", "-D", "--defined-only", k3mx.LIB_PATH],
                          capture_output=True, text=True, check=True).stdout
     exported = set(re.findall(r"\sT\s(k3mx_\w+)", out))
@@ -148,3 +148,48 @@ def test_noalloc_refuses_bad_arguments():
     # the fixed 8 MiB array holds the decode layout of the largest batch, either dtype
     for dt in (0, 1):
         assert k3mx.k3mx_moe_workspace_size(k3mx.K3MX_NOALLOC_MAX_TOKENS, dt, 1) <= 8 << 20
+
+
+def test_binding_refuses_mismatched_shapes():
+    """The Python binding checks every tensor against the token count before
+    any device check or library call (the C ABI sees raw pointers only, so a
+    short output would be written past its end)."""
+    f32 = lambda *s: torch.zeros(*s, dtype=torch.float32)
+    table = torch.zeros(896, 6, dtype=torch.int64)
+    ws = torch.zeros(16, dtype=torch.uint8)
+    bad = [
+        # x must be [T, 3584]: a 1-D x would read as 3584 tokens
+        lambda: k3mx.k3mx_moe_routed(f32(3584), f32(3584), table, f32(896), f32(896), ws),
+        # y shorter than the batch
+        lambda: k3mx.k3mx_moe_routed(f32(1, 3584), f32(8, 3584), table, f32(8, 896), f32(896), ws),
+        # logits of another batch
+        lambda: k3mx.k3mx_moe_routed(f32(8, 3584), f32(8, 3584), table, f32(4, 896), f32(896), ws),
+        # routing outputs too short
+        lambda: k3mx.k3mx_moe_routed(f32(8, 3584), f32(8, 3584), table, f32(8, 896), f32(896), ws,
+                                     idx_out=torch.zeros(16, dtype=torch.int32)),
+        # expert table of the wrong shape or type
+        lambda: k3mx.k3mx_moe_routed(f32(2, 3584), f32(2, 3584), table[:100], f32(2, 896), f32(896), ws),
+        lambda: k3mx.k3mx_moe_routed(f32(2, 3584), f32(2, 3584), table.int(), f32(2, 896), f32(896), ws),
+        lambda: k3mx.k3mx_moe_routed_topp(f32(2, 3584), f32(2, 3584), table, f32(2, 896), f32(895), ws, 0.5),
+        lambda: k3mx.k3mx_moe_decode_noalloc(f32(3, 3584), f32(2, 3584), table, f32(2, 896), f32(896)),
+        lambda: k3mx.k3mx_moe_routed_host(f32(2, 3584), f32(2, 3583), table, f32(2, 896), f32(896), ws),
+        lambda: k3mx.k3mx_route_topk(torch.zeros(2, 16, dtype=torch.int32), f32(2, 8), f32(2, 896), f32(896)),
+        lambda: k3mx.k3mx_route_topp(torch.zeros(2, 16, dtype=torch.int32), f32(2, 16), f32(896), f32(896), 0.5),
+        lambda: k3mx.k3mx_group(torch.zeros(896, dtype=torch.int32), torch.zeros(896, dtype=torch.int32),
+                                torch.zeros(32, dtype=torch.int32), torch.zeros(2, 16, dtype=torch.int32), ws),
+        lambda: k3mx.k3mx_router(f32(2, 896), torch.zeros(2, 16, dtype=torch.int32), f32(2, 16), f32(2, 7000),
+                                 torch.zeros(896, 7168, dtype=torch.int16), f32(896)),
+        lambda: k3mx.k3mx_latent_moe(f32(2, 3584), f32(2, 7168), None, table, ws),
+        lambda: k3mx.k3mx_expert_ffn(f32(3584), f32(3072), None, ws),
+        lambda: k3mx.k3mx_gemv(f32(64), f32(128), torch.zeros(64, 64, dtype=torch.uint8),
+                               torch.zeros(64, 3, dtype=torch.uint8)),
+        lambda: k3mx.k3mx_gemv(f32(63), f32(128), torch.zeros(64, 64, dtype=torch.uint8),
+                               torch.zeros(64, 4, dtype=torch.uint8)),
+    ]
+    for i, call in enumerate(bad):
+        with pytest.raises(TypeError) as err:
+            call()
+        assert "CUDA" not in str(err.value), (i, str(err.value))    # refused for its shape, not its device
+    # well-shaped host tensors pass the shape checks and stop at the device check
+    with pytest.raises(TypeError, match="CUDA"):
+        k3mx.k3mx_moe_routed(f32(2, 3584), f32(2, 3584), table, f32(2, 896), f32(896), ws)

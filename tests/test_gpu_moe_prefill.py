@@ -1,6 +1,6 @@
 """The routed-expert layer on the two prefill paths (bf16 activations,
-grouped tcgen05 GEMMs: weights dequantised to f16, or x and h as four MXFP4
-pieces on the block-scaled MMAs) against the oracle.  Routing bit-exact;
+grouped tcgen05 GEMMs: weights dequantised to f16, or x as six and h as four
+MXFP4 pieces on the block-scaled MMAs) against the oracle.  Routing bit-exact;
 per sampled token the relative L2 error of y is at most 1e-2 (the
 bf16-activation tolerance)."""
 import numpy as np
@@ -10,7 +10,7 @@ import torch
 import mxfp4_routed_expert_k3mx_gb300 as k3mx
 import oracle
 import synth
-from helpers import moe_oracle
+from helpers import arena_expert_bytes, moe_oracle, moe_oracle_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -57,8 +57,14 @@ def test_prefill_4096_tokens(arena, cuda_dev, path):
     counts = np.bincount(ir.ravel(), minlength=896)
     assert counts.min() > 0 and 60 < counts.mean() < 90
     assert np.all(np.isfinite(y))
-    worst = check_tokens(y, x, ir, wr, [0, 1, 2, 777, 2048, 3001, 4094, 4095], "prefill 4096")
-    assert worst < 5e-3
+    # a seeded 512-token subset (the first and last tokens included)
+    rng = np.random.default_rng(4096)
+    tokens = sorted(set([0, 1, 4095] + rng.choice(T, 509, replace=False).tolist()))
+    yr = moe_oracle_rows(x, ir, wr, tokens, arena_expert_bytes)
+    rel = [np.linalg.norm(y[t].astype(np.float64) - yr[i].astype(np.float64)) / np.linalg.norm(yr[i].astype(np.float64))
+           for i, t in enumerate(tokens)]
+    assert max(rel) <= 1e-2, f"prefill 4096: worst token {tokens[int(np.argmax(rel))]} relative L2 {max(rel):.3e}"
+    assert max(rel) < 5e-3
 
 
 @pytest.mark.parametrize("path", PATHS)

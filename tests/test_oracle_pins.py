@@ -232,6 +232,57 @@ def test_expert_composition_tiny():
     assert np.all(np.abs(y - y_ref) <= 2.0 ** -24 * np.abs(y_ref) + 1e-12 * absdot)
 
 
+def test_expert_bound_brute_force_tiny():
+    """The decode tolerance helper, brute force on a D=96, F=64 expert with
+    NaN groups: bound_i = sum_j |w2_ij| (|h_j| + 30 E_j) with
+    E_j = sum_c (|w1_jc| + |w3_jc|) |x_c|, NaN groups excluded, from the
+    dequantised matrices.  A wrong factor, a dropped term or a NaN group
+    counted changes the result by far more than rounding."""
+    D, F = 96, 64
+    buf = synth.expert(6, seed=10, D=D, F=F, nan_frac=0.05)
+    w = synth.split_expert(buf, D=D, F=F)
+    x = synth.token_inputs(1, seed=10, D=D)[0]
+    _, _, _, h = oracle.expert(x, *w, intermediates=True)
+    b = oracle.expert_bound(x, h, *w)
+    W1, W3, W2 = dequant(w[0], w[1]), dequant(w[2], w[3]), dequant(w[4], w[5])
+    E = (np.abs(W1) + np.abs(W3)) @ np.abs(x.astype(np.float64))
+    ref = np.abs(W2) @ (np.abs(h.astype(np.float64)) + 30.0 * E)
+    assert np.allclose(b, ref, rtol=1e-12, atol=0)
+    assert (w[1] == 255).any() and (w[5] == 255).any()
+
+
+def test_expert_bound_covers_admissible_errors():
+    """What the bound is for: if g and u each move by at most 1e-5 of their
+    GEMV bound (sum_c |w_jc| |x_c|) and h by at most 1e-5 |h|, y moves by at
+    most 1e-5 * bound.  Checked in double on a tiny expert with the signs of
+    the moves set against each output row (the worst case of a linear
+    model) and with random moves, through the exact SiTU-GLU."""
+    D, F = 96, 64
+    buf = synth.expert(7, seed=11, D=D, F=F, nan_frac=0.02)
+    w = synth.split_expert(buf, D=D, F=F)
+    rng = np.random.default_rng(11)
+    W1, W3, W2 = dequant(w[0], w[1]), dequant(w[2], w[3]), dequant(w[4], w[5])
+    situ = np.vectorize(oracle.situ)
+    for scale in (0.05, 1.0, 20.0):
+        x = (synth.token_inputs(1, seed=12, D=D)[0] * scale).astype(np.float32)
+        xd = x.astype(np.float64)
+        g, u = W1 @ xd, W3 @ xd
+        h = situ(g, u)
+        b = oracle.expert_bound(x, h.astype(np.float32), *w)
+        e1 = 1e-5 * (np.abs(W1) @ np.abs(xd))
+        e3 = 1e-5 * (np.abs(W3) @ np.abs(xd))
+        for trial in range(6):
+            if trial < 2:
+                sg = np.sign(W2[trial]) if trial == 0 else -np.sign(W2[trial])
+                dg, du = sg * e1, sg * e3
+            else:
+                dg, du = rng.uniform(-1, 1, F) * e1, rng.uniform(-1, 1, F) * e3
+            h2 = situ(g + dg, u + du)
+            h2 = h2 + rng.uniform(-1, 1, F) * 1e-5 * np.abs(h2)
+            dy = np.abs(W2 @ h2 - W2 @ h)
+            assert np.all(dy <= 1e-5 * b * (1 + 1e-9)), (scale, trial, np.max(dy / (1e-5 * b)))
+
+
 def test_expert_w1_is_gate():
     """Zeroing W3 (u = 0) zeroes h; zeroing W1 (g = 0) zeroes h too, but a
     large positive W1 row saturates the gate so h = 100 tanh(u/25)."""
