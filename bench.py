@@ -858,6 +858,43 @@ def run_profile_case(args):
         if st[0] != 0:
             sys.exit(1)
         return
+    if args.profile_case == "gemv":
+        # `iters` graph replays of 64 GEMVs over distinct copies of the
+        # 3072 x 3584 matrix (374 MB)
+        p, s, x = synth.gemv_inputs(seed=0)
+        P, S = torch.from_numpy(p).to(dev), torch.from_numpy(s).to(dev)
+        Ps, Ss = [P.clone() for _ in range(64)], [S.clone() for _ in range(64)]
+        xd = torch.from_numpy(x).to(dev)
+        ys = torch.empty((64, GEMV_ROWS), dtype=torch.float32, device=dev)
+        for i in range(64):
+            k3mx.k3mx_gemv(ys[i], xd, Ps[i], Ss[i])
+        g = graph_of(k3mx, dev, [lambda i=i: k3mx.k3mx_gemv(ys[i], xd, Ps[i], Ss[i]) for i in range(64)])
+        for _ in range(args.iters):
+            g.replay()
+        torch.cuda.synchronize(dev)
+        st = k3mx.k3mx_device_status()
+        print(json.dumps({"profile_case": "gemv", "iters": args.iters, "status": st}), flush=True)
+        if st[0] != 0:
+            sys.exit(1)
+        return
+    if args.profile_case == "expert":
+        # `iters` rounds of k3mx_expert_ffn over R resident experts, one token each
+        R = args.resident
+        arena = synth.expert_arena_device(dev, seed=0, lo=118, hi=128, n_experts=R)
+        offs = k3mx.expert_offsets()
+        exs = [k3mx.expert_struct(*[arena.data_ptr() + e * EXPERT_BYTES + o for o in offs]) for e in range(R)]
+        xs = torch.from_numpy(synth.token_inputs(R, seed=77)).to(dev)
+        ys = torch.empty((R, D), dtype=torch.float32, device=dev)
+        ws = torch.empty(k3mx.k3mx_expert_ffn_workspace_size(), dtype=torch.uint8, device=dev)
+        for _ in range(args.iters):
+            for e in range(R):
+                k3mx.k3mx_expert_ffn(ys[e], xs[e], exs[e], ws)
+        torch.cuda.synchronize(dev)
+        st = k3mx.k3mx_device_status()
+        print(json.dumps({"profile_case": "expert", "resident": R, "iters": args.iters, "status": st}), flush=True)
+        if st[0] != 0:
+            sys.exit(1)
+        return
     if args.profile_case == "router":
         # the router alone: fp32 states up to 16 tokens, bf16 beyond
         T = args.tokens
@@ -913,7 +950,7 @@ def main():
     ap.add_argument("--primary-only", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
-    ap.add_argument("--profile-case", choices=["decode", "prefill", "router", "latent"])
+    ap.add_argument("--profile-case", choices=["decode", "prefill", "router", "latent", "gemv", "expert"])
     ap.add_argument("--tokens", type=int, default=1)
     ap.add_argument("--resident", type=int, default=64)
     ap.add_argument("--confine", action="store_true")

@@ -9,12 +9,11 @@
 //   down:    Y = W2 H^T over K = 3072, y[t] += w_tk * Y (fp32 atomics)
 //
 // MXFP4 -> f16 in shared memory.  tcgen05 kind::f16 takes A and B of one
-// type; the weights are dequantised to f16 and the activations are f16 too:
-// x is converted once, each token scaled by a power of two 2^-k_t that puts
-// its largest |x| in [2^13, 2^14), so no bf16 value overflows f16 and every
-// value within 2^-11 of the token's largest is exact (bf16 keeps 8
-// significant bits, f16 11); the gate/up epilogue multiplies g and u by
-// 2^k_t.  An e2m1 code is exact in f16 (cvt.rn.f16x2.e2m1x2);
+// type; the weights are dequantised to f16 and the activations are f16 too
+// (x is converted once: a bf16 value is exact in f16 from 2^-14 to 65504;
+// larger ones overflow and smaller ones lose bits, so this path takes
+// activations in that range, and h below 2^-14 loses bits the same way).
+// An e2m1 code is exact in f16 (cvt.rn.f16x2.e2m1x2);
 // its group scale 2^(s - 127) is split into a per-row reference 2^(sref-127),
 // sref the row's largest scale, applied to the fp32 accumulator in the
 // epilogue, and 2^(s - sref) <= 1 multiplied into the f16 value (exact while
@@ -65,8 +64,7 @@ struct PArgs {
     const k3mx_expert *experts;
     const int32_t *units, *n_units, *perm;
     const float *w;            // routing weights by pair
-    const __half *xh;          // [T][D] f16 activations, token t scaled by 2^-xexp[t]
-    const int *xexp;           // [T]
+    const __half *xh;          // [T][D] f16 activations
     __half *H;                 // [16T][F] f16 h rows in grouped order
     float *y;                  // [T][D]
     int *status;
@@ -80,11 +78,6 @@ __device__ __forceinline__ __half2 pow2_h2(int k) {
     else b = (uint32_t)(k + 15) << 10;
     b |= b << 16;
     return *reinterpret_cast<__half2 *>(&b);
-}
-
-// v * 2^e: one multiply when 2^e is a normal float, else ldexpf
-__device__ __forceinline__ float scale_pow2(float v, int e) {
-    return (e >= -126 && e <= 127) ? v * __int_as_float((e + 127) << 23) : ldexpf(v, e);
 }
 
 // spread of the f16 dequantisation below the row's reference scale
@@ -323,31 +316,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_prefill(PArgs a) {
             const k3mx_expert ex = a.experts[e];
             const int row = mt * kBM + r;
             if (PH == kPhaseGateUp) {
-                const int e1 = row_sref(ex.s1 + (size_t)row * G, ex.w1 + (size_t)row * (K / 2), G) - 127;
-                const int e3 = row_sref(ex.s3 + (size_t)row * G, ex.w3 + (size_t)row * (K / 2), G) - 127;
+                const float f1 = ldexpf(1.f, row_sref(ex.s1 + (size_t)row * G, ex.w1 + (size_t)row * (K / 2), G) - 127);
+                const float f3 = ldexpf(1.f, row_sref(ex.s3 + (size_t)row * G, ex.w3 + (size_t)row * (K / 2), G) - 127);
                 const uint32_t tg = tmem + lane_base + (uint32_t)(ab * 256);
-                // the unit's token exponents k_t, lane l holding tokens l, l + 32, l + 64, l + 96
-                int ktv[kUnitTokens / 32];
-#pragma unroll
-                for (int qq = 0; qq < kUnitTokens / 32; qq++) {
-                    const int n = lane + 32 * qq;
-                    ktv[qq] = n < ntok ? __ldg(a.xexp + __ldg(a.perm + off + n) / kK) : 0;
-                }
                 for (int n0 = 0; n0 < npad; n0 += 16) {
                     uint32_t gv[16], uv[16];
                     tmem_ld16(tg + n0, gv);
                     tmem_ld16(tg + 128 + n0, uv);
                     tmem_ld_wait();
-                    const int qsel = n0 >> 5;
-                    const int kreg = qsel == 0 ? ktv[0] : qsel == 1 ? ktv[1] : qsel == 2 ? ktv[2] : ktv[3];
 #pragma unroll
                     for (int j = 0; j < 16; j++) {
                         const int n = n0 + j;
-                        const int kt = __shfl_sync(0xffffffffu, kreg, n & 31);
                         if (n < ntok) {
-                            // the row's reference scale and the token's 2^k_t, one rounding
-                            const float h = situ_glu(scale_pow2(__uint_as_float(gv[j]), e1 + kt),
-                                                     scale_pow2(__uint_as_float(uv[j]), e3 + kt));
+                            const float h = situ_glu(__uint_as_float(gv[j]) * f1, __uint_as_float(uv[j]) * f3);
                             a.H[(size_t)(off + n) * kF + row] = __float2half_rn(h);
                         }
                     }
@@ -463,39 +444,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_prefill(PArgs a) {
     }
 }
 
-// x (bf16 bits) -> f16 activations, token t scaled by 2^-k_t (k_t = the
-// exponent of its largest |x| minus 13; 0 for a token of zeros or one
-// holding Inf or NaN); y = 0.  One warp per token.
-__global__ void __launch_bounds__(256) k_prefill_prep(__half *xh, int *xexp, float *y, const uint16_t *x,
-                                                      int n_tokens) {
-    const int t = (int)(((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
-    if (t >= n_tokens) return;
-    const uint2 *src = reinterpret_cast<const uint2 *>(x + (size_t)t * kD);
-    constexpr int NV = kD / 4 / 32;                 // 28 four-value words per lane
-    uint2 v[NV];
-    uint32_t mb = 0;
-#pragma unroll
-    for (int i = 0; i < NV; i++) {
-        v[i] = __ldg(src + lane + 32 * i);
-        mb = max(mb, max(max(v[i].x & 0x7FFFu, (v[i].x >> 16) & 0x7FFFu), max(v[i].y & 0x7FFFu, (v[i].y >> 16) & 0x7FFFu)));
-    }
-    mb = __reduce_max_sync(0xffffffffu, mb);
-    // the largest |x| as bf16 bits: biased exponent in bits 7-14 (0: zero or subnormal)
-    int k = 0;
-    if (mb != 0 && mb < 0x7F80u) k = (mb >= 0x80u ? (int)(mb >> 7) - 127 : -133 + (31 - __clz((int)mb))) - 13;
-    __half *dst = xh + (size_t)t * kD;
-    float *yz = y + (size_t)t * kD;
-#pragma unroll
-    for (int i = 0; i < NV; i++) {
-        const int c = 4 * (lane + 32 * i);
-        const float f0 = ldexpf(__uint_as_float(v[i].x << 16), -k), f1 = ldexpf(__uint_as_float(v[i].x & 0xFFFF0000u), -k);
-        const float f2 = ldexpf(__uint_as_float(v[i].y << 16), -k), f3 = ldexpf(__uint_as_float(v[i].y & 0xFFFF0000u), -k);
+// x (bf16 bits) -> f16 activations; y = 0
+__global__ void k_prefill_prep(__half *xh, float *y, const uint16_t *x, size_t n) {
+    const size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+    if (i + 3 < n) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(x + i);
+        const float f0 = __uint_as_float(v.x << 16), f1 = __uint_as_float(v.x & 0xFFFF0000u);
+        const float f2 = __uint_as_float(v.y << 16), f3 = __uint_as_float(v.y & 0xFFFF0000u);
         __half2 h01 = __floats2half2_rn(f0, f1), h23 = __floats2half2_rn(f2, f3);
-        *reinterpret_cast<uint2 *>(dst + c) =
+        *reinterpret_cast<uint2 *>(xh + i) =
             make_uint2(*reinterpret_cast<uint32_t *>(&h01), *reinterpret_cast<uint32_t *>(&h23));
-        *reinterpret_cast<float4 *>(yz + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4 *>(y + i) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    if (lane == 0) xexp[t] = k;
 }
 
 // Work units: every active expert's pair list cut into runs of at most 128
@@ -571,8 +531,7 @@ int prefill_max_units(int n_tokens) {
 
 size_t prefill_scratch_bytes(int n_tokens) {
     const size_t T = n_tokens;
-    return up256(T * kD * 2) + up256(T * kK * kF * 2) + up256((size_t)prefill_max_units(n_tokens) * 3 * 4) + 256 +
-           up256(T * 4);
+    return up256(T * kD * 2) + up256(T * kK * kF * 2) + up256((size_t)prefill_max_units(n_tokens) * 3 * 4) + 256;
 }
 
 cudaError_t launch_prefill(const Ctx &c, const PrefillArgs &p) {
@@ -582,10 +541,10 @@ cudaError_t launch_prefill(const Ctx &c, const PrefillArgs &p) {
     __half *H = reinterpret_cast<__half *>(ws + up256(T * kD * 2));
     int32_t *units = reinterpret_cast<int32_t *>(ws + up256(T * kD * 2) + up256(T * kK * kF * 2));
     int32_t *n_units = units + up256((size_t)prefill_max_units(p.n_tokens) * 3 * 4) / 4;
-    int *xexp = reinterpret_cast<int *>(reinterpret_cast<char *>(n_units) + 256);
 
+    const size_t n = T * kD;
     cudaError_t err = traced("prefill_prep", c.stream, [&] {
-        k_prefill_prep<<<(unsigned)((T * 32 + 255) / 256), 256, 0, c.stream>>>(xh, xexp, p.y, p.x, (int)T);
+        k_prefill_prep<<<(unsigned)((n / 4 + 255) / 256), 256, 0, c.stream>>>(xh, p.y, p.x, n);
         k_prefill_units<<<1, 1024, 0, c.stream>>>(p.counts, p.offsets, units, n_units);
         return cudaGetLastError();
     });
@@ -598,7 +557,6 @@ cudaError_t launch_prefill(const Ctx &c, const PrefillArgs &p) {
     a.perm = p.perm;
     a.w = p.w;
     a.xh = xh;
-    a.xexp = xexp;
     a.H = H;
     a.y = p.y;
     a.status = c.status;
