@@ -596,7 +596,7 @@ constexpr int SMEM = 1024 + FIXED + S * STAGE;
 constexpr int SFA_COL = 2 * 2 * 8;               // accumulators [2][2][8] first
 constexpr int SFB_COL = SFA_COL + S * 16;
 constexpr int TMEM_COLS = 256;
-constexpr int NSEG = 2;                          // work segments: gate/up, down
+constexpr int NSEG = 4;                          // work segments: gate/up A, gate/up B, down A, down B
 constexpr int PARTIAL = 2 * 128;                 // floats per hand-over slot: the summed pieces
 constexpr int SYNC_HDONE = NSEG * kMaxGrid, SYNC_TILE = SYNC_HDONE + kK;   // after the segments' flags
 constexpr int SYNC_INTS = SYNC_TILE + 64;
@@ -607,7 +607,6 @@ static_assert(S >= 3 && S <= 10, "pipeline depth");
 static_assert(SFB_COL + (kD / 128) * 4 <= TMEM_COLS, "TMEM budget");
 static_assert(SMEM <= kSmemLimit, "shared memory budget");
 static_assert(kE * (int)sizeof(k3mx_expert) <= S * STAGE, "the expert table is staged in the ring");
-constexpr int PREFETCH = 12;                     // down stages pulled into L2 while h is pending
 }  // namespace f1
 
 __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
@@ -649,12 +648,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
     const uint32_t tmem = hd->tmem;
     volatile int *abort_flag = &hd->abort;
 
-    // Two work segments, every gate/up stage (unit-major) and then every
-    // down stage, each cut in equal stage ranges over the CTAs (stream-K)
-    // when there is enough work, else in whole items: every CTA runs its
-    // gate/up share, then its down share.  (Splitting the units into two
-    // halves run as gate/up A, gate/up B, down A, down B measured no faster:
-    // the extra short parts cost what the shorter wait for h saved.)
+    // Four work segments: the gate/up stages of the first half of the
+    // units (A), of the second half (B), then the down stages of A and of B,
+    // each cut in equal stage ranges over the CTAs (stream-K) when there is
+    // enough work, else in whole items.  Every CTA runs its share of each
+    // segment in that order, so the h of A is complete while the CTAs
+    // stream gate/up B, and the down parts of A start without waiting; by
+    // the time they reach down B, B's h is complete too.
     struct Sched {
         int gu, r0[NSEG], r1[NSEG], cum[NSEG + 1];
         bool sk;
@@ -664,8 +664,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
         const int GU = nu * MTG * KCG, GDn = nu * MTD * KCD;
         const int G = gridDim.x, B = blockIdx.x;
         sc.gu = GU;
-        sc.sk = a.partials != nullptr && GU >= G * (KCG + 1) && GDn >= G * (KCD + 1);
-        const int st[NSEG] = {0, GU}, len[NSEG] = {GU, GDn}, kc[NSEG] = {KCG, KCD};
+        const int nA = (nu + 1) / 2;
+        const int GA = nA * MTG * KCG, DA = nA * MTD * KCD;
+        sc.sk = a.partials != nullptr && GA >= G * (KCG + 1) && DA >= G * (KCD + 1);
+        const int st[NSEG] = {0, GA, GU, GU + DA}, len[NSEG] = {GA, GU - GA, DA, GDn - DA};
+        const int kc[NSEG] = {KCG, KCG, KCD, KCD};
         sc.cum[0] = 0;
 #pragma unroll
         for (int i = 0; i < NSEG; i++) {
@@ -751,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
     __syncthreads();
     const int n_units = s_nunits;
     if (n_units != MAX_UNITS) sc = plan(n_units);
-    const int nseg = 2;
+    const int nseg = NSEG;
     auto fail = [&](int detail) {
         report_status(a.status, kStatusWaitTimeout, detail);
         *abort_flag = 1;
@@ -814,11 +817,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
         int q = 0;
         uint32_t su = 0, bl = 0;
         bool x_first = false;            // epoch 0 held x (which overlaps both h buffers)
-        bool prefetched = false;
-        auto prefetch_down = [&](const uint8_t *m, int c, int mt) {
-            tma_prefetch_2d(m, (2 * c) * 128, mt * 128);
-            tma_prefetch_2d(m, (2 * c + 1) * 128, mt * 128);
-        };
         Part p;
         while (!*abort_flag && next_part(q, p)) {
             const Unit &u = p.u;
@@ -880,27 +878,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
                     nb = XB;
                     ns = XS;
                 } else {
-                    if (!prefetched) {
-                        // The pair's h may still be pending (the gate/up pass
-                        // drains unevenly over the CTAs): the next down
-                        // stages of this CTA, after those in the ring, go
-                        // into L2 meanwhile, so the weight stream does not
-                        // pause.
-                        prefetched = true;
-                        if (lane == 0) {
-                            int budget = PREFETCH, t = q;
-                            for (int c = p.lo + pre; c < p.hi && budget > 0; c++, budget--)
-                                prefetch_down(map0, c, p.mt);
-                            Part np;
-                            while (budget > 0 && next_part(t, np)) {
-                                if (np.ph != 1) continue;
-                                const uint8_t *m = a.maps + ((size_t)np.u.e * kMapsPerExpert + 2) * kMapBytes;
-                                acquire_map(m);
-                                for (int c = np.lo; c < np.hi && budget > 0; c++, budget--) prefetch_down(m, c, np.mt);
-                            }
-                        }
-                        __syncwarp();
-                    }
                     // the pair's h: every gate/up item of the pair has written its block
                     const int pair = (int)key;
                     const int *cnt = a.sync + SYNC_HDONE + (a.experts == nullptr ? 0 : pair % kK);
