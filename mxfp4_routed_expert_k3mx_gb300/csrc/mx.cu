@@ -1316,7 +1316,7 @@ cudaError_t launch_mx_ximg(const Ctx &c, const void *x, int x_bf16, int n_tokens
     const long long warps = (long long)n_tokens * (kD / 32);
     const int piece_ctas = (int)((warps + 7) / 8);
     const int n_map_experts = one != nullptr ? 1 : kE;
-    const int map_ctas = (n_map_experts * kMapsPerExpert + 7) / 8;
+    const int map_ctas = (n_map_experts * kMapsPerExpert + kMapsPerCta - 1) / kMapsPerCta;
     const k3mx_expert single = one != nullptr ? *one : k3mx_expert{};
     k_mx_ximg<<<(unsigned)(piece_ctas + map_ctas), 256, 0, c.stream>>>(
         x, x_bf16, n_tokens, ximg, reinterpret_cast<int *>(sk), sk != nullptr ? mx_streamk_flag_count() : 0, piece_ctas,

@@ -906,7 +906,7 @@ cudaError_t launch_prefill_mx(const Ctx &c, const PrefillArgs &p) {
 
     cudaError_t err = traced("prefill_prep", c.stream, [&] {
         k_px_units<<<1, 1024, 0, c.stream>>>(p.counts, p.offsets, units, n_units, slot_of_pair, (int)S);
-        const int map_ctas = (kE * kMapsPerExpert + 7) / 8;
+        const int map_ctas = (kE * kMapsPerExpert + kMapsPerCta - 1) / kMapsPerCta;
         k_px_slots<<<(unsigned)(U + map_ctas), 256, 0, c.stream>>>(units, n_units, p.perm, slot_un, slot_of_pair, U,
                                                                      maps, p.experts, w13, w2);
         const long long threads = (long long)p.n_tokens * (kD / 32);

@@ -716,7 +716,7 @@ cudaError_t launch_route_prep(const Ctx &c, int32_t *idx, float *w, const float 
     int map_ctas = 0;
     if (maps != nullptr && experts != nullptr) {
         if (!weight_map_templates(w13, w2)) return cudaErrorNotSupported;
-        map_ctas = (kE * kMapsPerExpert + 7) / 8;
+        map_ctas = (kE * kMapsPerExpert + kMapsPerCta - 1) / kMapsPerCta;
     }
     GroupOut g{};
     if (g_one != nullptr && n_tokens == 1) g = *g_one;

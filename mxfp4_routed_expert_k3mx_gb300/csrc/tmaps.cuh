@@ -59,18 +59,26 @@ __device__ __forceinline__ void acquire_map(const void *map) {
     // delayed the next acquire and that copy by about 0.7 us each)
 }
 
-// Warps of the map-building CTAs (8 warps each, 1 KB of static shared
-// memory): warp w of CTA b builds map b * 8 + w of n_experts * 3.  `table`
-// is the device expert table, or nullptr with `one` as expert 0.
+// Map-building CTAs: 8 warps (1 KB of static shared memory), each warp
+// building kMapsPerWarp maps one after another, so few CTAs (and SMs) are
+// taken: warp w of CTA b builds maps (8 b + w) * kMapsPerWarp + j of
+// n_experts * 3.  `table` is the device expert table, or nullptr with `one`
+// as expert 0.
+constexpr int kMapsPerWarp = 8;
+constexpr int kMapsPerCta = 8 * kMapsPerWarp;
 __device__ __forceinline__ void build_maps_cta(uint8_t *maps, int n_experts, const k3mx_expert *table,
                                                const k3mx_expert &one, const CUtensorMap &w13,
                                                const CUtensorMap &w2, int cta) {
     __shared__ __align__(128) uint8_t stage[8][kMapBytes];
     const int warp = threadIdx.x >> 5;
-    const int i = cta * 8 + warp;
-    if (warp >= 8 || i >= n_experts * kMapsPerExpert) return;
-    const k3mx_expert ex = table != nullptr ? table[i / kMapsPerExpert] : one;
-    build_expert_map(maps, i, (uint32_t)__cvta_generic_to_shared(stage[warp]), ex, w13, w2);
+    if (warp >= 8) return;
+    for (int j = 0; j < kMapsPerWarp; j++) {
+        const int i = (cta * 8 + warp) * kMapsPerWarp + j;
+        if (i >= n_experts * kMapsPerExpert) return;
+        const k3mx_expert ex = table != nullptr ? table[i / kMapsPerExpert] : one;
+        build_expert_map(maps, i, (uint32_t)__cvta_generic_to_shared(stage[warp]), ex, w13, w2);
+        __syncwarp();                     // the staging slot is reused
+    }
 }
 
 }  // namespace k3mx
