@@ -15,6 +15,21 @@
  * k3mx_device_status().  Arguments are refused, never defaulted: a size or
  * pointer outside what a function documents returns an error code.
  *
+ * Kernels are launched as programmatic dependents of the kernel before them
+ * on the stream: each may start while that kernel finishes and waits for its
+ * results before it reads an input.  The bf16 weight matrices of
+ * k3mx_router and k3mx_latent_moe are read before that wait (the first
+ * weight tiles go out while the kernel before ends), so they must not be
+ * written by the kernel launched immediately before the call on the same
+ * stream: put an event wait, a copy or another kernel between.  Every other
+ * argument may come from the kernel right before.
+ *
+ * Host threads: the library's one-time set-up per device (device
+ * properties, kernel attributes, tensor-map templates) is serialised
+ * internally, so first calls may come from several threads at once.  Calls
+ * that share a workspace, or the fixed array of k3mx_moe_decode_noalloc,
+ * must be ordered by the caller (one stream, or events between streams).
+ *
  * Weight format (Kimi K3 engine (c/kimi_k3.c), "Weights"): a matrix of
  * `rows` x `in` weights is two arrays, both row-major:
  *   packed [rows][in/2] bytes: e2m1 codes, two per byte, the LOW nibble is
@@ -66,7 +81,7 @@ enum {
     K3MX_PATH_AUTO = 0,       /* PREFILL_MX when x is bf16 and n_tokens >= K3MX_PREFILL_MIN_TOKENS, else DECODE */
     K3MX_PATH_DECODE = 1,     /* fp32 activations; x and h as 8 MXFP4 pieces, kind::mxf4 MMAs   */
     K3MX_PATH_PREFILL = 2,    /* bf16 activations; weights dequantised to f16, kind::f16 MMAs   */
-    K3MX_PATH_PREFILL_MX = 3  /* bf16 activations; x and h as 4 MXFP4 pieces, kind::mxf4 MMAs   */
+    K3MX_PATH_PREFILL_MX = 3  /* bf16 activations; x as 6, h as 4 MXFP4 pieces, kind::mxf4 MMAs */
 };
 #define K3MX_PREFILL_MIN_TOKENS 256
 #define K3MX_MAX_TOKENS         65536
@@ -251,8 +266,9 @@ k3mx_status k3mx_group(int32_t *counts, int32_t *offsets, int32_t *perm,
  * PREFILL converts x (bf16) to f16, dequantises the
  * weights to f16, rounds h to f16 and multiplies f16 x f16 on the tensor
  * cores with fp32 accumulation: per-token relative L2 error within 1e-2.
- * PREFILL_MX splits x and h (h from a hardware-tanh SiTU) into four MXFP4
- * pieces per 32-column block (residual below 4^-4 of the block's largest
+ * PREFILL_MX splits x into six and h (from a hardware-tanh SiTU, staged as
+ * f16 under a power-of-two scale per 32-column block) into four MXFP4
+ * pieces per 32-column block (residual below 4^-6, resp. 4^-4, of the block's largest
  * value) and multiplies them with the weights as stored on the
  * block-scaled tensor cores with fp32 accumulation: per-token relative L2
  * error within 1e-2 (about 3e-4 on the synthetic workload).  DECODE is

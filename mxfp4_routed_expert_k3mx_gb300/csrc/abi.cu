@@ -17,7 +17,7 @@ __device__ int g_status[4];       // [0] first failure code, [1] detail
 
 constexpr int kMaxDevices = 64;
 struct DevInfo {
-    bool init;
+    std::atomic<bool> init;               // set last, after the fields below
     bool ok;
     int num_sms;
     int *status;
@@ -30,18 +30,21 @@ k3mx_status device_ctx(cudaStream_t stream, Ctx &c) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return K3MX_ECUDA;
     DevInfo &di = g_dev[dev];
-    if (!di.init) {
-        int major = 0, minor = 0, sms = 0;
-        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return K3MX_ECUDA;
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return K3MX_ECUDA;
-        di.ok = (major == 10 && minor == 3);
-        di.num_sms = sms;
-        di.status = static_cast<int *>(p);
-        di.init = true;
+    if (!di.init.load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(setup_mutex());
+        if (!di.init.load(std::memory_order_relaxed)) {
+            int major = 0, minor = 0, sms = 0;
+            if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+                return K3MX_ECUDA;
+            void *p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return K3MX_ECUDA;
+            di.ok = (major == 10 && minor == 3);
+            di.num_sms = sms;
+            di.status = static_cast<int *>(p);
+            di.init.store(true, std::memory_order_release);
+        }
     }
     if (!di.ok) return K3MX_EDEVICE;
     c.stream = stream;
@@ -58,21 +61,44 @@ k3mx_status device_ctx(cudaStream_t stream, Ctx &c) {
 // before it reads it, so nothing here needs clearing between calls.
 constexpr size_t kNoallocBytes = size_t(8) << 20;
 __device__ __align__(256) unsigned char g_noalloc_ws[kNoallocBytes];
-void *g_noalloc_ptr[kMaxDevices];
+std::atomic<void *> g_noalloc_ptr[kMaxDevices];
 
 }  // namespace
+
+std::mutex &setup_mutex() {
+    static std::mutex m;
+    return m;
+}
+
+cudaError_t ensure_smem(const void *fn, int bytes, std::atomic<uint64_t> &done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    const uint64_t bit = uint64_t(1) << dev;
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(setup_mutex());
+    if (done.load(std::memory_order_relaxed) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
 
 // Device address of the library's fixed scratch array on the current device
 // (looked up once per device), or nullptr.
 void *library_scratch() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    if (!g_noalloc_ptr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_ws) != cudaSuccess) return nullptr;
-        g_noalloc_ptr[dev] = p;
+    void *p = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+        std::lock_guard<std::mutex> lock(setup_mutex());
+        p = g_noalloc_ptr[dev].load(std::memory_order_relaxed);
+        if (p == nullptr) {
+            if (cudaGetSymbolAddress(&p, g_noalloc_ws) != cudaSuccess) return nullptr;
+            g_noalloc_ptr[dev].store(p, std::memory_order_release);
+        }
     }
-    return g_noalloc_ptr[dev];
+    return p;
 }
 size_t library_scratch_bytes() { return kNoallocBytes; }
 

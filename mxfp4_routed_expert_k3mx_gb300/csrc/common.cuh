@@ -2,8 +2,10 @@
 // the sm_103a kernels of the MXFP4 routed-expert layer.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
@@ -350,6 +352,16 @@ cudaError_t set_wait_polls_px(uint32_t polls);
 cudaError_t set_wait_polls_prefill(uint32_t polls);
 cudaError_t set_wait_polls_decode(uint32_t polls);
 cudaError_t set_wait_polls_dense(uint32_t polls);
+
+// Host side.  The library's lazily filled per-device state (device
+// properties, CUDA function attributes, tensor-map templates, the fixed
+// scratch array's address) is set up under one lock, with a flag read
+// without the lock afterwards, so first calls from several host threads
+// are safe.
+std::mutex &setup_mutex();
+// cudaFuncSetAttribute(max dynamic shared memory) once per kernel and
+// device; `done` holds one bit per device
+cudaError_t ensure_smem(const void *fn, int bytes, std::atomic<uint64_t> &done);
 
 // The library's fixed device scratch array (abi.cu): its address on the
 // current device, looked up on first use, and its size.

@@ -19,6 +19,7 @@
 
 #include "common.cuh"
 #include "dense.cuh"
+#include "tmaps.cuh"
 
 namespace k3mx {
 namespace {
@@ -542,22 +543,9 @@ __global__ void __launch_bounds__(256) k_rmsnorm_bf16(const float *__restrict__ 
     }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 dense_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (fn == nullptr) {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    }
-    return fn;
-}
-
 // bf16 [rows][K] row-major, boxes of box_rows x 64 (128 bytes, 128-byte swizzle)
 bool encode_bf16_rows(CUtensorMap &m, const void *base, int K, uint64_t rows, uint32_t box_rows) {
-    auto enc = dense_encoder();
+    auto enc = tensor_map_encoder();
     if (enc == nullptr) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)K, rows}, strides[1] = {(cuuint64_t)K * 2};
     const cuuint32_t box[2] = {(cuuint32_t)kGK, box_rows}, es[2] = {1, 1};
@@ -566,18 +554,10 @@ bool encode_bf16_rows(CUtensorMap &m, const void *base, int K, uint64_t rows, ui
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename F>
-cudaError_t configure_once(F kernel, int smem, bool &done) {
-    if (done) return cudaSuccess;
-    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e == cudaSuccess) done = true;
-    return e;
-}
-
 template <int K, int XF>
 cudaError_t gemv_t(const Ctx &c, const GemvArgs &a) {
-    static bool done = false;
-    const cudaError_t e = configure_once(k_gemv<K, XF>, GemvShape<K>::SMEM_MAX, done);
+    static std::atomic<uint64_t> done{0};
+    const cudaError_t e = ensure_smem((const void *)k_gemv<K, XF>, GemvShape<K>::SMEM_MAX, done);
     if (e != cudaSuccess) return e;
     const int chunk = a.n_tokens < kGemvTok ? a.n_tokens : kGemvTok;
     // one CTA per SM, at least 4 rows each
@@ -591,8 +571,8 @@ cudaError_t gemv_t(const Ctx &c, const GemvArgs &a) {
 template <int K, bool ADD>
 cudaError_t gemm_t(const Ctx &c, const uint16_t *W, const uint16_t *W2, int rows, const uint16_t *x,
                    const GemmOut &o) {
-    static bool done = false;
-    const cudaError_t e = configure_once(k_gemm<K, ADD>, kGSmem, done);
+    static std::atomic<uint64_t> done{0};
+    const cudaError_t e = ensure_smem((const void *)k_gemm<K, ADD>, kGSmem, done);
     if (e != cudaSuccess) return e;
     CUtensorMap wm, wm2, xm;
     const int rows2 = rows - o.m_split;

@@ -1195,13 +1195,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
 template <int PH, int NTOK>
 cudaError_t launch_mx_t(const Ctx &c, MxArgs a, bool pdl) {
     using Sh = MxShape<PH, NTOK>;
-    static bool configured = false;
-    if (!configured) {
-        const cudaError_t e =
-            cudaFuncSetAttribute(k_mx<PH, NTOK>, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static std::atomic<uint64_t> configured{0};
+    const cudaError_t e = ensure_smem((const void *)k_mx<PH, NTOK>, Sh::SMEM, configured);
+    if (e != cudaSuccess) return e;
     a.status = c.status;
     int grid = c.num_sms < kMaxGrid ? c.num_sms : kMaxGrid;
     cudaLaunchConfig_t cfg{};
@@ -1232,39 +1228,51 @@ MxArgs mx_args(const DecodeExperts &d) {
 
 }  // namespace
 
+// The driver entry point, resolved once (a function-local static, so the
+// first calls from several threads are safe).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        const bool ok = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                                         &q) == cudaSuccess &&
+                        q == cudaDriverEntryPointSuccess;
+        return ok ? reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f) : nullptr;
+    }();
+    return fn;
+}
+
 // Tensor-map templates (tmaps.cuh), encoded once per device.  They point at
 // the library's own scratch array (larger than one matrix), so a map is
 // never left pointing at memory that is not allocated.
 bool weight_map_templates(CUtensorMap &w13, CUtensorMap &w2) {
     constexpr int kDevs = 64;
-    static int state[kDevs];              // 0 not tried, 1 ok, 2 failed
+    static std::atomic<int> state[kDevs];  // 0 not tried, 1 ok, 2 failed
     static CUtensorMap t13[kDevs], t2[kDevs];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) return false;
-    if (state[dev] == 0) {
-        state[dev] = 2;
-        void *fn = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        void *base = library_scratch();
-        if (base != nullptr && library_scratch_bytes() >= (size_t)kD / 2 * kF &&
-            library_scratch_bytes() >= (size_t)kF / 2 * kD &&
-            cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess && fn != nullptr) {
-            auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-            const cuuint32_t box[2] = {128, 128}, es[2] = {1, 1};
-            const cuuint64_t d13[2] = {(cuuint64_t)kD / 2, (cuuint64_t)kF}, s13[1] = {(cuuint64_t)kD / 2};
-            const cuuint64_t d2[2] = {(cuuint64_t)kF / 2, (cuuint64_t)kD}, s2[1] = {(cuuint64_t)kF / 2};
-            const CUresult r1 = enc(&t13[dev], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, d13, s13, box, es,
-                                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-            const CUresult r2 = enc(&t2[dev], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, d2, s2, box, es,
-                                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-            if (r1 == CUDA_SUCCESS && r2 == CUDA_SUCCESS) state[dev] = 1;
+    if (state[dev].load(std::memory_order_acquire) == 0) {
+        void *base = library_scratch();   // takes the set-up lock itself
+        auto enc = tensor_map_encoder();
+        std::lock_guard<std::mutex> lock(setup_mutex());
+        if (state[dev].load(std::memory_order_relaxed) == 0) {
+            bool ok = base != nullptr && enc != nullptr && library_scratch_bytes() >= (size_t)kD / 2 * kF &&
+                      library_scratch_bytes() >= (size_t)kF / 2 * kD;
+            if (ok) {
+                const cuuint32_t box[2] = {128, 128}, es[2] = {1, 1};
+                const cuuint64_t d13[2] = {(cuuint64_t)kD / 2, (cuuint64_t)kF}, s13[1] = {(cuuint64_t)kD / 2};
+                const cuuint64_t d2[2] = {(cuuint64_t)kF / 2, (cuuint64_t)kD}, s2[1] = {(cuuint64_t)kF / 2};
+                ok = enc(&t13[dev], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, d13, s13, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS &&
+                     enc(&t2[dev], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, d2, s2, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            }
+            state[dev].store(ok ? 1 : 2, std::memory_order_release);
         }
     }
-    if (state[dev] != 1) return false;
+    if (state[dev].load(std::memory_order_acquire) != 1) return false;
     w13 = t13[dev];
     w2 = t2[dev];
     return true;
@@ -1279,12 +1287,9 @@ constexpr size_t kSkPartBytes = (size_t)f1::NSEG * kMaxGrid * f1::PARTIAL * size
 }  // namespace
 cudaError_t launch_mx_fused1(const Ctx &c, const DecodeExperts &d, const uint8_t *ximg, uint8_t *himg, float *gu,
                              float *stage, const float *w, float *y, const uint8_t *maps, uint8_t *sk) {
-    static bool configured = false;
-    if (!configured) {
-        const cudaError_t e = cudaFuncSetAttribute(k_mx1, cudaFuncAttributeMaxDynamicSharedMemorySize, f1::SMEM);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static std::atomic<uint64_t> configured{0};
+    const cudaError_t e = ensure_smem((const void *)k_mx1, f1::SMEM, configured);
+    if (e != cudaSuccess) return e;
     MxArgs a = mx_args(d);
     a.img_in = ximg;
     a.img_out = himg;

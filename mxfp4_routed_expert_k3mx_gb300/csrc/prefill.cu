@@ -506,12 +506,9 @@ size_t prefill_smem() {
 template <int PH>
 cudaError_t launch_phase(const Ctx &c, const PArgs &a, long long max_items) {
     const size_t smem = prefill_smem<PH>();
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(k_prefill<PH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static std::atomic<uint64_t> configured{0};
+    const cudaError_t e = ensure_smem((const void *)k_prefill<PH>, (int)smem, configured);
+    if (e != cudaSuccess) return e;
     long long grid = c.num_sms;
     if (grid > max_items) grid = max_items;
     k_prefill<PH><<<(unsigned)grid, kThreads, smem, c.stream>>>(a);

@@ -773,34 +773,18 @@ k_px_xprep(const uint16_t *__restrict__ x, int n_tokens, const int32_t *__restri
 template <int PH>
 cudaError_t launch_px_t(const Ctx &c, const PxArgs &a, const PxBMaps &bmaps, long long max_items) {
     using Sh = PxShape<PH>;
-    static bool configured = false;
-    if (!configured) {
-        const cudaError_t e = cudaFuncSetAttribute(k_px<PH>, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static std::atomic<uint64_t> configured{0};
+    const cudaError_t e = ensure_smem((const void *)k_px<PH>, Sh::SMEM, configured);
+    if (e != cudaSuccess) return e;
     long long grid = c.num_sms;
     if (grid > max_items) grid = max_items;
     if (grid < 1) grid = 1;
     return launch_pdl(k_px<PH>, dim3((unsigned)grid), dim3(kPxThreads), (size_t)Sh::SMEM, c.stream, a, bmaps);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (fn == nullptr) {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    }
-    return fn;
-}
-
 // 2-D uint8 map: rows x row_bytes, boxes of box_rows x 64 bytes, 64-byte swizzle
 bool encode_sw64(CUtensorMap &m, const void *base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
-    auto enc = tmap_encoder();
+    auto enc = tensor_map_encoder();
     if (enc == nullptr) return false;
     const cuuint64_t dims[2] = {row_bytes, rows}, strides[1] = {row_bytes};
     const cuuint32_t box[2] = {64, box_rows}, es[2] = {1, 1};
@@ -814,18 +798,21 @@ bool encode_sw64(CUtensorMap &m, const void *base, uint64_t row_bytes, uint64_t 
 // a template; the device replaces it per expert)
 bool px_weight_templates(CUtensorMap &w13, CUtensorMap &w2) {
     constexpr int kDevs = 64;
-    static int state[kDevs];
+    static std::atomic<int> state[kDevs];  // 0 not tried, 1 ok, 2 failed
     static CUtensorMap t13[kDevs], t2[kDevs];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) return false;
-    if (state[dev] == 0) {
-        state[dev] = 2;
+    if (state[dev].load(std::memory_order_acquire) == 0) {
         void *base = library_scratch();
-        if (base != nullptr && library_scratch_bytes() >= (size_t)kD / 2 * kF &&
-            encode_sw64(t13[dev], base, kD / 2, kF, 128) && encode_sw64(t2[dev], base, kF / 2, kD, 128))
-            state[dev] = 1;
+        std::lock_guard<std::mutex> lock(setup_mutex());
+        if (state[dev].load(std::memory_order_relaxed) == 0) {
+            const bool ok = base != nullptr && library_scratch_bytes() >= (size_t)kD / 2 * kF &&
+                            encode_sw64(t13[dev], base, kD / 2, kF, 128) &&
+                            encode_sw64(t2[dev], base, kF / 2, kD, 128);
+            state[dev].store(ok ? 1 : 2, std::memory_order_release);
+        }
     }
-    if (state[dev] != 1) return false;
+    if (state[dev].load(std::memory_order_acquire) != 1) return false;
     w13 = t13[dev];
     w2 = t2[dev];
     return true;
@@ -835,7 +822,7 @@ bool px_weight_templates(CUtensorMap &w13, CUtensorMap &w2) {
 // 64 bytes x box_rows rows x all planes, 64-byte swizzle
 bool encode_planes(CUtensorMap &m, const void *base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows,
                    int planes) {
-    auto enc = tmap_encoder();
+    auto enc = tensor_map_encoder();
     if (enc == nullptr) return false;
     const cuuint64_t dims[3] = {row_bytes, rows, (cuuint64_t)planes}, strides[2] = {row_bytes, row_bytes * rows};
     const cuuint32_t box[3] = {64, box_rows, (cuuint32_t)planes}, es[3] = {1, 1, 1};

@@ -10,6 +10,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "common.cuh"
 
@@ -17,6 +18,10 @@ namespace k3mx {
 
 constexpr int kMapBytes = 128;
 constexpr int kMapsPerExpert = 3;        // w1, w3, w2
+
+// the driver's cuTensorMapEncodeTiled, looked up once per process
+// (nullptr when unavailable)
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 // templates for the current device (encoded once per device); false when
 // the driver entry point or the encoding is unavailable
