@@ -65,7 +65,7 @@ typedef struct CUstream_st *k3mx_stream_t;
 typedef enum k3mx_status {
     K3MX_OK = 0,
     K3MX_EINVAL = 1,      /* NULL pointer, unknown enum value              */
-    K3MX_EALIGN = 2,      /* a pointer is not 16-byte aligned              */
+    K3MX_EALIGN = 2,      /* a pointer is not aligned as required          */
     K3MX_ESHAPE = 3,      /* a size outside the documented range           */
     K3MX_EWORKSPACE = 4,  /* workspace NULL or smaller than required       */
     K3MX_ECUDA = 5,       /* a CUDA runtime call or a launch failed        */
@@ -81,7 +81,7 @@ enum {
     K3MX_PATH_AUTO = 0,       /* PREFILL_MX when x is bf16 and n_tokens >= K3MX_PREFILL_MIN_TOKENS, else DECODE */
     K3MX_PATH_DECODE = 1,     /* fp32 activations; x and h as 8 MXFP4 pieces, kind::mxf4 MMAs   */
     K3MX_PATH_PREFILL = 2,    /* bf16 activations; weights dequantised to f16, kind::f16 MMAs   */
-    K3MX_PATH_PREFILL_MX = 3  /* bf16 activations; x as 6, h as 4 MXFP4 pieces, kind::mxf4 MMAs */
+    K3MX_PATH_PREFILL_MX = 3  /* bf16 activations; x, h as 2 MXFP8 pieces, kind::mxf8f6f4 MMAs */
 };
 #define K3MX_PREFILL_MIN_TOKENS 256
 #define K3MX_MAX_TOKENS         65536
@@ -91,7 +91,11 @@ enum {
  * "Streaming design": the six tensors of an expert; "Architecture notes":
  * GLU experts, inter 3072, in the 3584 latent).  w1 (gate) and w3 (up) are
  * [F x D] = [3072 x 3584]; w2 (down) is [D x F] = [3584 x 3072].  Each
- * pointer must be 16-byte aligned.
+ * pointer must be 16-byte aligned; the PREFILL_MX path of k3mx_moe_routed
+ * (and AUTO from K3MX_PREFILL_MIN_TOKENS bf16 tokens) also needs w1, w3
+ * and w2 32-byte aligned.  The table lives in device memory, so a violation
+ * is found there: the expert's pairs are skipped and k3mx_device_status
+ * reports K3MX_EALIGN with the expert's index.
  */
 typedef struct k3mx_expert {
     const uint8_t *w1, *s1;     /* gate: packed [F][D/2], scales [F][D/32] */
@@ -266,11 +270,12 @@ k3mx_status k3mx_group(int32_t *counts, int32_t *offsets, int32_t *perm,
  * PREFILL converts x (bf16) to f16, dequantises the
  * weights to f16, rounds h to f16 and multiplies f16 x f16 on the tensor
  * cores with fp32 accumulation: per-token relative L2 error within 1e-2.
- * PREFILL_MX splits x into six and h (from a hardware-tanh SiTU, staged as
- * f16 under a power-of-two scale per 32-column block) into four MXFP4
- * pieces per 32-column block (residual below 4^-6, resp. 4^-4, of the block's largest
- * value) and multiplies them with the weights as stored on the
- * block-scaled tensor cores with fp32 accumulation: per-token relative L2
+ * PREFILL_MX splits x and h (h from a hardware-tanh SiTU, staged as f16
+ * under a power-of-two scale per 32-column block) into two MXFP8 (e4m3)
+ * pieces per 32-column block (two pieces reproduce a bf16 x exactly, and h
+ * to about 2^-9 of each value) and multiplies them with the weights as
+ * stored (e2m1 codes and ue8m0 scales, kind::mxf8f6f4) with fp32
+ * accumulation: per-token relative L2
  * error within 1e-2 (about 3e-4 on the synthetic workload).  DECODE is
  * deterministic; both prefill paths add the 16 expert contributions of a
  * token with fp32 atomics, so the order of those adds, and the last bits

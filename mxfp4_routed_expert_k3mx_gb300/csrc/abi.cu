@@ -385,7 +385,7 @@ const char *k3mx_status_str(k3mx_status s) {
     switch (s) {
     case K3MX_OK: return "ok";
     case K3MX_EINVAL: return "invalid argument";
-    case K3MX_EALIGN: return "pointer not 16-byte aligned";
+    case K3MX_EALIGN: return "pointer not aligned as required";
     case K3MX_ESHAPE: return "size out of range";
     case K3MX_EWORKSPACE: return "workspace missing or too small";
     case K3MX_ECUDA: return "CUDA error";

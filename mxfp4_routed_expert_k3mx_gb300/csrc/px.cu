@@ -1,29 +1,30 @@
 // px.cu - prefill on block-scaled 5th-generation tensor-core MMAs
-// (tcgen05 kind::mxf4): the grouped expert GEMMs of many tokens with the
+// (tcgen05 kind::mxf8f6f4): the grouped expert GEMMs of many tokens with the
 // packed MXFP4 weights and their ue8m0 group scales fed to the tensor cores
-// exactly as stored (Kimi K3 engine (c/kimi_k3.c), "Weights"), with no
-// per-weight work in registers.
+// as stored (Kimi K3 engine (c/kimi_k3.c), "Weights"), with no per-weight
+// work in registers: the copy engine spreads each 16 packed e2m1 codes of a
+// weight tile over 16 bytes of shared memory (the operand layout this MMA
+// kind reads for 4-bit types), the codes themselves untouched.
 //
-// Activations.  kind::mxf4 multiplies e2m1 by e2m1, so every activation
-// row (x of a token for gate/up, h of a pair for down) is split into PP
-// MXFP4 pieces per 32-column block (pieces.cuh: piece i takes the scale
-// that maps the block's largest residual into (3, 6] and the nearest e2m1
-// value of every residual); PP pieces leave a residual below 4^-PP of the
-// block's largest value.  x takes six pieces: SiTU-GLU's gate turns an
-// absolute error of g into a large change of h where g is near 0, and with
-// four pieces a block holding one value 10^2-10^3 times the others leaves its
-// small values with two pieces' precision (layer errors up to 2e-2 in
-// simulation, below 4e-5 with six).  h (|h| <= 100, read linearly) takes
-// four.  The MMA sums the pieces itself: piece p of every token of a work
-// unit is one B operand, and the MMAs of a K step accumulate into the same
-// columns.
+// Activations.  The MMA multiplies e2m1 weights by e4m3 activations, so
+// every activation row (x of a token for gate/up, h of a pair for down) is
+// split into two MXFP8 (e4m3) pieces per 32-column block: piece i takes the
+// scale 2^e that maps the block's largest residual |value| into (224, 448]
+// and the nearest e4m3 value of every residual / 2^e; the next residual is
+// exact in fp32.  A piece keeps four significant bits of every value within
+// 2^15 of the block's largest (e4m3's exponent range), so two pieces
+// reproduce a bf16 x exactly in all but extreme blocks, and h (from an f16
+// staging copy, 11 bits) to about 2^-9 of each value.  The two pieces of
+// every pair of a work unit are one B operand side by side (N = 2 x the
+// unit's box rows); the epilogue adds the two accumulator halves.
 //
 // Work.  A unit is one expert and at most kUT of its (token, slot) pairs,
 // contiguous in the grouped order (Kimi K3 engine (c/kimi_k3.c), "Chunked
 // prefill": each unique expert is loaded once for all its tokens).  Item =
 // (unit, 128-row tile); a CTA per SM takes every grid-th item.  Per
 // item K streams in 128-column stages:
-//   warp 0      A producer: TMA of the weight tiles (128 rows x 64 B, 64-byte
+//   warp 0      A producer: TMA of the weight tiles (128 rows x 128 codes:
+//               64 B each in global memory, 128 B in shared memory, 128-byte
 //               swizzle) through per-expert tensor maps into an A ring
 //   warp 1      scale loader: the tile's scale bytes (16 per row, four
 //               stages ahead) from global into registers, then per stage the
@@ -31,11 +32,11 @@
 //               255 gets scale 0 and its codes are zeroed once the tile has
 //               landed, so it adds exactly 0
 //   warp 2      TMEM owner; lane 0 copies the scale atoms to TMEM and issues,
-//               per stage, 2 K steps x PP / 2 piece pairs x NMAT MMAs (M = 128,
-//               N = the unit's tokens rounded up to 16, K = 64)
-//   warp 3      B producer: one 3-D TMA per stage for all pieces of the
-//               unit's rows (box of 16, 32, ..., 96 rows) and one bulk copy
-//               of the stage's B scale atoms into a B ring
+//               per stage, 4 K steps x NMAT MMAs (M = 128, N = 2 x the unit's
+//               box rows, K = 32)
+//   warp 3      B producer: one 3-D TMA per stage for both pieces of the
+//               unit's rows (box of 16, 32, ..., 96 rows x 128 B) and one
+//               bulk copy of the stage's B scale atoms into a B ring
 //   warps 4-11  epilogue, two warps per TMEM lane quarter, each half the
 //               unit's tokens: gate/up h = SiTU(g, u) split into pieces
 //               (rows of the grouped h planes + the unit's B scale atoms for
@@ -54,12 +55,13 @@
 namespace k3mx {
 namespace {
 
-constexpr int kPPx = 6;                 // pieces of x (gate/up's B)
-constexpr int kPPh = 4;                 // pieces of h (down's B)
-constexpr int kUT = 96;                 // pairs per unit (MMA N <= 96)
-constexpr int kKS = 128;                // K columns per stage (64 packed bytes per row)
-constexpr int kATile = 128 * 64;        // A tile: 128 rows x 64 B
-constexpr int kBPiece = kUT * 64;       // one piece of the unit's B: 96 rows x 64 B
+constexpr int kPPx = 2;                 // e4m3 pieces of x (gate/up's B)
+constexpr int kPPh = 2;                 // e4m3 pieces of h (down's B)
+constexpr int kUT = 96;                 // pairs per unit (MMA N = 2 x rows <= 192)
+constexpr int kKS = 128;                // K columns per stage
+constexpr int kATile = 128 * 128;       // A tile in shared memory: 128 rows x 128 B (expanded codes)
+constexpr int kATx = 128 * 64;          // the bytes one A tile copy moves (packed codes)
+constexpr int kBPiece = kUT * 128;      // one piece of the unit's B: 96 rows x 128 B (e4m3)
 constexpr int kBoxes = kUT / 16;
 __host__ __device__ constexpr int b_rows(int i) { return 16 * (i + 1); }   // B box heights: 16, 32, ..., 96
 // the B box of a unit of n pairs: the smallest height holding them
@@ -77,10 +79,10 @@ constexpr int kPxSmemLimit = 227 * 1024;
 
 template <int PH> struct PxCfg;
 template <> struct PxCfg<0> {           // gate/up: g = W1 x, u = W3 x
-    static constexpr int NMAT = 2, K = kD, M = kF, SA = 4, SB = 3, PP = kPPx;
+    static constexpr int NMAT = 2, K = kD, M = kF, SA = 3, SB = 3, PP = kPPx;
 };
 template <> struct PxCfg<1> {           // down: Y = W2 h
-    static constexpr int NMAT = 1, K = kF, M = kD, SA = 6, SB = 6, PP = kPPh;
+    static constexpr int NMAT = 1, K = kF, M = kD, SA = 6, SB = 4, PP = kPPh;
 };
 
 template <int PH> struct PxShape {
@@ -88,7 +90,7 @@ template <int PH> struct PxShape {
     static constexpr int NMAT = C::NMAT, K = C::K, M = C::M, SA = C::SA, SB = C::SB, PP = C::PP;
     static constexpr int KC = K / kKS, MT = M / 128, G = K / 32;
     static constexpr int ASTAGE = ((NMAT * (kATile + kAtomB)) + 1023) / 1024 * 1024;
-    static constexpr int BSTAGE = PP * kBPiece + PP * kAtomB;            // 39 KB (x), 26 KB (h)
+    static constexpr int BSTAGE = PP * kBPiece + PP * kAtomB;            // 25 KB
     // gate/up: per epilogue warp two rounds of h, 32 tokens x 32 features
     // in f16 (rows of 17 words: conflict-free both ways), to turn (feature,
     // token) into (token, feature); a token's 32 values are scaled by a
@@ -98,11 +100,11 @@ template <int PH> struct PxShape {
     static constexpr int TROW = 68;
     static constexpr int TRANS = PH == 0 ? 8 * 2 * 32 * TROW : 0;
     static constexpr int SMEM = 1024 + 1024 + SA * ASTAGE + SB * BSTAGE + TRANS;  // alignment slack, header
-    // Two pieces side by side in one B operand (N = 2 x the box rows): MMAs
-    // per K step halve, and each accumulator holds an even-piece and an
-    // odd-piece half that the epilogue adds.  Gate/up's two matrices leave
-    // TMEM for one accumulator buffer: its epilogue releases the buffer as
-    // soon as h is staged in shared memory.
+    // The two pieces side by side in one B operand (N = 2 x the box rows):
+    // each accumulator holds a piece-0 and a piece-1 half that the epilogue
+    // adds.  Gate/up's two matrices leave TMEM for one accumulator buffer:
+    // its epilogue releases the buffer as soon as h is staged in shared
+    // memory.
     static constexpr int NACC = 2 * kUT;                       // accumulator columns per matrix
     static constexpr int NBUF = PH == 0 ? 1 : 2;
     // TMEM: accumulators [NBUF][NMAT][NACC], A scales [SA][NMAT][4], B scales [SB][PP][4]
@@ -111,7 +113,7 @@ template <int PH> struct PxShape {
     static constexpr int SFB_COL = SFA_COL + SA * NMAT * 4;
     static constexpr int TMEM_COLS = 512;
     static_assert(SFB_COL + SB * PP * 4 <= TMEM_COLS, "TMEM budget");
-    static_assert(PP % 2 == 0, "pieces go two to an operand");
+    static_assert(PP == 2, "the two pieces form one operand");
     static_assert(SMEM <= kPxSmemLimit, "shared memory budget");
     static_assert(K % (4 * kKS) == 0, "scale rows load in 16-byte groups of four stages");
     static_assert(ASTAGE % 1024 == 0 && BSTAGE % 1024 == 0, "stage alignment");
@@ -125,7 +127,7 @@ struct PxArgs {
     const uint8_t *maps;           // per-expert weight tensor maps [expert][w1, w3, w2]
     const k3mx_expert *experts;    // device table [896]
     const uint8_t *b_atoms;        // B scale atoms of the pass's input [unit][KC][PP][512]
-    uint8_t *h_planes;             // gate/up: h pieces [kPPh][slots][F / 2]
+    uint8_t *h_planes;             // gate/up: h pieces [kPPh][slots][F] (e4m3)
     uint8_t *h_atoms;              // gate/up: down's B scale atoms [unit][F / 128][kPPh][512]
     size_t slots;                  // 16 T: rows of one piece plane
     float *y;                      // down: [T][D], accumulated
@@ -153,14 +155,14 @@ __device__ __forceinline__ float situ_fast(float g, float u) {
     return (4.0f * tanh_hw(0.25f * g) * sg) * (25.0f * tanh_hw(u * 0.04f));
 }
 
-// The NP pieces of 32 values held by one lane (v, column order): piece p
-// takes the scale 2^e that maps the largest remaining |v| into (3, 6] and the
-// nearest e2m1 code of every v / 2^e (hardware conversion, two columns per
-// byte, the even column in the low nibble); v keeps the exact residual.
-// words[p] are the piece's 16 packed bytes, scale[p] its ue8m0 byte (255
-// when the values hold Inf or NaN; 0, with nothing taken, below 2^-124).
+// The NP MXFP8 pieces of 32 values held by one lane (v, column order):
+// piece p takes the scale 2^e that maps the largest remaining |v| into
+// (224, 448] (2^-126 at least) and the nearest e4m3 value of every v / 2^e
+// (hardware conversion, column j in byte j); v keeps the exact residual.
+// bytes[p] are the piece's 32 bytes, scale[p] its ue8m0 byte (255 when the
+// values hold Inf or NaN, with zero bytes; 0 when they are all zero).
 template <int NP>
-__device__ __forceinline__ void lane_pieces(float (&v)[32], uint4 (&words)[NP], uint32_t (&scale)[NP]) {
+__device__ __forceinline__ void lane_pieces_e4m3(float (&v)[32], uint4 (&bytes)[NP][2], uint32_t (&scale)[NP]) {
 #pragma unroll
     for (int p = 0; p < NP; p++) {
         // the largest |v| (non-negative floats order as their bit patterns;
@@ -169,30 +171,32 @@ __device__ __forceinline__ void lane_pieces(float (&v)[32], uint4 (&words)[NP], 
 #pragma unroll
         for (int j = 0; j < 32; j++) mb = max(mb, __float_as_uint(fabsf(v[j])));
         const int E = (int)(mb >> 23) - 127;
-        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
         uint32_t sb = 0;
         if (E == 128) {
             sb = 255;
-        } else if (E >= -124) {
-            const int e = (mb & 0x7FFFFFu) <= 0x400000u ? E - 2 : E - 1;   // max / 2^e in (3, 6]
+        } else if (mb != 0) {
+            // 448 = 1.75 x 2^8: max / 2^e in (224, 448]
+            const int e = max((mb & 0x7FFFFFu) <= 0x600000u ? E - 8 : E - 7, -126);
             const float down = exp2i(-e), up = exp2i(e);
 #pragma unroll
             for (int j = 0; j < 16; j++) {
-                uint32_t byte, h2;
-                asm("{\n\t.reg .b8 t;\n\t"
-                    "cvt.rn.satfinite.e2m1x2.f32 t, %2, %3;\n\t"
-                    "cvt.u32.u8 %0, t;\n\t"
-                    "cvt.rn.f16x2.e2m1x2 %1, t;\n\t}"
-                    : "=r"(byte), "=r"(h2)
+                uint32_t pair, h2;
+                asm("{\n\t.reg .b16 t;\n\t"
+                    "cvt.rn.satfinite.e4m3x2.f32 t, %2, %3;\n\t"
+                    "cvt.u32.u16 %0, t;\n\t"
+                    "cvt.rn.f16x2.e4m3x2 %1, t;\n\t}"
+                    : "=r"(pair), "=r"(h2)
                     : "f"(v[2 * j + 1] * down), "f"(v[2 * j] * down));
                 const float2 q = __half22float2(*reinterpret_cast<const __half2 *>(&h2));
                 v[2 * j] = fmaf(-q.x, up, v[2 * j]);             // exact
                 v[2 * j + 1] = fmaf(-q.y, up, v[2 * j + 1]);
-                w[j >> 2] |= (byte & 0xFFu) << (8 * (j & 3));
+                w[j >> 1] |= (pair & 0xFFFFu) << (16 * (j & 1));
             }
             sb = (uint32_t)(e + 127);
         }
-        words[p] = make_uint4(w[0], w[1], w[2], w[3]);
+        bytes[p][0] = make_uint4(w[0], w[1], w[2], w[3]);
+        bytes[p][1] = make_uint4(w[4], w[5], w[6], w[7]);
         scale[p] = sb;
     }
 }
@@ -208,8 +212,9 @@ __device__ __forceinline__ size_t atom_byte_pair(int unit, int kc_total, int c, 
            (size_t)(r & 31) * 16 + ((r >> 5) & 3) * 4 + kb4;
 }
 
-// an item's unit and whether its expert's pointers are usable (16-byte
-// aligned; the maps of another expert are never used)
+// an item's unit and whether its expert's pointers are usable (weights
+// 32-byte aligned, as the expanding copies need, scales 16-byte aligned;
+// the maps of another expert are never used)
 struct PxItem {
     int unit, mt, e, off, ntok;
     bool ok;
@@ -224,7 +229,8 @@ __device__ __forceinline__ PxItem px_item(const PxArgs &a, long long item) {
     r.ntok = __ldg(a.units + 3 * r.unit + 2);
     const uint4 *q = reinterpret_cast<const uint4 *>(a.experts + r.e);
     const uint4 v0 = __ldg(q), v1 = __ldg(q + 1), v2 = __ldg(q + 2);
-    r.ok = ((v0.x | v0.z | v1.x | v1.z | v2.x | v2.z) & 15u) == 0 && r.ntok >= 1 && r.ntok <= kUT;
+    r.ok = ((v0.x | v1.x | v2.x) & 31u) == 0 && ((v0.z | v1.z | v2.z) & 15u) == 0 && r.ntok >= 1 &&
+           r.ntok <= kUT;
     return r;
 }
 __device__ __forceinline__ const uint8_t *px_scales(const PxArgs &a, int e, int m, int ph) {
@@ -331,9 +337,9 @@ __global__ void __launch_bounds__(kPxThreads, 1)
                 }
                 if (lane == 0) {
                     const uint32_t dst = ar0 + s * Sh::ASTAGE;
-                    mbar_arrive_expect_tx(atfull0 + 8 * s, NMAT * kATile);
-                    tma_2d(dst, map0, c * 64, it.mt * 128, atfull0 + 8 * s, pol);
-                    if (NMAT == 2) tma_2d(dst + kATile, map1, c * 64, it.mt * 128, atfull0 + 8 * s, pol);
+                    mbar_arrive_expect_tx(atfull0 + 8 * s, NMAT * kATx);
+                    tma_2d(dst, map0, c * kKS, it.mt * 128, atfull0 + 8 * s, pol);
+                    if (NMAT == 2) tma_2d(dst + kATile, map1, c * kKS, it.mt * 128, atfull0 + 8 * s, pol);
                 }
                 __syncwarp();
             }
@@ -413,7 +419,7 @@ __global__ void __launch_bounds__(kPxThreads, 1)
 #pragma unroll
                             for (int m = 0; m < NMAT; m++)
 #pragma unroll
-                                for (int i = 0; i < 4; i++) zero_nan_groups_sw64(ast + m * kATile, lane + 32 * i, wq[m][i]);
+                                for (int i = 0; i < 4; i++) zero_nan_groups_x128(ast + m * kATile, lane + 32 * i, wq[m][i]);
                         }
 #pragma unroll
                         for (int m = 0; m < NMAT; m++)
@@ -461,9 +467,9 @@ __global__ void __launch_bounds__(kPxThreads, 1)
                 if (lane == 0) {
                     const uint32_t dst = br0 + s * Sh::BSTAGE;
                     const uint32_t bf = bfull0 + 8 * s;
-                    mbar_arrive_expect_tx(bf, (uint32_t)(Sh::PP * rows * 64 + Sh::PP * kAtomB));
-                    // pieces land `rows` rows apart: [piece][rows][64 B]
-                    tma_3d(dst, bm, c * 64, it.off, 0, bf, pol);
+                    mbar_arrive_expect_tx(bf, (uint32_t)(Sh::PP * rows * 128 + Sh::PP * kAtomB));
+                    // pieces land `rows` rows apart: [piece][rows][128 B]
+                    tma_3d(dst, bm, c * kKS, it.off, 0, bf, pol);
                     bulk_g2s(dst + Sh::PP * kBPiece, a.b_atoms + ((size_t)it.unit * KC + c) * Sh::PP * kAtomB,
                              Sh::PP * kAtomB, bf, pol);
                 }
@@ -480,12 +486,11 @@ __global__ void __launch_bounds__(kPxThreads, 1)
             for (long long item = i0; item < items && run && !*abort_flag; item += istep) {
                 const PxItem it = px_item<MT>(a, item);
                 if (!it.ok) continue;
-                const int npad = (it.ntok + 15) & ~15;
-                const uint32_t pstride = 64u * (uint32_t)b_rows(b_sel(it.ntok));
-                // paired pieces: N covers two box heights (both pieces' rows)
+                // both pieces: N covers two box heights
                 const int nmma = 2 * b_rows(b_sel(it.ntok));
-                (void)npad;
-                const uint32_t id0 = idesc_mxf4(nmma, 0), id1 = idesc_mxf4(nmma, 2);
+                uint32_t idk[4];
+#pragma unroll
+                for (int ks = 0; ks < 4; ks++) idk[ks] = idesc_e2m1_e4m3(nmma, ks);
                 const int b = itn % Sh::NBUF;
                 if (!mbar_wait(acce0 + 8 * b, ((itn / Sh::NBUF) & 1) ^ 1)) {
                     fail(330 + PH);
@@ -507,23 +512,18 @@ __global__ void __launch_bounds__(kPxThreads, 1)
 #pragma unroll
                     for (int m = 0; m < NMAT; m++)
                         tmem_cp_atom(sfa + m * 4, desc_atom(ast + NMAT * kATile + m * kAtomB, 128));
-                    // B scales: per piece one atom of 128 rows, or per piece
-                    // pair two atoms of 256 combined rows (4 columns each)
+                    // B scales: two atoms over the 2 x rows combined rows of
+                    // the operand (4 columns each)
 #pragma unroll
                     for (int p = 0; p < Sh::PP; p++)
                         tmem_cp_atom(sfb + p * 4, desc_atom(bst + Sh::PP * kBPiece + p * kAtomB, 128));
-                    constexpr int NB = Sh::PP / 2;                     // B operands per K step
 #pragma unroll
                     for (int m = 0; m < NMAT; m++)
 #pragma unroll
-                        for (int ks = 0; ks < 2; ks++)
-#pragma unroll
-                            for (int q = 0; q < NB; q++) {
-                                const int p0 = 2 * q;                      // first piece of the operand
-                                mma_mxf4(tmem + (b * NMAT + m) * Sh::NACC, desc_sw64(ast + m * kATile + 32 * ks),
-                                         desc_sw64(bst + p0 * pstride + 32 * ks), ks ? id1 : id0, sfa + m * 4,
-                                         sfb + 8 * q, (c | ks | q) != 0 ? 1u : 0u);
-                            }
+                        for (int ks = 0; ks < 4; ks++)
+                            mma_mxf8f6f4(tmem + (b * NMAT + m) * Sh::NACC, umma_desc_sw128(ast + m * kATile + 32 * ks),
+                                         umma_desc_sw128(bst + 32 * ks), idk[ks], sfa + m * 4, sfb,
+                                         (c | ks) != 0 ? 1u : 0u);
                     umma_commit(aempty0 + 8 * s_a);
                     umma_commit(bempty0 + 8 * s_b);
                 }
@@ -561,7 +561,7 @@ __global__ void __launch_bounds__(kPxThreads, 1)
                 const int kb = it.mt * 4 + q4;                   // the warp's 32-feature block of h
                 const int hrows = b_rows(b_sel(it.ntok));         // the unit's B box height
                 uint8_t *tiles = smem + 1024 + SA * Sh::ASTAGE + SB * Sh::BSTAGE + (warp - kEpi0) * 2 * 32 * Sh::TROW;
-                const size_t plane = a.slots * (kF / 2);
+                const size_t plane = a.slots * kF;
                 int nr = 0;
                 for (int nb = 32 * half; nb < it.ntok; nb += 64, nr++) {
                     uint8_t *tile = tiles + nr * 32 * Sh::TROW;
@@ -611,13 +611,14 @@ __global__ void __launch_bounds__(kPxThreads, 1)
                         v[2 * wd + 1] = f.y * up;
                     }
                     if (n < it.ntok) {
-                        uint4 wds[kPPh];
+                        uint4 wds[kPPh][2];
                         uint32_t sc[kPPh];
-                        lane_pieces<kPPh>(v, wds, sc);
-                        uint8_t *dst = a.h_planes + ((size_t)it.off + n) * (kF / 2) + (size_t)kb * 16;
+                        lane_pieces_e4m3<kPPh>(v, wds, sc);
+                        uint8_t *dst = a.h_planes + ((size_t)it.off + n) * kF + (size_t)kb * 32;
 #pragma unroll
                         for (int p = 0; p < kPPh; p++) {
-                            *reinterpret_cast<uint4 *>(dst + p * plane) = wds[p];
+                            reinterpret_cast<uint4 *>(dst + p * plane)[0] = wds[p][0];
+                            reinterpret_cast<uint4 *>(dst + p * plane)[1] = wds[p][1];
                             a.h_atoms[atom_byte_pair<kPPh>(it.unit, kF / kKS, it.mt, p, n, hrows, q4)] = (uint8_t)sc[p];
                         }
                     }
@@ -720,7 +721,7 @@ k_px_slots(const int32_t *units, const int32_t *n_units, const int32_t *perm, in
         }
         return;
     }
-    build_maps_cta(maps, kE, table, k3mx_expert{}, w13, w2, blockIdx.x - max_units);
+    build_maps_cta(maps, kE, table, k3mx_expert{}, w13, w2, blockIdx.x - max_units, 32);
 }
 
 // One thread per (token, 32-column block): x (bf16) -> kPPx pieces, written
@@ -750,19 +751,20 @@ k_px_xprep(const uint16_t *__restrict__ x, int n_tokens, const int32_t *__restri
     float4 *yz = reinterpret_cast<float4 *>(y + i0);
 #pragma unroll
     for (int q = 0; q < 8; q++) yz[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-    uint4 wds[kPPx];
+    uint4 wds[kPPx][2];
     uint32_t sc[kPPx];
-    lane_pieces<kPPx>(v, wds, sc);
+    lane_pieces_e4m3<kPPx>(v, wds, sc);
 #pragma unroll 4
     for (int k = 0; k < kK; k++) {
         const int slot = __ldg(slot_of_pair + (size_t)t * kK + k);
         if (slot < 0) continue;                          // dropped by top-p
         const int un = __ldg(slot_un + slot);
         const int rows = b_rows(b_sel(__ldg(units + 3 * (un >> 8) + 2)));
-        uint8_t *dst = planes + (size_t)slot * (kD / 2) + (size_t)kb * 16;
+        uint8_t *dst = planes + (size_t)slot * kD + (size_t)kb * 32;
 #pragma unroll
         for (int p = 0; p < kPPx; p++) {
-            *reinterpret_cast<uint4 *>(dst + (size_t)p * slots * (kD / 2)) = wds[p];
+            reinterpret_cast<uint4 *>(dst + (size_t)p * slots * kD)[0] = wds[p][0];
+            reinterpret_cast<uint4 *>(dst + (size_t)p * slots * kD)[1] = wds[p][1];
             atoms[atom_byte_pair<kPPx>(un >> 8, KC, kb >> 2, p, un & 255, rows, kb & 3)] = (uint8_t)sc[p];
         }
     }
@@ -782,20 +784,22 @@ cudaError_t launch_px_t(const Ctx &c, const PxArgs &a, const PxBMaps &bmaps, lon
     return launch_pdl(k_px<PH>, dim3((unsigned)grid), dim3(kPxThreads), (size_t)Sh::SMEM, c.stream, a, bmaps);
 }
 
-// 2-D uint8 map: rows x row_bytes, boxes of box_rows x 64 bytes, 64-byte swizzle
-bool encode_sw64(CUtensorMap &m, const void *base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
+// 2-D map over a packed e2m1 matrix of `rows` rows of `cols` codes: boxes
+// of 128 rows x 128 codes, each 16 packed codes (8 bytes) landing in a
+// 16-byte chunk of shared memory (128-byte rows, 128-byte swizzle)
+bool encode_e2m1_x128(CUtensorMap &m, const void *base, uint64_t cols, uint64_t rows) {
     auto enc = tensor_map_encoder();
     if (enc == nullptr) return false;
-    const cuuint64_t dims[2] = {row_bytes, rows}, strides[1] = {row_bytes};
-    const cuuint32_t box[2] = {64, box_rows}, es[2] = {1, 1};
-    return enc(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+    const cuuint64_t dims[2] = {cols, rows}, strides[1] = {cols / 2};
+    const cuuint32_t box[2] = {128, 128}, es[2] = {1, 1};
+    return enc(&m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void *>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// weight map templates of the prefill path (128 rows x 64 B boxes), encoded
-// once per device over the library's scratch array (any address works for
-// a template; the device replaces it per expert)
+// weight map templates of the prefill path, encoded once per device over
+// the library's scratch array (any 32-byte aligned address works for a
+// template; the device replaces it per expert)
 bool px_weight_templates(CUtensorMap &w13, CUtensorMap &w2) {
     constexpr int kDevs = 64;
     static std::atomic<int> state[kDevs];  // 0 not tried, 1 ok, 2 failed
@@ -807,8 +811,7 @@ bool px_weight_templates(CUtensorMap &w13, CUtensorMap &w2) {
         std::lock_guard<std::mutex> lock(setup_mutex());
         if (state[dev].load(std::memory_order_relaxed) == 0) {
             const bool ok = base != nullptr && library_scratch_bytes() >= (size_t)kD / 2 * kF &&
-                            encode_sw64(t13[dev], base, kD / 2, kF, 128) &&
-                            encode_sw64(t2[dev], base, kF / 2, kD, 128);
+                            encode_e2m1_x128(t13[dev], base, kD, kF) && encode_e2m1_x128(t2[dev], base, kF, kD);
             state[dev].store(ok ? 1 : 2, std::memory_order_release);
         }
     }
@@ -819,15 +822,15 @@ bool px_weight_templates(CUtensorMap &w13, CUtensorMap &w2) {
 }
 
 // 3-D uint8 map over `planes` planes of `rows` rows of row_bytes: boxes of
-// 64 bytes x box_rows rows x all planes, 64-byte swizzle
+// 128 bytes x box_rows rows x all planes, 128-byte swizzle
 bool encode_planes(CUtensorMap &m, const void *base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows,
                    int planes) {
     auto enc = tensor_map_encoder();
     if (enc == nullptr) return false;
     const cuuint64_t dims[3] = {row_bytes, rows, (cuuint64_t)planes}, strides[2] = {row_bytes, row_bytes * rows};
-    const cuuint32_t box[3] = {64, box_rows, (cuuint32_t)planes}, es[3] = {1, 1, 1};
+    const cuuint32_t box[3] = {128, box_rows, (cuuint32_t)planes}, es[3] = {1, 1, 1};
     return enc(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -845,8 +848,8 @@ PxLayout px_layout(int n_tokens) {
         o += up256(b);
         return at;
     };
-    L.xplanes = take(kPPx * S * (kD / 2));
-    L.hplanes = take(kPPh * S * (kF / 2));
+    L.xplanes = take(kPPx * S * kD);
+    L.hplanes = take(kPPh * S * kF);
     L.xatoms = take(U * (kD / kKS) * kPPx * kAtomB);
     L.hatoms = take(U * (kF / kKS) * kPPh * kAtomB);
     L.units = take(U * 3 * 4);
@@ -887,8 +890,8 @@ cudaError_t launch_prefill_mx(const Ctx &c, const PrefillArgs &p) {
     PxBMaps xmap, hmap;
     if (!px_weight_templates(w13, w2)) return cudaErrorNotSupported;
     for (int i = 0; i < kBoxes; i++)
-        if (!encode_planes(xmap.m[i], xplanes, kD / 2, S, b_rows(i), kPPx) ||
-            !encode_planes(hmap.m[i], hplanes, kF / 2, S, b_rows(i), kPPh))
+        if (!encode_planes(xmap.m[i], xplanes, kD, S, b_rows(i), kPPx) ||
+            !encode_planes(hmap.m[i], hplanes, kF, S, b_rows(i), kPPh))
             return cudaErrorNotSupported;
 
     cudaError_t err = traced("prefill_prep", c.stream, [&] {

@@ -45,6 +45,21 @@ __device__ __forceinline__ void mma_mxf4(uint32_t d, uint64_t adesc, uint64_t bd
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
         : "memory");
 }
+// instruction descriptor, kind::mxf8f6f4 with e2m1 A (each 16 packed codes
+// spread over 16 bytes by the copy engine) and e4m3 B, ue8m0 scales, K-major, M = 128,
+// N = n; sf_id picks the scale byte (the 32-column block of a K = 128 step)
+__device__ __forceinline__ uint32_t idesc_e2m1_e4m3(int n, int sf_id) {
+    return ((uint32_t)sf_id << 4) | (5u << 7) | (0u << 10) | ((uint32_t)(n >> 3) << 17) | (1u << 23) |
+           ((uint32_t)(128 >> 4) << 24) | ((uint32_t)sf_id << 29);
+}
+__device__ __forceinline__ void mma_mxf8f6f4(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t sfa, uint32_t sfb, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+        : "memory");
+}
 __device__ __forceinline__ void tma_2d(uint32_t dst, const void *map, int x, int y, uint32_t bar,
                                        uint64_t policy) {
     asm volatile(
@@ -124,6 +139,19 @@ __device__ __forceinline__ void zero_nan_groups_sw64(uint32_t tile, int r, uint3
     for (int g = 0; g < 4; g++)
         if ((m >> (8 * g)) & 1u)
             sts128(tile + (uint32_t)(r * 64) + (uint32_t)(((g ^ (r >> 1)) & 3) << 4), 0u, 0u, 0u, 0u);
+}
+// Tile of expanded e2m1 codes (rows of 128 codes in 128-byte rows, 128-byte
+// swizzle; the copy engine puts each 16 packed codes into 8 bytes of a
+// 16-byte chunk): the four 32-code groups of row r whose scale byte in `sc`
+// is 255 get zero codes (both chunks of the group cleared).
+__device__ __forceinline__ void zero_nan_groups_x128(uint32_t tile, int r, uint32_t sc) {
+    const uint32_t row = tile + (uint32_t)r * 128;
+#pragma unroll
+    for (int g = 0; g < 4; g++)
+        if (((sc >> (8 * g)) & 0xFFu) == 0xFFu) {
+            sts128(row + (((uint32_t)(2 * g) ^ (uint32_t)r) & 7u) * 16, 0u, 0u, 0u, 0u);
+            sts128(row + (((uint32_t)(2 * g + 1) ^ (uint32_t)r) & 7u) * 16, 0u, 0u, 0u, 0u);
+        }
 }
 
 

@@ -31,10 +31,11 @@ bool weight_map_templates(CUtensorMap &w13, CUtensorMap &w2);
 inline size_t expert_maps_bytes(int n_experts) { return (size_t)n_experts * kMapsPerExpert * kMapBytes; }
 
 // Map `i` of the table (expert i / 3, matrix i % 3) built by one warp with
-// a 128-byte shared staging slot `smap`.  A misaligned weight pointer keeps
-// the template's address (the passes skip that expert).
+// a 128-byte shared staging slot `smap`.  A weight pointer not aligned to
+// `align` bytes (16, or 32 for maps that expand e2m1 codes) keeps the
+// template's address (the passes skip that expert).
 __device__ __forceinline__ void build_expert_map(uint8_t *table, int i, uint32_t smap, const k3mx_expert &ex,
-                                                 const CUtensorMap &w13, const CUtensorMap &w2) {
+                                                 const CUtensorMap &w13, const CUtensorMap &w2, uint32_t align) {
     const int lane = threadIdx.x & 31, mat = i % kMapsPerExpert;
     const CUtensorMap &tmpl = mat < 2 ? w13 : w2;
     const uint8_t *addr = mat == 0 ? ex.w1 : mat == 1 ? ex.w3 : ex.w2;
@@ -45,7 +46,7 @@ __device__ __forceinline__ void build_expert_map(uint8_t *table, int i, uint32_t
                      : "memory");
     }
     __syncwarp();
-    if (lane == 0 && (reinterpret_cast<uintptr_t>(addr) & 15u) == 0)
+    if (lane == 0 && (reinterpret_cast<uintptr_t>(addr) & (uintptr_t)(align - 1)) == 0)
         asm volatile("tensormap.replace.tile.global_address.shared::cta.b1024.b64 [%0], %1;" ::"r"(smap),
                      "l"(reinterpret_cast<uint64_t>(addr))
                      : "memory");
@@ -73,7 +74,7 @@ constexpr int kMapsPerWarp = 8;
 constexpr int kMapsPerCta = 8 * kMapsPerWarp;
 __device__ __forceinline__ void build_maps_cta(uint8_t *maps, int n_experts, const k3mx_expert *table,
                                                const k3mx_expert &one, const CUtensorMap &w13,
-                                               const CUtensorMap &w2, int cta) {
+                                               const CUtensorMap &w2, int cta, uint32_t align = 16) {
     __shared__ __align__(128) uint8_t stage[8][kMapBytes];
     const int warp = threadIdx.x >> 5;
     if (warp >= 8) return;
@@ -81,7 +82,7 @@ __device__ __forceinline__ void build_maps_cta(uint8_t *maps, int n_experts, con
         const int i = (cta * 8 + warp) * kMapsPerWarp + j;
         if (i >= n_experts * kMapsPerExpert) return;
         const k3mx_expert ex = table != nullptr ? table[i / kMapsPerExpert] : one;
-        build_expert_map(maps, i, (uint32_t)__cvta_generic_to_shared(stage[warp]), ex, w13, w2);
+        build_expert_map(maps, i, (uint32_t)__cvta_generic_to_shared(stage[warp]), ex, w13, w2, align);
         __syncwarp();                     // the staging slot is reused
     }
 }

@@ -1,6 +1,7 @@
 """The routed-expert layer on the two prefill paths (bf16 activations,
-grouped tcgen05 GEMMs: weights dequantised to f16, or x as six and h as four
-MXFP4 pieces on the block-scaled MMAs) against the oracle.  Routing bit-exact;
+grouped tcgen05 GEMMs: weights dequantised to f16, or x and h as two MXFP8
+pieces each against the weights as stored on the block-scaled MMAs) against
+the oracle.  Routing bit-exact;
 per sampled token the relative L2 error of y is at most 1e-2 (the
 bf16-activation tolerance)."""
 import numpy as np
