@@ -78,16 +78,18 @@ constexpr int kEpiThreads = 8 * 32;
 constexpr int kPxSmemLimit = 227 * 1024;
 
 template <int PH> struct PxCfg;
+// PF: weight stages prefetched into L2 ahead of the copies into the A ring
+// (the ring itself holds too few bytes in flight to cover HBM latency)
 template <> struct PxCfg<0> {           // gate/up: g = W1 x, u = W3 x
-    static constexpr int NMAT = 2, K = kD, M = kF, SA = 3, SB = 3, PP = kPPx;
+    static constexpr int NMAT = 2, K = kD, M = kF, SA = 3, SB = 3, PP = kPPx, PF = 6;
 };
 template <> struct PxCfg<1> {           // down: Y = W2 h
-    static constexpr int NMAT = 1, K = kF, M = kD, SA = 6, SB = 4, PP = kPPh;
+    static constexpr int NMAT = 1, K = kF, M = kD, SA = 6, SB = 4, PP = kPPh, PF = 6;
 };
 
 template <int PH> struct PxShape {
     using C = PxCfg<PH>;
-    static constexpr int NMAT = C::NMAT, K = C::K, M = C::M, SA = C::SA, SB = C::SB, PP = C::PP;
+    static constexpr int NMAT = C::NMAT, K = C::K, M = C::M, SA = C::SA, SB = C::SB, PP = C::PP, PF = C::PF;
     static constexpr int KC = K / kKS, MT = M / 128, G = K / 32;
     static constexpr int ASTAGE = ((NMAT * (kATile + kAtomB)) + 1023) / 1024 * 1024;
     static constexpr int BSTAGE = PP * kBPiece + PP * kAtomB;            // 25 KB
@@ -137,7 +139,9 @@ struct PxArgs {
 struct PxHdr {
     // afull: the A stage's scale atoms (32 scale-loader lanes); atfull: its
     // weight tiles (the producer's expect_tx and the copies' bytes)
-    uint64_t afull[16], atfull[16], aempty[16], bfull[8], bempty[8], accf[2], acce[2], done;
+    // aempty[s] completes when the MMAs of the stage in slot s are done: the
+    // A and B rings advance together (SA >= SB), so it frees B slots too
+    uint64_t afull[16], atfull[16], aempty[16], bfull[8], accf[2], acce[2], done;
     uint32_t tmem;
     int abort;
 };
@@ -251,6 +255,7 @@ __global__ void __launch_bounds__(kPxThreads, 1)
     using Sh = PxShape<PH>;
     constexpr int NMAT = Sh::NMAT, KC = Sh::KC, MT = Sh::MT, G = Sh::G, SA = Sh::SA, SB = Sh::SB;
     static_assert(SA <= 16 && SB <= 8, "barrier slots");
+    static_assert(SA >= SB, "a B slot is freed by the A ring's empty barrier");
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -261,7 +266,7 @@ __global__ void __launch_bounds__(kPxThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t afull0 = smem_addr(hd->afull), aempty0 = smem_addr(hd->aempty);
     const uint32_t atfull0 = smem_addr(hd->atfull);
-    const uint32_t bfull0 = smem_addr(hd->bfull), bempty0 = smem_addr(hd->bempty);
+    const uint32_t bfull0 = smem_addr(hd->bfull);
     const uint32_t accf0 = smem_addr(hd->accf), acce0 = smem_addr(hd->acce);
     const uint32_t done = smem_addr(&hd->done);
 
@@ -273,7 +278,6 @@ __global__ void __launch_bounds__(kPxThreads, 1)
         }
         for (int i = 0; i < SB; i++) {
             mbar_init(bfull0 + 8 * i, 1);
-            mbar_init(bempty0 + 8 * i, 1);
         }
         for (int i = 0; i < 2; i++) {
             mbar_init(accf0 + 8 * i, 1);
@@ -311,8 +315,40 @@ __global__ void __launch_bounds__(kPxThreads, 1)
         uint32_t sa = 0;
         int cur_e = -1;
         const uint8_t *map0 = nullptr, *map1 = nullptr;
+        // L2 prefetch cursor: Sh::PF stages ahead of the copies, over the
+        // same sequence of (item, stage)
+        long long pf_item = i0;
+        int pf_c = 0, pf_e = -1;
+        PxItem pit = pf_item < items ? px_item<MT>(a, pf_item) : PxItem{};
+        auto prefetch_next = [&]() {
+            while (pf_item < items && !pit.ok) {
+                pf_item += istep;
+                pf_c = 0;
+                if (pf_item < items) pit = px_item<MT>(a, pf_item);
+            }
+            if (pf_item >= items) return;
+            if (lane == 0) {
+                const uint8_t *em = a.maps + (size_t)pit.e * kMapsPerExpert * kMapBytes;
+                const uint8_t *m0 = em + (PH == 0 ? 0 : 2) * kMapBytes, *m1 = em + kMapBytes;
+                if (pit.e != pf_e) {
+                    acquire_map(m0);
+                    if (NMAT == 2) acquire_map(m1);
+                }
+                tma_prefetch_2d(m0, pf_c * kKS, pit.mt * 128);
+                if (NMAT == 2) tma_prefetch_2d(m1, pf_c * kKS, pit.mt * 128);
+            }
+            pf_e = pit.e;
+            if (++pf_c == KC) {
+                pf_c = 0;
+                pf_item += istep;
+                if (pf_item < items) pit = px_item<MT>(a, pf_item);
+            }
+        };
+        for (int k = 0; k < Sh::PF; k++) prefetch_next();
+        PxItem nxt = i0 < items ? px_item<MT>(a, i0) : PxItem{};
         for (long long item = i0; item < items && !*abort_flag; item += istep) {
-            const PxItem it = px_item<MT>(a, item);
+            const PxItem it = nxt;                 // decoded one item ahead (dependent loads)
+            if (item + istep < items) nxt = px_item<MT>(a, item + istep);
             if (!it.ok) {
                 if (lane == 0 && it.mt == 0) report_status(a.status, kStatusBadPointer, it.e);
                 continue;
@@ -341,6 +377,7 @@ __global__ void __launch_bounds__(kPxThreads, 1)
                     tma_2d(dst, map0, c * kKS, it.mt * 128, atfull0 + 8 * s, pol);
                     if (NMAT == 2) tma_2d(dst + kATile, map1, c * kKS, it.mt * 128, atfull0 + 8 * s, pol);
                 }
+                prefetch_next();
                 __syncwarp();
             }
             if (!ok) break;
@@ -382,8 +419,10 @@ __global__ void __launch_bounds__(kPxThreads, 1)
         have2 = have2 && advance(la_item, la_g);
         if (have2) load_group(la_item, la_g, n2);
         uint32_t sa = 0;
+        PxItem nxt = i0 < items ? px_item<MT>(a, i0) : PxItem{};
         for (long long item = i0; item < items && !*abort_flag; item += istep) {
-            const PxItem it = px_item<MT>(a, item);
+            const PxItem it = nxt;                 // decoded one item ahead (dependent loads)
+            if (item + istep < items) nxt = px_item<MT>(a, item + istep);
             bool ok = true;
             for (int g = 0; g < NG && ok; g++) {
                 if (it.ok) {
@@ -450,8 +489,10 @@ __global__ void __launch_bounds__(kPxThreads, 1)
         if (PH == 1) pdl_wait();                               // h of every pair is written
         const uint64_t pol = l2_evict_normal_policy();
         uint32_t sb = 0;
+        PxItem nxt = i0 < items ? px_item<MT>(a, i0) : PxItem{};
         for (long long item = i0; item < items && !*abort_flag; item += istep) {
-            const PxItem it = px_item<MT>(a, item);
+            const PxItem it = nxt;                 // decoded one item ahead (dependent loads)
+            if (item + istep < items) nxt = px_item<MT>(a, item + istep);
             if (!it.ok) continue;
             const int hsel = b_sel(it.ntok);
             const void *bm = &bmaps.m[hsel];
@@ -459,10 +500,17 @@ __global__ void __launch_bounds__(kPxThreads, 1)
             bool ok = true;
             for (int c = 0; c < KC; c++, sb++) {
                 const int s = sb % SB;
-                if (!mbar_wait(bempty0 + 8 * s, ((sb / SB) & 1) ^ 1)) {
-                    if (lane == 0) fail(320 + PH);
-                    ok = false;
-                    break;
+                // slot s last held stage sb - SB: its MMAs are done when
+                // aempty of that stage's A slot completes phase (sb - SB) / SA
+                // (that barrier cannot run a phase further ahead: it would
+                // need stage sb - SB + SA >= sb, not yet filled here)
+                if (sb >= (uint32_t)SB) {
+                    const uint32_t j = sb - SB;
+                    if (!mbar_wait(aempty0 + 8 * (j % SA), (j / SA) & 1)) {
+                        if (lane == 0) fail(320 + PH);
+                        ok = false;
+                        break;
+                    }
                 }
                 if (lane == 0) {
                     const uint32_t dst = br0 + s * Sh::BSTAGE;
@@ -483,8 +531,14 @@ __global__ void __launch_bounds__(kPxThreads, 1)
         if (lane == 0) {
             uint32_t sa = 0, sb = 0, itn = 0;
             bool run = true;
+            // the next stage's three barriers, polled while the last MMA of
+            // a stage issues: when they had completed, that stage starts
+            // without the waits' shared-memory round trips
+            bool ready = false;
+            PxItem nxt = i0 < items ? px_item<MT>(a, i0) : PxItem{};
             for (long long item = i0; item < items && run && !*abort_flag; item += istep) {
-                const PxItem it = px_item<MT>(a, item);
+                const PxItem it = nxt;             // decoded one item ahead (dependent loads)
+                if (item + istep < items) nxt = px_item<MT>(a, item + istep);
                 if (!it.ok) continue;
                 // both pieces: N covers two box heights
                 const int nmma = 2 * b_rows(b_sel(it.ntok));
@@ -499,8 +553,9 @@ __global__ void __launch_bounds__(kPxThreads, 1)
                 tc_fence_after();
                 for (int c = 0; c < KC; c++, sa++, sb++) {
                     const int s_a = sa % SA, s_b = sb % SB;
-                    if (!mbar_wait(atfull0 + 8 * s_a, (sa / SA) & 1) || !mbar_wait(afull0 + 8 * s_a, (sa / SA) & 1) ||
-                        !mbar_wait(bfull0 + 8 * s_b, (sb / SB) & 1)) {
+                    if (!ready && (!mbar_wait(atfull0 + 8 * s_a, (sa / SA) & 1) ||
+                                   !mbar_wait(afull0 + 8 * s_a, (sa / SA) & 1) ||
+                                   !mbar_wait(bfull0 + 8 * s_b, (sb / SB) & 1))) {
                         fail(340 + PH);
                         run = false;
                         break;
@@ -520,12 +575,21 @@ __global__ void __launch_bounds__(kPxThreads, 1)
 #pragma unroll
                     for (int m = 0; m < NMAT; m++)
 #pragma unroll
-                        for (int ks = 0; ks < 4; ks++)
-                            mma_mxf8f6f4(tmem + (b * NMAT + m) * Sh::NACC, umma_desc_sw128(ast + m * kATile + 32 * ks),
-                                         umma_desc_sw128(bst + 32 * ks), idk[ks], sfa + m * 4, sfb,
-                                         (c | ks) != 0 ? 1u : 0u);
+                        for (int ks = 0; ks < 4; ks++) {
+                            const uint32_t d = tmem + (b * NMAT + m) * Sh::NACC;
+                            const uint64_t ad = umma_desc_sw128(ast + m * kATile + 32 * ks), bd = umma_desc_sw128(bst + 32 * ks);
+                            const uint32_t acc = (c | ks) != 0 ? 1u : 0u;
+                            if (m == NMAT - 1 && ks == 3) {
+                                // the barriers of stage sa + 1 (of this item or the next)
+                                const uint32_t na = (sa + 1) % SA, pa = ((sa + 1) / SA) & 1;
+                                const uint32_t nb = (sb + 1) % SB, pb = ((sb + 1) / SB) & 1;
+                                ready = mma_mxf8f6f4_poll3(d, ad, bd, idk[ks], sfa + m * 4, sfb, acc, atfull0 + 8 * na, pa,
+                                                           afull0 + 8 * na, pa, bfull0 + 8 * nb, pb);
+                            } else {
+                                mma_mxf8f6f4(d, ad, bd, idk[ks], sfa + m * 4, sfb, acc);
+                            }
+                        }
                     umma_commit(aempty0 + 8 * s_a);
-                    umma_commit(bempty0 + 8 * s_b);
                 }
                 if (!run) break;
                 umma_commit(accf0 + 8 * b);
@@ -541,8 +605,10 @@ __global__ void __launch_bounds__(kPxThreads, 1)
         const int row_in_tile = 32 * q4 + lane;
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
         uint32_t itn = 0;
+        PxItem nxt = i0 < items ? px_item<MT>(a, i0) : PxItem{};
         for (long long item = i0; item < items && !*abort_flag; item += istep) {
-            const PxItem it = px_item<MT>(a, item);
+            const PxItem it = nxt;                 // decoded one item ahead (dependent loads)
+            if (item + istep < items) nxt = px_item<MT>(a, item + istep);
             if (!it.ok) continue;
             const int b = itn % Sh::NBUF;
             if (!mbar_wait(accf0 + 8 * b, (itn / Sh::NBUF) & 1)) {

@@ -60,6 +60,30 @@ __device__ __forceinline__ void mma_mxf8f6f4(uint32_t d, uint64_t adesc, uint64_
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
         : "memory");
 }
+// The same MMA, with three mbarrier phases polled (non-blocking) just ahead
+// of it in the same instruction stream: the polls' shared-memory round trips
+// overlap the MMA's issue.  True when all three phases had completed.
+__device__ __forceinline__ bool mma_mxf8f6f4_poll3(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                   uint32_t sfa, uint32_t sfb, uint32_t acc, uint32_t bar0,
+                                                   uint32_t par0, uint32_t bar1, uint32_t par1, uint32_t bar2,
+                                                   uint32_t par2) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p, q0, q1, q2;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q0, [%8], %9;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q1, [%10], %11;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q2, [%12], %13;\n\t"
+        "setp.ne.b32 p, %7, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%1], %2, %3, %4, [%5], [%6], p;\n\t"
+        "and.pred q0, q0, q1;\n\t"
+        "and.pred q0, q0, q2;\n\t"
+        "selp.u32 %0, 1, 0, q0;\n\t}"
+        : "=r"(ok)
+        : "r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc), "r"(bar0), "r"(par0), "r"(bar1),
+          "r"(par1), "r"(bar2), "r"(par2)
+        : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ void tma_2d(uint32_t dst, const void *map, int x, int y, uint32_t bar,
                                        uint64_t policy) {
     asm volatile(
