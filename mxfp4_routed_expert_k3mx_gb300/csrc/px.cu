@@ -35,7 +35,7 @@
 //               per stage, 4 K steps x NMAT MMAs (M = 128, N = 2 x the unit's
 //               box rows, K = 32)
 //   warp 3      B producer: one 3-D TMA per stage for both pieces of the
-//               unit's rows (box of 16, 32, ..., 96 rows x 128 B) and one
+//               unit's rows (box of 8, 16, ..., 96 rows x 128 B) and one
 //               bulk copy of the stage's B scale atoms into a B ring
 //   warps 4-11  epilogue, two warps per TMEM lane quarter, each half the
 //               unit's tokens: gate/up h = SiTU(g, u) split into pieces
@@ -62,10 +62,10 @@ constexpr int kKS = 128;                // K columns per stage
 constexpr int kATile = 128 * 128;       // A tile in shared memory: 128 rows x 128 B (expanded codes)
 constexpr int kATx = 128 * 64;          // the bytes one A tile copy moves (packed codes)
 constexpr int kBPiece = kUT * 128;      // one piece of the unit's B: 96 rows x 128 B (e4m3)
-constexpr int kBoxes = kUT / 16;
-__host__ __device__ constexpr int b_rows(int i) { return 16 * (i + 1); }   // B box heights: 16, 32, ..., 96
+constexpr int kBoxes = kUT / 8;
+__host__ __device__ constexpr int b_rows(int i) { return 8 * (i + 1); }    // B box heights: 8, 16, ..., 96
 // the B box of a unit of n pairs: the smallest height holding them
-__host__ __device__ constexpr int b_sel(int n) { return n <= 16 ? 0 : (n + 15) / 16 - 1; }
+__host__ __device__ constexpr int b_sel(int n) { return n <= 8 ? 0 : (n + 7) / 8 - 1; }
 
 // the B tensor maps of one pass, one per box height
 struct PxBMaps {
@@ -147,16 +147,24 @@ struct PxHdr {
 };
 
 // SiTU-GLU for the prefill epilogue (Kimi K3 engine (c/kimi_k3.c),
-// "Architecture notes": 4 tanh(g/4) sigma(g) 25 tanh(u/25)) with the
-// hardware tanh (relative error about 2^-11), sigma(g) = (1 + tanh(g/2)) / 2
-__device__ __forceinline__ float tanh_hw(float v) {
-    float r;
-    asm("tanh.approx.f32 %0, %1;" : "=f"(r) : "f"(v));
-    return r;
+// "Architecture notes": 4 tanh(g/4) sigma(g) 25 tanh(u/25)), sigma(g) =
+// (1 + tanh(g/2)) / 2, for two tokens at once with the hardware tanh on
+// f16 pairs (relative error about 2^-10; arguments below 2^-6 in magnitude
+// give tanh(x) = x, within x^2 / 3, so small g and u keep their precision)
+__device__ __forceinline__ float2 tanh2_f16(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    uint32_t r;
+    asm("tanh.approx.f16x2 %0, %1;" : "=r"(r) : "r"(*reinterpret_cast<const uint32_t *>(&h)));
+    float2 t = __half22float2(*reinterpret_cast<const __half2 *>(&r));
+    if (fabsf(a) < 0.015625f) t.x = a;
+    if (fabsf(b) < 0.015625f) t.y = b;
+    return t;
 }
-__device__ __forceinline__ float situ_fast(float g, float u) {
-    const float sg = 0.5f + 0.5f * tanh_hw(0.5f * g);
-    return (4.0f * tanh_hw(0.25f * g) * sg) * (25.0f * tanh_hw(u * 0.04f));
+__device__ __forceinline__ float2 situ_fast2(float g0, float u0, float g1, float u1) {
+    const float2 t4 = tanh2_f16(0.25f * g0, 0.25f * g1), t2 = tanh2_f16(0.5f * g0, 0.5f * g1);
+    const float2 tu = tanh2_f16(0.04f * u0, 0.04f * u1);
+    return make_float2((4.0f * t4.x * (0.5f + 0.5f * t2.x)) * (25.0f * tu.x),
+                       (4.0f * t4.y * (0.5f + 0.5f * t2.y)) * (25.0f * tu.y));
 }
 
 // The NP MXFP8 pieces of 32 values held by one lane (v, column order):
@@ -619,64 +627,66 @@ __global__ void __launch_bounds__(kPxThreads, 1)
             const int n0 = half * (kUT / 2), n1 = min(it.ntok, n0 + kUT / 2);
             const int row = it.mt * 128 + row_in_tile;
             if (PH == 0) {
-                // Rounds of 32 tokens (this warp: tokens 32 half + 64 k ...).
-                // First every round's h (g and u: even-piece plus odd-piece
-                // columns) into the warp's f16 tiles, scaled per token, then
+                // Groups of 16 tokens, dealt alternately to the two warps of
+                // a lane quarter (this warp: groups half, half + 2, half + 4).
+                // First each group's h (g and u: piece-0 plus piece-1
+                // columns) into the warp's f16 tile, scaled per token, then
                 // the accumulator is released, then each lane splits one
                 // token's 32 features.
                 const int kb = it.mt * 4 + q4;                   // the warp's 32-feature block of h
                 const int hrows = b_rows(b_sel(it.ntok));         // the unit's B box height
                 uint8_t *tiles = smem + 1024 + SA * Sh::ASTAGE + SB * Sh::BSTAGE + (warp - kEpi0) * 2 * 32 * Sh::TROW;
                 const size_t plane = a.slots * kF;
-                int nr = 0;
-                for (int nb = 32 * half; nb < it.ntok; nb += 64, nr++) {
-                    uint8_t *tile = tiles + nr * 32 * Sh::TROW;
+                const int ng = (it.ntok + 15) >> 4;               // groups of the unit
+                int nslot = 0;                                    // this warp's groups, tile rows 16 i ...
+                for (int gi = half; gi < ng; gi += 2, nslot++) {
+                    uint8_t *tile = tiles + nslot * 16 * Sh::TROW;
+                    uint32_t g0[16], g1[16], u0[16], u1[16];
+                    const uint32_t cg = tmem + lane_base + (uint32_t)(16 * gi), cu = cg + Sh::NACC;
+                    tmem_ld16(cg, g0);
+                    tmem_ld16(cg + hrows, g1);
+                    tmem_ld16(cu, u0);
+                    tmem_ld16(cu + hrows, u1);
+                    tmem_ld_wait();
+                    float hv[16];
 #pragma unroll
-                    for (int hh = 0; hh < 2; hh++) {
-                        uint32_t g0[16], g1[16], u0[16], u1[16];
-                        const uint32_t cg = tmem + lane_base + (uint32_t)nb + 16 * hh, cu = cg + Sh::NACC;
-                        tmem_ld16(cg, g0);
-                        tmem_ld16(cg + hrows, g1);
-                        tmem_ld16(cu, u0);
-                        tmem_ld16(cu + hrows, u1);
-                        tmem_ld_wait();
-                        float hv[16];
+                    for (int j = 0; j < 16; j += 2) {
+                        const float2 h2 = situ_fast2(__uint_as_float(g0[j]) + __uint_as_float(g1[j]),
+                                                     __uint_as_float(u0[j]) + __uint_as_float(u1[j]),
+                                                     __uint_as_float(g0[j + 1]) + __uint_as_float(g1[j + 1]),
+                                                     __uint_as_float(u0[j + 1]) + __uint_as_float(u1[j + 1]));
+                        hv[j] = h2.x;
+                        hv[j + 1] = h2.y;
+                    }
+                    // each token's block of 32 features: its largest |h| sets the scale
+                    uint32_t mb[16];
 #pragma unroll
-                        for (int j = 0; j < 16; j++) {
-                            const float g = __uint_as_float(g0[j]) + __uint_as_float(g1[j]);
-                            const float u = __uint_as_float(u0[j]) + __uint_as_float(u1[j]);
-                            hv[j] = situ_fast(g, u);
-                        }
-                        // each token's block of 32 features: its largest |h| sets the scale
-                        uint32_t mb[16];
+                    for (int j = 0; j < 16; j++) mb[j] = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv[j])));
 #pragma unroll
-                        for (int j = 0; j < 16; j++) mb[j] = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv[j])));
-#pragma unroll
-                        for (int j = 0; j < 16; j++) {
-                            const int E = (int)(mb[j] >> 23);
-                            const int es = (E == 0 || E == 255) ? 0 : max(-100, min(100, E - 127 - 14));
-                            uint8_t *trow = tile + (16 * hh + j) * Sh::TROW;
-                            *reinterpret_cast<__half *>(trow + 2 * lane) =
-                                __float2half_rn(hv[j] * __int_as_float((127 - es) << 23));
-                            if (lane == j) *reinterpret_cast<int *>(trow + 64) = es;
-                        }
+                    for (int j = 0; j < 16; j++) {
+                        const int E = (int)(mb[j] >> 23);
+                        const int es = (E == 0 || E == 255) ? 0 : max(-100, min(100, E - 127 - 14));
+                        uint8_t *trow = tile + j * Sh::TROW;
+                        *reinterpret_cast<__half *>(trow + 2 * lane) = __float2half_rn(hv[j] * __int_as_float((127 - es) << 23));
+                        if (lane == j) *reinterpret_cast<int *>(trow + 64) = es;
                     }
                 }
                 tc_fence_before();
                 mbar_arrive(acce0 + 8 * b);
                 __syncwarp();
-                for (int r = 0; r < nr; r++) {
-                    const int n = 32 * half + 64 * r + lane;
-                    const uint8_t *row = tiles + (r * 32 + lane) * Sh::TROW;
-                    const float up = __int_as_float((127 + *reinterpret_cast<const int *>(row + 64)) << 23);
-                    float v[32];
+                for (int r0 = 0; r0 < 16 * nslot; r0 += 32) {
+                    const int r = r0 + lane;                      // tile row: slot r / 16, token 16 (half + 2 slot) + r % 16
+                    const int n = 16 * (half + 2 * (r >> 4)) + (r & 15);
+                    const uint8_t *row = tiles + r * Sh::TROW;
+                    if (r < 16 * nslot && n < it.ntok) {
+                        const float up = __int_as_float((127 + *reinterpret_cast<const int *>(row + 64)) << 23);
+                        float v[32];
 #pragma unroll
-                    for (int wd = 0; wd < 16; wd++) {
-                        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(row + 4 * wd));
-                        v[2 * wd] = f.x * up;
-                        v[2 * wd + 1] = f.y * up;
-                    }
-                    if (n < it.ntok) {
+                        for (int wd = 0; wd < 16; wd++) {
+                            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(row + 4 * wd));
+                            v[2 * wd] = f.x * up;
+                            v[2 * wd + 1] = f.y * up;
+                        }
                         uint4 wds[kPPh][2];
                         uint32_t sc[kPPh];
                         lane_pieces_e4m3<kPPh>(v, wds, sc);
