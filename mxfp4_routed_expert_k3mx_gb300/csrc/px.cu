@@ -91,7 +91,10 @@ template <int PH> struct PxShape {
     using C = PxCfg<PH>;
     static constexpr int NMAT = C::NMAT, K = C::K, M = C::M, SA = C::SA, SB = C::SB, PP = C::PP, PF = C::PF;
     static constexpr int KC = K / kKS, MT = M / 128, G = K / 32;
-    static constexpr int ASTAGE = ((NMAT * (kATile + kAtomB)) + 1023) / 1024 * 1024;
+    // A stage: the tiles, then the scale source: gate/up one 128 x 32-byte
+    // source for both matrices (one copy into TMEM), down one 32-line atom
+    static constexpr int ASCALE = NMAT == 2 ? 128 * 32 : kAtomB;
+    static constexpr int ASTAGE = ((NMAT * kATile + ASCALE) + 1023) / 1024 * 1024;
     static constexpr int BSTAGE = PP * kBPiece + PP * kAtomB;            // 25 KB
     // gate/up: per epilogue warp two rounds of h, 32 tokens x 32 features
     // in f16 (rows of 17 words: conflict-free both ways), to turn (feature,
@@ -468,10 +471,19 @@ __global__ void __launch_bounds__(kPxThreads, 1)
 #pragma unroll
                                 for (int i = 0; i < 4; i++) zero_nan_groups_x128(ast + m * kATile, lane + 32 * i, wq[m][i]);
                         }
+                        if (NMAT == 2) {
+                            // row lane + 32 i: word i the gate's scales, word 4 + i the up's
 #pragma unroll
-                        for (int m = 0; m < NMAT; m++)
-                            sts128(at0 + m * kAtomB + 16 * lane, drop_nan_scales(wq[m][0]), drop_nan_scales(wq[m][1]),
-                                   drop_nan_scales(wq[m][2]), drop_nan_scales(wq[m][3]));
+                            for (int m = 0; m < NMAT; m++)
+#pragma unroll
+                                for (int i = 0; i < 4; i++)
+                                    asm volatile("st.shared.u32 [%0], %1;" ::"r"(at0 + rows32_offset(lane + 32 * i, 4 * m + i)),
+                                                 "r"(drop_nan_scales(wq[m][i]))
+                                                 : "memory");
+                        } else {
+                            sts128(at0 + 16 * lane, drop_nan_scales(wq[0][0]), drop_nan_scales(wq[0][1]),
+                                   drop_nan_scales(wq[0][2]), drop_nan_scales(wq[0][3]));
+                        }
                         fence_async_smem();
                         mbar_arrive(afull0 + 8 * s);
                         sa++;
@@ -572,9 +584,10 @@ __global__ void __launch_bounds__(kPxThreads, 1)
                     const uint32_t ast = ar0 + s_a * Sh::ASTAGE, bst = br0 + s_b * Sh::BSTAGE;
                     const uint32_t sfa = tmem + Sh::SFA_COL + s_a * NMAT * 4;
                     const uint32_t sfb = tmem + Sh::SFB_COL + s_b * Sh::PP * 4;
-#pragma unroll
-                    for (int m = 0; m < NMAT; m++)
-                        tmem_cp_atom(sfa + m * 4, desc_atom(ast + NMAT * kATile + m * kAtomB, 128));
+                    if (NMAT == 2)
+                        tmem_cp_rows32(sfa, desc_rows32(ast + NMAT * kATile));
+                    else
+                        tmem_cp_atom(sfa, desc_atom(ast + NMAT * kATile, 128));
                     // B scales: two atoms over the 2 x rows combined rows of
                     // the operand (4 columns each)
 #pragma unroll

@@ -31,6 +31,23 @@ __device__ __forceinline__ uint64_t desc_atom(uint32_t saddr, uint32_t sbo) {
 __device__ __forceinline__ void tmem_cp_atom(uint32_t taddr, uint64_t desc) {
     asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
 }
+// tcgen05.cp.128x256b source: 128 rows of 32 B as [row / 8][16-byte half]
+// [row % 8][16 B] (halves 128 B apart, 8-row groups 256 B apart), no swizzle
+__device__ __forceinline__ uint64_t desc_rows32(uint32_t saddr) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | (uint64_t)(128u >> 4) << 16 | (uint64_t)(256u >> 4) << 32 |
+           (uint64_t)1 << 46;
+}
+// byte offset of 32-bit word j of row r in that source
+__host__ __device__ constexpr uint32_t rows32_offset(int r, int j) {
+    return (uint32_t)((r >> 3) * 256 + (j >> 2) * 128 + (r & 7) * 16 + (j & 3) * 4);
+}
+// 128 rows x 8 words into TMEM lanes 0..127, 8 columns (row r -> lane r).
+// For an M = 128 block-scaled MMA the lanes of quarter q read their scale
+// word at column (scale address + q), so word q of row r = 32 q + l feeds
+// one matrix and word 4 + q another: two matrices' A scales in one copy.
+__device__ __forceinline__ void tmem_cp_rows32(uint32_t taddr, uint64_t desc) {
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
 // instruction descriptor, kind::mxf4: e2m1 A and B, ue8m0 scales, K-major,
 // M = 128, N = n; sf_id picks the byte pair of the scale columns
 __device__ __forceinline__ uint32_t idesc_mxf4(int n, int sf_id) {
