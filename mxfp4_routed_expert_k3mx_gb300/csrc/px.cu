@@ -28,15 +28,17 @@
 //               swizzle) through per-expert tensor maps into an A ring
 //   warp 1      scale loader: the tile's scale bytes (16 per row, four
 //               stages ahead) from global into registers, then per stage the
-//               32-line scale-factor atoms tcgen05.cp reads; a group of scale
+//               scale source tcgen05.cp reads (one 128x256b source for both
+//               gate/up matrices, a 32-line atom for down); a group of scale
 //               255 gets scale 0 and its codes are zeroed once the tile has
 //               landed, so it adds exactly 0
 //   warp 2      TMEM owner; lane 0 copies the scale atoms to TMEM and issues,
 //               per stage, 4 K steps x NMAT MMAs (M = 128, N = 2 x the unit's
 //               box rows, K = 32)
 //   warp 3      B producer: one 3-D TMA per stage for both pieces of the
-//               unit's rows (box of 8, 16, ..., 96 rows x 128 B) and one
-//               bulk copy of the stage's B scale atoms into a B ring
+//               unit's rows (box of 8, 16, ..., 96 rows x 128 B) and the
+//               stage's 1 KB block of B scales, copied four times (once per
+//               TMEM lane quarter), into a B ring
 //   warps 4-11  epilogue, two warps per TMEM lane quarter, each half the
 //               unit's tokens: gate/up h = SiTU(g, u) split into pieces
 //               (rows of the grouped h planes + the unit's B scale atoms for
@@ -72,6 +74,7 @@ struct PxBMaps {
     CUtensorMap m[kBoxes];
 };
 constexpr int kAtomB = 512;             // scale-factor atom: 32 lines x 16 B
+constexpr int kBScaleBlock = 1024;      // a stage's B scales for one lane quarter
 constexpr int kPxThreads = 12 * 32;
 constexpr int kAProd = 0, kSfW = 1, kMmaW = 2, kBProd = 3, kEpi0 = 4;
 constexpr int kEpiThreads = 8 * 32;
@@ -95,15 +98,19 @@ template <int PH> struct PxShape {
     // source for both matrices (one copy into TMEM), down one 32-line atom
     static constexpr int ASCALE = NMAT == 2 ? 128 * 32 : kAtomB;
     static constexpr int ASTAGE = ((NMAT * kATile + ASCALE) + 1023) / 1024 * 1024;
-    static constexpr int BSTAGE = PP * kBPiece + PP * kAtomB;            // 25 KB
-    // gate/up: per epilogue warp two rounds of h, 32 tokens x 32 features
-    // in f16 (rows of 17 words: conflict-free both ways), to turn (feature,
-    // token) into (token, feature); a token's 32 values are scaled by a
-    // power of two that puts their largest magnitude in [2^14, 2^15), its
-    // exponent kept in the row's 17th word, so h keeps 11 bits whatever
-    // its size
+    // B stage: both pieces' rows, then the stage's B scales as the 4 KB
+    // source of one 128x256b copy into TMEM: a 1 KB block (kBScaleBlock)
+    // four times, once per lane quarter (every quarter reads every column's
+    // scale)
+    static constexpr int BSTAGE = PP * kBPiece + 4 * kBScaleBlock;      // 28 KB
+    // gate/up: per epilogue warp three groups of h, 16 tokens x 32 features
+    // each, in f16 (rows of 17 words: conflict-free both ways), to turn
+    // (feature, token) into (token, feature); a token's 32 values are
+    // scaled by a power of two that puts their largest magnitude in
+    // [2^14, 2^15), its exponent kept in the row's 17th word, so h keeps 11
+    // bits whatever its size
     static constexpr int TROW = 68;
-    static constexpr int TRANS = PH == 0 ? 8 * 2 * 32 * TROW : 0;
+    static constexpr int TRANS = PH == 0 ? 8 * 48 * TROW : 0;
     static constexpr int SMEM = 1024 + 1024 + SA * ASTAGE + SB * BSTAGE + TRANS;  // alignment slack, header
     // The two pieces side by side in one B operand (N = 2 x the box rows):
     // each accumulator holds a piece-0 and a piece-1 half that the epilogue
@@ -131,9 +138,9 @@ struct PxArgs {
     const float *w;                // routing weights by pair
     const uint8_t *maps;           // per-expert weight tensor maps [expert][w1, w3, w2]
     const k3mx_expert *experts;    // device table [896]
-    const uint8_t *b_atoms;        // B scale atoms of the pass's input [unit][KC][PP][512]
+    const uint8_t *b_atoms;        // B scales of the pass's input [unit][KC][1 KB] (atom_byte_pair)
     uint8_t *h_planes;             // gate/up: h pieces [kPPh][slots][F] (e4m3)
-    uint8_t *h_atoms;              // gate/up: down's B scale atoms [unit][F / 128][kPPh][512]
+    uint8_t *h_atoms;              // gate/up: down's B scales [unit][F / 128][1 KB]
     size_t slots;                  // 16 T: rows of one piece plane
     float *y;                      // down: [T][D], accumulated
     int *status;
@@ -216,15 +223,15 @@ __device__ __forceinline__ void lane_pieces_e4m3(float (&v)[32], uint4 (&bytes)[
     }
 }
 
-// byte of a pass's B scale atoms (PP pieces), pieces side by side: piece
-// pair p / 2 of stage c holds two atoms over the combined rows r = (p % 2) *
-// rows + n (rows = the unit's box height); atom r / 128, line r % 32,
-// column (r / 32) % 4
+// byte of a pass's B scales: per (unit, stage c) one 1 KB block over the
+// two pieces' combined rows r = p * rows + n (rows = the unit's box height),
+// row r's scale bytes in word r / 32 of line r % 32 of a 128x256b copy
+// source (rows32_offset), block kb4 of the stage the byte in the word
 template <int PP>
 __device__ __forceinline__ size_t atom_byte_pair(int unit, int kc_total, int c, int p, int n, int rows, int kb4) {
-    const int r = (p & 1) * rows + n;
-    return (((size_t)unit * kc_total + c) * (PP / 2) + (p >> 1)) * (2 * kAtomB) + (size_t)(r >> 7) * kAtomB +
-           (size_t)(r & 31) * 16 + ((r >> 5) & 3) * 4 + kb4;
+    static_assert(PP == 2, "two pieces");
+    const int r = p * rows + n;
+    return ((size_t)unit * kc_total + c) * kBScaleBlock + rows32_offset(r & 31, r >> 5) + kb4;
 }
 
 // an item's unit and whether its expert's pointers are usable (weights
@@ -535,11 +542,14 @@ __global__ void __launch_bounds__(kPxThreads, 1)
                 if (lane == 0) {
                     const uint32_t dst = br0 + s * Sh::BSTAGE;
                     const uint32_t bf = bfull0 + 8 * s;
-                    mbar_arrive_expect_tx(bf, (uint32_t)(Sh::PP * rows * 128 + Sh::PP * kAtomB));
+                    mbar_arrive_expect_tx(bf, (uint32_t)(Sh::PP * rows * 128 + 4 * kBScaleBlock));
                     // pieces land `rows` rows apart: [piece][rows][128 B]
                     tma_3d(dst, bm, c * kKS, it.off, 0, bf, pol);
-                    bulk_g2s(dst + Sh::PP * kBPiece, a.b_atoms + ((size_t)it.unit * KC + c) * Sh::PP * kAtomB,
-                             Sh::PP * kAtomB, bf, pol);
+                    // the stage's scale block once per lane quarter
+                    const uint8_t *sblk = a.b_atoms + ((size_t)it.unit * KC + c) * kBScaleBlock;
+#pragma unroll
+                    for (int q = 0; q < 4; q++)
+                        bulk_g2s(dst + Sh::PP * kBPiece + q * kBScaleBlock, sblk, kBScaleBlock, bf, pol);
                 }
                 __syncwarp();
             }
@@ -588,11 +598,9 @@ __global__ void __launch_bounds__(kPxThreads, 1)
                         tmem_cp_rows32(sfa, desc_rows32(ast + NMAT * kATile));
                     else
                         tmem_cp_atom(sfa, desc_atom(ast + NMAT * kATile, 128));
-                    // B scales: two atoms over the 2 x rows combined rows of
-                    // the operand (4 columns each)
-#pragma unroll
-                    for (int p = 0; p < Sh::PP; p++)
-                        tmem_cp_atom(sfb + p * 4, desc_atom(bst + Sh::PP * kBPiece + p * kAtomB, 128));
+                    // B scales: the 2 x rows combined rows of the operand, 8
+                    // columns in one copy
+                    tmem_cp_rows32(sfb, desc_rows32(bst + Sh::PP * kBPiece));
 #pragma unroll
                     for (int m = 0; m < NMAT; m++)
 #pragma unroll
@@ -648,7 +656,7 @@ __global__ void __launch_bounds__(kPxThreads, 1)
                 // token's 32 features.
                 const int kb = it.mt * 4 + q4;                   // the warp's 32-feature block of h
                 const int hrows = b_rows(b_sel(it.ntok));         // the unit's B box height
-                uint8_t *tiles = smem + 1024 + SA * Sh::ASTAGE + SB * Sh::BSTAGE + (warp - kEpi0) * 2 * 32 * Sh::TROW;
+                uint8_t *tiles = smem + 1024 + SA * Sh::ASTAGE + SB * Sh::BSTAGE + (warp - kEpi0) * 48 * Sh::TROW;
                 const size_t plane = a.slots * kF;
                 const int ng = (it.ntok + 15) >> 4;               // groups of the unit
                 int nslot = 0;                                    // this warp's groups, tile rows 16 i ...
@@ -939,8 +947,8 @@ PxLayout px_layout(int n_tokens) {
     };
     L.xplanes = take(kPPx * S * kD);
     L.hplanes = take(kPPh * S * kF);
-    L.xatoms = take(U * (kD / kKS) * kPPx * kAtomB);
-    L.hatoms = take(U * (kF / kKS) * kPPh * kAtomB);
+    L.xatoms = take(U * (kD / kKS) * kBScaleBlock);
+    L.hatoms = take(U * (kF / kKS) * kBScaleBlock);
     L.units = take(U * 3 * 4);
     L.n_units = take(4);
     L.slot_un = take(S * 4);
