@@ -29,7 +29,7 @@
 //   warp 1      scale loader: the tile's scale bytes (16 per row, four
 //               stages ahead) from global into registers, then per stage the
 //               scale source tcgen05.cp reads (one 128x256b source for both
-//               gate/up matrices, a 32-line atom for down); a group of scale
+//               gate/up matrices, one 128x128b source for down); a group of scale
 //               255 gets scale 0 and its codes are zeroed once the tile has
 //               landed, so it adds exactly 0
 //   warp 2      TMEM owner; lane 0 copies the scale atoms to TMEM and issues,
@@ -73,7 +73,6 @@ __host__ __device__ constexpr int b_sel(int n) { return n <= 8 ? 0 : (n + 7) / 8
 struct PxBMaps {
     CUtensorMap m[kBoxes];
 };
-constexpr int kAtomB = 512;             // scale-factor atom: 32 lines x 16 B
 constexpr int kBScaleBlock = 1024;      // a stage's B scales for one lane quarter
 constexpr int kPxThreads = 12 * 32;
 constexpr int kAProd = 0, kSfW = 1, kMmaW = 2, kBProd = 3, kEpi0 = 4;
@@ -84,7 +83,7 @@ template <int PH> struct PxCfg;
 // PF: weight stages prefetched into L2 ahead of the copies into the A ring
 // (the ring itself holds too few bytes in flight to cover HBM latency)
 template <> struct PxCfg<0> {           // gate/up: g = W1 x, u = W3 x
-    static constexpr int NMAT = 2, K = kD, M = kF, SA = 3, SB = 3, PP = kPPx, PF = 6;
+    static constexpr int NMAT = 2, K = kD, M = kF, SA = 3, SB = 3, PP = kPPx, PF = 10;
 };
 template <> struct PxCfg<1> {           // down: Y = W2 h
     static constexpr int NMAT = 1, K = kF, M = kD, SA = 6, SB = 4, PP = kPPh, PF = 6;
@@ -94,9 +93,9 @@ template <int PH> struct PxShape {
     using C = PxCfg<PH>;
     static constexpr int NMAT = C::NMAT, K = C::K, M = C::M, SA = C::SA, SB = C::SB, PP = C::PP, PF = C::PF;
     static constexpr int KC = K / kKS, MT = M / 128, G = K / 32;
-    // A stage: the tiles, then the scale source: gate/up one 128 x 32-byte
-    // source for both matrices (one copy into TMEM), down one 32-line atom
-    static constexpr int ASCALE = NMAT == 2 ? 128 * 32 : kAtomB;
+    // A stage: the tiles, then the scale source of one copy into TMEM:
+    // gate/up 128 x 32 bytes for both matrices, down 128 x 16 bytes
+    static constexpr int ASCALE = NMAT == 2 ? 128 * 32 : 128 * 16;
     static constexpr int ASTAGE = ((NMAT * kATile + ASCALE) + 1023) / 1024 * 1024;
     // B stage: both pieces' rows, then the stage's B scales as the 4 KB
     // source of one 128x256b copy into TMEM: a 1 KB block (kBScaleBlock)
@@ -488,8 +487,12 @@ __global__ void __launch_bounds__(kPxThreads, 1)
                                                  "r"(drop_nan_scales(wq[m][i]))
                                                  : "memory");
                         } else {
-                            sts128(at0 + 16 * lane, drop_nan_scales(wq[0][0]), drop_nan_scales(wq[0][1]),
-                                   drop_nan_scales(wq[0][2]), drop_nan_scales(wq[0][3]));
+                            // row lane + 32 i of a 128 x 16-byte source: word i its scales
+#pragma unroll
+                            for (int i = 0; i < 4; i++)
+                                asm volatile("st.shared.u32 [%0], %1;" ::"r"(at0 + 16 * (lane + 32 * i) + 4 * i),
+                                             "r"(drop_nan_scales(wq[0][i]))
+                                             : "memory");
                         }
                         fence_async_smem();
                         mbar_arrive(afull0 + 8 * s);
@@ -597,7 +600,7 @@ __global__ void __launch_bounds__(kPxThreads, 1)
                     if (NMAT == 2)
                         tmem_cp_rows32(sfa, desc_rows32(ast + NMAT * kATile));
                     else
-                        tmem_cp_atom(sfa, desc_atom(ast + NMAT * kATile, 128));
+                        tmem_cp_rows16(sfa, desc_atom(ast + NMAT * kATile, 128));
                     // B scales: the 2 x rows combined rows of the operand, 8
                     // columns in one copy
                     tmem_cp_rows32(sfb, desc_rows32(bst + Sh::PP * kBPiece));
@@ -650,50 +653,62 @@ __global__ void __launch_bounds__(kPxThreads, 1)
             if (PH == 0) {
                 // Groups of 16 tokens, dealt alternately to the two warps of
                 // a lane quarter (this warp: groups half, half + 2, half + 4).
-                // First each group's h (g and u: piece-0 plus piece-1
-                // columns) into the warp's f16 tile, scaled per token, then
-                // the accumulator is released, then each lane splits one
-                // token's 32 features.
+                // First each group's g and u (piece-0 plus piece-1 columns)
+                // into registers and the accumulator is released; then each
+                // group's h into the warp's f16 tile, scaled per token, and
+                // each lane splits one token's 32 features.
                 const int kb = it.mt * 4 + q4;                   // the warp's 32-feature block of h
                 const int hrows = b_rows(b_sel(it.ntok));         // the unit's B box height
                 uint8_t *tiles = smem + 1024 + SA * Sh::ASTAGE + SB * Sh::BSTAGE + (warp - kEpi0) * 48 * Sh::TROW;
                 const size_t plane = a.slots * kF;
                 const int ng = (it.ntok + 15) >> 4;               // groups of the unit
-                int nslot = 0;                                    // this warp's groups, tile rows 16 i ...
-                for (int gi = half; gi < ng; gi += 2, nslot++) {
-                    uint8_t *tile = tiles + nslot * 16 * Sh::TROW;
-                    uint32_t g0[16], g1[16], u0[16], u1[16];
-                    const uint32_t cg = tmem + lane_base + (uint32_t)(16 * gi), cu = cg + Sh::NACC;
-                    tmem_ld16(cg, g0);
-                    tmem_ld16(cg + hrows, g1);
-                    tmem_ld16(cu, u0);
-                    tmem_ld16(cu + hrows, u1);
-                    tmem_ld_wait();
-                    float hv[16];
+                const int nslot = ng > half ? (ng - half + 1) >> 1 : 0;   // this warp's groups, tile rows 16 i ...
+                static_assert(kUT <= 6 * 16, "three groups of 16 tokens per epilogue warp");
+                float gs[3][16], us[3][16];
 #pragma unroll
-                    for (int j = 0; j < 16; j += 2) {
-                        const float2 h2 = situ_fast2(__uint_as_float(g0[j]) + __uint_as_float(g1[j]),
-                                                     __uint_as_float(u0[j]) + __uint_as_float(u1[j]),
-                                                     __uint_as_float(g0[j + 1]) + __uint_as_float(g1[j + 1]),
-                                                     __uint_as_float(u0[j + 1]) + __uint_as_float(u1[j + 1]));
-                        hv[j] = h2.x;
-                        hv[j + 1] = h2.y;
-                    }
-                    // each token's block of 32 features: its largest |h| sets the scale
-                    uint32_t mb[16];
+                for (int i = 0; i < 3; i++) {
+                    if (i < nslot) {
+                        uint32_t p0[16], p1[16];
+                        const uint32_t cg = tmem + lane_base + (uint32_t)(16 * (half + 2 * i)), cu = cg + Sh::NACC;
+                        tmem_ld16(cg, p0);
+                        tmem_ld16(cg + hrows, p1);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 16; j++) mb[j] = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv[j])));
+                        for (int j = 0; j < 16; j++) gs[i][j] = __uint_as_float(p0[j]) + __uint_as_float(p1[j]);
+                        tmem_ld16(cu, p0);
+                        tmem_ld16(cu + hrows, p1);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 16; j++) {
-                        const int E = (int)(mb[j] >> 23);
-                        const int es = (E == 0 || E == 255) ? 0 : max(-100, min(100, E - 127 - 14));
-                        uint8_t *trow = tile + j * Sh::TROW;
-                        *reinterpret_cast<__half *>(trow + 2 * lane) = __float2half_rn(hv[j] * __int_as_float((127 - es) << 23));
-                        if (lane == j) *reinterpret_cast<int *>(trow + 64) = es;
+                        for (int j = 0; j < 16; j++) us[i][j] = __uint_as_float(p0[j]) + __uint_as_float(p1[j]);
                     }
                 }
                 tc_fence_before();
                 mbar_arrive(acce0 + 8 * b);
+#pragma unroll
+                for (int i = 0; i < 3; i++) {
+                    if (i < nslot) {
+                        uint8_t *tile = tiles + i * 16 * Sh::TROW;
+                        float hv[16];
+#pragma unroll
+                        for (int j = 0; j < 16; j += 2) {
+                            const float2 h2 = situ_fast2(gs[i][j], us[i][j], gs[i][j + 1], us[i][j + 1]);
+                            hv[j] = h2.x;
+                            hv[j + 1] = h2.y;
+                        }
+                        // each token's block of 32 features: its largest |h| sets the scale
+                        uint32_t mb[16];
+#pragma unroll
+                        for (int j = 0; j < 16; j++) mb[j] = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv[j])));
+#pragma unroll
+                        for (int j = 0; j < 16; j++) {
+                            const int E = (int)(mb[j] >> 23);
+                            const int es = (E == 0 || E == 255) ? 0 : max(-100, min(100, E - 127 - 14));
+                            uint8_t *trow = tile + j * Sh::TROW;
+                            *reinterpret_cast<__half *>(trow + 2 * lane) = __float2half_rn(hv[j] * __int_as_float((127 - es) << 23));
+                            if (lane == j) *reinterpret_cast<int *>(trow + 64) = es;
+                        }
+                    }
+                }
                 __syncwarp();
                 for (int r0 = 0; r0 < 16 * nslot; r0 += 32) {
                     const int r = r0 + lane;                      // tile row: slot r / 16, token 16 (half + 2 slot) + r % 16
@@ -801,10 +816,17 @@ __global__ void __launch_bounds__(1024) k_px_units(const int32_t *counts, const 
     if (e == 0) *n_units = tmp[32];
 }
 
-// CTAs below max_units: unit u's slots -> (unit, row) and each pair's slot;
-// the CTAs after them build the weight tensor maps of the expert table.
+// A pair's place in its unit, packed: unit u, row n < kUT, box height
+// index b_sel(pairs of the unit) (u stays below 2^20 for any workspace that
+// fits in memory)
+__host__ __device__ constexpr int32_t pack_pair_un(int u, int n, int bsel) { return (u << 11) | (n << 4) | bsel; }
+static_assert(kUT <= 128 && kBoxes <= 16, "pack_pair_un fields");
+
+// CTAs below max_units: each pair of unit u gets its slot and its place in
+// the unit; the CTAs after them build the weight tensor maps of the expert
+// table.
 __global__ void __launch_bounds__(256)
-k_px_slots(const int32_t *units, const int32_t *n_units, const int32_t *perm, int32_t *slot_un,
+k_px_slots(const int32_t *units, const int32_t *n_units, const int32_t *perm, int32_t *pair_un,
            int32_t *slot_of_pair, int max_units, uint8_t *maps, const k3mx_expert *table,
            const __grid_constant__ CUtensorMap w13, const __grid_constant__ CUtensorMap w2) {
     if ((int)blockIdx.x < max_units) {
@@ -812,32 +834,55 @@ k_px_slots(const int32_t *units, const int32_t *n_units, const int32_t *perm, in
         if (u >= __ldg(n_units)) return;
         const int off = units[3 * u + 1], ntok = units[3 * u + 2];
         for (int n = threadIdx.x; n < ntok; n += blockDim.x) {
-            const int slot = off + n;
-            slot_un[slot] = (u << 8) | n;
-            slot_of_pair[perm[slot]] = slot;
+            const int slot = off + n, pair = perm[slot];
+            pair_un[pair] = pack_pair_un(u, n, b_sel(ntok));
+            slot_of_pair[pair] = slot;
         }
         return;
     }
     build_maps_cta(maps, kE, table, k3mx_expert{}, w13, w2, blockIdx.x - max_units, 32);
 }
 
+__device__ __forceinline__ int lane_id() { return (int)(threadIdx.x & 31); }
+__device__ __forceinline__ uint4 shfl_u4(uint4 v, int from) {
+    return make_uint4(__shfl_sync(0xffffffffu, v.x, from), __shfl_sync(0xffffffffu, v.y, from),
+                      __shfl_sync(0xffffffffu, v.z, from), __shfl_sync(0xffffffffu, v.w, from));
+}
+
 // One thread per (token, 32-column block): x (bf16) -> kPPx pieces, written
 // to the token's 16 slots (rows of the piece planes and bytes of the units'
-// B scale atoms); y of the token's block zeroed for the down pass's sums.
+// B scale blocks); y of the token's block zeroed for the down pass's sums.
+// A half-warp holds 16 blocks of one token (512 contiguous bytes of a piece
+// row): per slot and piece the warp stores them in two fully used 512-byte
+// runs, lane L writing 16 bytes of each.
 __global__ void __launch_bounds__(256)
 k_px_xprep(const uint16_t *__restrict__ x, int n_tokens, const int32_t *__restrict__ slot_of_pair,
-           const int32_t *__restrict__ slot_un, const int32_t *__restrict__ units, uint8_t *__restrict__ planes,
-           uint8_t *__restrict__ atoms, size_t slots, float *__restrict__ y) {
+           const int32_t *__restrict__ pair_un, uint8_t *__restrict__ planes, uint8_t *__restrict__ atoms,
+           size_t slots, float *__restrict__ y) {
     constexpr int NB = kD / 32, KC = kD / kKS;
+    static_assert(NB % 16 == 0, "a token's blocks fill whole half-warps");
     const long long w = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (w >= (long long)n_tokens * NB) return;
-    const int t = (int)(w / NB), kb = (int)(w % NB);
+    // every lane of the warp takes part in the shuffles below; lanes past the
+    // last block (whole half-warps, as NB is a multiple of 16) only idle
+    const bool active = w < (long long)n_tokens * NB;
+    const int t = active ? (int)(w / NB) : 0, kb = active ? (int)(w % NB) : 0;
     const size_t i0 = (size_t)t * kD + (size_t)kb * 32;
+    // the token's slots and places in units: independent loads, issued first
+    int slot[kK], info[kK];
+#pragma unroll
+    for (int q = 0; q < kK / 4; q++) {
+        const int4 s4 = active ? __ldg(reinterpret_cast<const int4 *>(slot_of_pair + (size_t)t * kK) + q)
+                               : make_int4(-1, -1, -1, -1);
+        const int4 u4 = active ? __ldg(reinterpret_cast<const int4 *>(pair_un + (size_t)t * kK) + q)
+                               : make_int4(0, 0, 0, 0);
+        slot[4 * q] = s4.x, slot[4 * q + 1] = s4.y, slot[4 * q + 2] = s4.z, slot[4 * q + 3] = s4.w;
+        info[4 * q] = u4.x, info[4 * q + 1] = u4.y, info[4 * q + 2] = u4.z, info[4 * q + 3] = u4.w;
+    }
     float v[32];
     const uint4 *src = reinterpret_cast<const uint4 *>(x + i0);
 #pragma unroll
     for (int q = 0; q < 4; q++) {
-        const uint4 u = __ldg(src + q);
+        const uint4 u = active ? __ldg(src + q) : make_uint4(0u, 0u, 0u, 0u);
         const uint32_t ws[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int k = 0; k < 4; k++) {
@@ -845,24 +890,50 @@ k_px_xprep(const uint16_t *__restrict__ x, int n_tokens, const int32_t *__restri
             v[8 * q + 2 * k + 1] = __uint_as_float(ws[k] & 0xFFFF0000u);
         }
     }
-    float4 *yz = reinterpret_cast<float4 *>(y + i0);
+    if (active) {
+        float4 *yz = reinterpret_cast<float4 *>(y + i0);
 #pragma unroll
-    for (int q = 0; q < 8; q++) yz[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q = 0; q < 8; q++) yz[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     uint4 wds[kPPx][2];
     uint32_t sc[kPPx];
     lane_pieces_e4m3<kPPx>(v, wds, sc);
-#pragma unroll 4
+    // the four blocks of a 128-column stage are four consecutive lanes: their
+    // scale bytes form one word of the stage's scale block, stored by the first
+    uint32_t word[kPPx];
+#pragma unroll
+    for (int p = 0; p < kPPx; p++) {
+        const uint32_t b1 = __shfl_down_sync(0xffffffffu, sc[p], 1), b2 = __shfl_down_sync(0xffffffffu, sc[p], 2);
+        const uint32_t b3 = __shfl_down_sync(0xffffffffu, sc[p], 3);
+        word[p] = (sc[p] & 0xFFu) | (b1 & 0xFFu) << 8 | (b2 & 0xFFu) << 16 | (b3 & 0xFFu) << 24;
+    }
+    // chunk L of half-warp h's 512 bytes (16 B): half L % 2 of lane 16 h + L / 2
+    uint4 ch[kPPx][2];
+#pragma unroll
+    for (int p = 0; p < kPPx; p++)
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+            const int from = 16 * h + (lane_id() >> 1);
+            const uint4 lo = shfl_u4(wds[p][0], from), hi = shfl_u4(wds[p][1], from);
+            ch[p][h] = (lane_id() & 1) ? hi : lo;
+        }
+    const int kb0 = __shfl_sync(0xffffffffu, kb, 0), kb1 = __shfl_sync(0xffffffffu, kb, 16);
+    const bool first = active && (kb & 3) == 0;
+#pragma unroll
     for (int k = 0; k < kK; k++) {
-        const int slot = __ldg(slot_of_pair + (size_t)t * kK + k);
-        if (slot < 0) continue;                          // dropped by top-p
-        const int un = __ldg(slot_un + slot);
-        const int rows = b_rows(b_sel(__ldg(units + 3 * (un >> 8) + 2)));
-        uint8_t *dst = planes + (size_t)slot * kD + (size_t)kb * 32;
+        // -1: a dropped pair (top-p) or a half-warp past the last token
+        const int s0 = __shfl_sync(0xffffffffu, slot[k], 0), s1 = __shfl_sync(0xffffffffu, slot[k], 16);
 #pragma unroll
         for (int p = 0; p < kPPx; p++) {
-            reinterpret_cast<uint4 *>(dst + (size_t)p * slots * kD)[0] = wds[p][0];
-            reinterpret_cast<uint4 *>(dst + (size_t)p * slots * kD)[1] = wds[p][1];
-            atoms[atom_byte_pair<kPPx>(un >> 8, KC, kb >> 2, p, un & 255, rows, kb & 3)] = (uint8_t)sc[p];
+            uint8_t *plane = planes + (size_t)p * slots * kD + 16 * lane_id();
+            if (s0 >= 0) *reinterpret_cast<uint4 *>(plane + (size_t)s0 * kD + (size_t)kb0 * 32) = ch[p][0];
+            if (s1 >= 0) *reinterpret_cast<uint4 *>(plane + (size_t)s1 * kD + (size_t)kb1 * 32) = ch[p][1];
+        }
+        if (first && slot[k] >= 0) {
+            const int u = info[k] >> 11, n = (info[k] >> 4) & 127, rows = b_rows(info[k] & 15);
+#pragma unroll
+            for (int p = 0; p < kPPx; p++)
+                *reinterpret_cast<uint32_t *>(atoms + atom_byte_pair<kPPx>(u, KC, kb >> 2, p, n, rows, 0)) = word[p];
         }
     }
 }
@@ -934,7 +1005,7 @@ bool encode_planes(CUtensorMap &m, const void *base, uint64_t row_bytes, uint64_
 inline size_t up256(size_t n) { return (n + 255) & ~size_t(255); }
 
 struct PxLayout {
-    size_t xplanes, hplanes, xatoms, hatoms, units, n_units, slot_un, slot_of_pair, maps, total;
+    size_t xplanes, hplanes, xatoms, hatoms, units, n_units, pair_un, slot_of_pair, maps, total;
 };
 PxLayout px_layout(int n_tokens) {
     PxLayout L{};
@@ -951,7 +1022,7 @@ PxLayout px_layout(int n_tokens) {
     L.hatoms = take(U * (kF / kKS) * kBScaleBlock);
     L.units = take(U * 3 * 4);
     L.n_units = take(4);
-    L.slot_un = take(S * 4);
+    L.pair_un = take(S * 4);
     L.slot_of_pair = take(S * 4);
     L.maps = take(expert_maps_bytes(kE));
     L.total = o;
@@ -977,7 +1048,7 @@ cudaError_t launch_prefill_mx(const Ctx &c, const PrefillArgs &p) {
     const int U = prefill_mx_max_units(p.n_tokens);
     int32_t *units = reinterpret_cast<int32_t *>(at(L.units));
     int32_t *n_units = reinterpret_cast<int32_t *>(at(L.n_units));
-    int32_t *slot_un = reinterpret_cast<int32_t *>(at(L.slot_un));
+    int32_t *pair_un = reinterpret_cast<int32_t *>(at(L.pair_un));
     int32_t *slot_of_pair = reinterpret_cast<int32_t *>(at(L.slot_of_pair));
     uint8_t *xplanes = reinterpret_cast<uint8_t *>(at(L.xplanes));
     uint8_t *hplanes = reinterpret_cast<uint8_t *>(at(L.hplanes));
@@ -994,11 +1065,11 @@ cudaError_t launch_prefill_mx(const Ctx &c, const PrefillArgs &p) {
     cudaError_t err = traced("prefill_prep", c.stream, [&] {
         k_px_units<<<1, 1024, 0, c.stream>>>(p.counts, p.offsets, units, n_units, slot_of_pair, (int)S);
         const int map_ctas = (kE * kMapsPerExpert + kMapsPerCta - 1) / kMapsPerCta;
-        k_px_slots<<<(unsigned)(U + map_ctas), 256, 0, c.stream>>>(units, n_units, p.perm, slot_un, slot_of_pair, U,
+        k_px_slots<<<(unsigned)(U + map_ctas), 256, 0, c.stream>>>(units, n_units, p.perm, pair_un, slot_of_pair, U,
                                                                      maps, p.experts, w13, w2);
         const long long threads = (long long)p.n_tokens * (kD / 32);
         k_px_xprep<<<(unsigned)((threads + 255) / 256), 256, 0, c.stream>>>(
-            p.x, p.n_tokens, slot_of_pair, slot_un, units, xplanes, reinterpret_cast<uint8_t *>(at(L.xatoms)), S, p.y);
+            p.x, p.n_tokens, slot_of_pair, pair_un, xplanes, reinterpret_cast<uint8_t *>(at(L.xatoms)), S, p.y);
         return cudaGetLastError();
     });
     if (err != cudaSuccess) return err;

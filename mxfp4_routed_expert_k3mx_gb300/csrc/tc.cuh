@@ -31,6 +31,12 @@ __device__ __forceinline__ uint64_t desc_atom(uint32_t saddr, uint32_t sbo) {
 __device__ __forceinline__ void tmem_cp_atom(uint32_t taddr, uint64_t desc) {
     asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
 }
+// 128 rows x 4 words into TMEM lanes 0..127, 4 columns (row r -> lane r);
+// source: 128 rows of 16 B back to back (desc_atom with 8-row groups 128 B
+// apart)
+__device__ __forceinline__ void tmem_cp_rows16(uint32_t taddr, uint64_t desc) {
+    asm volatile("tcgen05.cp.cta_group::1.128x128b [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
 // tcgen05.cp.128x256b source: 128 rows of 32 B as [row / 8][16-byte half]
 // [row % 8][16 B] (halves 128 B apart, 8-row groups 256 B apart), no swizzle
 __device__ __forceinline__ uint64_t desc_rows32(uint32_t saddr) {
