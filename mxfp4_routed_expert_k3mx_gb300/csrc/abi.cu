@@ -84,6 +84,24 @@ cudaError_t ensure_smem(const void *fn, int bytes, std::atomic<uint64_t> &done) 
     return e;
 }
 
+// A small kernel that precedes a large-shared-memory one (with programmatic
+// dependent launch) asks for the largest shared-memory carve-out: an SM that
+// runs it is then already configured for the next kernel's CTA, which can
+// start there at once instead of waiting for the SM to drain.
+cudaError_t ensure_max_carveout(const void *fn, std::atomic<uint64_t> &done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    const uint64_t bit = uint64_t(1) << dev;
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(setup_mutex());
+    if (done.load(std::memory_order_relaxed) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
+
 // Device address of the library's fixed scratch array on the current device
 // (looked up once per device), or nullptr.
 void *library_scratch() {

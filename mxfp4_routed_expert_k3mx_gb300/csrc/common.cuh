@@ -362,6 +362,8 @@ std::mutex &setup_mutex();
 // cudaFuncSetAttribute(max dynamic shared memory) once per kernel and
 // device; `done` holds one bit per device
 cudaError_t ensure_smem(const void *fn, int bytes, std::atomic<uint64_t> &done);
+// the largest shared-memory carve-out for `fn`, once per device
+cudaError_t ensure_max_carveout(const void *fn, std::atomic<uint64_t> &done);
 
 // The library's fixed device scratch array (abi.cu): its address on the
 // current device, looked up on first use, and its size.

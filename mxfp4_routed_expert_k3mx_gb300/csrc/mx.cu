@@ -106,6 +106,7 @@ struct Hdr {
     // full: the stage's scale atoms (32 scale-loader lanes); tfull: its weight
     // tiles (the producer's expect_tx and the copies' bytes)
     uint64_t full[10], tfull[10], empty[10], accf[2], acce[2], bfull[2], bempty[2], sfull[2], done;
+    uint64_t table;                      // the single-token pass's staged expert table
     uint32_t tmem;
     int abort;
 };
@@ -624,12 +625,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
     const uint32_t accf0 = smem_addr(hd->accf), acce0 = smem_addr(hd->acce);
     const uint32_t bfull0 = smem_addr(hd->bfull), bempty0 = smem_addr(hd->bempty);
     const uint32_t sfull0 = smem_addr(hd->sfull), done = smem_addr(&hd->done);
+    const uint32_t tbar = smem_addr(&hd->table);
     if (tid == 0) {
         for (int i = 0; i < S; i++) {
             mbar_init(full0 + 8 * i, 32);
             mbar_init(tfull0 + 8 * i, 1);
             mbar_init(empty0 + 8 * i, 1);
         }
+        mbar_init(tbar, 1);
         for (int i = 0; i < 2; i++) {
             mbar_init(accf0 + 8 * i, 1);
             mbar_init(acce0 + 8 * i, 128);
@@ -689,16 +692,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
     // is an input of the call that no kernel of the step writes, so it is
     // staged now in the stage ring (unused until the first weight copy),
     // and a unit's pointers become a shared-memory lookup.
+    // One bulk copy, waited for only where the producer first looks a unit
+    // up: a CTA that starts late (its SM still held by blocks of the
+    // kernel before) does not spend its start on the copy.
     Sched sc = plan(MAX_UNITS);
     const uint2 *tab = reinterpret_cast<const uint2 *>(smem + 1024);
-    if (a.experts != nullptr) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(a.experts);   // 16-byte aligned (checked)
-        uint4 *dst = reinterpret_cast<uint4 *>(smem + 1024);
-        for (int i = tid; i < kE * 3; i += kThreads) dst[i] = __ldg(src + i);
+    constexpr uint32_t kTableBytes = kE * (uint32_t)sizeof(k3mx_expert);
+    static_assert(kTableBytes % 16 == 0, "bulk copy size");
+    if (a.experts != nullptr && tid == 0) {
+        mbar_arrive_expect_tx(tbar, kTableBytes);
+        bulk_g2s(st0, a.experts, kTableBytes, tbar, l2_evict_last_policy());   // 16-byte aligned (checked)
     }
     pdl_wait();
     pdl_launch_dependents();
-    __syncthreads();                     // every warp's share of the table is staged
+    __syncthreads();
 
     // the token's work units (at most 16): the unit count, the unit list
     // and perm in one round of loads (all 16 entries lie in the workspace)
@@ -720,6 +727,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
                 p0 = __ldg(a.units + 3 * lane + 1);
                 p1 = __ldg(a.units + 3 * lane + 2);
                 pr = __ldg(a.perm + lane);
+            }
+            if (!mbar_wait(tbar, 0)) {
+                if (lane == 0) report_status(a.status, kStatusWaitTimeout, 15);
+                *abort_flag = 1;
             }
             const int nu = min(max(n_raw, 0), MAX_UNITS);
             const int pair = __shfl_sync(0xffffffffu, pr, p0 & (MAX_UNITS - 1));

@@ -720,6 +720,9 @@ cudaError_t launch_route_prep(const Ctx &c, int32_t *idx, float *w, const float 
     }
     GroupOut g{};
     if (g_one != nullptr && n_tokens == 1) g = *g_one;
+    static std::atomic<uint64_t> carveout{0};
+    const cudaError_t e = ensure_max_carveout((const void *)k_route_prep, carveout);
+    if (e != cudaSuccess) return e;
     const dim3 grid(n_tokens + piece_ctas + map_ctas);
     if (pdl)
         return launch_pdl(k_route_prep, grid, dim3(kRT), 0, c.stream, idx, w, logits, bias, n_tokens, x, x_bf16,
