@@ -20,10 +20,10 @@ calls with fresh logits, then prints the device status.  With --confine the
 bias keeps routing on the R resident experts, so each expert a launch
 touches is a distinct one, as in the full workload.
 
-Timing: CUDA events on the launching stream around each step, with a few
-milliseconds of device work queued ahead of the timed steps so that the
-host's launches run ahead of the device and the events time device work,
-not host launch latency (which the end-to-end figure "e2e" includes).  The inputs
+Timing: one CUDA event pair on the launching stream around the K timed
+steps, with a few milliseconds of device work queued ahead of them so that
+the host's launches run ahead of the device and the events time device
+work, not host launch latency (which the end-to-end figure "e2e" includes).  The inputs
 of every step are larger than L2 (129 MB): a decode step streams 16 experts
 it has not just used (280.8 MB; 10.7 GB at batch 64), a prefill step all
 15.7 GB, so L2 is not flushed between timed steps; the batch-1 line also
@@ -278,17 +278,24 @@ def time_workload(k3mx, wl, table, dev, steps, warmup, dist, flush):
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    # timed steps: only the step's own kernels between the two events (the
-    # library chains them as programmatic dependents, which per-kernel
-    # events would serialise)
+    # timed steps: one event pair around all of them, so consecutive steps
+    # follow each other as they would in a run (the library chains its
+    # kernels as programmatic dependents, which an event between steps
+    # would serialise); with an L2 flush between steps (outside the events)
+    # an event pair around each step instead
     device_ahead(torch, steps)
+    if flush is None:
+        ev[0][0].record(stream)
     for i in range(steps):
         if flush is not None:
             flush.zero_()
-        ev[i][0].record(stream)
+            ev[i][0].record(stream)
         k3mx.k3mx_moe_routed(y, xs[warmup + i], table, lgs[warmup + i], bias, ws, path=wl.path,
                              idx_out=idx[i], w_out=w)
-        ev[i][1].record(stream)
+        if flush is not None:
+            ev[i][1].record(stream)
+    if flush is None:
+        ev[0][1].record(stream)
     torch.cuda.synchronize(dev)
     if dist is not None:
         dist.barrier()
@@ -308,7 +315,7 @@ def time_workload(k3mx, wl, table, dev, steps, warmup, dist, flush):
     st, det = k3mx.k3mx_device_status()
     if st != 0:
         raise RuntimeError(f"device status {st} ({det})")
-    ms = [a.elapsed_time(b) for a, b in ev]
+    ms = [a.elapsed_time(b) for a, b in ev] if flush is not None else [ev[0][0].elapsed_time(ev[0][1]) / steps] * steps
     distinct = [int(torch.unique(idx[i]).numel()) for i in range(steps)]
     return {"ms": ms, "trace": trace, "distinct": distinct}
 
@@ -650,12 +657,12 @@ def time_latent_block(k3mx, dev, table, steps, warmup, bf16_peak, hbm_peak):
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         distinct = []
         device_ahead(torch, steps)
+        ev[0][0].record(stream)
         for i in range(steps):
-            ev[i][0].record(stream)
             k3mx.k3mx_latent_moe(y, hts[warmup + i], blk, table, ws, idx_out=idx)
-            ev[i][1].record(stream)
             if T == 1:
                 distinct.append(16)
+        ev[0][1].record(stream)
         torch.cuda.synchronize(dev)
         k3mx.k3mx_trace_read()
         device_ahead(torch, 1)
@@ -664,7 +671,7 @@ def time_latent_block(k3mx, dev, table, steps, warmup, bf16_peak, hbm_peak):
         torch.cuda.synchronize(dev)
         k3mx.k3mx_trace_enable(False)
         tr = k3mx.k3mx_trace_read()
-        ms = statistics.median([a.elapsed_time(b) for a, b in ev])
+        ms = ev[0][0].elapsed_time(ev[0][1]) / steps
         r = {"us_per_call": round(1e3 * ms, 2), "tokens_per_s": round(T / (ms / 1e3), 1),
              "kernels": {k: {"launches": v[0], "avg_us": round(1e3 * v[1] / max(1, v[0]), 2)} for k, v in tr.items()},
              "l2": "not flushed (inputs exceed L2)"}
@@ -759,8 +766,8 @@ def run_ours(args):
                    "l2": "not flushed: every step streams 280.8 MB of experts it has not just used "
                          "(2.2x the 129 MB L2)",
                    "parallelism": f"replicas x{world}",
-                   "timing": "device time: a spin kernel queued ahead of the timed steps keeps the host's "
-                             "launches ahead of the device"},
+                   "timing": "one event pair around the timed steps; a spin kernel queued ahead of them keeps "
+                             "the host's launches ahead of the device"},
         "l2_flushed": {"value": round(fl_bytes / (fl_ms / 1e3) / 1e9, 2), "unit": "GB/s",
                        "ms_per_step": round(fl_ms / len(res_fl["ms"]), 4),
                        "flush": "256 MB write between timed steps, outside the events"},

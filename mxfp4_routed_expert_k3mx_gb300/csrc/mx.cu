@@ -672,12 +672,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_mx1(const MxArgs a) {
         sc.sk = a.partials != nullptr && GA >= G * (KCG + 1) && DA >= G * (KCD + 1);
         const int st[NSEG] = {0, GA, GU, GU + DA}, len[NSEG] = {GA, GU - GA, DA, GDn - DA};
         const int kc[NSEG] = {KCG, KCG, KCD, KCD};
+        // stream-K cuts: CTA B's stages before segment i's range, taken from
+        // cuts of the running totals (GA, GU, GU + DA, all stages) so that
+        // the CTAs' totals over the four segments differ by at most one
+        // stage (cutting each segment alone, a CTA could draw the shorter
+        // share in all four)
+        auto before = [&](int i, int b) -> int {
+            const long long cA = (long long)GA * b / G, cU = (long long)GU * b / G, cD = (long long)DA * b / G;
+            const long long cT = (long long)(GU + GDn) * b / G;
+            return (int)(i == 0 ? cA : i == 1 ? cU - cA : i == 2 ? cD : cT - cU - cD);
+        };
         sc.cum[0] = 0;
 #pragma unroll
         for (int i = 0; i < NSEG; i++) {
             if (sc.sk) {
-                sc.r0[i] = st[i] + len[i] * B / G;
-                sc.r1[i] = st[i] + len[i] * (B + 1) / G;
+                sc.r0[i] = st[i] + before(i, B);
+                sc.r1[i] = st[i] + before(i, B + 1);
             } else {
                 const int items = len[i] / kc[i];
                 sc.r0[i] = st[i] + items * B / G * kc[i];
