@@ -472,17 +472,17 @@ __device__ void route_cta(const float *__restrict__ lt, const float *__restrict_
             g0 = max(g0, sm.tmax[lane + 64 * q]);
             g1 = max(g1, sm.tmax[lane + 32 + 64 * q]);
         }
-        uint32_t m16 = 0;
-#pragma unroll 1
-        for (int k = 0; k < kK; k++) {
-            const uint32_t best = max(g0, g1);
-            m16 = __reduce_max_sync(0xffffffffu, best);
-            const int owner = __ffs(__ballot_sync(0xffffffffu, best == m16)) - 1;
-            if (lane == owner) {
-                if (g0 == m16) g0 = 0;
-                else g1 = 0;
-            }
+        // the 16th largest with multiplicity: the smallest value that fewer
+        // than 16 of the 64 exceed (each lane counts, for its two values, the
+        // values greater than them: 64 independent comparisons, no chain)
+        int c0 = 0, c1 = 0;
+#pragma unroll
+        for (int u = 0; u < 32; u++) {
+            const uint32_t a0 = __shfl_sync(0xffffffffu, g0, u), a1 = __shfl_sync(0xffffffffu, g1, u);
+            c0 += (a0 > g0) + (a1 > g0);
+            c1 += (a0 > g1) + (a1 > g1);
         }
+        const uint32_t m16 = __reduce_min_sync(0xffffffffu, min(c0 < kK ? g0 : 0xFFFFFFFFu, c1 < kK ? g1 : 0xFFFFFFFFu));
         if (lane == 0) {
             // a non-finite v (infinite keys) keeps every expert: exact path
             const float v = key_of_order(m16);
