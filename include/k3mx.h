@@ -24,6 +24,14 @@
  * stream: put an event wait, a copy or another kernel between.  Every other
  * argument may come from the kernel right before.
  *
+ * Co-residency: the one-token decode pass (the routed layer at one token,
+ * k3mx_expert_ffn, k3mx_latent_moe at one token) runs one block per SM, and
+ * its blocks wait (bounded) for one another's partial results.  If a kernel
+ * of another stream holds SMs until those waits give up, the call reports
+ * K3MX_ETIMEOUT through k3mx_device_status() instead of a result; nothing
+ * faults and the next call is unaffected.  Run it where no other stream's
+ * kernels occupy SMs for long (milliseconds), or on its own stream order.
+ *
  * Host threads: the library's one-time set-up per device (device
  * properties, kernel attributes, tensor-map templates) is serialised
  * internally, so first calls may come from several threads at once.  Calls
