@@ -102,14 +102,16 @@ template <int PH> struct PxShape {
     // four times, once per lane quarter (every quarter reads every column's
     // scale)
     static constexpr int BSTAGE = PP * kBPiece + 4 * kBScaleBlock;      // 28 KB
-    // gate/up: per epilogue warp three groups of h, 16 tokens x 32 features
-    // each, in f16 (rows of 17 words: conflict-free both ways), to turn
-    // (feature, token) into (token, feature); a token's 32 values are
-    // scaled by a power of two that puts their largest magnitude in
-    // [2^14, 2^15), its exponent kept in the row's 17th word, so h keeps 11
-    // bits whatever its size
-    static constexpr int TROW = 68;
-    static constexpr int TRANS = PH == 0 ? 8 * 48 * TROW : 0;
+    // gate/up: the item's h tile, to turn (feature, token) into (token,
+    // feature): per 32-feature block a plane of up to kUT tokens x 32 f16
+    // (64 bytes a token), then the exponents [token][block]; a token's 32
+    // values of a block are scaled by a power of two that puts their
+    // largest magnitude in [2^14, 2^15), so h keeps 11 bits whatever its
+    // size.  Planes lie 4 kUT + 1 16-byte units apart, so the eight lanes
+    // of a 16-byte load phase (two tokens x four blocks) hit eight
+    // different bank groups; a warp's f16 stores fill 64 contiguous bytes.
+    static constexpr int HPLANE = (4 * kUT + 1) * 16;
+    static constexpr int TRANS = PH == 0 ? 4 * HPLANE + kUT * 4 * 4 : 0;
     static constexpr int SMEM = 1024 + 1024 + SA * ASTAGE + SB * BSTAGE + TRANS;  // alignment slack, header
     // The two pieces side by side in one B operand (N = 2 x the box rows):
     // each accumulator holds a piece-0 and a piece-1 half that the epilogue
@@ -151,6 +153,9 @@ struct PxHdr {
     // aempty[s] completes when the MMAs of the stage in slot s are done: the
     // A and B rings advance together (SA >= SB), so it frees B slots too
     uint64_t afull[16], atfull[16], aempty[16], bfull[8], accf[2], acce[2], done;
+    // gate/up's h tile: written by all eight epilogue warps (hfull), read
+    // by all eight (hfree); one arrival per warp
+    uint64_t hfull, hfree;
     uint32_t tmem;
     int abort;
 };
@@ -160,6 +165,12 @@ struct PxHdr {
 // (1 + tanh(g/2)) / 2, for two tokens at once with the hardware tanh on
 // f16 pairs (relative error about 2^-10; arguments below 2^-6 in magnitude
 // give tanh(x) = x, within x^2 / 3, so small g and u keep their precision)
+__device__ __forceinline__ int lane_id() { return (int)(threadIdx.x & 31); }
+__device__ __forceinline__ uint4 shfl_u4(uint4 v, int from) {
+    return make_uint4(__shfl_sync(0xffffffffu, v.x, from), __shfl_sync(0xffffffffu, v.y, from),
+                      __shfl_sync(0xffffffffu, v.z, from), __shfl_sync(0xffffffffu, v.w, from));
+}
+
 __device__ __forceinline__ float2 tanh2_f16(float a, float b) {
     const __half2 h = __floats2half2_rn(a, b);
     uint32_t r;
@@ -286,6 +297,7 @@ __global__ void __launch_bounds__(kPxThreads, 1)
     const uint32_t bfull0 = smem_addr(hd->bfull);
     const uint32_t accf0 = smem_addr(hd->accf), acce0 = smem_addr(hd->acce);
     const uint32_t done = smem_addr(&hd->done);
+    const uint32_t hfull = smem_addr(&hd->hfull), hfree = smem_addr(&hd->hfree);
 
     if (tid == 0) {
         for (int i = 0; i < SA; i++) {
@@ -301,6 +313,8 @@ __global__ void __launch_bounds__(kPxThreads, 1)
             mbar_init(acce0 + 8 * i, kEpiThreads);
         }
         mbar_init(done, 1);
+        mbar_init(hfull, kEpiThreads / 32);
+        mbar_init(hfree, kEpiThreads / 32);
         hd->abort = 0;
         fence_mbar_init();
     }
@@ -636,7 +650,7 @@ __global__ void __launch_bounds__(kPxThreads, 1)
         (void)half;
         const int row_in_tile = 32 * q4 + lane;
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
-        uint32_t itn = 0;
+        uint32_t itn = 0, hit = 0;       // items done; gate/up items through the h tile
         PxItem nxt = i0 < items ? px_item<MT>(a, i0) : PxItem{};
         for (long long item = i0; item < items && !*abort_flag; item += istep) {
             const PxItem it = nxt;                 // decoded one item ahead (dependent loads)
@@ -655,14 +669,17 @@ __global__ void __launch_bounds__(kPxThreads, 1)
                 // a lane quarter (this warp: groups half, half + 2, half + 4).
                 // First each group's g and u (piece-0 plus piece-1 columns)
                 // into registers and the accumulator is released; then each
-                // group's h into the warp's f16 tile, scaled per token, and
-                // each lane splits one token's 32 features.
-                const int kb = it.mt * 4 + q4;                   // the warp's 32-feature block of h
+                // group's h, in f16 scaled per token and 32-feature block,
+                // into the item's shared h tile; then the eight warps split
+                // the tile by (token, 32-feature block) into the two pieces,
+                // four neighbouring lanes storing a token's 128 bytes of a
+                // piece row whole.
                 const int hrows = b_rows(b_sel(it.ntok));         // the unit's B box height
-                uint8_t *tiles = smem + 1024 + SA * Sh::ASTAGE + SB * Sh::BSTAGE + (warp - kEpi0) * 48 * Sh::TROW;
+                uint8_t *htile = smem + 1024 + SA * Sh::ASTAGE + SB * Sh::BSTAGE;
+                int *hexp = reinterpret_cast<int *>(htile + 4 * Sh::HPLANE);
                 const size_t plane = a.slots * kF;
                 const int ng = (it.ntok + 15) >> 4;               // groups of the unit
-                const int nslot = ng > half ? (ng - half + 1) >> 1 : 0;   // this warp's groups, tile rows 16 i ...
+                const int nslot = ng > half ? (ng - half + 1) >> 1 : 0;   // this warp's groups
                 static_assert(kUT <= 6 * 16, "three groups of 16 tokens per epilogue warp");
                 float gs[3][16], us[3][16];
 #pragma unroll
@@ -684,10 +701,16 @@ __global__ void __launch_bounds__(kPxThreads, 1)
                 }
                 tc_fence_before();
                 mbar_arrive(acce0 + 8 * b);
+                // the tile is free once every epilogue warp has read the
+                // previous item's
+                if (hit > 0 && !mbar_wait(hfree, (hit - 1) & 1)) {
+                    if (lane == 0) fail(356);
+                    break;
+                }
 #pragma unroll
                 for (int i = 0; i < 3; i++) {
                     if (i < nslot) {
-                        uint8_t *tile = tiles + i * 16 * Sh::TROW;
+                        const int n0 = 16 * (half + 2 * i);           // the group's first token
                         float hv[16];
 #pragma unroll
                         for (int j = 0; j < 16; j += 2) {
@@ -703,39 +726,70 @@ __global__ void __launch_bounds__(kPxThreads, 1)
                         for (int j = 0; j < 16; j++) {
                             const int E = (int)(mb[j] >> 23);
                             const int es = (E == 0 || E == 255) ? 0 : max(-100, min(100, E - 127 - 14));
-                            uint8_t *trow = tile + j * Sh::TROW;
-                            *reinterpret_cast<__half *>(trow + 2 * lane) = __float2half_rn(hv[j] * __int_as_float((127 - es) << 23));
-                            if (lane == j) *reinterpret_cast<int *>(trow + 64) = es;
+                            *reinterpret_cast<__half *>(htile + q4 * Sh::HPLANE + (n0 + j) * 64 + 2 * lane) =
+                                __float2half_rn(hv[j] * __int_as_float((127 - es) << 23));
+                            if (lane == j) hexp[(n0 + j) * 4 + q4] = es;
                         }
                     }
                 }
                 __syncwarp();
-                for (int r0 = 0; r0 < 16 * nslot; r0 += 32) {
-                    const int r = r0 + lane;                      // tile row: slot r / 16, token 16 (half + 2 slot) + r % 16
-                    const int n = 16 * (half + 2 * (r >> 4)) + (r & 15);
-                    const uint8_t *row = tiles + r * Sh::TROW;
-                    if (r < 16 * nslot && n < it.ntok) {
-                        const float up = __int_as_float((127 + *reinterpret_cast<const int *>(row + 64)) << 23);
-                        float v[32];
+                if (lane == 0) mbar_arrive(hfull);
+                if (!mbar_wait(hfull, hit & 1)) {
+                    if (lane == 0) fail(357);
+                    break;
+                }
+                const int te = (warp - kEpi0) * 32 + lane;
+                const int sub = lane & 3;                         // the lane's block within its token's four
+#pragma unroll 1
+                for (int k0 = 0; k0 < 4 * kUT; k0 += kEpiThreads) {
+                    const int n = (k0 + te) >> 2;                 // token of the unit
+                    const bool live = n < it.ntok;
+                    float v[32];
+                    if (live) {
+                        const float up = __int_as_float((127 + hexp[n * 4 + sub]) << 23);
+                        const uint8_t *src = htile + sub * Sh::HPLANE + n * 64;
 #pragma unroll
-                        for (int wd = 0; wd < 16; wd++) {
-                            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(row + 4 * wd));
-                            v[2 * wd] = f.x * up;
-                            v[2 * wd + 1] = f.y * up;
-                        }
-                        uint4 wds[kPPh][2];
-                        uint32_t sc[kPPh];
-                        lane_pieces_e4m3<kPPh>(v, wds, sc);
-                        uint8_t *dst = a.h_planes + ((size_t)it.off + n) * kF + (size_t)kb * 32;
+                        for (int c = 0; c < 4; c++) {
+                            const uint4 q = reinterpret_cast<const uint4 *>(src)[c];
+                            const uint32_t ws[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-                        for (int p = 0; p < kPPh; p++) {
-                            reinterpret_cast<uint4 *>(dst + p * plane)[0] = wds[p][0];
-                            reinterpret_cast<uint4 *>(dst + p * plane)[1] = wds[p][1];
-                            a.h_atoms[atom_byte_pair<kPPh>(it.unit, kF / kKS, it.mt, p, n, hrows, q4)] = (uint8_t)sc[p];
+                            for (int k = 0; k < 4; k++) {
+                                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&ws[k]));
+                                v[8 * c + 2 * k] = f.x * up;
+                                v[8 * c + 2 * k + 1] = f.y * up;
+                            }
                         }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 32; k++) v[k] = 0.f;
+                    }
+                    uint4 wds[kPPh][2];
+                    uint32_t sc[kPPh];
+                    lane_pieces_e4m3<kPPh>(v, wds, sc);
+                    // the token's four lanes hold its 128 bytes of a piece row
+                    // as 8 chunks of 16 (chunk c: half c % 2 of lane c / 2):
+                    // the first store writes chunks 0-3, the second 4-7
+                    const int g0 = lane & ~3;
+                    uint8_t *dst = a.h_planes + ((size_t)it.off + n) * kF + (size_t)it.mt * 128 + 16 * sub;
+#pragma unroll
+                    for (int p = 0; p < kPPh; p++) {
+#pragma unroll
+                        for (int h = 0; h < 2; h++) {
+                            const int from = g0 + 2 * h + (sub >> 1);
+                            const uint4 lo = shfl_u4(wds[p][0], from), hi = shfl_u4(wds[p][1], from);
+                            if (live) reinterpret_cast<uint4 *>(dst + p * plane + 64 * h)[0] = (sub & 1) ? hi : lo;
+                        }
+                        // the four blocks' scale bytes: one word of the stage's scale block
+                        const uint32_t b1 = __shfl_down_sync(0xffffffffu, sc[p], 1), b2 = __shfl_down_sync(0xffffffffu, sc[p], 2);
+                        const uint32_t b3 = __shfl_down_sync(0xffffffffu, sc[p], 3);
+                        if (live && sub == 0)
+                            *reinterpret_cast<uint32_t *>(a.h_atoms + atom_byte_pair<kPPh>(it.unit, kF / kKS, it.mt, p, n, hrows, 0)) =
+                                (sc[p] & 0xFFu) | (b1 & 0xFFu) << 8 | (b2 & 0xFFu) << 16 | (b3 & 0xFFu) << 24;
                     }
                 }
                 __syncwarp();
+                if (lane == 0) mbar_arrive(hfree);
+                hit++;
             } else {
                 // token n's sum: the even-piece column n plus the odd-piece
                 // column rows + n
@@ -843,11 +897,6 @@ k_px_slots(const int32_t *units, const int32_t *n_units, const int32_t *perm, in
     build_maps_cta(maps, kE, table, k3mx_expert{}, w13, w2, blockIdx.x - max_units, 32);
 }
 
-__device__ __forceinline__ int lane_id() { return (int)(threadIdx.x & 31); }
-__device__ __forceinline__ uint4 shfl_u4(uint4 v, int from) {
-    return make_uint4(__shfl_sync(0xffffffffu, v.x, from), __shfl_sync(0xffffffffu, v.y, from),
-                      __shfl_sync(0xffffffffu, v.z, from), __shfl_sync(0xffffffffu, v.w, from));
-}
 
 // One thread per (token, 32-column block): x (bf16) -> kPPx pieces, written
 // to the token's 16 slots (rows of the piece planes and bytes of the units'
