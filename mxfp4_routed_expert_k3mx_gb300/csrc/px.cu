@@ -25,14 +25,15 @@
 // item K streams in 128-column stages:
 //   warp 0      A producer: TMA of the weight tiles (128 rows x 128 codes:
 //               64 B each in global memory, 128 B in shared memory, 128-byte
-//               swizzle) through per-expert tensor maps into an A ring
+//               swizzle) through per-expert tensor maps into an A ring, the
+//               tiles some stages ahead prefetched into L2
 //   warp 1      scale loader: the tile's scale bytes (16 per row, four
 //               stages ahead) from global into registers, then per stage the
 //               scale source tcgen05.cp reads (one 128x256b source for both
 //               gate/up matrices, one 128x128b source for down); a group of scale
 //               255 gets scale 0 and its codes are zeroed once the tile has
 //               landed, so it adds exactly 0
-//   warp 2      TMEM owner; lane 0 copies the scale atoms to TMEM and issues,
+//   warp 2      TMEM owner; lane 0 copies the scales to TMEM and issues,
 //               per stage, 4 K steps x NMAT MMAs (M = 128, N = 2 x the unit's
 //               box rows, K = 32)
 //   warp 3      B producer: one 3-D TMA per stage for both pieces of the
@@ -40,12 +41,15 @@
 //               stage's 1 KB block of B scales, copied four times (once per
 //               TMEM lane quarter), into a B ring
 //   warps 4-11  epilogue, two warps per TMEM lane quarter, each half the
-//               unit's tokens: gate/up h = SiTU(g, u) split into pieces
-//               (rows of the grouped h planes + the unit's B scale atoms for
-//               down); down y[t] += w_tk * Y (fp32 atomics)
-// Two accumulator buffers let the epilogue of one item overlap the MMAs of
-// the next.  Every wait is bounded; a timeout is reported on the device
-// status word and every role leaves its loop.
+//               unit's tokens: gate/up takes g and u into registers and
+//               releases the accumulator, then h = SiTU(g, u) through the
+//               item's shared h tile split into pieces (rows of the grouped
+//               h planes + the unit's B scales for down); down y[t] +=
+//               w_tk * Y (fp32 atomics)
+// Down keeps two accumulator buffers, so the epilogue of one item overlaps
+// the MMAs of the next; gate/up's two matrices leave TMEM room for one,
+// released as soon as it is read.  Every wait is bounded; a timeout is
+// reported on the device status word and every role leaves its loop.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -148,7 +152,7 @@ struct PxArgs {
 };
 
 struct PxHdr {
-    // afull: the A stage's scale atoms (32 scale-loader lanes); atfull: its
+    // afull: the A stage's scales (32 scale-loader lanes); atfull: its
     // weight tiles (the producer's expect_tx and the copies' bytes)
     // aempty[s] completes when the MMAs of the stage in slot s are done: the
     // A and B rings advance together (SA >= SB), so it frees B slots too
