@@ -18,9 +18,10 @@
 // of its pairs (so one fixed token set).  A CTA per SM takes a contiguous
 // range of items.  Per item the K dimension streams in 256-column chunks:
 //   warp 0      TMA: each matrix's 128 x 128-byte tile (128-byte swizzle,
-//               K-major) through a per-CTA tensor map whose global address is
-//               replaced on the device for each expert; bulk copies of the
-//               unit's piece images (B operand and its scales) once per unit
+//               K-major) through the expert's tensor maps (built on the
+//               device by the kernel before, one per matrix and expert);
+//               bulk copies of the unit's piece images (B operand and its
+//               scales) once per unit
 //   warp 1      scale loader: the tile's 128 x 8 scale bytes per matrix into
 //               the 32-row scale-factor atoms tcgen05.cp reads; a group of
 //               scale 255 ("contributes nothing") gets scale 0 and, once the
@@ -572,8 +573,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // waits for another to drain and the weight stream does not pause between
 // them.  Stages are 32 KB: a gate/up stage is one 256-column chunk of W1
 // and of W3, a down stage two consecutive 256-column chunks of W2.  The
-// sequence of stages (every gate/up item, then every down item) is cut in
-// equal ranges over the CTAs (stream-K); an item split between two CTAs
+// sequence of stages (every gate/up item, then every down item, in four
+// segments) is cut in ranges over the CTAs (stream-K); an item split between two CTAs
 // is finished by the one holding its first stage, which adds the other's
 // summed pieces in a fixed order.  A down item starts its MMAs once every
 // gate/up item of its pair has written its block of h (a per-pair count);
