@@ -251,9 +251,13 @@ __device__ __forceinline__ size_t atom_byte_pair(int unit, int kc_total, int c, 
 // an item's unit and whether its expert's pointers are usable (weights
 // 32-byte aligned, as the expanding copies need, scales 16-byte aligned;
 // the maps of another expert are never used)
+// A work item as loaded: ntok < 0 marks a unit whose expert pointers are
+// unusable (checked once by k_px_units).  Nothing here computes on the
+// loaded values, so decoding the next item only issues its loads: a role
+// does not wait for them until that item is its current one.
 struct PxItem {
     int unit, mt, e, off, ntok;
-    bool ok;
+    __device__ __forceinline__ bool ok() const { return ntok > 0; }
 };
 template <int MT>
 __device__ __forceinline__ PxItem px_item(const PxArgs &a, long long item) {
@@ -263,10 +267,6 @@ __device__ __forceinline__ PxItem px_item(const PxArgs &a, long long item) {
     r.e = __ldg(a.units + 3 * r.unit);
     r.off = __ldg(a.units + 3 * r.unit + 1);
     r.ntok = __ldg(a.units + 3 * r.unit + 2);
-    const uint4 *q = reinterpret_cast<const uint4 *>(a.experts + r.e);
-    const uint4 v0 = __ldg(q), v1 = __ldg(q + 1), v2 = __ldg(q + 2);
-    r.ok = ((v0.x | v1.x | v2.x) & 31u) == 0 && ((v0.z | v1.z | v2.z) & 15u) == 0 && r.ntok >= 1 &&
-           r.ntok <= kUT;
     return r;
 }
 __device__ __forceinline__ const uint8_t *px_scales(const PxArgs &a, int e, int m, int ph) {
@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(kPxThreads, 1)
         int pf_c = 0, pf_e = -1;
         PxItem pit = pf_item < items ? px_item<MT>(a, pf_item) : PxItem{};
         auto prefetch_next = [&]() {
-            while (pf_item < items && !pit.ok) {
+            while (pf_item < items && !pit.ok()) {
                 pf_item += istep;
                 pf_c = 0;
                 if (pf_item < items) pit = px_item<MT>(a, pf_item);
@@ -384,7 +384,7 @@ __global__ void __launch_bounds__(kPxThreads, 1)
         for (long long item = i0; item < items && !*abort_flag; item += istep) {
             const PxItem it = nxt;                 // decoded one item ahead (dependent loads)
             if (item + istep < items) nxt = px_item<MT>(a, item + istep);
-            if (!it.ok) {
+            if (!it.ok()) {
                 if (lane == 0 && it.mt == 0) report_status(a.status, kStatusBadPointer, it.e);
                 continue;
             }
@@ -436,7 +436,7 @@ __global__ void __launch_bounds__(kPxThreads, 1)
         };
         auto load_group = [&](long long item, int g, uint4 (&dst)[NMAT][4]) {
             const PxItem it = px_item<MT>(a, item);
-            if (!it.ok) return;
+            if (!it.ok()) return;
 #pragma unroll
             for (int m = 0; m < NMAT; m++) {
                 const uint8_t *base = px_scales(a, it.e, m, PH) + (size_t)(it.mt * 128 + lane) * G + 16 * g;
@@ -460,7 +460,7 @@ __global__ void __launch_bounds__(kPxThreads, 1)
             if (item + istep < items) nxt = px_item<MT>(a, item + istep);
             bool ok = true;
             for (int g = 0; g < NG && ok; g++) {
-                if (it.ok) {
+                if (it.ok()) {
 #pragma unroll
                     for (int j = 0; j < 4; j++) {
                         const int s = (int)(sa % SA);
@@ -541,7 +541,7 @@ __global__ void __launch_bounds__(kPxThreads, 1)
         for (long long item = i0; item < items && !*abort_flag; item += istep) {
             const PxItem it = nxt;                 // decoded one item ahead (dependent loads)
             if (item + istep < items) nxt = px_item<MT>(a, item + istep);
-            if (!it.ok) continue;
+            if (!it.ok()) continue;
             const int hsel = b_sel(it.ntok);
             const void *bm = &bmaps.m[hsel];
             const int rows = b_rows(hsel);
@@ -590,7 +590,7 @@ __global__ void __launch_bounds__(kPxThreads, 1)
             for (long long item = i0; item < items && run && !*abort_flag; item += istep) {
                 const PxItem it = nxt;             // decoded one item ahead (dependent loads)
                 if (item + istep < items) nxt = px_item<MT>(a, item + istep);
-                if (!it.ok) continue;
+                if (!it.ok()) continue;
                 // both pieces: N covers two box heights
                 const int nmma = 2 * b_rows(b_sel(it.ntok));
                 uint32_t idk[4];
@@ -659,7 +659,7 @@ __global__ void __launch_bounds__(kPxThreads, 1)
         for (long long item = i0; item < items && !*abort_flag; item += istep) {
             const PxItem it = nxt;                 // decoded one item ahead (dependent loads)
             if (item + istep < items) nxt = px_item<MT>(a, item + istep);
-            if (!it.ok) continue;
+            if (!it.ok()) continue;
             const int b = itn % Sh::NBUF;
             if (!mbar_wait(accf0 + 8 * b, (itn / Sh::NBUF) & 1)) {
                 if (lane == 0) fail(350 + PH);
@@ -834,7 +834,7 @@ __global__ void __launch_bounds__(kPxThreads, 1)
 // nearly equal length (one 1024-thread CTA, expert e on thread e).
 __global__ void __launch_bounds__(1024) k_px_units(const int32_t *counts, const int32_t *offsets,
                                                    int32_t *units, int32_t *n_units, int32_t *slot_of_pair,
-                                                   int n_pairs) {
+                                                   int n_pairs, const k3mx_expert *experts) {
     __shared__ int tmp[33];
     const int e = threadIdx.x, lane = e & 31, wp = e >> 5;
     const int cnt = e < kE ? counts[e] : 0;
@@ -864,11 +864,17 @@ __global__ void __launch_bounds__(1024) k_px_units(const int32_t *counts, const 
     for (int i = threadIdx.x; i < n_pairs; i += blockDim.x) slot_of_pair[i] = -1;
     if (e < kE && nu > 0) {
         const int o0 = offsets[e];
+        // the expert's weights 32-byte and scales 16-byte aligned, else its
+        // units carry minus their pair counts (reported, and skipped, by
+        // the passes)
+        const uint4 *q = reinterpret_cast<const uint4 *>(experts + e);
+        const uint4 v0 = __ldg(q), v1 = __ldg(q + 1), v2 = __ldg(q + 2);
+        const bool usable = ((v0.x | v1.x | v2.x) & 31u) == 0 && ((v0.z | v1.z | v2.z) & 15u) == 0;
         for (int k = 0; k < nu; k++) {
             const int lo = (int)((long long)cnt * k / nu), hi = (int)((long long)cnt * (k + 1) / nu);
             units[3 * (pos + k) + 0] = e;
             units[3 * (pos + k) + 1] = o0 + lo;
-            units[3 * (pos + k) + 2] = hi - lo;
+            units[3 * (pos + k) + 2] = usable ? hi - lo : lo - hi;       // 1 <= hi - lo <= kUT
         }
     }
     if (e == 0) *n_units = tmp[32];
@@ -1116,7 +1122,7 @@ cudaError_t launch_prefill_mx(const Ctx &c, const PrefillArgs &p) {
             return cudaErrorNotSupported;
 
     cudaError_t err = traced("prefill_prep", c.stream, [&] {
-        k_px_units<<<1, 1024, 0, c.stream>>>(p.counts, p.offsets, units, n_units, slot_of_pair, (int)S);
+        k_px_units<<<1, 1024, 0, c.stream>>>(p.counts, p.offsets, units, n_units, slot_of_pair, (int)S, p.experts);
         const int map_ctas = (kE * kMapsPerExpert + kMapsPerCta - 1) / kMapsPerCta;
         k_px_slots<<<(unsigned)(U + map_ctas), 256, 0, c.stream>>>(units, n_units, p.perm, pair_un, slot_of_pair, U,
                                                                      maps, p.experts, w13, w2);
