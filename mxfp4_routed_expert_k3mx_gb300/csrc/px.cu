@@ -799,15 +799,28 @@ __global__ void __launch_bounds__(kPxThreads, 1)
                 // column rows + n
                 const int rows = b_rows(b_sel(it.ntok));
                 for (int nb = n0; nb < n1; nb += 16) {
+                    // the group's pairs and routing weights: lane j < 16
+                    // loads token nb + j's (one round trip for the group, not
+                    // two dependent loads per token), shared by shuffles
+                    const int nn = min(16, n1 - nb);
+                    int pj = 0;
+                    float wj = 0.f;
+                    if (lane < nn) {
+                        pj = __ldg(a.perm + it.off + nb + lane);
+                        wj = __ldg(a.w + pj);
+                    }
                     uint32_t dv[16], dw[16];
                     tmem_ld16(tmem + lane_base + (uint32_t)b * Sh::NACC + nb, dv);
                     tmem_ld16(tmem + lane_base + (uint32_t)b * Sh::NACC + rows + nb, dw);   // NMAT = 1
                     tmem_ld_wait();
-                    const int nn = min(16, n1 - nb);
-                    for (int j = 0; j < nn; j++) {
-                        const int pair = __ldg(a.perm + it.off + nb + j);
-                        const float yv = __uint_as_float(dv[j]) + __uint_as_float(dw[j]);
-                        atomicAdd(a.y + (size_t)(pair / kK) * kD + row, __ldg(a.w + pair) * yv);
+#pragma unroll
+                    for (int j = 0; j < 16; j++) {
+                        const int pair = __shfl_sync(0xffffffffu, pj, j);
+                        const float wt = __shfl_sync(0xffffffffu, wj, j);
+                        if (j < nn) {
+                            const float yv = __uint_as_float(dv[j]) + __uint_as_float(dw[j]);
+                            atomicAdd(a.y + (size_t)(pair / kK) * kD + row, wt * yv);
+                        }
                     }
                 }
             }
