@@ -337,16 +337,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_prefill(PArgs a) {
                 const float f2 = ldexpf(1.f, row_sref(ex.s2 + (size_t)row * G, ex.w2 + (size_t)row * (K / 2), G) - 127);
                 const uint32_t td = tmem + lane_base + (uint32_t)(ab * 128);
                 for (int n0 = 0; n0 < npad; n0 += 16) {
+                    // the group's pairs and routing weights: lane j < 16
+                    // loads token n0 + j's (one round trip for the group),
+                    // shared by shuffles
+                    int pj = 0;
+                    float wj = 0.f;
+                    if (lane < 16 && n0 + lane < ntok) {
+                        pj = a.perm[off + n0 + lane];
+                        wj = __ldg(a.w + pj);
+                    }
                     uint32_t dv[16];
                     tmem_ld16(td + n0, dv);
                     tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < 16; j++) {
-                        const int n = n0 + j;
-                        if (n < ntok) {
-                            const int p = a.perm[off + n];
-                            atomicAdd(a.y + (size_t)(p / kK) * kD + row, __ldg(a.w + p) * __uint_as_float(dv[j]) * f2);
-                        }
+                        const int p = __shfl_sync(0xffffffffu, pj, j);
+                        const float wt = __shfl_sync(0xffffffffu, wj, j);
+                        if (n0 + j < ntok) atomicAdd(a.y + (size_t)(p / kK) * kD + row, wt * __uint_as_float(dv[j]) * f2);
                     }
                 }
             }
